@@ -1,0 +1,524 @@
+"""CPU oracle for integer-only training: plain C primitives (oracle.c) plus the
+order of one training step, written out here.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the package's smoke check
+and by the benchmark's CPU-baseline leg, never by the product path. It shares no
+code with the CUDA library and never imports it.
+
+Sources:
+  "Integer On-Device Training: Overview" (TI C2000 MCU AI user guide):
+    section 3, NITI dynamic shifts, Steps 1-5 and the delta-propagation note;
+    section 4, the training loop (forward, compute_loss writes dy, backward
+    reads it and updates weights).
+  "Mixed Precision Training of Convolutional Neural Networks using Integer
+    Operations": section 3 and 3.1, DFP tensors and primitives.
+
+Step order (one reading, stated): forward through all layers; top error;
+then for each layer from the top down: delta propagation with the weights as
+they were before this step's update (not for the first layer), weight
+gradient, weight update.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+
+TARGET_BITS = 7      # NITI target_bits, for forward, delta and weight gradient
+MU_WEIGHT = 2        # NITI mu_weight
+TARGET_MAG = 64      # integer target on the true class
+DFP_BITS = 15        # DFP-16 mantissa: 15 magnitude bits plus sign
+DFP_ETA = 8          # DFP16 integer SGD: learning rate 2^-eta
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library (gcc, OpenMP over output rows)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-Wall", "-Wextra", "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, u32, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
+        sig = {
+            "ora_bitlen": (i32, [u64]),
+            "ora_shift_from_max": (i32, [u64, i32]),
+            "ora_rhu": (i64, [i64, i32]),
+            "ora_sat8": (i64, [i64]),
+            "ora_sat16": (i64, [i64]),
+            "ora_absmax32": (u32, [P, i64]),
+            "ora_absmax64": (u64, [P, i64]),
+            "ora_requant": (i32, [P, i64, i32, ctypes.c_int, P, P]),
+            "ora_requant_mask": (i32, [P, P, i64, i32, P, P]),
+            "ora_top_error": (None, [P, P, ctypes.c_int, ctypes.c_int, i32, P]),
+            "ora_niti_update": (i64, [P, P, i64, i32, i32, P, P, P]),
+            "ora_linear_fwd": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_linear_dgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_linear_wgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_conv2d_fwd": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
+            "ora_conv2d_dgrad": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
+            "ora_conv2d_wgrad": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
+            "ora_gap_fwd": (None, [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]),
+            "ora_gap_bwd": (None, [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]),
+            "ora_dfp_linear_fwd": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_dfp_linear_dgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_dfp_linear_wgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_dfp_down": (i32, [P, i64, i32, P, P]),
+            "ora_dfp_update": (i64, [P, P, i64, i32]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dt):
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+# ------------------------------------------------------------------ scalars
+
+def bitlen(m: int) -> int:
+    return lib().ora_bitlen(m)
+
+
+def shift_from_max(m: int, target_bits: int = TARGET_BITS) -> int:
+    return lib().ora_shift_from_max(m, target_bits)
+
+
+def rhu(x: int, s: int) -> int:
+    return lib().ora_rhu(x, s)
+
+
+def sat8(v: int) -> int:
+    return lib().ora_sat8(v)
+
+
+def sat16(v: int) -> int:
+    return lib().ora_sat16(v)
+
+
+# ---------------------------------------------------------- tensor primitives
+
+def absmax32(v) -> int:
+    v = _c(v, np.int32)
+    return lib().ora_absmax32(_p(v), v.size)
+
+
+def requant(Y, relu: bool, target_bits: int = TARGET_BITS):
+    """-> (int8 tensor, shift, max|Y|)"""
+    Y = _c(Y, np.int32)
+    out = np.empty(Y.shape, np.int8)
+    m = ctypes.c_uint32()
+    s = lib().ora_requant(_p(Y), Y.size, target_bits, int(relu), _p(out), ctypes.byref(m))
+    return out, s, m.value
+
+
+def requant_mask(D, a_prev, target_bits: int = TARGET_BITS):
+    """-> (int8 delta, shift, max|D|); a_prev None means no ReLU gate."""
+    D = _c(D, np.int32)
+    out = np.empty(D.shape, np.int8)
+    m = ctypes.c_uint32()
+    if a_prev is None:
+        ap = None
+    else:
+        a_prev = _c(a_prev, np.int8)
+        assert a_prev.size == D.size
+        ap = _p(a_prev)
+    s = lib().ora_requant_mask(_p(D), ap, D.size, target_bits, _p(out), ctypes.byref(m))
+    return out, s, m.value
+
+
+def top_error(logits, labels, target_mag: int = TARGET_MAG):
+    logits = _c(logits, np.int8)
+    labels = _c(labels, np.int32)
+    B, C = logits.shape
+    out = np.empty((B, C), np.int8)
+    lib().ora_top_error(_p(logits), _p(labels), B, C, target_mag, _p(out))
+    return out
+
+
+def niti_update(W, G, target_bits: int = TARGET_BITS, mu_weight: int = MU_WEIGHT):
+    """Returns (new W, shift, weight_shift, max|G|, nonzero count); W is not modified."""
+    Wn = np.array(W, dtype=np.int8, copy=True, order="C")
+    G = _c(G, np.int32)
+    assert G.size == Wn.size
+    s, ws, m = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_uint32()
+    nz = lib().ora_niti_update(_p(Wn), _p(G), G.size, target_bits, mu_weight,
+                               ctypes.byref(s), ctypes.byref(ws), ctypes.byref(m))
+    return Wn, s.value, ws.value, m.value, nz
+
+
+def linear_fwd(X, W):
+    X, W = _c(X, np.int8), _c(W, np.int8)
+    B, IC = X.shape
+    OC = W.shape[0]
+    assert W.shape == (OC, IC)
+    Y = np.empty((B, OC), np.int32)
+    lib().ora_linear_fwd(_p(X), _p(W), B, IC, OC, _p(Y))
+    return Y
+
+
+def linear_dgrad(delta, W):
+    delta, W = _c(delta, np.int8), _c(W, np.int8)
+    B, OC = delta.shape
+    IC = W.shape[1]
+    assert W.shape == (OC, IC)
+    D = np.empty((B, IC), np.int32)
+    lib().ora_linear_dgrad(_p(delta), _p(W), B, IC, OC, _p(D))
+    return D
+
+
+def linear_wgrad(delta, A):
+    delta, A = _c(delta, np.int8), _c(A, np.int8)
+    B, OC = delta.shape
+    IC = A.shape[1]
+    assert A.shape[0] == B
+    G = np.empty((OC, IC), np.int32)
+    lib().ora_linear_wgrad(_p(delta), _p(A), B, IC, OC, _p(G))
+    return G
+
+
+# Exact float64 route for large contractions. Every product of two integers
+# is exact in float64, and every partial sum is an integer bounded by
+# K * max|A| * max|B|; below 2^53 all of them are exactly representable, so the
+# BLAS result is the exact integer sum whatever order or fused multiply-add the
+# library uses. The bound is checked before the call.
+
+def _exact_matmul(A, B_T):
+    """A [M, K] @ B_T [K, N] over integers, exact in float64 (bound checked)."""
+    K = A.shape[1]
+    ma = int(np.abs(A.astype(np.int64)).max(initial=0))
+    mb = int(np.abs(B_T.astype(np.int64)).max(initial=0))
+    if K * ma * mb >= (1 << 53):
+        raise OverflowError("float64 route not exact for this contraction")
+    r = A.astype(np.float64) @ B_T.astype(np.float64)
+    return np.rint(r).astype(np.int64)
+
+
+def _to_i32(v):
+    if v.size and (v.max() > np.iinfo(np.int32).max or v.min() < np.iinfo(np.int32).min):
+        raise OverflowError("int32 overflow in a contraction result")
+    return v.astype(np.int32)
+
+
+def linear_fwd_f64(X, W):
+    return _to_i32(_exact_matmul(np.asarray(X), np.asarray(W).T))
+
+
+def linear_dgrad_f64(delta, W):
+    return _to_i32(_exact_matmul(np.asarray(delta), np.asarray(W)))
+
+
+def linear_wgrad_f64(delta, A):
+    return _to_i32(_exact_matmul(np.asarray(delta).T, np.asarray(A)))
+
+
+def dfp_linear_fwd_f64(X, W):
+    return _exact_matmul(np.asarray(X), np.asarray(W).T)
+
+
+def dfp_linear_dgrad_f64(delta, W):
+    return _exact_matmul(np.asarray(delta), np.asarray(W))
+
+
+def dfp_linear_wgrad_f64(delta, A):
+    return _exact_matmul(np.asarray(delta).T, np.asarray(A))
+
+
+def conv_out(n: int, k: int = 3, stride: int = 1, pad: int = 1) -> int:
+    return (n + 2 * pad - k) // stride + 1
+
+
+def conv2d_fwd(X, Wt, stride: int, pad: int = 1):
+    X, Wt = _c(X, np.int8), _c(Wt, np.int8)
+    B, H, Wd, IC = X.shape
+    OC, KH, KW, IC2 = Wt.shape
+    assert IC == IC2
+    OH, OW = conv_out(H, KH, stride, pad), conv_out(Wd, KW, stride, pad)
+    Y = np.empty((B, OH, OW, OC), np.int32)
+    lib().ora_conv2d_fwd(_p(X), _p(Wt), B, H, Wd, IC, OC, KH, KW, stride, pad, _p(Y))
+    return Y
+
+
+def conv2d_dgrad(delta, Wt, in_hw, stride: int, pad: int = 1):
+    delta, Wt = _c(delta, np.int8), _c(Wt, np.int8)
+    B = delta.shape[0]
+    OC, KH, KW, IC = Wt.shape
+    H, Wd = in_hw
+    assert delta.shape == (B, conv_out(H, KH, stride, pad), conv_out(Wd, KW, stride, pad), OC)
+    D = np.empty((B, H, Wd, IC), np.int32)
+    lib().ora_conv2d_dgrad(_p(delta), _p(Wt), B, H, Wd, IC, OC, KH, KW, stride, pad, _p(D))
+    return D
+
+
+def conv2d_wgrad(delta, X, k: int, stride: int, pad: int = 1):
+    delta, X = _c(delta, np.int8), _c(X, np.int8)
+    B, H, Wd, IC = X.shape
+    OC = delta.shape[3]
+    assert delta.shape == (B, conv_out(H, k, stride, pad), conv_out(Wd, k, stride, pad), OC)
+    G = np.empty((OC, k, k, IC), np.int32)
+    lib().ora_conv2d_wgrad(_p(delta), _p(X), B, H, Wd, IC, OC, k, k, stride, pad, _p(G))
+    return G
+
+
+def gap_fwd(A):
+    A = _c(A, np.int8)
+    B, H, Wd, C = A.shape
+    P = np.empty((B, C), np.int32)
+    lib().ora_gap_fwd(_p(A), B, H * Wd, C, _p(P))
+    return P
+
+
+def gap_bwd(dP, A):
+    dP, A = _c(dP, np.int8), _c(A, np.int8)
+    B, H, Wd, C = A.shape
+    assert dP.shape == (B, C)
+    D = np.empty(A.shape, np.int8)
+    lib().ora_gap_bwd(_p(dP), _p(A), B, H * Wd, C, _p(D))
+    return D
+
+
+def dfp_linear_fwd(X, W):
+    X, W = _c(X, np.int16), _c(W, np.int16)
+    B, IC = X.shape
+    OC = W.shape[0]
+    assert W.shape == (OC, IC)
+    P = np.empty((B, OC), np.int64)
+    lib().ora_dfp_linear_fwd(_p(X), _p(W), B, IC, OC, _p(P))
+    return P
+
+
+def dfp_linear_dgrad(delta, W):
+    delta, W = _c(delta, np.int16), _c(W, np.int16)
+    B, OC = delta.shape
+    IC = W.shape[1]
+    assert W.shape == (OC, IC)
+    P = np.empty((B, IC), np.int64)
+    lib().ora_dfp_linear_dgrad(_p(delta), _p(W), B, IC, OC, _p(P))
+    return P
+
+
+def dfp_linear_wgrad(delta, A):
+    delta, A = _c(delta, np.int16), _c(A, np.int16)
+    B, OC = delta.shape
+    IC = A.shape[1]
+    P = np.empty((OC, IC), np.int64)
+    lib().ora_dfp_linear_wgrad(_p(delta), _p(A), B, IC, OC, _p(P))
+    return P
+
+
+def dfp_down(P, exp_in: int, target_bits: int = DFP_BITS):
+    """-> (int16 mantissas, new exponent, Rs, max|P|). Raises if the new
+    exponent leaves the signed 8-bit range the DFP format stores it in."""
+    P = _c(P, np.int64)
+    out = np.empty(P.shape, np.int16)
+    m = ctypes.c_uint64()
+    rs = lib().ora_dfp_down(_p(P), P.size, target_bits, _p(out), ctypes.byref(m))
+    e = exp_in + rs
+    if not -128 <= e <= 127:
+        raise OverflowError("DFP exponent %d outside int8" % e)
+    return out, e, rs, m.value
+
+
+def dfp_update(W, Gm, k: int):
+    Wn = np.array(W, dtype=np.int16, copy=True, order="C")
+    Gm = _c(Gm, np.int16)
+    nz = lib().ora_dfp_update(_p(Wn), _p(Gm), Gm.size, k)
+    return Wn, nz
+
+
+# ------------------------------------------------------------- training steps
+
+def _linear_ops(route):
+    if route == "loops":
+        return linear_fwd, linear_dgrad, linear_wgrad
+    if route == "f64":
+        return linear_fwd_f64, linear_dgrad_f64, linear_wgrad_f64
+    raise ValueError(route)
+
+
+def mlp_step(weights, x, labels, target_bits=TARGET_BITS, mu_weight=MU_WEIGHT,
+             target_mag=TARGET_MAG, route="loops"):
+    """One NITI step of a sequential int8 MLP: Linear+ReLU layers and a final
+    Linear producing int8 logits. `weights` is a list of int8 [OC, IC]; the
+    updated weights are returned in the record (inputs are not modified).
+
+    Record names (layer l counted from 0): y{l} int32 forward contraction,
+    ymax{l}/ys{l} its max and shift, a{l} int8 output; e{l} int8 delta at the
+    output of layer l (e{L-1} is the top error); d{l} int32 delta-propagation
+    contraction of layer l (l >= 1) with dmax{l}/ds{l}; g{l} int32 weight
+    gradient with gmax{l}/gs{l}/ws{l}; w{l} updated weights; nz{l} nonzero
+    weight steps. route: "loops" (C loops) or "f64" (exact float64 BLAS)."""
+    fwd, dgrad, wgrad = _linear_ops(route)
+    L = len(weights)
+    r = {}
+    act = [np.ascontiguousarray(x, np.int8)]
+    for l in range(L):
+        y = fwd(act[-1], weights[l])
+        a, s, m = requant(y, relu=(l < L - 1), target_bits=target_bits)
+        r["y%d" % l], r["ymax%d" % l], r["ys%d" % l], r["a%d" % l] = y, m, s, a
+        act.append(a)
+    e = top_error(act[-1], labels, target_mag)
+    r["e%d" % (L - 1)] = e
+    for l in range(L - 1, -1, -1):
+        if l > 0:
+            d = dgrad(e, weights[l])
+            e_prev, s, m = requant_mask(d, act[l], target_bits)
+            r["d%d" % l], r["dmax%d" % l], r["ds%d" % l], r["e%d" % (l - 1)] = d, m, s, e_prev
+        g = wgrad(e, act[l])
+        wn, s, ws, m, nz = niti_update(weights[l], g, target_bits, mu_weight)
+        r["g%d" % l], r["gmax%d" % l], r["gs%d" % l], r["ws%d" % l] = g, m, s, ws
+        r["w%d" % l], r["nz%d" % l] = wn, nz
+        if l > 0:
+            e = e_prev
+    return r
+
+
+def cnn_step(weights, x, labels, convs, target_bits=TARGET_BITS, mu_weight=MU_WEIGHT,
+             target_mag=TARGET_MAG):
+    """One NITI step of the integer CNN: 3x3 Conv+ReLU layers (pad 1, strides
+    from `convs`), integer-sum global pooling requantised without ReLU, and a
+    final Linear to logits. weights = conv [OC,3,3,IC] ..., then fc [C, F].
+
+    Extra record names: p int32 pooled sum with pmax/ps, pa int8 pooled
+    activation; the fc layer is layer n = len(convs): y{n}, a{n} (logits),
+    e{n} top error, d{n} its delta-propagation contraction and pe (pooled delta,
+    no ReLU gate), then e{n-1} = pooling backward gated by a{n-1} > 0."""
+    n = len(convs)
+    r = {}
+    act = [np.ascontiguousarray(x, np.int8)]
+    for l, (_ic, _oc, stride) in enumerate(convs):
+        y = conv2d_fwd(act[-1], weights[l], stride)
+        a, s, m = requant(y, relu=True, target_bits=target_bits)
+        r["y%d" % l], r["ymax%d" % l], r["ys%d" % l], r["a%d" % l] = y, m, s, a
+        act.append(a)
+    p = gap_fwd(act[-1])
+    pa, s, m = requant(p, relu=False, target_bits=target_bits)
+    r["p"], r["pmax"], r["ps"], r["pa"] = p, m, s, pa
+    y = linear_fwd(pa, weights[n])
+    logits, s, m = requant(y, relu=False, target_bits=target_bits)
+    r["y%d" % n], r["ymax%d" % n], r["ys%d" % n], r["a%d" % n] = y, m, s, logits
+    e = top_error(logits, labels, target_mag)
+    r["e%d" % n] = e
+    # fc layer
+    d = linear_dgrad(e, weights[n])
+    pe, s, m = requant_mask(d, None, target_bits)
+    r["d%d" % n], r["dmax%d" % n], r["ds%d" % n], r["pe"] = d, m, s, pe
+    g = linear_wgrad(e, pa)
+    wn, s, ws, m, nz = niti_update(weights[n], g, target_bits, mu_weight)
+    r["g%d" % n], r["gmax%d" % n], r["gs%d" % n], r["ws%d" % n] = g, m, s, ws
+    r["w%d" % n], r["nz%d" % n] = wn, nz
+    e = gap_bwd(pe, act[n])
+    r["e%d" % (n - 1)] = e
+    for l in range(n - 1, -1, -1):
+        stride = convs[l][2]
+        if l > 0:
+            H, Wd = act[l].shape[1:3]
+            d = conv2d_dgrad(e, weights[l], (H, Wd), stride)
+            e_prev, s, m = requant_mask(d, act[l], target_bits)
+            r["d%d" % l], r["dmax%d" % l], r["ds%d" % l], r["e%d" % (l - 1)] = d, m, s, e_prev
+        g = conv2d_wgrad(e, act[l], 3, stride)
+        wn, s, ws, m, nz = niti_update(weights[l], g, target_bits, mu_weight)
+        r["g%d" % l], r["gmax%d" % l], r["gs%d" % l], r["ws%d" % l] = g, m, s, ws
+        r["w%d" % l], r["nz%d" % l] = wn, nz
+        if l > 0:
+            e = e_prev
+    return r
+
+
+def dfp16_step(weights, exp_w, x, exp_x, eta=DFP_ETA, target_bits=DFP_BITS, route="loops"):
+    """One integer training step of a stack of DFP-16 Linear layers (no ReLU).
+    weights: list of int16 mantissa tensors [OC, IC] sharing exponent exp_w
+    (held fixed); x: int16 mantissas [B, IC0] with exponent exp_x.
+
+    Every contraction is exact in int64 and is down-converted to DFP-16 with a
+    new exponent. The top error is the output itself (an MSE error against a
+    zero target). The update is integer SGD with rate 2^-eta (ora_dfp_update).
+
+    Record names: p{l} int64 forward contraction, pmax{l}, rs{l}, y{l} int16,
+    ey{l} exponent; e{l}/ee{l} delta at the output of layer l; pd{l} int64
+    delta-propagation contraction (l >= 1) with pdmax{l}, rsd{l}; pg{l} int64
+    weight gradient with pgmax{l}, rsg{l}, g{l} int16, eg{l}; k{l} the update
+    shift; w{l} updated weights; nz{l}. route: "loops" or "f64"."""
+    if route == "loops":
+        dfwd, ddgrad, dwgrad = dfp_linear_fwd, dfp_linear_dgrad, dfp_linear_wgrad
+    elif route == "f64":
+        dfwd, ddgrad, dwgrad = dfp_linear_fwd_f64, dfp_linear_dgrad_f64, dfp_linear_wgrad_f64
+    else:
+        raise ValueError(route)
+    L = len(weights)
+    r = {}
+    act = [np.ascontiguousarray(x, np.int16)]
+    ex = [exp_x]
+    for l in range(L):
+        p = dfwd(act[-1], weights[l])
+        y, e_y, rs, m = dfp_down(p, ex[-1] + exp_w, target_bits)
+        r["p%d" % l], r["pmax%d" % l], r["rs%d" % l], r["y%d" % l], r["ey%d" % l] = p, m, rs, y, e_y
+        act.append(y)
+        ex.append(e_y)
+    e, ee = act[-1], ex[-1]
+    r["e%d" % (L - 1)], r["ee%d" % (L - 1)] = e, ee
+    for l in range(L - 1, -1, -1):
+        if l > 0:
+            pd = ddgrad(e, weights[l])
+            e_prev, ee_prev, rs, m = dfp_down(pd, ee + exp_w, target_bits)
+            r["pd%d" % l], r["pdmax%d" % l], r["rsd%d" % l] = pd, m, rs
+            r["e%d" % (l - 1)], r["ee%d" % (l - 1)] = e_prev, ee_prev
+        pg = dwgrad(e, act[l])
+        g, eg, rs, m = dfp_down(pg, ee + ex[l], target_bits)
+        k = exp_w + eta - eg
+        wn, nz = dfp_update(weights[l], g, k)
+        r["pg%d" % l], r["pgmax%d" % l], r["rsg%d" % l], r["g%d" % l], r["eg%d" % l] = pg, m, rs, g, eg
+        r["k%d" % l], r["w%d" % l], r["nz%d" % l] = k, wn, nz
+        if l > 0:
+            e, ee = e_prev, ee_prev
+    return r
+
+
+def run_steps(workload, steps: int, start_weights=None, callback=None, route="loops"):
+    """Run `steps` training steps of a seeded workload (seeded_inputs.Workload),
+    feeding each step's updated weights to the next. callback(t, record) is
+    called after every step. Returns the final weights."""
+    import seeded_inputs as si
+    w = workload
+    weights = [np.array(a) for a in (start_weights or si.make_weights(w))]
+    for t in range(steps):
+        x, labels = si.make_batch(w, t)
+        if w.kind == "mlp":
+            rec = mlp_step(weights, x, labels, route=route)
+        elif w.kind == "cnn":
+            rec = cnn_step(weights, x, labels, w.convs)
+        elif w.kind == "dfp16":
+            rec = dfp16_step(weights, w.exp_w, x, w.exp_x, route=route)
+        else:
+            raise ValueError(w.kind)
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+        if callback is not None:
+            callback(t, rec)
+    return weights
