@@ -1,0 +1,320 @@
+#!/usr/bin/env python
+"""Benchmark of the integer-only (NITI) training step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload INDEX]
+
+Default workload: the large integer MLP (batch 8192, Linear 4096->4096 x4 +
+ReLU, Linear 4096->1000), one full forward / delta propagation / weight
+gradient / NITI update per step, seeded synthetic int8 data.
+
+Prints one JSON line (rank 0). `value` is training samples/s of the whole job
+(every rank runs its own replica: the step has no cross-GPU exchange here);
+device time per step is taken with CUDA events on the step's stream, with L2
+flushed (a 256 MB write) before every timed step and the flush left out of the
+timing. `roofline` is the tensor-core contraction class timed live with events
+around each of its launches; `e2e` is the same metric through the host-buffer
+C-ABI call (ito_train_step_host: input copy, step, stats copy back);
+`cpu_baseline` is the CPU oracle on a bounded sample of the same workload.
+
+--impl reference runs the CPU oracle (the reference of this build: the pages
+publish no implementation) on the same workload, a bounded batch slice per
+step, and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "integer training samples/s and INT8 TOPS (% of dense INT8 peak), bit-exact"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def algorithmic_ops(w):
+    """Integer ops (2 per multiply-accumulate) of one training step."""
+    if w.kind != "mlp":
+        raise ValueError("bench covers the MLP workloads")
+    B, d = w.batch, w.dims
+    fwd = sum(d[i] * d[i + 1] for i in range(len(d) - 1))
+    dgrad = sum(d[i] * d[i + 1] for i in range(1, len(d) - 1))
+    return 2.0 * B * (2 * fwd + dgrad)
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "ito_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                p = [t.strip() for t in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, sample_batch):
+    """The CPU oracle (plain C loops, OpenMP over output rows) on one training
+    step of `sample_batch` samples of workload w."""
+    import numpy as np
+    import oracle as O
+    import seeded_inputs as si
+    O.build()
+    weights = si.make_weights(w)
+    x, labels = si.make_batch(w, 0)
+    x, labels = np.ascontiguousarray(x[:sample_batch]), np.ascontiguousarray(labels[:sample_batch])
+    t0 = time.perf_counter()
+    O.mlp_step(weights, x, labels, route="loops")
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return sample_batch / dt, dt, cores
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle as O
+    import seeded_inputs as si
+    O.build()
+    sample = args.ref_batch
+    weights = si.make_weights(w)
+    batches = []
+    for t in range(2):
+        x, labels = si.make_batch(w, t)
+        batches.append((np.ascontiguousarray(x[:sample]), np.ascontiguousarray(labels[:sample])))
+    for i in range(args.warmup):
+        x, lab = batches[i % 2]
+        O.mlp_step(weights, x, lab, route="loops")
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        x, lab = batches[i % 2]
+        rec = O.mlp_step(weights, x, lab, route="loops")
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+    dt = time.perf_counter() - t0
+    value = sample * args.steps / dt
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims),
+                   "reference_step_batch": sample},
+        "cpu_baseline": {"value": value, "unit": "samples/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: one oracle training step on %d of the %d samples" % (sample, w.batch)},
+        "e2e": {"value": value, "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "int_tops": algorithmic_ops(w) * sample / w.batch * args.steps / dt / 1e12,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import integer_only_nn_gb300 as ito
+    import seeded_inputs as si
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # cpu baseline first (rank 0, one GPU): before the GPU work, so no CUDA
+    # context competes with the host cores
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, cores = cpu_baseline(w, args.cpu_batch)
+        cpu = {"value": v, "unit": "samples/s", "cores": cores, "kind": "oracle",
+               "sample": "one oracle training step (C loops) on %d of the %d samples of %s, %.1f s"
+                         % (args.cpu_batch, w.batch, w.name, dt)}
+
+    stream = torch.cuda.current_stream()
+    model = ito.Model(ito.layers_for(w), w.batch)
+    for l, W in enumerate(si.make_weights(w)):
+        model.set_weights(l, W)
+    xs, ls = [], []
+    for t in range(2):
+        x, labels = si.make_batch(w, t)
+        xs.append(torch.from_numpy(x).cuda())
+        ls.append(torch.from_numpy(labels).cuda())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    K, Wm = args.steps, args.warmup
+
+    for i in range(Wm):
+        model.train_step(xs[i % 2], ls[i % 2])
+    torch.cuda.synchronize()
+    assert ito.ito_get_error() == 0
+
+    model.profile(True)
+    model.profile_read()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = Clocks(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for k in range(K):
+        flush.fill_(k & 0xFF)
+        starts[k].record(stream)
+        model.train_step(xs[k % 2], ls[k % 2])
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    prof = model.profile_read()
+    model.profile(False)
+    err = ito.ito_get_error()
+    if err != 0:
+        raise RuntimeError("device error word %d after the timed steps" % err)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    launches = model.kernels_per_step()
+
+    # end to end through the host-buffer entry point
+    x_h = torch.from_numpy(si.make_batch(w, 0)[0]).pin_memory()
+    l_h = torch.from_numpy(si.make_batch(w, 0)[1]).pin_memory()
+    st_h = torch.zeros(model.num_stats(), dtype=torch.int32).pin_memory()
+    for _ in range(2):
+        model.train_step_host(x_h, l_h, st_h)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        model.train_step_host(x_h, l_h, st_h)
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    pk, pk_src = peaks()
+    samples = world * w.batch * K
+    value = samples / (total_ms / 1000.0)
+    g_ms, g_work, g_n = prof["gemm"]
+    g_tflops = g_work / (g_ms / 1000.0) / 1e12
+    peak = float(pk["bf16_tflops_sustained"])
+    r_ms, r_work, _ = prof["requant"]
+    u_ms, u_work, _ = prof["update"]
+    hbm = float(pk["hbm_gbs"])
+    line = {
+        "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims),
+                   "l2": "flushed by a 256 MB write before every timed step; flush not timed",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "int_tops": algorithmic_ops(w) * world * K / (total_ms / 1000.0) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (bf16-embedded int8 contractions, all GEMM launches)",
+                     "achieved": g_tflops, "peak": peak, "unit": "TFLOP/s", "frac": g_tflops / peak,
+                     "peak_source": "bf16_tflops_sustained, %s" % pk_src, "traffic": None,
+                     "launches_timed": g_n},
+        "passes": {"requant_gbs": r_work / (r_ms / 1000.0) / 1e9 if r_ms else None,
+                   "update_gbs": u_work / (u_ms / 1000.0) / 1e9 if u_ms else None,
+                   "hbm_peak_gbs": hbm, "peak_source": pk_src,
+                   "ms_per_step": {k: v[0] / K for k, v in prof.items()}},
+        "e2e": {"value": samples / e2e_s, "unit": "samples/s",
+                "h2d_bytes_per_step": int(x_h.numel() + 4 * l_h.numel()),
+                "d2h_bytes_per_step": int(4 * st_h.numel())},
+        "gpu_launches": launches * K,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="3")
+    ap.add_argument("--cpu-batch", type=int, default=128, help="samples in the CPU-oracle baseline step")
+    ap.add_argument("--ref-batch", type=int, default=16, help="samples per reference-arm oracle step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    import seeded_inputs as si
+    w = si.by_name(int(args.workload) if args.workload.isdigit() else args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

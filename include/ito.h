@@ -1,0 +1,275 @@
+/*
+ * ito.h -- C ABI of the integer-only training library for one GB300 GPU
+ * (sm_103a).
+ *
+ * What it computes: the NITI integer training step -- int8 x int8 -> int32
+ * contractions for the forward pass, delta propagation and weight gradient,
+ * each followed by a per-tensor dynamic-shift requantisation, and the NITI
+ * integer weight update -- as described in "Integer On-Device Training:
+ * Overview" (TI C2000 MCU AI user guide), section 3 "The NITI Algorithm",
+ * "The Solution: Dynamic Shifts", Steps 1-5:
+ *
+ *   max_val  = max |G|                                   (Step 1)
+ *   shift    = max(0, ceil(log2(max_val + 1)) - target_bits)   (Step 2)
+ *   Gq       = round-half-up(G >> shift), saturated to int8     (Step 3)
+ *   wshift   = max(0, shift - mu_weight)                 (Step 4)
+ *   W        = sat_int8(W - round-half-up(Gq >> wshift)) (Steps 4-5)
+ *
+ * Conventions (all entry points):
+ *  - Tensors are row-major. Linear weights are indexed W[oc * IC + ic]
+ *    (TiGrIS "Compilation Pipeline", pass 3 "Matrix product relabel");
+ *    activations are [B][features]; conv activations are NHWC and conv weights
+ *    [OC][3][3][IC] (the same page, emission stage "Layout transpose").
+ *  - Tensor pointers are DEVICE pointers owned by the caller unless an entry
+ *    point says "host". The library never frees them and never keeps them after
+ *    the call returns (a model keeps only memory it allocated itself).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Calls only enqueue work on it and return before it runs, unless
+ *    the entry point says it synchronises.
+ *  - Max and shift scalars stay on the device, in caller buffers.
+ *  - Return value: an ito_status. ITO_ERR_ARG / ITO_ERR_SHAPE are detected on
+ *    the host before anything is enqueued; ITO_ERR_CUDA reports a failed launch
+ *    or runtime call (ito_last_error_string() gives its text). Kernels never
+ *    trap: a failure they detect (a bounded wait that gave up) is written to a
+ *    per-device error word that ito_get_error() reads and clears.
+ *  - Rounding "round-half-up" is floor(x / 2^s + 1/2): ties go toward +inf.
+ *    sat_int8 clamps to [-128, 127].
+ */
+#ifndef ITO_H
+#define ITO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ito_status {
+    ITO_OK = 0,
+    ITO_ERR_ARG = 1,          /* null or misaligned pointer, unknown enum value */
+    ITO_ERR_SHAPE = 2,        /* non-positive, inconsistent or too large size */
+    ITO_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed */
+    ITO_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (device error word) */
+    ITO_ERR_EXPONENT = 5,     /* a DFP16 shared exponent left the signed 8-bit range */
+    ITO_ERR_UNSUPPORTED = 6   /* a valid request this library does not implement */
+} ito_status;
+
+/* NITI parameters: target_bits (7 for int8 tensors) and mu_weight (the
+ * learning-rate control of Step 4). */
+typedef struct ito_niti_params {
+    int32_t target_bits;
+    int32_t mu_weight;
+} ito_niti_params;
+
+/* ------------------------------------------------------------------------
+ * Library state
+ * ---------------------------------------------------------------------- */
+
+/* Reads and clears the current device's error word (ITO_OK if no kernel
+ * reported a failure). Synchronises the device. */
+int ito_get_error(void);
+
+/* Text of the last ITO_ERR_CUDA / ITO_ERR_ARG / ITO_ERR_SHAPE raised on this
+ * host thread; never NULL. */
+const char *ito_last_error_string(void);
+
+/* Library version, for the Python binding's sanity check. */
+int ito_version(void);
+
+/* ------------------------------------------------------------------------
+ * Single-layer operations (int8 Linear layer, NITI)
+ *
+ * Contractions run on the tensor cores with bf16 operands that hold the int8
+ * values exactly; sums are exact (fp32 accumulation over K chunks of at most
+ * 1024 terms, each chunk's integer result added in int32). A caller workspace
+ * of ito_linear_workspace_size() bytes holds the bf16 operand copies.
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of device workspace any of ito_linear_fwd / _bwd_delta / _wgrad needs
+ * for these sizes (0 on invalid sizes). */
+size_t ito_linear_workspace_size(int B, int IC, int OC);
+
+/* Forward contraction + requantisation of one Linear layer ("Integer
+ * On-Device Training: Overview", section 3, Steps 1-3 applied to the layer
+ * output; section 7 layer types Linear and Linear+ReLU):
+ *   y32[b][oc] = sum_ic x[b][ic] * W[oc][ic]        (int32, exact)
+ *   *d_max     = max |y32|   (uint32; |INT32_MIN| = 2^31 fits)
+ *   *d_shift   = max(0, bitlen(*d_max) - p.target_bits)
+ *   y[b][oc]   = sat_int8(round-half-up(y32 >> shift)), then max(0, .) if relu
+ * x: int8 [B][IC]; W: int8 [OC][IC]; y32: int32 [B][OC]; y: int8 [B][OC].
+ * d_max, d_shift: one device scalar each. workspace: device, 256-byte
+ * aligned, workspace_bytes >= ito_linear_workspace_size(B, IC, OC).
+ * Errors: ITO_ERR_ARG (null pointer, misaligned workspace),
+ * ITO_ERR_SHAPE (B, IC or OC < 1, or a contraction length above 2^20). */
+int ito_linear_fwd(const int8_t *x, const int8_t *W, int B, int IC, int OC, int relu,
+                   ito_niti_params p, void *workspace, size_t workspace_bytes,
+                   int32_t *y32, uint32_t *d_max, int32_t *d_shift, int8_t *y, void *stream);
+
+/* Delta propagation of one Linear layer (same page, the note under Step 5:
+ * the propagated delta is requantised to target_bits = 7 so it fits int8),
+ * gated by the ReLU of the layer below:
+ *   d32[b][ic]      = sum_oc delta[b][oc] * W[oc][ic]    (int32, exact)
+ *   *d_max, *d_shift as in ito_linear_fwd
+ *   delta_prev[b][ic] = (a_prev == NULL || a_prev[b][ic] > 0)
+ *                        ? sat_int8(round-half-up(d32 >> shift)) : 0
+ * delta: int8 [B][OC]; W: int8 [OC][IC] (the weights before this step's
+ * update); a_prev: int8 [B][IC] or NULL; d32: int32 [B][IC];
+ * delta_prev: int8 [B][IC]. Errors as ito_linear_fwd. */
+int ito_linear_bwd_delta(const int8_t *delta, const int8_t *W, const int8_t *a_prev, int B, int IC,
+                         int OC, ito_niti_params p, void *workspace, size_t workspace_bytes,
+                         int32_t *d32, uint32_t *d_max, int32_t *d_shift, int8_t *delta_prev,
+                         void *stream);
+
+/* Weight gradient of one Linear layer, summed over the batch (the
+ * "accumulated gradient tensor G for one weight matrix" of Step 1):
+ *   G[oc][ic] = sum_b delta[b][oc] * a_prev[b][ic]    (int32, exact)
+ *   *d_max    = max |G|
+ * delta: int8 [B][OC]; a_prev: int8 [B][IC] (the layer's input);
+ * G: int32 [OC][IC]. Errors as ito_linear_fwd. */
+int ito_linear_wgrad(const int8_t *delta, const int8_t *a_prev, int B, int IC, int OC,
+                     void *workspace, size_t workspace_bytes, int32_t *G, uint32_t *d_max,
+                     void *stream);
+
+/* NITI weight update, Steps 2-5, in place (reading of Step 4: its operand is
+ * G_quantized, the tensor already shifted and saturated in Step 3):
+ *   s = max(0, bitlen(*d_max) - p.target_bits); ws = max(0, s - p.mu_weight)
+ *   W[i] = sat_int8(W[i] - round-half-up(sat_int8(round-half-up(G[i] >> s)) >> ws))
+ * W: int8 [n] (updated in place); G: int32 [n]; d_max: max|G| (as written
+ * by ito_linear_wgrad). d_shift, d_wshift: device scalars receiving s and
+ * ws (may be NULL). d_nonzero: device uint32 to which the number of nonzero
+ * weight steps is ADDED (may be NULL; the caller zeroes it).
+ * Errors: ITO_ERR_ARG (null W, G or d_max), ITO_ERR_SHAPE (n < 1). */
+int ito_niti_update(int8_t *W, const int32_t *G, int64_t n, const uint32_t *d_max,
+                    ito_niti_params p, int32_t *d_shift, int32_t *d_wshift, uint32_t *d_nonzero,
+                    void *stream);
+
+/* Top error written by the user's compute_loss ("Integer On-Device Training:
+ * Overview", section 4: compute_loss reads the int8 logits and writes dy):
+ *   delta[b][j] = sat_int8(logits[b][j] - target_mag * [j == labels[b]])
+ * logits: int8 [B][C]; labels: int32 [B] in [0, C); delta: int8 [B][C].
+ * A label outside [0, C) contributes no target (the row is copied).
+ * Errors: ITO_ERR_ARG, ITO_ERR_SHAPE. */
+int ito_top_error(const int8_t *logits, const int32_t *labels, int B, int C, int32_t target_mag,
+                  int8_t *delta, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Models: a sequential stack of trainable layers ("Integer On-Device
+ * Training: Overview", section 4: INT_LAYERS[], an array of layer descriptors
+ * with mutable int8 weights; INTODT_Forward / INTODT_Backward / INTODT_Infer).
+ * A model owns all its device memory (allocated at creation, nothing is
+ * allocated per step) and keeps every intermediate tensor of the last step.
+ * ---------------------------------------------------------------------- */
+
+typedef enum ito_layer_kind {
+    ITO_LAYER_LINEAR = 0,        /* Linear producing logits (last layer) */
+    ITO_LAYER_LINEAR_RELU = 1,   /* Linear + ReLU */
+    ITO_LAYER_CONV3X3_RELU = 2,  /* 3x3 Conv2D + ReLU, pad 1, NHWC, weights [OC][3][3][IC] */
+    ITO_LAYER_GAP = 3            /* global integer sum pooling + requantisation (no weights) */
+} ito_layer_kind;
+
+typedef struct ito_layer_desc {
+    int32_t kind;          /* ito_layer_kind */
+    int32_t in_features;   /* IC (channels for conv / GAP) */
+    int32_t out_features;  /* OC (ignored for GAP: equals in_features) */
+    int32_t in_h, in_w;    /* spatial input size (conv / GAP); 0 for Linear */
+    int32_t stride;        /* conv stride (1 or 2); 0 otherwise */
+} ito_layer_desc;
+
+typedef struct ito_model ito_model;
+
+/* Creates a model on the current device. The stack must be a sequence of
+ * conv layers, optionally one GAP, then Linear(+ReLU) layers ending with one
+ * ITO_LAYER_LINEAR. Weights start at zero (set them with
+ * ito_model_set_weights). target_mag: the integer target of the true class
+ * in the top error (64).
+ * Errors: ITO_ERR_ARG, ITO_ERR_SHAPE (inconsistent sizes),
+ * ITO_ERR_UNSUPPORTED (a layer order outside the one above), ITO_ERR_CUDA
+ * (allocation failed). */
+int ito_model_create(const ito_layer_desc *layers, int n_layers, int batch, ito_niti_params p,
+                     int32_t target_mag, ito_model **out);
+
+/* Frees the model's device memory. Synchronises the device. NULL is a no-op. */
+int ito_model_destroy(ito_model *m);
+
+/* Copies weights of trainable layer `layer` (counted over layers that have
+ * weights) in or out. W points to int8 [OC][IC] or [OC][3][3][IC]; host
+ * memory if `on_host` != 0, else device memory. Enqueued on `stream`; with
+ * host memory the call synchronises the stream. */
+int ito_model_set_weights(ito_model *m, int layer, const int8_t *W, int on_host, void *stream);
+int ito_model_get_weights(const ito_model *m, int layer, int8_t *W, int on_host, void *stream);
+
+/* Looks up a named device tensor of the last step (names as in the CPU
+ * oracle: "y0" int32 forward contraction of layer 0, "a0" its int8 output,
+ * "e0" int8 delta at the output of layer 0, "d1" int32 delta-propagation
+ * contraction of layer 1, "g0" int32 weight gradient, "w0" int8 weights,
+ * "stats" int32 scalars; see ito_model_stat_index). Writes the device
+ * pointer, the element type (1 = int8, 2 = int16, 4 = int32, 8 = int64) and
+ * element count. The pointer stays valid until ito_model_destroy.
+ * Errors: ITO_ERR_ARG (unknown name). */
+int ito_model_tensor(const ito_model *m, const char *name, void **dev_ptr, int *elem_bytes,
+                     int64_t *numel);
+
+/* Position of a named scalar in the model's "stats" array (int32), e.g.
+ * "ymax0", "ys0", "dmax1", "ds1", "gmax0", "gs0", "ws0", "nz0", "pmax",
+ * "ps"; -1 if unknown. Max values are stored as their uint32 bit pattern. */
+int ito_model_stat_index(const ito_model *m, const char *name);
+
+/* Number of int32 entries in the stats array. */
+int ito_model_num_stats(const ito_model *m);
+
+/* One training step on one batch (device pointers): forward through all
+ * layers, top error against `labels`, then for each layer from the top down:
+ * delta propagation with the pre-update weights (not for the first layer),
+ * weight gradient, NITI update. x: int8 [batch][in_features] (NHWC for a conv
+ * first layer); labels: int32 [batch]. Enqueued on `stream`; no host
+ * synchronisation. */
+int ito_train_step(ito_model *m, const int8_t *x, const int32_t *labels, void *stream);
+
+/* The same step from HOST buffers: copies x and labels into the model's
+ * device buffers, runs the step, copies the stats array (ito_model_num_stats
+ * int32) back to stats_host (may be NULL), and synchronises the stream.
+ * Host buffers should be pinned for full copy speed. */
+int ito_train_step_host(ito_model *m, const int8_t *x_host, const int32_t *labels_host,
+                        int32_t *stats_host, void *stream);
+
+/* Forward pass only ("INTODT_Infer"): writes the int8 logits [batch][C]. */
+int ito_infer(ito_model *m, const int8_t *x, int8_t *logits, void *stream);
+
+/* Checkpoint ("Trained Weights in RAM": snapshot the weight arrays and
+ * restore them before training resumes): raw little-endian int8 weights of
+ * every trainable layer after a small header with the layer shapes.
+ * Synchronise the device. Errors: ITO_ERR_ARG (path), ITO_ERR_SHAPE (file
+ * does not match the model). */
+int ito_model_save(const ito_model *m, const char *path);
+int ito_model_load(ito_model *m, const char *path);
+
+/* ------------------------------------------------------------------------
+ * Measurement hooks (no counterpart in the pages; used by the benchmark)
+ * ---------------------------------------------------------------------- */
+
+typedef enum ito_prof_class {
+    ITO_PROF_GEMM = 0,      /* tensor-core contractions; work = 2*M*N*K integer ops */
+    ITO_PROF_REQUANT = 1,   /* requantisation passes; work = algorithmic HBM bytes */
+    ITO_PROF_UPDATE = 2,    /* NITI weight updates; work = algorithmic HBM bytes */
+    ITO_PROF_OTHER = 3,     /* conversion, im2col/col2im, pooling, top error; work = bytes */
+    ITO_PROF_NCLASS = 4
+} ito_prof_class;
+
+/* Enables (1) or disables (0) per-kernel timing: when enabled, every kernel a
+ * step launches is bracketed by CUDA events recorded on the step's stream. */
+int ito_model_profile(ito_model *m, int enable);
+
+/* Adds up the timings of all steps since the last read (waiting for their
+ * events) and clears them: ms[c], work[c] and launches[c] for each of the
+ * ITO_PROF_NCLASS classes (arrays of ITO_PROF_NCLASS entries). */
+int ito_model_profile_read(ito_model *m, double *ms, double *work, int64_t *launches);
+
+/* Number of kernels the model launches per training step. */
+int ito_model_kernels_per_step(const ito_model *m);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ITO_H */

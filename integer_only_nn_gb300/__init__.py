@@ -1,0 +1,328 @@
+"""Python binding of libito.so, the integer-only (NITI / DFP16) training library
+for one GB300 GPU.
+
+Argument marshalling only: every function here hands torch tensors' device
+pointers and the current CUDA stream to the C ABI declared in include/ito.h,
+under the same names. All arithmetic runs in the library's CUDA kernels. If the
+shared library has not been built, importing this package raises ImportError;
+there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libito.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libito.so is not built: run `python -m integer_only_nn_gb300.build` "
+                      "(or __graft_entry__.build()) on a machine with nvcc")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+ITO_OK, ITO_ERR_ARG, ITO_ERR_SHAPE, ITO_ERR_CUDA, ITO_ERR_TIMEOUT, ITO_ERR_EXPONENT, ITO_ERR_UNSUPPORTED = range(7)
+ITO_LAYER_LINEAR, ITO_LAYER_LINEAR_RELU, ITO_LAYER_CONV3X3_RELU, ITO_LAYER_GAP = range(4)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+
+class NitiParams(ctypes.Structure):
+    _fields_ = [("target_bits", ctypes.c_int32), ("mu_weight", ctypes.c_int32)]
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("in_features", ctypes.c_int32), ("out_features", ctypes.c_int32),
+                ("in_h", ctypes.c_int32), ("in_w", ctypes.c_int32), ("stride", ctypes.c_int32)]
+
+
+_SIGS = {
+    "ito_version": (_I, []),
+    "ito_get_error": (_I, []),
+    "ito_last_error_string": (ctypes.c_char_p, []),
+    "ito_linear_workspace_size": (_SZ, [_I, _I, _I]),
+    "ito_linear_fwd": (_I, [_P, _P, _I, _I, _I, _I, NitiParams, _P, _SZ, _P, _P, _P, _P, _P]),
+    "ito_linear_bwd_delta": (_I, [_P, _P, _P, _I, _I, _I, NitiParams, _P, _SZ, _P, _P, _P, _P, _P]),
+    "ito_linear_wgrad": (_I, [_P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P]),
+    "ito_niti_update": (_I, [_P, _P, _I64, _P, NitiParams, _P, _P, _P, _P]),
+    "ito_top_error": (_I, [_P, _P, _I, _I, _I32, _P, _P]),
+    "ito_model_create": (_I, [ctypes.POINTER(LayerDesc), _I, _I, NitiParams, _I32, ctypes.POINTER(_P)]),
+    "ito_model_destroy": (_I, [_P]),
+    "ito_model_set_weights": (_I, [_P, _I, _P, _I, _P]),
+    "ito_model_get_weights": (_I, [_P, _I, _P, _I, _P]),
+    "ito_model_tensor": (_I, [_P, ctypes.c_char_p, ctypes.POINTER(_P), ctypes.POINTER(_I), ctypes.POINTER(_I64)]),
+    "ito_model_stat_index": (_I, [_P, ctypes.c_char_p]),
+    "ito_model_num_stats": (_I, [_P]),
+    "ito_train_step": (_I, [_P, _P, _P, _P]),
+    "ito_train_step_host": (_I, [_P, _P, _P, _P, _P]),
+    "ito_infer": (_I, [_P, _P, _P, _P]),
+    "ito_model_save": (_I, [_P, ctypes.c_char_p]),
+    "ito_model_load": (_I, [_P, ctypes.c_char_p]),
+    "ito_model_profile": (_I, [_P, _I]),
+    "ito_model_profile_read": (_I, [_P, _P, _P, _P]),
+    "ito_model_kernels_per_step": (_I, [_P]),
+}
+
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+class ItoError(RuntimeError):
+    def __init__(self, code, text):
+        super().__init__("ito status %d: %s" % (code, text))
+        self.code = code
+
+
+def _check(code):
+    if code != ITO_OK:
+        raise ItoError(code, _lib.ito_last_error_string().decode(errors="replace"))
+    return code
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def params(target_bits=7, mu_weight=2) -> NitiParams:
+    return NitiParams(target_bits, mu_weight)
+
+
+def ito_version() -> int:
+    return _lib.ito_version()
+
+
+def ito_get_error() -> int:
+    return _lib.ito_get_error()
+
+
+# ----------------------------------------------------------- single layer
+
+def _workspace(B, IC, OC, device):
+    torch = _torch()
+    n = _lib.ito_linear_workspace_size(B, IC, OC)
+    return torch.empty(n + 256, dtype=torch.uint8, device=device), n
+
+
+def _aligned256(buf):
+    off = (-buf.data_ptr()) % 256
+    return ctypes.c_void_p(buf.data_ptr() + off)
+
+
+def ito_linear_fwd(x, W, relu, p=None, stream=None):
+    """-> (y32 int32 [B][OC], d_max uint32 as int32 [1], d_shift int32 [1], y int8 [B][OC])"""
+    torch = _torch()
+    B, IC = x.shape
+    OC = W.shape[0]
+    dev = x.device
+    y32 = torch.empty((B, OC), dtype=torch.int32, device=dev)
+    y = torch.empty((B, OC), dtype=torch.int8, device=dev)
+    mx = torch.zeros(1, dtype=torch.int32, device=dev)
+    sh = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws, n = _workspace(B, IC, OC, dev)
+    _check(_lib.ito_linear_fwd(_ptr(x), _ptr(W), B, IC, OC, int(relu), p or params(), _aligned256(ws), n,
+                               _ptr(y32), _ptr(mx), _ptr(sh), _ptr(y), _stream(stream)))
+    return y32, mx, sh, y
+
+
+def ito_linear_bwd_delta(delta, W, a_prev, p=None, stream=None):
+    """-> (d32 int32 [B][IC], d_max, d_shift, delta_prev int8 [B][IC])"""
+    torch = _torch()
+    B, OC = delta.shape
+    IC = W.shape[1]
+    dev = delta.device
+    d32 = torch.empty((B, IC), dtype=torch.int32, device=dev)
+    dp = torch.empty((B, IC), dtype=torch.int8, device=dev)
+    mx = torch.zeros(1, dtype=torch.int32, device=dev)
+    sh = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws, n = _workspace(B, IC, OC, dev)
+    _check(_lib.ito_linear_bwd_delta(_ptr(delta), _ptr(W), _ptr(a_prev), B, IC, OC, p or params(),
+                                     _aligned256(ws), n, _ptr(d32), _ptr(mx), _ptr(sh), _ptr(dp), _stream(stream)))
+    return d32, mx, sh, dp
+
+
+def ito_linear_wgrad(delta, a_prev, stream=None):
+    """-> (G int32 [OC][IC], d_max)"""
+    torch = _torch()
+    B, OC = delta.shape
+    IC = a_prev.shape[1]
+    dev = delta.device
+    G = torch.empty((OC, IC), dtype=torch.int32, device=dev)
+    mx = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws, n = _workspace(B, IC, OC, dev)
+    _check(_lib.ito_linear_wgrad(_ptr(delta), _ptr(a_prev), B, IC, OC, _aligned256(ws), n, _ptr(G), _ptr(mx),
+                                 _stream(stream)))
+    return G, mx
+
+
+def ito_niti_update(W, G, d_max, p=None, stream=None):
+    """In place on W; -> (d_shift, d_wshift, d_nonzero) device int32 [1] each."""
+    torch = _torch()
+    dev = W.device
+    sh = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(1, dtype=torch.int32, device=dev)
+    nz = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(_lib.ito_niti_update(_ptr(W), _ptr(G), W.numel(), _ptr(d_max), p or params(), _ptr(sh), _ptr(ws),
+                                _ptr(nz), _stream(stream)))
+    return sh, ws, nz
+
+
+def ito_top_error(logits, labels, target_mag=64, stream=None):
+    torch = _torch()
+    B, C = logits.shape
+    d = torch.empty((B, C), dtype=torch.int8, device=logits.device)
+    _check(_lib.ito_top_error(_ptr(logits), _ptr(labels), B, C, target_mag, _ptr(d), _stream(stream)))
+    return d
+
+
+# ------------------------------------------------------------------ model
+
+_DTYPES = {1: "int8", 2: "int16", 4: "int32", 8: "int64"}
+
+
+def layers_for(workload):
+    """ito layer descriptors of a seeded_inputs.Workload (mlp or cnn)."""
+    out = []
+    if workload.kind == "mlp":
+        d = workload.dims
+        for i in range(len(d) - 1):
+            kind = ITO_LAYER_LINEAR if i == len(d) - 2 else ITO_LAYER_LINEAR_RELU
+            out.append(LayerDesc(kind, d[i], d[i + 1], 0, 0, 0))
+    elif workload.kind == "cnn":
+        H, W, C = workload.image
+        for (ic, oc, s) in workload.convs:
+            out.append(LayerDesc(ITO_LAYER_CONV3X3_RELU, ic, oc, H, W, s))
+            H, W = (H + 2 - 3) // s + 1, (W + 2 - 3) // s + 1
+        out.append(LayerDesc(ITO_LAYER_GAP, workload.convs[-1][1], workload.convs[-1][1], H, W, 0))
+        out.append(LayerDesc(ITO_LAYER_LINEAR, workload.fc[0], workload.fc[1], 0, 0, 0))
+    else:
+        raise ValueError(workload.kind)
+    return out
+
+
+class Model:
+    """An ito_model: a sequential int8 layer stack that trains with NITI."""
+
+    def __init__(self, layers, batch, target_bits=7, mu_weight=2, target_mag=64):
+        arr = (LayerDesc * len(layers))(*layers)
+        h = ctypes.c_void_p()
+        _check(_lib.ito_model_create(arr, len(layers), batch, NitiParams(target_bits, mu_weight), target_mag,
+                                     ctypes.byref(h)))
+        self._h = h
+        self.batch = batch
+        self.n_weight_layers = sum(1 for l in layers if l.kind != ITO_LAYER_GAP)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.ito_model_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_weights(self, layer, W, stream=None):
+        """W: torch int8 tensor on the GPU, or a numpy int8 array (host)."""
+        if hasattr(W, "data_ptr"):
+            _check(_lib.ito_model_set_weights(self._h, layer, _ptr(W.contiguous()), 0, _stream(stream)))
+        else:
+            import numpy as np
+            a = np.ascontiguousarray(W, dtype=np.int8)
+            _check(_lib.ito_model_set_weights(self._h, layer, a.ctypes.data_as(ctypes.c_void_p), 1,
+                                              _stream(stream)))
+
+    def tensor(self, name):
+        """A torch view (on the GPU) of a named model tensor."""
+        torch = _torch()
+        ptr, eb, n = ctypes.c_void_p(), ctypes.c_int(), ctypes.c_int64()
+        _check(_lib.ito_model_tensor(self._h, name.encode(), ctypes.byref(ptr), ctypes.byref(eb), ctypes.byref(n)))
+        dt = getattr(torch, _DTYPES[eb.value])
+        return _from_ptr(ptr.value, n.value, dt, eb.value)
+
+    def stat_index(self, name) -> int:
+        return _lib.ito_model_stat_index(self._h, name.encode())
+
+    def num_stats(self) -> int:
+        return _lib.ito_model_num_stats(self._h)
+
+    def stats(self) -> dict:
+        """All named scalars of the last step, read back to the host."""
+        v = self.tensor("stats").cpu().tolist()
+        out = {}
+        for key in ("ymax", "ys", "dmax", "ds", "gmax", "gs", "ws", "nz"):
+            l = 0
+            while True:
+                i = self.stat_index("%s%d" % (key, l))
+                if i < 0:
+                    break
+                val = v[i]
+                out["%s%d" % (key, l)] = val & 0xFFFFFFFF if key in ("ymax", "dmax", "gmax", "nz") else val
+                l += 1
+        for key in ("pmax", "ps"):
+            i = self.stat_index(key)
+            out[key] = v[i] & 0xFFFFFFFF if key == "pmax" else v[i]
+        return out
+
+    def train_step(self, x, labels, stream=None):
+        _check(_lib.ito_train_step(self._h, _ptr(x), _ptr(labels), _stream(stream)))
+
+    def train_step_host(self, x_host, labels_host, stats_host=None, stream=None):
+        """Host (pinned) torch tensors in, stats out; synchronises."""
+        _check(_lib.ito_train_step_host(self._h, _ptr(x_host), _ptr(labels_host), _ptr(stats_host),
+                                        _stream(stream)))
+
+    def infer(self, x, logits, stream=None):
+        _check(_lib.ito_infer(self._h, _ptr(x), _ptr(logits), _stream(stream)))
+
+    def profile(self, enable=True):
+        _check(_lib.ito_model_profile(self._h, int(enable)))
+
+    def profile_read(self):
+        """{class: (ms, work, launches)} summed since the last read."""
+        ms = (ctypes.c_double * 4)()
+        work = (ctypes.c_double * 4)()
+        n = (ctypes.c_int64 * 4)()
+        _check(_lib.ito_model_profile_read(self._h, ms, work, n))
+        return {name: (ms[i], work[i], n[i]) for i, name in enumerate(("gemm", "requant", "update", "other"))}
+
+    def kernels_per_step(self) -> int:
+        return _lib.ito_model_kernels_per_step(self._h)
+
+    def save(self, path):
+        _check(_lib.ito_model_save(self._h, path.encode()))
+
+    def load(self, path):
+        _check(_lib.ito_model_load(self._h, path.encode()))
+
+
+class _CudaArray:
+    """Minimal __cuda_array_interface__ holder to view library-owned memory."""
+
+    def __init__(self, ptr, n, typestr):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (ptr, False), "version": 3}
+
+
+def _from_ptr(ptr, n, dtype, eb):
+    torch = _torch()
+    typestr = {1: "|i1", 2: "<i2", 4: "<i4", 8: "<i8"}[eb]
+    return torch.as_tensor(_CudaArray(ptr, n, typestr), device="cuda")

@@ -1,0 +1,281 @@
+// Bandwidth-bound kernels of the NITI step: requantisation of the int32
+// contraction results (with ReLU or a ReLU gate), the NITI weight update, the
+// top error, and int8 -> bf16 operand conversion. Each reads the per-tensor
+// max written by the contraction epilogue (the grid-wide dependency of NITI
+// Step 1 is the kernel boundary between them) and streams its tensor once,
+// eight elements per thread step with 16-byte accesses where the row length
+// allows.
+//
+// Rules: "Integer On-Device Training: Overview", section 3 "The NITI
+// Algorithm", Steps 1-5 (per-tensor max, bits_needed, shift, round-half-up,
+// weight_shift = shift - mu_weight, sat_int8 update) and the delta
+// propagation note (target_bits = 7).
+#include <cstdarg>
+#include <cstdio>
+
+#include "ito_device.cuh"
+#include "ito_internal.h"
+
+namespace ito {
+
+int launch_grid_blocks(int64_t work_items, int threads)
+{
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = kNumSMsHint;
+    }
+    int64_t b = (work_items + threads - 1) / threads;
+    int64_t cap = (int64_t)sms * 8;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return (int)b;
+}
+
+static inline bool aligned(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// ------------------------------------------------------------- conversion
+
+__global__ void k_i8_to_bf16_v8(const int8_t* __restrict__ src, int64_t rows, int64_t cols,
+                                uint16_t* __restrict__ dst, int64_t ldd)
+{
+    const int64_t groups = rows * (cols >> 3);
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i0 = g << 3;
+        const int64_t r = i0 / cols, c = i0 - r * cols;
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(src + i0));
+        const int8_t* b = reinterpret_cast<const int8_t*>(&v);
+        uint4 o;
+        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            ow[i] = (uint32_t)int_to_bf16_bits(b[2 * i]) | ((uint32_t)int_to_bf16_bits(b[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4*>(dst + r * ldd + c) = o;
+    }
+}
+
+__global__ void k_i8_to_bf16_1(const int8_t* __restrict__ src, int64_t rows, int64_t cols, uint16_t* __restrict__ dst,
+                               int64_t ldd)
+{
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i - r * cols;
+        dst[r * ldd + c] = int_to_bf16_bits(src[i]);
+    }
+}
+
+int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* dst, int64_t ldd, cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    if (cols % 8 == 0 && ldd % 8 == 0 && aligned(src, 8) && aligned(dst, 16))
+        k_i8_to_bf16_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(src, rows, cols, dst, ldd);
+    else
+        k_i8_to_bf16_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(src, rows, cols, dst, ldd);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "convert launch: %s", cudaGetErrorString(e));
+}
+
+// --------------------------------------------------------------- requant
+
+// q = sat8(rhu(y, s)); ReLU; gate
+__device__ __forceinline__ int32_t requant_one(int32_t y, int s, int relu, int gate_ok)
+{
+    int32_t q = sat8(rhu32(y, s));
+    if (relu && q < 0) q = 0;
+    return gate_ok ? q : 0;
+}
+
+__global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
+                             const uint32_t* __restrict__ d_max, int target_bits, int relu,
+                             const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
+                             int64_t ldb, int32_t* __restrict__ d_shift)
+{
+    const int s = shift_for(*d_max, target_bits);
+    if (d_shift && blockIdx.x == 0 && threadIdx.x == 0) *d_shift = s;
+    const int64_t groups = rows * (cols >> 3);
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i0 = g << 3;
+        const int4 y0 = __ldcs(reinterpret_cast<const int4*>(Y + i0));
+        const int4 y1 = __ldcs(reinterpret_cast<const int4*>(Y + i0 + 4));
+        const int32_t y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+        int8_t gv[8] = {1, 1, 1, 1, 1, 1, 1, 1};
+        if (gate) *reinterpret_cast<uint2*>(gv) = __ldg(reinterpret_cast<const uint2*>(gate + i0));
+        int8_t q8[8];
+        uint32_t qb[4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q8[i] = (int8_t)requant_one(y[i], s, relu, gv[i] > 0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            qb[i] = (uint32_t)int_to_bf16_bits(q8[2 * i]) | ((uint32_t)int_to_bf16_bits(q8[2 * i + 1]) << 16);
+        *reinterpret_cast<uint2*>(out8 + i0) = *reinterpret_cast<const uint2*>(q8);
+        if (outb) {
+            const int64_t r = i0 / cols, c = i0 - r * cols;
+            *reinterpret_cast<uint4*>(outb + r * ldb + c) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
+        }
+    }
+}
+
+__global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
+                            const uint32_t* __restrict__ d_max, int target_bits, int relu,
+                            const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
+                            int64_t ldb, int32_t* __restrict__ d_shift)
+{
+    const int s = shift_for(*d_max, target_bits);
+    if (d_shift && blockIdx.x == 0 && threadIdx.x == 0) *d_shift = s;
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t q = requant_one(Y[i], s, relu, gate ? gate[i] > 0 : 1);
+        out8[i] = (int8_t)q;
+        if (outb) {
+            const int64_t r = i / cols, c = i - r * cols;
+            outb[r * ldb + c] = int_to_bf16_bits(q);
+        }
+    }
+}
+
+int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
+                   const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    const bool vec = cols % 8 == 0 && aligned(Y, 16) && aligned(out8, 8) && (!gate || aligned(gate, 8)) &&
+                     (!outb || (aligned(outb, 16) && ldb % 8 == 0));
+    if (vec)
+        k_requant_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(Y, rows, cols, d_max, target_bits,
+                                                                               relu, gate, out8, outb, ldb, d_shift);
+    else
+        k_requant_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(Y, rows, cols, d_max, target_bits, relu,
+                                                                          gate, out8, outb, ldb, d_shift);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "requant launch: %s", cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------ NITI update
+
+// weight_delta of Steps 3-4: round(sat8(round(G >> s)) >> ws); the operand
+// of the second shift is G_quantized, as the step is written.
+__device__ __forceinline__ int32_t niti_step_delta(int32_t g, int s, int ws)
+{
+    const int32_t gq = sat8(rhu32(g, s));     // Step 3
+    return rhu32(gq, ws);                     // Step 4
+}
+
+__device__ __forceinline__ void count_nonzero(uint32_t cnt, uint32_t* d_nonzero)
+{
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(d_nonzero, cnt);
+}
+
+__global__ void k_niti_update_v8(int8_t* __restrict__ W, uint16_t* __restrict__ Wb, int64_t ldb,
+                                 const int32_t* __restrict__ G, int64_t rows, int64_t cols,
+                                 const uint32_t* __restrict__ d_max, int target_bits, int mu_weight,
+                                 int32_t* __restrict__ d_shift, int32_t* __restrict__ d_wshift,
+                                 uint32_t* __restrict__ d_nonzero)
+{
+    const int s = shift_for(*d_max, target_bits);
+    const int ws = s - mu_weight > 0 ? s - mu_weight : 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (d_shift) *d_shift = s;
+        if (d_wshift) *d_wshift = ws;
+    }
+    uint32_t cnt = 0;
+    const int64_t groups = rows * (cols >> 3);
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i0 = g << 3;
+        const int4 g0 = __ldcs(reinterpret_cast<const int4*>(G + i0));
+        const int4 g1 = __ldcs(reinterpret_cast<const int4*>(G + i0 + 4));
+        const int32_t gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        int8_t w8[8];
+        *reinterpret_cast<uint2*>(w8) = *reinterpret_cast<const uint2*>(W + i0);
+        uint32_t wb[4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int32_t dw = niti_step_delta(gv[i], s, ws);
+            cnt += dw != 0;
+            w8[i] = (int8_t)sat8(w8[i] - dw);          // Step 5
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            wb[i] = (uint32_t)int_to_bf16_bits(w8[2 * i]) | ((uint32_t)int_to_bf16_bits(w8[2 * i + 1]) << 16);
+        *reinterpret_cast<uint2*>(W + i0) = *reinterpret_cast<const uint2*>(w8);
+        if (Wb) {
+            const int64_t r = i0 / cols, c = i0 - r * cols;
+            *reinterpret_cast<uint4*>(Wb + r * ldb + c) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        }
+    }
+    if (d_nonzero) count_nonzero(cnt, d_nonzero);
+}
+
+__global__ void k_niti_update_1(int8_t* __restrict__ W, uint16_t* __restrict__ Wb, int64_t ldb,
+                                const int32_t* __restrict__ G, int64_t rows, int64_t cols,
+                                const uint32_t* __restrict__ d_max, int target_bits, int mu_weight,
+                                int32_t* __restrict__ d_shift, int32_t* __restrict__ d_wshift,
+                                uint32_t* __restrict__ d_nonzero)
+{
+    const int s = shift_for(*d_max, target_bits);
+    const int ws = s - mu_weight > 0 ? s - mu_weight : 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (d_shift) *d_shift = s;
+        if (d_wshift) *d_wshift = ws;
+    }
+    uint32_t cnt = 0;
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t dw = niti_step_delta(G[i], s, ws);
+        cnt += dw != 0;
+        const int8_t nw = (int8_t)sat8(W[i] - dw);
+        W[i] = nw;
+        if (Wb) {
+            const int64_t r = i / cols, c = i - r * cols;
+            Wb[r * ldb + c] = int_to_bf16_bits(nw);
+        }
+    }
+    if (d_nonzero) count_nonzero(cnt, d_nonzero);
+}
+
+int launch_niti_update(int8_t* W, uint16_t* Wb, int64_t ldb, const int32_t* G, int64_t rows, int64_t cols,
+                       const uint32_t* d_max, int target_bits, int mu_weight, int32_t* d_shift, int32_t* d_wshift,
+                       uint32_t* d_nonzero, cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    const bool vec = cols % 8 == 0 && aligned(W, 8) && aligned(G, 16) && (!Wb || (aligned(Wb, 16) && ldb % 8 == 0));
+    if (vec)
+        k_niti_update_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(
+            W, Wb, ldb, G, rows, cols, d_max, target_bits, mu_weight, d_shift, d_wshift, d_nonzero);
+    else
+        k_niti_update_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(
+            W, Wb, ldb, G, rows, cols, d_max, target_bits, mu_weight, d_shift, d_wshift, d_nonzero);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "update launch: %s", cudaGetErrorString(e));
+}
+
+// -------------------------------------------------------------- top error
+
+__global__ void k_top_error(const int8_t* __restrict__ logits, const int32_t* __restrict__ labels, int B, int C,
+                            int target_mag, int8_t* __restrict__ delta, uint16_t* __restrict__ deltab, int64_t ldb)
+{
+    const int64_t n = (int64_t)B * C;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int b = (int)(i / C), j = (int)(i - (int64_t)b * C);
+        const int32_t t = (labels[b] == j) ? target_mag : 0;
+        const int32_t d = sat8((int32_t)logits[i] - t);
+        delta[i] = (int8_t)d;
+        if (deltab) deltab[(int64_t)b * ldb + j] = int_to_bf16_bits(d);
+    }
+}
+
+int launch_top_error(const int8_t* logits, const int32_t* labels, int B, int C, int target_mag, int8_t* delta,
+                     uint16_t* deltab, int64_t ldb, cudaStream_t s)
+{
+    if (B < 1 || C < 1) return ITO_OK;
+    k_top_error<<<launch_grid_blocks((int64_t)B * C, 256), 256, 0, s>>>(logits, labels, B, C, target_mag, delta,
+                                                                         deltab, ldb);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "top error launch: %s", cudaGetErrorString(e));
+}
+
+}  // namespace ito

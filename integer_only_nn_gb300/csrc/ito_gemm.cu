@@ -1,0 +1,442 @@
+// Exact integer contractions C[M][N] = sum_k A(m,k) * B(n,k) for int8 data
+// ("Integer On-Device Training: Overview", section 2.1: the training pass is
+// dominated by multiply-accumulates across weight matrices; section 3: each
+// contraction result G is an int32 tensor whose max |G| drives the shift).
+//
+// Tensor-core path (k_gemm_tc): sm_103a has no integer tcgen05 MMA kind, so the
+// operands are bf16 tensors holding int8 values (every integer of magnitude
+// <= 256 is exact in bf16) and the MMA accumulates in fp32 in tensor memory.
+// Each product is at most 2^14 in magnitude, so a chunk of up to 1024
+// products sums to at most 2^24: every partial sum is an integer that fp32
+// represents exactly, whatever the order of additions. The K loop is cut
+// into such chunks; after each chunk the epilogue warps read the fp32
+// accumulator from tensor memory, convert it to int32 and add it into int32
+// registers, while the MMA warp fills the other of two accumulator buffers.
+// The epilogue of a tile writes the int32 tile and folds its max |C| into a
+// global atomicMax (the first half of the grid-wide max of NITI Step 1).
+//
+// Operands are loaded by TMA with 128-byte swizzle, either K-major
+// ([rows][K], K contiguous) or MN-major ([K][rows], rows contiguous), so the
+// forward (x.W^T), delta-propagation (delta.W) and weight-gradient
+// (delta^T.a) contractions read the same row-major tensors without any
+// transpose pass.
+//
+// SIMT path (k_gemm_simt): a plain tiled int32 kernel with arbitrary strides,
+// used as an independent on-GPU cross-check of the tensor-core path.
+#include <cstdio>
+#include <cstring>
+
+#include <cudaTypedefs.h>
+
+#include "ito_device.cuh"
+#include "ito_internal.h"
+
+namespace ito {
+
+// The device error word of this library (one per device).
+__device__ int g_device_error = 0;
+
+int* device_error_word()
+{
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
+}
+
+// ------------------------------------------------------------ tile schedule
+
+struct TileSched {
+    int num_m, num_n, group;
+    __device__ __forceinline__ void coords(int t, int& tm, int& tn) const
+    {
+        // groups of `group` m-tiles sweep all n-tiles, so consecutive CTAs
+        // share B tiles and a band of A tiles in L2
+        const int per_group = group * num_n;
+        const int g = t / per_group;
+        const int first_m = g * group;
+        const int gm = min(group, num_m - first_m);
+        const int r = t - g * per_group;
+        tm = first_m + r % gm;
+        tn = r / gm;
+    }
+};
+
+// ----------------------------------------------------- tensor-core kernel
+
+template <int BN>
+struct TcCfg {
+    static constexpr int BM = 128;
+    static constexpr int BK = 64;                          // 64 bf16 = one 128-byte swizzle row
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + EPI_WARPS * 32;    // producer warp, MMA warp, 8 epilogue warps
+    static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+              int K, int chunk_kb, int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max,
+              int* __restrict__ err)
+{
+    using Cfg = TcCfg<BN>;
+    constexpr int BM = Cfg::BM, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int HALF = BN / 2;                             // columns per epilogue warp
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t* empty_bar = full_bar + STAGES;
+    uint64_t* accf_bar = empty_bar + STAGES;   // [2] accumulator buffer filled
+    uint64_t* acce_bar = accf_bar + 2;         // [2] accumulator buffer drained
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const TileSched sched{(M + BM - 1) / BM, (N + BN - 1) / BN, 16};
+    const int num_tiles = sched.num_m * sched.num_n;
+    const int num_kb = (K + BK - 1) / BK;
+    const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf_bar[b], 1);
+            mbar_init(&acce_bar[b], Cfg::EPI_WARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                int tm, tn;
+                sched.coords(t, tm, tn);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
+                    uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
+                    uint8_t* sB = sA + Cfg::A_BYTES;
+                    if (!A_MN) {
+                        tma_load_2d(&tmA, &full_bar[stage], sA, kb * BK, tm * BM);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            tma_load_2d(&tmA, &full_bar[stage], sA + j * 8192, tm * BM + j * 64, kb * BK);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(&tmB, &full_bar[stage], sB, kb * BK, tn * BN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(&tmB, &full_bar[stage], sB + j * 8192, tn * BN + j * 64, kb * BK);
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (one thread)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                for (int c = 0; ok && c < num_chunks; ++c) {
+                    if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                    const int kb0 = c * chunk_kb;
+                    const int kb1 = min(num_kb, kb0 + chunk_kb);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full_bar[stage], phase, abort_flag, err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                        const uint32_t b0 = a0 + Cfg::A_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            // K-major: the 16-element K step is 32 bytes inside the swizzled row;
+                            // MN-major: it is 16 rows of 128 bytes
+                            const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, 8192, 1024)
+                                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                            const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
+                                                     : smem_desc_sw128(b0 + k * 32, 16, 1024);
+                            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        tc_commit(&empty_bar[stage]);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    tc_commit(&accf_bar[buf]);
+                    if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue: drain chunks into int32, then max + store
+        const int e = warp - 2;
+        const int quad = warp & 3;               // TMEM lanes this warp may access
+        const int half = e >> 2;                 // which half of the tile's columns
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            int tm, tn;
+            sched.coords(t, tm, tn);
+            int32_t acc[HALF];
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) acc[i] = 0;
+            for (int c = 0; c < num_chunks; ++c) {
+                if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + half * HALF);
+#pragma unroll
+                for (int j = 0; j < HALF / 32; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + j * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[j * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acce_bar[buf]);
+                if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+            }
+            if (!ok) break;
+            // out-of-range rows and columns read zero-filled operands, so they hold 0
+            uint32_t mx = 0;
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) mx = max(mx, abs_u32(acc[i]));
+            mx = __reduce_max_sync(0xffffffffu, mx);
+            if (lane == 0 && mx != 0) atomicMax(d_max, mx);
+            const int row = tm * BM + quad * 32 + lane;
+            const int col0 = tn * BN + half * HALF;
+            if (row < M) {
+                int32_t* dst = C + (int64_t)row * ldc + col0;
+                if (col0 + HALF <= N && (ldc & 3) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
+#pragma unroll
+                    for (int i = 0; i < HALF; i += 4)
+                        *reinterpret_cast<int4*>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i)
+                        if (col0 + i < N) dst[i] = acc[i];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// --------------------------------------------------------------- SIMT path
+
+constexpr int SIMT_BM = 64, SIMT_BN = 64, SIMT_BK = 32;
+
+__global__ void __launch_bounds__(256)
+    k_gemm_simt(const int8_t* __restrict__ A, int64_t sam, int64_t sak, const int8_t* __restrict__ B, int64_t sbn,
+                int64_t sbk, int M, int N, int K, int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max)
+{
+    __shared__ int8_t As[SIMT_BK][SIMT_BM];
+    __shared__ int8_t Bs[SIMT_BK][SIMT_BN];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int m0 = blockIdx.y * SIMT_BM, n0 = blockIdx.x * SIMT_BN;
+    int32_t acc[4][4] = {};
+    for (int k0 = 0; k0 < K; k0 += SIMT_BK) {
+#pragma unroll
+        for (int i = 0; i < (SIMT_BM * SIMT_BK) / 256; ++i) {
+            const int idx = threadIdx.x + 256 * i;
+            const int r = idx % SIMT_BM, k = idx / SIMT_BM;
+            const int gm = m0 + r, gn = n0 + r, gk = k0 + k;
+            As[k][r] = (gm < M && gk < K) ? A[gm * sam + gk * sak] : (int8_t)0;
+            Bs[k][r] = (gn < N && gk < K) ? B[gn * sbn + gk * sbk] : (int8_t)0;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < SIMT_BK; ++k) {
+            int32_t a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[i] = As[k][ty * 4 + i];
+                b[i] = Bs[k][tx * 4 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] += a[i] * b[j];
+        }
+        __syncthreads();
+    }
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gm = m0 + ty * 4 + i, gn = n0 + tx * 4 + j;
+            if (gm < M && gn < N) {
+                C[gm * ldc + gn] = acc[i][j];
+                mx = max(mx, abs_u32(acc[i][j]));
+            }
+        }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((threadIdx.x & 31) == 0 && mx != 0) atomicMax(d_max, mx);
+}
+
+// ----------------------------------------------------------- host launchers
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// rows x cols row-major bf16 tensor with `pitch` elements per row; box of
+// box_cols (inner, 64 = 128 bytes) x box_rows, 128-byte swizzle, zero fill.
+static int make_map(CUtensorMap* map, const Bf16View& v, int box_rows)
+{
+    auto enc = get_encode();
+    if (!enc) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    if ((reinterpret_cast<uintptr_t>(v.ptr) & 15) || ((v.pitch * 2) & 15))
+        return set_error(ITO_ERR_ARG, "bf16 operand not 16-byte aligned");
+    cuuint64_t dims[2] = {(cuuint64_t)v.cols, (cuuint64_t)v.rows};
+    cuuint64_t strides[1] = {(cuuint64_t)v.pitch * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(v.ptr), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return ITO_OK;
+}
+
+static int num_sms()
+{
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = kNumSMsHint;
+    }
+    return n;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+static int launch_tc(const GemmPlan& p, cudaStream_t s)
+{
+    using Cfg = TcCfg<BN>;
+    auto kern = k_gemm_tc<BN, A_MN, B_MN>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
+        attr_set = true;
+    }
+    const int tiles = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + BN - 1) / BN);
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(p.mapA, p.mapB, p.M, p.N, p.K, p.chunk_kb, p.C, p.ldc,
+                                                     p.d_max, p.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+    return ITO_OK;
+}
+
+int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
+              int32_t* C, int64_t ldc, uint32_t* d_max)
+{
+    if (M < 1 || N < 1 || K < 1) return set_error(ITO_ERR_SHAPE, "gemm: empty contraction");
+    if (K > (1 << 20)) return set_error(ITO_ERR_SHAPE, "gemm: contraction longer than 2^20");
+    // operand extents must match the problem
+    if (a_mn ? (A.rows != K || A.cols != M) : (A.rows != M || A.cols != K))
+        return set_error(ITO_ERR_SHAPE, "gemm: A view does not match M x K");
+    if (b_mn ? (B.rows != K || B.cols != N) : (B.rows != N || B.cols != K))
+        return set_error(ITO_ERR_SHAPE, "gemm: B view does not match N x K");
+    memset(p, 0, sizeof(*p));
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->a_mn = a_mn;
+    p->b_mn = b_mn;
+    p->C = C;
+    p->ldc = ldc;
+    p->d_max = d_max;
+    p->chunk_kb = kExactChunk / 64;
+    p->err = device_error_word();
+    if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
+    p->bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+    int r = make_map(&p->mapA, A, a_mn ? 64 : 128);
+    if (r) return r;
+    return make_map(&p->mapB, B, b_mn ? 64 : p->bn);
+}
+
+int gemm_run(const GemmPlan& p, cudaStream_t s)
+{
+#define ITO_TC_CASE(BN)                                                            \
+    if (p.bn == BN) {                                                              \
+        if (!p.a_mn && !p.b_mn) return launch_tc<BN, false, false>(p, s);          \
+        if (!p.a_mn && p.b_mn) return launch_tc<BN, false, true>(p, s);            \
+        if (p.a_mn && p.b_mn) return launch_tc<BN, true, true>(p, s);              \
+        return launch_tc<BN, true, false>(p, s);                                   \
+    }
+    ITO_TC_CASE(256)
+    ITO_TC_CASE(128)
+    ITO_TC_CASE(64)
+#undef ITO_TC_CASE
+    return set_error(ITO_ERR_ARG, "gemm: bad tile width");
+}
+
+int gemm_simt(const int8_t* A, int64_t sam, int64_t sak, const int8_t* B, int64_t sbn, int64_t sbk, int M, int N,
+              int K, int32_t* C, int64_t ldc, uint32_t* d_max, cudaStream_t s)
+{
+    if (M < 1 || N < 1 || K < 1) return set_error(ITO_ERR_SHAPE, "gemm: empty contraction");
+    dim3 grid((N + SIMT_BN - 1) / SIMT_BN, (M + SIMT_BM - 1) / SIMT_BM);
+    k_gemm_simt<<<grid, 256, 0, s>>>(A, sam, sak, B, sbn, sbk, M, N, K, C, ldc, d_max);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "simt gemm launch: %s", cudaGetErrorString(e));
+    return ITO_OK;
+}
+
+}  // namespace ito

@@ -1,0 +1,75 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ito.h"
+
+namespace ito {
+
+// Records an error text for ito_last_error_string() and returns `code`.
+int set_error(int code, const char* fmt, ...);
+
+// Number of K terms per exactly-accumulated tensor-core chunk: products of
+// two int8 values are at most 2^14 in magnitude, so 1024 of them sum to at
+// most 2^24, the largest range in which fp32 holds every integer.
+constexpr int kExactChunk = 1024;
+
+inline int64_t pad8(int64_t n) { return (n + 7) & ~int64_t(7); }
+
+// A row-major bf16 tensor [rows][cols] with `pitch` elements per row
+// (pitch * 2 bytes must be a multiple of 16 for TMA).
+struct Bf16View {
+    const uint16_t* ptr;
+    int64_t rows, cols, pitch;
+};
+
+// A prepared tensor-core contraction C[M][N] = sum_k A(m,k) B(n,k):
+// A is [M][K] (K-major) or [K][M] (a_mn); B is [N][K] or [K][N] (b_mn).
+struct GemmPlan {
+    CUtensorMap mapA, mapB;
+    int M, N, K, bn, chunk_kb;
+    bool a_mn, b_mn;
+    int32_t* C;
+    int64_t ldc;
+    uint32_t* d_max;
+    int* err;
+};
+
+// Device address of this library's error word on the current device.
+int* device_error_word();
+
+int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
+              int32_t* C, int64_t ldc, uint32_t* d_max);
+int gemm_run(const GemmPlan& p, cudaStream_t s);
+int gemm_simt(const int8_t* A, int64_t sam, int64_t sak, const int8_t* B, int64_t sbn, int64_t sbk, int M, int N,
+              int K, int32_t* C, int64_t ldc, uint32_t* d_max, cudaStream_t s);
+
+// ---- bandwidth kernels (ito_elementwise.cu)
+
+// dst[r][c] (pitch dst_pitch) = bf16(src[r][c]) for a row-major int8 tensor.
+int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* dst, int64_t dst_pitch,
+                      cudaStream_t s);
+
+// NITI Steps 1-3 on an int32 tensor Y [rows][cols] whose max |Y| is *d_max:
+// out8 = sat8(rhu(Y, s)) (ReLU'd if relu), plus the bf16 copy outb (pitch
+// ldb, may be null) and *d_shift = s (may be null). If gate is non-null the
+// result is zeroed where gate <= 0 (delta propagation through a ReLU).
+int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
+                   const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s);
+
+// NITI Steps 2-5 in place on W [rows][cols] (int8) with gradient G (int32),
+// refreshing the bf16 copy Wb (pitch ldb, may be null).
+int launch_niti_update(int8_t* W, uint16_t* Wb, int64_t ldb, const int32_t* G, int64_t rows, int64_t cols,
+                       const uint32_t* d_max, int target_bits, int mu_weight, int32_t* d_shift, int32_t* d_wshift,
+                       uint32_t* d_nonzero, cudaStream_t s);
+
+// delta = sat8(logits - target_mag * onehot(labels)), plus bf16 copy.
+int launch_top_error(const int8_t* logits, const int32_t* labels, int B, int C, int target_mag, int8_t* delta,
+                     uint16_t* deltab, int64_t ldb, cudaStream_t s);
+
+int launch_grid_blocks(int64_t work_items, int threads);
+
+}  // namespace ito

@@ -1,0 +1,635 @@
+// The model: a sequential stack of trainable int8 layers and the whole NITI
+// training step ("Integer On-Device Training: Overview", section 4:
+// INT_LAYERS[] of layer descriptors with mutable int8 weights, the training
+// loop INTODT_Forward -> compute_loss -> INTODT_Backward; section 3 for the
+// arithmetic; section 9, "Trained Weights in RAM", for the checkpoint).
+//
+// Layout in device memory (allocated once at creation):
+//   per layer l: W8 [OC][K] int8 (the weights) and Wb, its bf16 copy that the
+//   tensor cores read (row pitch rounded up to 8 elements); y32 [rows][OC]
+//   int32 forward contraction; a8 [rows][OC] int8 output (+ bf16 copy when a
+//   Linear layer reads it); e8/eb the delta at the layer output; d32 the int32
+//   delta-propagation contraction at the layer input; g32 [OC][K] int32
+//   weight gradient; for conv layers Pb, the bf16 im2col patches of the layer
+//   input, and dcol, the int32 patch-space delta.
+//   stats: int32 scalars, 8 per layer (ymax, ys, dmax, ds, gmax, gs, ws, nz)
+//   then pmax, ps of the pooling layer.
+// Step order: forward over all layers; top error; for each layer from the top
+// down: delta propagation with the weights before this step's update (not for
+// the first layer), weight gradient, NITI update.
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "ito_conv.h"
+#include "ito_device.cuh"
+#include "ito_internal.h"
+
+namespace ito {
+
+enum { ST_YMAX = 0, ST_YS, ST_DMAX, ST_DS, ST_GMAX, ST_GS, ST_WS, ST_NZ, ST_PER_LAYER };
+
+struct MLayer {
+    int kind;
+    int IC, OC;
+    int H, W, OH, OW, stride;   // conv
+    int64_t K;                  // forward contraction length (IC or 9*IC)
+    int64_t rows_in, rows_out;  // B or B*H*W / B*OH*OW
+    int8_t* W8 = nullptr;
+    uint16_t* Wb = nullptr;
+    int64_t ldw = 0;
+    uint16_t* Pb = nullptr;     // conv patches [rows_out][ldp]
+    int64_t ldp = 0;
+    int32_t* y32 = nullptr;
+    int8_t* a8 = nullptr;
+    uint16_t* ab = nullptr;     // bf16 copy of the output (read by a following Linear)
+    int64_t lda = 0;
+    int8_t* e8 = nullptr;       // delta at the output
+    uint16_t* eb = nullptr;
+    int64_t lde = 0;
+    int32_t* dcol = nullptr;    // conv: [rows_out][K]
+    int32_t* d32 = nullptr;     // [rows_in][IC]
+    int32_t* g32 = nullptr;     // [OC][K]
+    GemmPlan pf{}, pd{}, pg{};
+    bool has_dgrad = false;
+    bool relu = false;
+};
+
+}  // namespace ito
+
+struct ito_model {
+    int batch = 0;
+    ito_niti_params p{};
+    int32_t target_mag = 64;
+    int n_conv = 0;
+    bool has_pool = false;
+    int pool_C = 0, pool_HW = 0;
+    int in_features = 0;         // elements per sample of the input
+    std::vector<ito::MLayer> L;
+    // input
+    int8_t* x8 = nullptr;        // model-owned input (host-path steps)
+    int32_t* labels = nullptr;
+    uint16_t* xb = nullptr;      // bf16 copy of a Linear first layer's input
+    int64_t ldx = 0;
+    // pooling
+    int32_t* p32 = nullptr;
+    int8_t* pa8 = nullptr;
+    uint16_t* pab = nullptr;
+    int8_t* pe8 = nullptr;
+    int32_t* stats = nullptr;
+    int n_stats = 0;
+    uint32_t* discard_max = nullptr;   // max target of the patch-space conv delta (not a NITI tensor)
+    std::vector<void*> allocs;
+    std::vector<std::pair<std::string, int>> stat_names;
+    // measurement hooks
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_ev;      // pairs (begin, end)
+    std::vector<int> prof_cls;
+    std::vector<double> prof_work;
+    int prof_n = 0;
+    int launches = 0;                      // kernels launched by the current / last step
+
+    void mark_begin(cudaStream_t s)
+    {
+        ++launches;
+        if (!prof_on) return;
+        if ((size_t)(2 * prof_n + 2) > prof_ev.size()) {
+            for (int i = 0; i < 64; ++i) {
+                cudaEvent_t e;
+                cudaEventCreate(&e);
+                prof_ev.push_back(e);
+            }
+        }
+        cudaEventRecord(prof_ev[2 * prof_n], s);
+    }
+    void mark_end(cudaStream_t s, int cls, double work)
+    {
+        if (!prof_on) return;
+        cudaEventRecord(prof_ev[2 * prof_n + 1], s);
+        prof_cls.push_back(cls);
+        prof_work.push_back(work);
+        ++prof_n;
+    }
+
+    template <class T>
+    int alloc(T** out, size_t count)
+    {
+        void* p = nullptr;
+        if (count == 0) count = 1;
+        cudaError_t e = cudaMalloc(&p, count * sizeof(T));
+        if (e != cudaSuccess) return ito::set_error(ITO_ERR_CUDA, "cudaMalloc: %s", cudaGetErrorString(e));
+        cudaMemset(p, 0, count * sizeof(T));
+        allocs.push_back(p);
+        *out = static_cast<T*>(p);
+        return ITO_OK;
+    }
+    uint32_t* umax(int l, int which) { return reinterpret_cast<uint32_t*>(stats + l * ito::ST_PER_LAYER + which); }
+    int32_t* sval(int l, int which) { return stats + l * ito::ST_PER_LAYER + which; }
+};
+
+using namespace ito;
+
+#define ITO_TRY(x)                   \
+    do {                             \
+        int _r = (x);                \
+        if (_r != ITO_OK) return _r; \
+    } while (0)
+
+static int build_model(ito_model* m, const ito_layer_desc* d, int n)
+{
+    const int B = m->batch;
+    // parse: conv* [gap] linear* (last one ITO_LAYER_LINEAR)
+    int i = 0;
+    while (i < n && d[i].kind == ITO_LAYER_CONV3X3_RELU) ++i;
+    m->n_conv = i;
+    if (i < n && d[i].kind == ITO_LAYER_GAP) {
+        m->has_pool = true;
+        ++i;
+    }
+    const int first_linear = i;
+    for (; i < n; ++i) {
+        if (d[i].kind != ITO_LAYER_LINEAR_RELU && d[i].kind != ITO_LAYER_LINEAR)
+            return set_error(ITO_ERR_UNSUPPORTED, "layer %d: order must be conv*, [gap], linear*", i);
+        if (d[i].kind == ITO_LAYER_LINEAR && i != n - 1)
+            return set_error(ITO_ERR_UNSUPPORTED, "only the last layer may be a plain Linear");
+    }
+    if (first_linear >= n || d[n - 1].kind != ITO_LAYER_LINEAR)
+        return set_error(ITO_ERR_UNSUPPORTED, "the stack must end with one ITO_LAYER_LINEAR");
+    if (m->n_conv > 0 && !m->has_pool) return set_error(ITO_ERR_UNSUPPORTED, "conv layers must be followed by GAP");
+
+    // shapes
+    int H = 0, W = 0, C = 0;
+    if (m->n_conv > 0) {
+        H = d[0].in_h;
+        W = d[0].in_w;
+        C = d[0].in_features;
+        if (H < 1 || W < 1 || C < 1) return set_error(ITO_ERR_SHAPE, "conv input size");
+        m->in_features = H * W * C;
+    } else {
+        m->in_features = d[first_linear].in_features;
+    }
+    for (int l = 0; l < m->n_conv; ++l) {
+        const ito_layer_desc& q = d[l];
+        if (q.in_features != C || q.in_h != H || q.in_w != W) return set_error(ITO_ERR_SHAPE, "conv %d input", l);
+        if (q.stride != 1 && q.stride != 2) return set_error(ITO_ERR_SHAPE, "conv %d stride", l);
+        if (q.out_features < 1 || q.out_features % 8 || (l > 0 && C % 8))
+            return set_error(ITO_ERR_UNSUPPORTED, "conv %d channels must be multiples of 8", l);
+        MLayer L;
+        L.kind = q.kind;
+        L.IC = C;
+        L.OC = q.out_features;
+        L.H = H;
+        L.W = W;
+        L.stride = q.stride;
+        L.OH = (H + 2 - 3) / q.stride + 1;
+        L.OW = (W + 2 - 3) / q.stride + 1;
+        L.K = 9LL * C;
+        L.rows_in = (int64_t)B * H * W;
+        L.rows_out = (int64_t)B * L.OH * L.OW;
+        L.relu = true;
+        L.has_dgrad = l > 0;
+        m->L.push_back(L);
+        H = L.OH;
+        W = L.OW;
+        C = L.OC;
+    }
+    int F;
+    if (m->has_pool) {
+        const ito_layer_desc& q = d[m->n_conv];
+        if (m->n_conv == 0) return set_error(ITO_ERR_UNSUPPORTED, "GAP needs conv layers before it");
+        if (q.in_features != C) return set_error(ITO_ERR_SHAPE, "GAP channels");
+        m->pool_C = C;
+        m->pool_HW = H * W;
+        F = C;
+    } else {
+        F = m->in_features;
+    }
+    for (int l = first_linear; l < n; ++l) {
+        const ito_layer_desc& q = d[l];
+        if (q.in_features != F || q.out_features < 1) return set_error(ITO_ERR_SHAPE, "linear %d features", l);
+        MLayer L;
+        L.kind = q.kind;
+        L.IC = F;
+        L.OC = q.out_features;
+        L.H = L.W = L.OH = L.OW = 1;
+        L.stride = 0;
+        L.K = F;
+        L.rows_in = L.rows_out = B;
+        L.relu = q.kind == ITO_LAYER_LINEAR_RELU;
+        L.has_dgrad = !m->L.empty();
+        m->L.push_back(L);
+        F = q.out_features;
+    }
+    const int nl = (int)m->L.size();
+
+    // allocations
+    ITO_TRY(m->alloc(&m->x8, (size_t)B * m->in_features));
+    ITO_TRY(m->alloc(&m->labels, (size_t)B));
+    m->n_stats = nl * ST_PER_LAYER + 2;
+    ITO_TRY(m->alloc(&m->stats, (size_t)m->n_stats));
+    ITO_TRY(m->alloc(&m->discard_max, 1));
+    if (m->n_conv == 0) {
+        m->ldx = pad8(m->in_features);
+        ITO_TRY(m->alloc(&m->xb, (size_t)B * m->ldx));
+    }
+    if (m->has_pool) {
+        ITO_TRY(m->alloc(&m->p32, (size_t)B * m->pool_C));
+        ITO_TRY(m->alloc(&m->pa8, (size_t)B * m->pool_C));
+        ITO_TRY(m->alloc(&m->pab, (size_t)B * pad8(m->pool_C)));
+        ITO_TRY(m->alloc(&m->pe8, (size_t)B * m->pool_C));
+    }
+    for (int l = 0; l < nl; ++l) {
+        MLayer& L = m->L[l];
+        const bool conv = L.kind == ITO_LAYER_CONV3X3_RELU;
+        L.ldw = pad8(L.K);
+        ITO_TRY(m->alloc(&L.W8, (size_t)L.OC * L.K));
+        ITO_TRY(m->alloc(&L.Wb, (size_t)L.OC * L.ldw));
+        ITO_TRY(m->alloc(&L.y32, (size_t)L.rows_out * L.OC));
+        ITO_TRY(m->alloc(&L.a8, (size_t)L.rows_out * L.OC));
+        L.lda = pad8(L.OC);
+        const bool next_linear = l + 1 < nl && m->L[l + 1].kind != ITO_LAYER_CONV3X3_RELU && !conv;
+        if (next_linear) ITO_TRY(m->alloc(&L.ab, (size_t)L.rows_out * L.lda));
+        L.lde = pad8(L.OC);
+        ITO_TRY(m->alloc(&L.e8, (size_t)L.rows_out * L.OC));
+        ITO_TRY(m->alloc(&L.eb, (size_t)L.rows_out * L.lde));
+        ITO_TRY(m->alloc(&L.g32, (size_t)L.OC * L.K));
+        if (L.has_dgrad) ITO_TRY(m->alloc(&L.d32, (size_t)L.rows_in * L.IC));
+        if (conv) {
+            L.ldp = pad8(L.K);
+            ITO_TRY(m->alloc(&L.Pb, (size_t)L.rows_out * L.ldp));
+            if (L.has_dgrad) ITO_TRY(m->alloc(&L.dcol, (size_t)L.rows_out * L.K));
+        }
+    }
+
+    // contraction plans (tensor maps over the buffers above)
+    for (int l = 0; l < nl; ++l) {
+        MLayer& L = m->L[l];
+        const bool conv = L.kind == ITO_LAYER_CONV3X3_RELU;
+        uint32_t* ymax = m->umax(l, ST_YMAX);
+        uint32_t* dmax = m->umax(l, ST_DMAX);
+        uint32_t* gmax = m->umax(l, ST_GMAX);
+        const Bf16View wv{L.Wb, L.OC, L.K, L.ldw};
+        const Bf16View ev{L.eb, L.rows_out, L.OC, L.lde};
+        Bf16View in;
+        if (conv) {
+            in = Bf16View{L.Pb, L.rows_out, L.K, L.ldp};
+        } else if (l == m->n_conv && m->has_pool) {
+            in = Bf16View{m->pab, B, L.IC, pad8(L.IC)};
+        } else if (l == 0) {
+            in = Bf16View{m->xb, B, L.IC, m->ldx};
+        } else {
+            in = Bf16View{m->L[l - 1].ab, B, L.IC, m->L[l - 1].lda};
+        }
+        const int M = (int)L.rows_out;
+        // forward: Y[m][oc] = sum_k in[m][k] W[oc][k]
+        ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax));
+        // delta propagation: D[m][k] = sum_oc e[m][oc] W[oc][k]; for a conv this is the
+        // patch-space delta, whose max is not the NITI max (col2im takes that)
+        if (L.has_dgrad)
+            ITO_TRY(gemm_plan(&L.pd, ev, false, wv, true, M, (int)L.K, L.OC, conv ? L.dcol : L.d32, L.K,
+                              conv ? m->discard_max : dmax));
+        // weight gradient: G[oc][k] = sum_m e[m][oc] in[m][k]
+        ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax));
+    }
+
+    // names of the stats entries
+    const char* nm[ST_PER_LAYER] = {"ymax", "ys", "dmax", "ds", "gmax", "gs", "ws", "nz"};
+    for (int l = 0; l < nl; ++l)
+        for (int k = 0; k < ST_PER_LAYER; ++k) m->stat_names.push_back({std::string(nm[k]) + std::to_string(l),
+                                                                         l * ST_PER_LAYER + k});
+    m->stat_names.push_back({"pmax", nl * ST_PER_LAYER});
+    m->stat_names.push_back({"ps", nl * ST_PER_LAYER + 1});
+    return cudaDeviceSynchronize() == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "model init sync");
+}
+
+// Launch `call` bracketed by the model's measurement marks.
+#define ITO_LAUNCH(m, s, cls, work, call)      \
+    do {                                       \
+        (m)->mark_begin(s);                    \
+        int _r = (call);                       \
+        (m)->mark_end(s, cls, (double)(work)); \
+        if (_r != ITO_OK) return _r;           \
+    } while (0)
+
+static double gemm_ops(const GemmPlan& g) { return 2.0 * g.M * (double)g.N * g.K; }
+
+// algorithmic HBM bytes of a requantisation pass: int32 in, int8 out, bf16 copy, gate
+static double requant_bytes(int64_t n, bool bf16, bool gate)
+{
+    return (double)n * (4 + 1 + (bf16 ? 2 : 0) + (gate ? 1 : 0));
+}
+
+static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
+{
+    const int B = m->batch;
+    const int nl = (int)m->L.size();
+    const ito_niti_params p = m->p;
+    if (m->n_conv == 0)
+        ITO_LAUNCH(m, s, ITO_PROF_OTHER, 3.0 * B * m->in_features,
+                   launch_i8_to_bf16(x, B, m->in_features, m->xb, m->ldx, s));
+    const int8_t* in8 = x;
+    for (int l = 0; l < nl; ++l) {
+        MLayer& L = m->L[l];
+        if (L.kind == ITO_LAYER_CONV3X3_RELU) {
+            ITO_LAUNCH(m, s, ITO_PROF_OTHER, (double)L.rows_in * L.IC + 2.0 * L.rows_out * L.ldp,
+                       launch_im2col(in8, B, L.H, L.W, L.IC, L.OH, L.OW, L.stride, L.Pb, L.ldp, s));
+        } else if (l == m->n_conv && m->has_pool) {
+            const int pl = nl;   // pooling scalars follow the per-layer block
+            uint32_t* pmax = reinterpret_cast<uint32_t*>(m->stats + pl * ST_PER_LAYER);
+            ITO_LAUNCH(m, s, ITO_PROF_OTHER, (double)B * m->pool_C * (m->pool_HW + 4),
+                       launch_gap_fwd(in8, B, m->pool_HW, m->pool_C, m->p32, pmax, s));
+            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * m->pool_C, true, false),
+                       launch_requant(m->p32, B, m->pool_C, pmax, p.target_bits, 0, nullptr, m->pa8, m->pab,
+                                      pad8(m->pool_C), m->stats + pl * ST_PER_LAYER + 1, s));
+        }
+        ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
+        ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
+                   launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits, L.relu ? 1 : 0,
+                                  nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s));
+        in8 = L.a8;
+    }
+    return ITO_OK;
+}
+
+static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, cudaStream_t s)
+{
+    const int B = m->batch;
+    const int nl = (int)m->L.size();
+    const ito_niti_params p = m->p;
+    MLayer& top = m->L[nl - 1];
+    ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * top.OC + 4.0 * B,
+               launch_top_error(top.a8, labels, B, top.OC, m->target_mag, top.e8, top.eb, top.lde, s));
+    for (int l = nl - 1; l >= 0; --l) {
+        MLayer& L = m->L[l];
+        const bool conv = L.kind == ITO_LAYER_CONV3X3_RELU;
+        if (L.has_dgrad) {
+            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
+            MLayer& prev = m->L[l - 1];
+            if (conv) {
+                ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * L.rows_out * L.K + 4.0 * L.rows_in * L.IC,
+                           launch_col2im(L.dcol, B, L.H, L.W, L.IC, L.OH, L.OW, L.stride, L.d32,
+                                         m->umax(l, ST_DMAX), s));
+                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_in * L.IC, true, true),
+                           launch_requant(L.d32, L.rows_in, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0, prev.a8,
+                                          prev.e8, prev.eb, prev.lde, m->sval(l, ST_DS), s));
+            } else if (l == m->n_conv && m->has_pool) {
+                // pooled delta (the pooled activation has no ReLU), then the pooling backward
+                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, false, false),
+                           launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0, nullptr, m->pe8,
+                                          nullptr, 0, m->sval(l, ST_DS), s));
+                ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * m->pool_HW * m->pool_C,
+                           launch_gap_bwd(m->pe8, prev.a8, B, m->pool_HW, m->pool_C, prev.e8, prev.eb, s));
+            } else {
+                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, true, prev.relu),
+                           launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
+                                          prev.relu ? prev.a8 : nullptr, prev.e8, prev.eb, prev.lde,
+                                          m->sval(l, ST_DS), s));
+            }
+        }
+        ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
+        // G read (4 B), W read and written (1 + 1 B), bf16 copy written (2 B)
+        ITO_LAUNCH(m, s, ITO_PROF_UPDATE, 8.0 * L.OC * L.K,
+                   launch_niti_update(L.W8, L.Wb, L.ldw, L.g32, L.OC, L.K, m->umax(l, ST_GMAX), p.target_bits,
+                                      p.mu_weight, m->sval(l, ST_GS), m->sval(l, ST_WS),
+                                      reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ)), s));
+    }
+    (void)x;
+    return ITO_OK;
+}
+
+extern "C" {
+
+int ito_model_create(const ito_layer_desc* layers, int n_layers, int batch, ito_niti_params p, int32_t target_mag,
+                     ito_model** out)
+{
+    if (!layers || !out || n_layers < 1) return set_error(ITO_ERR_ARG, "NULL layers/out or no layers");
+    if (batch < 1 || batch > (1 << 20)) return set_error(ITO_ERR_SHAPE, "batch");
+    if (p.target_bits < 1 || p.target_bits > 8 || p.mu_weight < 0 || p.mu_weight > 31)
+        return set_error(ITO_ERR_ARG, "NITI parameters out of range");
+    *out = nullptr;
+    ito_model* m = new ito_model();
+    m->batch = batch;
+    m->p = p;
+    m->target_mag = target_mag;
+    int r = build_model(m, layers, n_layers);
+    if (r != ITO_OK) {
+        ito_model_destroy(m);
+        return r;
+    }
+    *out = m;
+    return ITO_OK;
+}
+
+int ito_model_destroy(ito_model* m)
+{
+    if (!m) return ITO_OK;
+    cudaDeviceSynchronize();
+    for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
+    for (void* p : m->allocs) cudaFree(p);
+    delete m;
+    return ITO_OK;
+}
+
+static int weight_layer(const ito_model* m, int layer)
+{
+    if (!m || layer < 0 || layer >= (int)m->L.size()) return -1;
+    return layer;
+}
+
+int ito_model_set_weights(ito_model* m, int layer, const int8_t* W, int on_host, void* stream)
+{
+    const int l = weight_layer(m, layer);
+    if (l < 0 || !W) return set_error(ITO_ERR_ARG, "bad model, layer or W");
+    MLayer& L = m->L[l];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)L.OC * L.K;
+    cudaError_t e = cudaMemcpyAsync(L.W8, W, bytes, on_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "weight copy: %s", cudaGetErrorString(e));
+    ITO_TRY(launch_i8_to_bf16(L.W8, L.OC, L.K, L.Wb, L.ldw, s));
+    if (on_host && cudaStreamSynchronize(s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+    return ITO_OK;
+}
+
+int ito_model_get_weights(const ito_model* m, int layer, int8_t* W, int on_host, void* stream)
+{
+    const int l = weight_layer(m, layer);
+    if (l < 0 || !W) return set_error(ITO_ERR_ARG, "bad model, layer or W");
+    const MLayer& L = m->L[l];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(W, L.W8, (size_t)L.OC * L.K,
+                                    on_host ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "weight copy: %s", cudaGetErrorString(e));
+    if (on_host && cudaStreamSynchronize(s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+    return ITO_OK;
+}
+
+int ito_model_tensor(const ito_model* m, const char* name, void** dev_ptr, int* elem_bytes, int64_t* numel)
+{
+    if (!m || !name || !dev_ptr || !elem_bytes || !numel) return set_error(ITO_ERR_ARG, "NULL argument");
+    const int nl = (int)m->L.size();
+    auto put = [&](const void* p, int eb, int64_t n) {
+        *dev_ptr = const_cast<void*>(p);
+        *elem_bytes = eb;
+        *numel = n;
+        return p ? ITO_OK : set_error(ITO_ERR_ARG, "tensor %s does not exist in this model", name);
+    };
+    const std::string s(name);
+    if (s == "stats") return put(m->stats, 4, m->n_stats);
+    if (s == "x") return put(m->x8, 1, (int64_t)m->batch * m->in_features);
+    if (s == "labels") return put(m->labels, 4, m->batch);
+    if (s == "p") return put(m->p32, 4, (int64_t)m->batch * m->pool_C);
+    if (s == "pa") return put(m->pa8, 1, (int64_t)m->batch * m->pool_C);
+    if (s == "pe") return put(m->pe8, 1, (int64_t)m->batch * m->pool_C);
+    if (s.size() >= 2) {
+        const char k = s[0];
+        char* end = nullptr;
+        const long l = strtol(s.c_str() + 1, &end, 10);
+        if (end && *end == 0 && l >= 0 && l < nl) {
+            const MLayer& L = m->L[l];
+            switch (k) {
+            case 'y': return put(L.y32, 4, L.rows_out * L.OC);
+            case 'a': return put(L.a8, 1, L.rows_out * L.OC);
+            case 'e': return put(L.e8, 1, L.rows_out * L.OC);
+            case 'd': return put(L.d32, 4, L.rows_in * L.IC);
+            case 'g': return put(L.g32, 4, (int64_t)L.OC * L.K);
+            case 'w': return put(L.W8, 1, (int64_t)L.OC * L.K);
+            default: break;
+            }
+        }
+    }
+    return set_error(ITO_ERR_ARG, "unknown tensor name %s", name);
+}
+
+int ito_model_stat_index(const ito_model* m, const char* name)
+{
+    if (!m || !name) return -1;
+    for (auto& kv : m->stat_names)
+        if (kv.first == name) return kv.second;
+    return -1;
+}
+
+int ito_model_num_stats(const ito_model* m) { return m ? m->n_stats : 0; }
+
+int ito_model_profile(ito_model* m, int enable)
+{
+    if (!m) return set_error(ITO_ERR_ARG, "NULL model");
+    m->prof_on = enable != 0;
+    return ITO_OK;
+}
+
+int ito_model_profile_read(ito_model* m, double* ms, double* work, int64_t* launches)
+{
+    if (!m || !ms || !work || !launches) return set_error(ITO_ERR_ARG, "NULL argument");
+    for (int c = 0; c < ITO_PROF_NCLASS; ++c) {
+        ms[c] = 0;
+        work[c] = 0;
+        launches[c] = 0;
+    }
+    for (int i = 0; i < m->prof_n; ++i) {
+        float t = 0;
+        if (cudaEventSynchronize(m->prof_ev[2 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&t, m->prof_ev[2 * i], m->prof_ev[2 * i + 1]) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "profile event read failed");
+        ms[m->prof_cls[i]] += t;
+        work[m->prof_cls[i]] += m->prof_work[i];
+        launches[m->prof_cls[i]] += 1;
+    }
+    m->prof_n = 0;
+    m->prof_cls.clear();
+    m->prof_work.clear();
+    return ITO_OK;
+}
+
+int ito_model_kernels_per_step(const ito_model* m) { return m ? m->launches : 0; }
+
+int ito_train_step(ito_model* m, const int8_t* x, const int32_t* labels, void* stream)
+{
+    if (!m || !x || !labels) return set_error(ITO_ERR_ARG, "NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    m->launches = 0;
+    cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * m->n_stats, s);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    ITO_TRY(model_forward(m, x, s));
+    return model_backward(m, x, labels, s);
+}
+
+int ito_train_step_host(ito_model* m, const int8_t* x_host, const int32_t* labels_host, int32_t* stats_host,
+                        void* stream)
+{
+    if (!m || !x_host || !labels_host) return set_error(ITO_ERR_ARG, "NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(m->x8, x_host, (size_t)m->batch * m->in_features, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(m->labels, labels_host, sizeof(int32_t) * m->batch, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "input copy: %s", cudaGetErrorString(e));
+    ITO_TRY(ito_train_step(m, m->x8, m->labels, stream));
+    if (stats_host) {
+        e = cudaMemcpyAsync(stats_host, m->stats, sizeof(int32_t) * m->n_stats, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "stats copy: %s", cudaGetErrorString(e));
+    }
+    e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "step: %s", cudaGetErrorString(e));
+}
+
+int ito_infer(ito_model* m, const int8_t* x, int8_t* logits, void* stream)
+{
+    if (!m || !x || !logits) return set_error(ITO_ERR_ARG, "NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    m->launches = 0;
+    cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * m->n_stats, s);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    ITO_TRY(model_forward(m, x, s));
+    const MLayer& top = m->L.back();
+    e = cudaMemcpyAsync(logits, top.a8, (size_t)top.rows_out * top.OC, cudaMemcpyDeviceToDevice, s);
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "logits copy: %s", cudaGetErrorString(e));
+}
+
+static const uint32_t kMagic = 0x3149544fu;   // "OTI1"
+
+int ito_model_save(const ito_model* m, const char* path)
+{
+    if (!m || !path) return set_error(ITO_ERR_ARG, "NULL argument");
+    if (cudaDeviceSynchronize() != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+    FILE* f = fopen(path, "wb");
+    if (!f) return set_error(ITO_ERR_ARG, "cannot open %s", path);
+    const uint32_t n = (uint32_t)m->L.size();
+    bool ok = fwrite(&kMagic, 4, 1, f) == 1 && fwrite(&n, 4, 1, f) == 1;
+    std::vector<int8_t> buf;
+    for (const MLayer& L : m->L) {
+        const int64_t shape[2] = {L.OC, L.K};
+        ok = ok && fwrite(shape, 8, 2, f) == 2;
+    }
+    for (const MLayer& L : m->L) {
+        buf.resize((size_t)L.OC * L.K);
+        ok = ok && cudaMemcpy(buf.data(), L.W8, buf.size(), cudaMemcpyDeviceToHost) == cudaSuccess;
+        ok = ok && fwrite(buf.data(), 1, buf.size(), f) == buf.size();
+    }
+    fclose(f);
+    return ok ? ITO_OK : set_error(ITO_ERR_ARG, "write to %s failed", path);
+}
+
+int ito_model_load(ito_model* m, const char* path)
+{
+    if (!m || !path) return set_error(ITO_ERR_ARG, "NULL argument");
+    FILE* f = fopen(path, "rb");
+    if (!f) return set_error(ITO_ERR_ARG, "cannot open %s", path);
+    uint32_t magic = 0, n = 0;
+    bool ok = fread(&magic, 4, 1, f) == 1 && fread(&n, 4, 1, f) == 1 && magic == kMagic && n == m->L.size();
+    for (const MLayer& L : m->L) {
+        int64_t shape[2] = {0, 0};
+        ok = ok && fread(shape, 8, 2, f) == 2 && shape[0] == L.OC && shape[1] == L.K;
+    }
+    std::vector<int8_t> buf;
+    for (size_t l = 0; ok && l < m->L.size(); ++l) {
+        MLayer& L = m->L[l];
+        buf.resize((size_t)L.OC * L.K);
+        ok = fread(buf.data(), 1, buf.size(), f) == buf.size();
+        ok = ok && ito_model_set_weights(m, (int)l, buf.data(), 1, nullptr) == ITO_OK;
+    }
+    fclose(f);
+    if (!ok) return set_error(ITO_ERR_SHAPE, "checkpoint %s does not match the model", path);
+    return cudaDeviceSynchronize() == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "sync");
+}
+
+}  // extern "C"

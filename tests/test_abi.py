@@ -1,0 +1,73 @@
+"""The C ABI: the library loads on a machine without a GPU, exports every
+entry point include/ito.h declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _lib_path():
+    # the build script is loaded by path: importing the package would bind the library first
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "ito_build", os.path.join(ROOT, "integer_only_nn_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
+def declared_entry_points():
+    text = open(os.path.join(ROOT, "include", "ito.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ito_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for n in ("ito_linear_fwd", "ito_linear_bwd_delta", "ito_linear_wgrad", "ito_niti_update",
+              "ito_top_error", "ito_train_step", "ito_model_create"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(_lib_path())
+    missing = [n for n in declared_entry_points() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    _lib_path()
+    import integer_only_nn_gb300 as ito
+    assert set(declared_entry_points()) <= set(ito.EXPORTED)
+
+
+def test_host_side_argument_errors():
+    _lib_path()
+    import integer_only_nn_gb300 as ito
+    L = ito._lib
+    p = ito.params()
+    assert L.ito_version() == 1
+    assert L.ito_linear_workspace_size(0, 4, 4) == 0
+    assert L.ito_linear_workspace_size(8, 4, 4) > 0
+    # NULL tensors are rejected before anything is enqueued
+    assert L.ito_linear_fwd(None, None, 4, 4, 4, 1, p, None, 0, None, None, None, None, None) == ito.ITO_ERR_ARG
+    dummy = ctypes.c_void_p(256)
+    assert L.ito_linear_fwd(dummy, dummy, 0, 4, 4, 1, p, dummy, 1 << 20, dummy, dummy, None, dummy,
+                            None) == ito.ITO_ERR_SHAPE
+    # misaligned workspace
+    assert L.ito_linear_fwd(dummy, dummy, 4, 4, 4, 1, p, ctypes.c_void_p(257), 1 << 20, dummy, dummy, None,
+                            dummy, None) == ito.ITO_ERR_ARG
+    assert L.ito_niti_update(dummy, dummy, 0, dummy, p, None, None, None, None) == ito.ITO_ERR_SHAPE
+    assert L.ito_top_error(None, dummy, 1, 1, 64, dummy, None) == ito.ITO_ERR_ARG
+    h = ctypes.c_void_p()
+    arr = (ito.LayerDesc * 1)(ito.LayerDesc(ito.ITO_LAYER_LINEAR, 4, 4, 0, 0, 0))
+    assert L.ito_model_create(arr, 1, 8, ito.NitiParams(0, 2), 64, ctypes.byref(h)) == ito.ITO_ERR_ARG
+    assert L.ito_model_create(arr, 0, 8, p, 64, ctypes.byref(h)) == ito.ITO_ERR_ARG
+    assert L.ito_model_create(arr, 1, 0, p, 64, ctypes.byref(h)) == ito.ITO_ERR_SHAPE
+    assert L.ito_model_stat_index(None, b"ys0") == -1
+    assert L.ito_model_destroy(None) == ito.ITO_OK
+    assert b"" != L.ito_last_error_string()

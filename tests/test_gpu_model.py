@@ -1,0 +1,60 @@
+"""Whole training steps of the CUDA model against the CPU oracle: every int8
+and int32 tensor and every shift/max scalar after every step.
+
+Short runs are compared tensor by tensor with the oracle run live; the
+100-step runs are compared against per-step digests of the oracle's tensors
+(tests/golden/digests_*.jsonl, written by tests/golden/make_digests.py from
+the oracle alone)."""
+import numpy as np
+import pytest
+
+import oracle as O
+import seeded_inputs as si
+from gpu_util import GpuRun, compare_records, digest, load_digests
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_step(w, weights, t, route):
+    x, labels = si.make_batch(w, t)
+    if w.kind == "mlp":
+        return O.mlp_step(weights, x, labels, route=route)
+    return O.cnn_step(weights, x, labels, w.convs)
+
+
+@pytest.mark.parametrize("index,steps,route", [(0, 100, "loops"), (1, 3, "loops"), (2, 2, "loops"),
+                                               (3, 1, "f64")])
+def test_model_lockstep_live(index, steps, route):
+    w = si.by_name(index)
+    g = GpuRun(w)
+    weights = si.make_weights(w)
+    for t in range(steps):
+        rec = _oracle_step(w, weights, t, route)
+        g.step(t)
+        compare_records(rec, g.record(), t)
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+    assert g.ito.ito_get_error() == 0
+
+
+@pytest.mark.parametrize("index", [1, 2, 3])
+def test_model_100_steps_digests(index):
+    w = si.by_name(index)
+    ref = load_digests(w)
+    assert ref is not None, "digest file for %s missing" % w.name
+    g = GpuRun(w)
+    full_steps = 3                       # int32 tensors too for the first steps
+    for t, d in enumerate(ref):
+        x, labels = g.step(t)
+        assert digest(x) == d["in.x"] and digest(labels) == d["in.labels"], "input generator diverged"
+        kinds = ("y", "a", "e", "d", "g", "w") if t < full_steps else ("a", "e", "w")
+        r = g.record(kinds)
+        bad = []
+        for k, v in r.items():
+            want = d.get(k)
+            if want is None:
+                continue
+            got = digest(v) if isinstance(v, np.ndarray) else int(v)
+            if got != want:
+                bad.append(k)
+        assert not bad, "step %d differs from the oracle in %s" % (t, bad)
+    assert len(ref) == 100
