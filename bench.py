@@ -296,6 +296,36 @@ def run_ours(args, w):
     return 0
 
 
+def run_op(args):
+    """Times one standalone single-layer call (the contraction plus its
+    requantisation) at a given shape; prints a JSON line. Used as the small
+    case for kernel profiles: python bench.py --op fwd --shape 8192,4096,4096"""
+    import numpy as np
+    import torch
+    import integer_only_nn_gb300 as ito
+    B, IC, OC = (int(v) for v in args.shape.split(","))
+    rng = np.random.default_rng(5)
+    x = torch.from_numpy(rng.integers(-127, 128, (B, IC)).astype(np.int8)).cuda()
+    W = torch.from_numpy(rng.integers(-127, 128, (OC, IC)).astype(np.int8)).cuda()
+    e = torch.from_numpy(rng.integers(-127, 128, (B, OC)).astype(np.int8)).cuda()
+    call = {"fwd": lambda: ito.ito_linear_fwd(x, W, 1),
+            "dgrad": lambda: ito.ito_linear_bwd_delta(e, W, x),
+            "wgrad": lambda: ito.ito_linear_wgrad(e, x)}[args.op]
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(args.steps):
+        call()
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / args.steps
+    print(json.dumps({"op": args.op, "shape": [B, IC, OC], "ms_per_call": ms,
+                      "tflops_incl_conversions": 2.0 * B * IC * OC / (ms / 1000.0) / 1e12}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -306,9 +336,13 @@ def main():
     ap.add_argument("--cpu-batch", type=int, default=128, help="samples in the CPU-oracle baseline step")
     ap.add_argument("--ref-batch", type=int, default=16, help="samples per reference-arm oracle step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=("fwd", "dgrad", "wgrad"), help="time one single-layer call instead")
+    ap.add_argument("--shape", default="8192,4096,4096", help="B,IC,OC for --op")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op:
+        return run_op(args)
     import seeded_inputs as si
     w = si.by_name(int(args.workload) if args.workload.isdigit() else args.workload)
     if args.impl == "reference":
