@@ -106,6 +106,33 @@ int ito_linear_fwd(const int8_t *x, const int8_t *W, int B, int IC, int OC, int 
                    ito_niti_params p, void *workspace, size_t workspace_bytes,
                    int32_t *y32, uint32_t *d_max, int32_t *d_shift, int8_t *y, void *stream);
 
+/* Bytes of the scratch array built into the library for
+ * ito_linear_fwd_noalloc (16 MiB). */
+#define ITO_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* ito_linear_fwd without a workspace argument, for callers that cannot
+ * allocate device memory while they run -- for example code inside a CUDA
+ * host callback (where CUDA calls that allocate are not permitted), or a
+ * plug-in whose host framework owns all device memory and forbids allocation
+ * in its execute hook. The pages have no counterpart to this entry point.
+ *
+ * It computes exactly what ito_linear_fwd computes, with the same arguments
+ * minus workspace/workspace_bytes, and allocates nothing: its scratch (the
+ * bf16 copies of x and W, ito_linear_workspace_size(B, IC, OC) bytes) is a
+ * fixed device array of ITO_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library holds until the process exits.
+ *  - Sizes whose scratch need exceeds ITO_NOALLOC_SCRATCH_BYTES are rejected
+ *    with ITO_ERR_SHAPE before anything is enqueued.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (the device must be current); make that first call before any
+ *    stream capture.
+ *  - All calls share the array: calls whose work overlaps on the GPU (for
+ *    instance on two streams without ordering) race on it. Serialise them.
+ * Outputs, errors and stream semantics as ito_linear_fwd. */
+int ito_linear_fwd_noalloc(const int8_t *x, const int8_t *W, int B, int IC, int OC, int relu,
+                           ito_niti_params p, int32_t *y32, uint32_t *d_max, int32_t *d_shift,
+                           int8_t *y, void *stream);
+
 /* Delta propagation of one Linear layer (same page, the note under Step 5:
  * the propagated delta is requantised to target_bits = 7 so it fits int8),
  * gated by the ReLU of the layer below:

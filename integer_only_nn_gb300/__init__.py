@@ -46,6 +46,7 @@ _SIGS = {
     "ito_last_error_string": (ctypes.c_char_p, []),
     "ito_linear_workspace_size": (_SZ, [_I, _I, _I]),
     "ito_linear_fwd": (_I, [_P, _P, _I, _I, _I, _I, NitiParams, _P, _SZ, _P, _P, _P, _P, _P]),
+    "ito_linear_fwd_noalloc": (_I, [_P, _P, _I, _I, _I, _I, NitiParams, _P, _P, _P, _P, _P]),
     "ito_linear_bwd_delta": (_I, [_P, _P, _P, _I, _I, _I, NitiParams, _P, _SZ, _P, _P, _P, _P, _P]),
     "ito_linear_wgrad": (_I, [_P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P]),
     "ito_niti_update": (_I, [_P, _P, _I64, _P, NitiParams, _P, _P, _P, _P]),
@@ -140,6 +141,23 @@ def ito_linear_fwd(x, W, relu, p=None, stream=None):
     ws, n = _workspace(B, IC, OC, dev)
     _check(_lib.ito_linear_fwd(_ptr(x), _ptr(W), B, IC, OC, int(relu), p or params(), _aligned256(ws), n,
                                _ptr(y32), _ptr(mx), _ptr(sh), _ptr(y), _stream(stream)))
+    return y32, mx, sh, y
+
+
+def ito_linear_fwd_noalloc(x, W, relu, p=None, stream=None, out=None):
+    """ito_linear_fwd using the library's built-in scratch instead of a
+    workspace (the library allocates nothing). `out` may hold preallocated
+    (y32, d_max, d_shift, y) tensors; -> the same four tensors."""
+    torch = _torch()
+    B, IC = x.shape
+    OC = W.shape[0]
+    dev = x.device
+    if out is None:
+        out = (torch.empty((B, OC), dtype=torch.int32, device=dev), torch.zeros(1, dtype=torch.int32, device=dev),
+               torch.zeros(1, dtype=torch.int32, device=dev), torch.empty((B, OC), dtype=torch.int8, device=dev))
+    y32, mx, sh, y = out
+    _check(_lib.ito_linear_fwd_noalloc(_ptr(x), _ptr(W), B, IC, OC, int(relu), p or params(), _ptr(y32), _ptr(mx),
+                                       _ptr(sh), _ptr(y), _stream(stream)))
     return y32, mx, sh, y
 
 
