@@ -74,14 +74,15 @@ struct TcCfg {
     static constexpr int EPI_WARPS = 8;
     static constexpr int THREADS = 64 + EPI_WARPS * 32;    // producer warp, MMA warp, 8 epilogue warps
     static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int STAGING_BYTES = EPI_WARPS * 4096;   // one 32x32 int32 store box per epilogue warp
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
-              int K, int chunk_kb, int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max,
-              int* __restrict__ err)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
+              int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
     using Cfg = TcCfg<BN>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -90,7 +91,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint8_t* staging = smem + STAGES * Cfg::STAGE_BYTES;     // 1024-aligned, for the swizzled store boxes
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
     uint64_t* empty_bar = full_bar + STAGES;
     uint64_t* accf_bar = empty_bar + STAGES;   // [2] accumulator buffer filled
     uint64_t* acce_bar = accf_bar + 2;         // [2] accumulator buffer drained
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
         const int e = warp - 2;
         const int quad = warp & 3;               // TMEM lanes this warp may access
         const int half = e >> 2;                 // which half of the tile's columns
+        uint8_t* stg = staging + e * 4096;       // this warp's 32 x 32 int32 store box
+        const uint32_t stg_row = smem_u32(stg) + lane * 128;
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
@@ -219,12 +223,12 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + half * HALF);
 #pragma unroll
-                for (int j = 0; j < HALF / 32; ++j) {
-                    uint32_t r[32];
-                    tmem_ld32(taddr + j * 32, r);
+                for (int j = 0; j < HALF / 16; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + j * 16, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[j * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                    for (int i = 0; i < 16; ++i) acc[j * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -238,21 +242,38 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
             for (int i = 0; i < HALF; ++i) mx = max(mx, abs_u32(acc[i]));
             mx = __reduce_max_sync(0xffffffffu, mx);
             if (lane == 0 && mx != 0) atomicMax(d_max, mx);
-            const int row = tm * BM + quad * 32 + lane;
+            const int row0 = tm * BM + quad * 32;
             const int col0 = tn * BN + half * HALF;
-            if (row < M) {
-                int32_t* dst = C + (int64_t)row * ldc + col0;
-                if (col0 + HALF <= N && (ldc & 3) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
+            if (use_tma_store) {
+                // 32 x 32 boxes through shared memory (128-byte swizzle: 16-byte chunk j of
+                // row r sits at chunk j ^ (r % 8)), written out by TMA; the edges are clipped
 #pragma unroll
-                    for (int i = 0; i < HALF; i += 4)
-                        *reinterpret_cast<int4*>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-                } else {
+                for (int g = 0; g < HALF / 32; ++g) {
+                    if (row0 >= M || col0 + g * 32 >= N) continue;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), acc[g * 32 + 4 * j], acc[g * 32 + 4 * j + 1],
+                                     acc[g * 32 + 4 * j + 2], acc[g * 32 + 4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, stg, col0 + g * 32, row0);
+                        bulk_commit();
+                    }
+                }
+            } else {
+                const int row = row0 + lane;
+                if (row < M) {
+                    int32_t* dst = C + (int64_t)row * ldc + col0;
 #pragma unroll
                     for (int i = 0; i < HALF; ++i)
                         if (col0 + i < N) dst[i] = acc[i];
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -377,8 +398,8 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
     }
     const int tiles = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + BN - 1) / BN);
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(p.mapA, p.mapB, p.M, p.N, p.K, p.chunk_kb, p.C, p.ldc,
-                                                     p.d_max, p.err);
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(p.mapA, p.mapB, p.mapC, p.use_tma_store, p.M, p.N, p.K,
+                                                     p.chunk_kb, p.C, p.ldc, p.d_max, p.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
     return ITO_OK;
@@ -409,7 +430,23 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
     p->bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
     int r = make_map(&p->mapA, A, a_mn ? 64 : 128);
     if (r) return r;
-    return make_map(&p->mapB, B, b_mn ? 64 : p->bn);
+    r = make_map(&p->mapB, B, b_mn ? 64 : p->bn);
+    if (r) return r;
+    // int32 output through TMA stores when its rows are 16-byte aligned; plain stores otherwise
+    p->use_tma_store = 0;
+    if ((reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 3) == 0) {
+        auto enc = get_encode();
+        cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)ldc * 4};
+        cuuint32_t box[2] = {32, 32};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult cr = enc(&p->mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, C, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)cr);
+        p->use_tma_store = 1;
+    }
+    return ITO_OK;
 }
 
 int gemm_run(const GemmPlan& p, cudaStream_t s)

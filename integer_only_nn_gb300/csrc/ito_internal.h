@@ -29,7 +29,8 @@ struct Bf16View {
 // A prepared tensor-core contraction C[M][N] = sum_k A(m,k) B(n,k):
 // A is [M][K] (K-major) or [K][M] (a_mn); B is [N][K] or [K][N] (b_mn).
 struct GemmPlan {
-    CUtensorMap mapA, mapB;
+    CUtensorMap mapA, mapB, mapC;
+    int use_tma_store;
     int M, N, K, bn, chunk_kb;
     bool a_mn, b_mn;
     int32_t* C;
