@@ -272,6 +272,88 @@ int ito_model_save(const ito_model *m, const char *path);
 int ito_model_load(ito_model *m, const char *path);
 
 /* ------------------------------------------------------------------------
+ * DFP16: dynamic fixed point tensors ("Mixed Precision Training of
+ * Convolutional Neural Networks using Integer Operations", section 3 "The
+ * Dynamic Fixed Point Format" and 3.1 "DFP Tensor Primitives"): an int16
+ * mantissa tensor i with one shared signed 8-bit exponent E (value i * 2^E).
+ * A product tensor carries exponent Ea + Eb; down-conversion to DFP16 shifts
+ * right by Rs and adds Rs to the exponent.
+ *
+ * Readings used here (the page leaves them open): contractions are exact in
+ * int64 (no 32-bit wrap); Rs = max(0, bitlen(max|P|) - 15); the shift rounds
+ * half up and the mantissa saturates to [-32767, 32767]. Exponents are int32
+ * device scalars holding int8 values; a result exponent outside [-128, 127]
+ * raises ITO_ERR_EXPONENT in the device error word (ito_get_error).
+ *
+ * Contractions run on the tensor cores: each int16 is split into two bf16
+ * limbs (v = 256*h + l, l in [-128, 127]), four limb products per term are
+ * accumulated exactly in fp32 over chunks of 512 terms and combined in int64.
+ * Workspace: ito_dfp16_workspace_size() bytes, 256-byte aligned, for the limb
+ * planes of both operands.
+ * ---------------------------------------------------------------------- */
+
+size_t ito_dfp16_workspace_size(int B, int IC, int OC);
+
+/* p64[b][oc] = sum_ic x[b][ic] * W[oc][ic] (int64, exact); *d_max = max|p64|
+ * (uint64); *d_rs = Rs; y = sat16(round-half-up(p64 >> Rs)) (int16 [B][OC]);
+ * *d_exp_y = *d_exp_x + *d_exp_w + Rs. x: int16 [B][IC]; W: int16 [OC][IC].
+ * Errors: ITO_ERR_ARG, ITO_ERR_SHAPE. */
+int ito_dfp16_linear_fwd(const int16_t *x, const int32_t *d_exp_x, const int16_t *W,
+                         const int32_t *d_exp_w, int B, int IC, int OC, void *workspace,
+                         size_t workspace_bytes, int64_t *p64, uint64_t *d_max, int16_t *y,
+                         int32_t *d_exp_y, int32_t *d_rs, void *stream);
+
+/* p64[b][ic] = sum_oc delta[b][oc] * W[oc][ic]; down-converted into
+ * delta_prev (int16 [B][IC]) with exponent *d_exp_delta + *d_exp_w + Rs. */
+int ito_dfp16_linear_bwd_delta(const int16_t *delta, const int32_t *d_exp_delta, const int16_t *W,
+                               const int32_t *d_exp_w, int B, int IC, int OC, void *workspace,
+                               size_t workspace_bytes, int64_t *p64, uint64_t *d_max,
+                               int16_t *delta_prev, int32_t *d_exp_prev, int32_t *d_rs, void *stream);
+
+/* p64[oc][ic] = sum_b delta[b][oc] * x[b][ic]; down-converted into g (int16
+ * [OC][IC]) with exponent *d_exp_delta + *d_exp_x + Rs. */
+int ito_dfp16_linear_wgrad(const int16_t *delta, const int32_t *d_exp_delta, const int16_t *x,
+                           const int32_t *d_exp_x, int B, int IC, int OC, void *workspace,
+                           size_t workspace_bytes, int64_t *p64, uint64_t *d_max, int16_t *g,
+                           int32_t *d_exp_g, int32_t *d_rs, void *stream);
+
+/* Integer SGD on DFP16 weights with a fixed exponent exp_w and learning rate
+ * 2^-eta (a reading: the page trains with FP32 SGD): k = exp_w + eta - *d_exp_g,
+ * dW = round-half-up(g >> k) for k >= 0, g * 2^-k for k < 0, then
+ * W = sat16(W - dW) in place. *d_k receives k (may be NULL); the number of
+ * nonzero dW is ADDED to *d_nonzero (may be NULL). W, g: int16 [n]. */
+int ito_dfp16_update(int16_t *W, const int16_t *g, const int32_t *d_exp_g, int64_t n, int32_t exp_w,
+                     int32_t eta, int32_t *d_k, uint32_t *d_nonzero, void *stream);
+
+typedef struct ito_dfp16_model ito_dfp16_model;
+
+/* A stack of DFP16 Linear layers dims[0] -> dims[1] -> ... -> dims[n_layers]
+ * (no ReLU), weights with the fixed shared exponent exp_w, integer SGD rate
+ * 2^-eta. Owns all its device memory. */
+int ito_dfp16_model_create(const int32_t *dims, int n_layers, int batch, int32_t exp_w, int32_t eta,
+                           ito_dfp16_model **out);
+int ito_dfp16_model_destroy(ito_dfp16_model *m);
+/* W: int16 [OC][IC] mantissas, host (on_host != 0) or device memory. */
+int ito_dfp16_model_set_weights(ito_dfp16_model *m, int layer, const int16_t *W, int on_host,
+                                void *stream);
+/* Named device tensors of the last step: "x", "p<l>" int64, "y<l>", "e<l>",
+ * "pd<l>" int64, "pg<l>" int64, "g<l>", "w<l>" (int16 unless stated). */
+int ito_dfp16_model_tensor(const ito_dfp16_model *m, const char *name, void **dev_ptr, int *elem_bytes,
+                           int64_t *numel);
+/* Scalars of the last step ("ey<l>", "ee<l>", "rs<l>", "rsd<l>", "rsg<l>",
+ * "eg<l>", "k<l>", "nz<l>", "pmax<l>", "pdmax<l>", "pgmax<l>"), copied to
+ * host_out (n >= ito_dfp16_model_num_stats) at ito_dfp16_model_stat_index;
+ * synchronises the device. */
+int ito_dfp16_model_num_stats(const ito_dfp16_model *m);
+int ito_dfp16_model_stat_index(const ito_dfp16_model *m, const char *name);
+int ito_dfp16_model_read_stats(const ito_dfp16_model *m, int64_t *host_out, int n);
+/* One training step: forward (each layer down-converted), top error = the
+ * output (MSE against a zero target), then per layer from the top: delta
+ * propagation with the pre-update weights (not the first layer), weight
+ * gradient, update. x: int16 [batch][dims[0]] with exponent exp_x. */
+int ito_dfp16_train_step(ito_dfp16_model *m, const int16_t *x, int32_t exp_x, void *stream);
+
+/* ------------------------------------------------------------------------
  * Measurement hooks (no counterpart in the pages; used by the benchmark)
  * ---------------------------------------------------------------------- */
 

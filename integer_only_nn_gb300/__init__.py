@@ -63,6 +63,20 @@ _SIGS = {
     "ito_infer": (_I, [_P, _P, _P, _P]),
     "ito_model_save": (_I, [_P, ctypes.c_char_p]),
     "ito_model_load": (_I, [_P, ctypes.c_char_p]),
+    "ito_dfp16_workspace_size": (_SZ, [_I, _I, _I]),
+    "ito_dfp16_linear_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P, _P, _P, _P]),
+    "ito_dfp16_linear_bwd_delta": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P, _P, _P, _P]),
+    "ito_dfp16_linear_wgrad": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P, _P, _P, _P]),
+    "ito_dfp16_update": (_I, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P]),
+    "ito_dfp16_model_create": (_I, [_P, _I, _I, _I32, _I32, ctypes.POINTER(_P)]),
+    "ito_dfp16_model_destroy": (_I, [_P]),
+    "ito_dfp16_model_set_weights": (_I, [_P, _I, _P, _I, _P]),
+    "ito_dfp16_model_tensor": (_I, [_P, ctypes.c_char_p, ctypes.POINTER(_P), ctypes.POINTER(_I),
+                                    ctypes.POINTER(_I64)]),
+    "ito_dfp16_model_num_stats": (_I, [_P]),
+    "ito_dfp16_model_stat_index": (_I, [_P, ctypes.c_char_p]),
+    "ito_dfp16_model_read_stats": (_I, [_P, _P, _I]),
+    "ito_dfp16_train_step": (_I, [_P, _P, _I32, _P]),
     "ito_model_profile": (_I, [_P, _I]),
     "ito_model_profile_read": (_I, [_P, _P, _P, _P]),
     "ito_model_kernels_per_step": (_I, [_P]),
@@ -331,6 +345,111 @@ class Model:
 
     def load(self, path):
         _check(_lib.ito_model_load(self._h, path.encode()))
+
+
+# ------------------------------------------------------------------ DFP16
+
+def _i32dev(v):
+    torch = _torch()
+    return torch.tensor([int(v)], dtype=torch.int32, device="cuda")
+
+
+def _dfp_ws(B, IC, OC):
+    torch = _torch()
+    n = _lib.ito_dfp16_workspace_size(B, IC, OC)
+    return torch.empty(n + 256, dtype=torch.uint8, device="cuda"), n
+
+
+def _dfp_call(fn, a, ea, b, eb, B, IC, OC, p_shape, out_shape, stream):
+    torch = _torch()
+    p64 = torch.empty(p_shape, dtype=torch.int64, device="cuda")
+    out = torch.empty(out_shape, dtype=torch.int16, device="cuda")
+    mx = torch.zeros(1, dtype=torch.int64, device="cuda")
+    e_out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rs = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws, n = _dfp_ws(B, IC, OC)
+    _check(fn(_ptr(a), _ptr(ea), _ptr(b), _ptr(eb), B, IC, OC, _aligned256(ws), n, _ptr(p64), _ptr(mx), _ptr(out),
+              _ptr(e_out), _ptr(rs), _stream(stream)))
+    return p64, mx, out, e_out, rs
+
+
+def ito_dfp16_linear_fwd(x, exp_x, W, exp_w, stream=None):
+    """exp_x / exp_w: device int32 [1] tensors -> (p64, max, y, exp_y, rs)"""
+    B, IC = x.shape
+    OC = W.shape[0]
+    return _dfp_call(_lib.ito_dfp16_linear_fwd, x, exp_x, W, exp_w, B, IC, OC, (B, OC), (B, OC), stream)
+
+
+def ito_dfp16_linear_bwd_delta(delta, exp_delta, W, exp_w, stream=None):
+    B, OC = delta.shape
+    IC = W.shape[1]
+    return _dfp_call(_lib.ito_dfp16_linear_bwd_delta, delta, exp_delta, W, exp_w, B, IC, OC, (B, IC), (B, IC),
+                     stream)
+
+
+def ito_dfp16_linear_wgrad(delta, exp_delta, x, exp_x, stream=None):
+    B, OC = delta.shape
+    IC = x.shape[1]
+    return _dfp_call(_lib.ito_dfp16_linear_wgrad, delta, exp_delta, x, exp_x, B, IC, OC, (OC, IC), (OC, IC), stream)
+
+
+def ito_dfp16_update(W, g, exp_g, exp_w, eta, stream=None):
+    """In place on W -> (k, nonzero) device int32 [1] each."""
+    torch = _torch()
+    k = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nz = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(_lib.ito_dfp16_update(_ptr(W), _ptr(g), _ptr(exp_g), W.numel(), exp_w, eta, _ptr(k), _ptr(nz),
+                                 _stream(stream)))
+    return k, nz
+
+
+class Dfp16Model:
+    """An ito_dfp16_model: DFP16 Linear layers trained with integer SGD."""
+
+    def __init__(self, dims, batch, exp_w, eta=8):
+        arr = (ctypes.c_int32 * len(dims))(*dims)
+        h = ctypes.c_void_p()
+        _check(_lib.ito_dfp16_model_create(arr, len(dims) - 1, batch, exp_w, eta, ctypes.byref(h)))
+        self._h = h
+        self.batch = batch
+        self.n_layers = len(dims) - 1
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.ito_dfp16_model_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_weights(self, layer, W, stream=None):
+        import numpy as np
+        a = np.ascontiguousarray(W, dtype=np.int16)
+        _check(_lib.ito_dfp16_model_set_weights(self._h, layer, a.ctypes.data_as(ctypes.c_void_p), 1,
+                                                _stream(stream)))
+
+    def tensor(self, name):
+        ptr, eb, n = ctypes.c_void_p(), ctypes.c_int(), ctypes.c_int64()
+        _check(_lib.ito_dfp16_model_tensor(self._h, name.encode(), ctypes.byref(ptr), ctypes.byref(eb),
+                                           ctypes.byref(n)))
+        return _from_ptr(ptr.value, n.value, None, eb.value)
+
+    def stats(self) -> dict:
+        n = _lib.ito_dfp16_model_num_stats(self._h)
+        buf = (ctypes.c_int64 * n)()
+        _check(_lib.ito_dfp16_model_read_stats(self._h, buf, n))
+        out = {}
+        for l in range(self.n_layers):
+            for key in ("ey", "ee", "rs", "rsd", "rsg", "eg", "k", "nz", "pmax", "pdmax", "pgmax"):
+                i = _lib.ito_dfp16_model_stat_index(self._h, ("%s%d" % (key, l)).encode())
+                out["%s%d" % (key, l)] = buf[i]
+        return out
+
+    def train_step(self, x, exp_x, stream=None):
+        _check(_lib.ito_dfp16_train_step(self._h, _ptr(x), int(exp_x), _stream(stream)))
 
 
 class _CudaArray:

@@ -1,0 +1,453 @@
+// DFP16 (dynamic fixed point, one shared exponent per tensor) linear path
+// ("Mixed Precision Training of Convolutional Neural Networks using Integer
+// Operations", section 3 "The Dynamic Fixed Point Format" and 3.1 "DFP
+// Tensor Primitives": a tensor is an int16 mantissa tensor i with one shared
+// signed 8-bit exponent E, value i * 2^E; a product tensor carries exponent
+// Ea + Eb and its accumulation chain shares it; down-conversion right-shifts
+// the wide result by Rs and adds Rs to the exponent).
+//
+// Contraction: int16 x int16 products summed exactly in int64. Each int16 v is
+// split into balanced limbs v = 256 * h + l with l in [-128, 127] and h in
+// [-128, 128]; both are exact in bf16. Then
+//   sum v*w = 65536 * sum(h_v h_w) + 256 * sum(h_v l_w + l_v h_w) + sum(l_v l_w),
+// four bf16 tensor-core products into three fp32 accumulators in tensor memory.
+// Every limb product is at most 2^14 in magnitude, so over a chunk of 512 K
+// terms each accumulator stays within 2^24 (the middle one gets two products
+// per term) and holds an exact integer. After each chunk the epilogue combines
+// the three into an exact int64 partial sum in registers; the tile's int64
+// result and its max |P| (atomicMax) go to global memory.
+#include "ito_device.cuh"
+#include "ito_internal.h"
+
+namespace ito {
+
+struct DfpCfg {
+    static constexpr int BM = 128, BN = 64, BK = 64;
+    static constexpr int A_PLANE = BM * BK * 2;             // 16 KB per limb plane
+    static constexpr int B_PLANE = BN * BK * 2;             // 8 KB per limb plane
+    static constexpr int STAGE_BYTES = 2 * A_PLANE + 2 * B_PLANE;
+    static constexpr int STAGES = 4;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + EPI_WARPS * 32;
+    static constexpr int BUF_COLS = 256;                    // per accumulator buffer: hh, mid, ll at +0, +64, +128
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int CHUNK_KB = 512 / BK;               // exact chunk: 512 K terms
+    static constexpr int STAGING_BYTES = EPI_WARPS * 4096;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
+};
+
+__device__ __forceinline__ void limb_split(int32_t v, int32_t& h, int32_t& l)
+{
+    l = ((v + 128) & 255) - 128;
+    h = (v - l) >> 8;   // v - l is a multiple of 256
+}
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(DfpCfg::THREADS, 1)
+    k_gemm_dfp(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+               const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
+               const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K,
+               int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, int* __restrict__ err)
+{
+    using Cfg = DfpCfg;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int HALF = BN / 2;                        // 32 columns per epilogue warp
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* staging = smem + STAGES * Cfg::STAGE_BYTES;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
+    uint64_t* empty_bar = full_bar + STAGES;
+    uint64_t* accf_bar = empty_bar + STAGES;
+    uint64_t* acce_bar = accf_bar + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (K + BK - 1) / BK;
+    const int num_chunks = (num_kb + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf_bar[b], 1);
+            mbar_init(&acce_bar[b], Cfg::EPI_WARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // tiles in row-major order over (m, n): consecutive CTAs share the A band
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                const int tm = t / num_n, tn = t % num_n;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
+                    uint8_t* sAh = smem + stage * Cfg::STAGE_BYTES;
+                    uint8_t* sAl = sAh + Cfg::A_PLANE;
+                    uint8_t* sBh = sAl + Cfg::A_PLANE;
+                    uint8_t* sBl = sBh + Cfg::B_PLANE;
+                    if (!A_MN) {
+                        tma_load_2d(&tmAh, &full_bar[stage], sAh, kb * BK, tm * BM);
+                        tma_load_2d(&tmAl, &full_bar[stage], sAl, kb * BK, tm * BM);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j) {
+                            tma_load_2d(&tmAh, &full_bar[stage], sAh + j * 8192, tm * BM + j * 64, kb * BK);
+                            tma_load_2d(&tmAl, &full_bar[stage], sAl + j * 8192, tm * BM + j * 64, kb * BK);
+                        }
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(&tmBh, &full_bar[stage], sBh, kb * BK, tn * BN);
+                        tma_load_2d(&tmBl, &full_bar[stage], sBl, kb * BK, tn * BN);
+                    } else {
+                        tma_load_2d(&tmBh, &full_bar[stage], sBh, tn * BN, kb * BK);
+                        tma_load_2d(&tmBl, &full_bar[stage], sBl, tn * BN, kb * BK);
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                for (int c = 0; ok && c < num_chunks; ++c) {
+                    if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_hh = tmem_base + (uint32_t)(buf * Cfg::BUF_COLS);
+                    const uint32_t d_mid = d_hh + 64, d_ll = d_hh + 128;
+                    const int kb0 = c * Cfg::CHUNK_KB;
+                    const int kb1 = min(num_kb, kb0 + Cfg::CHUNK_KB);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full_bar[stage], phase, abort_flag, err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t ah0 = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                        const uint32_t al0 = ah0 + Cfg::A_PLANE;
+                        const uint32_t bh0 = al0 + Cfg::A_PLANE;
+                        const uint32_t bl0 = bh0 + Cfg::B_PLANE;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint32_t ao = A_MN ? k * 2048 : k * 32;
+                            const uint32_t bo = B_MN ? k * 2048 : k * 32;
+                            const uint32_t albo = A_MN ? 8192 : 16, blbo = B_MN ? 8192 : 16;
+                            const uint64_t ah = smem_desc_sw128(ah0 + ao, albo, 1024);
+                            const uint64_t al = smem_desc_sw128(al0 + ao, albo, 1024);
+                            const uint64_t bh = smem_desc_sw128(bh0 + bo, blbo, 1024);
+                            const uint64_t bl = smem_desc_sw128(bl0 + bo, blbo, 1024);
+                            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+                            tc_mma_bf16(d_hh, ah, bh, IDESC, acc);
+                            tc_mma_bf16(d_mid, ah, bl, IDESC, acc);
+                            tc_mma_bf16(d_mid, al, bh, IDESC, 1u);
+                            tc_mma_bf16(d_ll, al, bl, IDESC, acc);
+                        }
+                        tc_commit(&empty_bar[stage]);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    tc_commit(&accf_bar[buf]);
+                    if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+                }
+            }
+        }
+    } else {
+        const int e = warp - 2;
+        const int quad = warp & 3;
+        const int half = e >> 2;
+        uint8_t* stg = staging + e * 4096;
+        const uint32_t stg_row = smem_u32(stg) + lane * 128;
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            const int tm = t / num_n, tn = t % num_n;
+            int64_t acc[HALF];
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) acc[i] = 0;
+            for (int c = 0; c < num_chunks; ++c) {
+                if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) +
+                                       (uint32_t)(buf * Cfg::BUF_COLS + half * HALF);
+                // one accumulator at a time keeps 16 staging registers live
+#pragma unroll
+                for (int j = 0; j < HALF / 16; ++j) {
+#pragma unroll 1
+                    for (int part = 0; part < 3; ++part) {
+                        uint32_t r[16];
+                        tmem_ld16(taddr + part * 64 + j * 16, r);
+                        tmem_ld_wait();
+                        const int sh = part == 0 ? 16 : (part == 1 ? 8 : 0);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) << sh;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acce_bar[buf]);
+                if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+            }
+            if (!ok) break;
+            unsigned long long mx = 0;
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) {
+                const unsigned long long a = (unsigned long long)(acc[i] < 0 ? -acc[i] : acc[i]);
+                mx = a > mx ? a : mx;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long v = __shfl_xor_sync(0xffffffffu, mx, o);
+                mx = v > mx ? v : mx;
+            }
+            if (lane == 0 && mx != 0) atomicMax(d_max, mx);
+            const int row0 = tm * BM + quad * 32;
+            const int col0 = tn * BN + half * HALF;
+            if (use_tma_store) {
+                // two 16-column int64 boxes (128 bytes per row, 128-byte swizzle)
+#pragma unroll
+                for (int g = 0; g < HALF / 16; ++g) {
+                    if (row0 >= M || col0 + g * 16 >= N) continue;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int64_t a0 = acc[g * 16 + 2 * j], a1 = acc[g * 16 + 2 * j + 1];
+                        st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), (int32_t)(a0 & 0xffffffff),
+                                     (int32_t)(a0 >> 32), (int32_t)(a1 & 0xffffffff), (int32_t)(a1 >> 32));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, stg, col0 + g * 16, row0);
+                        bulk_commit();
+                    }
+                }
+            } else {
+                const int row = row0 + lane;
+                if (row < M) {
+                    int64_t* dst = C + (int64_t)row * ldc + col0;
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i)
+                        if (col0 + i < N) dst[i] = acc[i];
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <bool A_MN, bool B_MN>
+static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
+{
+    auto kern = k_gemm_dfp<A_MN, B_MN>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DfpCfg::SMEM_BYTES) !=
+            cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
+        attr_set = true;
+    }
+    const int tiles = ((p.M + DfpCfg::BM - 1) / DfpCfg::BM) * ((p.N + DfpCfg::BN - 1) / DfpCfg::BN);
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    kern<<<grid, DfpCfg::THREADS, DfpCfg::SMEM_BYTES, s>>>(p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.mapC,
+                                                           p.use_tma_store, p.M, p.N, p.K, p.C, p.ldc, p.d_max,
+                                                           p.err);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp gemm launch: %s", cudaGetErrorString(e));
+}
+
+int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a_mn, const Bf16View& Bh,
+                  const Bf16View& Bl, bool b_mn, int M, int N, int K, int64_t* C, int64_t ldc,
+                  unsigned long long* d_max)
+{
+    if (M < 1 || N < 1 || K < 1) return set_error(ITO_ERR_SHAPE, "dfp gemm: empty contraction");
+    if (K > (1 << 20)) return set_error(ITO_ERR_SHAPE, "dfp gemm: contraction longer than 2^20");
+    if (a_mn ? (Ah.rows != K || Ah.cols != M) : (Ah.rows != M || Ah.cols != K))
+        return set_error(ITO_ERR_SHAPE, "dfp gemm: A view does not match M x K");
+    if (b_mn ? (Bh.rows != K || Bh.cols != N) : (Bh.rows != N || Bh.cols != K))
+        return set_error(ITO_ERR_SHAPE, "dfp gemm: B view does not match N x K");
+    *p = DfpGemmPlan{};
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->a_mn = a_mn;
+    p->b_mn = b_mn;
+    p->C = C;
+    p->ldc = ldc;
+    p->d_max = d_max;
+    p->err = device_error_word();
+    if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
+    int r;
+    if ((r = make_map_bf16(&p->mapAh, Ah, a_mn ? 64 : 128)) || (r = make_map_bf16(&p->mapAl, Al, a_mn ? 64 : 128)) ||
+        (r = make_map_bf16(&p->mapBh, Bh, 64)) || (r = make_map_bf16(&p->mapBl, Bl, 64)))
+        return r;
+    p->use_tma_store = 0;
+    if ((reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 1) == 0) {
+        auto enc = get_encode();
+        cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)ldc * 8};
+        cuuint32_t box[2] = {16, 32};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult cr = enc(&p->mapC, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, C, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (P) failed (%d)", (int)cr);
+        p->use_tma_store = 1;
+    }
+    return ITO_OK;
+}
+
+int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s)
+{
+    if (!p.a_mn && !p.b_mn) return launch_dfp<false, false>(p, s);
+    if (!p.a_mn && p.b_mn) return launch_dfp<false, true>(p, s);
+    if (p.a_mn && p.b_mn) return launch_dfp<true, true>(p, s);
+    return launch_dfp<true, false>(p, s);
+}
+
+// ---------------------------------------------------------- limb planes
+
+__global__ void k_i16_to_limbs(const int16_t* __restrict__ src, int64_t rows, int64_t cols,
+                               uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int64_t ldl)
+{
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i - r * cols;
+        int32_t h, l;
+        limb_split(src[i], h, l);
+        hi[r * ldl + c] = int_to_bf16_bits(h);
+        lo[r * ldl + c] = int_to_bf16_bits(l);
+    }
+}
+
+int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t* hi, uint16_t* lo, int64_t ldl,
+                        cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    k_i16_to_limbs<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(src, rows, cols, hi, lo, ldl);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "limb launch: %s", cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------- down-conversion
+
+__global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t cols,
+                           const unsigned long long* __restrict__ d_max, const int32_t* __restrict__ d_ea,
+                           const int32_t* __restrict__ d_eb, int16_t* __restrict__ out16, uint16_t* __restrict__ hi,
+                           uint16_t* __restrict__ lo, int64_t ldl, int32_t* __restrict__ d_exp_out,
+                           int32_t* __restrict__ d_rs, int* __restrict__ err)
+{
+    // section 3.1: Rs brings max |P| within 15 magnitude bits; the new exponent is Ea + Eb + Rs
+    const unsigned long long m = *d_max;
+    const int bl = m ? 64 - __clzll((long long)m) : 0;
+    const int rs = bl > 15 ? bl - 15 : 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        const int e = *d_ea + (d_eb ? *d_eb : 0) + rs;
+        if (d_exp_out) *d_exp_out = e;
+        if (d_rs) *d_rs = rs;
+        if (e < -128 || e > 127) raise_device_error(err, ITO_ERR_EXPONENT);
+    }
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t v = (int32_t)sat16s(rhu64(__ldcs(P + i), rs));
+        out16[i] = (int16_t)v;
+        if (hi) {
+            const int64_t r = i / cols, c = i - r * cols;
+            int32_t h, l;
+            limb_split(v, h, l);
+            hi[r * ldl + c] = int_to_bf16_bits(h);
+            lo[r * ldl + c] = int_to_bf16_bits(l);
+        }
+    }
+}
+
+int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned long long* d_max, const int32_t* d_ea,
+                    const int32_t* d_eb, int16_t* out16, uint16_t* hi, uint16_t* lo, int64_t ldl, int32_t* d_exp_out,
+                    int32_t* d_rs, cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    int* err = device_error_word();
+    if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
+    k_dfp_down<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(P, rows, cols, d_max, d_ea, d_eb, out16, hi, lo,
+                                                                     ldl, d_exp_out, d_rs, err);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp down launch: %s", cudaGetErrorString(e));
+}
+
+// ----------------------------------------------------------------- update
+
+__global__ void k_dfp_update(int16_t* __restrict__ W, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
+                             int64_t ldl, const int16_t* __restrict__ G, int64_t rows, int64_t cols,
+                             const int32_t* __restrict__ d_exp_g, int32_t exp_w, int32_t eta, int32_t* __restrict__ d_k,
+                             uint32_t* __restrict__ d_nonzero)
+{
+    // W * 2^Ew <- W * 2^Ew - G * 2^Eg * 2^-eta  =>  dW = G * 2^-(Ew + eta - Eg)
+    const int k = exp_w + eta - *d_exp_g;
+    if (d_k && blockIdx.x == 0 && threadIdx.x == 0) *d_k = k;
+    uint32_t cnt = 0;
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = G[i];
+        // a left shift past 17 bits already saturates every difference
+        const int64_t dw = k >= 0 ? rhu64(g, k) : g * ((int64_t)1 << (-k > 17 ? 17 : -k));
+        cnt += dw != 0;
+        const int32_t w = (int32_t)sat16s((int64_t)W[i] - dw);
+        W[i] = (int16_t)w;
+        if (hi) {
+            const int64_t r = i / cols, c = i - r * cols;
+            int32_t h, l;
+            limb_split(w, h, l);
+            hi[r * ldl + c] = int_to_bf16_bits(h);
+            lo[r * ldl + c] = int_to_bf16_bits(l);
+        }
+    }
+    if (d_nonzero) {
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(d_nonzero, cnt);
+    }
+}
+
+int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const int16_t* G, int64_t rows,
+                      int64_t cols, const int32_t* d_exp_g, int32_t exp_w, int32_t eta, int32_t* d_k,
+                      uint32_t* d_nonzero, cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    k_dfp_update<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(W, hi, lo, ldl, G, rows, cols, d_exp_g, exp_w,
+                                                                       eta, d_k, d_nonzero);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp update launch: %s", cudaGetErrorString(e));
+}
+
+}  // namespace ito

@@ -1,0 +1,414 @@
+// DFP16 single-layer entry points and the DFP16 model: a stack of Linear
+// layers over dynamic-fixed-point tensors (int16 mantissas, one shared
+// exponent per tensor) trained with integer-only arithmetic ("Mixed
+// Precision Training of Convolutional Neural Networks using Integer
+// Operations", sections 3 and 3.1; section 4 names the forward, backward and
+// weight-gradient kernels, each of whose wide outputs is quantised for the
+// next operation).
+//
+// Step (one reading, since the page fixes no loss or update rule): forward
+// through all layers (no ReLU), each contraction down-converted to DFP16;
+// top error = the output itself (an MSE error against a zero target);
+// for each layer from the top down: delta propagation with the pre-update
+// weights (not for the first layer), weight gradient, then integer SGD with
+// rate 2^-eta on the mantissas: W <- sat16(W - G * 2^(Eg - eta - Ew)), with
+// the weight exponent Ew held fixed.
+//
+// Exponents live on the device (int32 scalars) and are updated by the kernels
+// that produce each tensor, so a step needs no host synchronisation.
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "ito_device.cuh"
+#include "ito_internal.h"
+
+namespace ito {
+
+__global__ void k_set_i32(int32_t* p, int32_t v) { *p = v; }
+__global__ void k_copy_i32(int32_t* dst, const int32_t* src) { *dst = *src; }
+
+enum { D_EY = 0, D_EE, D_RS, D_RSD, D_RSG, D_EG, D_K, D_NZ, D_N32 };
+enum { D_PMAX = 0, D_PDMAX, D_PGMAX, D_N64 };
+
+struct DLayer {
+    int IC, OC;
+    int16_t* W = nullptr;
+    uint16_t *Wh = nullptr, *Wl = nullptr;
+    int64_t ldw = 0;
+    int64_t* p64 = nullptr;
+    int16_t* y16 = nullptr;
+    uint16_t *yh = nullptr, *yl = nullptr;
+    int64_t ldy = 0;
+    int16_t* e16 = nullptr;     // delta at the output (the output itself for the top layer)
+    uint16_t *eh = nullptr, *el = nullptr;
+    int64_t* pd64 = nullptr;    // [B][IC]
+    int64_t* pg64 = nullptr;    // [OC][IC]
+    int16_t* g16 = nullptr;
+    DfpGemmPlan pf{}, pd{}, pg{};
+};
+
+}  // namespace ito
+
+struct ito_dfp16_model {
+    int batch = 0, exp_w = 0, eta = 0;
+    std::vector<ito::DLayer> L;
+    int16_t* x16 = nullptr;
+    uint16_t *xh = nullptr, *xl = nullptr;
+    int64_t ldx = 0;
+    int32_t* s32 = nullptr;            // [layers][D_N32] + [ex, ew]
+    unsigned long long* s64 = nullptr; // [layers][D_N64]
+    std::vector<void*> allocs;
+
+    template <class T>
+    int alloc(T** out, size_t count)
+    {
+        void* p = nullptr;
+        if (count == 0) count = 1;
+        cudaError_t e = cudaMalloc(&p, count * sizeof(T));
+        if (e != cudaSuccess) return ito::set_error(ITO_ERR_CUDA, "cudaMalloc: %s", cudaGetErrorString(e));
+        cudaMemset(p, 0, count * sizeof(T));
+        allocs.push_back(p);
+        *out = static_cast<T*>(p);
+        return ITO_OK;
+    }
+    int32_t* i32(int l, int k) { return s32 + l * ito::D_N32 + k; }
+    unsigned long long* u64(int l, int k) { return s64 + l * ito::D_N64 + k; }
+    int32_t* ex() { return s32 + (int)L.size() * ito::D_N32; }
+    int32_t* ew() { return s32 + (int)L.size() * ito::D_N32 + 1; }
+};
+
+using namespace ito;
+
+#define ITO_TRY(x)                   \
+    do {                             \
+        int _r = (x);                \
+        if (_r != ITO_OK) return _r; \
+    } while (0)
+
+static inline size_t al256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// standalone workspace: limb planes of operand A (x or delta) and operand B (W or x)
+static size_t dws_a(int B, int IC, int OC) { return al256((size_t)2 * 2 * B * pad8(IC > OC ? IC : OC)); }
+static size_t dws_b(int B, int IC, int OC) { return al256((size_t)2 * 2 * (OC > B ? OC : B) * pad8(IC)); }
+
+struct Planes {
+    uint16_t *h, *l;
+};
+
+static Planes planes_at(void* base, size_t plane_elems)
+{
+    uint16_t* h = static_cast<uint16_t*>(base);
+    return Planes{h, h + plane_elems};
+}
+
+static int dfp_check(const void* a, const void* b, const void* c, const void* d, int B, int IC, int OC, void* ws,
+                     size_t ws_bytes)
+{
+    if (!a || !b || !c || !d) return set_error(ITO_ERR_ARG, "NULL pointer");
+    if (B < 1 || IC < 1 || OC < 1) return set_error(ITO_ERR_SHAPE, "sizes must be >= 1");
+    if (B > (1 << 20) || IC > (1 << 20) || OC > (1 << 20)) return set_error(ITO_ERR_SHAPE, "size above 2^20");
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return set_error(ITO_ERR_ARG, "workspace NULL or misaligned");
+    if (ws_bytes < ito_dfp16_workspace_size(B, IC, OC)) return set_error(ITO_ERR_ARG, "workspace too small");
+    return ITO_OK;
+}
+
+extern "C" {
+
+size_t ito_dfp16_workspace_size(int B, int IC, int OC)
+{
+    if (B < 1 || IC < 1 || OC < 1) return 0;
+    return dws_a(B, IC, OC) + dws_b(B, IC, OC);
+}
+
+int ito_dfp16_linear_fwd(const int16_t* x, const int32_t* d_exp_x, const int16_t* W, const int32_t* d_exp_w, int B,
+                         int IC, int OC, void* workspace, size_t workspace_bytes, int64_t* p64, uint64_t* d_max,
+                         int16_t* y, int32_t* d_exp_y, int32_t* d_rs, void* stream)
+{
+    ITO_TRY(dfp_check(x, W, p64, y, B, IC, OC, workspace, workspace_bytes));
+    if (!d_exp_x || !d_exp_w || !d_max || !d_exp_y) return set_error(ITO_ERR_ARG, "NULL scalar pointer");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t ld = pad8(IC);
+    Planes xa = planes_at(workspace, (size_t)B * ld);
+    Planes wb = planes_at(static_cast<char*>(workspace) + dws_a(B, IC, OC), (size_t)OC * ld);
+    ITO_TRY(launch_i16_to_limbs(x, B, IC, xa.h, xa.l, ld, s));
+    ITO_TRY(launch_i16_to_limbs(W, OC, IC, wb.h, wb.l, ld, s));
+    if (cudaMemsetAsync(d_max, 0, 8, s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset");
+    DfpGemmPlan g;
+    ITO_TRY(dfp_gemm_plan(&g, Bf16View{xa.h, B, IC, ld}, Bf16View{xa.l, B, IC, ld}, false, Bf16View{wb.h, OC, IC, ld},
+                          Bf16View{wb.l, OC, IC, ld}, false, B, OC, IC, p64, OC,
+                          reinterpret_cast<unsigned long long*>(d_max)));
+    ITO_TRY(dfp_gemm_run(g, s));
+    return launch_dfp_down(p64, B, OC, reinterpret_cast<unsigned long long*>(d_max), d_exp_x, d_exp_w, y, nullptr,
+                           nullptr, 0, d_exp_y, d_rs, s);
+}
+
+int ito_dfp16_linear_bwd_delta(const int16_t* delta, const int32_t* d_exp_delta, const int16_t* W,
+                               const int32_t* d_exp_w, int B, int IC, int OC, void* workspace, size_t workspace_bytes,
+                               int64_t* p64, uint64_t* d_max, int16_t* delta_prev, int32_t* d_exp_prev,
+                               int32_t* d_rs, void* stream)
+{
+    ITO_TRY(dfp_check(delta, W, p64, delta_prev, B, IC, OC, workspace, workspace_bytes));
+    if (!d_exp_delta || !d_exp_w || !d_max || !d_exp_prev) return set_error(ITO_ERR_ARG, "NULL scalar pointer");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t lde = pad8(OC), ldw = pad8(IC);
+    Planes ea = planes_at(workspace, (size_t)B * lde);
+    Planes wb = planes_at(static_cast<char*>(workspace) + dws_a(B, IC, OC), (size_t)OC * ldw);
+    ITO_TRY(launch_i16_to_limbs(delta, B, OC, ea.h, ea.l, lde, s));
+    ITO_TRY(launch_i16_to_limbs(W, OC, IC, wb.h, wb.l, ldw, s));
+    if (cudaMemsetAsync(d_max, 0, 8, s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset");
+    DfpGemmPlan g;
+    ITO_TRY(dfp_gemm_plan(&g, Bf16View{ea.h, B, OC, lde}, Bf16View{ea.l, B, OC, lde}, false,
+                          Bf16View{wb.h, OC, IC, ldw}, Bf16View{wb.l, OC, IC, ldw}, true, B, IC, OC, p64, IC,
+                          reinterpret_cast<unsigned long long*>(d_max)));
+    ITO_TRY(dfp_gemm_run(g, s));
+    return launch_dfp_down(p64, B, IC, reinterpret_cast<unsigned long long*>(d_max), d_exp_delta, d_exp_w, delta_prev,
+                           nullptr, nullptr, 0, d_exp_prev, d_rs, s);
+}
+
+int ito_dfp16_linear_wgrad(const int16_t* delta, const int32_t* d_exp_delta, const int16_t* x, const int32_t* d_exp_x,
+                           int B, int IC, int OC, void* workspace, size_t workspace_bytes, int64_t* p64,
+                           uint64_t* d_max, int16_t* g, int32_t* d_exp_g, int32_t* d_rs, void* stream)
+{
+    ITO_TRY(dfp_check(delta, x, p64, g, B, IC, OC, workspace, workspace_bytes));
+    if (!d_exp_delta || !d_exp_x || !d_max || !d_exp_g) return set_error(ITO_ERR_ARG, "NULL scalar pointer");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t lde = pad8(OC), ldx = pad8(IC);
+    Planes ea = planes_at(workspace, (size_t)B * lde);
+    Planes xb = planes_at(static_cast<char*>(workspace) + dws_a(B, IC, OC), (size_t)B * ldx);
+    ITO_TRY(launch_i16_to_limbs(delta, B, OC, ea.h, ea.l, lde, s));
+    ITO_TRY(launch_i16_to_limbs(x, B, IC, xb.h, xb.l, ldx, s));
+    if (cudaMemsetAsync(d_max, 0, 8, s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset");
+    DfpGemmPlan gp;
+    ITO_TRY(dfp_gemm_plan(&gp, Bf16View{ea.h, B, OC, lde}, Bf16View{ea.l, B, OC, lde}, true,
+                          Bf16View{xb.h, B, IC, ldx}, Bf16View{xb.l, B, IC, ldx}, true, OC, IC, B, p64, IC,
+                          reinterpret_cast<unsigned long long*>(d_max)));
+    ITO_TRY(dfp_gemm_run(gp, s));
+    return launch_dfp_down(p64, OC, IC, reinterpret_cast<unsigned long long*>(d_max), d_exp_delta, d_exp_x, g, nullptr,
+                           nullptr, 0, d_exp_g, d_rs, s);
+}
+
+int ito_dfp16_update(int16_t* W, const int16_t* g, const int32_t* d_exp_g, int64_t n, int32_t exp_w, int32_t eta,
+                     int32_t* d_k, uint32_t* d_nonzero, void* stream)
+{
+    if (!W || !g || !d_exp_g) return set_error(ITO_ERR_ARG, "NULL pointer");
+    if (n < 1) return set_error(ITO_ERR_SHAPE, "n must be >= 1");
+    return launch_dfp_update(W, nullptr, nullptr, 0, g, 1, n, d_exp_g, exp_w, eta, d_k, d_nonzero,
+                             static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ model
+
+int ito_dfp16_model_destroy(ito_dfp16_model* m)
+{
+    if (!m) return ITO_OK;
+    cudaDeviceSynchronize();
+    for (void* p : m->allocs) cudaFree(p);
+    delete m;
+    return ITO_OK;
+}
+
+static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
+{
+    const int B = m->batch;
+    for (int l = 0; l < nl; ++l) {
+        if (dims[l] < 1 || dims[l + 1] < 1) return set_error(ITO_ERR_SHAPE, "layer %d size", l);
+        DLayer L;
+        L.IC = dims[l];
+        L.OC = dims[l + 1];
+        m->L.push_back(L);
+    }
+    ITO_TRY(m->alloc(&m->s32, (size_t)nl * D_N32 + 2));
+    ITO_TRY(m->alloc(&m->s64, (size_t)nl * D_N64));
+    m->ldx = pad8(dims[0]);
+    ITO_TRY(m->alloc(&m->x16, (size_t)B * dims[0]));
+    ITO_TRY(m->alloc(&m->xh, (size_t)B * m->ldx));
+    ITO_TRY(m->alloc(&m->xl, (size_t)B * m->ldx));
+    for (int l = 0; l < nl; ++l) {
+        DLayer& L = m->L[l];
+        L.ldw = pad8(L.IC);
+        L.ldy = pad8(L.OC);
+        ITO_TRY(m->alloc(&L.W, (size_t)L.OC * L.IC));
+        ITO_TRY(m->alloc(&L.Wh, (size_t)L.OC * L.ldw));
+        ITO_TRY(m->alloc(&L.Wl, (size_t)L.OC * L.ldw));
+        ITO_TRY(m->alloc(&L.p64, (size_t)B * L.OC));
+        ITO_TRY(m->alloc(&L.y16, (size_t)B * L.OC));
+        ITO_TRY(m->alloc(&L.yh, (size_t)B * L.ldy));
+        ITO_TRY(m->alloc(&L.yl, (size_t)B * L.ldy));
+        if (l == nl - 1) {
+            L.e16 = L.y16;   // the top error is the output itself
+            L.eh = L.yh;
+            L.el = L.yl;
+        } else {
+            ITO_TRY(m->alloc(&L.e16, (size_t)B * L.OC));
+            ITO_TRY(m->alloc(&L.eh, (size_t)B * L.ldy));
+            ITO_TRY(m->alloc(&L.el, (size_t)B * L.ldy));
+        }
+        if (l > 0) ITO_TRY(m->alloc(&L.pd64, (size_t)B * L.IC));
+        ITO_TRY(m->alloc(&L.pg64, (size_t)L.OC * L.IC));
+        ITO_TRY(m->alloc(&L.g16, (size_t)L.OC * L.IC));
+    }
+    for (int l = 0; l < nl; ++l) {
+        DLayer& L = m->L[l];
+        const Bf16View wh{L.Wh, L.OC, L.IC, L.ldw}, wl{L.Wl, L.OC, L.IC, L.ldw};
+        const Bf16View eh{L.eh, B, L.OC, L.ldy}, el{L.el, B, L.OC, L.ldy};
+        Bf16View ih, il;
+        if (l == 0) {
+            ih = Bf16View{m->xh, B, L.IC, m->ldx};
+            il = Bf16View{m->xl, B, L.IC, m->ldx};
+        } else {
+            ih = Bf16View{m->L[l - 1].yh, B, L.IC, m->L[l - 1].ldy};
+            il = Bf16View{m->L[l - 1].yl, B, L.IC, m->L[l - 1].ldy};
+        }
+        ITO_TRY(dfp_gemm_plan(&L.pf, ih, il, false, wh, wl, false, B, L.OC, L.IC, L.p64, L.OC, m->u64(l, D_PMAX)));
+        if (l > 0)
+            ITO_TRY(dfp_gemm_plan(&L.pd, eh, el, false, wh, wl, true, B, L.IC, L.OC, L.pd64, L.IC, m->u64(l, D_PDMAX)));
+        ITO_TRY(dfp_gemm_plan(&L.pg, eh, el, true, ih, il, true, L.OC, L.IC, B, L.pg64, L.IC, m->u64(l, D_PGMAX)));
+    }
+    k_set_i32<<<1, 1>>>(m->ew(), m->exp_w);
+    return cudaDeviceSynchronize() == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp model init");
+}
+
+int ito_dfp16_model_create(const int32_t* dims, int n_layers, int batch, int32_t exp_w, int32_t eta,
+                           ito_dfp16_model** out)
+{
+    if (!dims || !out || n_layers < 1) return set_error(ITO_ERR_ARG, "NULL dims/out or no layers");
+    if (batch < 1 || batch > (1 << 20)) return set_error(ITO_ERR_SHAPE, "batch");
+    if (exp_w < -128 || exp_w > 127 || eta < 0 || eta > 62) return set_error(ITO_ERR_ARG, "exponent or eta");
+    *out = nullptr;
+    ito_dfp16_model* m = new ito_dfp16_model();
+    m->batch = batch;
+    m->exp_w = exp_w;
+    m->eta = eta;
+    int r = dfp_build(m, dims, n_layers);
+    if (r != ITO_OK) {
+        ito_dfp16_model_destroy(m);
+        return r;
+    }
+    *out = m;
+    return ITO_OK;
+}
+
+int ito_dfp16_model_set_weights(ito_dfp16_model* m, int layer, const int16_t* W, int on_host, void* stream)
+{
+    if (!m || !W || layer < 0 || layer >= (int)m->L.size()) return set_error(ITO_ERR_ARG, "bad model, layer or W");
+    DLayer& L = m->L[layer];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(L.W, W, sizeof(int16_t) * L.OC * L.IC,
+                                    on_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "weight copy: %s", cudaGetErrorString(e));
+    ITO_TRY(launch_i16_to_limbs(L.W, L.OC, L.IC, L.Wh, L.Wl, L.ldw, s));
+    if (on_host && cudaStreamSynchronize(s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+    return ITO_OK;
+}
+
+int ito_dfp16_model_tensor(const ito_dfp16_model* m, const char* name, void** dev_ptr, int* elem_bytes,
+                           int64_t* numel)
+{
+    if (!m || !name || !dev_ptr || !elem_bytes || !numel) return set_error(ITO_ERR_ARG, "NULL argument");
+    const int B = m->batch;
+    auto put = [&](const void* p, int eb, int64_t n) {
+        *dev_ptr = const_cast<void*>(p);
+        *elem_bytes = eb;
+        *numel = n;
+        return p ? ITO_OK : set_error(ITO_ERR_ARG, "tensor %s does not exist in this model", name);
+    };
+    const std::string s(name);
+    if (s == "x") return put(m->x16, 2, (int64_t)B * m->L[0].IC);
+    size_t pos = 0;
+    while (pos < s.size() && (s[pos] < '0' || s[pos] > '9')) ++pos;
+    if (pos == 0 || pos == s.size()) return set_error(ITO_ERR_ARG, "unknown tensor name %s", name);
+    const std::string key = s.substr(0, pos);
+    char* end = nullptr;
+    const long l = strtol(s.c_str() + pos, &end, 10);
+    if (!end || *end || l < 0 || l >= (long)m->L.size()) return set_error(ITO_ERR_ARG, "unknown tensor %s", name);
+    const DLayer& L = m->L[l];
+    if (key == "w") return put(L.W, 2, (int64_t)L.OC * L.IC);
+    if (key == "p") return put(L.p64, 8, (int64_t)B * L.OC);
+    if (key == "y") return put(L.y16, 2, (int64_t)B * L.OC);
+    if (key == "e") return put(L.e16, 2, (int64_t)B * L.OC);
+    if (key == "pd") return put(L.pd64, 8, (int64_t)B * L.IC);
+    if (key == "pg") return put(L.pg64, 8, (int64_t)L.OC * L.IC);
+    if (key == "g") return put(L.g16, 2, (int64_t)L.OC * L.IC);
+    return set_error(ITO_ERR_ARG, "unknown tensor name %s", name);
+}
+
+static const char* kD32[D_N32] = {"ey", "ee", "rs", "rsd", "rsg", "eg", "k", "nz"};
+static const char* kD64[D_N64] = {"pmax", "pdmax", "pgmax"};
+
+int ito_dfp16_model_num_stats(const ito_dfp16_model* m)
+{
+    return m ? (int)m->L.size() * (D_N32 + D_N64) : 0;
+}
+
+int ito_dfp16_model_stat_index(const ito_dfp16_model* m, const char* name)
+{
+    if (!m || !name) return -1;
+    const int nl = (int)m->L.size();
+    for (int l = 0; l < nl; ++l) {
+        for (int k = 0; k < D_N32; ++k)
+            if (std::string(kD32[k]) + std::to_string(l) == name) return l * (D_N32 + D_N64) + k;
+        for (int k = 0; k < D_N64; ++k)
+            if (std::string(kD64[k]) + std::to_string(l) == name) return l * (D_N32 + D_N64) + D_N32 + k;
+    }
+    return -1;
+}
+
+int ito_dfp16_model_read_stats(const ito_dfp16_model* m, int64_t* host_out, int n)
+{
+    if (!m || !host_out || n < ito_dfp16_model_num_stats(m)) return set_error(ITO_ERR_ARG, "bad arguments");
+    const int nl = (int)m->L.size();
+    std::vector<int32_t> a((size_t)nl * D_N32);
+    std::vector<unsigned long long> b((size_t)nl * D_N64);
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(a.data(), m->s32, a.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(b.data(), m->s64, b.size() * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "stats read failed");
+    for (int l = 0; l < nl; ++l) {
+        for (int k = 0; k < D_N32; ++k) host_out[l * (D_N32 + D_N64) + k] = a[l * D_N32 + k];
+        for (int k = 0; k < D_N64; ++k) host_out[l * (D_N32 + D_N64) + D_N32 + k] = (int64_t)b[l * D_N64 + k];
+    }
+    return ITO_OK;
+}
+
+int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, void* stream)
+{
+    if (!m || !x) return set_error(ITO_ERR_ARG, "NULL argument");
+    if (exp_x < -128 || exp_x > 127) return set_error(ITO_ERR_EXPONENT, "input exponent outside int8");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int B = m->batch;
+    const int nl = (int)m->L.size();
+    if (cudaMemsetAsync(m->s32, 0, sizeof(int32_t) * nl * D_N32, s) != cudaSuccess ||
+        cudaMemsetAsync(m->s64, 0, sizeof(unsigned long long) * nl * D_N64, s) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "memset");
+    k_set_i32<<<1, 1, 0, s>>>(m->ex(), exp_x);
+    ITO_TRY(launch_i16_to_limbs(x, B, m->L[0].IC, m->xh, m->xl, m->ldx, s));
+    for (int l = 0; l < nl; ++l) {
+        DLayer& L = m->L[l];
+        const int32_t* e_in = l == 0 ? m->ex() : m->i32(l - 1, D_EY);
+        ITO_TRY(dfp_gemm_run(L.pf, s));
+        ITO_TRY(launch_dfp_down(L.p64, B, L.OC, m->u64(l, D_PMAX), e_in, m->ew(), L.y16, L.yh, L.yl, L.ldy,
+                                m->i32(l, D_EY), m->i32(l, D_RS), s));
+    }
+    k_copy_i32<<<1, 1, 0, s>>>(m->i32(nl - 1, D_EE), m->i32(nl - 1, D_EY));
+    for (int l = nl - 1; l >= 0; --l) {
+        DLayer& L = m->L[l];
+        const int32_t* e_in = l == 0 ? m->ex() : m->i32(l - 1, D_EY);
+        if (l > 0) {
+            DLayer& P = m->L[l - 1];
+            ITO_TRY(dfp_gemm_run(L.pd, s));
+            ITO_TRY(launch_dfp_down(L.pd64, B, L.IC, m->u64(l, D_PDMAX), m->i32(l, D_EE), m->ew(), P.e16, P.eh, P.el,
+                                    P.ldy, m->i32(l - 1, D_EE), m->i32(l, D_RSD), s));
+        }
+        ITO_TRY(dfp_gemm_run(L.pg, s));
+        ITO_TRY(launch_dfp_down(L.pg64, L.OC, L.IC, m->u64(l, D_PGMAX), m->i32(l, D_EE), e_in, L.g16, nullptr, nullptr,
+                                0, m->i32(l, D_EG), m->i32(l, D_RSG), s));
+        ITO_TRY(launch_dfp_update(L.W, L.Wh, L.Wl, L.ldw, L.g16, L.OC, L.IC, m->i32(l, D_EG), m->exp_w, m->eta,
+                                  m->i32(l, D_K), reinterpret_cast<uint32_t*>(m->i32(l, D_NZ)), s));
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp step: %s", cudaGetErrorString(e));
+}
+
+}  // extern "C"

@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(256)
 
 // ----------------------------------------------------------- host launchers
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+PFN_cuTensorMapEncodeTiled_v12000 get_encode()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -356,7 +356,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
 
 // rows x cols row-major bf16 tensor with `pitch` elements per row; box of
 // box_cols (inner, 64 = 128 bytes) x box_rows, 128-byte swizzle, zero fill.
-static int make_map(CUtensorMap* map, const Bf16View& v, int box_rows)
+int make_map_bf16(CUtensorMap* map, const Bf16View& v, int box_rows)
 {
     auto enc = get_encode();
     if (!enc) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -373,7 +373,7 @@ static int make_map(CUtensorMap* map, const Bf16View& v, int box_rows)
     return ITO_OK;
 }
 
-static int num_sms()
+int num_sms()
 {
     static int n = 0;
     if (!n) {
@@ -428,9 +428,9 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
     p->err = device_error_word();
     if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     p->bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
-    int r = make_map(&p->mapA, A, a_mn ? 64 : 128);
+    int r = make_map_bf16(&p->mapA, A, a_mn ? 64 : 128);
     if (r) return r;
-    r = make_map(&p->mapB, B, b_mn ? 64 : p->bn);
+    r = make_map_bf16(&p->mapB, B, b_mn ? 64 : p->bn);
     if (r) return r;
     // int32 output through TMA stores when its rows are 16-byte aligned; plain stores otherwise
     p->use_tma_store = 0;

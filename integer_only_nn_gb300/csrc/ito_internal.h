@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "ito.h"
@@ -41,6 +42,48 @@ struct GemmPlan {
 
 // Device address of this library's error word on the current device.
 int* device_error_word();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (nullptr if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 get_encode();
+// SM count of the current device.
+int num_sms();
+// Tensor map over a bf16 view: box of 64 columns (128 bytes) x box_rows rows,
+// 128-byte swizzle, zero fill outside the view.
+int make_map_bf16(CUtensorMap* map, const Bf16View& v, int box_rows);
+
+// ---- DFP16 limb contraction (ito_dfp.cu)
+
+// P[M][N] (int64, exact) = sum_k A(m,k) B(n,k) for int16 operands given as two
+// bf16 limb planes each (value = 256 * hi + lo).
+struct DfpGemmPlan {
+    CUtensorMap mapAh, mapAl, mapBh, mapBl, mapC;
+    int use_tma_store;
+    int M, N, K;
+    bool a_mn, b_mn;
+    int64_t* C;
+    int64_t ldc;
+    unsigned long long* d_max;
+    int* err;
+};
+
+int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a_mn, const Bf16View& Bh,
+                  const Bf16View& Bl, bool b_mn, int M, int N, int K, int64_t* C, int64_t ldc,
+                  unsigned long long* d_max);
+int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s);
+
+// int16 [rows][cols] -> bf16 limb planes hi/lo [rows][ldl]
+int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t* hi, uint16_t* lo, int64_t ldl,
+                        cudaStream_t s);
+// DFP down-conversion of P with exponent *d_ea + *d_eb: Rs from *d_max,
+// out16 = sat16(rhu(P, Rs)) (+ limb planes if hi != null), *d_exp_out = Ea + Eb + Rs,
+// *d_rs = Rs; an exponent outside int8 raises ITO_ERR_EXPONENT in the error word.
+int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned long long* d_max, const int32_t* d_ea,
+                    const int32_t* d_eb, int16_t* out16, uint16_t* hi, uint16_t* lo, int64_t ldl, int32_t* d_exp_out,
+                    int32_t* d_rs, cudaStream_t s);
+// W <- sat16(W - dW), dW = rhu(G, k) (k >= 0) or G * 2^-k (k < 0), k = exp_w + eta - *d_exp_g
+int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const int16_t* G, int64_t rows,
+                      int64_t cols, const int32_t* d_exp_g, int32_t exp_w, int32_t eta, int32_t* d_k,
+                      uint32_t* d_nonzero, cudaStream_t s);
 
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
               int32_t* C, int64_t ldc, uint32_t* d_max);

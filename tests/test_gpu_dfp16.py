@@ -1,0 +1,173 @@
+"""DFP16 path on the GPU against the CPU oracle: exact int64 limb contractions
+(ragged shapes, extreme mantissas, chunk boundaries), down-conversion with its
+exponent, the integer update, and whole training steps in lockstep."""
+import numpy as np
+import pytest
+
+import oracle as O
+import seeded_inputs as si
+from gpu_util import compare_records, digest, import_ito, load_digests
+
+pytestmark = pytest.mark.gpu
+
+rng = np.random.default_rng(4242)
+
+
+@pytest.fixture(scope="module")
+def ito():
+    return import_ito()
+
+
+def _dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _h(t):
+    return t.cpu().numpy()
+
+
+def i16(shape, lim=32767):
+    return rng.integers(-lim, lim + 1, shape).astype(np.int16)
+
+
+SHAPES = [(1, 1, 1), (3, 27, 10), (16, 64, 48), (129, 513, 70), (200, 1025, 257), (64, 2048, 128)]
+
+
+def _check_down(P_ref, e_in, out, e_out, rs, mx):
+    m_ref, e_ref, rs_ref, mx_ref = O.dfp_down(P_ref, e_in)
+    assert np.array_equal(_h(out), m_ref)
+    assert int(_h(e_out)[0]) == e_ref and int(_h(rs)[0]) == rs_ref
+    assert int(_h(mx)[0]) == mx_ref
+
+
+@pytest.mark.parametrize("B,IC,OC", SHAPES)
+def test_dfp_fwd(ito, B, IC, OC):
+    x, W = i16((B, IC)), i16((OC, IC))
+    x[0, :] = -32767
+    W[0, :] = -32767
+    ex, ew = -12, -17
+    p64, mx, y, ey, rs = ito.ito_dfp16_linear_fwd(_dev(x), ito._i32dev(ex), _dev(W), ito._i32dev(ew))
+    P = O.dfp_linear_fwd(x, W)
+    assert np.array_equal(_h(p64), P)
+    _check_down(P, ex + ew, y, ey, rs, mx)
+
+
+@pytest.mark.parametrize("B,IC,OC", SHAPES)
+def test_dfp_bwd_delta(ito, B, IC, OC):
+    e, W = i16((B, OC)), i16((OC, IC))
+    p64, mx, dp, ee, rs = ito.ito_dfp16_linear_bwd_delta(_dev(e), ito._i32dev(-20), _dev(W), ito._i32dev(-17))
+    P = O.dfp_linear_dgrad(e, W)
+    assert np.array_equal(_h(p64), P)
+    _check_down(P, -37, dp, ee, rs, mx)
+
+
+@pytest.mark.parametrize("B,IC,OC", SHAPES + [(2048, 40, 24)])
+def test_dfp_wgrad(ito, B, IC, OC):
+    e, x = i16((B, OC)), i16((B, IC))
+    p64, mx, g, eg, rs = ito.ito_dfp16_linear_wgrad(_dev(e), ito._i32dev(-20), _dev(x), ito._i32dev(-12))
+    P = O.dfp_linear_wgrad(e, x)
+    assert np.array_equal(_h(p64), P)
+    _check_down(P, -32, g, eg, rs, mx)
+
+
+def test_dfp_extreme_chunks(ito):
+    """All products (-32767)^2: every limb accumulator reaches its chunk bound."""
+    for K in (511, 512, 513, 1024, 2048):
+        x = np.full((128, K), -32767, np.int16)
+        W = np.full((64, K), -32767, np.int16)
+        W[1::2] = 32767
+        p64, _, _, _, _ = ito.ito_dfp16_linear_fwd(_dev(x), ito._i32dev(0), _dev(W), ito._i32dev(0))
+        P = _h(p64)
+        assert (P[:, 0::2] == K * 32767 * 32767).all() and (P[:, 1::2] == -K * 32767 * 32767).all()
+
+
+@pytest.mark.parametrize("k_target", [-20, -3, 0, 5, 8, 15, 40])
+def test_dfp_update(ito, k_target):
+    n = 10007
+    W, g = i16(n), i16(n)
+    W[:3] = [32767, -32767, 0]
+    ew, eta = -17, 8
+    eg = ew + eta - k_target
+    Wd = _dev(W)
+    k, nz = ito.ito_dfp16_update(Wd, _dev(g), ito._i32dev(eg), ew, eta)
+    Wn, nzo = O.dfp_update(W, g, k_target)
+    assert int(_h(k)[0]) == k_target and int(_h(nz)[0]) == nzo
+    assert np.array_equal(_h(Wd), Wn)
+
+
+def test_dfp_exponent_overflow_is_reported(ito):
+    x, W = i16((8, 64)), i16((8, 64))
+    ito.ito_dfp16_linear_fwd(_dev(x), ito._i32dev(120), _dev(W), ito._i32dev(100))
+    assert ito.ito_get_error() == ito.ITO_ERR_EXPONENT
+    assert ito.ito_get_error() == 0          # read clears the word
+
+
+class DfpRun:
+    def __init__(self, w):
+        import torch
+        self.torch = torch
+        self.ito = import_ito()
+        self.w = w
+        self.m = self.ito.Dfp16Model(list(w.dims), w.batch, w.exp_w, O.DFP_ETA)
+        for l, W in enumerate(si.make_weights(w)):
+            self.m.set_weights(l, W)
+
+    def step(self, t):
+        x, _ = si.make_batch(self.w, t)
+        self.m.train_step(self.torch.from_numpy(x).cuda(), self.w.exp_x)
+        self.torch.cuda.synchronize()
+        return x
+
+    def record(self, kinds=("p", "y", "e", "pd", "pg", "g", "w")):
+        r = {}
+        L = self.m.n_layers
+        for l in range(L):
+            for k in kinds:
+                if k == "pd" and l == 0:
+                    continue
+                r["%s%d" % (k, l)] = self.m.tensor("%s%d" % (k, l)).cpu().numpy()
+        st = self.m.stats()
+        for k, v in st.items():
+            if (k.startswith("rsd") or k.startswith("pdmax")) and k.endswith("0") and len(k) in (4, 6):
+                continue
+            r[k] = v
+        return r
+
+
+def test_dfp_model_small_lockstep():
+    w = si.Workload(97, "dfp16_small", "dfp16", 16, dims=(64, 48, 32), sigma=4096.0, lim=32767,
+                    exp_x=-12, exp_w=-17)
+    g = DfpRun(w)
+    weights = si.make_weights(w)
+    for t in range(5):
+        x, _ = si.make_batch(w, t)
+        rec = O.dfp16_step(weights, w.exp_w, x, w.exp_x)
+        g.step(t)
+        compare_records(rec, g.record(), t)
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+
+
+def test_dfp_model_full_size_live_step():
+    w = si.by_name(4)
+    g = DfpRun(w)
+    weights = si.make_weights(w)
+    x, _ = si.make_batch(w, 0)
+    rec = O.dfp16_step(weights, w.exp_w, x, w.exp_x, route="f64")
+    g.step(0)
+    compare_records(rec, g.record(), 0)
+
+
+def test_dfp_model_100_steps_digests():
+    w = si.by_name(4)
+    ref = load_digests(w)
+    assert ref is not None and len(ref) == 100
+    g = DfpRun(w)
+    for t, d in enumerate(ref):
+        x = g.step(t)
+        assert digest(x) == d["in.x"], "input generator diverged"
+        kinds = ("p", "y", "e", "pd", "pg", "g", "w") if t < 3 else ("y", "e", "g", "w")
+        r = g.record(kinds)
+        bad = [k for k, v in r.items() if k in d and
+               (digest(v) if isinstance(v, np.ndarray) else int(v)) != d[k]]
+        assert not bad, "step %d differs from the oracle in %s" % (t, bad)
