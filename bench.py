@@ -48,14 +48,51 @@ def peaks():
         return dict(FALLBACK), "fallback"
 
 
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "k_gemm_tc__dram_per_launch__mlp4096x4-1000_b8192.md")
+GEMM_SOURCES = [os.path.join(ROOT, "integer_only_nn_gb300", "csrc", f) for f in ("ito_gemm.cu", "ito_device.cuh")]
+
+
+def gemm_traffic_per_launch(w):
+    """DRAM bytes per contraction launch from the committed ncu summary, or
+    None when the summary is for another workload or the kernel source has
+    changed since the counters were taken."""
+    import hashlib
+    if w.name != "mlp4096x4-1000_b8192":
+        return None
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+        h = hashlib.sha256(b"".join(open(f, "rb").read() for f in GEMM_SOURCES)).hexdigest()[:16]
+    except OSError:
+        return None
+    fields = dict(line.split(": ", 1) for line in text.splitlines() if ": " in line and line[:1].isalpha())
+    if fields.get("kernel_source_sha256_16", "").strip() != h:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch_avg"])
+    except (KeyError, ValueError):
+        return None
+
+
 def algorithmic_ops(w):
-    """Integer ops (2 per multiply-accumulate) of one training step."""
-    if w.kind != "mlp":
-        raise ValueError("bench covers the MLP workloads")
-    B, d = w.batch, w.dims
-    fwd = sum(d[i] * d[i + 1] for i in range(len(d) - 1))
-    dgrad = sum(d[i] * d[i + 1] for i in range(1, len(d) - 1))
-    return 2.0 * B * (2 * fwd + dgrad)
+    """Integer ops (2 per multiply-accumulate) of one training step: forward,
+    weight gradient and delta propagation (not for the first layer). For the
+    DFP16 workload these are int16 multiply-accumulates; its tensor cores
+    execute four bf16 limb products for each."""
+    B = w.batch
+    if w.kind in ("mlp", "dfp16"):
+        d = w.dims
+        fwd = sum(d[i] * d[i + 1] for i in range(len(d) - 1))
+        dgrad = sum(d[i] * d[i + 1] for i in range(1, len(d) - 1))
+        return 2.0 * B * (2 * fwd + dgrad)
+    H, W, _ = w.image
+    fwd = dgrad = 0
+    for l, (ic, oc, s) in enumerate(w.convs):
+        H, W = (H + 2 - 3) // s + 1, (W + 2 - 3) // s + 1
+        macs = B * H * W * oc * 9 * ic
+        fwd += macs
+        dgrad += macs if l > 0 else 0
+    fc = B * w.fc[0] * w.fc[1]
+    return 2.0 * (2 * (fwd + fc) + dgrad + fc)
 
 
 class Clocks:
@@ -108,6 +145,16 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def oracle_step(w, weights, x, labels):
+    """One CPU-oracle training step (plain C loops) of workload w."""
+    import oracle as O
+    if w.kind == "mlp":
+        return O.mlp_step(weights, x, labels, route="loops")
+    if w.kind == "cnn":
+        return O.cnn_step(weights, x, labels, w.convs)
+    return O.dfp16_step(weights, w.exp_w, x, w.exp_x, route="loops")
+
+
 def cpu_baseline(w, sample_batch):
     """The CPU oracle (plain C loops, OpenMP over output rows) on one training
     step of `sample_batch` samples of workload w."""
@@ -117,9 +164,10 @@ def cpu_baseline(w, sample_batch):
     O.build()
     weights = si.make_weights(w)
     x, labels = si.make_batch(w, 0)
-    x, labels = np.ascontiguousarray(x[:sample_batch]), np.ascontiguousarray(labels[:sample_batch])
+    x = np.ascontiguousarray(x[:sample_batch])
+    labels = None if labels is None else np.ascontiguousarray(labels[:sample_batch])
     t0 = time.perf_counter()
-    O.mlp_step(weights, x, labels, route="loops")
+    oracle_step(w, weights, x, labels)
     dt = time.perf_counter() - t0
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return sample_batch / dt, dt, cores
@@ -138,14 +186,15 @@ def run_reference(args, w):
     batches = []
     for t in range(2):
         x, labels = si.make_batch(w, t)
-        batches.append((np.ascontiguousarray(x[:sample]), np.ascontiguousarray(labels[:sample])))
+        batches.append((np.ascontiguousarray(x[:sample]),
+                        None if labels is None else np.ascontiguousarray(labels[:sample])))
     for i in range(args.warmup):
         x, lab = batches[i % 2]
-        O.mlp_step(weights, x, lab, route="loops")
+        oracle_step(w, weights, x, lab)
     t0 = time.perf_counter()
     for i in range(args.steps):
         x, lab = batches[i % 2]
-        rec = O.mlp_step(weights, x, lab, route="loops")
+        rec = oracle_step(w, weights, x, lab)
         weights = [rec["w%d" % l] for l in range(len(weights))]
     dt = time.perf_counter() - t0
     value = sample * args.steps / dt
@@ -192,6 +241,8 @@ def run_ours(args, w):
                "sample": "one oracle training step (C loops) on %d of the %d samples of %s, %.1f s"
                          % (args.cpu_batch, w.batch, w.name, dt)}
 
+    if w.kind == "dfp16":
+        return run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local)
     stream = torch.cuda.current_stream()
     model = ito.Model(ito.layers_for(w), w.batch)
     for l, W in enumerate(si.make_weights(w)):
@@ -276,7 +327,8 @@ def run_ours(args, w):
         "int_tops": algorithmic_ops(w) * world * K / (total_ms / 1000.0) / 1e12,
         "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (bf16-embedded int8 contractions, all GEMM launches)",
                      "achieved": g_tflops, "peak": peak, "unit": "TFLOP/s", "frac": g_tflops / peak,
-                     "peak_source": "bf16_tflops_sustained, %s" % pk_src, "traffic": None,
+                     "peak_source": "bf16_tflops_sustained, %s" % pk_src,
+                     "traffic": gemm_traffic_per_launch(w), "traffic_unit": "bytes per launch (ncu, committed summary)",
                      "launches_timed": g_n},
         "passes": {"requant_gbs": r_work / (r_ms / 1000.0) / 1e9 if r_ms else None,
                    "update_gbs": u_work / (u_ms / 1000.0) / 1e9 if u_ms else None,
@@ -323,6 +375,54 @@ def run_op(args):
     ms = s0.elapsed_time(s1) / args.steps
     print(json.dumps({"op": args.op, "shape": [B, IC, OC], "ms_per_call": ms,
                       "tflops_incl_conversions": 2.0 * B * IC * OC / (ms / 1000.0) / 1e12}), flush=True)
+    return 0
+
+
+def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local):
+    """Step time of the DFP16 workload (device-timed with CUDA events)."""
+    import torch
+    import integer_only_nn_gb300 as ito
+    import oracle as O
+    import seeded_inputs as si
+    stream = torch.cuda.current_stream()
+    model = ito.Dfp16Model(list(w.dims), w.batch, w.exp_w, O.DFP_ETA)
+    for l, W in enumerate(si.make_weights(w)):
+        model.set_weights(l, W)
+    xs = [torch.from_numpy(si.make_batch(w, t)[0]).cuda() for t in range(2)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    K = args.steps
+    for i in range(args.warmup):
+        model.train_step(xs[i % 2], w.exp_x)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = Clocks(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for k in range(K):
+        flush.fill_(k & 0xFF)
+        starts[k].record(stream)
+        model.train_step(xs[k % 2], w.exp_x)
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    if ito.ito_get_error() != 0:
+        raise RuntimeError("device error word set after the timed steps")
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if rank != 0:
+        return 0
+    ops = algorithmic_ops(w)
+    line = {"metric": METRIC, "value": world * w.batch * K / (total_ms / 1000.0), "unit": "samples/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int16 (DFP16)",
+            "data": "synthetic", "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims)},
+            "int16_tops": ops * world * K / (total_ms / 1000.0) / 1e12,
+            "executed_limb_tops": 4 * ops * world * K / (total_ms / 1000.0) / 1e12, "clocks": clk}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
     return 0
 
 
