@@ -24,6 +24,7 @@
 // SIMT path (k_gemm_simt): a plain tiled int32 kernel with arbitrary strides,
 // used as an independent on-GPU cross-check of the tensor-core path.
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include <cudaTypedefs.h>
@@ -284,6 +285,239 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     }
 }
 
+
+// --------------------------------------------- CTA-pair tensor-core kernel
+//
+// A cluster of two CTAs on one TPC computes a 256 x 256 tile with
+// tcgen05.mma.cta_group::2: each CTA loads its 128 rows of A and its half (128
+// rows) of the B tile, both halves' TMA loads complete on the leader CTA's
+// barrier, the leader's single MMA thread issues the M = 256 MMAs, and each
+// CTA's tensor memory receives its 128 rows of the accumulator. Per SM this
+// halves the B bytes moved from L2 and stored in shared memory, so six 32 KB
+// stages hold twice the MMA work of the single-CTA kernel's four 48 KB stages.
+// Exactness and the epilogue are as in k_gemm_tc; both CTAs' epilogue warps
+// release an accumulator buffer on the leader's barrier.
+
+struct Tc2Cfg {
+    static constexpr int BM = 128;                          // rows of A per CTA (256 per pair)
+    static constexpr int BN = 256;                          // columns per pair tile
+    static constexpr int BK = 64;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = (BN / 2) * BK * 2;       // this CTA's half of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = 6;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + EPI_WARPS * 32;
+    static constexpr int TMEM_COLS = 512;                   // two 256-column fp32 accumulators
+    static constexpr int STAGING_BYTES = EPI_WARPS * 4096;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
+    k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
+               int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max, int* __restrict__ err)
+{
+    using Cfg = Tc2Cfg;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int HALF = BN / 2;
+    constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* staging = smem + STAGES * Cfg::STAGE_BYTES;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
+    uint64_t* empty_bar = full_bar + STAGES;
+    uint64_t* accf_bar = empty_bar + STAGES;
+    uint64_t* acce_bar = accf_bar + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
+    const TileSched sched{(M + 2 * BM - 1) / (2 * BM), (N + BN - 1) / BN, 16};
+    const int num_tiles = sched.num_m * sched.num_n;
+    const int num_kb = (K + BK - 1) / BK;
+    const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf_bar[b], 1);
+            mbar_init(&acce_bar[b], 2 * Cfg::EPI_WARPS);   // epilogue warps of both CTAs
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs): loads complete on the leader's barrier
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+                int tm, tn;
+                sched.coords(t, tm, tn);
+                const int rowA = tm * 2 * BM + rank * BM;
+                const int rowB = tn * BN + rank * (BN / 2);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
+                    const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                    uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
+                    uint8_t* sB = sA + Cfg::A_BYTES;
+                    if (!A_MN) {
+                        tma_load_2d_pair(&tmA, fb, sA, kb * BK, rowA);
+                    } else {
+                        tma_load_2d_pair(&tmA, fb, sA, rowA, kb * BK);
+                        tma_load_2d_pair(&tmA, fb, sA + 8192, rowA + 64, kb * BK);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d_pair(&tmB, fb, sB, kb * BK, rowB);
+                    } else {
+                        tma_load_2d_pair(&tmB, fb, sB, rowB, kb * BK);
+                        tma_load_2d_pair(&tmB, fb, sB + 8192, rowB + 64, kb * BK);
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: one thread of the leader CTA
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+                for (int c = 0; ok && c < num_chunks; ++c) {
+                    if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                    const int kb0 = c * chunk_kb;
+                    const int kb1 = min(num_kb, kb0 + chunk_kb);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full_bar[stage], phase, abort_flag, err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                        const uint32_t b0 = a0 + Cfg::A_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, 8192, 1024)
+                                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                            const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
+                                                     : smem_desc_sw128(b0 + k * 32, 16, 1024);
+                            tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        tc_commit_pair_mc(&empty_bar[stage], 0x3);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_mc(&accf_bar[buf], 0x3);
+                    if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile
+        const int e = warp - 2;
+        const int quad = warp & 3;
+        const int half = e >> 2;
+        uint8_t* stg = staging + e * 4096;
+        const uint32_t stg_row = smem_u32(stg) + lane * 128;
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        bool ok = true;
+        for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+            int tm, tn;
+            sched.coords(t, tm, tn);
+            int32_t acc[HALF];
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) acc[i] = 0;
+            for (int c = 0; c < num_chunks; ++c) {
+                if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + half * HALF);
+#pragma unroll
+                for (int j = 0; j < HALF / 16; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + j * 16, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[j * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[buf]), 0));
+                if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+            }
+            if (!ok) break;
+            uint32_t mx = 0;
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) mx = max(mx, abs_u32(acc[i]));
+            mx = __reduce_max_sync(0xffffffffu, mx);
+            if (lane == 0 && mx != 0) atomicMax(d_max, mx);
+            const int row0 = tm * 2 * BM + (int)rank * BM + quad * 32;
+            const int col0 = tn * BN + half * HALF;
+            if (use_tma_store) {
+#pragma unroll
+                for (int g = 0; g < HALF / 32; ++g) {
+                    if (row0 >= M || col0 + g * 32 >= N) continue;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), acc[g * 32 + 4 * j], acc[g * 32 + 4 * j + 1],
+                                     acc[g * 32 + 4 * j + 2], acc[g * 32 + 4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, stg, col0 + g * 32, row0);
+                        bulk_commit();
+                    }
+                }
+            } else {
+                const int row = row0 + lane;
+                if (row < M) {
+                    int32_t* dst = C + (int64_t)row * ldc + col0;
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i)
+                        if (col0 + i < N) dst[i] = acc[i];
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    cluster_sync();   // the pair's MMAs and drains are complete in both CTAs
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
 // --------------------------------------------------------------- SIMT path
 
 constexpr int SIMT_BM = 64, SIMT_BN = 64, SIMT_BK = 32;
@@ -405,6 +639,51 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
     return ITO_OK;
 }
 
+template <bool A_MN, bool B_MN>
+static int launch_tc2(const GemmPlan& p, cudaStream_t s)
+{
+    using Cfg = Tc2Cfg;
+    auto kern = k_gemm_tc2<A_MN, B_MN>;
+    static int max_clusters = 0;
+    if (!max_clusters) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(2 * num_sms());
+        q.blockDim = dim3(Cfg::THREADS);
+        q.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = 2;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1)
+            return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
+        max_clusters = n;
+    }
+    const int tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
+    const int clusters = tiles < max_clusters ? tiles : max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.use_tma_store, p.M, p.N, p.K,
+                                       p.chunk_kb, p.C, p.ldc, p.d_max, p.err);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "pair gemm launch: %s", cudaGetErrorString(e));
+    return ITO_OK;
+}
+
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
               int32_t* C, int64_t ldc, uint32_t* d_max)
 {
@@ -428,9 +707,16 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
     p->err = device_error_word();
     if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     p->bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+    // CTA-pair kernel for large tiles; ITO_GEMM_PAIR=0 in the environment forces the single-CTA kernel
+    static const int pair_env = [] {
+        const char* v = getenv("ITO_GEMM_PAIR");
+        return v ? atoi(v) : 1;
+    }();
+    p->pair = pair_env != 0 && M >= 256 && N >= 256;
     int r = make_map_bf16(&p->mapA, A, a_mn ? 64 : 128);
     if (r) return r;
-    r = make_map_bf16(&p->mapB, B, b_mn ? 64 : p->bn);
+    // the pair kernel loads half of a 256-wide B tile per CTA
+    r = make_map_bf16(&p->mapB, B, b_mn ? 64 : (p->pair ? 128 : p->bn));
     if (r) return r;
     // int32 output through TMA stores when its rows are 16-byte aligned; plain stores otherwise
     p->use_tma_store = 0;
@@ -451,6 +737,12 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
 
 int gemm_run(const GemmPlan& p, cudaStream_t s)
 {
+    if (p.pair) {
+        if (!p.a_mn && !p.b_mn) return launch_tc2<false, false>(p, s);
+        if (!p.a_mn && p.b_mn) return launch_tc2<false, true>(p, s);
+        if (p.a_mn && p.b_mn) return launch_tc2<true, true>(p, s);
+        return launch_tc2<true, false>(p, s);
+    }
 #define ITO_TC_CASE(BN)                                                            \
     if (p.bn == BN) {                                                              \
         if (!p.a_mn && !p.b_mn) return launch_tc<BN, false, false>(p, s);          \

@@ -32,6 +32,7 @@ struct Bf16View {
 struct GemmPlan {
     CUtensorMap mapA, mapB, mapC;
     int use_tma_store;
+    int pair;   // CTA-pair (cta_group::2) kernel
     int M, N, K, bn, chunk_kb;
     bool a_mn, b_mn;
     int32_t* C;
