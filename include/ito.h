@@ -87,7 +87,9 @@ int ito_version(void);
  * ---------------------------------------------------------------------- */
 
 /* Bytes of device workspace any of ito_linear_fwd / _bwd_delta / _wgrad needs
- * for these sizes (0 on invalid sizes). */
+ * for these sizes (0 on invalid sizes): the bf16 operand copies, plus room for
+ * int32 partial results when a contraction with few output tiles and a long
+ * K is split along K across SMs (partials summed exactly afterwards). */
 size_t ito_linear_workspace_size(int B, int IC, int OC);
 
 /* Forward contraction + requantisation of one Linear layer ("Integer
@@ -118,9 +120,10 @@ int ito_linear_fwd(const int8_t *x, const int8_t *W, int B, int IC, int OC, int 
  *
  * It computes exactly what ito_linear_fwd computes, with the same arguments
  * minus workspace/workspace_bytes, and allocates nothing: its scratch (the
- * bf16 copies of x and W, ito_linear_workspace_size(B, IC, OC) bytes) is a
- * fixed device array of ITO_NOALLOC_SCRATCH_BYTES inside the library, which
- * every GPU that loads the library holds until the process exits.
+ * bf16 copies of x and W, rows padded to 8 elements, each copy rounded up to
+ * 256 bytes) is a fixed device array of ITO_NOALLOC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. (It never splits the contraction along K.)
  *  - Sizes whose scratch need exceeds ITO_NOALLOC_SCRATCH_BYTES are rejected
  *    with ITO_ERR_SHAPE before anything is enqueued.
  *  - The first call on a device looks up the array's device address on that

@@ -27,6 +27,17 @@ static inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 // slot 1 the bf16 copy of the weight or of the layer input.
 static size_t ws_slot0(int B, int IC, int OC) { return align256((size_t)2 * B * pad8(IC > OC ? IC : OC)); }
 static size_t ws_slot1(int B, int IC, int OC) { return align256((size_t)2 * (OC > B ? OC : B) * pad8(IC)); }
+// slot 2: split-K partials of whichever of the three contractions needs most
+static size_t ws_slot2(int B, int IC, int OC)
+{
+    size_t a = gemm_split_ws_bytes(B, OC, IC, OC), b = gemm_split_ws_bytes(B, IC, OC, IC),
+           c = gemm_split_ws_bytes(OC, IC, B, IC);
+    return align256(a > b ? (a > c ? a : c) : (b > c ? b : c));
+}
+static int32_t* ws_split(void* ws, int B, int IC, int OC)
+{
+    return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + ws_slot0(B, IC, OC) + ws_slot1(B, IC, OC));
+}
 
 static int check_sizes(int B, int IC, int OC)
 {
@@ -80,7 +91,7 @@ int ito_get_error(void)
 size_t ito_linear_workspace_size(int B, int IC, int OC)
 {
     if (B < 1 || IC < 1 || OC < 1) return 0;
-    return ws_slot0(B, IC, OC) + ws_slot1(B, IC, OC);
+    return ws_slot0(B, IC, OC) + ws_slot1(B, IC, OC) + ws_slot2(B, IC, OC);
 }
 
 int ito_linear_fwd(const int8_t* x, const int8_t* W, int B, int IC, int OC, int relu, ito_niti_params p,
@@ -99,7 +110,7 @@ int ito_linear_fwd(const int8_t* x, const int8_t* W, int B, int IC, int OC, int 
     ITO_TRY(cuda_ok(cudaMemsetAsync(d_max, 0, sizeof(uint32_t), s), "memset"));
     GemmPlan g;
     ITO_TRY(gemm_plan(&g, Bf16View{xb, B, IC, ld}, false, Bf16View{Wb, OC, IC, ld}, false, B, OC, IC, y32, OC,
-                      d_max));
+                      d_max, ws_split(workspace, B, IC, OC), ws_slot2(B, IC, OC)));
     ITO_TRY(gemm_run(g, s));
     return launch_requant(y32, B, OC, d_max, p.target_bits, relu, nullptr, y, nullptr, 0, d_shift, s);
 }
@@ -121,7 +132,7 @@ int ito_linear_bwd_delta(const int8_t* delta, const int8_t* W, const int8_t* a_p
     GemmPlan g;
     // D[b][ic] = sum_oc delta[b][oc] W[oc][ic]: A = delta (K-major), B = W read as [K=OC][N=IC] (MN-major)
     ITO_TRY(gemm_plan(&g, Bf16View{eb, B, OC, lde}, false, Bf16View{Wb, OC, IC, ldw}, true, B, IC, OC, d32, IC,
-                      d_max));
+                      d_max, ws_split(workspace, B, IC, OC), ws_slot2(B, IC, OC)));
     ITO_TRY(gemm_run(g, s));
     return launch_requant(d32, B, IC, d_max, p.target_bits, 0, a_prev, delta_prev, nullptr, 0, d_shift, s);
 }
@@ -141,7 +152,8 @@ int ito_linear_wgrad(const int8_t* delta, const int8_t* a_prev, int B, int IC, i
     ITO_TRY(cuda_ok(cudaMemsetAsync(d_max, 0, sizeof(uint32_t), s), "memset"));
     GemmPlan g;
     // G[oc][ic] = sum_b delta[b][oc] a[b][ic]: A = delta read as [K=B][M=OC], B = a read as [K=B][N=IC]
-    ITO_TRY(gemm_plan(&g, Bf16View{eb, B, OC, lde}, true, Bf16View{ab, B, IC, lda}, true, OC, IC, B, G, IC, d_max));
+    ITO_TRY(gemm_plan(&g, Bf16View{eb, B, OC, lde}, true, Bf16View{ab, B, IC, lda}, true, OC, IC, B, G, IC, d_max,
+                      ws_split(workspace, B, IC, OC), ws_slot2(B, IC, OC)));
     return gemm_run(g, s);
 }
 

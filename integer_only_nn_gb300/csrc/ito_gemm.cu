@@ -83,8 +83,12 @@ template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
-              int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max, int* __restrict__ err)
+              int splits, int kb_per_split, int64_t split_stride, int32_t* __restrict__ C, int64_t ldc,
+              uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
+    // Work item w covers output tile w / splits and the K slice w % splits; with
+    // splits > 1 each slice writes an int32 partial tile at C + slice * split_stride
+    // (plain stores, no max) and a reduction kernel adds the slices.
     using Cfg = TcCfg<BN>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;                             // columns per epilogue warp
@@ -104,9 +108,13 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     const TileSched sched{(M + BM - 1) / BM, (N + BN - 1) / BN, 16};
-    const int num_tiles = sched.num_m * sched.num_n;
+    const int num_items = sched.num_m * sched.num_n * splits;
     const int num_kb = (K + BK - 1) / BK;
-    const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
+    // K-block range and chunk count of work item w
+    auto kb_range = [&](int w, int& lo, int& hi) {
+        lo = (w % splits) * kb_per_split;
+        hi = min(num_kb, lo + kb_per_split);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -137,10 +145,11 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                int tm, tn;
-                sched.coords(t, tm, tn);
-                for (int kb = 0; kb < num_kb; ++kb) {
+            for (int w = blockIdx.x; ok && w < num_items; w += gridDim.x) {
+                int tm, tn, kb_lo, kb_hi;
+                sched.coords(w / splits, tm, tn);
+                kb_range(w, kb_lo, kb_hi);
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
                     uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
@@ -171,13 +180,16 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            for (int w = blockIdx.x; ok && w < num_items; w += gridDim.x) {
+                int kb_lo, kb_hi;
+                kb_range(w, kb_lo, kb_hi);
+                const int num_chunks = (kb_hi - kb_lo + chunk_kb - 1) / chunk_kb;
                 for (int c = 0; ok && c < num_chunks; ++c) {
                     if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                    const int kb0 = c * chunk_kb;
-                    const int kb1 = min(num_kb, kb0 + chunk_kb);
+                    const int kb0 = kb_lo + c * chunk_kb;
+                    const int kb1 = min(kb_hi, kb0 + chunk_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&full_bar[stage], phase, abort_flag, err)) { ok = false; break; }
                         tc_fence_after();
@@ -212,9 +224,12 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            int tm, tn;
-            sched.coords(t, tm, tn);
+        for (int w = blockIdx.x; ok && w < num_items; w += gridDim.x) {
+            int tm, tn, kb_lo, kb_hi;
+            sched.coords(w / splits, tm, tn);
+            kb_range(w, kb_lo, kb_hi);
+            const int num_chunks = (kb_hi - kb_lo + chunk_kb - 1) / chunk_kb;
+            int32_t* Cw = C + (int64_t)(w % splits) * split_stride;
             int32_t acc[HALF];
 #pragma unroll
             for (int i = 0; i < HALF; ++i) acc[i] = 0;
@@ -242,7 +257,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < HALF; ++i) mx = max(mx, abs_u32(acc[i]));
             mx = __reduce_max_sync(0xffffffffu, mx);
-            if (lane == 0 && mx != 0) atomicMax(d_max, mx);
+            if (lane == 0 && mx != 0 && d_max) atomicMax(d_max, mx);
             const int row0 = tm * BM + quad * 32;
             const int col0 = tn * BN + half * HALF;
             if (use_tma_store) {
@@ -267,7 +282,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
             } else {
                 const int row = row0 + lane;
                 if (row < M) {
-                    int32_t* dst = C + (int64_t)row * ldc + col0;
+                    int32_t* dst = Cw + (int64_t)row * ldc + col0;
 #pragma unroll
                     for (int i = 0; i < HALF; ++i)
                         if (col0 + i < N) dst[i] = acc[i];
@@ -619,6 +634,25 @@ int num_sms()
     return n;
 }
 
+// C[r][c] = sum over slices of P[s][r][c]; max |C| folded into *d_max. Integer
+// addition wraps modulo 2^32, so the slice order cannot change a result that fits int32.
+__global__ void k_splitk_reduce(const int32_t* __restrict__ P, int splits, int64_t stride, int M, int N, int64_t ldc,
+                                int32_t* __restrict__ C, uint32_t* __restrict__ d_max)
+{
+    const int64_t n = (int64_t)M * N;
+    uint32_t mx = 0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / N, c = i - r * N;
+        const int64_t off = r * ldc + c;
+        int32_t acc = 0;
+        for (int s = 0; s < splits; ++s) acc += __ldcs(P + s * stride + off);
+        C[off] = acc;
+        mx = max(mx, abs_u32(acc));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+}
+
 template <int BN, bool A_MN, bool B_MN>
 static int launch_tc(const GemmPlan& p, cudaStream_t s)
 {
@@ -630,12 +664,21 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
             return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
         attr_set = true;
     }
-    const int tiles = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + BN - 1) / BN);
-    const int grid = tiles < num_sms() ? tiles : num_sms();
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(p.mapA, p.mapB, p.mapC, p.use_tma_store, p.M, p.N, p.K,
-                                                     p.chunk_kb, p.C, p.ldc, p.d_max, p.err);
+    const int items = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + BN - 1) / BN) * p.splits;
+    const int grid = items < num_sms() ? items : num_sms();
+    const bool split = p.splits > 1;
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(p.mapA, p.mapB, p.mapC, split ? 0 : p.use_tma_store, p.M, p.N,
+                                                     p.K, p.chunk_kb, p.splits, p.kb_per_split, p.split_stride,
+                                                     split ? p.split_ws : p.C, p.ldc, split ? nullptr : p.d_max,
+                                                     p.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+    if (split) {
+        k_splitk_reduce<<<launch_grid_blocks((int64_t)p.M * p.N, 256), 256, 0, s>>>(
+            p.split_ws, p.splits, p.split_stride, p.M, p.N, p.ldc, p.C, p.d_max);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "split-K reduce launch: %s", cudaGetErrorString(e));
+    }
     return ITO_OK;
 }
 
@@ -684,8 +727,29 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     return ITO_OK;
 }
 
+// K slices for a contraction with few output tiles and a long K on the
+// single-CTA kernel (1 = no split): enough work items to cover the SMs, each
+// slice at least one K block.
+static int split_count(int M, int N, int K)
+{
+    const int bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+    const int tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+    const int num_kb = (K + 63) / 64;
+    if (num_kb < 32 || 2 * tiles > num_sms()) return 1;
+    int splits = num_sms() / tiles;
+    if (splits > num_kb) splits = num_kb;
+    const int per = (num_kb + splits - 1) / splits;
+    return (num_kb + per - 1) / per;
+}
+
+size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc)
+{
+    const int s = split_count(M, N, K);
+    return s > 1 ? (size_t)s * M * ldc * sizeof(int32_t) : 0;
+}
+
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
-              int32_t* C, int64_t ldc, uint32_t* d_max)
+              int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws, size_t split_ws_bytes)
 {
     if (M < 1 || N < 1 || K < 1) return set_error(ITO_ERR_SHAPE, "gemm: empty contraction");
     if (K > (1 << 20)) return set_error(ITO_ERR_SHAPE, "gemm: contraction longer than 2^20");
@@ -712,7 +776,17 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
         const char* v = getenv("ITO_GEMM_PAIR");
         return v ? atoi(v) : 1;
     }();
-    p->pair = pair_env != 0 && M >= 256 && N >= 256;
+    p->splits = 1;
+    p->kb_per_split = (K + 63) / 64;
+    const int splits = split_count(M, N, K);
+    if (splits > 1 && split_ws && split_ws_bytes >= (size_t)splits * M * ldc * sizeof(int32_t)) {
+        const int num_kb = (K + 63) / 64;
+        p->splits = splits;
+        p->kb_per_split = (num_kb + splits - 1) / splits;
+        p->split_ws = split_ws;
+        p->split_stride = (int64_t)M * ldc;
+    }
+    p->pair = pair_env != 0 && M >= 256 && N >= 256 && p->splits == 1;
     int r = make_map_bf16(&p->mapA, A, a_mn ? 64 : 128);
     if (r) return r;
     // the pair kernel loads half of a 256-wide B tile per CTA

@@ -34,6 +34,9 @@ struct GemmPlan {
     int use_tma_store;
     int pair;   // CTA-pair (cta_group::2) kernel
     int M, N, K, bn, chunk_kb;
+    int splits, kb_per_split;     // split-K: slices of kb_per_split K blocks (splits == 1: none)
+    int32_t* split_ws;            // [splits][M][ldc] int32 partials
+    int64_t split_stride;
     bool a_mn, b_mn;
     int32_t* C;
     int64_t ldc;
@@ -86,8 +89,12 @@ int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const
                       int64_t cols, const int32_t* d_exp_g, int32_t exp_w, int32_t eta, int32_t* d_k,
                       uint32_t* d_nonzero, cudaStream_t s);
 
+// split_ws (optional): room for split-K partials; without it (or when too
+// small) the contraction is not split.
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
-              int32_t* C, int64_t ldc, uint32_t* d_max);
+              int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws = nullptr, size_t split_ws_bytes = 0);
+// bytes of split-K partials gemm_plan would use for this contraction (0: no split)
+size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc);
 int gemm_run(const GemmPlan& p, cudaStream_t s);
 int gemm_simt(const int8_t* A, int64_t sam, int64_t sak, const int8_t* B, int64_t sbn, int64_t sbk, int M, int N,
               int K, int32_t* C, int64_t ldc, uint32_t* d_max, cudaStream_t s);

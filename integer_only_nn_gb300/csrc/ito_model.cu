@@ -17,6 +17,7 @@
 // Step order: forward over all layers; top error; for each layer from the top
 // down: delta propagation with the weights before this step's update (not for
 // the first layer), weight gradient, NITI update.
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -80,6 +81,8 @@ struct ito_model {
     int32_t* stats = nullptr;
     int n_stats = 0;
     uint32_t* discard_max = nullptr;   // max target of the patch-space conv delta (not a NITI tensor)
+    int32_t* split_ws = nullptr;       // split-K partials, shared by the step's contractions (one stream)
+    size_t split_ws_bytes = 0;
     std::vector<void*> allocs;
     std::vector<std::pair<std::string, int>> stat_names;
     // measurement hooks
@@ -262,6 +265,17 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         }
     }
 
+    // split-K partials: one buffer for the largest need (the step's kernels run in order)
+    for (int l = 0; l < nl; ++l) {
+        const MLayer& L = m->L[l];
+        const int M = (int)L.rows_out;
+        size_t need = gemm_split_ws_bytes(M, L.OC, (int)L.K, L.OC);
+        if (L.has_dgrad) need = std::max(need, gemm_split_ws_bytes(M, (int)L.K, L.OC, L.K));
+        need = std::max(need, gemm_split_ws_bytes(L.OC, (int)L.K, M, L.K));
+        m->split_ws_bytes = std::max(m->split_ws_bytes, need);
+    }
+    if (m->split_ws_bytes) ITO_TRY(m->alloc(&m->split_ws, m->split_ws_bytes / sizeof(int32_t)));
+
     // contraction plans (tensor maps over the buffers above)
     for (int l = 0; l < nl; ++l) {
         MLayer& L = m->L[l];
@@ -283,14 +297,16 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         }
         const int M = (int)L.rows_out;
         // forward: Y[m][oc] = sum_k in[m][k] W[oc][k]
-        ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax));
+        ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax, m->split_ws,
+                          m->split_ws_bytes));
         // delta propagation: D[m][k] = sum_oc e[m][oc] W[oc][k]; for a conv this is the
         // patch-space delta, whose max is not the NITI max (col2im takes that)
         if (L.has_dgrad)
             ITO_TRY(gemm_plan(&L.pd, ev, false, wv, true, M, (int)L.K, L.OC, conv ? L.dcol : L.d32, L.K,
-                              conv ? m->discard_max : dmax));
+                              conv ? m->discard_max : dmax, m->split_ws, m->split_ws_bytes));
         // weight gradient: G[oc][k] = sum_m e[m][oc] in[m][k]
-        ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax));
+        ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax, m->split_ws,
+                          m->split_ws_bytes));
     }
 
     // names of the stats entries
