@@ -243,41 +243,52 @@ def run_ours(args, w):
 
     if w.kind == "dfp16":
         return run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local)
-    stream = torch.cuda.current_stream()
+    # the step runs on a side stream so that it can replay from CUDA graphs
+    stream = torch.cuda.Stream()
     model = ito.Model(ito.layers_for(w), w.batch)
     for l, W in enumerate(si.make_weights(w)):
-        model.set_weights(l, W)
+        model.set_weights(l, W, stream=stream)
+    model.use_graphs(not args.no_graphs)
     xs, ls = [], []
     for t in range(2):
         x, labels = si.make_batch(w, t)
         xs.append(torch.from_numpy(x).cuda())
         ls.append(torch.from_numpy(labels).cuda())
+    torch.cuda.synchronize()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     K, Wm = args.steps, args.warmup
 
     for i in range(Wm):
-        model.train_step(xs[i % 2], ls[i % 2])
-    torch.cuda.synchronize()
+        model.train_step(xs[i % 2], ls[i % 2], stream=stream)
+    stream.synchronize()
     assert ito.ito_get_error() == 0
 
+    # per-kernel timing events (captured into the step graphs): re-capture, then read per step
     model.profile(True)
+    for i in range(4):
+        model.train_step(xs[i % 2], ls[i % 2], stream=stream)
     model.profile_read()
+    prof = {c: [0.0, 0.0, 0] for c in ("gemm", "requant", "update", "other")}
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     clocks = Clocks(local)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
-    for k in range(K):
-        flush.fill_(k & 0xFF)
-        starts[k].record(stream)
-        model.train_step(xs[k % 2], ls[k % 2])
-        ends[k].record(stream)
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            flush.fill_(k & 0xFF)
+            starts[k].record(stream)
+            model.train_step(xs[k % 2], ls[k % 2], stream=stream)
+            ends[k].record(stream)
+            for c, (ms, work, n) in model.profile_read().items():
+                prof[c][0] += ms
+                prof[c][1] += work
+                prof[c][2] += n
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    prof = model.profile_read()
     model.profile(False)
     err = ito.ito_get_error()
     if err != 0:
@@ -292,12 +303,12 @@ def run_ours(args, w):
     x_h = torch.from_numpy(si.make_batch(w, 0)[0]).pin_memory()
     l_h = torch.from_numpy(si.make_batch(w, 0)[1]).pin_memory()
     st_h = torch.zeros(model.num_stats(), dtype=torch.int32).pin_memory()
-    for _ in range(2):
-        model.train_step_host(x_h, l_h, st_h)
+    for _ in range(3):
+        model.train_step_host(x_h, l_h, st_h, stream=stream)
     barrier()
     t0 = time.perf_counter()
     for _ in range(K):
-        model.train_step_host(x_h, l_h, st_h)
+        model.train_step_host(x_h, l_h, st_h, stream=stream)
     e2e_s = time.perf_counter() - t0
     if dist is not None:
         t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
@@ -312,6 +323,7 @@ def run_ours(args, w):
     samples = world * w.batch * K
     value = samples / (total_ms / 1000.0)
     g_ms, g_work, g_n = prof["gemm"]
+    prof = {c: tuple(v) for c, v in prof.items()}
     g_tflops = g_work / (g_ms / 1000.0) / 1e12
     peak = float(pk["bf16_tflops_sustained"])
     r_ms, r_work, _ = prof["requant"]
@@ -323,6 +335,7 @@ def run_ours(args, w):
         "dtype": "int8", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims),
                    "l2": "flushed by a 256 MB write before every timed step; flush not timed",
+                   "graphs": not args.no_graphs,
                    "parallelism": "replicas" if world > 1 else "single"},
         "int_tops": algorithmic_ops(w) * world * K / (total_ms / 1000.0) / 1e12,
         "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (bf16-embedded int8 contractions, all GEMM launches)",
@@ -436,6 +449,7 @@ def main():
     ap.add_argument("--cpu-batch", type=int, default=128, help="samples in the CPU-oracle baseline step")
     ap.add_argument("--ref-batch", type=int, default=16, help="samples per reference-arm oracle step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true", help="launch every kernel directly (no CUDA graphs)")
     ap.add_argument("--op", choices=("fwd", "dgrad", "wgrad"), help="time one single-layer call instead")
     ap.add_argument("--shape", default="8192,4096,4096", help="B,IC,OC for --op")
     args = ap.parse_args()

@@ -256,6 +256,15 @@ int ito_model_num_stats(const ito_model *m);
  * synchronisation. */
 int ito_train_step(ito_model *m, const int8_t *x, const int32_t *labels, void *stream);
 
+/* Replays whole training steps as CUDA graphs (enable != 0) or launches
+ * every kernel directly (0, the default). With graphs on, a step called on a
+ * non-default stream runs directly the first time, is captured into a graph the
+ * next time for its (x, labels) pointer pair (up to 8 pairs are kept), and is
+ * replayed from then on; the legacy default stream (NULL) and steps run with
+ * ito_model_profile enabled always launch directly. Synchronises the device;
+ * frees all captured graphs. */
+int ito_model_use_graphs(ito_model *m, int enable);
+
 /* The same step from HOST buffers: copies x and labels into the model's
  * device buffers, runs the step, copies the stats array (ito_model_num_stats
  * int32) back to stats_host (may be NULL), and synchronises the stream.
@@ -369,12 +378,16 @@ typedef enum ito_prof_class {
 } ito_prof_class;
 
 /* Enables (1) or disables (0) per-kernel timing: when enabled, every kernel a
- * step launches is bracketed by CUDA events recorded on the step's stream. */
+ * step launches is bracketed by CUDA events recorded on the step's stream
+ * (inside the graph when steps replay from CUDA graphs). Synchronises the
+ * device and frees captured graphs. */
 int ito_model_profile(ito_model *m, int enable);
 
 /* Adds up the timings of all steps since the last read (waiting for their
  * events) and clears them: ms[c], work[c] and launches[c] for each of the
- * ITO_PROF_NCLASS classes (arrays of ITO_PROF_NCLASS entries). */
+ * ITO_PROF_NCLASS classes (arrays of ITO_PROF_NCLASS entries). Steps replayed
+ * from a graph reuse its events, so with graphs only the last replay is held:
+ * read after every step. */
 int ito_model_profile_read(ito_model *m, double *ms, double *work, int64_t *launches);
 
 /* Number of kernels the model launches per training step. */

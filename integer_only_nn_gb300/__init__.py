@@ -77,6 +77,7 @@ _SIGS = {
     "ito_dfp16_model_stat_index": (_I, [_P, ctypes.c_char_p]),
     "ito_dfp16_model_read_stats": (_I, [_P, _P, _I]),
     "ito_dfp16_train_step": (_I, [_P, _P, _I32, _P]),
+    "ito_model_use_graphs": (_I, [_P, _I]),
     "ito_model_profile": (_I, [_P, _I]),
     "ito_model_profile_read": (_I, [_P, _P, _P, _P]),
     "ito_model_kernels_per_step": (_I, [_P]),
@@ -325,6 +326,9 @@ class Model:
 
     def infer(self, x, logits, stream=None):
         _check(_lib.ito_infer(self._h, _ptr(x), _ptr(logits), _stream(stream)))
+
+    def use_graphs(self, enable=True):
+        _check(_lib.ito_model_use_graphs(self._h, int(enable)))
 
     def profile(self, enable=True):
         _check(_lib.ito_model_profile(self._h, int(enable)))

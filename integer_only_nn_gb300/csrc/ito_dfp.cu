@@ -393,6 +393,53 @@ __global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t 
     }
 }
 
+// four elements per thread step: 32 bytes of P in, 8 bytes of mantissas and
+// 8 + 8 bytes of limbs out; cols % 4 == 0 and rows * cols < 2^31
+__global__ void k_dfp_down_v4(const int64_t* __restrict__ P, int rows, int cols,
+                              const unsigned long long* __restrict__ d_max, const int32_t* __restrict__ d_ea,
+                              const int32_t* __restrict__ d_eb, int16_t* __restrict__ out16,
+                              uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int ldl,
+                              int32_t* __restrict__ d_exp_out, int32_t* __restrict__ d_rs, int* __restrict__ err)
+{
+    const unsigned long long m = *d_max;
+    const int bl = m ? 64 - __clzll((long long)m) : 0;
+    const int rs = bl > 15 ? bl - 15 : 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        const int e = *d_ea + (d_eb ? *d_eb : 0) + rs;
+        if (d_exp_out) *d_exp_out = e;
+        if (d_rs) *d_rs = rs;
+        if (e < -128 || e > 127) raise_device_error(err, ITO_ERR_EXPONENT);
+    }
+    const int groups = rows * (cols >> 2);
+    const int gpr = cols >> 2;
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += gridDim.x * blockDim.x) {
+        const int r = g / gpr, c = (g - r * gpr) << 2;
+        const int64_t i0 = (int64_t)r * cols + c;
+        const longlong2 p0 = __ldcs(reinterpret_cast<const longlong2*>(P + i0));
+        const longlong2 p1 = __ldcs(reinterpret_cast<const longlong2*>(P + i0 + 2));
+        const int64_t pv[4] = {p0.x, p0.y, p1.x, p1.y};
+        int16_t v[4];
+        uint16_t h[4], l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int32_t q = (int32_t)sat16s(rhu64(pv[k], rs));
+            int32_t hh, ll;
+            limb_split(q, hh, ll);
+            v[k] = (int16_t)q;
+            h[k] = int_to_bf16_bits(hh);
+            l[k] = int_to_bf16_bits(ll);
+        }
+        *reinterpret_cast<uint2*>(out16 + i0) = *reinterpret_cast<const uint2*>(v);
+        if (hi) {
+            const int64_t o = (int64_t)r * ldl + c;
+            *reinterpret_cast<uint2*>(hi + o) = *reinterpret_cast<const uint2*>(h);
+            *reinterpret_cast<uint2*>(lo + o) = *reinterpret_cast<const uint2*>(l);
+        }
+    }
+}
+
+static inline bool al(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
 int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned long long* d_max, const int32_t* d_ea,
                     const int32_t* d_eb, int16_t* out16, uint16_t* hi, uint16_t* lo, int64_t ldl, int32_t* d_exp_out,
                     int32_t* d_rs, cudaStream_t s)
@@ -400,8 +447,13 @@ int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned
     if (rows < 1 || cols < 1) return ITO_OK;
     int* err = device_error_word();
     if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
-    k_dfp_down<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(P, rows, cols, d_max, d_ea, d_eb, out16, hi, lo,
-                                                                     ldl, d_exp_out, d_rs, err);
+    if (cols % 4 == 0 && rows * cols < (1LL << 31) && ldl % 4 == 0 && al(P, 16) && al(out16, 8) &&
+        (!hi || (al(hi, 8) && al(lo, 8))))
+        k_dfp_down_v4<<<launch_grid_blocks(rows * cols / 4, 256), 256, 0, s>>>(
+            P, (int)rows, (int)cols, d_max, d_ea, d_eb, out16, hi, lo, (int)ldl, d_exp_out, d_rs, err);
+    else
+        k_dfp_down<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(P, rows, cols, d_max, d_ea, d_eb, out16, hi,
+                                                                         lo, ldl, d_exp_out, d_rs, err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp down launch: %s", cudaGetErrorString(e));
 }
@@ -439,13 +491,61 @@ __global__ void k_dfp_update(int16_t* __restrict__ W, uint16_t* __restrict__ hi,
     }
 }
 
+// four weights per thread step; cols % 4 == 0 and rows * cols < 2^31
+__global__ void k_dfp_update_v4(int16_t* __restrict__ W, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
+                                int ldl, const int16_t* __restrict__ G, int rows, int cols,
+                                const int32_t* __restrict__ d_exp_g, int32_t exp_w, int32_t eta,
+                                int32_t* __restrict__ d_k, uint32_t* __restrict__ d_nonzero)
+{
+    const int k = exp_w + eta - *d_exp_g;
+    if (d_k && blockIdx.x == 0 && threadIdx.x == 0) *d_k = k;
+    const int kl = -k > 17 ? 17 : -k;     // a left shift past 17 bits saturates every difference anyway
+    uint32_t cnt = 0;
+    const int gpr = cols >> 2;
+    const int groups = rows * gpr;
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += gridDim.x * blockDim.x) {
+        const int r = g / gpr, c = (g - r * gpr) << 2;
+        const int64_t i0 = (int64_t)r * cols + c;
+        int16_t w[4], gv[4];
+        *reinterpret_cast<uint2*>(w) = *reinterpret_cast<const uint2*>(W + i0);
+        *reinterpret_cast<uint2*>(gv) = __ldcs(reinterpret_cast<const uint2*>(G + i0));
+        uint16_t h[4], l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t dw = k >= 0 ? rhu64(gv[j], k) : (int64_t)gv[j] * ((int64_t)1 << kl);
+            cnt += dw != 0;
+            const int32_t nw = (int32_t)sat16s((int64_t)w[j] - dw);
+            int32_t hh, ll;
+            limb_split(nw, hh, ll);
+            w[j] = (int16_t)nw;
+            h[j] = int_to_bf16_bits(hh);
+            l[j] = int_to_bf16_bits(ll);
+        }
+        *reinterpret_cast<uint2*>(W + i0) = *reinterpret_cast<const uint2*>(w);
+        if (hi) {
+            const int64_t o = (int64_t)r * ldl + c;
+            *reinterpret_cast<uint2*>(hi + o) = *reinterpret_cast<const uint2*>(h);
+            *reinterpret_cast<uint2*>(lo + o) = *reinterpret_cast<const uint2*>(l);
+        }
+    }
+    if (d_nonzero) {
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(d_nonzero, cnt);
+    }
+}
+
 int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const int16_t* G, int64_t rows,
                       int64_t cols, const int32_t* d_exp_g, int32_t exp_w, int32_t eta, int32_t* d_k,
                       uint32_t* d_nonzero, cudaStream_t s)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
-    k_dfp_update<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(W, hi, lo, ldl, G, rows, cols, d_exp_g, exp_w,
-                                                                       eta, d_k, d_nonzero);
+    if (cols % 4 == 0 && rows * cols < (1LL << 31) && ldl % 4 == 0 && al(W, 8) && al(G, 8) &&
+        (!hi || (al(hi, 8) && al(lo, 8))))
+        k_dfp_update_v4<<<launch_grid_blocks(rows * cols / 4, 256), 256, 0, s>>>(
+            W, hi, lo, (int)ldl, G, (int)rows, (int)cols, d_exp_g, exp_w, eta, d_k, d_nonzero);
+    else
+        k_dfp_update<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(W, hi, lo, ldl, G, rows, cols, d_exp_g,
+                                                                           exp_w, eta, d_k, d_nonzero);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp update launch: %s", cudaGetErrorString(e));
 }

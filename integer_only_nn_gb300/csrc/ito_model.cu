@@ -85,6 +85,19 @@ struct ito_model {
     size_t split_ws_bytes = 0;
     std::vector<void*> allocs;
     std::vector<std::pair<std::string, int>> stat_names;
+    // CUDA-graph replay of whole steps, keyed by the caller's input pointers
+    struct GraphEntry {
+        const void* x;
+        const void* labels;
+        cudaGraphExec_t exec;
+        int launches;
+        std::vector<int> prof_cls;       // event pairs captured into the graph (profiling on)
+        std::vector<double> prof_work;
+    };
+    bool graph_on = false;
+    bool graph_warm = false;
+    bool capturing = false;      // a step is being captured into a graph
+    std::vector<GraphEntry> graphs;
     // measurement hooks
     bool prof_on = false;
     std::vector<cudaEvent_t> prof_ev;      // pairs (begin, end)
@@ -93,23 +106,34 @@ struct ito_model {
     int prof_n = 0;
     int launches = 0;                      // kernels launched by the current / last step
 
+    // during a capture the record must be "external" to become a graph node (the flag is
+    // rejected on a stream that is not capturing)
+    void record(cudaEvent_t e, cudaStream_t s)
+    {
+        if (capturing)
+            cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+        else
+            cudaEventRecord(e, s);
+    }
+    void grow_events(size_t n)
+    {
+        while (prof_ev.size() < n) {
+            cudaEvent_t e;
+            cudaEventCreate(&e);
+            prof_ev.push_back(e);
+        }
+    }
     void mark_begin(cudaStream_t s)
     {
         ++launches;
         if (!prof_on) return;
-        if ((size_t)(2 * prof_n + 2) > prof_ev.size()) {
-            for (int i = 0; i < 64; ++i) {
-                cudaEvent_t e;
-                cudaEventCreate(&e);
-                prof_ev.push_back(e);
-            }
-        }
-        cudaEventRecord(prof_ev[2 * prof_n], s);
+        if ((size_t)(2 * prof_n + 2) > prof_ev.size()) grow_events(prof_ev.size() + 128);
+        record(prof_ev[2 * prof_n], s);
     }
     void mark_end(cudaStream_t s, int cls, double work)
     {
         if (!prof_on) return;
-        cudaEventRecord(prof_ev[2 * prof_n + 1], s);
+        record(prof_ev[2 * prof_n + 1], s);
         prof_cls.push_back(cls);
         prof_work.push_back(work);
         ++prof_n;
@@ -437,10 +461,18 @@ int ito_model_create(const ito_layer_desc* layers, int n_layers, int batch, ito_
     return ITO_OK;
 }
 
+static void drop_graphs(ito_model* m)
+{
+    for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
+    m->graphs.clear();
+    m->graph_warm = false;
+}
+
 int ito_model_destroy(ito_model* m)
 {
     if (!m) return ITO_OK;
     cudaDeviceSynchronize();
+    drop_graphs(m);
     for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
     for (void* p : m->allocs) cudaFree(p);
     delete m;
@@ -530,7 +562,14 @@ int ito_model_num_stats(const ito_model* m) { return m ? m->n_stats : 0; }
 int ito_model_profile(ito_model* m, int enable)
 {
     if (!m) return set_error(ITO_ERR_ARG, "NULL model");
+    if (cudaDeviceSynchronize() != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+    // graphs captured with and without timing events differ
+    drop_graphs(m);
     m->prof_on = enable != 0;
+    m->prof_n = 0;
+    m->prof_cls.clear();
+    m->prof_work.clear();
+    if (m->prof_on) m->grow_events(256);
     return ITO_OK;
 }
 
@@ -559,15 +598,76 @@ int ito_model_profile_read(ito_model* m, double* ms, double* work, int64_t* laun
 
 int ito_model_kernels_per_step(const ito_model* m) { return m ? m->launches : 0; }
 
-int ito_train_step(ito_model* m, const int8_t* x, const int32_t* labels, void* stream)
+int ito_model_use_graphs(ito_model* m, int enable)
 {
-    if (!m || !x || !labels) return set_error(ITO_ERR_ARG, "NULL argument");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!m) return set_error(ITO_ERR_ARG, "NULL model");
+    if (cudaDeviceSynchronize() != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+    drop_graphs(m);
+    m->graph_on = enable != 0;
+    return ITO_OK;
+}
+
+static int step_direct(ito_model* m, const int8_t* x, const int32_t* labels, cudaStream_t s)
+{
     m->launches = 0;
     cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * m->n_stats, s);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
     ITO_TRY(model_forward(m, x, s));
     return model_backward(m, x, labels, s);
+}
+
+int ito_train_step(ito_model* m, const int8_t* x, const int32_t* labels, void* stream)
+{
+    if (!m || !x || !labels) return set_error(ITO_ERR_ARG, "NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // graphs need a capturable (non-default) stream
+    if (!m->graph_on || s == nullptr) return step_direct(m, x, labels, s);
+    for (auto& g : m->graphs)
+        if (g.x == x && g.labels == labels) {
+            m->launches = g.launches;
+            if (m->prof_on) {
+                // the replay re-records the graph's timing events: the last replay's timings are readable
+                m->prof_n = (int)g.prof_cls.size();
+                m->prof_cls = g.prof_cls;
+                m->prof_work = g.prof_work;
+            }
+            cudaError_t e = cudaGraphLaunch(g.exec, s);
+            return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "graph launch: %s", cudaGetErrorString(e));
+        }
+    if (!m->graph_warm) {
+        // one direct step first: kernel attributes and tensor maps are set up outside any capture
+        m->graph_warm = true;
+        return step_direct(m, x, labels, s);
+    }
+    if (m->graphs.size() >= 8) {
+        drop_graphs(m);
+        m->graph_warm = true;
+    }
+    // timing events of earlier direct steps are read before capture reuses the pool
+    if (m->prof_on && m->prof_n > 0 && cudaStreamSynchronize(s) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "sync before capture");
+    m->prof_n = 0;
+    m->prof_cls.clear();
+    m->prof_work.clear();
+    cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "begin capture: %s", cudaGetErrorString(e));
+    m->capturing = true;
+    const int r = step_direct(m, x, labels, s);
+    m->capturing = false;
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(s, &graph);
+    if (r != ITO_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return r;
+    }
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "end capture: %s", cudaGetErrorString(e));
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    m->graphs.push_back({x, labels, exec, m->launches, m->prof_cls, m->prof_work});
+    e = cudaGraphLaunch(exec, s);
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "graph launch: %s", cudaGetErrorString(e));
 }
 
 int ito_train_step_host(ito_model* m, const int8_t* x_host, const int32_t* labels_host, int32_t* stats_host,

@@ -58,3 +58,29 @@ def test_model_100_steps_digests(index):
                 bad.append(k)
         assert not bad, "step %d differs from the oracle in %s" % (t, bad)
     assert len(ref) == 100
+
+
+@pytest.mark.parametrize("index,steps", [(0, 100), (2, 3)])
+def test_model_graph_replay_lockstep(index, steps):
+    """Steps replayed from captured CUDA graphs (side stream, two fixed input
+    buffers) match the oracle step by step."""
+    import torch
+    w = si.by_name(index)
+    g = GpuRun(w)
+    g.model.use_graphs(True)
+    stream = torch.cuda.Stream()
+    bufs = [(torch.empty(si.input_shape(w), dtype=torch.int8, device="cuda"),
+             torch.empty(w.batch, dtype=torch.int32, device="cuda")) for _ in range(2)]
+    weights = si.make_weights(w)
+    for t in range(steps):
+        x, labels = si.make_batch(w, t)
+        xb, lb = bufs[t % 2]
+        with torch.cuda.stream(stream):
+            xb.copy_(torch.from_numpy(x))
+            lb.copy_(torch.from_numpy(labels))
+            g.model.train_step(xb, lb, stream=stream)
+        stream.synchronize()
+        rec = _oracle_step(w, weights, t, "loops")
+        compare_records(rec, g.record(), t)
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+    assert g.ito.ito_get_error() == 0
