@@ -95,6 +95,22 @@ def algorithmic_ops(w):
     return 2.0 * (2 * (fwd + fc) + dgrad + fc)
 
 
+def max_over_ranks(value, dist, device="cuda"):
+    """The largest `value` over all ranks (the slowest rank's time); the value
+    itself when running alone."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(samples_per_rank, world, slowest_seconds):
+    """Whole-job samples/s: every rank's samples over the slowest rank's time."""
+    return samples_per_rank * world / slowest_seconds
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -293,10 +309,7 @@ def run_ours(args, w):
     err = ito.ito_get_error()
     if err != 0:
         raise RuntimeError("device error word %d after the timed steps" % err)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist)
     launches = model.kernels_per_step()
 
     # end to end through the host-buffer entry point
@@ -310,10 +323,7 @@ def run_ours(args, w):
     for _ in range(K):
         model.train_step_host(x_h, l_h, st_h, stream=stream)
     e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dist)
 
     if rank != 0:
         if dist is not None:
@@ -321,7 +331,7 @@ def run_ours(args, w):
         return 0
     pk, pk_src = peaks()
     samples = world * w.batch * K
-    value = samples / (total_ms / 1000.0)
+    value = job_throughput(w.batch * K, world, total_ms / 1000.0)
     g_ms, g_work, g_n = prof["gemm"]
     prof = {c: tuple(v) for c, v in prof.items()}
     g_tflops = g_work / (g_ms / 1000.0) / 1e12
