@@ -219,6 +219,30 @@ typedef struct ito_model ito_model;
 int ito_model_create(const ito_layer_desc *layers, int n_layers, int batch, ito_niti_params p,
                      int32_t target_mag, ito_model **out);
 
+/* Options of ito_model_create_ex ("Integer On-Device Training: Overview",
+ * section 5 "Full Model vs Partial Model" and section 8 "Memory
+ * Considerations"):
+ *  - input_uint8: the first layer (a Linear) receives UINT8 activations in
+ *    [0, 255], as from a frozen prefix whose last layer has a ReLU;
+ *  - trainable_from: layers before this index are frozen (forward only: no
+ *    weight gradient, no update, and no delta is propagated into them) --
+ *    trainable_layers_from_last = n_layers - trainable_from;
+ *  - packed_masks: the ReLU masks of the backward pass are kept bit-packed,
+ *    ceil(out_size / 8) bytes per sample and ReLU layer (each such layer's
+ *    output width must be a multiple of 8). */
+typedef struct ito_model_options {
+    int32_t input_uint8;
+    int32_t trainable_from;
+    int32_t packed_masks;
+} ito_model_options;
+
+/* ito_model_create with options (NULL = all zero, the same as
+ * ito_model_create). Errors: as ito_model_create; ITO_ERR_UNSUPPORTED for a
+ * UINT8 input to a conv layer or packed masks on a width not a multiple of 8;
+ * ITO_ERR_ARG for trainable_from outside [0, number of weight layers). */
+int ito_model_create_ex(const ito_layer_desc *layers, int n_layers, int batch, ito_niti_params p,
+                        int32_t target_mag, const ito_model_options *opt, ito_model **out);
+
 /* Frees the model's device memory. Synchronises the device. NULL is a no-op. */
 int ito_model_destroy(ito_model *m);
 
@@ -231,6 +255,7 @@ int ito_model_get_weights(const ito_model *m, int layer, int8_t *W, int on_host,
 
 /* Looks up a named device tensor of the last step (names as in the CPU
  * oracle: "y0" int32 forward contraction of layer 0, "a0" its int8 output,
+ * "m0" its bit-packed ReLU mask (packed_masks models),
  * "e0" int8 delta at the output of layer 0, "d1" int32 delta-propagation
  * contraction of layer 1, "g0" int32 weight gradient, "w0" int8 weights,
  * "stats" int32 scalars; see ito_model_stat_index). Writes the device

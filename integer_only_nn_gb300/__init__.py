@@ -35,6 +35,11 @@ class NitiParams(ctypes.Structure):
     _fields_ = [("target_bits", ctypes.c_int32), ("mu_weight", ctypes.c_int32)]
 
 
+class ModelOptions(ctypes.Structure):
+    _fields_ = [("input_uint8", ctypes.c_int32), ("trainable_from", ctypes.c_int32),
+                ("packed_masks", ctypes.c_int32)]
+
+
 class LayerDesc(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("in_features", ctypes.c_int32), ("out_features", ctypes.c_int32),
                 ("in_h", ctypes.c_int32), ("in_w", ctypes.c_int32), ("stride", ctypes.c_int32)]
@@ -52,6 +57,8 @@ _SIGS = {
     "ito_niti_update": (_I, [_P, _P, _I64, _P, NitiParams, _P, _P, _P, _P]),
     "ito_top_error": (_I, [_P, _P, _I, _I, _I32, _P, _P]),
     "ito_model_create": (_I, [ctypes.POINTER(LayerDesc), _I, _I, NitiParams, _I32, ctypes.POINTER(_P)]),
+    "ito_model_create_ex": (_I, [ctypes.POINTER(LayerDesc), _I, _I, NitiParams, _I32, ctypes.POINTER(ModelOptions),
+                                 ctypes.POINTER(_P)]),
     "ito_model_destroy": (_I, [_P]),
     "ito_model_set_weights": (_I, [_P, _I, _P, _I, _P]),
     "ito_model_get_weights": (_I, [_P, _I, _P, _I, _P]),
@@ -254,11 +261,13 @@ def layers_for(workload):
 class Model:
     """An ito_model: a sequential int8 layer stack that trains with NITI."""
 
-    def __init__(self, layers, batch, target_bits=7, mu_weight=2, target_mag=64):
+    def __init__(self, layers, batch, target_bits=7, mu_weight=2, target_mag=64, input_uint8=False,
+                 trainable_from=0, packed_masks=False):
         arr = (LayerDesc * len(layers))(*layers)
         h = ctypes.c_void_p()
-        _check(_lib.ito_model_create(arr, len(layers), batch, NitiParams(target_bits, mu_weight), target_mag,
-                                     ctypes.byref(h)))
+        opt = ModelOptions(int(input_uint8), int(trainable_from), int(packed_masks))
+        _check(_lib.ito_model_create_ex(arr, len(layers), batch, NitiParams(target_bits, mu_weight), target_mag,
+                                        ctypes.byref(opt), ctypes.byref(h)))
         self._h = h
         self.batch = batch
         self.n_weight_layers = sum(1 for l in layers if l.kind != ITO_LAYER_GAP)

@@ -78,6 +78,47 @@ int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* d
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "convert launch: %s", cudaGetErrorString(e));
 }
 
+// uint8 input (a partial model's input from a frozen prefix): values 0..255, exact in bf16
+__global__ void k_u8_to_bf16_v8(const uint8_t* __restrict__ src, int64_t rows, int64_t cols,
+                                uint16_t* __restrict__ dst, int64_t ldd)
+{
+    const int64_t groups = rows * (cols >> 3);
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i0 = g << 3;
+        const int64_t r = i0 / cols, c = i0 - r * cols;
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(src + i0));
+        const uint8_t* b = reinterpret_cast<const uint8_t*>(&v);
+        uint4 o;
+        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            ow[i] = (uint32_t)int_to_bf16_bits(b[2 * i]) | ((uint32_t)int_to_bf16_bits(b[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4*>(dst + r * ldd + c) = o;
+    }
+}
+
+__global__ void k_u8_to_bf16_1(const uint8_t* __restrict__ src, int64_t rows, int64_t cols, uint16_t* __restrict__ dst,
+                               int64_t ldd)
+{
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i - r * cols;
+        dst[r * ldd + c] = int_to_bf16_bits(src[i]);
+    }
+}
+
+int launch_u8_to_bf16(const uint8_t* src, int64_t rows, int64_t cols, uint16_t* dst, int64_t ldd, cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    if (cols % 8 == 0 && ldd % 8 == 0 && aligned(src, 8) && aligned(dst, 16))
+        k_u8_to_bf16_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(src, rows, cols, dst, ldd);
+    else
+        k_u8_to_bf16_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(src, rows, cols, dst, ldd);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "convert launch: %s", cudaGetErrorString(e));
+}
+
 // --------------------------------------------------------------- requant
 
 // q = sat8(rhu(y, s)); ReLU; gate
@@ -88,10 +129,14 @@ __device__ __forceinline__ int32_t requant_one(int32_t y, int s, int relu, int g
     return gate_ok ? q : 0;
 }
 
+// The optional bit-packed ReLU masks hold one byte per eight elements of a
+// row (cols / 8 bytes per row; bit j is element j of the group): mask_out
+// receives (q > 0) of the result, gate_bits replaces the int8 gate.
 __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
                              const uint32_t* __restrict__ d_max, int target_bits, int relu,
                              const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
-                             int64_t ldb, int32_t* __restrict__ d_shift)
+                             int64_t ldb, int32_t* __restrict__ d_shift, const uint8_t* __restrict__ gate_bits,
+                             uint8_t* __restrict__ mask_out)
 {
     const int s = shift_for(*d_max, target_bits);
     if (d_shift && blockIdx.x == 0 && threadIdx.x == 0) *d_shift = s;
@@ -104,10 +149,20 @@ __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_
         const int32_t y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
         int8_t gv[8] = {1, 1, 1, 1, 1, 1, 1, 1};
         if (gate) *reinterpret_cast<uint2*>(gv) = __ldg(reinterpret_cast<const uint2*>(gate + i0));
+        if (gate_bits) {
+            const uint32_t bits = __ldg(gate_bits + g);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) gv[i] = (bits >> i) & 1;
+        }
         int8_t q8[8];
         uint32_t qb[4];
+        uint32_t mbits = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q8[i] = (int8_t)requant_one(y[i], s, relu, gv[i] > 0);
+        for (int i = 0; i < 8; ++i) {
+            q8[i] = (int8_t)requant_one(y[i], s, relu, gv[i] > 0);
+            mbits |= (q8[i] > 0 ? 1u : 0u) << i;
+        }
+        if (mask_out) mask_out[g] = (uint8_t)mbits;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             qb[i] = (uint32_t)int_to_bf16_bits(q8[2 * i]) | ((uint32_t)int_to_bf16_bits(q8[2 * i + 1]) << 16);
@@ -138,14 +193,17 @@ __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t
 }
 
 int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
-                   const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s)
+                   const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
+                   const uint8_t* gate_bits, uint8_t* mask_out)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
     const bool vec = cols % 8 == 0 && aligned(Y, 16) && aligned(out8, 8) && (!gate || aligned(gate, 8)) &&
                      (!outb || (aligned(outb, 16) && ldb % 8 == 0));
+    if ((gate_bits || mask_out) && !vec)
+        return set_error(ITO_ERR_UNSUPPORTED, "bit-packed masks need rows of a multiple of 8 elements");
     if (vec)
-        k_requant_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(Y, rows, cols, d_max, target_bits,
-                                                                               relu, gate, out8, outb, ldb, d_shift);
+        k_requant_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(
+            Y, rows, cols, d_max, target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out);
     else
         k_requant_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(Y, rows, cols, d_max, target_bits, relu,
                                                                           gate, out8, outb, ldb, d_shift);

@@ -749,8 +749,10 @@ size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc)
 }
 
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
-              int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws, size_t split_ws_bytes)
+              int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws, size_t split_ws_bytes, int chunk_terms)
 {
+    if (chunk_terms < 64 || chunk_terms > kExactChunk || chunk_terms % 64)
+        return set_error(ITO_ERR_ARG, "gemm: exact chunk must be a multiple of 64 up to %d", kExactChunk);
     if (M < 1 || N < 1 || K < 1) return set_error(ITO_ERR_SHAPE, "gemm: empty contraction");
     if (K > (1 << 20)) return set_error(ITO_ERR_SHAPE, "gemm: contraction longer than 2^20");
     // operand extents must match the problem
@@ -767,7 +769,7 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
     p->C = C;
     p->ldc = ldc;
     p->d_max = d_max;
-    p->chunk_kb = kExactChunk / 64;
+    p->chunk_kb = chunk_terms / 64;
     p->err = device_error_word();
     if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     p->bn = N > 128 ? 256 : (N > 64 ? 128 : 64);

@@ -17,6 +17,8 @@ int set_error(int code, const char* fmt, ...);
 // two int8 values are at most 2^14 in magnitude, so 1024 of them sum to at
 // most 2^24, the largest range in which fp32 holds every integer.
 constexpr int kExactChunk = 1024;
+// uint8 x int8 products reach 255 * 128 < 2^15: 512 terms stay within 2^24.
+constexpr int kExactChunkU8 = 512;
 
 inline int64_t pad8(int64_t n) { return (n + 7) & ~int64_t(7); }
 
@@ -91,8 +93,10 @@ int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const
 
 // split_ws (optional): room for split-K partials; without it (or when too
 // small) the contraction is not split.
+// chunk_terms: K terms per exact fp32 chunk (a multiple of 64, at most kExactChunk).
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
-              int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws = nullptr, size_t split_ws_bytes = 0);
+              int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws = nullptr, size_t split_ws_bytes = 0,
+              int chunk_terms = kExactChunk);
 // bytes of split-K partials gemm_plan would use for this contraction (0: no split)
 size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc);
 int gemm_run(const GemmPlan& p, cudaStream_t s);
@@ -109,8 +113,12 @@ int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* d
 // out8 = sat8(rhu(Y, s)) (ReLU'd if relu), plus the bf16 copy outb (pitch
 // ldb, may be null) and *d_shift = s (may be null). If gate is non-null the
 // result is zeroed where gate <= 0 (delta propagation through a ReLU).
+// gate_bits / mask_out (optional, cols % 8 == 0): bit-packed ReLU masks, one
+// byte per 8 elements: read in place of the int8 gate / written from the result.
 int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
-                   const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s);
+                   const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
+                   const uint8_t* gate_bits = nullptr, uint8_t* mask_out = nullptr);
+int launch_u8_to_bf16(const uint8_t* src, int64_t rows, int64_t cols, uint16_t* dst, int64_t ldd, cudaStream_t s);
 
 // NITI Steps 2-5 in place on W [rows][cols] (int8) with gradient G (int32),
 // refreshing the bf16 copy Wb (pitch ldb, may be null).

@@ -52,6 +52,7 @@ struct MLayer {
     int32_t* dcol = nullptr;    // conv: [rows_out][K]
     int32_t* d32 = nullptr;     // [rows_in][IC]
     int32_t* g32 = nullptr;     // [OC][K]
+    uint8_t* mask = nullptr;    // bit-packed ReLU mask of the output [rows][OC / 8] (packed_masks)
     GemmPlan pf{}, pd{}, pg{};
     bool has_dgrad = false;
     bool relu = false;
@@ -62,6 +63,7 @@ struct MLayer {
 struct ito_model {
     int batch = 0;
     ito_niti_params p{};
+    ito_model_options opt{};
     int32_t target_mag = 64;
     int n_conv = 0;
     bool has_pool = false;
@@ -215,7 +217,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         L.rows_in = (int64_t)B * H * W;
         L.rows_out = (int64_t)B * L.OH * L.OW;
         L.relu = true;
-        L.has_dgrad = l > 0;
+        L.has_dgrad = l > m->opt.trainable_from;
         m->L.push_back(L);
         H = L.OH;
         W = L.OW;
@@ -244,11 +246,19 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         L.K = F;
         L.rows_in = L.rows_out = B;
         L.relu = q.kind == ITO_LAYER_LINEAR_RELU;
-        L.has_dgrad = !m->L.empty();
+        L.has_dgrad = (int)m->L.size() > m->opt.trainable_from;
         m->L.push_back(L);
         F = q.out_features;
     }
     const int nl = (int)m->L.size();
+    if (m->opt.trainable_from < 0 || m->opt.trainable_from >= nl)
+        return set_error(ITO_ERR_ARG, "trainable_from must be in [0, %d)", nl);
+    if (m->opt.input_uint8 && m->n_conv > 0)
+        return set_error(ITO_ERR_UNSUPPORTED, "UINT8 input is supported for a Linear first layer");
+    if (m->opt.packed_masks)
+        for (int l = 0; l < nl; ++l)
+            if (m->L[l].relu && m->L[l].OC % 8)
+                return set_error(ITO_ERR_UNSUPPORTED, "packed masks need ReLU widths that are multiples of 8");
 
     // allocations
     ITO_TRY(m->alloc(&m->x8, (size_t)B * m->in_features));
@@ -281,6 +291,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         ITO_TRY(m->alloc(&L.e8, (size_t)L.rows_out * L.OC));
         ITO_TRY(m->alloc(&L.eb, (size_t)L.rows_out * L.lde));
         ITO_TRY(m->alloc(&L.g32, (size_t)L.OC * L.K));
+        if (m->opt.packed_masks && L.relu) ITO_TRY(m->alloc(&L.mask, (size_t)L.rows_out * (L.OC / 8)));
         if (L.has_dgrad) ITO_TRY(m->alloc(&L.d32, (size_t)L.rows_in * L.IC));
         if (conv) {
             L.ldp = pad8(L.K);
@@ -320,9 +331,11 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
             in = Bf16View{m->L[l - 1].ab, B, L.IC, m->L[l - 1].lda};
         }
         const int M = (int)L.rows_out;
+        // a UINT8 input makes products up to 255 * 128: shorter exact chunks
+        const int chunk = (l == 0 && m->opt.input_uint8) ? kExactChunkU8 : kExactChunk;
         // forward: Y[m][oc] = sum_k in[m][k] W[oc][k]
         ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax, m->split_ws,
-                          m->split_ws_bytes));
+                          m->split_ws_bytes, chunk));
         // delta propagation: D[m][k] = sum_oc e[m][oc] W[oc][k]; for a conv this is the
         // patch-space delta, whose max is not the NITI max (col2im takes that)
         if (L.has_dgrad)
@@ -330,7 +343,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
                               conv ? m->discard_max : dmax, m->split_ws, m->split_ws_bytes));
         // weight gradient: G[oc][k] = sum_m e[m][oc] in[m][k]
         ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax, m->split_ws,
-                          m->split_ws_bytes));
+                          m->split_ws_bytes, chunk));
     }
 
     // names of the stats entries
@@ -365,7 +378,10 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
     const int B = m->batch;
     const int nl = (int)m->L.size();
     const ito_niti_params p = m->p;
-    if (m->n_conv == 0)
+    if (m->n_conv == 0 && m->opt.input_uint8)
+        ITO_LAUNCH(m, s, ITO_PROF_OTHER, 3.0 * B * m->in_features,
+                   launch_u8_to_bf16(reinterpret_cast<const uint8_t*>(x), B, m->in_features, m->xb, m->ldx, s));
+    else if (m->n_conv == 0)
         ITO_LAUNCH(m, s, ITO_PROF_OTHER, 3.0 * B * m->in_features,
                    launch_i8_to_bf16(x, B, m->in_features, m->xb, m->ldx, s));
     const int8_t* in8 = x;
@@ -386,7 +402,7 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
         ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
         ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
                    launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits, L.relu ? 1 : 0,
-                                  nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s));
+                                  nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr, L.mask));
         in8 = L.a8;
     }
     return ITO_OK;
@@ -400,7 +416,7 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
     MLayer& top = m->L[nl - 1];
     ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * top.OC + 4.0 * B,
                launch_top_error(top.a8, labels, B, top.OC, m->target_mag, top.e8, top.eb, top.lde, s));
-    for (int l = nl - 1; l >= 0; --l) {
+    for (int l = nl - 1; l >= m->opt.trainable_from; --l) {
         MLayer& L = m->L[l];
         const bool conv = L.kind == ITO_LAYER_CONV3X3_RELU;
         if (L.has_dgrad) {
@@ -411,8 +427,9 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
                            launch_col2im(L.dcol, B, L.H, L.W, L.IC, L.OH, L.OW, L.stride, L.d32,
                                          m->umax(l, ST_DMAX), s));
                 ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_in * L.IC, true, true),
-                           launch_requant(L.d32, L.rows_in, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0, prev.a8,
-                                          prev.e8, prev.eb, prev.lde, m->sval(l, ST_DS), s));
+                           launch_requant(L.d32, L.rows_in, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
+                                          prev.mask ? nullptr : prev.a8, prev.e8, prev.eb, prev.lde,
+                                          m->sval(l, ST_DS), s, prev.mask, nullptr));
             } else if (l == m->n_conv && m->has_pool) {
                 // pooled delta (the pooled activation has no ReLU), then the pooling backward
                 ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, false, false),
@@ -423,8 +440,8 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
             } else {
                 ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, true, prev.relu),
                            launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
-                                          prev.relu ? prev.a8 : nullptr, prev.e8, prev.eb, prev.lde,
-                                          m->sval(l, ST_DS), s));
+                                          (prev.relu && !prev.mask) ? prev.a8 : nullptr, prev.e8, prev.eb, prev.lde,
+                                          m->sval(l, ST_DS), s, prev.mask, nullptr));
             }
         }
         ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
@@ -443,6 +460,12 @@ extern "C" {
 int ito_model_create(const ito_layer_desc* layers, int n_layers, int batch, ito_niti_params p, int32_t target_mag,
                      ito_model** out)
 {
+    return ito_model_create_ex(layers, n_layers, batch, p, target_mag, nullptr, out);
+}
+
+int ito_model_create_ex(const ito_layer_desc* layers, int n_layers, int batch, ito_niti_params p,
+                        int32_t target_mag, const ito_model_options* opt, ito_model** out)
+{
     if (!layers || !out || n_layers < 1) return set_error(ITO_ERR_ARG, "NULL layers/out or no layers");
     if (batch < 1 || batch > (1 << 20)) return set_error(ITO_ERR_SHAPE, "batch");
     if (p.target_bits < 1 || p.target_bits > 8 || p.mu_weight < 0 || p.mu_weight > 31)
@@ -452,6 +475,7 @@ int ito_model_create(const ito_layer_desc* layers, int n_layers, int batch, ito_
     m->batch = batch;
     m->p = p;
     m->target_mag = target_mag;
+    if (opt) m->opt = *opt;
     int r = build_model(m, layers, n_layers);
     if (r != ITO_OK) {
         ito_model_destroy(m);
@@ -542,6 +566,7 @@ int ito_model_tensor(const ito_model* m, const char* name, void** dev_ptr, int* 
             case 'd': return put(L.d32, 4, L.rows_in * L.IC);
             case 'g': return put(L.g32, 4, (int64_t)L.OC * L.K);
             case 'w': return put(L.W8, 1, (int64_t)L.OC * L.K);
+            case 'm': return put(L.mask, 1, L.rows_out * (L.OC / 8));
             default: break;
             }
         }

@@ -73,6 +73,9 @@ def lib():
             "ora_linear_fwd": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
             "ora_linear_dgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
             "ora_linear_wgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_linear_fwd_u8": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_linear_wgrad_u8": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
+            "ora_pack_relu_mask": (None, [P, ctypes.c_int, ctypes.c_int, P]),
             "ora_conv2d_fwd": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
             "ora_conv2d_dgrad": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
             "ora_conv2d_wgrad": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
@@ -202,6 +205,34 @@ def linear_wgrad(delta, A):
     G = np.empty((OC, IC), np.int32)
     lib().ora_linear_wgrad(_p(delta), _p(A), B, IC, OC, _p(G))
     return G
+
+
+def linear_fwd_u8(X, W):
+    X, W = _c(X, np.uint8), _c(W, np.int8)
+    B, IC = X.shape
+    OC = W.shape[0]
+    assert W.shape == (OC, IC)
+    Y = np.empty((B, OC), np.int32)
+    lib().ora_linear_fwd_u8(_p(X), _p(W), B, IC, OC, _p(Y))
+    return Y
+
+
+def linear_wgrad_u8(delta, A):
+    delta, A = _c(delta, np.int8), _c(A, np.uint8)
+    B, OC = delta.shape
+    IC = A.shape[1]
+    assert A.shape[0] == B
+    G = np.empty((OC, IC), np.int32)
+    lib().ora_linear_wgrad_u8(_p(delta), _p(A), B, IC, OC, _p(G))
+    return G
+
+
+def pack_relu_mask(A):
+    A = _c(A, np.int8)
+    B, F = A.shape
+    out = np.empty((B, (F + 7) // 8), np.uint8)
+    lib().ora_pack_relu_mask(_p(A), B, F, _p(out))
+    return out
 
 
 # Exact float64 route for large contractions. Every product of two integers
@@ -364,7 +395,7 @@ def _linear_ops(route):
 
 
 def mlp_step(weights, x, labels, target_bits=TARGET_BITS, mu_weight=MU_WEIGHT,
-             target_mag=TARGET_MAG, route="loops"):
+             target_mag=TARGET_MAG, route="loops", trainable_from=0):
     """One NITI step of a sequential int8 MLP: Linear+ReLU layers and a final
     Linear producing int8 logits. `weights` is a list of int8 [OC, IC]; the
     updated weights are returned in the record (inputs are not modified).
@@ -374,29 +405,44 @@ def mlp_step(weights, x, labels, target_bits=TARGET_BITS, mu_weight=MU_WEIGHT,
     output of layer l (e{L-1} is the top error); d{l} int32 delta-propagation
     contraction of layer l (l >= 1) with dmax{l}/ds{l}; g{l} int32 weight
     gradient with gmax{l}/gs{l}/ws{l}; w{l} updated weights; nz{l} nonzero
-    weight steps. route: "loops" (C loops) or "f64" (exact float64 BLAS)."""
+    weight steps. route: "loops" (C loops) or "f64" (exact float64 BLAS).
+
+    Partial-model training ("Integer On-Device Training: Overview", section 5,
+    trainable_layers_from_last): layers before `trainable_from` are frozen and
+    run forward only; backward stops at layer trainable_from (no delta is
+    propagated into the frozen part). A uint8 `x` is the UINT8 input the
+    library receives from a frozen prefix ending in ReLU (values 0..255)."""
     fwd, dgrad, wgrad = _linear_ops(route)
     L = len(weights)
     r = {}
-    act = [np.ascontiguousarray(x, np.int8)]
+    u8_input = np.asarray(x).dtype == np.uint8
+    act = [np.ascontiguousarray(x, np.uint8 if u8_input else np.int8)]
     for l in range(L):
-        y = fwd(act[-1], weights[l])
+        if l == 0 and u8_input:
+            y = linear_fwd_u8(act[-1], weights[l]) if route == "loops" else linear_fwd_f64(act[-1], weights[l])
+        else:
+            y = fwd(act[-1], weights[l])
         a, s, m = requant(y, relu=(l < L - 1), target_bits=target_bits)
         r["y%d" % l], r["ymax%d" % l], r["ys%d" % l], r["a%d" % l] = y, m, s, a
         act.append(a)
     e = top_error(act[-1], labels, target_mag)
     r["e%d" % (L - 1)] = e
-    for l in range(L - 1, -1, -1):
-        if l > 0:
+    for l in range(L - 1, trainable_from - 1, -1):
+        if l > trainable_from:
             d = dgrad(e, weights[l])
             e_prev, s, m = requant_mask(d, act[l], target_bits)
             r["d%d" % l], r["dmax%d" % l], r["ds%d" % l], r["e%d" % (l - 1)] = d, m, s, e_prev
-        g = wgrad(e, act[l])
+        if l == 0 and u8_input:
+            g = linear_wgrad_u8(e, act[0]) if route == "loops" else linear_wgrad_f64(e, act[0])
+        else:
+            g = wgrad(e, act[l])
         wn, s, ws, m, nz = niti_update(weights[l], g, target_bits, mu_weight)
         r["g%d" % l], r["gmax%d" % l], r["gs%d" % l], r["ws%d" % l] = g, m, s, ws
         r["w%d" % l], r["nz%d" % l] = wn, nz
-        if l > 0:
+        if l > trainable_from:
             e = e_prev
+    for l in range(trainable_from):
+        r["w%d" % l] = np.array(weights[l], copy=True)      # frozen
     return r
 
 
@@ -511,7 +557,7 @@ def run_steps(workload, steps: int, start_weights=None, callback=None, route="lo
     for t in range(steps):
         x, labels = si.make_batch(w, t)
         if w.kind == "mlp":
-            rec = mlp_step(weights, x, labels, route=route)
+            rec = mlp_step(weights, x, labels, route=route, trainable_from=w.trainable_from)
         elif w.kind == "cnn":
             rec = cnn_step(weights, x, labels, w.convs)
         elif w.kind == "dfp16":

@@ -293,6 +293,63 @@ void ora_linear_wgrad(const int8_t *delta, const int8_t *A, int B, int IC, int O
     }
 }
 
+/* UINT8-input variants for the first trainable layer of a partial model
+ * ([ODT] section 4: the frozen part ends in a ReLU layer, so the library
+ * receives UINT8 activations in [0, 255]). */
+void ora_linear_fwd_u8(const uint8_t *X, const int8_t *W, int B, int IC, int OC, int32_t *Y)
+{
+#pragma omp parallel for schedule(static)
+    for (int b = 0; b < B; b++) {
+        const uint8_t *x = X + (int64_t)b * IC;
+        for (int oc = 0; oc < OC; oc++) {
+            const int8_t *w = W + (int64_t)oc * IC;
+            int64_t acc = 0;
+            for (int ic = 0; ic < IC; ic++)
+                acc += (int64_t)x[ic] * (int64_t)w[ic];
+            Y[(int64_t)b * OC + oc] = checked_i32(acc);
+        }
+    }
+}
+
+void ora_linear_wgrad_u8(const int8_t *delta, const uint8_t *A, int B, int IC, int OC, int32_t *G)
+{
+#pragma omp parallel
+    {
+        int64_t *acc = (int64_t *)malloc(sizeof(int64_t) * (size_t)(IC > 0 ? IC : 1));
+        if (!acc) ora_fail("out of memory");
+#pragma omp for schedule(static)
+        for (int oc = 0; oc < OC; oc++) {
+            for (int ic = 0; ic < IC; ic++) acc[ic] = 0;
+            for (int b = 0; b < B; b++) {
+                int64_t d = delta[(int64_t)b * OC + oc];
+                const uint8_t *a = A + (int64_t)b * IC;
+                for (int ic = 0; ic < IC; ic++)
+                    acc[ic] += d * (int64_t)a[ic];
+            }
+            for (int ic = 0; ic < IC; ic++)
+                G[(int64_t)oc * IC + ic] = checked_i32(acc[ic]);
+        }
+        free(acc);
+    }
+}
+
+/* ReLU mask bits ([ODT] section 8, "ReLU Mask Buffers": BATCH_SIZE *
+ * ceil(out_size / 8) bytes per ReLU layer): bit j % 8 of byte j / 8 of row b
+ * is 1 where A[b][j] > 0. */
+void ora_pack_relu_mask(const int8_t *A, int B, int F, uint8_t *mask)
+{
+    int64_t bytes = (F + 7) / 8;
+    for (int b = 0; b < B; b++)
+        for (int64_t k = 0; k < bytes; k++) {
+            unsigned v = 0;
+            for (int j = 0; j < 8; j++) {
+                int64_t f = k * 8 + j;
+                if (f < F && A[(int64_t)b * F + f] > 0) v |= 1u << j;
+            }
+            mask[(int64_t)b * bytes + k] = (uint8_t)v;
+        }
+}
+
 /* ------------------------------------------------------ int8 conv (NHWC) */
 
 static int conv_out(int in, int k, int stride, int pad)

@@ -112,6 +112,8 @@ class Workload:
     lim: int = 127            # clamp for weights and inputs
     exp_x: int = 0            # dfp16 shared exponents of input and weights
     exp_w: int = 0
+    input_uint8: bool = False # mlp: UINT8 input in [0, 255] (partial-model training)
+    trainable_from: int = 0   # mlp: layers before this one are frozen
 
     @property
     def seed(self) -> int:
@@ -127,6 +129,9 @@ WORKLOADS = (
              classes=1000),
     Workload(4, "dfp16_2048x3_b2048", "dfp16", 2048, dims=(2048, 2048, 2048, 2048),
              sigma=4096.0, lim=32767, exp_x=-12, exp_w=-17),
+    # partial-model training: UINT8 input, the last two of four layers trainable
+    Workload(5, "mlp784-1024x3-10_b256_u8_last2", "mlp", 256, dims=(784, 1024, 1024, 1024, 10),
+             classes=10, input_uint8=True, trainable_from=2),
 )
 
 
@@ -165,15 +170,18 @@ def input_shape(w: Workload) -> tuple:
 
 
 def make_batch(w: Workload, step: int):
-    """(x, labels) for one step. mlp/cnn: int8 x uniform in [-127, 127], int32
-    labels uniform in [0, classes). dfp16: int16 x = round(N(0, sigma)) clamped,
-    labels None."""
+    """(x, labels) for one step. mlp/cnn: int8 x uniform in [-127, 127] (uint8
+    in [0, 255] for a UINT8-input workload), int32 labels uniform in
+    [0, classes). dfp16: int16 x = round(N(0, sigma)) clamped, labels None."""
     shp = input_shape(w)
     n = int(np.prod(shp))
     if w.kind == "dfp16":
         x = round_clamp_normal(w.seed, batch_stream(step, 0), n, w.sigma, w.lim)
         return x.astype(np.int16).reshape(shp), None
-    x = uniform_int(w.seed, batch_stream(step, 0), n, -127, 127).astype(np.int8).reshape(shp)
+    if w.input_uint8:
+        x = uniform_int(w.seed, batch_stream(step, 0), n, 0, 255).astype(np.uint8).reshape(shp)
+    else:
+        x = uniform_int(w.seed, batch_stream(step, 0), n, -127, 127).astype(np.int8).reshape(shp)
     labels = uniform_int(w.seed, batch_stream(step, 1), w.batch, 0, w.classes - 1).astype(np.int32)
     return x, labels
 

@@ -36,13 +36,14 @@ def import_ito():
 class GpuRun:
     """A CUDA model of a seeded mlp/cnn workload, stepped one batch at a time."""
 
-    def __init__(self, workload, batch=None):
+    def __init__(self, workload, batch=None, packed_masks=False):
         import torch
         self.torch = torch
         self.ito = import_ito()
         self.w = workload
         self.batch = batch or workload.batch
-        self.model = self.ito.Model(self.ito.layers_for(workload), self.batch)
+        self.model = self.ito.Model(self.ito.layers_for(workload), self.batch, input_uint8=workload.input_uint8,
+                                    trainable_from=workload.trainable_from, packed_masks=packed_masks)
         self.n_layers = self.model.n_weight_layers
         for l, W in enumerate(si.make_weights(workload)):
             self.model.set_weights(l, W)
@@ -58,9 +59,12 @@ class GpuRun:
 
     def names(self, kinds=("y", "a", "e", "d", "g", "w")):
         out = []
+        first = self.w.trainable_from
         for l in range(self.n_layers):
             for k in kinds:
-                if k == "d" and l == 0:
+                if k == "d" and l <= first:
+                    continue
+                if k in ("e", "g") and l < first:
                     continue
                 out.append("%s%d" % (k, l))
         if self.w.kind == "cnn":

@@ -140,3 +140,26 @@ def test_top_error(ito):
     logits[1, labels[1]] = -128
     d = ito.ito_top_error(_dev(logits), _dev(labels), 64)
     assert np.array_equal(_host(d), O.top_error(logits, labels, 64))
+
+
+def test_wgrad_longest_contraction_extreme_values(ito):
+    """K = 131072 terms of (-128) * 127 = -16256: the sum -2,130,706,432 is just
+    inside int32 (split-K slices and chunk drains must add exactly)."""
+    B, IC, OC = 131072, 27, 64
+    e = np.full((B, OC), -128, np.int8)
+    a = np.full((B, IC), 127, np.int8)
+    e[:, 1] = 127                      # column 1: +16129 per term
+    a[::2, 2] = -127                   # column 2 alternates sign: sums to 0 for column 0
+    G, mx = ito.ito_linear_wgrad(_dev(e), _dev(a))
+    Gh = _host(G)
+    assert Gh[0, 0] == -128 * 127 * B and Gh[1, 0] == 127 * 127 * B
+    assert Gh[0, 2] == 0
+    assert _u32(mx) == 128 * 127 * B
+
+
+def test_update_zero_gradient_leaves_weights(ito):
+    W = i8(4096)
+    Wd = _dev(W)
+    sh, ws, nz = ito.ito_niti_update(Wd, _dev(np.zeros(4096, np.int32)), _dev(np.zeros(1, np.int32)))
+    assert (int(_host(sh)[0]), int(_host(ws)[0]), int(_host(nz)[0])) == (0, 0, 0)
+    assert np.array_equal(_host(Wd), W)

@@ -117,3 +117,40 @@ def test_dfp16_routes_agree():
     b = O.dfp16_step(weights, w.exp_w, x, w.exp_x, route="f64")
     for k in a:
         assert np.array_equal(np.asarray(a[k]), np.asarray(b[k])), k
+
+
+def test_partial_training_equals_training_the_suffix():
+    """Training with the first k layers frozen ("trainable_layers_from_last")
+    equals training the remaining layers on the frozen prefix's output; the
+    frozen weights do not change."""
+    w = si.by_name(5)
+    weights = si.make_weights(w)
+    x, labels = si.make_batch(w, 0)
+    k = w.trainable_from
+    r = O.mlp_step(weights, x, labels, trainable_from=k)
+    for l in range(k):
+        assert np.array_equal(r["w%d" % l], weights[l])
+        assert "g%d" % l not in r and "d%d" % (l + 1) not in r
+    prefix_out = r["a%d" % (k - 1)]
+    s = O.mlp_step(weights[k:], prefix_out, labels)
+    for name in ("y", "a", "e", "d", "g", "w"):
+        for l in range(len(weights) - k):
+            key = "%s%d" % (name, l)
+            if key in s:
+                assert np.array_equal(s[key], r["%s%d" % (name, l + k)]), key
+
+
+def test_partial_planted_leak_into_frozen_layer_is_caught():
+    """A backward that does not stop at the frozen boundary (planted here by
+    moving the boundary one layer down) propagates a delta into the last frozen
+    layer and computes its weight gradient: exactly the records the identity
+    above requires to be absent."""
+    w = si.by_name(5)
+    weights = si.make_weights(w)
+    x, labels = si.make_batch(w, 0)
+    k = w.trainable_from
+    good = O.mlp_step(weights, x, labels, trainable_from=k)
+    leaked = O.mlp_step(weights, x, labels, trainable_from=k - 1)
+    for key in ("d%d" % k, "g%d" % (k - 1)):
+        assert key in leaked and key not in good
+    assert np.array_equal(good["w%d" % k], leaked["w%d" % k])   # the boundary layer itself agrees

@@ -341,3 +341,34 @@ def test_dfp_update_cases():
     assert Wn.tolist() == [-2048, 3172, -32767, 32767, 5]
     Wn, _ = O.dfp_update(W, G, -40)         # any left shift past 17 bits saturates the same way
     assert Wn.tolist() == [-32767, 32767, -32767, 32767, 5]
+
+
+# ------------------------------------------------- partial-model (UINT8 input)
+
+@pytest.mark.parametrize("B,IC,OC", [(1, 1, 1), (2, 5, 3), (4, 3, 4)])
+def test_u8_contractions_brute_force(B, IC, OC):
+    X = rng.integers(0, 256, (B, IC)).astype(np.uint8)
+    X[0, 0] = 255
+    W = rng.integers(-128, 128, (OC, IC)).astype(np.int8)
+    E = rng.integers(-128, 128, (B, OC)).astype(np.int8)
+    assert (O.linear_fwd_u8(X, W) == brute_fwd(X, W)).all()
+    assert (O.linear_wgrad_u8(E, X) == brute_wgrad(E, X)).all()
+    # a uint8 value is not its int8 bit pattern: 255 must not read as -1
+    assert O.linear_fwd_u8(np.array([[255]], np.uint8), np.array([[2]], np.int8))[0, 0] == 510
+
+
+def test_u8_contractions_vs_float64_medium():
+    X = rng.integers(0, 256, (70, 513)).astype(np.uint8)
+    W = rng.integers(-128, 128, (33, 513)).astype(np.int8)
+    E = rng.integers(-128, 128, (70, 33)).astype(np.int8)
+    assert (O.linear_fwd_u8(X, W) == O.linear_fwd_f64(X, W)).all()
+    assert (O.linear_wgrad_u8(E, X) == O.linear_wgrad_f64(E, X)).all()
+
+
+def test_pack_relu_mask_hand_case():
+    A = np.array([[1, 0, -1, 5, 0, 0, 0, 127, 3, -128],
+                  [0, 0, 0, 0, 0, 0, 0, 0, 0, 1]], np.int8)
+    m = O.pack_relu_mask(A)
+    assert m.shape == (2, 2)
+    assert m[0].tolist() == [0b10001001, 0b00000001]
+    assert m[1].tolist() == [0, 0b00000010]
