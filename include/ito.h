@@ -265,6 +265,22 @@ int ito_model_get_weights(const ito_model *m, int layer, int8_t *W, int on_host,
 int ito_model_tensor(const ito_model *m, const char *name, void **dev_ptr, int *elem_bytes,
                      int64_t *numel);
 
+/* Static per-channel requantisation of a Linear layer's forward output, the
+ * TI library's own forward ("Integer On-Device Training: Overview", section
+ * 4: each layer holds INT32 offsets, mutable and updated by the backward
+ * pass, and const k (shift) and mult arrays from the exported OSS chain
+ * Add(offset) -> Mul -> Mul -> Floor -> Clip). Readings: the layer output is
+ *   a[b][c] = clip(floor((y32[b][c] + offset[c]) * mult[c] / 2^shift[c]),
+ *                  relu ? 0 : -128, 127)      (int64 product)
+ * in place of the dynamic NITI shift; each step the offsets' gradient
+ * g[c] = sum_b delta[b][c] updates them with NITI Steps 1-5 (saturating to
+ * int32). offset, mult, shift: int32 [OC], host or device memory (on_host);
+ * shift in 0..62. Names of the offsets and their gradient in
+ * ito_model_tensor: "off<l>", "og<l>"; stats "ogmax<l>", "ogs<l>", "ows<l>",
+ * "onz<l>". Errors: ITO_ERR_ARG, ITO_ERR_UNSUPPORTED (a conv layer). */
+int ito_model_set_static_requant(ito_model *m, int layer, const int32_t *offset, const int32_t *mult,
+                                 const int32_t *shift, int on_host, void *stream);
+
 /* Position of a named scalar in the model's "stats" array (int32), e.g.
  * "ymax0", "ys0", "dmax1", "ds1", "gmax0", "gs0", "ws0", "nz0", "pmax",
  * "ps"; -1 if unknown. Max values are stored as their uint32 bit pattern. */
@@ -300,9 +316,11 @@ int ito_train_step_host(ito_model *m, const int8_t *x_host, const int32_t *label
 /* Forward pass only ("INTODT_Infer"): writes the int8 logits [batch][C]. */
 int ito_infer(ito_model *m, const int8_t *x, int8_t *logits, void *stream);
 
-/* Checkpoint ("Trained Weights in RAM": snapshot the weight arrays and
- * restore them before training resumes): raw little-endian int8 weights of
- * every trainable layer after a small header with the layer shapes.
+/* Checkpoint ("Trained Weights in RAM": snapshot the weight and offset arrays
+ * and restore them before training resumes): raw little-endian int8 weights
+ * of every layer after a small header with the layer shapes, then per layer a
+ * static-requantisation flag followed (when set) by its offsets, mult and
+ * shift arrays.
  * Synchronise the device. Errors: ITO_ERR_ARG (path), ITO_ERR_SHAPE (file
  * does not match the model). */
 int ito_model_save(const ito_model *m, const char *path);

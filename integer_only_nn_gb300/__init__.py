@@ -85,6 +85,7 @@ _SIGS = {
     "ito_dfp16_model_read_stats": (_I, [_P, _P, _I]),
     "ito_dfp16_train_step": (_I, [_P, _P, _I32, _P]),
     "ito_model_use_graphs": (_I, [_P, _I]),
+    "ito_model_set_static_requant": (_I, [_P, _I, _P, _P, _P, _I, _P]),
     "ito_model_profile": (_I, [_P, _I]),
     "ito_model_profile_read": (_I, [_P, _P, _P, _P]),
     "ito_model_kernels_per_step": (_I, [_P]),
@@ -293,6 +294,13 @@ class Model:
             _check(_lib.ito_model_set_weights(self._h, layer, a.ctypes.data_as(ctypes.c_void_p), 1,
                                               _stream(stream)))
 
+    def set_static_requant(self, layer, offset, mult, shift, stream=None):
+        """numpy int32 [OC] arrays (host)."""
+        import numpy as np
+        arrs = [np.ascontiguousarray(a, dtype=np.int32) for a in (offset, mult, shift)]
+        _check(_lib.ito_model_set_static_requant(self._h, layer, *[a.ctypes.data_as(ctypes.c_void_p) for a in arrs],
+                                                 1, _stream(stream)))
+
     def tensor(self, name):
         """A torch view (on the GPU) of a named model tensor."""
         torch = _torch()
@@ -311,14 +319,14 @@ class Model:
         """All named scalars of the last step, read back to the host."""
         v = self.tensor("stats").cpu().tolist()
         out = {}
-        for key in ("ymax", "ys", "dmax", "ds", "gmax", "gs", "ws", "nz"):
+        for key in ("ymax", "ys", "dmax", "ds", "gmax", "gs", "ws", "nz", "ogmax", "ogs", "ows", "onz"):
             l = 0
             while True:
                 i = self.stat_index("%s%d" % (key, l))
                 if i < 0:
                     break
                 val = v[i]
-                out["%s%d" % (key, l)] = val & 0xFFFFFFFF if key in ("ymax", "dmax", "gmax", "nz") else val
+                out["%s%d" % (key, l)] = val & 0xFFFFFFFF if key in ("ymax", "dmax", "gmax", "nz", "ogmax", "onz") else val
                 l += 1
         for key in ("pmax", "ps"):
             i = self.stat_index(key)

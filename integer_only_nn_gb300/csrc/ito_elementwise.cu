@@ -211,6 +211,136 @@ int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t*
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "requant launch: %s", cudaGetErrorString(e));
 }
 
+// ------------------------------------------- static requantisation + offsets
+
+// out = clip(floor((Y + offset[c]) * mult[c] / 2^k[c]), relu ? 0 : -128, 127)
+// ("Integer On-Device Training: Overview", section 4: INT32 offsets and const
+// k / mult arrays; the exported chain Add(offset) -> Mul -> Mul -> Floor -> Clip)
+__device__ __forceinline__ int32_t static_one(int32_t y, int32_t off, int32_t mult, int32_t k, int32_t lo)
+{
+    const int64_t v = ((int64_t)y + off) * (int64_t)mult;
+    int64_t q = v >> k;                   // arithmetic shift = floor division by 2^k
+    q = q < lo ? lo : (q > 127 ? 127 : q);
+    return (int32_t)q;
+}
+
+__global__ void k_requant_static_v8(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
+                                    const int32_t* __restrict__ off, const int32_t* __restrict__ mult,
+                                    const int32_t* __restrict__ ksh, int relu, int8_t* __restrict__ out8,
+                                    uint16_t* __restrict__ outb, int64_t ldb, uint8_t* __restrict__ mask_out)
+{
+    const int32_t lo = relu ? 0 : -128;
+    const int64_t groups = rows * (cols >> 3);
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i0 = g << 3;
+        const int64_t r = i0 / cols, c = i0 - r * cols;
+        const int4 y0 = __ldcs(reinterpret_cast<const int4*>(Y + i0));
+        const int4 y1 = __ldcs(reinterpret_cast<const int4*>(Y + i0 + 4));
+        const int32_t y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+        int8_t q8[8];
+        uint32_t qb[4], mbits = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            q8[i] = (int8_t)static_one(y[i], __ldg(off + c + i), __ldg(mult + c + i), __ldg(ksh + c + i), lo);
+            mbits |= (q8[i] > 0 ? 1u : 0u) << i;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            qb[i] = (uint32_t)int_to_bf16_bits(q8[2 * i]) | ((uint32_t)int_to_bf16_bits(q8[2 * i + 1]) << 16);
+        *reinterpret_cast<uint2*>(out8 + i0) = *reinterpret_cast<const uint2*>(q8);
+        if (outb) *reinterpret_cast<uint4*>(outb + r * ldb + c) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
+        if (mask_out) mask_out[g] = (uint8_t)mbits;
+    }
+}
+
+__global__ void k_requant_static_1(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
+                                   const int32_t* __restrict__ off, const int32_t* __restrict__ mult,
+                                   const int32_t* __restrict__ ksh, int relu, int8_t* __restrict__ out8,
+                                   uint16_t* __restrict__ outb, int64_t ldb)
+{
+    const int32_t lo = relu ? 0 : -128;
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i - r * cols;
+        const int32_t q = static_one(Y[i], off[c], mult[c], ksh[c], lo);
+        out8[i] = (int8_t)q;
+        if (outb) outb[r * ldb + c] = int_to_bf16_bits(q);
+    }
+}
+
+int launch_requant_static(const int32_t* Y, int64_t rows, int64_t cols, const int32_t* off, const int32_t* mult,
+                          const int32_t* ksh, int relu, int8_t* out8, uint16_t* outb, int64_t ldb, uint8_t* mask_out,
+                          cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    const bool vec = cols % 8 == 0 && aligned(Y, 16) && aligned(out8, 8) && (!outb || (aligned(outb, 16) && ldb % 8 == 0));
+    if (mask_out && !vec) return set_error(ITO_ERR_UNSUPPORTED, "bit-packed masks need rows of a multiple of 8");
+    if (vec)
+        k_requant_static_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(Y, rows, cols, off, mult, ksh,
+                                                                                      relu, out8, outb, ldb, mask_out);
+    else
+        k_requant_static_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(Y, rows, cols, off, mult, ksh, relu,
+                                                                                 out8, outb, ldb);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "static requant launch: %s", cudaGetErrorString(e));
+}
+
+// g[c] = sum over rows of delta[r][c] (the offsets' gradient); max |g| into *d_max
+__global__ void k_offset_grad(const int8_t* __restrict__ delta, int64_t rows, int64_t cols, int32_t* __restrict__ g,
+                              uint32_t* __restrict__ d_max)
+{
+    uint32_t mx = 0;
+    for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols; c += (int64_t)gridDim.x * blockDim.x) {
+        int32_t acc = 0;
+        for (int64_t r = 0; r < rows; ++r) acc += delta[r * cols + c];
+        g[c] = acc;
+        mx = max(mx, abs_u32(acc));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+}
+
+// NITI Steps 2-5 on INT32 offsets, saturating to int32
+__global__ void k_offset_update(int32_t* __restrict__ off, const int32_t* __restrict__ g, int64_t n,
+                                const uint32_t* __restrict__ d_max, int target_bits, int mu_weight,
+                                int32_t* __restrict__ d_shift, int32_t* __restrict__ d_wshift,
+                                uint32_t* __restrict__ d_nonzero)
+{
+    const int s = shift_for(*d_max, target_bits);
+    const int ws = s - mu_weight > 0 ? s - mu_weight : 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (d_shift) *d_shift = s;
+        if (d_wshift) *d_wshift = ws;
+    }
+    uint32_t cnt = 0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t d = rhu32(sat8(rhu32(g[i], s)), ws);
+        cnt += d != 0;
+        int64_t v = (int64_t)off[i] - d;
+        v = v < INT32_MIN ? INT32_MIN : (v > INT32_MAX ? INT32_MAX : v);
+        off[i] = (int32_t)v;
+    }
+    if (d_nonzero) {
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(d_nonzero, cnt);
+    }
+}
+
+int launch_offset_grad_update(const int8_t* delta, int64_t rows, int64_t cols, int32_t* g, uint32_t* d_max,
+                              int32_t* off, int target_bits, int mu_weight, int32_t* d_shift, int32_t* d_wshift,
+                              uint32_t* d_nonzero, cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    k_offset_grad<<<launch_grid_blocks(cols, 256), 256, 0, s>>>(delta, rows, cols, g, d_max);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "offset grad launch: %s", cudaGetErrorString(e));
+    k_offset_update<<<launch_grid_blocks(cols, 256), 256, 0, s>>>(off, g, cols, d_max, target_bits, mu_weight, d_shift,
+                                                                  d_wshift, d_nonzero);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "offset update launch: %s", cudaGetErrorString(e));
+}
+
 // ------------------------------------------------------------ NITI update
 
 // weight_delta of Steps 3-4: round(sat8(round(G >> s)) >> ws); the operand

@@ -119,6 +119,14 @@ int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t*
                    const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
                    const uint8_t* gate_bits = nullptr, uint8_t* mask_out = nullptr);
 int launch_u8_to_bf16(const uint8_t* src, int64_t rows, int64_t cols, uint16_t* dst, int64_t ldd, cudaStream_t s);
+// static per-channel requantisation: clip(floor((Y + off[c]) * mult[c] / 2^k[c]), relu ? 0 : -128, 127)
+int launch_requant_static(const int32_t* Y, int64_t rows, int64_t cols, const int32_t* off, const int32_t* mult,
+                          const int32_t* ksh, int relu, int8_t* out8, uint16_t* outb, int64_t ldb, uint8_t* mask_out,
+                          cudaStream_t s);
+// offset gradient g[c] = sum_r delta[r][c] (max |g| into *d_max), then the NITI update of the INT32 offsets
+int launch_offset_grad_update(const int8_t* delta, int64_t rows, int64_t cols, int32_t* g, uint32_t* d_max,
+                              int32_t* off, int target_bits, int mu_weight, int32_t* d_shift, int32_t* d_wshift,
+                              uint32_t* d_nonzero, cudaStream_t s);
 
 // NITI Steps 2-5 in place on W [rows][cols] (int8) with gradient G (int32),
 // refreshing the bf16 copy Wb (pitch ldb, may be null).

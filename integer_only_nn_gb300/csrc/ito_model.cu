@@ -29,7 +29,11 @@
 
 namespace ito {
 
-enum { ST_YMAX = 0, ST_YS, ST_DMAX, ST_DS, ST_GMAX, ST_GS, ST_WS, ST_NZ, ST_PER_LAYER };
+enum {
+    ST_YMAX = 0, ST_YS, ST_DMAX, ST_DS, ST_GMAX, ST_GS, ST_WS, ST_NZ,
+    ST_OGMAX, ST_OGS, ST_OWS, ST_ONZ,   // offsets of a statically requantised layer
+    ST_PER_LAYER
+};
 
 struct MLayer {
     int kind;
@@ -53,6 +57,8 @@ struct MLayer {
     int32_t* d32 = nullptr;     // [rows_in][IC]
     int32_t* g32 = nullptr;     // [OC][K]
     uint8_t* mask = nullptr;    // bit-packed ReLU mask of the output [rows][OC / 8] (packed_masks)
+    bool static_q = false;      // static per-channel requantisation with trained INT32 offsets
+    int32_t *off32 = nullptr, *mult32 = nullptr, *k32 = nullptr, *og32 = nullptr;   // [OC] (Linear layers)
     GemmPlan pf{}, pd{}, pg{};
     bool has_dgrad = false;
     bool relu = false;
@@ -292,6 +298,12 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         ITO_TRY(m->alloc(&L.eb, (size_t)L.rows_out * L.lde));
         ITO_TRY(m->alloc(&L.g32, (size_t)L.OC * L.K));
         if (m->opt.packed_masks && L.relu) ITO_TRY(m->alloc(&L.mask, (size_t)L.rows_out * (L.OC / 8)));
+        if (!conv) {
+            ITO_TRY(m->alloc(&L.off32, (size_t)L.OC));
+            ITO_TRY(m->alloc(&L.mult32, (size_t)L.OC));
+            ITO_TRY(m->alloc(&L.k32, (size_t)L.OC));
+            ITO_TRY(m->alloc(&L.og32, (size_t)L.OC));
+        }
         if (L.has_dgrad) ITO_TRY(m->alloc(&L.d32, (size_t)L.rows_in * L.IC));
         if (conv) {
             L.ldp = pad8(L.K);
@@ -347,7 +359,8 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
     }
 
     // names of the stats entries
-    const char* nm[ST_PER_LAYER] = {"ymax", "ys", "dmax", "ds", "gmax", "gs", "ws", "nz"};
+    const char* nm[ST_PER_LAYER] = {"ymax", "ys", "dmax", "ds", "gmax", "gs", "ws", "nz",
+                                    "ogmax", "ogs", "ows", "onz"};
     for (int l = 0; l < nl; ++l)
         for (int k = 0; k < ST_PER_LAYER; ++k) m->stat_names.push_back({std::string(nm[k]) + std::to_string(l),
                                                                          l * ST_PER_LAYER + k});
@@ -400,9 +413,14 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
                                       pad8(m->pool_C), m->stats + pl * ST_PER_LAYER + 1, s));
         }
         ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
-        ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
-                   launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits, L.relu ? 1 : 0,
-                                  nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr, L.mask));
+        if (L.static_q)
+            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
+                       launch_requant_static(L.y32, L.rows_out, L.OC, L.off32, L.mult32, L.k32, L.relu ? 1 : 0, L.a8,
+                                             L.ab, L.lda, L.mask, s));
+        else
+            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
+                       launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits, L.relu ? 1 : 0,
+                                      nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr, L.mask));
         in8 = L.a8;
     }
     return ITO_OK;
@@ -450,6 +468,11 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
                    launch_niti_update(L.W8, L.Wb, L.ldw, L.g32, L.OC, L.K, m->umax(l, ST_GMAX), p.target_bits,
                                       p.mu_weight, m->sval(l, ST_GS), m->sval(l, ST_WS),
                                       reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ)), s));
+        if (L.static_q)
+            ITO_LAUNCH(m, s, ITO_PROF_UPDATE, (double)L.rows_out * L.OC + 12.0 * L.OC,
+                       launch_offset_grad_update(L.e8, L.rows_out, L.OC, L.og32, m->umax(l, ST_OGMAX), L.off32,
+                                                 p.target_bits, p.mu_weight, m->sval(l, ST_OGS), m->sval(l, ST_OWS),
+                                                 reinterpret_cast<uint32_t*>(m->sval(l, ST_ONZ)), s));
     }
     (void)x;
     return ITO_OK;
@@ -553,25 +576,49 @@ int ito_model_tensor(const ito_model* m, const char* name, void** dev_ptr, int* 
     if (s == "p") return put(m->p32, 4, (int64_t)m->batch * m->pool_C);
     if (s == "pa") return put(m->pa8, 1, (int64_t)m->batch * m->pool_C);
     if (s == "pe") return put(m->pe8, 1, (int64_t)m->batch * m->pool_C);
-    if (s.size() >= 2) {
-        const char k = s[0];
-        char* end = nullptr;
-        const long l = strtol(s.c_str() + 1, &end, 10);
-        if (end && *end == 0 && l >= 0 && l < nl) {
-            const MLayer& L = m->L[l];
-            switch (k) {
-            case 'y': return put(L.y32, 4, L.rows_out * L.OC);
-            case 'a': return put(L.a8, 1, L.rows_out * L.OC);
-            case 'e': return put(L.e8, 1, L.rows_out * L.OC);
-            case 'd': return put(L.d32, 4, L.rows_in * L.IC);
-            case 'g': return put(L.g32, 4, (int64_t)L.OC * L.K);
-            case 'w': return put(L.W8, 1, (int64_t)L.OC * L.K);
-            case 'm': return put(L.mask, 1, L.rows_out * (L.OC / 8));
-            default: break;
-            }
-        }
-    }
+    // per-layer tensors: a name prefix followed by the layer index
+    size_t pos = 0;
+    while (pos < s.size() && (s[pos] < '0' || s[pos] > '9')) ++pos;
+    if (pos == 0 || pos == s.size()) return set_error(ITO_ERR_ARG, "unknown tensor name %s", name);
+    char* end = nullptr;
+    const long l = strtol(s.c_str() + pos, &end, 10);
+    if (!end || *end || l < 0 || l >= nl) return set_error(ITO_ERR_ARG, "unknown tensor name %s", name);
+    const MLayer& L = m->L[l];
+    const std::string key = s.substr(0, pos);
+    if (key == "y") return put(L.y32, 4, L.rows_out * L.OC);
+    if (key == "a") return put(L.a8, 1, L.rows_out * L.OC);
+    if (key == "e") return put(L.e8, 1, L.rows_out * L.OC);
+    if (key == "d") return put(L.d32, 4, L.rows_in * L.IC);
+    if (key == "g") return put(L.g32, 4, (int64_t)L.OC * L.K);
+    if (key == "w") return put(L.W8, 1, (int64_t)L.OC * L.K);
+    if (key == "m") return put(L.mask, 1, L.rows_out * (L.OC / 8));
+    if (key == "off") return put(L.off32, 4, L.OC);
+    if (key == "og") return put(L.og32, 4, L.OC);
     return set_error(ITO_ERR_ARG, "unknown tensor name %s", name);
+}
+
+int ito_model_set_static_requant(ito_model* m, int layer, const int32_t* offset, const int32_t* mult,
+                                 const int32_t* shift, int on_host, void* stream)
+{
+    const int l = weight_layer(m, layer);
+    if (l < 0 || !offset || !mult || !shift) return set_error(ITO_ERR_ARG, "bad model, layer or array");
+    MLayer& L = m->L[l];
+    if (!L.off32) return set_error(ITO_ERR_UNSUPPORTED, "static requantisation is for Linear layers");
+    if (on_host) {
+        for (int c = 0; c < L.OC; ++c)
+            if (shift[c] < 0 || shift[c] > 62) return set_error(ITO_ERR_ARG, "shift[%d] outside 0..62", c);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaMemcpyKind kind = on_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    const size_t bytes = sizeof(int32_t) * L.OC;
+    if (cudaMemcpyAsync(L.off32, offset, bytes, kind, s) != cudaSuccess ||
+        cudaMemcpyAsync(L.mult32, mult, bytes, kind, s) != cudaSuccess ||
+        cudaMemcpyAsync(L.k32, shift, bytes, kind, s) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "static requant copy failed");
+    if (on_host && cudaStreamSynchronize(s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+    L.static_q = true;
+    drop_graphs(m);
+    return ITO_OK;
 }
 
 int ito_model_stat_index(const ito_model* m, const char* name)
@@ -726,7 +773,7 @@ int ito_infer(ito_model* m, const int8_t* x, int8_t* logits, void* stream)
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "logits copy: %s", cudaGetErrorString(e));
 }
 
-static const uint32_t kMagic = 0x3149544fu;   // "OTI1"
+static const uint32_t kMagic = 0x3249544fu;   // "OTI2": weights, then per Linear layer a static flag and offsets
 
 int ito_model_save(const ito_model* m, const char* path)
 {
@@ -745,6 +792,17 @@ int ito_model_save(const ito_model* m, const char* path)
         buf.resize((size_t)L.OC * L.K);
         ok = ok && cudaMemcpy(buf.data(), L.W8, buf.size(), cudaMemcpyDeviceToHost) == cudaSuccess;
         ok = ok && fwrite(buf.data(), 1, buf.size(), f) == buf.size();
+    }
+    std::vector<int32_t> o;
+    for (const MLayer& L : m->L) {
+        const int32_t flag = L.static_q ? 1 : 0;
+        ok = ok && fwrite(&flag, 4, 1, f) == 1;
+        if (!flag) continue;
+        for (const int32_t* src : {L.off32, L.mult32, L.k32}) {
+            o.resize(L.OC);
+            ok = ok && cudaMemcpy(o.data(), src, 4 * o.size(), cudaMemcpyDeviceToHost) == cudaSuccess;
+            ok = ok && fwrite(o.data(), 4, o.size(), f) == o.size();
+        }
     }
     fclose(f);
     return ok ? ITO_OK : set_error(ITO_ERR_ARG, "write to %s failed", path);
@@ -767,6 +825,16 @@ int ito_model_load(ito_model* m, const char* path)
         buf.resize((size_t)L.OC * L.K);
         ok = fread(buf.data(), 1, buf.size(), f) == buf.size();
         ok = ok && ito_model_set_weights(m, (int)l, buf.data(), 1, nullptr) == ITO_OK;
+    }
+    for (size_t l = 0; ok && l < m->L.size(); ++l) {
+        MLayer& L = m->L[l];
+        int32_t flag = 0;
+        ok = fread(&flag, 4, 1, f) == 1;
+        if (!ok || !flag) continue;
+        std::vector<int32_t> off(L.OC), mult(L.OC), k(L.OC);
+        ok = fread(off.data(), 4, L.OC, f) == (size_t)L.OC && fread(mult.data(), 4, L.OC, f) == (size_t)L.OC &&
+             fread(k.data(), 4, L.OC, f) == (size_t)L.OC;
+        ok = ok && ito_model_set_static_requant(m, (int)l, off.data(), mult.data(), k.data(), 1, nullptr) == ITO_OK;
     }
     fclose(f);
     if (!ok) return set_error(ITO_ERR_SHAPE, "checkpoint %s does not match the model", path);

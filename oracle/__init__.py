@@ -76,6 +76,9 @@ def lib():
             "ora_linear_fwd_u8": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
             "ora_linear_wgrad_u8": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
             "ora_pack_relu_mask": (None, [P, ctypes.c_int, ctypes.c_int, P]),
+            "ora_requant_static": (None, [P, ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int, P]),
+            "ora_offset_grad": (None, [P, ctypes.c_int, ctypes.c_int, P]),
+            "ora_offset_update": (i64, [P, P, ctypes.c_int, i32, i32, P, P, P]),
             "ora_conv2d_fwd": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
             "ora_conv2d_dgrad": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
             "ora_conv2d_wgrad": (None, [P, P] + [ctypes.c_int] * 9 + [P]),
@@ -225,6 +228,34 @@ def linear_wgrad_u8(delta, A):
     G = np.empty((OC, IC), np.int32)
     lib().ora_linear_wgrad_u8(_p(delta), _p(A), B, IC, OC, _p(G))
     return G
+
+
+def requant_static(Y, offset, mult, k, relu: bool):
+    Y = _c(Y, np.int32)
+    B, C = Y.shape
+    offset, mult, k = _c(offset, np.int32), _c(mult, np.int32), _c(k, np.int32)
+    assert offset.size == mult.size == k.size == C
+    out = np.empty((B, C), np.int8)
+    lib().ora_requant_static(_p(Y), B, C, _p(offset), _p(mult), _p(k), int(relu), _p(out))
+    return out
+
+
+def offset_grad(delta):
+    delta = _c(delta, np.int8)
+    B, C = delta.shape
+    g = np.empty(C, np.int32)
+    lib().ora_offset_grad(_p(delta), B, C, _p(g))
+    return g
+
+
+def offset_update(offset, g, target_bits: int = TARGET_BITS, mu_weight: int = MU_WEIGHT):
+    """-> (new offsets, shift, weight_shift, max|g|, nonzero count)"""
+    on = np.array(offset, dtype=np.int32, copy=True, order="C")
+    g = _c(g, np.int32)
+    s, ws, m = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_uint32()
+    nz = lib().ora_offset_update(_p(on), _p(g), g.size, target_bits, mu_weight, ctypes.byref(s), ctypes.byref(ws),
+                                 ctypes.byref(m))
+    return on, s.value, ws.value, m.value, nz
 
 
 def pack_relu_mask(A):
@@ -395,7 +426,7 @@ def _linear_ops(route):
 
 
 def mlp_step(weights, x, labels, target_bits=TARGET_BITS, mu_weight=MU_WEIGHT,
-             target_mag=TARGET_MAG, route="loops", trainable_from=0):
+             target_mag=TARGET_MAG, route="loops", trainable_from=0, static_q=None):
     """One NITI step of a sequential int8 MLP: Linear+ReLU layers and a final
     Linear producing int8 logits. `weights` is a list of int8 [OC, IC]; the
     updated weights are returned in the record (inputs are not modified).
@@ -411,7 +442,12 @@ def mlp_step(weights, x, labels, target_bits=TARGET_BITS, mu_weight=MU_WEIGHT,
     trainable_layers_from_last): layers before `trainable_from` are frozen and
     run forward only; backward stops at layer trainable_from (no delta is
     propagated into the frozen part). A uint8 `x` is the UINT8 input the
-    library receives from a frozen prefix ending in ReLU (values 0..255)."""
+    library receives from a frozen prefix ending in ReLU (values 0..255).
+
+    static_q: None, or per layer None / dict(offset, mult, k) for the TI
+    library's static forward requantisation (requant_static) with trained
+    INT32 offsets: record names off{l} (updated offsets), og{l} offset
+    gradient, ogmax{l}/ogs{l}/ows{l}/onz{l}."""
     fwd, dgrad, wgrad = _linear_ops(route)
     L = len(weights)
     r = {}
@@ -422,8 +458,13 @@ def mlp_step(weights, x, labels, target_bits=TARGET_BITS, mu_weight=MU_WEIGHT,
             y = linear_fwd_u8(act[-1], weights[l]) if route == "loops" else linear_fwd_f64(act[-1], weights[l])
         else:
             y = fwd(act[-1], weights[l])
-        a, s, m = requant(y, relu=(l < L - 1), target_bits=target_bits)
-        r["y%d" % l], r["ymax%d" % l], r["ys%d" % l], r["a%d" % l] = y, m, s, a
+        sq = static_q[l] if static_q else None
+        if sq is not None:
+            a = requant_static(y, sq["offset"], sq["mult"], sq["k"], relu=(l < L - 1))
+            r["y%d" % l], r["ymax%d" % l], r["a%d" % l] = y, absmax32(y), a
+        else:
+            a, s, m = requant(y, relu=(l < L - 1), target_bits=target_bits)
+            r["y%d" % l], r["ymax%d" % l], r["ys%d" % l], r["a%d" % l] = y, m, s, a
         act.append(a)
     e = top_error(act[-1], labels, target_mag)
     r["e%d" % (L - 1)] = e
@@ -439,10 +480,18 @@ def mlp_step(weights, x, labels, target_bits=TARGET_BITS, mu_weight=MU_WEIGHT,
         wn, s, ws, m, nz = niti_update(weights[l], g, target_bits, mu_weight)
         r["g%d" % l], r["gmax%d" % l], r["gs%d" % l], r["ws%d" % l] = g, m, s, ws
         r["w%d" % l], r["nz%d" % l] = wn, nz
+        sq = static_q[l] if static_q else None
+        if sq is not None:
+            og = offset_grad(e)
+            on, s, ws, m, nz = offset_update(sq["offset"], og, target_bits, mu_weight)
+            r["og%d" % l], r["ogmax%d" % l], r["ogs%d" % l], r["ows%d" % l] = og, m, s, ws
+            r["off%d" % l], r["onz%d" % l] = on, nz
         if l > trainable_from:
             e = e_prev
     for l in range(trainable_from):
         r["w%d" % l] = np.array(weights[l], copy=True)      # frozen
+        if static_q and static_q[l] is not None:
+            r["off%d" % l] = np.array(static_q[l]["offset"], dtype=np.int32, copy=True)
     return r
 
 
@@ -549,15 +598,18 @@ def dfp16_step(weights, exp_w, x, exp_x, eta=DFP_ETA, target_bits=DFP_BITS, rout
 
 def run_steps(workload, steps: int, start_weights=None, callback=None, route="loops"):
     """Run `steps` training steps of a seeded workload (seeded_inputs.Workload),
-    feeding each step's updated weights to the next. callback(t, record) is
-    called after every step. Returns the final weights."""
+    feeding each step's updated weights (and offsets) to the next.
+    callback(t, record) is called after every step. Returns the final weights."""
     import seeded_inputs as si
     w = workload
     weights = [np.array(a) for a in (start_weights or si.make_weights(w))]
+    static_q = si.make_static_requant(w)
     for t in range(steps):
         x, labels = si.make_batch(w, t)
         if w.kind == "mlp":
-            rec = mlp_step(weights, x, labels, route=route, trainable_from=w.trainable_from)
+            rec = mlp_step(weights, x, labels, route=route, trainable_from=w.trainable_from, static_q=static_q)
+            if static_q:
+                static_q = [None if q is None else dict(q, offset=rec["off%d" % l]) for l, q in enumerate(static_q)]
         elif w.kind == "cnn":
             rec = cnn_step(weights, x, labels, w.convs)
         elif w.kind == "dfp16":

@@ -293,6 +293,66 @@ void ora_linear_wgrad(const int8_t *delta, const int8_t *A, int B, int IC, int O
     }
 }
 
+/* Static per-channel requantisation of the TI library's forward ([ODT]
+ * section 4: each layer holds INT32 offsets and const k (shift) and mult
+ * arrays; section 6, step 2: the exported OSS chain Add(offset) -> Mul ->
+ * Mul -> Floor -> Clip). Reading: the two multiplies are the integer mult
+ * and a right shift by k, i.e.
+ *   out[b][c] = clip(floor((Y[b][c] + offset[c]) * mult[c] / 2^k[c]), lo, 127)
+ * with lo = 0 for a ReLU layer (the clamp at the output zero point) and -128
+ * otherwise; the product is formed in int64. */
+void ora_requant_static(const int32_t *Y, int B, int C, const int32_t *offset, const int32_t *mult,
+                        const int32_t *k, int relu, int8_t *out)
+{
+    for (int b = 0; b < B; b++)
+        for (int c = 0; c < C; c++) {
+            if (k[c] < 0 || k[c] > 62) ora_fail("static shift out of range");
+            int64_t v = ((int64_t)Y[(int64_t)b * C + c] + offset[c]) * (int64_t)mult[c];
+            int64_t q = floor_div_pow2(v, k[c]);
+            int64_t lo = relu ? 0 : -128;
+            if (q < lo) q = lo;
+            if (q > 127) q = 127;
+            out[(int64_t)b * C + c] = (int8_t)q;
+        }
+}
+
+/* Gradient of the offsets: the offset is added to every row of Y, so its
+ * gradient is the delta summed over the batch rows: g[c] = sum_b delta[b][c]. */
+void ora_offset_grad(const int8_t *delta, int B, int C, int32_t *g)
+{
+    for (int c = 0; c < C; c++) {
+        int64_t acc = 0;
+        for (int b = 0; b < B; b++) acc += delta[(int64_t)b * C + c];
+        g[c] = checked_i32(acc);
+    }
+}
+
+/* Update of the INT32 offsets. Reading (the pages say only that offsets are
+ * updated by the backward pass): the same NITI Steps 1-5 as for weights,
+ * applied to the offset gradient, with the result saturated to int32:
+ * s = max(0, bitlen(max|g|) - target_bits), Gq = sat8(rhu(g, s)),
+ * dO = rhu(Gq, max(0, s - mu)), offset = sat32(offset - dO). */
+int64_t ora_offset_update(int32_t *offset, const int32_t *g, int C, int32_t target_bits, int32_t mu_weight,
+                          int32_t *shift_out, int32_t *wshift_out, uint32_t *max_out)
+{
+    uint32_t m = ora_absmax32(g, C);
+    int32_t s = ora_shift_from_max(m, target_bits);
+    int32_t ws = s - mu_weight > 0 ? s - mu_weight : 0;
+    int64_t nonzero = 0;
+    for (int c = 0; c < C; c++) {
+        int64_t d = ora_rhu(ora_sat8(ora_rhu(g[c], s)), ws);
+        if (d != 0) nonzero++;
+        int64_t v = (int64_t)offset[c] - d;
+        if (v < INT32_MIN) v = INT32_MIN;
+        if (v > INT32_MAX) v = INT32_MAX;
+        offset[c] = (int32_t)v;
+    }
+    if (shift_out) *shift_out = s;
+    if (wshift_out) *wshift_out = ws;
+    if (max_out) *max_out = m;
+    return nonzero;
+}
+
 /* UINT8-input variants for the first trainable layer of a partial model
  * ([ODT] section 4: the frozen part ends in a ReLU layer, so the library
  * receives UINT8 activations in [0, 255]). */

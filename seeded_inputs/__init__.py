@@ -114,6 +114,7 @@ class Workload:
     exp_w: int = 0
     input_uint8: bool = False # mlp: UINT8 input in [0, 255] (partial-model training)
     trainable_from: int = 0   # mlp: layers before this one are frozen
+    static_requant: tuple = ()  # mlp: per layer (k_lo, k_hi) of a static requantisation, () = dynamic
 
     @property
     def seed(self) -> int:
@@ -132,6 +133,9 @@ WORKLOADS = (
     # partial-model training: UINT8 input, the last two of four layers trainable
     Workload(5, "mlp784-1024x3-10_b256_u8_last2", "mlp", 256, dims=(784, 1024, 1024, 1024, 10),
              classes=10, input_uint8=True, trainable_from=2),
+    # the TI library's forward: static per-channel requantisation with trained INT32 offsets
+    Workload(6, "mlp784-1024x3-10_b256_static", "mlp", 256, dims=(784, 1024, 1024, 1024, 10), classes=10,
+             static_requant=((24, 25), (24, 25), (24, 25), (22, 23))),
 )
 
 
@@ -160,6 +164,22 @@ def make_weights(w: Workload) -> list:
         n = int(np.prod(shp))
         v = round_clamp_normal(w.seed, weight_stream(l), n, w.sigma, w.lim)
         out.append(v.astype(dt).reshape(shp))
+    return out
+
+
+def make_static_requant(w: Workload):
+    """Per layer None, or dict(offset int32 [OC] = round(N(0, 2^14)), mult
+    int32 [OC] uniform in [2^14, 2^15), k int32 [OC] uniform in [k_lo, k_hi])
+    for a workload with a static requantisation (streams 40 + 3l .. 42 + 3l)."""
+    if not w.static_requant:
+        return None
+    out = []
+    for l, (klo, khi) in enumerate(w.static_requant):
+        oc = w.dims[l + 1]
+        off = round_clamp_normal(w.seed, 40 + 3 * l, oc, 16384.0, 1 << 30).astype(np.int32)
+        mult = uniform_int(w.seed, 41 + 3 * l, oc, 1 << 14, (1 << 15) - 1).astype(np.int32)
+        k = uniform_int(w.seed, 42 + 3 * l, oc, klo, khi).astype(np.int32)
+        out.append(dict(offset=off, mult=mult, k=k))
     return out
 
 

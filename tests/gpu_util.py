@@ -47,6 +47,11 @@ class GpuRun:
         self.n_layers = self.model.n_weight_layers
         for l, W in enumerate(si.make_weights(workload)):
             self.model.set_weights(l, W)
+        self.static_q = si.make_static_requant(workload) if workload.kind == "mlp" else None
+        if self.static_q:
+            for l, q in enumerate(self.static_q):
+                if q is not None:
+                    self.model.set_static_requant(l, q["offset"], q["mult"], q["k"])
 
     def step(self, t):
         x, labels = si.make_batch(self.w, t)
@@ -69,6 +74,10 @@ class GpuRun:
                 out.append("%s%d" % (k, l))
         if self.w.kind == "cnn":
             out += ["p", "pa", "pe"]
+        if self.static_q:
+            out += ["off%d" % l for l in range(self.n_layers)]
+            if "g" in kinds:
+                out += ["og%d" % l for l in range(self.w.trainable_from, self.n_layers)]
         return out
 
     def tensor(self, name):

@@ -372,3 +372,38 @@ def test_pack_relu_mask_hand_case():
     assert m.shape == (2, 2)
     assert m[0].tolist() == [0b10001001, 0b00000001]
     assert m[1].tolist() == [0, 0b00000010]
+
+
+# ------------------------------------- static requantisation with INT32 offsets
+
+def test_requant_static_hand_cases():
+    Y = np.array([[100, -100, 5, -7, 1000]], np.int32)
+    off = np.array([10, 0, -5, 0, 0], np.int32)
+    mult = np.array([3, 2, 1, 1, 1], np.int32)
+    k = np.array([2, 1, 0, 1, 0], np.int32)
+    # (110*3)/4 = 82.5 -> 82; (-200)/2 = -100; 0; -7/2 = -3.5 -> floor -4; 1000 -> clip 127
+    assert O.requant_static(Y, off, mult, k, relu=False).tolist() == [[82, -100, 0, -4, 127]]
+    assert O.requant_static(Y, off, mult, k, relu=True).tolist() == [[82, 0, 0, 0, 127]]
+    big = np.array([[-(1 << 30)]], np.int32)
+    assert O.requant_static(big, np.array([0], np.int32), np.array([1 << 14], np.int32),
+                            np.array([30], np.int32), relu=False).tolist() == [[-128]]   # -2^44 >> 30 = -2^14, clip
+
+
+def test_requant_static_identity_case_is_plain_clip():
+    Y = rng.integers(-400, 400, (7, 9)).astype(np.int32)
+    z = np.zeros(9, np.int32)
+    one = np.ones(9, np.int32)
+    assert (O.requant_static(Y, z, one, z, relu=False) == np.clip(Y, -128, 127)).all()
+    assert (O.requant_static(Y, z, one, z, relu=True) == np.clip(Y, 0, 127)).all()
+
+
+def test_offset_grad_and_update():
+    d = np.array([[1, -128, 5], [2, -128, -5], [3, -128, 0]], np.int8)
+    g = O.offset_grad(d)
+    assert g.tolist() == [6, -384, 0]
+    # max 384 -> 9 bits -> shift 2, weight shift 0: Gq = [2 (1.5 -> 2), -96, 0]
+    on, s, ws, m, nz = O.offset_update(np.array([0, np.iinfo(np.int32).max, 7], np.int32), g)
+    assert (s, ws, m, nz) == (2, 0, 384, 2)
+    assert on.tolist() == [-2, np.iinfo(np.int32).max, 7]       # +96 saturates at INT32_MAX
+    on, *_ = O.offset_update(np.array([np.iinfo(np.int32).min + 1], np.int32), np.array([100], np.int32))
+    assert on.tolist() == [np.iinfo(np.int32).min]
