@@ -380,6 +380,30 @@ int ito_dfp16_linear_wgrad(const int16_t *delta, const int32_t *d_exp_delta, con
 int ito_dfp16_update(int16_t *W, const int16_t *g, const int32_t *d_exp_g, int64_t n, int32_t exp_w,
                      int32_t eta, int32_t *d_k, uint32_t *d_nonzero, void *stream);
 
+/* Float -> DFP16 ("Mixed Precision Training...", section 3.1: a floating-
+ * point tensor's shared exponent is derived from its absolute maximum's
+ * exponent). Reading: with max|f| = frac * 2^e (frac in [0.5, 1)), E = e - 15;
+ * mant[i] = f[i] * 2^-E rounded to nearest (ties to even), saturated to
+ * [-32767, 32767]; an all-zero tensor gets E = 0. f: float [n] (finite);
+ * d_max_bits: device uint32 scratch (receives the bits of max|f|); mant:
+ * int16 [n]; *d_exp = E. A non-finite input raises ITO_ERR_ARG and an E
+ * outside int8 ITO_ERR_EXPONENT in the device error word. */
+int ito_dfp16_from_float(const float *f, int64_t n, uint32_t *d_max_bits, int16_t *mant, int32_t *d_exp,
+                         void *stream);
+
+/* DFP16 -> float: f[i] = mant[i] * 2^(*d_exp), rounded once to float. */
+int ito_dfp16_to_float(const int16_t *mant, const int32_t *d_exp, int64_t n, float *f, void *stream);
+
+/* DFP16 Linear forward with an FP32 output (the page's section 4: the
+ * kernels consume DFP-16 tensors and produce FP32 outputs, quantised for the
+ * next layer, e.g. with ito_dfp16_from_float): p64 as in ito_dfp16_linear_fwd
+ * (exact int64), then y[b][oc] = float(p64[b][oc]) * 2^(*d_exp_x + *d_exp_w)
+ * (p64 rounded to float to nearest even, then scaled). y: float [B][OC];
+ * d_max: device uint64 scratch (max |p64|). Workspace as ito_dfp16_linear_fwd. */
+int ito_dfp16_linear_fwd_f32(const int16_t *x, const int32_t *d_exp_x, const int16_t *W, const int32_t *d_exp_w,
+                             int B, int IC, int OC, void *workspace, size_t workspace_bytes, int64_t *p64,
+                             uint64_t *d_max, float *y, void *stream);
+
 typedef struct ito_dfp16_model ito_dfp16_model;
 
 /* A stack of DFP16 Linear layers dims[0] -> dims[1] -> ... -> dims[n_layers]

@@ -75,6 +75,9 @@ _SIGS = {
     "ito_dfp16_linear_bwd_delta": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P, _P, _P, _P]),
     "ito_dfp16_linear_wgrad": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P, _P, _P, _P]),
     "ito_dfp16_update": (_I, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P]),
+    "ito_dfp16_from_float": (_I, [_P, _I64, _P, _P, _P, _P]),
+    "ito_dfp16_to_float": (_I, [_P, _P, _I64, _P, _P]),
+    "ito_dfp16_linear_fwd_f32": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P, _P]),
     "ito_dfp16_model_create": (_I, [_P, _I, _I, _I32, _I32, ctypes.POINTER(_P)]),
     "ito_dfp16_model_destroy": (_I, [_P]),
     "ito_dfp16_model_set_weights": (_I, [_P, _I, _P, _I, _P]),
@@ -422,6 +425,37 @@ def ito_dfp16_update(W, g, exp_g, exp_w, eta, stream=None):
     _check(_lib.ito_dfp16_update(_ptr(W), _ptr(g), _ptr(exp_g), W.numel(), exp_w, eta, _ptr(k), _ptr(nz),
                                  _stream(stream)))
     return k, nz
+
+
+def ito_dfp16_from_float(f, stream=None):
+    """float32 device tensor -> (int16 mantissas, device int32 [1] exponent)."""
+    torch = _torch()
+    mant = torch.empty(f.shape, dtype=torch.int16, device="cuda")
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bits = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(_lib.ito_dfp16_from_float(_ptr(f), f.numel(), _ptr(bits), _ptr(mant), _ptr(e), _stream(stream)))
+    return mant, e
+
+
+def ito_dfp16_to_float(mant, exp, stream=None):
+    torch = _torch()
+    f = torch.empty(mant.shape, dtype=torch.float32, device="cuda")
+    _check(_lib.ito_dfp16_to_float(_ptr(mant), _ptr(exp), mant.numel(), _ptr(f), _stream(stream)))
+    return f
+
+
+def ito_dfp16_linear_fwd_f32(x, exp_x, W, exp_w, stream=None):
+    """-> (p64 int64 [B][OC], y float32 [B][OC])"""
+    torch = _torch()
+    B, IC = x.shape
+    OC = W.shape[0]
+    p64 = torch.empty((B, OC), dtype=torch.int64, device="cuda")
+    y = torch.empty((B, OC), dtype=torch.float32, device="cuda")
+    mx = torch.zeros(1, dtype=torch.int64, device="cuda")
+    ws, n = _dfp_ws(B, IC, OC)
+    _check(_lib.ito_dfp16_linear_fwd_f32(_ptr(x), _ptr(exp_x), _ptr(W), _ptr(exp_w), B, IC, OC, _aligned256(ws), n,
+                                         _ptr(p64), _ptr(mx), _ptr(y), _stream(stream)))
+    return p64, y
 
 
 class Dfp16Model:

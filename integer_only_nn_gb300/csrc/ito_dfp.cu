@@ -458,6 +458,97 @@ int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp down launch: %s", cudaGetErrorString(e));
 }
 
+// --------------------------------------------------- float <-> DFP16
+
+// 2^k as a double (k in [-1022, 1023]): scaling by it is exact, so converting the
+// product to float or int rounds once, like ldexpf
+__device__ __forceinline__ double pow2d(int k) { return __longlong_as_double((long long)(k + 1023) << 52); }
+
+// max |f| as float bits (non-negative floats order like their bit patterns)
+__global__ void k_absmax_f32(const float* __restrict__ f, int64_t n, unsigned int* __restrict__ d_bits)
+{
+    uint32_t mx = 0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        mx = max(mx, __float_as_uint(f[i]) & 0x7fffffffu);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_bits, mx);
+}
+
+// frexp exponent e of a positive finite float given by its bits: m = frac * 2^e, frac in [0.5, 1)
+__device__ __forceinline__ int frexp_exponent(uint32_t bits)
+{
+    const int ef = (int)(bits >> 23);
+    if (ef != 0) return ef - 126;
+    const uint32_t mant = bits & 0x7fffffu;             // subnormal: mant * 2^-149
+    return (32 - __clz(mant)) - 149;
+}
+
+// section 3.1: the shared exponent comes from the absolute maximum's exponent:
+// E = e - 15 so that |f| * 2^-E < 2^15; mantissas round to nearest even, saturate
+__global__ void k_dfp_from_float(const float* __restrict__ f, int64_t n, const unsigned int* __restrict__ d_bits,
+                                 int16_t* __restrict__ out, int32_t* __restrict__ d_exp, int* __restrict__ err)
+{
+    const uint32_t bits = *d_bits;
+    const int E = bits ? frexp_exponent(bits) - 15 : 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *d_exp = E;
+        if (bits >= 0x7f800000u) raise_device_error(err, ITO_ERR_ARG);      // inf or nan in the input
+        if (E < -128 || E > 127) raise_device_error(err, ITO_ERR_EXPONENT);
+    }
+    const double sc = pow2d(-E);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        int q = __double2int_rn((double)f[i] * sc);
+        q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
+        out[i] = (int16_t)q;
+    }
+}
+
+__global__ void k_dfp_to_float(const int16_t* __restrict__ m, int64_t n, const int32_t* __restrict__ d_exp,
+                               float* __restrict__ out)
+{
+    const double sc = pow2d(*d_exp);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = __double2float_rn((double)m[i] * sc);
+}
+
+// float(P) (round to nearest even) times 2^(Ea + Eb), one more rounding at most
+__global__ void k_p64_to_float(const int64_t* __restrict__ P, int64_t n, const int32_t* __restrict__ d_ea,
+                               const int32_t* __restrict__ d_eb, float* __restrict__ out)
+{
+    const double sc = pow2d(*d_ea + *d_eb);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = __double2float_rn((double)__ll2float_rn(P[i]) * sc);
+}
+
+int launch_dfp_from_float(const float* f, int64_t n, unsigned int* d_bits, int16_t* out, int32_t* d_exp, cudaStream_t s)
+{
+    if (n < 1) return ITO_OK;
+    int* err = device_error_word();
+    if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
+    if (cudaMemsetAsync(d_bits, 0, sizeof(unsigned int), s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset");
+    k_absmax_f32<<<launch_grid_blocks(n, 256), 256, 0, s>>>(f, n, d_bits);
+    k_dfp_from_float<<<launch_grid_blocks(n, 256), 256, 0, s>>>(f, n, d_bits, out, d_exp, err);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "float->dfp launch: %s", cudaGetErrorString(e));
+}
+
+int launch_dfp_to_float(const int16_t* m, int64_t n, const int32_t* d_exp, float* out, cudaStream_t s)
+{
+    if (n < 1) return ITO_OK;
+    k_dfp_to_float<<<launch_grid_blocks(n, 256), 256, 0, s>>>(m, n, d_exp, out);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp->float launch: %s", cudaGetErrorString(e));
+}
+
+int launch_p64_to_float(const int64_t* P, int64_t n, const int32_t* d_ea, const int32_t* d_eb, float* out,
+                        cudaStream_t s)
+{
+    if (n < 1) return ITO_OK;
+    k_p64_to_float<<<launch_grid_blocks(n, 256), 256, 0, s>>>(P, n, d_ea, d_eb, out);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "p64->float launch: %s", cudaGetErrorString(e));
+}
+
 // ----------------------------------------------------------------- update
 
 __global__ void k_dfp_update(int16_t* __restrict__ W, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,

@@ -189,6 +189,42 @@ int ito_dfp16_linear_wgrad(const int16_t* delta, const int32_t* d_exp_delta, con
                            nullptr, 0, d_exp_g, d_rs, s);
 }
 
+int ito_dfp16_from_float(const float* f, int64_t n, uint32_t* d_max_bits, int16_t* mant, int32_t* d_exp,
+                         void* stream)
+{
+    if (!f || !d_max_bits || !mant || !d_exp) return set_error(ITO_ERR_ARG, "NULL pointer");
+    if (n < 1) return set_error(ITO_ERR_SHAPE, "n must be >= 1");
+    return launch_dfp_from_float(f, n, d_max_bits, mant, d_exp, static_cast<cudaStream_t>(stream));
+}
+
+int ito_dfp16_to_float(const int16_t* mant, const int32_t* d_exp, int64_t n, float* f, void* stream)
+{
+    if (!f || !mant || !d_exp) return set_error(ITO_ERR_ARG, "NULL pointer");
+    if (n < 1) return set_error(ITO_ERR_SHAPE, "n must be >= 1");
+    return launch_dfp_to_float(mant, n, d_exp, f, static_cast<cudaStream_t>(stream));
+}
+
+int ito_dfp16_linear_fwd_f32(const int16_t* x, const int32_t* d_exp_x, const int16_t* W, const int32_t* d_exp_w,
+                             int B, int IC, int OC, void* workspace, size_t workspace_bytes, int64_t* p64,
+                             uint64_t* d_max, float* y, void* stream)
+{
+    ITO_TRY(dfp_check(x, W, p64, y, B, IC, OC, workspace, workspace_bytes));
+    if (!d_exp_x || !d_exp_w || !d_max) return set_error(ITO_ERR_ARG, "NULL scalar pointer");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t ld = pad8(IC);
+    Planes xa = planes_at(workspace, (size_t)B * ld);
+    Planes wb = planes_at(static_cast<char*>(workspace) + dws_a(B, IC, OC), (size_t)OC * ld);
+    ITO_TRY(launch_i16_to_limbs(x, B, IC, xa.h, xa.l, ld, s));
+    ITO_TRY(launch_i16_to_limbs(W, OC, IC, wb.h, wb.l, ld, s));
+    if (cudaMemsetAsync(d_max, 0, 8, s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset");
+    DfpGemmPlan g;
+    ITO_TRY(dfp_gemm_plan(&g, Bf16View{xa.h, B, IC, ld}, Bf16View{xa.l, B, IC, ld}, false, Bf16View{wb.h, OC, IC, ld},
+                          Bf16View{wb.l, OC, IC, ld}, false, B, OC, IC, p64, OC,
+                          reinterpret_cast<unsigned long long*>(d_max)));
+    ITO_TRY(dfp_gemm_run(g, s));
+    return launch_p64_to_float(p64, (int64_t)B * OC, d_exp_x, d_exp_w, y, s);
+}
+
 int ito_dfp16_update(int16_t* W, const int16_t* g, const int32_t* d_exp_g, int64_t n, int32_t exp_w, int32_t eta,
                      int32_t* d_k, uint32_t* d_nonzero, void* stream)
 {

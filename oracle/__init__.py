@@ -89,6 +89,9 @@ def lib():
             "ora_dfp_linear_wgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
             "ora_dfp_down": (i32, [P, i64, i32, P, P]),
             "ora_dfp_update": (i64, [P, P, i64, i32]),
+            "ora_dfp_from_float": (i32, [P, i64, P]),
+            "ora_dfp_to_float": (None, [P, i64, i32, P]),
+            "ora_p64_to_float": (None, [P, i64, i32, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -406,6 +409,28 @@ def dfp_down(P, exp_in: int, target_bits: int = DFP_BITS):
     if not -128 <= e <= 127:
         raise OverflowError("DFP exponent %d outside int8" % e)
     return out, e, rs, m.value
+
+
+def dfp_from_float(f):
+    """float32 tensor -> (int16 mantissas, shared exponent)."""
+    f = _c(f, np.float32)
+    out = np.empty(f.shape, np.int16)
+    e = lib().ora_dfp_from_float(_p(f), f.size, _p(out))
+    return out, e
+
+
+def dfp_to_float(m, e: int):
+    m = _c(m, np.int16)
+    out = np.empty(m.shape, np.float32)
+    lib().ora_dfp_to_float(_p(m), m.size, e, _p(out))
+    return out
+
+
+def p64_to_float(P, e: int):
+    P = _c(P, np.int64)
+    out = np.empty(P.shape, np.float32)
+    lib().ora_p64_to_float(_p(P), P.size, e, _p(out))
+    return out
 
 
 def dfp_update(W, Gm, k: int):

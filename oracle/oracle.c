@@ -32,6 +32,7 @@
  *
  * Readings where the pages leave a step open are stated at each function.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -620,6 +621,49 @@ int32_t ora_dfp_down(const int64_t *P, int64_t n, int32_t target_bits, int16_t *
         out[i] = (int16_t)ora_sat16(ora_rhu(P[i], rs));
     if (max_out) *max_out = m;
     return rs;
+}
+
+/* [DFP] 3.1: converting a floating-point tensor to DFP-16 derives the shared
+ * exponent from the exponent of its absolute maximum. Reading: with
+ * max|f| = frac * 2^e (frac in [0.5, 1)), E = e - 15, so every mantissa
+ * f * 2^-E is below 2^15 in magnitude; mantissas are rounded to nearest, ties
+ * to even (the IEEE default), and saturated to [-32767, 32767]. An all-zero
+ * tensor gets exponent 0. Inputs must be finite. Returns E (the caller checks
+ * the int8 range). */
+int32_t ora_dfp_from_float(const float *f, int64_t n, int16_t *out)
+{
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; i++) {
+        float a = fabsf(f[i]);
+        if (!(a <= 3.4028235e38f)) ora_fail("non-finite input");
+        if (a > m) m = a;
+    }
+    int e = 0;
+    if (m > 0.0f) frexpf(m, &e);
+    int32_t E = m > 0.0f ? e - 15 : 0;
+    for (int64_t i = 0; i < n; i++) {
+        float v = ldexpf(f[i], -E);          /* exact: a power-of-two scaling below 2^15 */
+        long q = lrintf(v);                  /* round to nearest, ties to even */
+        if (q > 32767) q = 32767;
+        if (q < -32767) q = -32767;
+        out[i] = (int16_t)q;
+    }
+    return E;
+}
+
+/* DFP-16 to float: f = i * 2^E ([DFP] 3.1), one rounding at most (exact
+ * whenever the result is a normal or exactly representable subnormal float). */
+void ora_dfp_to_float(const int16_t *m, int64_t n, int32_t E, float *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = ldexpf((float)m[i], E);
+}
+
+/* FP32 output of a DFP contraction ([DFP] section 4: the kernels produce FP32
+ * outputs): the exact int64 sum P rounded to float (to nearest, ties to even),
+ * then scaled by 2^(Ea + Eb). */
+void ora_p64_to_float(const int64_t *P, int64_t n, int32_t E, float *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = ldexpf((float)P[i], E);
 }
 
 /* Integer SGD on a DFP-16 weight tensor with a fixed exponent E_W, learning

@@ -171,3 +171,30 @@ def test_dfp_model_100_steps_digests():
         bad = [k for k, v in r.items() if k in d and
                (digest(v) if isinstance(v, np.ndarray) else int(v)) != d[k]]
         assert not bad, "step %d differs from the oracle in %s" % (t, bad)
+
+
+def test_dfp_from_to_float_parity(ito):
+    import torch
+    for scale in (1e-30, 1e-3, 1.0, 3.7e5, 1e30):
+        f = (rng.standard_normal(10001) * scale).astype(np.float32)
+        f[5] = 0.0
+        f[6] = np.float32(1e-42) * np.sign(scale)        # a subnormal input
+        mant, e = ito.ito_dfp16_from_float(torch.from_numpy(f).cuda())
+        m_ref, e_ref = O.dfp_from_float(f)
+        assert int(_h(e)[0]) == e_ref and np.array_equal(_h(mant), m_ref), scale
+        back = ito.ito_dfp16_to_float(mant, e)
+        assert np.array_equal(_h(back).view(np.int32), O.dfp_to_float(m_ref, e_ref).view(np.int32))
+    assert ito.ito_get_error() == 0
+
+
+def test_dfp_linear_fwd_f32_parity(ito):
+    B, IC, OC = 130, 1025, 70
+    x, W = i16((B, IC)), i16((OC, IC))
+    p64, y = ito.ito_dfp16_linear_fwd_f32(_dev(x), ito._i32dev(-12), _dev(W), ito._i32dev(-17))
+    P = O.dfp_linear_fwd(x, W)
+    assert np.array_equal(_h(p64), P)
+    assert np.array_equal(_h(y).view(np.int32), O.p64_to_float(P, -29).view(np.int32))
+    # the FP32 output re-quantised for the next layer (float -> DFP16)
+    mant, e = ito.ito_dfp16_from_float(y)
+    m_ref, e_ref = O.dfp_from_float(O.p64_to_float(P, -29))
+    assert int(_h(e)[0]) == e_ref and np.array_equal(_h(mant), m_ref)

@@ -407,3 +407,34 @@ def test_offset_grad_and_update():
     assert on.tolist() == [-2, np.iinfo(np.int32).max, 7]       # +96 saturates at INT32_MAX
     on, *_ = O.offset_update(np.array([np.iinfo(np.int32).min + 1], np.int32), np.array([100], np.int32))
     assert on.tolist() == [np.iinfo(np.int32).min]
+
+
+# ------------------------------------------------------- float <-> DFP16
+
+def test_dfp_from_float_hand_cases():
+    m, e = O.dfp_from_float(np.array([1.0, -0.5, 0.75, 3.0], np.float32))
+    assert e == -13 and m.tolist() == [8192, -4096, 6144, 24576]        # 3.0 = 0.75 * 2^2
+    assert O.dfp_to_float(m, e).tolist() == [1.0, -0.5, 0.75, 3.0]
+    # max 32768 = 0.5 * 2^16: E = 1; x / 2 rounds to nearest, ties to even
+    m, e = O.dfp_from_float(np.array([32768.0, 3.0, 5.0, 7.0, -5.0, -7.0], np.float32))
+    assert e == 1 and m.tolist() == [16384, 2, 2, 4, -2, -4]
+    # just below 2^15 with E = 0: 32767.75 rounds to 32768 and saturates
+    m, e = O.dfp_from_float(np.array([32767.75, -1.25], np.float32))
+    assert e == 0 and m.tolist() == [32767, -1]
+    m, e = O.dfp_from_float(np.zeros(5, np.float32))
+    assert e == 0 and not m.any()
+
+
+def test_dfp_from_float_error_bound():
+    f = (rng.standard_normal(5000) * 1e-3).astype(np.float32)
+    m, e = O.dfp_from_float(f)
+    back = m.astype(np.float64) * 2.0 ** e
+    assert np.abs(back - f.astype(np.float64)).max() <= 2.0 ** (e - 1)
+    assert np.abs(m).max() >= 16384                  # the exponent uses the full 15 bits
+
+
+def test_p64_to_float_rounds_once_then_scales():
+    P = np.array([(1 << 24) + 1, (1 << 24) + 3, -(1 << 40) - 1, 7], np.int64)
+    out = O.p64_to_float(P, -3)
+    # 2^24 + 1 is a tie between 2^24 and 2^24 + 2: to even (2^24); 2^24 + 3 -> 2^24 + 4
+    assert out.tolist() == [2.0 ** 21, (2.0 ** 24 + 4) / 8, -(2.0 ** 37), 7 / 8]
