@@ -184,6 +184,76 @@ int ito_top_error(const int8_t *logits, const int32_t *labels, int B, int C, int
                   int8_t *delta, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Single-layer operations: 3x3 Conv2D (+ReLU) and global integer pooling
+ * ("Integer On-Device Training: Overview", section 7: Conv2D and Conv2D+ReLU
+ * layers, dense, groups = 1, dilation = 1). Activations are NHWC, conv
+ * weights [OC][3][3][IC] (the channel-last layout of the TiGrIS "Compilation
+ * Pipeline" page, emission stage); padding is 1, so OH = (H - 1) / stride + 1
+ * and OW = (W - 1) / stride + 1. A conv is the Linear contraction over the
+ * im2col patch matrix [B*OH*OW][9*IC] in (kh, kw, ic) order; sums are exact
+ * as for the Linear operations.
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of device workspace any of ito_conv2d_fwd / _bwd_delta / _wgrad
+ * needs for these sizes (0 on invalid sizes): bf16 patch, weight and delta
+ * copies, the int32 patch-space delta, split-K partials and one scratch word. */
+size_t ito_conv2d_workspace_size(int B, int H, int W, int IC, int OC, int stride);
+
+/* Forward 3x3 conv + requantisation:
+ *   y32[b][oh][ow][oc] = sum_{kh,kw,ic} x[b][oh*stride-1+kh][ow*stride-1+kw][ic] * Wt[oc][kh][kw][ic]
+ *                        (taps outside the input are 0)
+ *   *d_max, *d_shift, y as in ito_linear_fwd (ReLU when relu != 0).
+ * x: int8 [B][H][W][IC]; Wt: int8 [OC][3][3][IC]; y32: int32 [B][OH][OW][OC];
+ * y: int8 [B][OH][OW][OC]. workspace: device, 256-byte aligned, at least
+ * ito_conv2d_workspace_size() bytes.
+ * Errors: ITO_ERR_ARG (null pointer, workspace misaligned or too small),
+ * ITO_ERR_SHAPE (a size < 1, stride outside 1..4, IC above 2^16, OC above
+ * 2^20, or B*OH*OW above 2^20). */
+int ito_conv2d_fwd(const int8_t *x, const int8_t *Wt, int B, int H, int W, int IC, int OC, int stride,
+                   int relu, ito_niti_params p, void *workspace, size_t workspace_bytes, int32_t *y32,
+                   uint32_t *d_max, int32_t *d_shift, int8_t *y, void *stream);
+
+/* Delta propagation of a 3x3 conv, gated by the ReLU of the layer below:
+ *   d32[b][ih][iw][ic] = sum over (oh, ow, kh, kw) with oh*stride-1+kh = ih and
+ *                        ow*stride-1+kw = iw of delta[b][oh][ow][oc] * Wt[oc][kh][kw][ic]
+ *                        (the transpose of the forward; int32, exact)
+ *   *d_max = max |d32|; *d_shift and delta_prev as in ito_linear_bwd_delta.
+ * delta: int8 [B][OH][OW][OC]; Wt: the weights before this step's update;
+ * a_prev: int8 [B][H][W][IC] or NULL; d32: int32 [B][H][W][IC];
+ * delta_prev: int8 [B][H][W][IC]. Errors as ito_conv2d_fwd. */
+int ito_conv2d_bwd_delta(const int8_t *delta, const int8_t *Wt, const int8_t *a_prev, int B, int H,
+                         int W, int IC, int OC, int stride, ito_niti_params p, void *workspace,
+                         size_t workspace_bytes, int32_t *d32, uint32_t *d_max, int32_t *d_shift,
+                         int8_t *delta_prev, void *stream);
+
+/* Weight gradient of a 3x3 conv, summed over the batch and the output
+ * positions:
+ *   G[oc][kh][kw][ic] = sum_{b,oh,ow} delta[b][oh][ow][oc] * x[b][oh*stride-1+kh][ow*stride-1+kw][ic]
+ *   *d_max = max |G|
+ * delta: int8 [B][OH][OW][OC]; x: int8 [B][H][W][IC] (the layer input);
+ * G: int32 [OC][3][3][IC]. Errors as ito_conv2d_fwd. */
+int ito_conv2d_wgrad(const int8_t *delta, const int8_t *x, int B, int H, int W, int IC, int OC,
+                     int stride, void *workspace, size_t workspace_bytes, int32_t *G, uint32_t *d_max,
+                     void *stream);
+
+/* Global integer sum pooling + requantisation without ReLU (no division: the
+ * NITI shift that follows rescales the sum):
+ *   P32[b][c] = sum_pos a[b][pos][c];  *d_max = max |P32|;
+ *   *d_shift = max(0, bitlen(*d_max) - p.target_bits);
+ *   pa[b][c] = sat_int8(round-half-up(P32 >> shift))
+ * a: int8 [B][HW][C] (NHWC with HW = H*W); P32: int32 [B][C]; pa: int8 [B][C].
+ * Errors: ITO_ERR_ARG (null pointer), ITO_ERR_SHAPE (a size < 1, HW above 2^24). */
+int ito_gap_fwd(const int8_t *a, int B, int HW, int C, ito_niti_params p, int32_t *P32,
+                uint32_t *d_max, int32_t *d_shift, int8_t *pa, void *stream);
+
+/* Backward of the pooling: the pooled delta is broadcast to every position,
+ * gated by the ReLU of the pooled layer (no rescale):
+ *   delta[b][pos][c] = (a[b][pos][c] > 0) ? dP[b][c] : 0
+ * dP: int8 [B][C]; a: int8 [B][HW][C]; delta: int8 [B][HW][C].
+ * Errors: ITO_ERR_ARG, ITO_ERR_SHAPE (a size < 1). */
+int ito_gap_bwd(const int8_t *dP, const int8_t *a, int B, int HW, int C, int8_t *delta, void *stream);
+
+/* ------------------------------------------------------------------------
  * Models: a sequential stack of trainable layers ("Integer On-Device
  * Training: Overview", section 4: INT_LAYERS[], an array of layer descriptors
  * with mutable int8 weights; INTODT_Forward / INTODT_Backward / INTODT_Infer).

@@ -56,6 +56,13 @@ _SIGS = {
     "ito_linear_wgrad": (_I, [_P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P]),
     "ito_niti_update": (_I, [_P, _P, _I64, _P, NitiParams, _P, _P, _P, _P]),
     "ito_top_error": (_I, [_P, _P, _I, _I, _I32, _P, _P]),
+    "ito_conv2d_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "ito_conv2d_fwd": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, NitiParams, _P, _SZ, _P, _P, _P, _P, _P]),
+    "ito_conv2d_bwd_delta": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, NitiParams, _P, _SZ, _P, _P, _P, _P,
+                                  _P]),
+    "ito_conv2d_wgrad": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P, _P]),
+    "ito_gap_fwd": (_I, [_P, _I, _I, _I, NitiParams, _P, _P, _P, _P, _P]),
+    "ito_gap_bwd": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "ito_model_create": (_I, [ctypes.POINTER(LayerDesc), _I, _I, NitiParams, _I32, ctypes.POINTER(_P)]),
     "ito_model_create_ex": (_I, [ctypes.POINTER(LayerDesc), _I, _I, NitiParams, _I32, ctypes.POINTER(ModelOptions),
                                  ctypes.POINTER(_P)]),
@@ -234,6 +241,91 @@ def ito_top_error(logits, labels, target_mag=64, stream=None):
     B, C = logits.shape
     d = torch.empty((B, C), dtype=torch.int8, device=logits.device)
     _check(_lib.ito_top_error(_ptr(logits), _ptr(labels), B, C, target_mag, _ptr(d), _stream(stream)))
+    return d
+
+
+def _conv_ws(B, H, W, IC, OC, stride, device):
+    torch = _torch()
+    n = _lib.ito_conv2d_workspace_size(B, H, W, IC, OC, stride)
+    if n == 0:
+        raise ItoError(ITO_ERR_SHAPE, "invalid conv sizes")
+    return torch.empty(n + 256, dtype=torch.uint8, device=device), n
+
+
+def _conv_out(n, stride):
+    return (n - 1) // stride + 1
+
+
+def ito_conv2d_fwd(x, Wt, stride, relu, p=None, stream=None):
+    """x int8 [B][H][W][IC], Wt int8 [OC][3][3][IC] -> (y32 int32 [B][OH][OW][OC],
+    d_max, d_shift, y int8 [B][OH][OW][OC])"""
+    torch = _torch()
+    B, H, W, IC = x.shape
+    OC = Wt.shape[0]
+    OH, OW = _conv_out(H, stride), _conv_out(W, stride)
+    dev = x.device
+    y32 = torch.empty((B, OH, OW, OC), dtype=torch.int32, device=dev)
+    y = torch.empty((B, OH, OW, OC), dtype=torch.int8, device=dev)
+    mx = torch.zeros(1, dtype=torch.int32, device=dev)
+    sh = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws, n = _conv_ws(B, H, W, IC, OC, stride, dev)
+    _check(_lib.ito_conv2d_fwd(_ptr(x), _ptr(Wt), B, H, W, IC, OC, stride, int(relu), p or params(),
+                               _aligned256(ws), n, _ptr(y32), _ptr(mx), _ptr(sh), _ptr(y), _stream(stream)))
+    return y32, mx, sh, y
+
+
+def ito_conv2d_bwd_delta(delta, Wt, a_prev, in_hw, stride, p=None, stream=None):
+    """delta int8 [B][OH][OW][OC], a_prev int8 [B][H][W][IC] or None ->
+    (d32 int32 [B][H][W][IC], d_max, d_shift, delta_prev int8 [B][H][W][IC])"""
+    torch = _torch()
+    B, OC = delta.shape[0], delta.shape[3]
+    IC = Wt.shape[3]
+    H, W = in_hw
+    dev = delta.device
+    d32 = torch.empty((B, H, W, IC), dtype=torch.int32, device=dev)
+    dp = torch.empty((B, H, W, IC), dtype=torch.int8, device=dev)
+    mx = torch.zeros(1, dtype=torch.int32, device=dev)
+    sh = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws, n = _conv_ws(B, H, W, IC, OC, stride, dev)
+    _check(_lib.ito_conv2d_bwd_delta(_ptr(delta), _ptr(Wt), _ptr(a_prev), B, H, W, IC, OC, stride, p or params(),
+                                     _aligned256(ws), n, _ptr(d32), _ptr(mx), _ptr(sh), _ptr(dp), _stream(stream)))
+    return d32, mx, sh, dp
+
+
+def ito_conv2d_wgrad(delta, x, stride, stream=None):
+    """-> (G int32 [OC][3][3][IC], d_max)"""
+    torch = _torch()
+    B, H, W, IC = x.shape
+    OC = delta.shape[3]
+    dev = x.device
+    G = torch.empty((OC, 3, 3, IC), dtype=torch.int32, device=dev)
+    mx = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws, n = _conv_ws(B, H, W, IC, OC, stride, dev)
+    _check(_lib.ito_conv2d_wgrad(_ptr(delta), _ptr(x), B, H, W, IC, OC, stride, _aligned256(ws), n, _ptr(G),
+                                 _ptr(mx), _stream(stream)))
+    return G, mx
+
+
+def ito_gap_fwd(a, p=None, stream=None):
+    """a int8 [B][H][W][C] -> (P32 int32 [B][C], d_max, d_shift, pa int8 [B][C])"""
+    torch = _torch()
+    B, H, W, C = a.shape
+    dev = a.device
+    P = torch.empty((B, C), dtype=torch.int32, device=dev)
+    pa = torch.empty((B, C), dtype=torch.int8, device=dev)
+    mx = torch.zeros(1, dtype=torch.int32, device=dev)
+    sh = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(_lib.ito_gap_fwd(_ptr(a), B, H * W, C, p or params(), _ptr(P), _ptr(mx), _ptr(sh), _ptr(pa),
+                            _stream(stream)))
+    return P, mx, sh, pa
+
+
+def ito_gap_bwd(dP, a, stream=None):
+    """dP int8 [B][C], a int8 [B][H][W][C] -> delta int8 [B][H][W][C]"""
+    torch = _torch()
+    B, H, W, C = a.shape
+    d = torch.empty(a.shape, dtype=torch.int8, device=a.device)
+    _check(_lib.ito_gap_bwd(_ptr(dP), _ptr(a), B, H * W, C, _ptr(d), _stream(stream)))
     return d
 
 

@@ -139,13 +139,50 @@ __global__ void k_col2im_v8(const int32_t* __restrict__ Dcol, int B, int H, int 
     if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
 }
 
+// one thread per input-space element (any IC)
+__global__ void k_col2im_1(const int32_t* __restrict__ Dcol, int B, int H, int W, int IC, int OH, int OW,
+                           int stride, int32_t* __restrict__ D, uint32_t* __restrict__ d_max)
+{
+    const int64_t ldc = 9 * (int64_t)IC;
+    const int64_t n = (int64_t)B * H * W * IC;
+    uint32_t mx = 0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int ic = (int)(i % IC);
+        const int64_t pix = i / IC;
+        const int iw = (int)(pix % W);
+        const int ih = (int)((pix / W) % H);
+        const int b = (int)(pix / ((int64_t)W * H));
+        int32_t acc = 0;
+        for (int kh = 0; kh < 3; ++kh) {
+            const int th = ih + 1 - kh;
+            if (th < 0 || th % stride) continue;
+            const int oh = th / stride;
+            if (oh >= OH) continue;
+            for (int kw = 0; kw < 3; ++kw) {
+                const int tw = iw + 1 - kw;
+                if (tw < 0 || tw % stride) continue;
+                const int ow = tw / stride;
+                if (ow >= OW) continue;
+                acc += __ldg(Dcol + (((int64_t)b * OH + oh) * OW + ow) * ldc + (kh * 3 + kw) * IC + ic);
+            }
+        }
+        D[i] = acc;
+        mx = max(mx, abs_u32(acc));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+}
+
 int launch_col2im(const int32_t* Dcol, int B, int H, int W, int IC, int OH, int OW, int stride, int32_t* D,
                   uint32_t* d_max, cudaStream_t s)
 {
-    if (IC % 8 != 0 || !aligned(Dcol, 16) || !aligned(D, 16))
-        return set_error(ITO_ERR_UNSUPPORTED, "col2im needs IC % 8 == 0");
-    const int64_t n = (int64_t)B * H * W * (IC / 8);
-    k_col2im_v8<<<launch_grid_blocks(n, 256), 256, 0, s>>>(Dcol, B, H, W, IC, OH, OW, stride, D, d_max);
+    if (IC % 8 == 0 && aligned(Dcol, 16) && aligned(D, 16)) {
+        const int64_t n = (int64_t)B * H * W * (IC / 8);
+        k_col2im_v8<<<launch_grid_blocks(n, 256), 256, 0, s>>>(Dcol, B, H, W, IC, OH, OW, stride, D, d_max);
+    } else {
+        const int64_t n = (int64_t)B * H * W * IC;
+        k_col2im_1<<<launch_grid_blocks(n, 256), 256, 0, s>>>(Dcol, B, H, W, IC, OH, OW, stride, D, d_max);
+    }
     return launched("col2im");
 }
 

@@ -332,7 +332,8 @@ template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
-               int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max, int* __restrict__ err)
+               int group, int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max,
+               int* __restrict__ err)
 {
     using Cfg = Tc2Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
     const bool leader = rank == 0;
     const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
-    const TileSched sched{(M + 2 * BM - 1) / (2 * BM), (N + BN - 1) / BN, 16};
+    const TileSched sched{(M + 2 * BM - 1) / (2 * BM), (N + BN - 1) / BN, group};
     const int num_tiles = sched.num_m * sched.num_n;
     const int num_kb = (K + BK - 1) / BK;
     const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
@@ -722,7 +723,7 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.use_tma_store, p.M, p.N, p.K,
-                                       p.chunk_kb, p.C, p.ldc, p.d_max, p.err);
+                                       p.chunk_kb, p.group, p.C, p.ldc, p.d_max, p.err);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "pair gemm launch: %s", cudaGetErrorString(e));
     return ITO_OK;
 }
@@ -789,6 +790,12 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
         p->split_stride = (int64_t)M * ldc;
     }
     p->pair = pair_env != 0 && M >= 256 && N >= 256 && p->splits == 1;
+    // tiles are rastered in groups of `group` row tiles; ITO_GEMM_GROUP overrides (tuning)
+    static const int group_env = [] {
+        const char* v = getenv("ITO_GEMM_GROUP");
+        return v ? atoi(v) : 0;
+    }();
+    p->group = group_env > 0 ? group_env : 16;
     int r = make_map_bf16(&p->mapA, A, a_mn ? 64 : 128);
     if (r) return r;
     // the pair kernel loads half of a 256-wide B tile per CTA

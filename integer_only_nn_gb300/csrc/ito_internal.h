@@ -35,6 +35,7 @@ struct GemmPlan {
     CUtensorMap mapA, mapB, mapC;
     int use_tma_store;
     int pair;   // CTA-pair (cta_group::2) kernel
+    int group;  // row tiles per raster group (L2 reuse)
     int M, N, K, bn, chunk_kb;
     int splits, kb_per_split;     // split-K: slices of kb_per_split K blocks (splits == 1: none)
     int32_t* split_ws;            // [splits][M][ldc] int32 partials
