@@ -168,7 +168,15 @@ def oracle_step(w, weights, x, labels):
         return O.mlp_step(weights, x, labels, route="loops")
     if w.kind == "cnn":
         return O.cnn_step(weights, x, labels, w.convs)
-    return O.dfp16_step(weights, w.exp_w, x, w.exp_x, route="loops")
+    if w.apt is not None:
+        # the first step of an adaptive-precision run: weights at the initial precision
+        ws, ew = [], []
+        for W in weights:
+            Wk, de = O.dfp_set_bits(W, 16, w.apt.k_init)
+            ws.append(Wk)
+            ew.append(w.exp_w + de)
+        return O.dfp16_step(ws, ew, x, w.exp_x, eta=w.eta, route="loops", wbits=[w.apt.k_init] * len(ws))
+    return O.dfp16_step(weights, w.exp_w, x, w.exp_x, eta=w.eta, route="loops")
 
 
 def cpu_baseline(w, sample_batch):
@@ -408,14 +416,27 @@ def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local):
     import oracle as O
     import seeded_inputs as si
     stream = torch.cuda.current_stream()
-    model = ito.Dfp16Model(list(w.dims), w.batch, w.exp_w, O.DFP_ETA)
+    model = ito.Dfp16Model(list(w.dims), w.batch, w.exp_w, w.eta)
     for l, W in enumerate(si.make_weights(w)):
         model.set_weights(l, W)
     xs = [torch.from_numpy(si.make_batch(w, t)[0]).cuda() for t in range(2)]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     K = args.steps
+    apt = w.apt
+    if apt is not None:
+        # adaptive precision (Algorithm 2): the epoch-end adjustment, with its host
+        # synchronisation, runs inside the timed window of the step that ends an epoch
+        model.apt_enable(apt.k_init, apt.k_min, apt.k_max, apt.t_min, apt.t_max, apt.eval_every)
+    step_no = [0]
+
+    def one_step(x):
+        model.train_step(x, w.exp_x)
+        if apt is not None and step_no[0] % apt.epoch == apt.epoch - 1:
+            model.apt_epoch_end()
+        step_no[0] += 1
+
     for i in range(args.warmup):
-        model.train_step(xs[i % 2], w.exp_x)
+        one_step(xs[i % 2])
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -426,7 +447,7 @@ def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local):
     for k in range(K):
         flush.fill_(k & 0xFF)
         starts[k].record(stream)
-        model.train_step(xs[k % 2], w.exp_x)
+        one_step(xs[k % 2])
         ends[k].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -440,9 +461,13 @@ def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local):
     line = {"metric": METRIC, "value": world * w.batch * K / (total_ms / 1000.0), "unit": "samples/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int16 (DFP16)",
-            "data": "synthetic", "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims)},
+            "data": "synthetic", "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims), "eta": w.eta},
             "int16_tops": ops * world * K / (total_ms / 1000.0) / 1e12,
             "executed_limb_tops": 4 * ops * world * K / (total_ms / 1000.0) / 1e12, "clocks": clk}
+    if apt is not None:
+        line["config"]["apt"] = {"k_init": apt.k_init, "k_min": apt.k_min, "k_max": apt.k_max, "t_min": apt.t_min,
+                                 "t_max": str(apt.t_max), "epoch_steps": apt.epoch, "eval_every": apt.eval_every}
+        line["apt_bits_after"] = [model.precision(l)[0] for l in range(model.n_layers)]
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)

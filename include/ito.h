@@ -477,12 +477,14 @@ int ito_dfp16_linear_fwd_f32(const int16_t *x, const int32_t *d_exp_x, const int
 typedef struct ito_dfp16_model ito_dfp16_model;
 
 /* A stack of DFP16 Linear layers dims[0] -> dims[1] -> ... -> dims[n_layers]
- * (no ReLU), weights with the fixed shared exponent exp_w, integer SGD rate
- * 2^-eta. Owns all its device memory. */
+ * (no ReLU), every layer's weights 16-bit mantissas with exponent exp_w
+ * (changed per layer only by the precision calls below), integer SGD rate
+ * 2^-eta on the batch-summed gradient. Owns all its device memory. */
 int ito_dfp16_model_create(const int32_t *dims, int n_layers, int batch, int32_t exp_w, int32_t eta,
                            ito_dfp16_model **out);
 int ito_dfp16_model_destroy(ito_dfp16_model *m);
-/* W: int16 [OC][IC] mantissas, host (on_host != 0) or device memory. */
+/* W: int16 [OC][IC] mantissas at the layer's current precision and exponent,
+ * host (on_host != 0) or device memory. */
 int ito_dfp16_model_set_weights(ito_dfp16_model *m, int layer, const int16_t *W, int on_host,
                                 void *stream);
 /* Named device tensors of the last step: "x", "p<l>" int64, "y<l>", "e<l>",
@@ -490,7 +492,8 @@ int ito_dfp16_model_set_weights(ito_dfp16_model *m, int layer, const int16_t *W,
 int ito_dfp16_model_tensor(const ito_dfp16_model *m, const char *name, void **dev_ptr, int *elem_bytes,
                            int64_t *numel);
 /* Scalars of the last step ("ey<l>", "ee<l>", "rs<l>", "rsd<l>", "rsg<l>",
- * "eg<l>", "k<l>", "nz<l>", "pmax<l>", "pdmax<l>", "pgmax<l>"), copied to
+ * "eg<l>", "k<l>", "nz<l>", "pmax<l>", "pdmax<l>", "pgmax<l>", "gabs<l>" =
+ * sum |g<l>| (kept by the weight-gradient down-conversion)), copied to
  * host_out (n >= ito_dfp16_model_num_stats) at ito_dfp16_model_stat_index;
  * synchronises the device. */
 int ito_dfp16_model_num_stats(const ito_dfp16_model *m);
@@ -499,8 +502,68 @@ int ito_dfp16_model_read_stats(const ito_dfp16_model *m, int64_t *host_out, int 
 /* One training step: forward (each layer down-converted), top error = the
  * output (MSE against a zero target), then per layer from the top: delta
  * propagation with the pre-update weights (not the first layer), weight
- * gradient, update. x: int16 [batch][dims[0]] with exponent exp_x. */
+ * gradient, update (saturated to the layer's precision). x: int16
+ * [batch][dims[0]] with exponent exp_x. */
 int ito_dfp16_train_step(ito_dfp16_model *m, const int16_t *x, int32_t exp_x, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Adaptive precision training on the DFP16 model ("Adaptive Precision
+ * Training for Resource Constrained Devices", section III: the Gavg metric of
+ * Equation 4, Algorithm 1 (precision adjustment), Algorithm 2 (metric
+ * evaluations inside an epoch, adjustment between epochs)).
+ *
+ * Representation (the page gives the formulas of epsilon and Gavg only as
+ * missing images; this is the reading): each layer's weights are bits-bit
+ * two's-complement mantissas, |W| <= 2^(bits-1) - 1, with one shared exponent
+ * E_W, so the minimum resolution is epsilon = 2^E_W. The update saturates to
+ * that range. Gavg of a layer = mean |g| / epsilon with g the batch-mean
+ * weight gradient: sum|G| * 2^(E_G - E_W) / (N * B) for the batch-summed DFP
+ * gradient G with exponent E_G, N weights and batch B (no learning rate, as
+ * the page specifies), computed in double from the exact integer sum.
+ * ---------------------------------------------------------------------- */
+
+typedef struct ito_apt_params {
+    int32_t k_init;      /* precision the weights start at (the page uses 6) */
+    int32_t k_min;       /* precision limits, 2 <= k_min <= k_init <= k_max <= 16 */
+    int32_t k_max;
+    int32_t eval_every;  /* Gavg is evaluated at steps 0, eval_every, 2*eval_every, ... of an epoch */
+    double t_min;        /* Algorithm 1: one more bit when Gavg < t_min ... */
+    double t_max;        /* ... one bit less when Gavg > t_max (may be +infinity) */
+} ito_apt_params;
+
+/* A layer's weight precision and exponent (host values; no synchronisation). */
+int ito_dfp16_model_get_precision(const ito_dfp16_model *m, int layer, int32_t *bits, int32_t *exp_w);
+
+/* Change a layer's weight precision to `bits` (2..16): d = bits - current;
+ * d > 0: W <- W * 2^d, E_W <- E_W - d (exact); d < 0: W <- clamp(rhu(W, -d),
+ * +-(2^(bits-1) - 1)), E_W <- E_W - d. Enqueued on `stream`.
+ * Errors: ITO_ERR_ARG, ITO_ERR_EXPONENT (E_W would leave int8). */
+int ito_dfp16_model_set_precision(ito_dfp16_model *m, int layer, int32_t bits, void *stream);
+
+/* Enable APT: every layer is set to p->k_init bits (ito_dfp16_model_set_precision)
+ * and the step counter of the epoch is reset. From then on every
+ * eval_every-th ito_dfp16_train_step of an epoch logs each layer's sum |G|
+ * and E_G on the device (at most 256 evaluations per epoch).
+ * Errors: ITO_ERR_ARG (parameters out of range), ITO_ERR_EXPONENT. */
+int ito_dfp16_model_apt_enable(ito_dfp16_model *m, const ito_apt_params *p, void *stream);
+
+/* End of an epoch (Algorithm 2): synchronises `stream`, computes each layer's
+ * Gavg for every logged evaluation and their mean (in evaluation order), and
+ * applies Algorithm 1: bits + 1 if mean < t_min and bits < k_max, else bits - 1
+ * if mean > t_max and bits > k_min. Writes the means to gavg[n_layers] and the
+ * new precisions to bits[n_layers] (either may be NULL) and starts a new epoch.
+ * Errors: ITO_ERR_ARG (APT not enabled, or no evaluation logged), ITO_ERR_CUDA,
+ * ITO_ERR_EXPONENT. */
+int ito_dfp16_model_apt_epoch_end(ito_dfp16_model *m, double *gavg, int32_t *bits, void *stream);
+
+/* Single-tensor forms: the DFP update of ito_dfp16_update with the result
+ * saturated to +-(2^(bits-1) - 1) (2 <= bits <= 16; bits = 16 is ito_dfp16_update),
+ * and the precision change of ito_dfp16_model_set_precision on an int16
+ * tensor of n mantissas (the caller adjusts its exponent by bits_old - bits_new).
+ * Errors: ITO_ERR_ARG (NULL pointer or bits out of range), ITO_ERR_SHAPE (n < 1). */
+int ito_dfp16_update_bits(int16_t *W, const int16_t *g, const int32_t *d_exp_g, int64_t n, int32_t exp_w,
+                          int32_t eta, int32_t bits, int32_t *d_k, uint32_t *d_nonzero, void *stream);
+int ito_dfp_set_bits(int16_t *W, int64_t n, int32_t bits_old, int32_t bits_new, void *stream);
 
 /* ------------------------------------------------------------------------
  * Measurement hooks (no counterpart in the pages; used by the benchmark)

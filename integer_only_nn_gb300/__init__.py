@@ -40,6 +40,11 @@ class ModelOptions(ctypes.Structure):
                 ("packed_masks", ctypes.c_int32)]
 
 
+class AptParams(ctypes.Structure):
+    _fields_ = [("k_init", ctypes.c_int32), ("k_min", ctypes.c_int32), ("k_max", ctypes.c_int32),
+                ("eval_every", ctypes.c_int32), ("t_min", ctypes.c_double), ("t_max", ctypes.c_double)]
+
+
 class LayerDesc(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("in_features", ctypes.c_int32), ("out_features", ctypes.c_int32),
                 ("in_h", ctypes.c_int32), ("in_w", ctypes.c_int32), ("stride", ctypes.c_int32)]
@@ -99,6 +104,12 @@ _SIGS = {
     "ito_model_profile": (_I, [_P, _I]),
     "ito_model_profile_read": (_I, [_P, _P, _P, _P]),
     "ito_model_kernels_per_step": (_I, [_P]),
+    "ito_dfp16_update_bits": (_I, [_P, _P, _P, _I64, _I32, _I32, _I32, _P, _P, _P]),
+    "ito_dfp_set_bits": (_I, [_P, _I64, _I32, _I32, _P]),
+    "ito_dfp16_model_get_precision": (_I, [_P, _I, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "ito_dfp16_model_set_precision": (_I, [_P, _I, _I32, _P]),
+    "ito_dfp16_model_apt_enable": (_I, [_P, ctypes.POINTER(AptParams), _P]),
+    "ito_dfp16_model_apt_epoch_end": (_I, [_P, _P, _P, _P]),
 }
 
 for _name, (_res, _args) in _SIGS.items():
@@ -519,6 +530,22 @@ def ito_dfp16_update(W, g, exp_g, exp_w, eta, stream=None):
     return k, nz
 
 
+def ito_dfp16_update_bits(W, g, exp_g, exp_w, eta, bits, stream=None):
+    """ito_dfp16_update saturating to +-(2^(bits-1) - 1); in place on W -> (k, nonzero)."""
+    torch = _torch()
+    k = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nz = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(_lib.ito_dfp16_update_bits(_ptr(W), _ptr(g), _ptr(exp_g), W.numel(), exp_w, eta, bits, _ptr(k),
+                                      _ptr(nz), _stream(stream)))
+    return k, nz
+
+
+def ito_dfp_set_bits(W, bits_old, bits_new, stream=None):
+    """Precision change of an int16 mantissa tensor, in place (the exponent changes by bits_old - bits_new)."""
+    _check(_lib.ito_dfp_set_bits(_ptr(W), W.numel(), bits_old, bits_new, _stream(stream)))
+    return W
+
+
 def ito_dfp16_from_float(f, stream=None):
     """float32 device tensor -> (int16 mantissas, device int32 [1] exponent)."""
     torch = _torch()
@@ -553,7 +580,7 @@ def ito_dfp16_linear_fwd_f32(x, exp_x, W, exp_w, stream=None):
 class Dfp16Model:
     """An ito_dfp16_model: DFP16 Linear layers trained with integer SGD."""
 
-    def __init__(self, dims, batch, exp_w, eta=8):
+    def __init__(self, dims, batch, exp_w, eta):
         arr = (ctypes.c_int32 * len(dims))(*dims)
         h = ctypes.c_void_p()
         _check(_lib.ito_dfp16_model_create(arr, len(dims) - 1, batch, exp_w, eta, ctypes.byref(h)))
@@ -590,13 +617,33 @@ class Dfp16Model:
         _check(_lib.ito_dfp16_model_read_stats(self._h, buf, n))
         out = {}
         for l in range(self.n_layers):
-            for key in ("ey", "ee", "rs", "rsd", "rsg", "eg", "k", "nz", "pmax", "pdmax", "pgmax"):
+            for key in ("ey", "ee", "rs", "rsd", "rsg", "eg", "k", "nz", "pmax", "pdmax", "pgmax", "gabs"):
                 i = _lib.ito_dfp16_model_stat_index(self._h, ("%s%d" % (key, l)).encode())
                 out["%s%d" % (key, l)] = buf[i]
         return out
 
     def train_step(self, x, exp_x, stream=None):
         _check(_lib.ito_dfp16_train_step(self._h, _ptr(x), int(exp_x), _stream(stream)))
+
+    def precision(self, layer):
+        """-> (bits, exp_w) of a layer's weights"""
+        b, e = ctypes.c_int32(), ctypes.c_int32()
+        _check(_lib.ito_dfp16_model_get_precision(self._h, layer, ctypes.byref(b), ctypes.byref(e)))
+        return b.value, e.value
+
+    def set_precision(self, layer, bits, stream=None):
+        _check(_lib.ito_dfp16_model_set_precision(self._h, layer, bits, _stream(stream)))
+
+    def apt_enable(self, k_init, k_min, k_max, t_min, t_max, eval_every=1, stream=None):
+        p = AptParams(k_init, k_min, k_max, eval_every, float(t_min), float(t_max))
+        _check(_lib.ito_dfp16_model_apt_enable(self._h, ctypes.byref(p), _stream(stream)))
+
+    def apt_epoch_end(self, stream=None):
+        """Algorithm 1 at the end of an epoch -> (mean Gavg per layer, new bits per layer)"""
+        g = (ctypes.c_double * self.n_layers)()
+        b = (ctypes.c_int32 * self.n_layers)()
+        _check(_lib.ito_dfp16_model_apt_epoch_end(self._h, g, b, _stream(stream)))
+        return list(g), list(b)
 
 
 class _CudaArray:

@@ -363,11 +363,20 @@ int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t
 
 // ------------------------------------------------------- down-conversion
 
+// adds a warp's partial sums of |mantissa| to *d_abs_sum (exact: integer atomics)
+__device__ __forceinline__ void add_abs_sum(unsigned long long* d_abs_sum, unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0 && v) atomicAdd(d_abs_sum, v);
+}
+
 __global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t cols,
                            const unsigned long long* __restrict__ d_max, const int32_t* __restrict__ d_ea,
                            const int32_t* __restrict__ d_eb, int16_t* __restrict__ out16, uint16_t* __restrict__ hi,
                            uint16_t* __restrict__ lo, int64_t ldl, int32_t* __restrict__ d_exp_out,
-                           int32_t* __restrict__ d_rs, int* __restrict__ err)
+                           int32_t* __restrict__ d_rs, unsigned long long* __restrict__ d_abs_sum,
+                           int* __restrict__ err)
 {
     // section 3.1: Rs brings max |P| within 15 magnitude bits; the new exponent is Ea + Eb + Rs
     const unsigned long long m = *d_max;
@@ -380,9 +389,11 @@ __global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t 
         if (e < -128 || e > 127) raise_device_error(err, ITO_ERR_EXPONENT);
     }
     const int64_t n = rows * cols;
+    unsigned long long asum = 0;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int32_t v = (int32_t)sat16s(rhu64(__ldcs(P + i), rs));
         out16[i] = (int16_t)v;
+        asum += (unsigned long long)(v < 0 ? -v : v);
         if (hi) {
             const int64_t r = i / cols, c = i - r * cols;
             int32_t h, l;
@@ -391,6 +402,7 @@ __global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t 
             lo[r * ldl + c] = int_to_bf16_bits(l);
         }
     }
+    if (d_abs_sum) add_abs_sum(d_abs_sum, asum);
 }
 
 // four elements per thread step: 32 bytes of P in, 8 bytes of mantissas and
@@ -399,7 +411,8 @@ __global__ void k_dfp_down_v4(const int64_t* __restrict__ P, int rows, int cols,
                               const unsigned long long* __restrict__ d_max, const int32_t* __restrict__ d_ea,
                               const int32_t* __restrict__ d_eb, int16_t* __restrict__ out16,
                               uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int ldl,
-                              int32_t* __restrict__ d_exp_out, int32_t* __restrict__ d_rs, int* __restrict__ err)
+                              int32_t* __restrict__ d_exp_out, int32_t* __restrict__ d_rs,
+                              unsigned long long* __restrict__ d_abs_sum, int* __restrict__ err)
 {
     const unsigned long long m = *d_max;
     const int bl = m ? 64 - __clzll((long long)m) : 0;
@@ -412,6 +425,7 @@ __global__ void k_dfp_down_v4(const int64_t* __restrict__ P, int rows, int cols,
     }
     const int groups = rows * (cols >> 2);
     const int gpr = cols >> 2;
+    unsigned long long asum = 0;
     for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += gridDim.x * blockDim.x) {
         const int r = g / gpr, c = (g - r * gpr) << 2;
         const int64_t i0 = (int64_t)r * cols + c;
@@ -425,6 +439,7 @@ __global__ void k_dfp_down_v4(const int64_t* __restrict__ P, int rows, int cols,
             const int32_t q = (int32_t)sat16s(rhu64(pv[k], rs));
             int32_t hh, ll;
             limb_split(q, hh, ll);
+            asum += (unsigned long long)(q < 0 ? -q : q);
             v[k] = (int16_t)q;
             h[k] = int_to_bf16_bits(hh);
             l[k] = int_to_bf16_bits(ll);
@@ -436,13 +451,14 @@ __global__ void k_dfp_down_v4(const int64_t* __restrict__ P, int rows, int cols,
             *reinterpret_cast<uint2*>(lo + o) = *reinterpret_cast<const uint2*>(l);
         }
     }
+    if (d_abs_sum) add_abs_sum(d_abs_sum, asum);
 }
 
 static inline bool al(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned long long* d_max, const int32_t* d_ea,
                     const int32_t* d_eb, int16_t* out16, uint16_t* hi, uint16_t* lo, int64_t ldl, int32_t* d_exp_out,
-                    int32_t* d_rs, cudaStream_t s)
+                    int32_t* d_rs, cudaStream_t s, unsigned long long* d_abs_sum)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
     int* err = device_error_word();
@@ -450,10 +466,10 @@ int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned
     if (cols % 4 == 0 && rows * cols < (1LL << 31) && ldl % 4 == 0 && al(P, 16) && al(out16, 8) &&
         (!hi || (al(hi, 8) && al(lo, 8))))
         k_dfp_down_v4<<<launch_grid_blocks(rows * cols / 4, 256), 256, 0, s>>>(
-            P, (int)rows, (int)cols, d_max, d_ea, d_eb, out16, hi, lo, (int)ldl, d_exp_out, d_rs, err);
+            P, (int)rows, (int)cols, d_max, d_ea, d_eb, out16, hi, lo, (int)ldl, d_exp_out, d_rs, d_abs_sum, err);
     else
         k_dfp_down<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(P, rows, cols, d_max, d_ea, d_eb, out16, hi,
-                                                                         lo, ldl, d_exp_out, d_rs, err);
+                                                                         lo, ldl, d_exp_out, d_rs, d_abs_sum, err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp down launch: %s", cudaGetErrorString(e));
 }
@@ -553,10 +569,10 @@ int launch_p64_to_float(const int64_t* P, int64_t n, const int32_t* d_ea, const 
 
 __global__ void k_dfp_update(int16_t* __restrict__ W, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
                              int64_t ldl, const int16_t* __restrict__ G, int64_t rows, int64_t cols,
-                             const int32_t* __restrict__ d_exp_g, int32_t exp_w, int32_t eta, int32_t* __restrict__ d_k,
-                             uint32_t* __restrict__ d_nonzero)
+                             const int32_t* __restrict__ d_exp_g, int32_t exp_w, int32_t eta, int32_t lim,
+                             int32_t* __restrict__ d_k, uint32_t* __restrict__ d_nonzero)
 {
-    // W * 2^Ew <- W * 2^Ew - G * 2^Eg * 2^-eta  =>  dW = G * 2^-(Ew + eta - Eg)
+    // W * 2^Ew <- W * 2^Ew - G * 2^Eg * 2^-eta  =>  dW = G * 2^-(Ew + eta - Eg); W saturates to +-lim
     const int k = exp_w + eta - *d_exp_g;
     if (d_k && blockIdx.x == 0 && threadIdx.x == 0) *d_k = k;
     uint32_t cnt = 0;
@@ -566,7 +582,8 @@ __global__ void k_dfp_update(int16_t* __restrict__ W, uint16_t* __restrict__ hi,
         // a left shift past 17 bits already saturates every difference
         const int64_t dw = k >= 0 ? rhu64(g, k) : g * ((int64_t)1 << (-k > 17 ? 17 : -k));
         cnt += dw != 0;
-        const int32_t w = (int32_t)sat16s((int64_t)W[i] - dw);
+        const int64_t d = (int64_t)W[i] - dw;
+        const int32_t w = (int32_t)(d > lim ? lim : (d < -lim ? -lim : d));
         W[i] = (int16_t)w;
         if (hi) {
             const int64_t r = i / cols, c = i - r * cols;
@@ -585,7 +602,7 @@ __global__ void k_dfp_update(int16_t* __restrict__ W, uint16_t* __restrict__ hi,
 // four weights per thread step; cols % 4 == 0 and rows * cols < 2^31
 __global__ void k_dfp_update_v4(int16_t* __restrict__ W, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
                                 int ldl, const int16_t* __restrict__ G, int rows, int cols,
-                                const int32_t* __restrict__ d_exp_g, int32_t exp_w, int32_t eta,
+                                const int32_t* __restrict__ d_exp_g, int32_t exp_w, int32_t eta, int32_t lim,
                                 int32_t* __restrict__ d_k, uint32_t* __restrict__ d_nonzero)
 {
     const int k = exp_w + eta - *d_exp_g;
@@ -605,7 +622,8 @@ __global__ void k_dfp_update_v4(int16_t* __restrict__ W, uint16_t* __restrict__ 
         for (int j = 0; j < 4; ++j) {
             const int64_t dw = k >= 0 ? rhu64(gv[j], k) : (int64_t)gv[j] * ((int64_t)1 << kl);
             cnt += dw != 0;
-            const int32_t nw = (int32_t)sat16s((int64_t)w[j] - dw);
+            const int64_t d = (int64_t)w[j] - dw;
+            const int32_t nw = (int32_t)(d > lim ? lim : (d < -lim ? -lim : d));
             int32_t hh, ll;
             limb_split(nw, hh, ll);
             w[j] = (int16_t)nw;
@@ -627,18 +645,58 @@ __global__ void k_dfp_update_v4(int16_t* __restrict__ W, uint16_t* __restrict__ 
 
 int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const int16_t* G, int64_t rows,
                       int64_t cols, const int32_t* d_exp_g, int32_t exp_w, int32_t eta, int32_t* d_k,
-                      uint32_t* d_nonzero, cudaStream_t s)
+                      uint32_t* d_nonzero, cudaStream_t s, int bits)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
+    if (bits < 2 || bits > 16) return set_error(ITO_ERR_ARG, "weight precision must be 2 .. 16 bits");
+    const int32_t lim = (1 << (bits - 1)) - 1;
     if (cols % 4 == 0 && rows * cols < (1LL << 31) && ldl % 4 == 0 && al(W, 8) && al(G, 8) &&
         (!hi || (al(hi, 8) && al(lo, 8))))
         k_dfp_update_v4<<<launch_grid_blocks(rows * cols / 4, 256), 256, 0, s>>>(
-            W, hi, lo, (int)ldl, G, (int)rows, (int)cols, d_exp_g, exp_w, eta, d_k, d_nonzero);
+            W, hi, lo, (int)ldl, G, (int)rows, (int)cols, d_exp_g, exp_w, eta, lim, d_k, d_nonzero);
     else
         k_dfp_update<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(W, hi, lo, ldl, G, rows, cols, d_exp_g,
-                                                                           exp_w, eta, d_k, d_nonzero);
+                                                                           exp_w, eta, lim, d_k, d_nonzero);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp update launch: %s", cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------ precision change
+//
+// "Adaptive Precision Training for Resource Constrained Devices", Algorithm 1
+// changes a layer's weight precision by one bit at a time. With the weights
+// held as bits-bit mantissas and one shared exponent, a change by d bits is
+// W * 2^d (d > 0, every value kept exactly; the exponent drops by d) or
+// round-half-up of W / 2^-d saturated to the new range (d < 0; the exponent
+// rises by -d). The bf16 limb planes are rewritten too.
+__global__ void k_dfp_set_bits(int16_t* __restrict__ W, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
+                               int64_t ldl, int64_t rows, int64_t cols, int d, int32_t lim)
+{
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t v = d >= 0 ? (int64_t)W[i] * ((int64_t)1 << d) : rhu64(W[i], -d);
+        const int32_t w = (int32_t)(v > lim ? lim : (v < -lim ? -lim : v));
+        W[i] = (int16_t)w;
+        if (hi) {
+            const int64_t r = i / cols, c = i - r * cols;
+            int32_t h, l;
+            limb_split(w, h, l);
+            hi[r * ldl + c] = int_to_bf16_bits(h);
+            lo[r * ldl + c] = int_to_bf16_bits(l);
+        }
+    }
+}
+
+int launch_dfp_set_bits(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, int64_t rows, int64_t cols,
+                        int bits_old, int bits_new, cudaStream_t s)
+{
+    if (bits_old < 2 || bits_old > 16 || bits_new < 2 || bits_new > 16)
+        return set_error(ITO_ERR_ARG, "weight precision must be 2 .. 16 bits");
+    if (rows < 1 || cols < 1 || bits_old == bits_new) return ITO_OK;
+    k_dfp_set_bits<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(W, hi, lo, ldl, rows, cols,
+                                                                       bits_new - bits_old, (1 << (bits_new - 1)) - 1);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "precision change launch: %s", cudaGetErrorString(e));
 }
 
 }  // namespace ito

@@ -16,6 +16,15 @@
 //
 // Exponents live on the device (int32 scalars) and are updated by the kernels
 // that produce each tensor, so a step needs no host synchronisation.
+//
+// Adaptive precision ("Adaptive Precision Training for Resource Constrained
+// Devices", section III): every layer's weights are bits-bit mantissas
+// (2 <= bits <= 16) with their own exponent E_W; the update saturates to the
+// layer's precision. With APT enabled, the weight-gradient down-conversion also
+// sums |g| exactly, each evaluated step logs (sum|g|, E_G) per layer on the
+// device, and ito_dfp16_model_apt_epoch_end applies Algorithm 1 to the mean
+// Gavg of the epoch's evaluations (Algorithm 2: adjustment between epochs).
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -30,7 +39,19 @@ __global__ void k_set_i32(int32_t* p, int32_t v) { *p = v; }
 __global__ void k_copy_i32(int32_t* dst, const int32_t* src) { *dst = *src; }
 
 enum { D_EY = 0, D_EE, D_RS, D_RSD, D_RSG, D_EG, D_K, D_NZ, D_N32 };
-enum { D_PMAX = 0, D_PDMAX, D_PGMAX, D_N64 };
+enum { D_PMAX = 0, D_PDMAX, D_PGMAX, D_GABS, D_N64 };
+constexpr int kAptMaxEvals = 256;   // logged Gavg evaluations per epoch
+
+// copies this step's (sum |g|, E_G) of every layer into one log slot
+__global__ void k_apt_log(const unsigned long long* __restrict__ s64, const int32_t* __restrict__ s32, int nl,
+                          unsigned long long* __restrict__ log_abs, int32_t* __restrict__ log_eg)
+{
+    const int l = threadIdx.x;
+    if (l < nl) {
+        log_abs[l] = s64[l * D_N64 + D_GABS];
+        log_eg[l] = s32[l * D_N32 + D_EG];
+    }
+}
 
 struct DLayer {
     int IC, OC;
@@ -54,6 +75,13 @@ struct DLayer {
 struct ito_dfp16_model {
     int batch = 0, exp_w = 0, eta = 0;
     std::vector<ito::DLayer> L;
+    std::vector<int32_t> wexp, wbits;  // per-layer weight exponent and precision (host copies)
+    int32_t* wexp_d = nullptr;         // device copy of wexp
+    bool apt = false;
+    ito_apt_params ap{};
+    int apt_step = 0, apt_nlog = 0;     // steps since the last epoch end; logged evaluations
+    unsigned long long* log_abs = nullptr;
+    int32_t* log_eg = nullptr;
     int16_t* x16 = nullptr;
     uint16_t *xh = nullptr, *xl = nullptr;
     int64_t ldx = 0;
@@ -234,6 +262,22 @@ int ito_dfp16_update(int16_t* W, const int16_t* g, const int32_t* d_exp_g, int64
                              static_cast<cudaStream_t>(stream));
 }
 
+int ito_dfp16_update_bits(int16_t* W, const int16_t* g, const int32_t* d_exp_g, int64_t n, int32_t exp_w, int32_t eta,
+                          int32_t bits, int32_t* d_k, uint32_t* d_nonzero, void* stream)
+{
+    if (!W || !g || !d_exp_g) return set_error(ITO_ERR_ARG, "NULL pointer");
+    if (n < 1) return set_error(ITO_ERR_SHAPE, "n must be >= 1");
+    return launch_dfp_update(W, nullptr, nullptr, 0, g, 1, n, d_exp_g, exp_w, eta, d_k, d_nonzero,
+                             static_cast<cudaStream_t>(stream), bits);
+}
+
+int ito_dfp_set_bits(int16_t* W, int64_t n, int32_t bits_old, int32_t bits_new, void* stream)
+{
+    if (!W) return set_error(ITO_ERR_ARG, "NULL pointer");
+    if (n < 1) return set_error(ITO_ERR_SHAPE, "n must be >= 1");
+    return launch_dfp_set_bits(W, nullptr, nullptr, 0, 1, n, bits_old, bits_new, static_cast<cudaStream_t>(stream));
+}
+
 // ------------------------------------------------------------------ model
 
 int ito_dfp16_model_destroy(ito_dfp16_model* m)
@@ -257,6 +301,11 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
     }
     ITO_TRY(m->alloc(&m->s32, (size_t)nl * D_N32 + 2));
     ITO_TRY(m->alloc(&m->s64, (size_t)nl * D_N64));
+    ITO_TRY(m->alloc(&m->wexp_d, (size_t)nl));
+    ITO_TRY(m->alloc(&m->log_abs, (size_t)kAptMaxEvals * nl));
+    ITO_TRY(m->alloc(&m->log_eg, (size_t)kAptMaxEvals * nl));
+    m->wexp.assign(nl, m->exp_w);
+    m->wbits.assign(nl, 16);
     m->ldx = pad8(dims[0]);
     ITO_TRY(m->alloc(&m->x16, (size_t)B * dims[0]));
     ITO_TRY(m->alloc(&m->xh, (size_t)B * m->ldx));
@@ -303,6 +352,8 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
         ITO_TRY(dfp_gemm_plan(&L.pg, eh, el, true, ih, il, true, L.OC, L.IC, B, L.pg64, L.IC, m->u64(l, D_PGMAX)));
     }
     k_set_i32<<<1, 1>>>(m->ew(), m->exp_w);
+    if (cudaMemcpy(m->wexp_d, m->wexp.data(), sizeof(int32_t) * nl, cudaMemcpyHostToDevice) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "weight exponent copy");
     return cudaDeviceSynchronize() == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp model init");
 }
 
@@ -371,7 +422,7 @@ int ito_dfp16_model_tensor(const ito_dfp16_model* m, const char* name, void** de
 }
 
 static const char* kD32[D_N32] = {"ey", "ee", "rs", "rsd", "rsg", "eg", "k", "nz"};
-static const char* kD64[D_N64] = {"pmax", "pdmax", "pgmax"};
+static const char* kD64[D_N64] = {"pmax", "pdmax", "pgmax", "gabs"};
 
 int ito_dfp16_model_num_stats(const ito_dfp16_model* m)
 {
@@ -424,7 +475,7 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
         DLayer& L = m->L[l];
         const int32_t* e_in = l == 0 ? m->ex() : m->i32(l - 1, D_EY);
         ITO_TRY(dfp_gemm_run(L.pf, s));
-        ITO_TRY(launch_dfp_down(L.p64, B, L.OC, m->u64(l, D_PMAX), e_in, m->ew(), L.y16, L.yh, L.yl, L.ldy,
+        ITO_TRY(launch_dfp_down(L.p64, B, L.OC, m->u64(l, D_PMAX), e_in, m->wexp_d + l, L.y16, L.yh, L.yl, L.ldy,
                                 m->i32(l, D_EY), m->i32(l, D_RS), s));
     }
     k_copy_i32<<<1, 1, 0, s>>>(m->i32(nl - 1, D_EE), m->i32(nl - 1, D_EY));
@@ -434,17 +485,108 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
         if (l > 0) {
             DLayer& P = m->L[l - 1];
             ITO_TRY(dfp_gemm_run(L.pd, s));
-            ITO_TRY(launch_dfp_down(L.pd64, B, L.IC, m->u64(l, D_PDMAX), m->i32(l, D_EE), m->ew(), P.e16, P.eh, P.el,
-                                    P.ldy, m->i32(l - 1, D_EE), m->i32(l, D_RSD), s));
+            ITO_TRY(launch_dfp_down(L.pd64, B, L.IC, m->u64(l, D_PDMAX), m->i32(l, D_EE), m->wexp_d + l, P.e16, P.eh,
+                                    P.el, P.ldy, m->i32(l - 1, D_EE), m->i32(l, D_RSD), s));
         }
         ITO_TRY(dfp_gemm_run(L.pg, s));
         ITO_TRY(launch_dfp_down(L.pg64, L.OC, L.IC, m->u64(l, D_PGMAX), m->i32(l, D_EE), e_in, L.g16, nullptr, nullptr,
-                                0, m->i32(l, D_EG), m->i32(l, D_RSG), s));
-        ITO_TRY(launch_dfp_update(L.W, L.Wh, L.Wl, L.ldw, L.g16, L.OC, L.IC, m->i32(l, D_EG), m->exp_w, m->eta,
-                                  m->i32(l, D_K), reinterpret_cast<uint32_t*>(m->i32(l, D_NZ)), s));
+                                0, m->i32(l, D_EG), m->i32(l, D_RSG), s, m->u64(l, D_GABS)));
+        ITO_TRY(launch_dfp_update(L.W, L.Wh, L.Wl, L.ldw, L.g16, L.OC, L.IC, m->i32(l, D_EG), m->wexp[l], m->eta,
+                                  m->i32(l, D_K), reinterpret_cast<uint32_t*>(m->i32(l, D_NZ)), s, m->wbits[l]));
+    }
+    if (m->apt) {
+        // Algorithm 2: Gavg is evaluated at every eval_every-th step of the epoch
+        if (m->apt_step % m->ap.eval_every == 0) {
+            if (m->apt_nlog >= kAptMaxEvals)
+                return set_error(ITO_ERR_ARG, "more than %d Gavg evaluations in one epoch", kAptMaxEvals);
+            k_apt_log<<<1, 32 * ((nl + 31) / 32), 0, s>>>(m->s64, m->s32, nl, m->log_abs + (size_t)m->apt_nlog * nl,
+                                                          m->log_eg + (size_t)m->apt_nlog * nl);
+            ++m->apt_nlog;
+        }
+        ++m->apt_step;
     }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp step: %s", cudaGetErrorString(e));
+}
+
+int ito_dfp16_model_get_precision(const ito_dfp16_model* m, int layer, int32_t* bits, int32_t* exp_w)
+{
+    if (!m || layer < 0 || layer >= (int)m->L.size()) return set_error(ITO_ERR_ARG, "bad model or layer");
+    if (bits) *bits = m->wbits[layer];
+    if (exp_w) *exp_w = m->wexp[layer];
+    return ITO_OK;
+}
+
+int ito_dfp16_model_set_precision(ito_dfp16_model* m, int layer, int32_t bits, void* stream)
+{
+    if (!m || layer < 0 || layer >= (int)m->L.size()) return set_error(ITO_ERR_ARG, "bad model or layer");
+    if (bits < 2 || bits > 16) return set_error(ITO_ERR_ARG, "weight precision must be 2 .. 16 bits");
+    const int d = bits - m->wbits[layer];
+    if (d == 0) return ITO_OK;
+    const int e = m->wexp[layer] - d;
+    if (e < -128 || e > 127) return set_error(ITO_ERR_EXPONENT, "weight exponent %d outside int8", e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DLayer& L = m->L[layer];
+    ITO_TRY(launch_dfp_set_bits(L.W, L.Wh, L.Wl, L.ldw, L.OC, L.IC, m->wbits[layer], bits, s));
+    k_set_i32<<<1, 1, 0, s>>>(m->wexp_d + layer, e);
+    m->wbits[layer] = bits;
+    m->wexp[layer] = e;
+    cudaError_t ce = cudaGetLastError();
+    return ce == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "precision change: %s", cudaGetErrorString(ce));
+}
+
+int ito_dfp16_model_apt_enable(ito_dfp16_model* m, const ito_apt_params* p, void* stream)
+{
+    if (!m || !p) return set_error(ITO_ERR_ARG, "NULL argument");
+    if (!(2 <= p->k_min && p->k_min <= p->k_init && p->k_init <= p->k_max && p->k_max <= 16))
+        return set_error(ITO_ERR_ARG, "need 2 <= k_min <= k_init <= k_max <= 16");
+    if (p->eval_every < 1) return set_error(ITO_ERR_ARG, "eval_every must be >= 1");
+    if (!(p->t_min <= p->t_max)) return set_error(ITO_ERR_ARG, "need t_min <= t_max");
+    if (m->L.size() > 1024) return set_error(ITO_ERR_UNSUPPORTED, "APT supports at most 1024 layers");
+    for (int l = 0; l < (int)m->L.size(); ++l) ITO_TRY(ito_dfp16_model_set_precision(m, l, p->k_init, stream));
+    m->ap = *p;
+    m->apt = true;
+    m->apt_step = 0;
+    m->apt_nlog = 0;
+    return ITO_OK;
+}
+
+int ito_dfp16_model_apt_epoch_end(ito_dfp16_model* m, double* gavg_out, int32_t* bits_out, void* stream)
+{
+    if (!m || !m->apt) return set_error(ITO_ERR_ARG, "APT is not enabled on this model");
+    if (m->apt_nlog < 1) return set_error(ITO_ERR_ARG, "no Gavg evaluation since the last epoch end");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int nl = (int)m->L.size();
+    const size_t cnt = (size_t)m->apt_nlog * nl;
+    std::vector<unsigned long long> ab(cnt);
+    std::vector<int32_t> eg(cnt);
+    if (cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpy(ab.data(), m->log_abs, cnt * sizeof(unsigned long long), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(eg.data(), m->log_eg, cnt * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "reading the Gavg log failed");
+    for (int l = 0; l < nl; ++l) {
+        // Equation 4 per evaluation: Gavg = sum|G| * 2^(E_G - E_W) / (N * B), the gradient taken
+        // as the batch mean; the epoch's value is the mean over its evaluations, in order
+        const double nb = (double)((int64_t)m->L[l].OC * m->L[l].IC * (int64_t)m->batch);
+        double acc = 0.0;
+        for (int i = 0; i < m->apt_nlog; ++i) {
+            const size_t j = (size_t)i * nl + l;
+            acc += ldexp((double)ab[j], eg[j] - m->wexp[l]) / nb;
+        }
+        const double g = acc / (double)m->apt_nlog;
+        // Algorithm 1
+        int k = m->wbits[l];
+        if (g < m->ap.t_min && k < m->ap.k_max)
+            ++k;
+        else if (g > m->ap.t_max && k > m->ap.k_min)
+            --k;
+        ITO_TRY(ito_dfp16_model_set_precision(m, l, k, stream));
+        if (gavg_out) gavg_out[l] = g;
+        if (bits_out) bits_out[l] = k;
+    }
+    m->apt_step = 0;
+    m->apt_nlog = 0;
+    return ITO_OK;
 }
 
 }  // extern "C"

@@ -84,9 +84,10 @@ int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t
 // DFP down-conversion of P with exponent *d_ea + *d_eb: Rs from *d_max,
 // out16 = sat16(rhu(P, Rs)) (+ limb planes if hi != null), *d_exp_out = Ea + Eb + Rs,
 // *d_rs = Rs; an exponent outside int8 raises ITO_ERR_EXPONENT in the error word.
+// d_abs_sum (optional): sum of |out16| is added to it (exact).
 int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned long long* d_max, const int32_t* d_ea,
                     const int32_t* d_eb, int16_t* out16, uint16_t* hi, uint16_t* lo, int64_t ldl, int32_t* d_exp_out,
-                    int32_t* d_rs, cudaStream_t s);
+                    int32_t* d_rs, cudaStream_t s, unsigned long long* d_abs_sum = nullptr);
 // float -> DFP16 (exponent from max |f|; d_bits: device scratch for the max's bits),
 // DFP16 -> float, and float(P) * 2^(Ea + Eb)
 int launch_dfp_from_float(const float* f, int64_t n, unsigned int* d_bits, int16_t* out, int32_t* d_exp,
@@ -94,10 +95,14 @@ int launch_dfp_from_float(const float* f, int64_t n, unsigned int* d_bits, int16
 int launch_dfp_to_float(const int16_t* m, int64_t n, const int32_t* d_exp, float* out, cudaStream_t s);
 int launch_p64_to_float(const int64_t* P, int64_t n, const int32_t* d_ea, const int32_t* d_eb, float* out,
                         cudaStream_t s);
-// W <- sat16(W - dW), dW = rhu(G, k) (k >= 0) or G * 2^-k (k < 0), k = exp_w + eta - *d_exp_g
+// W <- sat_bits(W - dW), dW = rhu(G, k) (k >= 0) or G * 2^-k (k < 0), k = exp_w + eta - *d_exp_g;
+// sat_bits clamps to +-(2^(bits-1) - 1) (bits = 16: sat16)
 int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const int16_t* G, int64_t rows,
                       int64_t cols, const int32_t* d_exp_g, int32_t exp_w, int32_t eta, int32_t* d_k,
-                      uint32_t* d_nonzero, cudaStream_t s);
+                      uint32_t* d_nonzero, cudaStream_t s, int bits = 16);
+// weight precision change bits_old -> bits_new (W * 2^d, or rhu + saturation), limbs rewritten
+int launch_dfp_set_bits(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, int64_t rows, int64_t cols,
+                        int bits_old, int bits_new, cudaStream_t s);
 
 // split_ws (optional): room for split-K partials; without it (or when too
 // small) the contraction is not split.

@@ -12,6 +12,9 @@ Sources:
     reads it and updates weights).
   "Mixed Precision Training of Convolutional Neural Networks using Integer
     Operations": section 3 and 3.1, DFP tensors and primitives.
+  "Adaptive Precision Training for Resource Constrained Devices": section III,
+    the Gavg metric (Equation 4), Algorithm 1 (precision adjustment) and
+    Algorithm 2 (adjustment between epochs), applied to DFP weights.
 
 Step order (one reading, stated): forward through all layers; top error;
 then for each layer from the top down: delta propagation with the weights as
@@ -21,6 +24,7 @@ gradient, weight update.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 
@@ -35,7 +39,7 @@ TARGET_BITS = 7      # NITI target_bits, for forward, delta and weight gradient
 MU_WEIGHT = 2        # NITI mu_weight
 TARGET_MAG = 64      # integer target on the true class
 DFP_BITS = 15        # DFP-16 mantissa: 15 magnitude bits plus sign
-DFP_ETA = 8          # DFP16 integer SGD: learning rate 2^-eta
+DFP_ETA = 20         # DFP16 integer SGD: learning rate 2^-eta on the batch-summed gradient
 
 
 def build(force: bool = False) -> str:
@@ -88,7 +92,9 @@ def lib():
             "ora_dfp_linear_dgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
             "ora_dfp_linear_wgrad": (None, [P, P] + [ctypes.c_int] * 3 + [P]),
             "ora_dfp_down": (i32, [P, i64, i32, P, P]),
-            "ora_dfp_update": (i64, [P, P, i64, i32]),
+            "ora_dfp_update": (i64, [P, P, i64, i32, i32]),
+            "ora_dfp_set_bits": (i32, [P, i64, i32, i32]),
+            "ora_abs_sum16": (i64, [P, i64]),
             "ora_dfp_from_float": (i32, [P, i64, P]),
             "ora_dfp_to_float": (None, [P, i64, i32, P]),
             "ora_p64_to_float": (None, [P, i64, i32, P]),
@@ -433,11 +439,101 @@ def p64_to_float(P, e: int):
     return out
 
 
-def dfp_update(W, Gm, k: int):
+def dfp_update(W, Gm, k: int, bits: int = 16):
+    """W <- sat_bits(W - rhu(Gm, k)) (left shift for k < 0) -> (W, nonzero count)"""
+    if not 2 <= bits <= 16:
+        raise ValueError("bits must be 2 .. 16")
     Wn = np.array(W, dtype=np.int16, copy=True, order="C")
     Gm = _c(Gm, np.int16)
-    nz = lib().ora_dfp_update(_p(Wn), _p(Gm), Gm.size, k)
+    nz = lib().ora_dfp_update(_p(Wn), _p(Gm), Gm.size, k, bits)
     return Wn, nz
+
+
+def dfp_set_bits(W, bits_old: int, bits_new: int):
+    """Change a weight tensor's precision (ora_dfp_set_bits) -> (W, exponent change)."""
+    if not (2 <= bits_old <= 16 and 2 <= bits_new <= 16):
+        raise ValueError("bits must be 2 .. 16")
+    Wn = np.array(W, dtype=np.int16, copy=True, order="C")
+    if bits_new > bits_old and np.abs(Wn.astype(np.int64)).max(initial=0) > (1 << (bits_old - 1)) - 1:
+        raise ValueError("weights exceed the old precision")
+    de = lib().ora_dfp_set_bits(_p(Wn), Wn.size, bits_old, bits_new)
+    return Wn, de
+
+
+def abs_sum16(x) -> int:
+    x = _c(x, np.int16)
+    return int(lib().ora_abs_sum16(_p(x), x.size))
+
+
+# ------------------------------------------------- adaptive precision (APT)
+#
+# "Adaptive Precision Training for Resource Constrained Devices", section III.
+# Equation 4 (its formula is missing from the page text; reading from the
+# prose): Gavg_i = (1/N_i) sum_j |g_ij| / eps_i, the mean gradient magnitude in
+# units of the layer's weight resolution, with no learning rate in it. Here
+# the weight gradient of the integer step is the batch SUM G * 2^E_G; the
+# gradient of minibatch SGD that the page's g_ij denotes is its batch mean, so
+# g = G * 2^E_G / B; eps = 2^E_W. Hence
+# Gavg = sum|G| * 2^(E_G - E_W) / (N * B), evaluated in float64 as written below.
+
+def apt_gavg(gabs: int, n: int, batch: int, exp_g: int, exp_w: int) -> float:
+    return math.ldexp(float(gabs), exp_g - exp_w) / float(n * batch)
+
+
+def apt_policy(bits, gavg, t_min: float, t_max: float, k_min: int, k_max: int):
+    """Algorithm 1: raise a layer's precision by one bit when Gavg < T_min,
+    lower it by one when Gavg > T_max, within [k_min, k_max]."""
+    out = []
+    for k, g in zip(bits, gavg):
+        if g < t_min and k < k_max:
+            k += 1
+        elif g > t_max and k > k_min:
+            k -= 1
+        out.append(k)
+    return out
+
+
+def apt_run(workload, steps: int, callback=None, route="loops"):
+    """Algorithm 2 on a DFP workload with an `apt` setting (seeded_inputs):
+    the weights start at apt.k_init bits; inside each epoch of apt.epoch
+    steps, Gavg is evaluated after every step whose index within the epoch is
+    a multiple of apt.eval_every; between epochs Algorithm 1 adjusts each
+    layer's precision from the mean of that epoch's evaluations.
+    callback(t, record, state) after every step; state = dict(bits, exp_w,
+    gavg (the means of the last finished epoch, or None)).
+    Returns (weights, exp_w list, bits list)."""
+    import seeded_inputs as si
+    w, a = workload, workload.apt
+    weights = [np.array(x) for x in si.make_weights(w)]
+    L = len(weights)
+    bits = [16] * L
+    exp_w = [w.exp_w] * L
+    for l in range(L):
+        weights[l], de = dfp_set_bits(weights[l], 16, a.k_init)
+        exp_w[l] += de
+        bits[l] = a.k_init
+    evals = [[] for _ in range(L)]
+    last = None
+    for t in range(steps):
+        x, _ = si.make_batch(w, t)
+        rec = dfp16_step(weights, exp_w, x, w.exp_x, eta=w.eta, route=route, wbits=bits)
+        weights = [rec["w%d" % l] for l in range(L)]
+        te = t % a.epoch
+        if te % a.eval_every == 0:
+            for l in range(L):
+                evals[l].append(apt_gavg(rec["gabs%d" % l], weights[l].size, w.batch, rec["eg%d" % l], exp_w[l]))
+        if te == a.epoch - 1:
+            last = [sum(v) / len(v) for v in evals]
+            new_bits = apt_policy(bits, last, a.t_min, a.t_max, a.k_min, a.k_max)
+            for l in range(L):
+                if new_bits[l] != bits[l]:
+                    weights[l], de = dfp_set_bits(weights[l], bits[l], new_bits[l])
+                    exp_w[l] += de
+            bits = new_bits
+            evals = [[] for _ in range(L)]
+        if callback is not None:
+            callback(t, rec, dict(bits=list(bits), exp_w=list(exp_w), gavg=last))
+    return weights, exp_w, bits
 
 
 # ------------------------------------------------------------- training steps
@@ -572,10 +668,12 @@ def cnn_step(weights, x, labels, convs, target_bits=TARGET_BITS, mu_weight=MU_WE
     return r
 
 
-def dfp16_step(weights, exp_w, x, exp_x, eta=DFP_ETA, target_bits=DFP_BITS, route="loops"):
+def dfp16_step(weights, exp_w, x, exp_x, eta=DFP_ETA, target_bits=DFP_BITS, route="loops", wbits=None):
     """One integer training step of a stack of DFP-16 Linear layers (no ReLU).
-    weights: list of int16 mantissa tensors [OC, IC] sharing exponent exp_w
-    (held fixed); x: int16 mantissas [B, IC0] with exponent exp_x.
+    weights: list of int16 mantissa tensors [OC, IC] with exponent exp_w (one
+    int for all layers, or a list per layer; held fixed by the step); x: int16
+    mantissas [B, IC0] with exponent exp_x. wbits: per-layer weight precision
+    in bits (default 16), the saturation range of the update.
 
     Every contraction is exact in int64 and is down-converted to DFP-16 with a
     new exponent. The top error is the output itself (an MSE error against a
@@ -585,7 +683,8 @@ def dfp16_step(weights, exp_w, x, exp_x, eta=DFP_ETA, target_bits=DFP_BITS, rout
     ey{l} exponent; e{l}/ee{l} delta at the output of layer l; pd{l} int64
     delta-propagation contraction (l >= 1) with pdmax{l}, rsd{l}; pg{l} int64
     weight gradient with pgmax{l}, rsg{l}, g{l} int16, eg{l}; k{l} the update
-    shift; w{l} updated weights; nz{l}. route: "loops" or "f64"."""
+    shift; w{l} updated weights; nz{l}; gabs{l} = sum |g{l}|. route: "loops"
+    or "f64"."""
     if route == "loops":
         dfwd, ddgrad, dwgrad = dfp_linear_fwd, dfp_linear_dgrad, dfp_linear_wgrad
     elif route == "f64":
@@ -593,12 +692,14 @@ def dfp16_step(weights, exp_w, x, exp_x, eta=DFP_ETA, target_bits=DFP_BITS, rout
     else:
         raise ValueError(route)
     L = len(weights)
+    ew = list(exp_w) if isinstance(exp_w, (list, tuple)) else [exp_w] * L
+    wb = list(wbits) if wbits is not None else [16] * L
     r = {}
     act = [np.ascontiguousarray(x, np.int16)]
     ex = [exp_x]
     for l in range(L):
         p = dfwd(act[-1], weights[l])
-        y, e_y, rs, m = dfp_down(p, ex[-1] + exp_w, target_bits)
+        y, e_y, rs, m = dfp_down(p, ex[-1] + ew[l], target_bits)
         r["p%d" % l], r["pmax%d" % l], r["rs%d" % l], r["y%d" % l], r["ey%d" % l] = p, m, rs, y, e_y
         act.append(y)
         ex.append(e_y)
@@ -607,13 +708,14 @@ def dfp16_step(weights, exp_w, x, exp_x, eta=DFP_ETA, target_bits=DFP_BITS, rout
     for l in range(L - 1, -1, -1):
         if l > 0:
             pd = ddgrad(e, weights[l])
-            e_prev, ee_prev, rs, m = dfp_down(pd, ee + exp_w, target_bits)
+            e_prev, ee_prev, rs, m = dfp_down(pd, ee + ew[l], target_bits)
             r["pd%d" % l], r["pdmax%d" % l], r["rsd%d" % l] = pd, m, rs
             r["e%d" % (l - 1)], r["ee%d" % (l - 1)] = e_prev, ee_prev
         pg = dwgrad(e, act[l])
         g, eg, rs, m = dfp_down(pg, ee + ex[l], target_bits)
-        k = exp_w + eta - eg
-        wn, nz = dfp_update(weights[l], g, k)
+        k = ew[l] + eta - eg
+        wn, nz = dfp_update(weights[l], g, k, wb[l])
+        r["gabs%d" % l] = abs_sum16(g)
         r["pg%d" % l], r["pgmax%d" % l], r["rsg%d" % l], r["g%d" % l], r["eg%d" % l] = pg, m, rs, g, eg
         r["k%d" % l], r["w%d" % l], r["nz%d" % l] = k, wn, nz
         if l > 0:
@@ -638,7 +740,7 @@ def run_steps(workload, steps: int, start_weights=None, callback=None, route="lo
         elif w.kind == "cnn":
             rec = cnn_step(weights, x, labels, w.convs)
         elif w.kind == "dfp16":
-            rec = dfp16_step(weights, w.exp_w, x, w.exp_x, route=route)
+            rec = dfp16_step(weights, w.exp_w, x, w.exp_x, eta=w.eta, route=route)
         else:
             raise ValueError(w.kind)
         weights = [rec["w%d" % l] for l in range(len(weights))]

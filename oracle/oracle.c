@@ -29,6 +29,9 @@
  *           and 3.1 "DFP Tensor Primitives" (f = i * 2^Es, one signed 8-bit
  *           exponent per tensor, products carry exponent Ea + Eb, down-convert
  *           by a right shift Rs with a new exponent).
+ *   [APT]   "Adaptive Precision Training for Resource Constrained Devices",
+ *           section III (k-bit weights, minimum resolution epsilon, Gavg,
+ *           Algorithm 1).
  *
  * Readings where the pages leave a step open are stated at each function.
  */
@@ -666,14 +669,17 @@ void ora_p64_to_float(const int64_t *P, int64_t n, int32_t E, float *out)
     for (int64_t i = 0; i < n; i++) out[i] = ldexpf((float)P[i], E);
 }
 
-/* Integer SGD on a DFP-16 weight tensor with a fixed exponent E_W, learning
- * rate 2^-eta: W <- W - G * 2^(E_G - eta - E_W). With k = E_W + eta - E_G the
- * step is dW = rhu(Gm, k) for k >= 0 and Gm * 2^-k for k < 0; then
- * W = sat16(W - dW). A left shift beyond 17 bits already exceeds every
- * representable difference, so it is capped at 17 without changing the
- * saturated result. Returns the number of nonzero dW. */
-int64_t ora_dfp_update(int16_t *W, const int16_t *Gm, int64_t n, int32_t k)
+/* Integer SGD on a DFP weight tensor of `bits`-bit mantissas (bits <= 16)
+ * with exponent E_W, learning rate 2^-eta: W <- W - G * 2^(E_G - eta - E_W).
+ * With k = E_W + eta - E_G the step is dW = rhu(Gm, k) for k >= 0 and
+ * Gm * 2^-k for k < 0; then W is saturated to the symmetric bits-bit range
+ * [-(2^(bits-1) - 1), 2^(bits-1) - 1] (bits = 16 is sat16). A left shift
+ * beyond 17 bits already exceeds every representable difference, so it is
+ * capped at 17 without changing the saturated result. Returns the number of
+ * nonzero dW. */
+int64_t ora_dfp_update(int16_t *W, const int16_t *Gm, int64_t n, int32_t k, int32_t bits)
 {
+    const int64_t lim = ((int64_t)1 << (bits - 1)) - 1;
     int64_t nonzero = 0;
     for (int64_t i = 0; i < n; i++) {
         int64_t dw;
@@ -682,7 +688,40 @@ int64_t ora_dfp_update(int16_t *W, const int16_t *Gm, int64_t n, int32_t k)
         else
             dw = (int64_t)Gm[i] * ((int64_t)1 << (-k > 17 ? 17 : -k));
         if (dw != 0) nonzero++;
-        W[i] = (int16_t)ora_sat16((int64_t)W[i] - dw);
+        int64_t v = (int64_t)W[i] - dw;
+        if (v > lim) v = lim;
+        if (v < -lim) v = -lim;
+        W[i] = (int16_t)v;
     }
     return nonzero;
+}
+
+/* [APT] "Adaptive Precision Training for Resource Constrained Devices",
+ * section III: a layer's weights are a k-bit quantised tensor; its precision k
+ * is raised or lowered by Algorithm 1. Reading: the weights are k-bit
+ * mantissas with one shared power-of-two exponent E (the DFP representation
+ * of [DFP] section 3), so the minimum resolution epsilon is 2^E. Going from
+ * bits_old to bits_new = bits_old + d:
+ *   d >= 0: W <- W * 2^d, E <- E - d (every value kept exactly);
+ *   d <  0: W <- clamp(rhu(W, -d), +-(2^(bits_new-1) - 1)), E <- E - d.
+ * Returns the exponent change (-d). */
+int32_t ora_dfp_set_bits(int16_t *W, int64_t n, int32_t bits_old, int32_t bits_new)
+{
+    const int32_t d = bits_new - bits_old;
+    const int64_t lim = ((int64_t)1 << (bits_new - 1)) - 1;
+    for (int64_t i = 0; i < n; i++) {
+        int64_t v = d >= 0 ? (int64_t)W[i] * ((int64_t)1 << d) : ora_rhu(W[i], -d);
+        if (v > lim) v = lim;
+        if (v < -lim) v = -lim;
+        W[i] = (int16_t)v;
+    }
+    return -d;
+}
+
+/* sum of |x| over an int16 tensor (the numerator of [APT] Equation 4's mean) */
+int64_t ora_abs_sum16(const int16_t *x, int64_t n)
+{
+    int64_t s = 0;
+    for (int64_t i = 0; i < n; i++) s += x[i] < 0 ? -(int64_t)x[i] : (int64_t)x[i];
+    return s;
 }

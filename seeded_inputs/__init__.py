@@ -98,6 +98,21 @@ def round_clamp_normal(seed: int, stream: int, n: int, sigma: float, lim: int) -
 # --------------------------------------------------------------------------
 
 @dataclasses.dataclass(frozen=True)
+class AptSetting:
+    """Adaptive precision training (Algorithms 1-2 of "Adaptive Precision
+    Training for Resource Constrained Devices"): initial weight precision,
+    precision limits, Gavg thresholds, epoch length in steps and the step
+    interval of Gavg evaluations within an epoch."""
+    k_init: int = 6
+    k_min: int = 2
+    k_max: int = 16
+    t_min: float = 1.0
+    t_max: float = float("inf")
+    epoch: int = 10
+    eval_every: int = 1
+
+
+@dataclasses.dataclass(frozen=True)
 class Workload:
     index: int
     name: str
@@ -112,9 +127,11 @@ class Workload:
     lim: int = 127            # clamp for weights and inputs
     exp_x: int = 0            # dfp16 shared exponents of input and weights
     exp_w: int = 0
+    eta: int = 20             # dfp16 integer SGD learning rate 2^-eta (on the batch-summed gradient)
     input_uint8: bool = False # mlp: UINT8 input in [0, 255] (partial-model training)
     trainable_from: int = 0   # mlp: layers before this one are frozen
     static_requant: tuple = ()  # mlp: per layer (k_lo, k_hi) of a static requantisation, () = dynamic
+    apt: AptSetting = None    # dfp16: adaptive per-layer weight precision
 
     @property
     def seed(self) -> int:
@@ -136,6 +153,10 @@ WORKLOADS = (
     # the TI library's forward: static per-channel requantisation with trained INT32 offsets
     Workload(6, "mlp784-1024x3-10_b256_static", "mlp", 256, dims=(784, 1024, 1024, 1024, 10), classes=10,
              static_requant=((24, 25), (24, 25), (24, 25), (22, 23))),
+    # adaptive precision training on the DFP16 stack: weights start at 6 bits
+    Workload(7, "dfp16_2048x3_b2048_apt6", "dfp16", 2048, dims=(2048, 2048, 2048, 2048),
+             sigma=4096.0, lim=32767, exp_x=-12, exp_w=-17,
+             apt=AptSetting(k_init=6, k_min=2, k_max=16, t_min=100.0, t_max=float("inf"), epoch=10, eval_every=1)),
 )
 
 

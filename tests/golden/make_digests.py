@@ -45,16 +45,27 @@ def main():
     tmp = path + ".tmp"
     t0 = time.time()
     with open(tmp, "w") as f:
-        def cb(t, rec):
+        def cb(t, rec, extra=None):
             x, labels = si.make_batch(w, t)
             d = {"step": t, "in.x": digest(x)}
             if labels is not None:
                 d["in.labels"] = digest(labels)
             d.update(record_digests(rec))
+            d.update(extra or {})
             f.write(json.dumps(d, sort_keys=True) + "\n")
             f.flush()
             print("step %d  %.1fs" % (t, time.time() - t0), flush=True)
-        O.run_steps(w, steps, callback=cb, route=route)
+        if w.apt is not None:
+            # adaptive precision: also the precision state after each step, and the
+            # epoch's mean Gavg per layer (float64, exact in JSON) when an epoch ends
+            def cb_apt(t, rec, st):
+                cb(t, rec, extra={**{"apt.bits%d" % l: b for l, b in enumerate(st["bits"])},
+                                  **{"apt.exp_w%d" % l: e for l, e in enumerate(st["exp_w"])},
+                                  **({"apt.gavg%d" % l: g for l, g in enumerate(st["gavg"])}
+                                     if st["gavg"] is not None and t % w.apt.epoch == w.apt.epoch - 1 else {})})
+            O.apt_run(w, steps, callback=cb_apt, route=route)
+        else:
+            O.run_steps(w, steps, callback=cb, route=route)
     os.replace(tmp, path)
 
 

@@ -109,7 +109,7 @@ class DfpRun:
         self.torch = torch
         self.ito = import_ito()
         self.w = w
-        self.m = self.ito.Dfp16Model(list(w.dims), w.batch, w.exp_w, O.DFP_ETA)
+        self.m = self.ito.Dfp16Model(list(w.dims), w.batch, w.exp_w, w.eta)
         for l, W in enumerate(si.make_weights(w)):
             self.m.set_weights(l, W)
 
@@ -137,12 +137,12 @@ class DfpRun:
 
 def test_dfp_model_small_lockstep():
     w = si.Workload(97, "dfp16_small", "dfp16", 16, dims=(64, 48, 32), sigma=4096.0, lim=32767,
-                    exp_x=-12, exp_w=-17)
+                    exp_x=-12, exp_w=-17, eta=8)
     g = DfpRun(w)
     weights = si.make_weights(w)
     for t in range(5):
         x, _ = si.make_batch(w, t)
-        rec = O.dfp16_step(weights, w.exp_w, x, w.exp_x)
+        rec = O.dfp16_step(weights, w.exp_w, x, w.exp_x, eta=w.eta)
         g.step(t)
         compare_records(rec, g.record(), t)
         weights = [rec["w%d" % l] for l in range(len(weights))]
@@ -153,7 +153,7 @@ def test_dfp_model_full_size_live_step():
     g = DfpRun(w)
     weights = si.make_weights(w)
     x, _ = si.make_batch(w, 0)
-    rec = O.dfp16_step(weights, w.exp_w, x, w.exp_x, route="f64")
+    rec = O.dfp16_step(weights, w.exp_w, x, w.exp_x, eta=w.eta, route="f64")
     g.step(0)
     compare_records(rec, g.record(), 0)
 

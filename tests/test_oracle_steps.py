@@ -36,7 +36,7 @@ def test_tiny_dfp16_step_hand_worked():
     g = load_golden("tiny_dfp16_step.txt")
     W0 = np.array(g["W0"], np.int16).reshape(1, 2)
     x = np.array([g["x"]], np.int16)
-    r = O.dfp16_step([W0], g["exp_w"][0], x, g["exp_x"][0])
+    r = O.dfp16_step([W0], g["exp_w"][0], x, g["exp_x"][0], eta=g["eta"][0])
     for k in ("p0", "y0", "pg0", "g0", "w0"):
         assert r[k].ravel().tolist() == g[k], k
     for k in ("rs0", "ey0", "rsg0", "eg0", "k0"):
@@ -96,7 +96,7 @@ def test_cnn_small_step_invariants():
 
 def test_dfp16_small_steps_exponents_track():
     w = si.Workload(99, "dfp16_small", "dfp16", 16, dims=(64, 48, 32), sigma=4096.0,
-                    lim=32767, exp_x=-12, exp_w=-17)
+                    lim=32767, exp_x=-12, exp_w=-17, eta=8)
     seen = []
 
     def cb(t, r):
