@@ -299,11 +299,17 @@ int ito_model_create(const ito_layer_desc *layers, int n_layers, int batch, ito_
  *    trainable_layers_from_last = n_layers - trainable_from;
  *  - packed_masks: the ReLU masks of the backward pass are kept bit-packed,
  *    ceil(out_size / 8) bytes per sample and ReLU layer (each such layer's
- *    output width must be a multiple of 8). */
+ *    output width must be a multiple of 8);
+ *  - pingpong_grads: the deltas of all layers share two buffers ("Grad
+ *    Buffers": two ping-pong buffers sized batch * the largest layer output)
+ *    instead of one per layer; layer l's delta lives in buffer l % 2, so after
+ *    a step only the deltas of layers 0 and 1 remain readable (the tensor
+ *    names e<l> of higher layers alias them). */
 typedef struct ito_model_options {
     int32_t input_uint8;
     int32_t trainable_from;
     int32_t packed_masks;
+    int32_t pingpong_grads;
 } ito_model_options;
 
 /* ito_model_create with options (NULL = all zero, the same as

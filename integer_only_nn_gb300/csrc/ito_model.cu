@@ -86,6 +86,9 @@ struct ito_model {
     int8_t* pa8 = nullptr;
     uint16_t* pab = nullptr;
     int8_t* pe8 = nullptr;
+    // ping-pong delta buffers (pingpong_grads)
+    int8_t* gbuf8[2] = {nullptr, nullptr};
+    uint16_t* gbufb[2] = {nullptr, nullptr};
     int32_t* stats = nullptr;
     int n_stats = 0;
     uint32_t* discard_max = nullptr;   // max target of the patch-space conv delta (not a NITI tensor)
@@ -294,8 +297,26 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         const bool next_linear = l + 1 < nl && m->L[l + 1].kind != ITO_LAYER_CONV3X3_RELU && !conv;
         if (next_linear) ITO_TRY(m->alloc(&L.ab, (size_t)L.rows_out * L.lda));
         L.lde = pad8(L.OC);
-        ITO_TRY(m->alloc(&L.e8, (size_t)L.rows_out * L.OC));
-        ITO_TRY(m->alloc(&L.eb, (size_t)L.rows_out * L.lde));
+        if (m->opt.pingpong_grads) {
+            // two delta buffers for all layers: layer l writes buffer l % 2, which no layer
+            // still needs (layer l + 2's delta was consumed by its weight gradient and update)
+            if (!m->gbuf8[0]) {
+                size_t n8 = 0, nb = 0;
+                for (const MLayer& Q : m->L) {
+                    n8 = std::max(n8, (size_t)Q.rows_out * Q.OC);
+                    nb = std::max(nb, (size_t)Q.rows_out * pad8(Q.OC));
+                }
+                for (int i = 0; i < 2; ++i) {
+                    ITO_TRY(m->alloc(&m->gbuf8[i], n8));
+                    ITO_TRY(m->alloc(&m->gbufb[i], nb));
+                }
+            }
+            L.e8 = m->gbuf8[l % 2];
+            L.eb = m->gbufb[l % 2];
+        } else {
+            ITO_TRY(m->alloc(&L.e8, (size_t)L.rows_out * L.OC));
+            ITO_TRY(m->alloc(&L.eb, (size_t)L.rows_out * L.lde));
+        }
         ITO_TRY(m->alloc(&L.g32, (size_t)L.OC * L.K));
         if (m->opt.packed_masks && L.relu) ITO_TRY(m->alloc(&L.mask, (size_t)L.rows_out * (L.OC / 8)));
         if (!conv) {

@@ -36,14 +36,16 @@ def import_ito():
 class GpuRun:
     """A CUDA model of a seeded mlp/cnn workload, stepped one batch at a time."""
 
-    def __init__(self, workload, batch=None, packed_masks=False):
+    def __init__(self, workload, batch=None, packed_masks=False, pingpong_grads=False):
         import torch
         self.torch = torch
         self.ito = import_ito()
         self.w = workload
         self.batch = batch or workload.batch
         self.model = self.ito.Model(self.ito.layers_for(workload), self.batch, input_uint8=workload.input_uint8,
-                                    trainable_from=workload.trainable_from, packed_masks=packed_masks)
+                                    trainable_from=workload.trainable_from, packed_masks=packed_masks,
+                                    pingpong_grads=pingpong_grads)
+        self.pingpong = pingpong_grads
         self.n_layers = self.model.n_weight_layers
         for l, W in enumerate(si.make_weights(workload)):
             self.model.set_weights(l, W)
@@ -71,6 +73,8 @@ class GpuRun:
                     continue
                 if k in ("e", "g") and l < first:
                     continue
+                if k == "e" and self.pingpong and l >= 2:
+                    continue    # aliases the buffer of layer l % 2
                 out.append("%s%d" % (k, l))
         if self.w.kind == "cnn":
             out += ["p", "pa", "pe"]

@@ -80,3 +80,24 @@ def test_u8_contraction_exact_at_extremes():
     assert (y0[:, 0::2] == 784 * 255 * -128).all() and (y0[:, 1::2] == 784 * 255 * 127).all()
     assert np.array_equal(y0, O.linear_fwd_u8(x, W0))
     assert ito.ito_get_error() == 0
+
+
+@pytest.mark.parametrize("index", [1, 2, 5])
+def test_pingpong_grads_lockstep(index):
+    """Deltas in two shared buffers ("Grad Buffers", section 8): the steps equal
+    the oracle's (every tensor still readable, the weights of every layer over
+    several steps); the buffers really are shared (e2 aliases e0)."""
+    w = si.by_name(index)
+    g = GpuRun(w, pingpong_grads=True)
+    weights = si.make_weights(w)
+    for t in range(3):
+        x, labels = si.make_batch(w, t)
+        if w.kind == "mlp":
+            rec = O.mlp_step(weights, x, labels, trainable_from=w.trainable_from)
+        else:
+            rec = O.cnn_step(weights, x, labels, w.convs)
+        g.step(t)
+        compare_records(rec, g.record(), t)
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+    if g.n_layers > 2:
+        assert g.model.tensor("e2").data_ptr() == g.model.tensor("e0").data_ptr()
