@@ -10,7 +10,9 @@
 // split into balanced limbs v = 256 * h + l with l in [-128, 127] and h in
 // [-128, 128]; both are exact in bf16. Then
 //   sum v*w = 65536 * sum(h_v h_w) + 256 * sum(h_v l_w + l_v h_w) + sum(l_v l_w),
-// four bf16 tensor-core products into three fp32 accumulators in tensor memory.
+// four limb products into three fp32 accumulators (hh, mid, ll) laid side by
+// side in tensor memory, issued as two tensor-core MMAs of twice the tile
+// width: h_v x [h_w | l_w] into [hh | mid] and l_v x [h_w | l_w] into [mid | ll].
 // Every limb product is at most 2^14 in magnitude, so over a chunk of 512 K
 // terms each accumulator stays within 2^24 (the middle one gets two products
 // per term) and holds an exact integer. After each chunk the epilogue combines
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;                        // 32 columns per epilogue warp
     constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    // the two B limb planes are adjacent in shared memory, so [B_hi | B_lo] is one N = 2 * BN operand
+    constexpr uint32_t IDESC2 = idesc_bf16_f32(BM, 2 * BN, A_MN, B_MN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -159,11 +163,18 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
                             const uint64_t al = smem_desc_sw128(al0 + ao, albo, 1024);
                             const uint64_t bh = smem_desc_sw128(bh0 + bo, blbo, 1024);
                             const uint64_t bl = smem_desc_sw128(bl0 + bo, blbo, 1024);
-                            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-                            tc_mma_bf16(d_hh, ah, bh, IDESC, acc);
-                            tc_mma_bf16(d_mid, ah, bl, IDESC, acc);
-                            tc_mma_bf16(d_mid, al, bh, IDESC, 1u);
-                            tc_mma_bf16(d_ll, al, bl, IDESC, acc);
+                            // A_hi x [B_hi | B_lo] accumulates into columns [hh | mid] and
+                            // A_lo x [B_hi | B_lo] into [mid | ll]: the middle accumulator gets
+                            // both cross products. The first step of a chunk starts ll on its own
+                            // so that it does not overwrite mid.
+                            if (kb > kb0 || k > 0) {
+                                tc_mma_bf16(d_hh, ah, bh, IDESC2, 1u);
+                                tc_mma_bf16(d_mid, al, bh, IDESC2, 1u);
+                            } else {
+                                tc_mma_bf16(d_hh, ah, bh, IDESC2, 0u);
+                                tc_mma_bf16(d_ll, al, bl, IDESC, 0u);
+                                tc_mma_bf16(d_mid, al, bh, IDESC, 1u);
+                            }
                         }
                         tc_commit(&empty_bar[stage]);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
