@@ -62,6 +62,23 @@ struct TileSched {
     }
 };
 
+// Work list of the CTA-pair kernel: the first `full` tiles whole, then each of
+// the remaining tiles (the last, partial wave) split along K into `parts`
+// chunk-aligned pieces, so that the partial wave keeps more SMs busy. A piece
+// writes its int32 partial tile to workspace slot `slot`; k_tail_reduce adds
+// the pieces exactly afterwards.
+struct WorkItem {
+    int tile, c0, c1, slot;   // chunks [c0, c1); slot -1: a whole tile written to C
+};
+
+__device__ __forceinline__ WorkItem work_item(int w, int full, int parts, int num_chunks)
+{
+    if (w < full) return WorkItem{w, 0, num_chunks, -1};
+    const int u = w - full;
+    const int ti = u / parts, part = u - ti * parts;
+    return WorkItem{full + ti, part * num_chunks / parts, (part + 1) * num_chunks / parts, u};
+}
+
 // ----------------------------------------------------- tensor-core kernel
 
 template <int BN>
@@ -331,9 +348,9 @@ struct Tc2Cfg {
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
-               int group, int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max,
-               int* __restrict__ err)
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP, int use_tma_store,
+               int M, int N, int K, int chunk_kb, int group, int full_tiles, int parts, int32_t* __restrict__ C,
+               int64_t ldc, uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
     using Cfg = Tc2Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -360,6 +377,7 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
     const int num_tiles = sched.num_m * sched.num_n;
     const int num_kb = (K + BK - 1) / BK;
     const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
+    const int total_work = full_tiles + (num_tiles - full_tiles) * parts;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -390,12 +408,14 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+            for (int w = cluster; ok && w < total_work; w += nclusters) {
+                const WorkItem wi = work_item(w, full_tiles, parts, num_chunks);
                 int tm, tn;
-                sched.coords(t, tm, tn);
+                sched.coords(wi.tile, tm, tn);
                 const int rowA = tm * 2 * BM + rank * BM;
                 const int rowB = tn * BN + rank * (BN / 2);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                const int kb_end = min(num_kb, wi.c1 * chunk_kb);
+                for (int kb = wi.c0 * chunk_kb; kb < kb_end; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
                     if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
                     const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
@@ -425,8 +445,9 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
-            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
-                for (int c = 0; ok && c < num_chunks; ++c) {
+            for (int w = cluster; ok && w < total_work; w += nclusters) {
+                const WorkItem wi = work_item(w, full_tiles, parts, num_chunks);
+                for (int c = wi.c0; ok && c < wi.c1; ++c) {
                     if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
@@ -464,13 +485,14 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
-        for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+        for (int w = cluster; ok && w < total_work; w += nclusters) {
+            const WorkItem wi = work_item(w, full_tiles, parts, num_chunks);
             int tm, tn;
-            sched.coords(t, tm, tn);
+            sched.coords(wi.tile, tm, tn);
             int32_t acc[HALF];
 #pragma unroll
             for (int i = 0; i < HALF; ++i) acc[i] = 0;
-            for (int c = 0; c < num_chunks; ++c) {
+            for (int c = wi.c0; c < wi.c1; ++c) {
                 if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr =
@@ -489,6 +511,27 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
                 if (++buf == 2) { buf = 0; buf_phase ^= 1; }
             }
             if (!ok) break;
+            if (wi.slot >= 0) {
+                // a piece of a split tile: its partial sum goes to workspace slot wi.slot
+                // (rows slot * 256 .. +255 of the partials map); k_tail_reduce finishes it
+                const int prow = wi.slot * 2 * BM + (int)rank * BM + quad * 32;
+#pragma unroll
+                for (int g = 0; g < HALF / 32; ++g) {
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), acc[g * 32 + 4 * j], acc[g * 32 + 4 * j + 1],
+                                     acc[g * 32 + 4 * j + 2], acc[g * 32 + 4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmP, stg, half * HALF + g * 32, prow);
+                        bulk_commit();
+                    }
+                }
+                continue;
+            }
             uint32_t mx = 0;
 #pragma unroll
             for (int i = 0; i < HALF; ++i) mx = max(mx, abs_u32(acc[i]));
@@ -654,6 +697,45 @@ __global__ void k_splitk_reduce(const int32_t* __restrict__ P, int splits, int64
     if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
 }
 
+// The split tiles of the pair kernel's last wave: C = the sum of each tile's
+// `parts` partial tiles (exact integer sums), written inside the M x N bounds;
+// max |C| folded into *d_max. P holds [tail tiles][parts][256][256] int32.
+__global__ void k_tail_reduce(const int32_t* __restrict__ P, int tail_tiles, int parts, int full_tiles,
+                              TileSched sched, int M, int N, int64_t ldc, int32_t* __restrict__ C,
+                              uint32_t* __restrict__ d_max)
+{
+    constexpr int T = 256;
+    const int64_t n = (int64_t)tail_tiles * T * (T / 4);
+    uint32_t mx = 0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int ti = (int)(i / (T * (T / 4)));
+        const int rem = (int)(i - (int64_t)ti * (T * (T / 4)));
+        const int r = rem / (T / 4), c = (rem % (T / 4)) * 4;
+        int4 acc = make_int4(0, 0, 0, 0);
+        for (int q = 0; q < parts; ++q) {
+            const int4 v = __ldcs(reinterpret_cast<const int4*>(P + (((int64_t)ti * parts + q) * T + r) * T + c));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        int tm, tn;
+        sched.coords(full_tiles + ti, tm, tn);
+        const int gr = tm * T + r, gc = tn * T + c;
+        if (gr < M) {
+            const int32_t a[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (gc + j < N) {
+                    C[(int64_t)gr * ldc + gc + j] = a[j];
+                    mx = max(mx, abs_u32(a[j]));
+                }
+        }
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+}
+
 template <int BN, bool A_MN, bool B_MN>
 static int launch_tc(const GemmPlan& p, cudaStream_t s)
 {
@@ -683,15 +765,17 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
     return ITO_OK;
 }
 
+// CTA pairs of k_gemm_tc2<A_MN, B_MN> that fit on the device at once (its
+// persistent grid); sets the kernel's shared-memory limit on first use.
 template <bool A_MN, bool B_MN>
-static int launch_tc2(const GemmPlan& p, cudaStream_t s)
+static int pair_clusters()
 {
     using Cfg = Tc2Cfg;
     auto kern = k_gemm_tc2<A_MN, B_MN>;
     static int max_clusters = 0;
     if (!max_clusters) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
-            return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
+            return 0;
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(2 * num_sms());
         q.blockDim = dim3(Cfg::THREADS);
@@ -704,12 +788,63 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
         q.attrs = qa;
         q.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1)
-            return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1) return 0;
         max_clusters = n;
     }
+    return max_clusters;
+}
+
+static int pair_clusters_for(bool a_mn, bool b_mn)
+{
+    if (!a_mn && !b_mn) return pair_clusters<false, false>();
+    if (!a_mn && b_mn) return pair_clusters<false, true>();
+    if (a_mn && b_mn) return pair_clusters<true, true>();
+    return pair_clusters<true, false>();
+}
+
+// Tail split of a pair-kernel contraction: how many of the tiles run whole and
+// into how many K pieces each remaining tile of the last, partial wave is cut.
+// Estimated time: waves of whole tiles + rounds of pieces (each 1/parts of a
+// tile), plus the reduction pass (the pieces written and read back once, at
+// about 5 TB/s, and one launch). A tile takes 2 * 256 * 256 * K operations at
+// about 23 TFLOP/s per CTA pair (the measured pair-kernel rate).
+struct TailSplit {
+    int full, parts;
+};
+
+static TailSplit tail_split(int tiles, int clusters, int num_chunks, int K)
+{
+    TailSplit best{tiles, 1};
+    if (clusters < 1 || tiles % clusters == 0) return best;
+    const int waves = tiles / clusters, r = tiles % clusters;
+    const double tile_us = 2.0 * 256 * 256 * K / 23.0e6;
+    double best_t = (waves + 1.0) * tile_us;
+    for (int parts = 2; parts <= 4 && parts <= num_chunks; ++parts) {
+        const double reduce_us = 3.0 + 2.0 * r * parts * 256.0 * 256 * 4 / 5.0e6;
+        const double t = (waves + (double)((r * parts + clusters - 1) / clusters) / parts) * tile_us + reduce_us;
+        if (t < best_t) {
+            best_t = t;
+            best = TailSplit{tiles - r, parts};
+        }
+    }
+    return best;
+}
+
+static size_t tail_ws_bytes(const TailSplit& ts, int tiles)
+{
+    return ts.parts > 1 ? (size_t)(tiles - ts.full) * ts.parts * 256 * 256 * sizeof(int32_t) : 0;
+}
+
+template <bool A_MN, bool B_MN>
+static int launch_tc2(const GemmPlan& p, cudaStream_t s)
+{
+    using Cfg = Tc2Cfg;
+    auto kern = k_gemm_tc2<A_MN, B_MN>;
+    const int max_clusters = pair_clusters<A_MN, B_MN>();
+    if (!max_clusters) return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
     const int tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
-    const int clusters = tiles < max_clusters ? tiles : max_clusters;
+    const int work = p.tail_full + (tiles - p.tail_full) * p.tail_parts;
+    const int clusters = work < max_clusters ? work : max_clusters;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(Cfg::THREADS);
@@ -722,9 +857,17 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.use_tma_store, p.M, p.N, p.K,
-                                       p.chunk_kb, p.group, p.C, p.ldc, p.d_max, p.err);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.mapP, p.use_tma_store, p.M, p.N, p.K,
+                                       p.chunk_kb, p.group, p.tail_full, p.tail_parts, p.C, p.ldc, p.d_max, p.err);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "pair gemm launch: %s", cudaGetErrorString(e));
+    if (p.tail_parts > 1) {
+        const TileSched sched{(p.M + 255) / 256, (p.N + 255) / 256, p.group};
+        const int tail = tiles - p.tail_full;
+        k_tail_reduce<<<launch_grid_blocks((int64_t)tail * 256 * 64, 256), 256, 0, s>>>(
+            p.split_ws, tail, p.tail_parts, p.tail_full, sched, p.M, p.N, p.ldc, p.C, p.d_max);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "tail reduce launch: %s", cudaGetErrorString(e));
+    }
     return ITO_OK;
 }
 
@@ -743,10 +886,24 @@ static int split_count(int M, int N, int K)
     return (num_kb + per - 1) / per;
 }
 
+static bool pair_eligible(int M, int N, int splits)
+{
+    static const int pair_env = [] {
+        const char* v = getenv("ITO_GEMM_PAIR");
+        return v ? atoi(v) : 1;
+    }();
+    return pair_env != 0 && M >= 256 && N >= 256 && splits == 1;
+}
+
 size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc)
 {
     const int s = split_count(M, N, K);
-    return s > 1 ? (size_t)s * M * ldc * sizeof(int32_t) : 0;
+    if (s > 1) return (size_t)s * M * ldc * sizeof(int32_t);
+    if (!pair_eligible(M, N, s)) return 0;
+    // pair kernel: partial tiles of the split last wave (operand layouts share one occupancy)
+    const int tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    const int num_chunks = ((K + 63) / 64 + kExactChunk / 64 - 1) / (kExactChunk / 64);
+    return tail_ws_bytes(tail_split(tiles, pair_clusters_for(false, false), num_chunks, K), tiles);
 }
 
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
@@ -775,10 +932,6 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
     if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     p->bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
     // CTA-pair kernel for large tiles; ITO_GEMM_PAIR=0 in the environment forces the single-CTA kernel
-    static const int pair_env = [] {
-        const char* v = getenv("ITO_GEMM_PAIR");
-        return v ? atoi(v) : 1;
-    }();
     p->splits = 1;
     p->kb_per_split = (K + 63) / 64;
     const int splits = split_count(M, N, K);
@@ -789,13 +942,39 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
         p->split_ws = split_ws;
         p->split_stride = (int64_t)M * ldc;
     }
-    p->pair = pair_env != 0 && M >= 256 && N >= 256 && p->splits == 1;
+    p->pair = pair_eligible(M, N, p->splits);
     // tiles are rastered in groups of `group` row tiles; ITO_GEMM_GROUP overrides (tuning)
     static const int group_env = [] {
         const char* v = getenv("ITO_GEMM_GROUP");
         return v ? atoi(v) : 0;
     }();
     p->group = group_env > 0 ? group_env : 16;
+    // pair kernel: split the last partial wave along K when the workspace holds the partial tiles
+    p->tail_full = ((M + 255) / 256) * ((N + 255) / 256);
+    p->tail_parts = 1;
+    if (p->pair && split_ws) {
+        const int tiles = p->tail_full;
+        const int num_chunks = ((K + 63) / 64 + p->chunk_kb - 1) / p->chunk_kb;
+        const int clusters = pair_clusters_for(a_mn, b_mn);
+        if (!clusters) return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
+        const TailSplit ts = tail_split(tiles, clusters, num_chunks, K);
+        const size_t need = tail_ws_bytes(ts, tiles);
+        if (ts.parts > 1 && need <= split_ws_bytes) {
+            p->tail_full = ts.full;
+            p->tail_parts = ts.parts;
+            p->split_ws = split_ws;
+            auto enc = get_encode();
+            cuuint64_t dims[2] = {256, (cuuint64_t)(tiles - ts.full) * ts.parts * 256};
+            cuuint64_t strides[1] = {256 * 4};
+            cuuint32_t box[2] = {32, 32};
+            cuuint32_t estr[2] = {1, 1};
+            CUresult cr = enc(&p->mapP, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, split_ws, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (cr != CUDA_SUCCESS)
+                return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (partials) failed (%d)", (int)cr);
+        }
+    }
     int r = make_map_bf16(&p->mapA, A, a_mn ? 64 : 128);
     if (r) return r;
     // the pair kernel loads half of a 256-wide B tile per CTA

@@ -33,9 +33,11 @@ struct Bf16View {
 // A is [M][K] (K-major) or [K][M] (a_mn); B is [N][K] or [K][N] (b_mn).
 struct GemmPlan {
     CUtensorMap mapA, mapB, mapC;
+    CUtensorMap mapP;             // pair kernel: partial tiles of the split last wave (in split_ws)
     int use_tma_store;
     int pair;   // CTA-pair (cta_group::2) kernel
     int group;  // row tiles per raster group (L2 reuse)
+    int tail_full, tail_parts;    // pair kernel: whole tiles, K pieces per remaining tile (1: no split)
     int M, N, K, bn, chunk_kb;
     int splits, kb_per_split;     // split-K: slices of kb_per_split K blocks (splits == 1: none)
     int32_t* split_ws;            // [splits][M][ldc] int32 partials

@@ -163,3 +163,28 @@ def test_update_zero_gradient_leaves_weights(ito):
     sh, ws, nz = ito.ito_niti_update(Wd, _dev(np.zeros(4096, np.int32)), _dev(np.zeros(1, np.int32)))
     assert (int(_host(sh)[0]), int(_host(ws)[0]), int(_host(nz)[0])) == (0, 0, 0)
     assert np.array_equal(_host(Wd), W)
+
+
+@pytest.mark.parametrize("B,IC,OC", [(8192, 2000, 3000), (8192, 4096, 4096)])
+def test_wgrad_last_wave_split(ito, B, IC, OC):
+    """Weight gradients whose last wave of 256 x 256 pair tiles is split along K
+    (3000 x 2000 outputs: 96 tiles, ragged edges; 4096 x 4096: 256 tiles)
+    against the oracle's exact float64 contraction."""
+    e, a = i8((B, OC)), i8((B, IC), 0, 127)
+    G, mx = ito.ito_linear_wgrad(_dev(e), _dev(a))
+    Gref = O.linear_wgrad_f64(e, a)
+    assert np.array_equal(_host(G), Gref)
+    assert _u32(mx) == O.absmax32(Gref)
+    assert ito.ito_get_error() == 0
+
+
+def test_fwd_last_wave_split(ito):
+    """A forward contraction (K-major operands) with a split last wave:
+    3000 x 2000 outputs, K = 8192, ragged edges."""
+    x, W = i8((3000, 8192)), i8((2000, 8192), -127, 127)
+    y32, mx, sh, y = ito.ito_linear_fwd(_dev(x), _dev(W), 1)
+    Y = O.linear_fwd_f64(x, W)
+    assert np.array_equal(_host(y32), Y)
+    a, s, m = O.requant(Y, relu=True)
+    assert (_u32(mx), int(_host(sh)[0])) == (m, s)
+    assert np.array_equal(_host(y), a)
