@@ -388,12 +388,25 @@ def run_op(args):
     import integer_only_nn_gb300 as ito
     B, IC, OC = (int(v) for v in args.shape.split(","))
     rng = np.random.default_rng(5)
-    x = torch.from_numpy(rng.integers(-127, 128, (B, IC)).astype(np.int8)).cuda()
-    W = torch.from_numpy(rng.integers(-127, 128, (OC, IC)).astype(np.int8)).cuda()
-    e = torch.from_numpy(rng.integers(-127, 128, (B, OC)).astype(np.int8)).cuda()
-    call = {"fwd": lambda: ito.ito_linear_fwd(x, W, 1),
-            "dgrad": lambda: ito.ito_linear_bwd_delta(e, W, x),
-            "wgrad": lambda: ito.ito_linear_wgrad(e, x)}[args.op]
+    if args.op in ("dfp16_fwd_f32", "bdfp16_fwd_f32"):
+        # DFP16 forward with FP32 output, one exponent per tensor or per block of IC
+        x = torch.from_numpy(rng.integers(-32767, 32768, (B, IC)).astype(np.int16)).cuda()
+        W = torch.from_numpy(rng.integers(-32767, 32768, (OC, IC)).astype(np.int16)).cuda()
+        nb = (IC + args.block - 1) // args.block
+        ex = torch.from_numpy(rng.integers(-40, 0, (B, nb)).astype(np.int8)).cuda()
+        ew = torch.from_numpy(rng.integers(-40, 0, (OC, nb)).astype(np.int8)).cuda()
+        exd, ewd = ito._i32dev(-12), ito._i32dev(-17)
+        call = {"dfp16_fwd_f32": lambda: ito.ito_dfp16_linear_fwd_f32(x, exd, W, ewd),
+                "bdfp16_fwd_f32": lambda: ito.ito_bdfp16_linear_fwd_f32(x, ex, W, ew, args.block)}[args.op]
+        ops_per_mac = 8.0      # four bf16 limb products per int16 multiply-accumulate
+    else:
+        x = torch.from_numpy(rng.integers(-127, 128, (B, IC)).astype(np.int8)).cuda()
+        W = torch.from_numpy(rng.integers(-127, 128, (OC, IC)).astype(np.int8)).cuda()
+        e = torch.from_numpy(rng.integers(-127, 128, (B, OC)).astype(np.int8)).cuda()
+        call = {"fwd": lambda: ito.ito_linear_fwd(x, W, 1),
+                "dgrad": lambda: ito.ito_linear_bwd_delta(e, W, x),
+                "wgrad": lambda: ito.ito_linear_wgrad(e, x)}[args.op]
+        ops_per_mac = 2.0
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
@@ -404,8 +417,11 @@ def run_op(args):
     s1.record()
     torch.cuda.synchronize()
     ms = s0.elapsed_time(s1) / args.steps
-    print(json.dumps({"op": args.op, "shape": [B, IC, OC], "ms_per_call": ms,
-                      "tflops_incl_conversions": 2.0 * B * IC * OC / (ms / 1000.0) / 1e12}), flush=True)
+    line = {"op": args.op, "shape": [B, IC, OC], "ms_per_call": ms,
+            "tflops_incl_conversions": ops_per_mac * B * IC * OC / (ms / 1000.0) / 1e12}
+    if args.op.startswith("bdfp"):
+        line["block"] = args.block
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -485,7 +501,9 @@ def main():
     ap.add_argument("--ref-batch", type=int, default=16, help="samples per reference-arm oracle step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graphs", action="store_true", help="launch every kernel directly (no CUDA graphs)")
-    ap.add_argument("--op", choices=("fwd", "dgrad", "wgrad"), help="time one single-layer call instead")
+    ap.add_argument("--op", choices=("fwd", "dgrad", "wgrad", "dfp16_fwd_f32", "bdfp16_fwd_f32"),
+                    help="time one single-layer call instead")
+    ap.add_argument("--block", type=int, default=512, help="Blocked-DFP block length for --op bdfp16_fwd_f32")
     ap.add_argument("--shape", default="8192,4096,4096", help="B,IC,OC for --op")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -480,6 +480,37 @@ int ito_dfp16_linear_fwd_f32(const int16_t *x, const int32_t *d_exp_x, const int
                              int B, int IC, int OC, void *workspace, size_t workspace_bytes, int64_t *p64,
                              uint64_t *d_max, float *y, void *stream);
 
+/* Blocked-DFP ("Mixed Precision Training of Convolutional Neural Networks
+ * using Integer Operations", section 3: Blocked-DFP raises the effective
+ * range with several fine-grained exponents per tensor; the page gives no
+ * block shape). Reading: each row of a [rows][cols] tensor is cut into blocks
+ * of `block` consecutive elements (the last one shorter when block does not
+ * divide cols), and each block is a DFP-16 tensor of its own with a signed
+ * 8-bit exponent, converted as ito_dfp16_from_float converts a tensor.
+ * mant: int16 [rows][cols]; exps: int8 [rows][ceil(cols / block)].
+ * A block exponent outside int8 sets ITO_ERR_EXPONENT in the device error
+ * word (the stored exponent is clamped), a non-finite input ITO_ERR_ARG.
+ * Errors: ITO_ERR_ARG (NULL pointer), ITO_ERR_SHAPE (a size < 1). */
+int ito_bdfp16_from_float(const float *f, int64_t rows, int64_t cols, int32_t block, int16_t *mant, int8_t *exps,
+                          void *stream);
+/* f = mant * 2^exp of its block (rounded once to float). */
+int ito_bdfp16_to_float(const int16_t *mant, const int8_t *exps, int64_t rows, int64_t cols, int32_t block, float *f,
+                        void *stream);
+
+/* Linear forward with FP32 output over Blocked-DFP operands blocked along the
+ * contraction with the same block length (section 4: the kernels produce FP32
+ * outputs from DFP operands):
+ *   y[b][oc] = float( sum over blocks j, in order, in double, of
+ *                     P_j * 2^(ex[b][j] + ew[oc][j]) ),  P_j = sum_{k in block j} x[b][k] * W[oc][k]
+ * P_j is exact (int64 via the limb contraction, one block per exact chunk) and
+ * each term is exact in double; the result is deterministic.
+ * x: int16 [B][IC]; ex: int8 [B][nb]; W: int16 [OC][IC]; ew: int8 [OC][nb];
+ * nb = ceil(IC / block); block: a multiple of 64 in [64, 512]; y: float [B][OC].
+ * Workspace: ito_dfp16_workspace_size(B, IC, OC) bytes, 256-byte aligned.
+ * Errors: ITO_ERR_ARG (NULL pointer, workspace, block), ITO_ERR_SHAPE. */
+int ito_bdfp16_linear_fwd_f32(const int16_t *x, const int8_t *ex, const int16_t *W, const int8_t *ew, int B, int IC,
+                              int OC, int32_t block, void *workspace, size_t workspace_bytes, float *y, void *stream);
+
 typedef struct ito_dfp16_model ito_dfp16_model;
 
 /* A stack of DFP16 Linear layers dims[0] -> dims[1] -> ... -> dims[n_layers]

@@ -106,6 +106,9 @@ _SIGS = {
     "ito_model_kernels_per_step": (_I, [_P]),
     "ito_dfp16_update_bits": (_I, [_P, _P, _P, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "ito_dfp_set_bits": (_I, [_P, _I64, _I32, _I32, _P]),
+    "ito_bdfp16_from_float": (_I, [_P, _I64, _I64, _I32, _P, _P, _P]),
+    "ito_bdfp16_to_float": (_I, [_P, _P, _I64, _I64, _I32, _P, _P]),
+    "ito_bdfp16_linear_fwd_f32": (_I, [_P, _P, _P, _P, _I, _I, _I, _I32, _P, _SZ, _P, _P]),
     "ito_dfp16_model_get_precision": (_I, [_P, _I, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "ito_dfp16_model_set_precision": (_I, [_P, _I, _I32, _P]),
     "ito_dfp16_model_apt_enable": (_I, [_P, ctypes.POINTER(AptParams), _P]),
@@ -544,6 +547,37 @@ def ito_dfp_set_bits(W, bits_old, bits_new, stream=None):
     """Precision change of an int16 mantissa tensor, in place (the exponent changes by bits_old - bits_new)."""
     _check(_lib.ito_dfp_set_bits(_ptr(W), W.numel(), bits_old, bits_new, _stream(stream)))
     return W
+
+
+def ito_bdfp16_from_float(f, block, stream=None):
+    """float32 [rows][cols] -> (int16 mantissas, int8 exponents [rows][ceil(cols / block)])"""
+    torch = _torch()
+    rows, cols = f.shape
+    nb = (cols + block - 1) // block
+    m = torch.empty((rows, cols), dtype=torch.int16, device=f.device)
+    e = torch.empty((rows, nb), dtype=torch.int8, device=f.device)
+    _check(_lib.ito_bdfp16_from_float(_ptr(f), rows, cols, block, _ptr(m), _ptr(e), _stream(stream)))
+    return m, e
+
+
+def ito_bdfp16_to_float(m, e, block, stream=None):
+    torch = _torch()
+    rows, cols = m.shape
+    f = torch.empty((rows, cols), dtype=torch.float32, device=m.device)
+    _check(_lib.ito_bdfp16_to_float(_ptr(m), _ptr(e), rows, cols, block, _ptr(f), _stream(stream)))
+    return f
+
+
+def ito_bdfp16_linear_fwd_f32(x, ex, W, ew, block, stream=None):
+    """Blocked-DFP x [B][IC], W [OC][IC] (int8 exponents per block of IC) -> float32 [B][OC]"""
+    torch = _torch()
+    B, IC = x.shape
+    OC = W.shape[0]
+    y = torch.empty((B, OC), dtype=torch.float32, device=x.device)
+    ws, n = _dfp_ws(B, IC, OC)
+    _check(_lib.ito_bdfp16_linear_fwd_f32(_ptr(x), _ptr(ex), _ptr(W), _ptr(ew), B, IC, OC, block, _aligned256(ws), n,
+                                          _ptr(y), _stream(stream)))
+    return y
 
 
 def ito_dfp16_from_float(f, stream=None):

@@ -44,12 +44,29 @@ __device__ __forceinline__ void limb_split(int32_t v, int32_t& h, int32_t& l)
     h = (v - l) >> 8;   // v - l is a multiple of 256
 }
 
-template <bool A_MN, bool B_MN>
+// 2^k as a double (k in [-1022, 1023]): scaling by it is exact, so converting the
+// product to float or int rounds once, like ldexpf
+__device__ __forceinline__ double pow2d(int k) { return __longlong_as_double((long long)(k + 1023) << 52); }
+
+// Blocked-DFP operands (BLOCKED): the exact chunk is one exponent block of the
+// contraction; after each chunk the epilogue scales its exact int64 partial by
+// 2^(ex[row][chunk] + ew[col][chunk]) and adds it in double, and the tile is
+// written as float (Y) instead of int64 (C).
+struct DfpBlocked {
+    const int8_t* ex;   // [M][nb]
+    const int8_t* ew;   // [N][nb]
+    int nb;
+    float* Y;           // [M][ldy]
+    int64_t ldy;
+};
+
+template <bool A_MN, bool B_MN, bool BLOCKED>
 __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
     k_gemm_dfp(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
-               const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K,
-               int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, int* __restrict__ err)
+               const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
+               int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, DfpBlocked bk,
+               int* __restrict__ err)
 {
     using Cfg = DfpCfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -73,7 +90,7 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
     const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
     const int num_tiles = num_m * num_n;
     const int num_kb = (K + BK - 1) / BK;
-    const int num_chunks = (num_kb + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
+    const int num_chunks = (num_kb + chunk_kb - 1) / chunk_kb;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -145,8 +162,8 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
                     tc_fence_after();
                     const uint32_t d_hh = tmem_base + (uint32_t)(buf * Cfg::BUF_COLS);
                     const uint32_t d_mid = d_hh + 64, d_ll = d_hh + 128;
-                    const int kb0 = c * Cfg::CHUNK_KB;
-                    const int kb1 = min(num_kb, kb0 + Cfg::CHUNK_KB);
+                    const int kb0 = c * chunk_kb;
+                    const int kb1 = min(num_kb, kb0 + chunk_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&full_bar[stage], phase, abort_flag, err)) { ok = false; break; }
                         tc_fence_after();
@@ -196,26 +213,56 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
         bool ok = true;
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             const int tm = t / num_n, tn = t % num_n;
+            // BLOCKED: the double sums live in the same registers as the int64 ones
             int64_t acc[HALF];
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) acc[i] = 0;
+            for (int i = 0; i < HALF; ++i) acc[i] = BLOCKED ? __double_as_longlong(0.0) : 0;
+            const int brow = tm * BM + quad * 32 + lane;                  // this thread's row (BLOCKED)
             for (int c = 0; c < num_chunks; ++c) {
                 if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) +
                                        (uint32_t)(buf * Cfg::BUF_COLS + half * HALF);
-                // one accumulator at a time keeps 16 staging registers live
+                if (!BLOCKED) {
+                    // one accumulator at a time keeps 16 staging registers live
 #pragma unroll
-                for (int j = 0; j < HALF / 16; ++j) {
+                    for (int j = 0; j < HALF / 16; ++j) {
 #pragma unroll 1
-                    for (int part = 0; part < 3; ++part) {
-                        uint32_t r[16];
-                        tmem_ld16(taddr + part * 64 + j * 16, r);
-                        tmem_ld_wait();
-                        const int sh = part == 0 ? 16 : (part == 1 ? 8 : 0);
+                        for (int part = 0; part < 3; ++part) {
+                            uint32_t r[16];
+                            tmem_ld16(taddr + part * 64 + j * 16, r);
+                            tmem_ld_wait();
+                            const int sh = part == 0 ? 16 : (part == 1 ? 8 : 0);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) << sh;
+                            for (int i = 0; i < 16; ++i)
+                                acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) << sh;
+                        }
+                    }
+                } else {
+                    const int exr = brow < M ? bk.ex[(int64_t)brow * bk.nb + c] : 0;
+#pragma unroll
+                    for (int j = 0; j < HALF / 16; ++j) {
+                        int64_t pj[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pj[i] = 0;
+#pragma unroll 1
+                        for (int part = 0; part < 3; ++part) {
+                            uint32_t r[16];
+                            tmem_ld16(taddr + part * 64 + j * 16, r);
+                            tmem_ld_wait();
+                            const int sh = part == 0 ? 16 : (part == 1 ? 8 : 0);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pj[i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) << sh;
+                        }
+                        // the chunk's exact partial (below 2^53) times a power of two: exact
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int col = tn * BN + half * HALF + j * 16 + i;
+                            const int e = exr + (col < N ? bk.ew[(int64_t)col * bk.nb + c] : 0);
+                            acc[j * 16 + i] = __double_as_longlong(__longlong_as_double(acc[j * 16 + i]) +
+                                                                   (double)pj[i] * pow2d(e));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -224,6 +271,16 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
                 if (++buf == 2) { buf = 0; buf_phase ^= 1; }
             }
             if (!ok) break;
+            if (BLOCKED) {
+                const int col0 = tn * BN + half * HALF;
+                if (brow < M) {
+                    float* dst = bk.Y + (int64_t)brow * bk.ldy + col0;
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i)
+                        if (col0 + i < N) dst[i] = __double2float_rn(__longlong_as_double(acc[i]));
+                }
+                continue;
+            }
             unsigned long long mx = 0;
 #pragma unroll
             for (int i = 0; i < HALF; ++i) {
@@ -279,10 +336,10 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
     }
 }
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, bool BLOCKED = false>
 static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
 {
-    auto kern = k_gemm_dfp<A_MN, B_MN>;
+    auto kern = k_gemm_dfp<A_MN, B_MN, BLOCKED>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DfpCfg::SMEM_BYTES) !=
@@ -292,9 +349,10 @@ static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
     }
     const int tiles = ((p.M + DfpCfg::BM - 1) / DfpCfg::BM) * ((p.N + DfpCfg::BN - 1) / DfpCfg::BN);
     const int grid = tiles < num_sms() ? tiles : num_sms();
+    const DfpBlocked bk{p.ex, p.ew, p.nb, p.Y, p.ldy};
     kern<<<grid, DfpCfg::THREADS, DfpCfg::SMEM_BYTES, s>>>(p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.mapC,
-                                                           p.use_tma_store, p.M, p.N, p.K, p.C, p.ldc, p.d_max,
-                                                           p.err);
+                                                           p.use_tma_store, p.M, p.N, p.K, p.chunk_kb, p.C, p.ldc,
+                                                           p.d_max, bk, p.err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp gemm launch: %s", cudaGetErrorString(e));
 }
@@ -310,6 +368,7 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
     if (b_mn ? (Bh.rows != K || Bh.cols != N) : (Bh.rows != N || Bh.cols != K))
         return set_error(ITO_ERR_SHAPE, "dfp gemm: B view does not match N x K");
     *p = DfpGemmPlan{};
+    p->chunk_kb = DfpCfg::CHUNK_KB;
     p->M = M;
     p->N = N;
     p->K = K;
@@ -325,7 +384,7 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
         (r = make_map_bf16(&p->mapBh, Bh, 64)) || (r = make_map_bf16(&p->mapBl, Bl, 64)))
         return r;
     p->use_tma_store = 0;
-    if ((reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 1) == 0) {
+    if (C && (reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 1) == 0) {
         auto enc = get_encode();
         cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
         cuuint64_t strides[1] = {(cuuint64_t)ldc * 8};
@@ -340,8 +399,29 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
     return ITO_OK;
 }
 
+int dfp_gemm_plan_blocked(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, const Bf16View& Bh,
+                          const Bf16View& Bl, int M, int N, int K, int block, const int8_t* ex, const int8_t* ew,
+                          float* Y, int64_t ldy)
+{
+    if (block < 64 || block > 512 || block % 64)
+        return set_error(ITO_ERR_ARG, "blocked DFP: block must be a multiple of 64 in [64, 512]");
+    if (!ex || !ew || !Y) return set_error(ITO_ERR_ARG, "blocked DFP: NULL exponent or output pointer");
+    // the int64 result and its max are not produced; C = nullptr keeps the int64 store map unused
+    int r = dfp_gemm_plan(p, Ah, Al, false, Bh, Bl, false, M, N, K, nullptr, 0, nullptr);
+    if (r) return r;
+    p->chunk_kb = block / 64;
+    p->blocked = 1;
+    p->ex = ex;
+    p->ew = ew;
+    p->nb = (K + block - 1) / block;
+    p->Y = Y;
+    p->ldy = ldy;
+    return ITO_OK;
+}
+
 int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s)
 {
+    if (p.blocked) return launch_dfp<false, false, true>(p, s);
     if (!p.a_mn && !p.b_mn) return launch_dfp<false, false>(p, s);
     if (!p.a_mn && p.b_mn) return launch_dfp<false, true>(p, s);
     if (p.a_mn && p.b_mn) return launch_dfp<true, true>(p, s);
@@ -487,10 +567,6 @@ int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned
 
 // --------------------------------------------------- float <-> DFP16
 
-// 2^k as a double (k in [-1022, 1023]): scaling by it is exact, so converting the
-// product to float or int rounds once, like ldexpf
-__device__ __forceinline__ double pow2d(int k) { return __longlong_as_double((long long)(k + 1023) << 52); }
-
 // max |f| as float bits (non-negative floats order like their bit patterns)
 __global__ void k_absmax_f32(const float* __restrict__ f, int64_t n, unsigned int* __restrict__ d_bits)
 {
@@ -557,6 +633,74 @@ int launch_dfp_from_float(const float* f, int64_t n, unsigned int* d_bits, int16
     k_dfp_from_float<<<launch_grid_blocks(n, 256), 256, 0, s>>>(f, n, d_bits, out, d_exp, err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "float->dfp launch: %s", cudaGetErrorString(e));
+}
+
+// Blocked-DFP ("Mixed Precision Training...", section 3: several fine-grained
+// exponents per tensor): every run of `block` consecutive elements of a row
+// (the last one shorter when block does not divide cols) is converted like a
+// DFP-16 tensor of its own. One warp per block: max |f| by a warp reduction,
+// then E = e - 15 and round-to-nearest-even mantissas, saturated.
+__global__ void k_bdfp_from_float(const float* __restrict__ f, int64_t rows, int64_t cols, int block,
+                                  int16_t* __restrict__ out, int8_t* __restrict__ exps, int* __restrict__ err)
+{
+    const int64_t nb = (cols + block - 1) / block;
+    const int64_t nblocks = rows * nb;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < nblocks; w += nwarps) {
+        const int64_t r = w / nb, j = w - r * nb;
+        const int64_t c0 = j * block;
+        const int len = (int)(cols - c0 < block ? cols - c0 : block);
+        const float* src = f + r * cols + c0;
+        uint32_t mx = 0;
+        for (int i = lane; i < len; i += 32) mx = max(mx, __float_as_uint(src[i]) & 0x7fffffffu);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        const int E = mx ? frexp_exponent(mx) - 15 : 0;
+        if (lane == 0) {
+            exps[w] = (int8_t)(E < -128 ? -128 : (E > 127 ? 127 : E));
+            if (mx >= 0x7f800000u) raise_device_error(err, ITO_ERR_ARG);    // inf or nan in the input
+            if (E < -128 || E > 127) raise_device_error(err, ITO_ERR_EXPONENT);
+        }
+        const double sc = pow2d(-E);
+        int16_t* dst = out + r * cols + c0;
+        for (int i = lane; i < len; i += 32) {
+            int q = __double2int_rn((double)src[i] * sc);
+            q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
+            dst[i] = (int16_t)q;
+        }
+    }
+}
+
+__global__ void k_bdfp_to_float(const int16_t* __restrict__ m, const int8_t* __restrict__ exps, int64_t rows,
+                                int64_t cols, int block, float* __restrict__ out)
+{
+    const int64_t nb = (cols + block - 1) / block;
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i - r * cols;
+        out[i] = __double2float_rn((double)m[i] * pow2d(exps[r * nb + c / block]));
+    }
+}
+
+int launch_bdfp_from_float(const float* f, int64_t rows, int64_t cols, int block, int16_t* out, int8_t* exps,
+                           cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    int* err = device_error_word();
+    if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
+    const int64_t nblocks = rows * ((cols + block - 1) / block);
+    k_bdfp_from_float<<<launch_grid_blocks(nblocks * 32, 256), 256, 0, s>>>(f, rows, cols, block, out, exps, err);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "float->bdfp launch: %s", cudaGetErrorString(e));
+}
+
+int launch_bdfp_to_float(const int16_t* m, const int8_t* exps, int64_t rows, int64_t cols, int block, float* out,
+                         cudaStream_t s)
+{
+    if (rows < 1 || cols < 1) return ITO_OK;
+    k_bdfp_to_float<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(m, exps, rows, cols, block, out);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "bdfp->float launch: %s", cudaGetErrorString(e));
 }
 
 int launch_dfp_to_float(const int16_t* m, int64_t n, const int32_t* d_exp, float* out, cudaStream_t s)

@@ -253,6 +253,40 @@ int ito_dfp16_linear_fwd_f32(const int16_t* x, const int32_t* d_exp_x, const int
     return launch_p64_to_float(p64, (int64_t)B * OC, d_exp_x, d_exp_w, y, s);
 }
 
+int ito_bdfp16_from_float(const float* f, int64_t rows, int64_t cols, int32_t block, int16_t* mant, int8_t* exps,
+                          void* stream)
+{
+    if (!f || !mant || !exps) return set_error(ITO_ERR_ARG, "NULL pointer");
+    if (rows < 1 || cols < 1 || block < 1) return set_error(ITO_ERR_SHAPE, "rows, cols and block must be >= 1");
+    return launch_bdfp_from_float(f, rows, cols, block, mant, exps, static_cast<cudaStream_t>(stream));
+}
+
+int ito_bdfp16_to_float(const int16_t* mant, const int8_t* exps, int64_t rows, int64_t cols, int32_t block, float* f,
+                        void* stream)
+{
+    if (!f || !mant || !exps) return set_error(ITO_ERR_ARG, "NULL pointer");
+    if (rows < 1 || cols < 1 || block < 1) return set_error(ITO_ERR_SHAPE, "rows, cols and block must be >= 1");
+    return launch_bdfp_to_float(mant, exps, rows, cols, block, f, static_cast<cudaStream_t>(stream));
+}
+
+int ito_bdfp16_linear_fwd_f32(const int16_t* x, const int8_t* ex, const int16_t* W, const int8_t* ew, int B, int IC,
+                              int OC, int32_t block, void* workspace, size_t workspace_bytes, float* y, void* stream)
+{
+    ITO_TRY(dfp_check(x, W, ex, y, B, IC, OC, workspace, workspace_bytes));
+    if (!ew) return set_error(ITO_ERR_ARG, "NULL pointer");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t ld = pad8(IC);
+    Planes xa = planes_at(workspace, (size_t)B * ld);
+    Planes wb = planes_at(static_cast<char*>(workspace) + dws_a(B, IC, OC), (size_t)OC * ld);
+    ITO_TRY(launch_i16_to_limbs(x, B, IC, xa.h, xa.l, ld, s));
+    ITO_TRY(launch_i16_to_limbs(W, OC, IC, wb.h, wb.l, ld, s));
+    DfpGemmPlan g;
+    ITO_TRY(dfp_gemm_plan_blocked(&g, Bf16View{xa.h, B, IC, ld}, Bf16View{xa.l, B, IC, ld},
+                                  Bf16View{wb.h, OC, IC, ld}, Bf16View{wb.l, OC, IC, ld}, B, OC, IC, block, ex, ew,
+                                  y, OC));
+    return dfp_gemm_run(g, s);
+}
+
 int ito_dfp16_update(int16_t* W, const int16_t* g, const int32_t* d_exp_g, int64_t n, int32_t exp_w, int32_t eta,
                      int32_t* d_k, uint32_t* d_nonzero, void* stream)
 {

@@ -68,16 +68,29 @@ struct DfpGemmPlan {
     CUtensorMap mapAh, mapAl, mapBh, mapBl, mapC;
     int use_tma_store;
     int M, N, K;
+    int chunk_kb;                 // K blocks of 64 per exact chunk
     bool a_mn, b_mn;
     int64_t* C;
     int64_t ldc;
     unsigned long long* d_max;
     int* err;
+    // Blocked-DFP forward (blocked != 0): one exponent per chunk-long block of K
+    int blocked;
+    const int8_t* ex;             // [M][nb]
+    const int8_t* ew;             // [N][nb]
+    int nb;
+    float* Y;                     // [M][ldy] float output
+    int64_t ldy;
 };
 
 int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a_mn, const Bf16View& Bh,
                   const Bf16View& Bl, bool b_mn, int M, int N, int K, int64_t* C, int64_t ldc,
                   unsigned long long* d_max);
+// Blocked-DFP forward: Y[m][n] = float(sum over K blocks j, in order, in double, of
+// P_j * 2^(ex[m][j] + ew[n][j])), P_j the exact int64 sum over block j (block: 64..512, multiple of 64)
+int dfp_gemm_plan_blocked(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, const Bf16View& Bh,
+                          const Bf16View& Bl, int M, int N, int K, int block, const int8_t* ex, const int8_t* ew,
+                          float* Y, int64_t ldy);
 int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s);
 
 // int16 [rows][cols] -> bf16 limb planes hi/lo [rows][ldl]
@@ -95,6 +108,11 @@ int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned
 int launch_dfp_from_float(const float* f, int64_t n, unsigned int* d_bits, int16_t* out, int32_t* d_exp,
                           cudaStream_t s);
 int launch_dfp_to_float(const int16_t* m, int64_t n, const int32_t* d_exp, float* out, cudaStream_t s);
+// Blocked-DFP conversions: blocks of `block` consecutive elements per row, int8 exponents [rows][nb]
+int launch_bdfp_from_float(const float* f, int64_t rows, int64_t cols, int block, int16_t* out, int8_t* exps,
+                           cudaStream_t s);
+int launch_bdfp_to_float(const int16_t* m, const int8_t* exps, int64_t rows, int64_t cols, int block, float* out,
+                         cudaStream_t s);
 int launch_p64_to_float(const int64_t* P, int64_t n, const int32_t* d_ea, const int32_t* d_eb, float* out,
                         cudaStream_t s);
 // W <- sat_bits(W - dW), dW = rhu(G, k) (k >= 0) or G * 2^-k (k < 0), k = exp_w + eta - *d_exp_g;

@@ -94,6 +94,9 @@ def lib():
             "ora_dfp_down": (i32, [P, i64, i32, P, P]),
             "ora_dfp_update": (i64, [P, P, i64, i32, i32]),
             "ora_dfp_set_bits": (i32, [P, i64, i32, i32]),
+            "ora_bdfp_from_float": (None, [P, i64, i64, i32, P, P]),
+            "ora_bdfp_to_float": (None, [P, P, i64, i64, i32, P]),
+            "ora_bdfp_linear_fwd_f32": (None, [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]),
             "ora_abs_sum16": (i64, [P, i64]),
             "ora_dfp_from_float": (i32, [P, i64, P]),
             "ora_dfp_to_float": (None, [P, i64, i32, P]),
@@ -437,6 +440,39 @@ def p64_to_float(P, e: int):
     out = np.empty(P.shape, np.float32)
     lib().ora_p64_to_float(_p(P), P.size, e, _p(out))
     return out
+
+
+def bdfp_from_float(f, block: int):
+    """float32 [rows][cols] -> (int16 mantissas, int32 exponents [rows][ceil(cols / block)])
+    (Blocked-DFP: ora_bdfp_from_float)."""
+    f = _c(f, np.float32)
+    rows, cols = f.shape
+    nb = (cols + block - 1) // block
+    out = np.empty(f.shape, np.int16)
+    ex = np.empty((rows, nb), np.int32)
+    lib().ora_bdfp_from_float(_p(f), rows, cols, block, _p(out), _p(ex))
+    if ex.size and (ex.min() < -128 or ex.max() > 127):
+        raise OverflowError("a block exponent leaves int8")
+    return out, ex
+
+
+def bdfp_to_float(m, ex, block: int):
+    m, ex = _c(m, np.int16), _c(ex, np.int32)
+    out = np.empty(m.shape, np.float32)
+    lib().ora_bdfp_to_float(_p(m), _p(ex), m.shape[0], m.shape[1], block, _p(out))
+    return out
+
+
+def bdfp_linear_fwd_f32(x, ex, W, ew, block: int):
+    x, W = _c(x, np.int16), _c(W, np.int16)
+    ex, ew = _c(ex, np.int32), _c(ew, np.int32)
+    B, IC = x.shape
+    OC = W.shape[0]
+    nb = (IC + block - 1) // block
+    assert W.shape == (OC, IC) and ex.shape == (B, nb) and ew.shape == (OC, nb)
+    y = np.empty((B, OC), np.float32)
+    lib().ora_bdfp_linear_fwd_f32(_p(x), _p(ex), _p(W), _p(ew), B, IC, OC, block, _p(y))
+    return y
 
 
 def dfp_update(W, Gm, k: int, bits: int = 16):

@@ -661,6 +661,58 @@ void ora_dfp_to_float(const int16_t *m, int64_t n, int32_t E, float *out)
     for (int64_t i = 0; i < n; i++) out[i] = ldexpf((float)m[i], E);
 }
 
+/* [DFP] section 3: Blocked-DFP gains range through several fine-grained
+ * exponents per tensor. The page gives no block shape; reading: each row of a
+ * [rows][cols] tensor is cut into blocks of `block` consecutive elements (the
+ * last one shorter when block does not divide cols), and every block is a
+ * DFP-16 tensor of its own (ora_dfp_from_float on the block).
+ * exps: [rows][ceil(cols / block)]. */
+void ora_bdfp_from_float(const float *f, int64_t rows, int64_t cols, int32_t block, int16_t *out, int32_t *exps)
+{
+    const int64_t nb = (cols + block - 1) / block;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t j = 0; j < nb; j++) {
+            const int64_t c0 = j * block;
+            const int64_t len = cols - c0 < block ? cols - c0 : block;
+            exps[r * nb + j] = ora_dfp_from_float(f + r * cols + c0, len, out + r * cols + c0);
+        }
+}
+
+void ora_bdfp_to_float(const int16_t *m, const int32_t *exps, int64_t rows, int64_t cols, int32_t block, float *out)
+{
+    const int64_t nb = (cols + block - 1) / block;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t j = 0; j < nb; j++) {
+            const int64_t c0 = j * block;
+            const int64_t len = cols - c0 < block ? cols - c0 : block;
+            ora_dfp_to_float(m + r * cols + c0, len, exps[r * nb + j], out + r * cols + c0);
+        }
+}
+
+/* Linear forward with FP32 output over Blocked-DFP operands whose blocks run
+ * along the contraction (x [B][IC] and W [OC][IC], both blocked along IC with
+ * the same block length): each block's products sum exactly in int64 (P_j,
+ * exponent Ex_j + Ew_j by [DFP] 3.1); the blocks are added in double, in
+ * block order, P_j * 2^(Ex_j + Ew_j) (each term exact), and the sum is rounded
+ * once to float ([DFP] section 4: the kernels produce FP32 outputs). */
+void ora_bdfp_linear_fwd_f32(const int16_t *x, const int32_t *ex, const int16_t *W, const int32_t *ew, int B, int IC,
+                             int OC, int block, float *y)
+{
+    const int nb = (IC + block - 1) / block;
+#pragma omp parallel for schedule(static)
+    for (int b = 0; b < B; b++)
+        for (int oc = 0; oc < OC; oc++) {
+            double acc = 0.0;
+            for (int j = 0; j < nb; j++) {
+                const int k1 = (j + 1) * block < IC ? (j + 1) * block : IC;
+                int64_t p = 0;
+                for (int k = j * block; k < k1; k++) p += (int64_t)x[(int64_t)b * IC + k] * W[(int64_t)oc * IC + k];
+                acc += ldexp((double)p, ex[b * nb + j] + ew[oc * nb + j]);
+            }
+            y[(int64_t)b * OC + oc] = (float)acc;
+        }
+}
+
 /* FP32 output of a DFP contraction ([DFP] section 4: the kernels produce FP32
  * outputs): the exact int64 sum P rounded to float (to nearest, ties to even),
  * then scaled by 2^(Ea + Eb). */
