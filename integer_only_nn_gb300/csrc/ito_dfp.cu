@@ -18,6 +18,8 @@
 // per term) and holds an exact integer. After each chunk the epilogue combines
 // the three into an exact int64 partial sum in registers; the tile's int64
 // result and its max |P| (atomicMax) go to global memory.
+#include <cstdlib>
+
 #include "ito_device.cuh"
 #include "ito_internal.h"
 
@@ -336,6 +338,283 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
     }
 }
 
+// ------------------------------------------------- CTA-pair limb kernel
+//
+// The same exact contraction on a CTA pair (tcgen05 cta_group::2): the pair
+// computes a 256 x 64 tile. Each CTA loads both limb planes of its 128 rows of
+// A and ONE limb plane of B -- the leader the high plane, the other CTA the low
+// plane -- so the pair's B operand [B_hi | B_lo] (N = 128) is split between the
+// two CTAs exactly as an M = 256 MMA reads it. Per CTA that is 40 KB per K
+// block instead of 48 KB for the same products. Two MMAs per k-step:
+// A_hi x [B_hi | B_lo] into [hh | mid1] and A_lo x [B_hi | B_lo] into
+// [mid2 | ll], four 64-column fp32 accumulators per buffer (two buffers fill
+// the 512 tensor-memory columns). Each accumulator gets one limb product per
+// K term (at most 2^14), so an exact chunk is 1024 terms. After a chunk the
+// epilogue forms 65536 hh + 256 (mid1 + mid2) + ll in int64.
+
+struct Dfp2Cfg {
+    static constexpr int BM = 128, BN = 64, BK = 64;       // BM rows per CTA (256 per pair)
+    static constexpr int A_PLANE = BM * BK * 2;             // 16 KB
+    static constexpr int B_PLANE = BN * BK * 2;             // 8 KB: one limb plane of the tile's B
+    static constexpr int STAGE_BYTES = 2 * A_PLANE + B_PLANE;
+    static constexpr int STAGES = 5;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + EPI_WARPS * 32;
+    static constexpr int BUF_COLS = 256;                    // hh, mid1, mid2, ll at +0, +64, +128, +192
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int CHUNK_KB = 1024 / BK;              // exact chunk: 1024 K terms
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
+    k_gemm_dfp2(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+                const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, int M, int N,
+                int K, int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max,
+                int* __restrict__ err)
+{
+    using Cfg = Dfp2Cfg;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int HALF = BN / 2;                         // 32 columns per epilogue warp
+    constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, 2 * BN, A_MN, B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t* empty_bar = full_bar + STAGES;
+    uint64_t* accf_bar = empty_bar + STAGES;
+    uint64_t* acce_bar = accf_bar + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int num_m = (M + 2 * BM - 1) / (2 * BM), num_n = (N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (K + BK - 1) / BK;
+    const int num_chunks = (num_kb + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf_bar[b], 1);
+            mbar_init(&acce_bar[b], 2 * Cfg::EPI_WARPS);   // epilogue warps of both CTAs
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // tiles in row-major order over (m, n): consecutive clusters share the A band
+    if (warp == 0) {
+        if (lane == 0) {
+            const CUtensorMap* tmB = leader ? &tmBh : &tmBl;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+                const int tm = t / num_n, tn = t % num_n;
+                const int rowA = tm * 2 * BM + (int)rank * BM;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
+                    const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                    uint8_t* sAh = smem + stage * Cfg::STAGE_BYTES;
+                    uint8_t* sAl = sAh + Cfg::A_PLANE;
+                    uint8_t* sB = sAl + Cfg::A_PLANE;
+                    if (!A_MN) {
+                        tma_load_2d_pair(&tmAh, fb, sAh, kb * BK, rowA);
+                        tma_load_2d_pair(&tmAl, fb, sAl, kb * BK, rowA);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j) {
+                            tma_load_2d_pair(&tmAh, fb, sAh + j * 8192, rowA + j * 64, kb * BK);
+                            tma_load_2d_pair(&tmAl, fb, sAl + j * 8192, rowA + j * 64, kb * BK);
+                        }
+                    }
+                    if (!B_MN)
+                        tma_load_2d_pair(tmB, fb, sB, kb * BK, tn * BN);
+                    else
+                        tma_load_2d_pair(tmB, fb, sB, tn * BN, kb * BK);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+                for (int c = 0; ok && c < num_chunks; ++c) {
+                    if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_hi = tmem_base + (uint32_t)(buf * Cfg::BUF_COLS);   // [hh | mid1]
+                    const uint32_t d_lo = d_hi + 2 * BN;                                  // [mid2 | ll]
+                    const int kb0 = c * Cfg::CHUNK_KB;
+                    const int kb1 = min(num_kb, kb0 + Cfg::CHUNK_KB);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full_bar[stage], phase, abort_flag, err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t ah0 = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                        const uint32_t al0 = ah0 + Cfg::A_PLANE;
+                        const uint32_t b0 = al0 + Cfg::A_PLANE;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint32_t ao = A_MN ? k * 2048 : k * 32;
+                            const uint32_t bo = B_MN ? k * 2048 : k * 32;
+                            const uint32_t albo = A_MN ? 8192 : 16, blbo = B_MN ? 8192 : 16;
+                            const uint64_t ah = smem_desc_sw128(ah0 + ao, albo, 1024);
+                            const uint64_t al = smem_desc_sw128(al0 + ao, albo, 1024);
+                            const uint64_t bd = smem_desc_sw128(b0 + bo, blbo, 1024);
+                            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+                            tc_mma_bf16_pair(d_hi, ah, bd, IDESC, acc);
+                            tc_mma_bf16_pair(d_lo, al, bd, IDESC, acc);
+                        }
+                        tc_commit_pair_mc(&empty_bar[stage], 0x3);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_mc(&accf_bar[buf], 0x3);
+                    if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile
+        const int e = warp - 2;
+        const int quad = warp & 3;
+        const int half = e >> 2;
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        bool ok = true;
+        for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+            const int tm = t / num_n, tn = t % num_n;
+            int64_t acc[HALF];
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) acc[i] = 0;
+            for (int c = 0; c < num_chunks; ++c) {
+                if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) +
+                                       (uint32_t)(buf * Cfg::BUF_COLS + half * HALF);
+#pragma unroll
+                for (int j = 0; j < HALF / 16; ++j) {
+#pragma unroll 1
+                    for (int part = 0; part < 4; ++part) {
+                        uint32_t r[16];
+                        tmem_ld16(taddr + part * BN + j * 16, r);
+                        tmem_ld_wait();
+                        const int sh = part == 0 ? 16 : (part == 3 ? 0 : 8);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) << sh;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[buf]), 0));
+                if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+            }
+            if (!ok) break;
+            unsigned long long mx = 0;
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) {
+                const unsigned long long a = (unsigned long long)(acc[i] < 0 ? -acc[i] : acc[i]);
+                mx = a > mx ? a : mx;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long v = __shfl_xor_sync(0xffffffffu, mx, o);
+                mx = v > mx ? v : mx;
+            }
+            if (lane == 0 && mx != 0) atomicMax(d_max, mx);
+            // the int64 result from registers: 32 consecutive values per row
+            const int row = tm * 2 * BM + (int)rank * BM + quad * 32 + lane;
+            const int col0 = tn * BN + half * HALF;
+            if (row < M) {
+                int64_t* dst = C + (int64_t)row * ldc + col0;
+                if (col0 + HALF <= N && (ldc & 1) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
+#pragma unroll
+                    for (int i = 0; i < HALF; i += 2)
+                        *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(acc[i], acc[i + 1]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i)
+                        if (col0 + i < N) dst[i] = acc[i];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();   // the pair's MMAs and drains are complete in both CTAs
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <bool A_MN, bool B_MN>
+static int launch_dfp2(const DfpGemmPlan& p, cudaStream_t s)
+{
+    using Cfg = Dfp2Cfg;
+    auto kern = k_gemm_dfp2<A_MN, B_MN>;
+    static int max_clusters = 0;
+    if (!max_clusters) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(2 * num_sms());
+        q.blockDim = dim3(Cfg::THREADS);
+        q.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = 2;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1)
+            return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
+        max_clusters = n;
+    }
+    const int tiles = ((p.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((p.N + Cfg::BN - 1) / Cfg::BN);
+    const int clusters = tiles < max_clusters ? tiles : max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.M, p.N, p.K, p.C, p.ldc,
+                                       p.d_max, p.err);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "dfp pair gemm launch: %s", cudaGetErrorString(e));
+    return ITO_OK;
+}
+
 template <bool A_MN, bool B_MN, bool BLOCKED = false>
 static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
 {
@@ -383,6 +662,12 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
     if ((r = make_map_bf16(&p->mapAh, Ah, a_mn ? 64 : 128)) || (r = make_map_bf16(&p->mapAl, Al, a_mn ? 64 : 128)) ||
         (r = make_map_bf16(&p->mapBh, Bh, 64)) || (r = make_map_bf16(&p->mapBl, Bl, 64)))
         return r;
+    // CTA-pair kernel when there are at least 256 rows; ITO_DFP_PAIR=0 forces the single-CTA kernel
+    static const int pair_env = [] {
+        const char* v = getenv("ITO_DFP_PAIR");
+        return v ? atoi(v) : 1;
+    }();
+    p->pair = pair_env != 0 && M >= 256 && C != nullptr;
     p->use_tma_store = 0;
     if (C && (reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 1) == 0) {
         auto enc = get_encode();
@@ -422,6 +707,12 @@ int dfp_gemm_plan_blocked(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al
 int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s)
 {
     if (p.blocked) return launch_dfp<false, false, true>(p, s);
+    if (p.pair) {
+        if (!p.a_mn && !p.b_mn) return launch_dfp2<false, false>(p, s);
+        if (!p.a_mn && p.b_mn) return launch_dfp2<false, true>(p, s);
+        if (p.a_mn && p.b_mn) return launch_dfp2<true, true>(p, s);
+        return launch_dfp2<true, false>(p, s);
+    }
     if (!p.a_mn && !p.b_mn) return launch_dfp<false, false>(p, s);
     if (!p.a_mn && p.b_mn) return launch_dfp<false, true>(p, s);
     if (p.a_mn && p.b_mn) return launch_dfp<true, true>(p, s);

@@ -69,6 +69,7 @@ struct DfpGemmPlan {
     int use_tma_store;
     int M, N, K;
     int chunk_kb;                 // K blocks of 64 per exact chunk
+    int pair;                     // CTA-pair kernel (256 x 64 tiles)
     bool a_mn, b_mn;
     int64_t* C;
     int64_t ldc;

@@ -71,6 +71,35 @@ def test_dfp_wgrad(ito, B, IC, OC):
     _check_down(P, -32, g, eg, rs, mx)
 
 
+# at least 256 rows: the CTA-pair limb kernel (256 x 64 tiles, 1024-term chunks)
+PAIR_SHAPES = [(256, 64, 64), (300, 1000, 130), (513, 2049, 200), (1024, 4096, 64), (2048, 1100, 96)]
+
+
+@pytest.mark.parametrize("B,IC,OC", PAIR_SHAPES)
+def test_dfp_pair_fwd_dgrad_wgrad(ito, B, IC, OC):
+    x, W = i16((B, IC)), i16((OC, IC))
+    e = i16((B, OC))
+    p64, _, _, _, _ = ito.ito_dfp16_linear_fwd(_dev(x), ito._i32dev(-12), _dev(W), ito._i32dev(-17))
+    assert np.array_equal(_h(p64), O.dfp_linear_fwd(x, W))
+    p64, _, _, _, _ = ito.ito_dfp16_linear_bwd_delta(_dev(e), ito._i32dev(-20), _dev(W), ito._i32dev(-17))
+    assert np.array_equal(_h(p64), O.dfp_linear_dgrad(e, W))
+    p64, _, _, _, _ = ito.ito_dfp16_linear_wgrad(_dev(e), ito._i32dev(-20), _dev(x), ito._i32dev(-12))
+    assert np.array_equal(_h(p64), O.dfp_linear_wgrad(e, x))
+    assert ito.ito_get_error() == 0
+
+
+def test_dfp_pair_extreme_chunks(ito):
+    """256+ rows, all products (-32767)^2: each of the pair kernel's four limb
+    accumulators reaches 2^24 exactly at a 1024-term chunk."""
+    for K in (1023, 1024, 1025, 2048, 4096):
+        x = np.full((300, K), -32767, np.int16)
+        W = np.full((70, K), -32767, np.int16)
+        W[1::2] = 32767
+        p64, _, _, _, _ = ito.ito_dfp16_linear_fwd(_dev(x), ito._i32dev(0), _dev(W), ito._i32dev(0))
+        P = _h(p64)
+        assert (P[:, 0::2] == K * 32767 * 32767).all() and (P[:, 1::2] == -K * 32767 * 32767).all()
+
+
 def test_dfp_extreme_chunks(ito):
     """All products (-32767)^2: every limb accumulator reaches its chunk bound."""
     for K in (511, 512, 513, 1024, 2048):
