@@ -135,8 +135,7 @@ __global__ void k_col2im_v8(const int32_t* __restrict__ Dcol, int B, int H, int 
 #pragma unroll
         for (int j = 0; j < 8; ++j) mx = max(mx, abs_u32(acc[j]));
     }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+    block_atomic_max(d_max, mx);
 }
 
 // one thread per input-space element (any IC)
@@ -169,8 +168,7 @@ __global__ void k_col2im_1(const int32_t* __restrict__ Dcol, int B, int H, int W
         D[i] = acc;
         mx = max(mx, abs_u32(acc));
     }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+    block_atomic_max(d_max, mx);
 }
 
 int launch_col2im(const int32_t* Dcol, int B, int H, int W, int IC, int OH, int OW, int stride, int32_t* D,
@@ -203,8 +201,7 @@ __global__ void k_gap_fwd(const int8_t* __restrict__ A, int B, int HW, int C, in
         P[i] = acc;
         mx = max(mx, abs_u32(acc));
     }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+    block_atomic_max(d_max, mx);
 }
 
 int launch_gap_fwd(const int8_t* A, int B, int HW, int C, int32_t* P, uint32_t* d_max, cudaStream_t s)

@@ -333,6 +333,63 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_ma
         : "memory");
 }
 
+// ------------------------------------------------ block-wide reductions
+//
+// Grid-stride kernels fold a per-thread value into one global word. One atomic
+// per warp puts thousands of atomics on a single address at the end of such a
+// kernel; these reduce over the block first (every thread of the block must
+// call them, after its loop) and issue one atomic per block.
+
+template <typename T, typename Op>
+__device__ __forceinline__ T block_reduce(T v, Op op)
+{
+    __shared__ T red[32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();                       // red[] may still be read by an earlier call
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    const int nw = (blockDim.x + 31) >> 5;
+    v = l < nw ? red[l] : T(0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;                              // every thread holds the block's result
+}
+
+struct MaxOp {
+    template <typename T>
+    __device__ __forceinline__ T operator()(T a, T b) const { return a > b ? a : b; }
+};
+struct AddOp {
+    template <typename T>
+    __device__ __forceinline__ T operator()(T a, T b) const { return a + b; }
+};
+
+__device__ __forceinline__ void block_atomic_max(uint32_t* dst, uint32_t v)
+{
+    v = block_reduce(v, MaxOp());
+    if (threadIdx.x == 0 && v) atomicMax(dst, v);
+}
+
+__device__ __forceinline__ void block_atomic_max(unsigned long long* dst, unsigned long long v)
+{
+    v = block_reduce(v, MaxOp());
+    if (threadIdx.x == 0 && v) atomicMax(dst, v);
+}
+
+__device__ __forceinline__ void block_atomic_add(uint32_t* dst, uint32_t v)
+{
+    v = block_reduce(v, AddOp());
+    if (threadIdx.x == 0 && v) atomicAdd(dst, v);
+}
+
+__device__ __forceinline__ void block_atomic_add(unsigned long long* dst, unsigned long long v)
+{
+    v = block_reduce(v, AddOp());
+    if (threadIdx.x == 0 && v) atomicAdd(dst, v);
+}
+
 // Shared-memory matrix descriptor for tcgen05.mma (128-byte swizzle).
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4
 //   bits 32-45 stride byte offset >> 4 bits 46-47 descriptor version (1)

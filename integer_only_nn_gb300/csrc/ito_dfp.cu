@@ -352,6 +352,59 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
 // K term (at most 2^14), so an exact chunk is 1024 terms. After a chunk the
 // epilogue forms 65536 hh + 256 (mid1 + mid2) + ll in int64.
 
+// Work list of the pair kernel: `full` whole tiles, then each remaining tile of
+// the last, partial wave cut into `parts` chunk-aligned K pieces (slot = piece
+// index; -1 for a whole tile).
+struct DfpWork {
+    int tile, c0, c1, slot;
+};
+
+__device__ __forceinline__ DfpWork dfp_work(int w, int full, int parts, int num_chunks)
+{
+    if (w < full) return DfpWork{w, 0, num_chunks, -1};
+    const int u = w - full;
+    const int ti = u / parts, part = u - ti * parts;
+    return DfpWork{full + ti, part * num_chunks / parts, (part + 1) * num_chunks / parts, u};
+}
+
+// C = the sum of the K pieces of each split tile (exact int64), inside the M x N
+// bounds; max |C| folded into *d_max. P: [tail tiles][parts][256][64] int64.
+__global__ void k_tail_reduce64(const int64_t* __restrict__ P, int tail_tiles, int parts, int full_tiles, int num_n,
+                                int M, int N, int64_t ldc, int64_t* __restrict__ C,
+                                unsigned long long* __restrict__ d_max)
+{
+    constexpr int TR = 256, TC = 64;
+    const int64_t n = (int64_t)tail_tiles * TR * (TC / 2);
+    unsigned long long mx = 0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int ti = (int)(i / (TR * (TC / 2)));
+        const int rem = (int)(i - (int64_t)ti * (TR * (TC / 2)));
+        const int r = rem / (TC / 2), c = (rem % (TC / 2)) * 2;
+        int64_t a0 = 0, a1 = 0;
+        for (int q = 0; q < parts; ++q) {
+            const longlong2 v =
+                __ldcs(reinterpret_cast<const longlong2*>(P + (((int64_t)ti * parts + q) * TR + r) * TC + c));
+            a0 += v.x;
+            a1 += v.y;
+        }
+        const int tile = full_tiles + ti;
+        const int gr = (tile / num_n) * TR + r, gc = (tile % num_n) * TC + c;
+        if (gr < M) {
+            if (gc < N) {
+                C[(int64_t)gr * ldc + gc] = a0;
+                const unsigned long long u = (unsigned long long)(a0 < 0 ? -a0 : a0);
+                mx = u > mx ? u : mx;
+            }
+            if (gc + 1 < N) {
+                C[(int64_t)gr * ldc + gc + 1] = a1;
+                const unsigned long long u = (unsigned long long)(a1 < 0 ? -a1 : a1);
+                mx = u > mx ? u : mx;
+            }
+        }
+    }
+    block_atomic_max(d_max, mx);
+}
+
 struct Dfp2Cfg {
     static constexpr int BM = 128, BN = 64, BK = 64;       // BM rows per CTA (256 per pair)
     static constexpr int A_PLANE = BM * BK * 2;             // 16 KB
@@ -370,8 +423,8 @@ template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
     k_gemm_dfp2(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                 const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, int M, int N,
-                int K, int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max,
-                int* __restrict__ err)
+                int K, int full_tiles, int parts, int64_t* __restrict__ C, int64_t ldc,
+                int64_t* __restrict__ tail_ws, unsigned long long* __restrict__ d_max, int* __restrict__ err)
 {
     using Cfg = Dfp2Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -396,6 +449,8 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
     const int num_tiles = num_m * num_n;
     const int num_kb = (K + BK - 1) / BK;
     const int num_chunks = (num_kb + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
+    // the last partial wave's tiles may be cut into `parts` K pieces (see work_item)
+    const int total_work = full_tiles + (num_tiles - full_tiles) * parts;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -425,10 +480,12 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
-                const int tm = t / num_n, tn = t % num_n;
+            for (int w = cluster; ok && w < total_work; w += nclusters) {
+                const DfpWork wi = dfp_work(w, full_tiles, parts, num_chunks);
+                const int tm = wi.tile / num_n, tn = wi.tile % num_n;
                 const int rowA = tm * 2 * BM + (int)rank * BM;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                const int kb_end = min(num_kb, wi.c1 * Cfg::CHUNK_KB);
+                for (int kb = wi.c0 * Cfg::CHUNK_KB; kb < kb_end; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
                     if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
                     const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
@@ -460,8 +517,9 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
-            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
-                for (int c = 0; ok && c < num_chunks; ++c) {
+            for (int w = cluster; ok && w < total_work; w += nclusters) {
+                const DfpWork wi = dfp_work(w, full_tiles, parts, num_chunks);
+                for (int c = wi.c0; ok && c < wi.c1; ++c) {
                     if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_hi = tmem_base + (uint32_t)(buf * Cfg::BUF_COLS);   // [hh | mid1]
@@ -503,12 +561,13 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
-        for (int t = cluster; ok && t < num_tiles; t += nclusters) {
-            const int tm = t / num_n, tn = t % num_n;
+        for (int w = cluster; ok && w < total_work; w += nclusters) {
+            const DfpWork wi = dfp_work(w, full_tiles, parts, num_chunks);
+            const int tm = wi.tile / num_n, tn = wi.tile % num_n;
             int64_t acc[HALF];
 #pragma unroll
             for (int i = 0; i < HALF; ++i) acc[i] = 0;
-            for (int c = 0; c < num_chunks; ++c) {
+            for (int c = wi.c0; c < wi.c1; ++c) {
                 if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) +
@@ -532,6 +591,16 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
                 if (++buf == 2) { buf = 0; buf_phase ^= 1; }
             }
             if (!ok) break;
+            if (wi.slot >= 0) {
+                // a K piece of a split tile: its exact partial goes to workspace slot wi.slot
+                // ([slot][256 rows][64 cols] int64); k_tail_reduce64 finishes the tile
+                int64_t* dst = tail_ws + ((int64_t)wi.slot * 2 * BM + (int)rank * BM + quad * 32 + lane) * BN +
+                               half * HALF;
+#pragma unroll
+                for (int i = 0; i < HALF; i += 2)
+                    *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(acc[i], acc[i + 1]);
+                continue;
+            }
             unsigned long long mx = 0;
 #pragma unroll
             for (int i = 0; i < HALF; ++i) {
@@ -595,8 +664,10 @@ static int launch_dfp2(const DfpGemmPlan& p, cudaStream_t s)
             return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
         max_clusters = n;
     }
-    const int tiles = ((p.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((p.N + Cfg::BN - 1) / Cfg::BN);
-    const int clusters = tiles < max_clusters ? tiles : max_clusters;
+    const int num_n = (p.N + Cfg::BN - 1) / Cfg::BN;
+    const int tiles = ((p.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * num_n;
+    const int work = p.tail_full + (tiles - p.tail_full) * p.tail_parts;
+    const int clusters = work < max_clusters ? work : max_clusters;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(Cfg::THREADS);
@@ -609,10 +680,87 @@ static int launch_dfp2(const DfpGemmPlan& p, cudaStream_t s)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.M, p.N, p.K, p.C, p.ldc,
-                                       p.d_max, p.err);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.M, p.N, p.K, p.tail_full,
+                                       p.tail_parts, p.C, p.ldc, p.tail_ws, p.d_max, p.err);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "dfp pair gemm launch: %s", cudaGetErrorString(e));
+    if (p.tail_parts > 1) {
+        const int tail = tiles - p.tail_full;
+        k_tail_reduce64<<<launch_grid_blocks((int64_t)tail * 256 * 32, 256), 256, 0, s>>>(
+            p.tail_ws, tail, p.tail_parts, p.tail_full, num_n, p.M, p.N, p.ldc, p.C, p.d_max);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "dfp tail reduce launch: %s", cudaGetErrorString(e));
+    }
     return ITO_OK;
+}
+
+// CTA pairs of k_gemm_dfp2 resident at once (all operand layouts share one occupancy).
+static int dfp2_clusters()
+{
+    using Cfg = Dfp2Cfg;
+    static int n = 0;
+    if (!n) {
+        auto kern = k_gemm_dfp2<false, false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+            return 0;
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(2 * num_sms());
+        q.blockDim = dim3(Cfg::THREADS);
+        q.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = 2;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, kern, &q) != cudaSuccess || c < 1) return 0;
+        n = c;
+    }
+    return n;
+}
+
+// Last-wave split of a pair-kernel limb contraction (whole tiles, K pieces per
+// remaining tile); estimated time = waves of whole tiles + rounds of pieces, plus
+// the reduction pass (pieces written and read once at about 5 TB/s, one launch).
+// A 256 x 64 tile takes 4 limb products of 2 * 256 * 64 * K operations at about
+// 13 TFLOP/s per pair (the measured pair-kernel rate).
+static void dfp_tail_split(int M, int N, int K, int* full, int* parts)
+{
+    using Cfg = Dfp2Cfg;
+    const int tiles = ((M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((N + Cfg::BN - 1) / Cfg::BN);
+    *full = tiles;
+    *parts = 1;
+    // ITO_DFP_TAIL=0 in the environment turns the split off
+    static const int tail_env = [] {
+        const char* v = getenv("ITO_DFP_TAIL");
+        return v ? atoi(v) : 1;
+    }();
+    if (!tail_env) return;
+    const int clusters = dfp2_clusters();
+    const int num_chunks = ((K + Cfg::BK - 1) / Cfg::BK + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
+    if (clusters < 1 || tiles % clusters == 0) return;
+    const int waves = tiles / clusters, r = tiles % clusters;
+    const double tile_us = 4.0 * 2 * 256 * 64 * (double)K / 13.0e6;
+    double best = (waves + 1.0) * tile_us;
+    for (int q = 2; q <= 4 && q <= num_chunks; ++q) {
+        const double red_us = 3.0 + 2.0 * r * q * 256.0 * 64 * 8 / 5.0e6;
+        const double t = (waves + (double)((r * q + clusters - 1) / clusters) / q) * tile_us + red_us;
+        if (t < best) {
+            best = t;
+            *full = tiles - r;
+            *parts = q;
+        }
+    }
+}
+
+size_t dfp_split_ws_bytes(int M, int N, int K)
+{
+    if (M < 256) return 0;
+    int full, parts;
+    dfp_tail_split(M, N, K, &full, &parts);
+    const int tiles = ((M + 255) / 256) * ((N + 63) / 64);
+    return parts > 1 ? (size_t)(tiles - full) * parts * 256 * 64 * sizeof(int64_t) : 0;
 }
 
 template <bool A_MN, bool B_MN, bool BLOCKED = false>
@@ -638,7 +786,7 @@ static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
 
 int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a_mn, const Bf16View& Bh,
                   const Bf16View& Bl, bool b_mn, int M, int N, int K, int64_t* C, int64_t ldc,
-                  unsigned long long* d_max)
+                  unsigned long long* d_max, int64_t* tail_ws, size_t tail_ws_bytes)
 {
     if (M < 1 || N < 1 || K < 1) return set_error(ITO_ERR_SHAPE, "dfp gemm: empty contraction");
     if (K > (1 << 20)) return set_error(ITO_ERR_SHAPE, "dfp gemm: contraction longer than 2^20");
@@ -668,6 +816,18 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
         return v ? atoi(v) : 1;
     }();
     p->pair = pair_env != 0 && M >= 256 && C != nullptr;
+    p->tail_full = ((M + 255) / 256) * ((N + 63) / 64);
+    p->tail_parts = 1;
+    if (p->pair && tail_ws) {
+        int full, parts;
+        dfp_tail_split(M, N, K, &full, &parts);
+        const size_t need = parts > 1 ? (size_t)(p->tail_full - full) * parts * 256 * 64 * sizeof(int64_t) : 0;
+        if (parts > 1 && need <= tail_ws_bytes) {
+            p->tail_full = full;
+            p->tail_parts = parts;
+            p->tail_ws = tail_ws;
+        }
+    }
     p->use_tma_store = 0;
     if (C && (reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 1) == 0) {
         auto enc = get_encode();
@@ -692,7 +852,7 @@ int dfp_gemm_plan_blocked(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al
         return set_error(ITO_ERR_ARG, "blocked DFP: block must be a multiple of 64 in [64, 512]");
     if (!ex || !ew || !Y) return set_error(ITO_ERR_ARG, "blocked DFP: NULL exponent or output pointer");
     // the int64 result and its max are not produced; C = nullptr keeps the int64 store map unused
-    int r = dfp_gemm_plan(p, Ah, Al, false, Bh, Bl, false, M, N, K, nullptr, 0, nullptr);
+    int r = dfp_gemm_plan(p, Ah, Al, false, Bh, Bl, false, M, N, K, nullptr, 0, nullptr, nullptr, 0);
     if (r) return r;
     p->chunk_kb = block / 64;
     p->blocked = 1;
@@ -745,12 +905,10 @@ int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t
 
 // ------------------------------------------------------- down-conversion
 
-// adds a warp's partial sums of |mantissa| to *d_abs_sum (exact: integer atomics)
+// adds the block's partial sums of |mantissa| to *d_abs_sum (exact: integer atomics)
 __device__ __forceinline__ void add_abs_sum(unsigned long long* d_abs_sum, unsigned long long v)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0 && v) atomicAdd(d_abs_sum, v);
+    block_atomic_add(d_abs_sum, v);
 }
 
 __global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t cols,
@@ -864,8 +1022,7 @@ __global__ void k_absmax_f32(const float* __restrict__ f, int64_t n, unsigned in
     uint32_t mx = 0;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         mx = max(mx, __float_as_uint(f[i]) & 0x7fffffffu);
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_bits, mx);
+    block_atomic_max(d_bits, mx);
 }
 
 // frexp exponent e of a positive finite float given by its bits: m = frac * 2^e, frac in [0.5, 1)
@@ -1039,10 +1196,7 @@ __global__ void k_dfp_update(int16_t* __restrict__ W, uint16_t* __restrict__ hi,
             lo[r * ldl + c] = int_to_bf16_bits(l);
         }
     }
-    if (d_nonzero) {
-        cnt = __reduce_add_sync(0xffffffffu, cnt);
-        if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(d_nonzero, cnt);
-    }
+    if (d_nonzero) block_atomic_add(d_nonzero, cnt);
 }
 
 // four weights per thread step; cols % 4 == 0 and rows * cols < 2^31
@@ -1083,10 +1237,7 @@ __global__ void k_dfp_update_v4(int16_t* __restrict__ W, uint16_t* __restrict__ 
             *reinterpret_cast<uint2*>(lo + o) = *reinterpret_cast<const uint2*>(l);
         }
     }
-    if (d_nonzero) {
-        cnt = __reduce_add_sync(0xffffffffu, cnt);
-        if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(d_nonzero, cnt);
-    }
+    if (d_nonzero) block_atomic_add(d_nonzero, cnt);
 }
 
 int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const int16_t* G, int64_t rows,

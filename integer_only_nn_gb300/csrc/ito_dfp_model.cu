@@ -24,6 +24,7 @@
 // sums |g| exactly, each evaluated step logs (sum|g|, E_G) per layer on the
 // device, and ito_dfp16_model_apt_epoch_end applies Algorithm 1 to the mean
 // Gavg of the epoch's evaluations (Algorithm 2: adjustment between epochs).
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -82,6 +83,8 @@ struct ito_dfp16_model {
     int apt_step = 0, apt_nlog = 0;     // steps since the last epoch end; logged evaluations
     unsigned long long* log_abs = nullptr;
     int32_t* log_eg = nullptr;
+    int64_t* tail_ws = nullptr;        // partial tiles of split last waves (shared by the step's contractions)
+    size_t tail_ws_bytes = 0;
     int16_t* x16 = nullptr;
     uint16_t *xh = nullptr, *xl = nullptr;
     int64_t ldx = 0;
@@ -120,6 +123,16 @@ static inline size_t al256(size_t n) { return (n + 255) & ~size_t(255); }
 // standalone workspace: limb planes of operand A (x or delta) and operand B (W or x)
 static size_t dws_a(int B, int IC, int OC) { return al256((size_t)2 * 2 * B * pad8(IC > OC ? IC : OC)); }
 static size_t dws_b(int B, int IC, int OC) { return al256((size_t)2 * 2 * (OC > B ? OC : B) * pad8(IC)); }
+// partial tiles of a split last wave, for whichever of the three contractions needs most
+static size_t dws_c(int B, int IC, int OC)
+{
+    const size_t a = dfp_split_ws_bytes(B, OC, IC), b = dfp_split_ws_bytes(B, IC, OC), c = dfp_split_ws_bytes(OC, IC, B);
+    return al256(a > b ? (a > c ? a : c) : (b > c ? b : c));
+}
+static int64_t* dws_tail(void* ws, int B, int IC, int OC)
+{
+    return reinterpret_cast<int64_t*>(static_cast<char*>(ws) + dws_a(B, IC, OC) + dws_b(B, IC, OC));
+}
 
 struct Planes {
     uint16_t *h, *l;
@@ -147,7 +160,7 @@ extern "C" {
 size_t ito_dfp16_workspace_size(int B, int IC, int OC)
 {
     if (B < 1 || IC < 1 || OC < 1) return 0;
-    return dws_a(B, IC, OC) + dws_b(B, IC, OC);
+    return dws_a(B, IC, OC) + dws_b(B, IC, OC) + dws_c(B, IC, OC);
 }
 
 int ito_dfp16_linear_fwd(const int16_t* x, const int32_t* d_exp_x, const int16_t* W, const int32_t* d_exp_w, int B,
@@ -166,7 +179,7 @@ int ito_dfp16_linear_fwd(const int16_t* x, const int32_t* d_exp_x, const int16_t
     DfpGemmPlan g;
     ITO_TRY(dfp_gemm_plan(&g, Bf16View{xa.h, B, IC, ld}, Bf16View{xa.l, B, IC, ld}, false, Bf16View{wb.h, OC, IC, ld},
                           Bf16View{wb.l, OC, IC, ld}, false, B, OC, IC, p64, OC,
-                          reinterpret_cast<unsigned long long*>(d_max)));
+                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC), dws_c(B, IC, OC)));
     ITO_TRY(dfp_gemm_run(g, s));
     return launch_dfp_down(p64, B, OC, reinterpret_cast<unsigned long long*>(d_max), d_exp_x, d_exp_w, y, nullptr,
                            nullptr, 0, d_exp_y, d_rs, s);
@@ -189,7 +202,7 @@ int ito_dfp16_linear_bwd_delta(const int16_t* delta, const int32_t* d_exp_delta,
     DfpGemmPlan g;
     ITO_TRY(dfp_gemm_plan(&g, Bf16View{ea.h, B, OC, lde}, Bf16View{ea.l, B, OC, lde}, false,
                           Bf16View{wb.h, OC, IC, ldw}, Bf16View{wb.l, OC, IC, ldw}, true, B, IC, OC, p64, IC,
-                          reinterpret_cast<unsigned long long*>(d_max)));
+                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC), dws_c(B, IC, OC)));
     ITO_TRY(dfp_gemm_run(g, s));
     return launch_dfp_down(p64, B, IC, reinterpret_cast<unsigned long long*>(d_max), d_exp_delta, d_exp_w, delta_prev,
                            nullptr, nullptr, 0, d_exp_prev, d_rs, s);
@@ -211,7 +224,7 @@ int ito_dfp16_linear_wgrad(const int16_t* delta, const int32_t* d_exp_delta, con
     DfpGemmPlan gp;
     ITO_TRY(dfp_gemm_plan(&gp, Bf16View{ea.h, B, OC, lde}, Bf16View{ea.l, B, OC, lde}, true,
                           Bf16View{xb.h, B, IC, ldx}, Bf16View{xb.l, B, IC, ldx}, true, OC, IC, B, p64, IC,
-                          reinterpret_cast<unsigned long long*>(d_max)));
+                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC), dws_c(B, IC, OC)));
     ITO_TRY(dfp_gemm_run(gp, s));
     return launch_dfp_down(p64, OC, IC, reinterpret_cast<unsigned long long*>(d_max), d_exp_delta, d_exp_x, g, nullptr,
                            nullptr, 0, d_exp_g, d_rs, s);
@@ -248,7 +261,7 @@ int ito_dfp16_linear_fwd_f32(const int16_t* x, const int32_t* d_exp_x, const int
     DfpGemmPlan g;
     ITO_TRY(dfp_gemm_plan(&g, Bf16View{xa.h, B, IC, ld}, Bf16View{xa.l, B, IC, ld}, false, Bf16View{wb.h, OC, IC, ld},
                           Bf16View{wb.l, OC, IC, ld}, false, B, OC, IC, p64, OC,
-                          reinterpret_cast<unsigned long long*>(d_max)));
+                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC), dws_c(B, IC, OC)));
     ITO_TRY(dfp_gemm_run(g, s));
     return launch_p64_to_float(p64, (int64_t)B * OC, d_exp_x, d_exp_w, y, s);
 }
@@ -368,6 +381,14 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
         ITO_TRY(m->alloc(&L.pg64, (size_t)L.OC * L.IC));
         ITO_TRY(m->alloc(&L.g16, (size_t)L.OC * L.IC));
     }
+    // partial tiles of split last waves: one buffer for the largest need (the step runs in order)
+    for (int l = 0; l < nl; ++l) {
+        const DLayer& L = m->L[l];
+        m->tail_ws_bytes = std::max(m->tail_ws_bytes, dfp_split_ws_bytes(B, L.OC, L.IC));
+        if (l > 0) m->tail_ws_bytes = std::max(m->tail_ws_bytes, dfp_split_ws_bytes(B, L.IC, L.OC));
+        m->tail_ws_bytes = std::max(m->tail_ws_bytes, dfp_split_ws_bytes(L.OC, L.IC, B));
+    }
+    if (m->tail_ws_bytes) ITO_TRY(m->alloc(&m->tail_ws, m->tail_ws_bytes / sizeof(int64_t)));
     for (int l = 0; l < nl; ++l) {
         DLayer& L = m->L[l];
         const Bf16View wh{L.Wh, L.OC, L.IC, L.ldw}, wl{L.Wl, L.OC, L.IC, L.ldw};
@@ -380,10 +401,13 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
             ih = Bf16View{m->L[l - 1].yh, B, L.IC, m->L[l - 1].ldy};
             il = Bf16View{m->L[l - 1].yl, B, L.IC, m->L[l - 1].ldy};
         }
-        ITO_TRY(dfp_gemm_plan(&L.pf, ih, il, false, wh, wl, false, B, L.OC, L.IC, L.p64, L.OC, m->u64(l, D_PMAX)));
+        ITO_TRY(dfp_gemm_plan(&L.pf, ih, il, false, wh, wl, false, B, L.OC, L.IC, L.p64, L.OC, m->u64(l, D_PMAX),
+                              m->tail_ws, m->tail_ws_bytes));
         if (l > 0)
-            ITO_TRY(dfp_gemm_plan(&L.pd, eh, el, false, wh, wl, true, B, L.IC, L.OC, L.pd64, L.IC, m->u64(l, D_PDMAX)));
-        ITO_TRY(dfp_gemm_plan(&L.pg, eh, el, true, ih, il, true, L.OC, L.IC, B, L.pg64, L.IC, m->u64(l, D_PGMAX)));
+            ITO_TRY(dfp_gemm_plan(&L.pd, eh, el, false, wh, wl, true, B, L.IC, L.OC, L.pd64, L.IC, m->u64(l, D_PDMAX),
+                                  m->tail_ws, m->tail_ws_bytes));
+        ITO_TRY(dfp_gemm_plan(&L.pg, eh, el, true, ih, il, true, L.OC, L.IC, B, L.pg64, L.IC, m->u64(l, D_PGMAX),
+                              m->tail_ws, m->tail_ws_bytes));
     }
     k_set_i32<<<1, 1>>>(m->ew(), m->exp_w);
     if (cudaMemcpy(m->wexp_d, m->wexp.data(), sizeof(int32_t) * nl, cudaMemcpyHostToDevice) != cudaSuccess)

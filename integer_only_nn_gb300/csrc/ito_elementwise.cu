@@ -297,8 +297,7 @@ __global__ void k_offset_grad(const int8_t* __restrict__ delta, int64_t rows, in
         g[c] = acc;
         mx = max(mx, abs_u32(acc));
     }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+    block_atomic_max(d_max, mx);
 }
 
 // NITI Steps 2-5 on INT32 offsets, saturating to int32
@@ -321,10 +320,7 @@ __global__ void k_offset_update(int32_t* __restrict__ off, const int32_t* __rest
         v = v < INT32_MIN ? INT32_MIN : (v > INT32_MAX ? INT32_MAX : v);
         off[i] = (int32_t)v;
     }
-    if (d_nonzero) {
-        cnt = __reduce_add_sync(0xffffffffu, cnt);
-        if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(d_nonzero, cnt);
-    }
+    if (d_nonzero) block_atomic_add(d_nonzero, cnt);
 }
 
 int launch_offset_grad_update(const int8_t* delta, int64_t rows, int64_t cols, int32_t* g, uint32_t* d_max,
@@ -353,8 +349,7 @@ __device__ __forceinline__ int32_t niti_step_delta(int32_t g, int s, int ws)
 
 __device__ __forceinline__ void count_nonzero(uint32_t cnt, uint32_t* d_nonzero)
 {
-    cnt = __reduce_add_sync(0xffffffffu, cnt);
-    if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(d_nonzero, cnt);
+    block_atomic_add(d_nonzero, cnt);
 }
 
 __global__ void k_niti_update_v8(int8_t* __restrict__ W, uint16_t* __restrict__ Wb, int64_t ldb,

@@ -693,8 +693,7 @@ __global__ void k_splitk_reduce(const int32_t* __restrict__ P, int splits, int64
         C[off] = acc;
         mx = max(mx, abs_u32(acc));
     }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+    block_atomic_max(d_max, mx);
 }
 
 // The split tiles of the pair kernel's last wave: C = the sum of each tile's
@@ -732,8 +731,7 @@ __global__ void k_tail_reduce(const int32_t* __restrict__ P, int tail_tiles, int
                 }
         }
     }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((threadIdx.x & 31) == 0 && mx) atomicMax(d_max, mx);
+    block_atomic_max(d_max, mx);
 }
 
 template <int BN, bool A_MN, bool B_MN>

@@ -70,6 +70,8 @@ struct DfpGemmPlan {
     int M, N, K;
     int chunk_kb;                 // K blocks of 64 per exact chunk
     int pair;                     // CTA-pair kernel (256 x 64 tiles)
+    int tail_full, tail_parts;    // pair kernel: whole tiles, K pieces per remaining tile (1: no split)
+    int64_t* tail_ws;             // [pieces][256][64] int64 partials of the split tiles
     bool a_mn, b_mn;
     int64_t* C;
     int64_t ldc;
@@ -84,9 +86,12 @@ struct DfpGemmPlan {
     int64_t ldy;
 };
 
+// tail_ws (optional): room for the int64 partial tiles of a split last wave
+// (dfp_split_ws_bytes); without it the pair kernel runs every tile whole.
 int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a_mn, const Bf16View& Bh,
                   const Bf16View& Bl, bool b_mn, int M, int N, int K, int64_t* C, int64_t ldc,
-                  unsigned long long* d_max);
+                  unsigned long long* d_max, int64_t* tail_ws = nullptr, size_t tail_ws_bytes = 0);
+size_t dfp_split_ws_bytes(int M, int N, int K);
 // Blocked-DFP forward: Y[m][n] = float(sum over K blocks j, in order, in double, of
 // P_j * 2^(ex[m][j] + ew[n][j])), P_j the exact int64 sum over block j (block: 64..512, multiple of 64)
 int dfp_gemm_plan_blocked(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, const Bf16View& Bh,
