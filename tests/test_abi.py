@@ -71,3 +71,39 @@ def test_host_side_argument_errors():
     assert L.ito_model_stat_index(None, b"ys0") == -1
     assert L.ito_model_destroy(None) == ito.ITO_OK
     assert b"" != L.ito_last_error_string()
+
+
+def test_host_side_argument_errors_new_entry_points():
+    """Conv/pooling, DFP precision and Blocked-DFP calls reject bad arguments on
+    the host, before anything is enqueued (no GPU needed)."""
+    _lib_path()
+    import integer_only_nn_gb300 as ito
+    L = ito._lib
+    p = ito.params()
+    dummy = ctypes.c_void_p(256)
+    # contraction longer than 2^20
+    assert L.ito_linear_fwd(dummy, dummy, 4, (1 << 20) + 1, 4, 1, p, dummy, 1 << 30, dummy, dummy, None, dummy,
+                            None) == ito.ITO_ERR_SHAPE
+    # conv: workspace size 0 for invalid shapes, stride outside 1..4, NULL tensors
+    assert L.ito_conv2d_workspace_size(1, 8, 8, 3, 16, 0) == 0
+    assert L.ito_conv2d_workspace_size(1, 8, 8, 3, 16, 5) == 0
+    assert L.ito_conv2d_workspace_size(1, 8, 8, 3, 16, 2) > 0
+    assert L.ito_conv2d_fwd(None, dummy, 1, 8, 8, 3, 16, 1, 1, p, dummy, 1 << 20, dummy, dummy, None, dummy,
+                            None) == ito.ITO_ERR_ARG
+    assert L.ito_conv2d_fwd(dummy, dummy, 1, 8, 8, 3, 16, 9, 1, p, dummy, 1 << 20, dummy, dummy, None, dummy,
+                            None) == ito.ITO_ERR_SHAPE
+    assert L.ito_conv2d_wgrad(dummy, dummy, 0, 8, 8, 3, 16, 1, dummy, 1 << 20, dummy, dummy,
+                              None) == ito.ITO_ERR_SHAPE
+    assert L.ito_gap_fwd(dummy, 0, 4, 4, p, dummy, dummy, None, dummy, None) == ito.ITO_ERR_SHAPE
+    assert L.ito_gap_bwd(None, dummy, 1, 4, 4, dummy, None) == ito.ITO_ERR_ARG
+    # DFP precision: bits outside 2..16
+    assert L.ito_dfp_set_bits(dummy, 16, 1, 8, None) == ito.ITO_ERR_ARG
+    assert L.ito_dfp_set_bits(dummy, 16, 8, 17, None) == ito.ITO_ERR_ARG
+    assert L.ito_dfp16_update_bits(dummy, dummy, dummy, 16, -10, 8, 17, None, None, None) == ito.ITO_ERR_ARG
+    assert L.ito_dfp16_model_set_precision(None, 0, 8, None) == ito.ITO_ERR_ARG
+    assert L.ito_dfp16_model_apt_epoch_end(None, None, None, None) == ito.ITO_ERR_ARG
+    # Blocked-DFP
+    assert L.ito_bdfp16_from_float(dummy, 4, 4, 0, dummy, dummy, None) == ito.ITO_ERR_SHAPE
+    assert L.ito_bdfp16_to_float(None, dummy, 4, 4, 2, dummy, None) == ito.ITO_ERR_ARG
+    assert L.ito_bdfp16_linear_fwd_f32(dummy, dummy, dummy, dummy, 4, 4, 4, 64, None, 0, dummy,
+                                       None) == ito.ITO_ERR_ARG
