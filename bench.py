@@ -335,6 +335,25 @@ def run_ours(args, w):
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, dist)
 
+    # the same kernels measured alone: one stream, so that no bandwidth pass shares the SMs
+    # with a contraction (the timed steps above overlap them); per-kernel figures only
+    model.set_overlap(0)
+    model.profile(True)
+    for i in range(4):
+        model.train_step(xs[i % 2], ls[i % 2], stream=stream)
+    model.profile_read()
+    iso_steps = 10
+    iso = {c: [0.0, 0.0, 0] for c in prof}
+    for k in range(iso_steps):
+        flush.fill_(k & 0xFF)
+        model.train_step(xs[k % 2], ls[k % 2], stream=stream)
+        for c, (ms, work, n) in model.profile_read().items():
+            iso[c][0] += ms
+            iso[c][1] += work
+            iso[c][2] += n
+    model.profile(False)
+    model.set_overlap(1)
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -356,6 +375,7 @@ def run_ours(args, w):
         "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims),
                    "l2": "flushed by a 256 MB write before every timed step; flush not timed",
                    "graphs": not args.no_graphs,
+                   "backward_overlap": "delta requantisation and updates on a second stream beside the contractions",
                    "parallelism": "replicas" if world > 1 else "single"},
         "int_tops": algorithmic_ops(w) * world * K / (total_ms / 1000.0) / 1e12,
         "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (bf16-embedded int8 contractions, all GEMM launches)",
@@ -367,6 +387,13 @@ def run_ours(args, w):
                    "update_gbs": u_work / (u_ms / 1000.0) / 1e9 if u_ms else None,
                    "hbm_peak_gbs": hbm, "peak_source": pk_src,
                    "ms_per_step": {k: v[0] / K for k, v in prof.items()}},
+        "isolated": {"note": "the step on one stream (no bandwidth pass beside a contraction), %d steps: "
+                             "per-kernel rates without co-running interference" % iso_steps,
+                     "gemm_tflops": iso["gemm"][1] / (iso["gemm"][0] / 1000.0) / 1e12,
+                     "gemm_frac": iso["gemm"][1] / (iso["gemm"][0] / 1000.0) / 1e12 / peak,
+                     "requant_gbs": iso["requant"][1] / (iso["requant"][0] / 1000.0) / 1e9,
+                     "update_gbs": iso["update"][1] / (iso["update"][0] / 1000.0) / 1e9,
+                     "ms_per_step": {c: v[0] / iso_steps for c, v in iso.items()}},
         "e2e": {"value": samples / e2e_s, "unit": "samples/s",
                 "h2d_bytes_per_step": int(x_h.numel() + 4 * l_h.numel()),
                 "d2h_bytes_per_step": int(4 * st_h.numel())},

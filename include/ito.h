@@ -382,6 +382,18 @@ int ito_train_step(ito_model *m, const int8_t *x, const int32_t *labels, void *s
  * frees all captured graphs. */
 int ito_model_use_graphs(ito_model *m, int enable);
 
+/* Stream layout of the backward pass (the results are the same in every mode):
+ *   0: every launch on the caller's stream;
+ *   1 (default): the requantisation of each propagated delta and the weight and
+ *      offset updates run on a second, model-owned stream beside the next
+ *      contractions (a bandwidth-bound pass shares the SMs with a tensor-core one);
+ *   2: only the weight updates run on the second stream.
+ * Events order every read after its write; the step ends joined on the caller's
+ * stream. Changing the mode synchronises the device and drops captured graphs.
+ * The environment variable ITO_OVERLAP sets the mode of new models.
+ * Errors: ITO_ERR_ARG (NULL model, mode outside 0..2). */
+int ito_model_set_overlap(ito_model *m, int mode);
+
 /* The same step from HOST buffers: copies x and labels into the model's
  * device buffers, runs the step, copies the stats array (ito_model_num_stats
  * int32) back to stats_host (may be NULL), and synchronises the stream.

@@ -100,6 +100,7 @@ _SIGS = {
     "ito_dfp16_model_read_stats": (_I, [_P, _P, _I]),
     "ito_dfp16_train_step": (_I, [_P, _P, _I32, _P]),
     "ito_model_use_graphs": (_I, [_P, _I]),
+    "ito_model_set_overlap": (_I, [_P, _I]),
     "ito_model_set_static_requant": (_I, [_P, _I, _P, _P, _P, _I, _P]),
     "ito_model_profile": (_I, [_P, _I]),
     "ito_model_profile_read": (_I, [_P, _P, _P, _P]),
@@ -452,6 +453,10 @@ class Model:
 
     def infer(self, x, logits, stream=None):
         _check(_lib.ito_infer(self._h, _ptr(x), _ptr(logits), _stream(stream)))
+
+    def set_overlap(self, mode):
+        """0: one stream; 1: backward bandwidth passes beside the contractions; 2: updates only"""
+        _check(_lib.ito_model_set_overlap(self._h, int(mode)))
 
     def use_graphs(self, enable=True):
         _check(_lib.ito_model_use_graphs(self._h, int(enable)))

@@ -18,6 +18,7 @@
 // down: delta propagation with the weights before this step's update (not for
 // the first layer), weight gradient, NITI update.
 #include <algorithm>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -109,6 +110,18 @@ struct ito_model {
     bool graph_warm = false;
     bool capturing = false;      // a step is being captured into a graph
     std::vector<GraphEntry> graphs;
+    // backward overlap: the bandwidth passes (requantisation of the propagated delta, the
+    // weight and offset updates) run on a second stream beside the next contractions
+    int overlap = 1;                    // 0: one stream; 1: requantisation and updates overlap; 2: updates only
+    cudaStream_t side = nullptr;
+    // [0] fork, [1] join, then per layer: propagated delta computed, requantised delta ready,
+    // weight gradient computed
+    std::vector<cudaEvent_t> sync_ev;
+    cudaEvent_t ev_fork() const { return sync_ev[0]; }
+    cudaEvent_t ev_join() const { return sync_ev[1]; }
+    cudaEvent_t ev_dgrad(int l) const { return sync_ev[2 + 3 * l]; }
+    cudaEvent_t ev_delta(int l) const { return sync_ev[3 + 3 * l]; }
+    cudaEvent_t ev_wgrad(int l) const { return sync_ev[4 + 3 * l]; }
     // measurement hooks
     bool prof_on = false;
     std::vector<cudaEvent_t> prof_ev;      // pairs (begin, end)
@@ -387,6 +400,22 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
                                                                          l * ST_PER_LAYER + k});
     m->stat_names.push_back({"pmax", nl * ST_PER_LAYER});
     m->stat_names.push_back({"ps", nl * ST_PER_LAYER + 1});
+
+    // second stream and ordering events of the backward overlap; ITO_OVERLAP=0 in the
+    // environment keeps every launch on the caller's stream
+    static const int overlap_env = [] {
+        const char* v = getenv("ITO_OVERLAP");
+        return v ? atoi(v) : 1;
+    }();
+    m->overlap = overlap_env >= 0 && overlap_env <= 2 ? overlap_env : 1;
+    if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "side stream creation failed");
+    for (int i = 0; i < 2 + 3 * nl; ++i) {
+        cudaEvent_t e;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "event creation failed");
+        m->sync_ev.push_back(e);
+    }
     return cudaDeviceSynchronize() == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "model init sync");
 }
 
@@ -447,54 +476,82 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
     return ITO_OK;
 }
 
+// Backward, top-down. Per layer: delta propagation with the pre-update weights (not
+// for the first layer), its requantisation, the weight gradient, the update. With the
+// overlap on, the contractions stay on `s` and the bandwidth passes go to the side
+// stream `b`: requantising layer l's propagated delta runs beside layer l's weight
+// gradient, and layer l's update beside layer l-1's delta propagation. Events order
+// every read after its write: b waits for the delta-propagation result (delta ready)
+// and for the weight gradient (before the update); s waits for the requantised delta
+// before the next layer's contractions read it; s joins b at the end of the step.
 static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, cudaStream_t s)
 {
     const int B = m->batch;
     const int nl = (int)m->L.size();
     const ito_niti_params p = m->p;
+    // b: the update stream; r: the stream of the delta requantisation
+    cudaStream_t b = m->overlap ? m->side : s;
+    cudaStream_t r = m->overlap == 1 ? m->side : s;
+    auto sync = [&](cudaEvent_t e, cudaStream_t from, cudaStream_t to) -> int {
+        if (from == to) return ITO_OK;
+        if (cudaEventRecord(e, from) != cudaSuccess || cudaStreamWaitEvent(to, e, 0) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "stream ordering event failed");
+        return ITO_OK;
+    };
     MLayer& top = m->L[nl - 1];
     ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * top.OC + 4.0 * B,
                launch_top_error(top.a8, labels, B, top.OC, m->target_mag, top.e8, top.eb, top.lde, s));
+    ITO_TRY(sync(m->ev_fork(), s, b));
     for (int l = nl - 1; l >= m->opt.trainable_from; --l) {
         MLayer& L = m->L[l];
         const bool conv = L.kind == ITO_LAYER_CONV3X3_RELU;
+        // this layer's delta (produced on b by the layer above) before its contractions
+        if (l < nl - 1 && r != s && cudaStreamWaitEvent(s, m->ev_delta(l + 1), 0) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "stream ordering event failed");
         if (L.has_dgrad) {
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
+            ITO_TRY(sync(m->ev_dgrad(l), s, r));   // the propagated delta is complete
             MLayer& prev = m->L[l - 1];
             if (conv) {
-                ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * L.rows_out * L.K + 4.0 * L.rows_in * L.IC,
+                ITO_LAUNCH(m, r, ITO_PROF_OTHER, 4.0 * L.rows_out * L.K + 4.0 * L.rows_in * L.IC,
                            launch_col2im(L.dcol, B, L.H, L.W, L.IC, L.OH, L.OW, L.stride, L.d32,
-                                         m->umax(l, ST_DMAX), s));
-                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_in * L.IC, true, true),
+                                         m->umax(l, ST_DMAX), r));
+                ITO_LAUNCH(m, r, ITO_PROF_REQUANT, requant_bytes(L.rows_in * L.IC, true, true),
                            launch_requant(L.d32, L.rows_in, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
                                           prev.mask ? nullptr : prev.a8, prev.e8, prev.eb, prev.lde,
-                                          m->sval(l, ST_DS), s, prev.mask, nullptr));
+                                          m->sval(l, ST_DS), r, prev.mask, nullptr));
             } else if (l == m->n_conv && m->has_pool) {
                 // pooled delta (the pooled activation has no ReLU), then the pooling backward
-                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, false, false),
+                ITO_LAUNCH(m, r, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, false, false),
                            launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0, nullptr, m->pe8,
-                                          nullptr, 0, m->sval(l, ST_DS), s));
-                ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * m->pool_HW * m->pool_C,
-                           launch_gap_bwd(m->pe8, prev.a8, B, m->pool_HW, m->pool_C, prev.e8, prev.eb, s));
+                                          nullptr, 0, m->sval(l, ST_DS), r));
+                ITO_LAUNCH(m, r, ITO_PROF_OTHER, 4.0 * B * m->pool_HW * m->pool_C,
+                           launch_gap_bwd(m->pe8, prev.a8, B, m->pool_HW, m->pool_C, prev.e8, prev.eb, r));
             } else {
-                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, true, prev.relu),
+                ITO_LAUNCH(m, r, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, true, prev.relu),
                            launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
                                           (prev.relu && !prev.mask) ? prev.a8 : nullptr, prev.e8, prev.eb, prev.lde,
-                                          m->sval(l, ST_DS), s, prev.mask, nullptr));
+                                          m->sval(l, ST_DS), r, prev.mask, nullptr));
             }
+            if (r != s && cudaEventRecord(m->ev_delta(l), r) != cudaSuccess)
+                return set_error(ITO_ERR_CUDA, "stream ordering event failed");
         }
         ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
+        ITO_TRY(sync(m->ev_wgrad(l), s, b));       // the weight gradient is complete
         // G read (4 B), W read and written (1 + 1 B), bf16 copy written (2 B)
-        ITO_LAUNCH(m, s, ITO_PROF_UPDATE, 8.0 * L.OC * L.K,
+        ITO_LAUNCH(m, b, ITO_PROF_UPDATE, 8.0 * L.OC * L.K,
                    launch_niti_update(L.W8, L.Wb, L.ldw, L.g32, L.OC, L.K, m->umax(l, ST_GMAX), p.target_bits,
                                       p.mu_weight, m->sval(l, ST_GS), m->sval(l, ST_WS),
-                                      reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ)), s));
+                                      reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ)), b));
+        // the offsets' gradient reads this layer's delta, whose (ping-pong) buffer the next
+        // requantisation overwrites: it runs on the requantisation stream, before that one
         if (L.static_q)
-            ITO_LAUNCH(m, s, ITO_PROF_UPDATE, (double)L.rows_out * L.OC + 12.0 * L.OC,
+            ITO_LAUNCH(m, r, ITO_PROF_UPDATE, (double)L.rows_out * L.OC + 12.0 * L.OC,
                        launch_offset_grad_update(L.e8, L.rows_out, L.OC, L.og32, m->umax(l, ST_OGMAX), L.off32,
                                                  p.target_bits, p.mu_weight, m->sval(l, ST_OGS), m->sval(l, ST_OWS),
-                                                 reinterpret_cast<uint32_t*>(m->sval(l, ST_ONZ)), s));
+                                                 reinterpret_cast<uint32_t*>(m->sval(l, ST_ONZ)), r));
     }
+    ITO_TRY(sync(m->ev_join(), b, s));
     (void)x;
     return ITO_OK;
 }
@@ -542,6 +599,8 @@ int ito_model_destroy(ito_model* m)
     cudaDeviceSynchronize();
     drop_graphs(m);
     for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
+    for (cudaEvent_t e : m->sync_ev) cudaEventDestroy(e);
+    if (m->side) cudaStreamDestroy(m->side);
     for (void* p : m->allocs) cudaFree(p);
     delete m;
     return ITO_OK;
@@ -690,6 +749,17 @@ int ito_model_profile_read(ito_model* m, double* ms, double* work, int64_t* laun
 }
 
 int ito_model_kernels_per_step(const ito_model* m) { return m ? m->launches : 0; }
+
+int ito_model_set_overlap(ito_model* m, int mode)
+{
+    if (!m || mode < 0 || mode > 2) return set_error(ITO_ERR_ARG, "bad model or overlap mode");
+    if (mode != m->overlap) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+        drop_graphs(m);   // captured steps encode the stream layout
+        m->overlap = mode;
+    }
+    return ITO_OK;
+}
 
 int ito_model_use_graphs(ito_model* m, int enable)
 {
