@@ -26,6 +26,7 @@
 // Gavg of the epoch's evaluations (Algorithm 2: adjustment between epochs).
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -85,6 +86,11 @@ struct ito_dfp16_model {
     int32_t* log_eg = nullptr;
     int64_t* tail_ws = nullptr;        // partial tiles of split last waves (shared by the step's contractions)
     size_t tail_ws_bytes = 0;
+    // backward overlap: down-conversions of the propagated delta and of the weight gradient,
+    // and the update, run on a second stream beside the next contraction (ITO_OVERLAP=0: off)
+    bool overlap = true;
+    cudaStream_t side = nullptr;
+    std::vector<cudaEvent_t> sync_ev;  // [0] fork, [1] join, per layer: delta propagated, delta ready, wgrad done
     int16_t* x16 = nullptr;
     uint16_t *xh = nullptr, *xl = nullptr;
     int64_t ldx = 0;
@@ -331,6 +337,8 @@ int ito_dfp16_model_destroy(ito_dfp16_model* m)
 {
     if (!m) return ITO_OK;
     cudaDeviceSynchronize();
+    for (cudaEvent_t e : m->sync_ev) cudaEventDestroy(e);
+    if (m->side) cudaStreamDestroy(m->side);
     for (void* p : m->allocs) cudaFree(p);
     delete m;
     return ITO_OK;
@@ -412,6 +420,19 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
     k_set_i32<<<1, 1>>>(m->ew(), m->exp_w);
     if (cudaMemcpy(m->wexp_d, m->wexp.data(), sizeof(int32_t) * nl, cudaMemcpyHostToDevice) != cudaSuccess)
         return set_error(ITO_ERR_CUDA, "weight exponent copy");
+    static const int overlap_env = [] {
+        const char* v = getenv("ITO_OVERLAP");
+        return v ? atoi(v) : 1;
+    }();
+    m->overlap = overlap_env != 0;
+    if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "side stream creation failed");
+    for (int i = 0; i < 2 + 3 * nl; ++i) {
+        cudaEvent_t e;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "event creation failed");
+        m->sync_ev.push_back(e);
+    }
     return cudaDeviceSynchronize() == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp model init");
 }
 
@@ -537,21 +558,41 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
                                 m->i32(l, D_EY), m->i32(l, D_RS), s));
     }
     k_copy_i32<<<1, 1, 0, s>>>(m->i32(nl - 1, D_EE), m->i32(nl - 1, D_EY));
+    // backward, top-down; with the overlap on, the contractions stay on s and the
+    // down-conversions and the update go to the side stream b: the propagated delta's
+    // down-conversion runs beside the weight gradient, the gradient's down-conversion
+    // and the update beside the next layer's delta propagation
+    cudaStream_t b = m->overlap ? m->side : s;
+    auto ev = [&](int l, int k) { return m->sync_ev[2 + 3 * l + k]; };   // k: 0 propagated, 1 ready, 2 wgrad
+    auto sync = [&](cudaEvent_t e, cudaStream_t from, cudaStream_t to) -> int {
+        if (from == to) return ITO_OK;
+        if (cudaEventRecord(e, from) != cudaSuccess || cudaStreamWaitEvent(to, e, 0) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "stream ordering event failed");
+        return ITO_OK;
+    };
+    ITO_TRY(sync(m->sync_ev[0], s, b));
     for (int l = nl - 1; l >= 0; --l) {
         DLayer& L = m->L[l];
         const int32_t* e_in = l == 0 ? m->ex() : m->i32(l - 1, D_EY);
+        if (l < nl - 1 && b != s && cudaStreamWaitEvent(s, ev(l + 1, 1), 0) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "stream ordering event failed");
         if (l > 0) {
             DLayer& P = m->L[l - 1];
             ITO_TRY(dfp_gemm_run(L.pd, s));
+            ITO_TRY(sync(ev(l, 0), s, b));
             ITO_TRY(launch_dfp_down(L.pd64, B, L.IC, m->u64(l, D_PDMAX), m->i32(l, D_EE), m->wexp_d + l, P.e16, P.eh,
-                                    P.el, P.ldy, m->i32(l - 1, D_EE), m->i32(l, D_RSD), s));
+                                    P.el, P.ldy, m->i32(l - 1, D_EE), m->i32(l, D_RSD), b));
+            if (b != s && cudaEventRecord(ev(l, 1), b) != cudaSuccess)
+                return set_error(ITO_ERR_CUDA, "stream ordering event failed");
         }
         ITO_TRY(dfp_gemm_run(L.pg, s));
+        ITO_TRY(sync(ev(l, 2), s, b));
         ITO_TRY(launch_dfp_down(L.pg64, L.OC, L.IC, m->u64(l, D_PGMAX), m->i32(l, D_EE), e_in, L.g16, nullptr, nullptr,
-                                0, m->i32(l, D_EG), m->i32(l, D_RSG), s, m->u64(l, D_GABS)));
+                                0, m->i32(l, D_EG), m->i32(l, D_RSG), b, m->u64(l, D_GABS)));
         ITO_TRY(launch_dfp_update(L.W, L.Wh, L.Wl, L.ldw, L.g16, L.OC, L.IC, m->i32(l, D_EG), m->wexp[l], m->eta,
-                                  m->i32(l, D_K), reinterpret_cast<uint32_t*>(m->i32(l, D_NZ)), s, m->wbits[l]));
+                                  m->i32(l, D_K), reinterpret_cast<uint32_t*>(m->i32(l, D_NZ)), b, m->wbits[l]));
     }
+    ITO_TRY(sync(m->sync_ev[1], b, s));
     if (m->apt) {
         // Algorithm 2: Gavg is evaluated at every eval_every-th step of the epoch
         if (m->apt_step % m->ap.eval_every == 0) {
