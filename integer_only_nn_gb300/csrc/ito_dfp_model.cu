@@ -132,7 +132,8 @@ static size_t dws_b(int B, int IC, int OC) { return al256((size_t)2 * 2 * (OC > 
 // partial tiles of a split last wave, for whichever of the three contractions needs most
 static size_t dws_c(int B, int IC, int OC)
 {
-    const size_t a = dfp_split_ws_bytes(B, OC, IC), b = dfp_split_ws_bytes(B, IC, OC), c = dfp_split_ws_bytes(OC, IC, B);
+    const size_t a = dfp_split_ws_bytes(B, OC, IC), b = dfp_split_ws_bytes(B, IC, OC),
+                 c = dfp_split_ws_bytes(OC, IC, B);
     return al256(a > b ? (a > c ? a : c) : (b > c ? b : c));
 }
 static int64_t* dws_tail(void* ws, int B, int IC, int OC)
@@ -185,7 +186,8 @@ int ito_dfp16_linear_fwd(const int16_t* x, const int32_t* d_exp_x, const int16_t
     DfpGemmPlan g;
     ITO_TRY(dfp_gemm_plan(&g, Bf16View{xa.h, B, IC, ld}, Bf16View{xa.l, B, IC, ld}, false, Bf16View{wb.h, OC, IC, ld},
                           Bf16View{wb.l, OC, IC, ld}, false, B, OC, IC, p64, OC,
-                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC), dws_c(B, IC, OC)));
+                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC),
+                          dws_c(B, IC, OC)));
     ITO_TRY(dfp_gemm_run(g, s));
     return launch_dfp_down(p64, B, OC, reinterpret_cast<unsigned long long*>(d_max), d_exp_x, d_exp_w, y, nullptr,
                            nullptr, 0, d_exp_y, d_rs, s);
@@ -208,7 +210,8 @@ int ito_dfp16_linear_bwd_delta(const int16_t* delta, const int32_t* d_exp_delta,
     DfpGemmPlan g;
     ITO_TRY(dfp_gemm_plan(&g, Bf16View{ea.h, B, OC, lde}, Bf16View{ea.l, B, OC, lde}, false,
                           Bf16View{wb.h, OC, IC, ldw}, Bf16View{wb.l, OC, IC, ldw}, true, B, IC, OC, p64, IC,
-                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC), dws_c(B, IC, OC)));
+                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC),
+                          dws_c(B, IC, OC)));
     ITO_TRY(dfp_gemm_run(g, s));
     return launch_dfp_down(p64, B, IC, reinterpret_cast<unsigned long long*>(d_max), d_exp_delta, d_exp_w, delta_prev,
                            nullptr, nullptr, 0, d_exp_prev, d_rs, s);
@@ -230,7 +233,8 @@ int ito_dfp16_linear_wgrad(const int16_t* delta, const int32_t* d_exp_delta, con
     DfpGemmPlan gp;
     ITO_TRY(dfp_gemm_plan(&gp, Bf16View{ea.h, B, OC, lde}, Bf16View{ea.l, B, OC, lde}, true,
                           Bf16View{xb.h, B, IC, ldx}, Bf16View{xb.l, B, IC, ldx}, true, OC, IC, B, p64, IC,
-                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC), dws_c(B, IC, OC)));
+                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC),
+                          dws_c(B, IC, OC)));
     ITO_TRY(dfp_gemm_run(gp, s));
     return launch_dfp_down(p64, OC, IC, reinterpret_cast<unsigned long long*>(d_max), d_exp_delta, d_exp_x, g, nullptr,
                            nullptr, 0, d_exp_g, d_rs, s);
@@ -267,7 +271,8 @@ int ito_dfp16_linear_fwd_f32(const int16_t* x, const int32_t* d_exp_x, const int
     DfpGemmPlan g;
     ITO_TRY(dfp_gemm_plan(&g, Bf16View{xa.h, B, IC, ld}, Bf16View{xa.l, B, IC, ld}, false, Bf16View{wb.h, OC, IC, ld},
                           Bf16View{wb.l, OC, IC, ld}, false, B, OC, IC, p64, OC,
-                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC), dws_c(B, IC, OC)));
+                          reinterpret_cast<unsigned long long*>(d_max), dws_tail(workspace, B, IC, OC),
+                          dws_c(B, IC, OC)));
     ITO_TRY(dfp_gemm_run(g, s));
     return launch_p64_to_float(p64, (int64_t)B * OC, d_exp_x, d_exp_w, y, s);
 }
