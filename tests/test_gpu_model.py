@@ -84,3 +84,24 @@ def test_model_graph_replay_lockstep(index, steps):
         compare_records(rec, g.record(), t)
         weights = [rec["w%d" % l] for l in range(len(weights))]
     assert g.ito.ito_get_error() == 0
+
+
+@pytest.mark.parametrize("index,pingpong", [(1, False), (6, True), (2, True)])
+def test_overlap_modes_give_identical_steps(index, pingpong):
+    """The backward overlap moves bandwidth passes to a second stream; every
+    tensor and statistic after three steps is the same in all three modes
+    (one stream, requantisation + updates overlapped, updates only). The
+    default, overlapped mode is the one the lockstep and digest tests compare
+    with the oracle."""
+    w = si.by_name(index)
+    results = []
+    for mode in (0, 1, 2):
+        g = GpuRun(w, pingpong_grads=pingpong)
+        g.model.set_overlap(mode)
+        for t in range(3):
+            g.step(t)
+        results.append(g.record())
+    for mode, r in zip((1, 2), results[1:]):
+        assert r.keys() == results[0].keys()
+        for k in r:
+            assert np.array_equal(np.asarray(r[k]), np.asarray(results[0][k])), (mode, k)
