@@ -77,6 +77,15 @@ const char *ito_last_error_string(void);
 /* Library version, for the Python binding's sanity check. */
 int ito_version(void);
 
+/* Self-test of failure detection (the pages have no counterpart): launches one
+ * CTA that waits on an mbarrier nothing completes, with the bounded wait every
+ * pipeline barrier of the contraction kernels uses. After the wait's limit
+ * (2 s) the kernel records ITO_ERR_TIMEOUT in the device error word and
+ * returns; the call synchronises `stream` and returns ITO_OK, and
+ * ito_get_error() then reports ITO_ERR_TIMEOUT. No GPU fault, trap or hang is
+ * involved; the context stays usable. Errors: ITO_ERR_CUDA. */
+int ito_selftest_wait_timeout(void *stream);
+
 /* ------------------------------------------------------------------------
  * Single-layer operations (int8 Linear layer, NITI)
  *

@@ -54,6 +54,7 @@ _SIGS = {
     "ito_version": (_I, []),
     "ito_get_error": (_I, []),
     "ito_last_error_string": (ctypes.c_char_p, []),
+    "ito_selftest_wait_timeout": (_I, [_P]),
     "ito_linear_workspace_size": (_SZ, [_I, _I, _I]),
     "ito_linear_fwd": (_I, [_P, _P, _I, _I, _I, _I, NitiParams, _P, _SZ, _P, _P, _P, _P, _P]),
     "ito_linear_fwd_noalloc": (_I, [_P, _P, _I, _I, _I, _I, NitiParams, _P, _P, _P, _P, _P]),
@@ -161,6 +162,11 @@ def ito_version() -> int:
 
 def ito_get_error() -> int:
     return _lib.ito_get_error()
+
+
+def ito_selftest_wait_timeout(stream=None):
+    """A kernel whose bounded wait runs out (about 2 s); ito_get_error() then reports ITO_ERR_TIMEOUT."""
+    _check(_lib.ito_selftest_wait_timeout(_stream(stream)))
 
 
 # ----------------------------------------------------------- single layer

@@ -149,6 +149,13 @@ int ito_get_error(void)
     return v;
 }
 
+int ito_selftest_wait_timeout(void* stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ITO_TRY(launch_wait_timeout_selftest(s));
+    return cuda_ok(cudaStreamSynchronize(s), "self-test");
+}
+
 size_t ito_linear_workspace_size(int B, int IC, int OC)
 {
     if (B < 1 || IC < 1 || OC < 1) return 0;

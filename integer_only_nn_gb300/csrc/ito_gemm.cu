@@ -630,6 +630,33 @@ __global__ void __launch_bounds__(256)
     if ((threadIdx.x & 31) == 0 && mx != 0) atomicMax(d_max, mx);
 }
 
+// ------------------------------------------------------ failure self-test
+
+// One CTA waits on an mbarrier that nothing completes: the bounded wait gives
+// up after its time limit, records ITO_ERR_TIMEOUT in the error word and the
+// kernel returns (the wait every pipeline barrier of the contractions uses).
+__global__ void k_wait_timeout_selftest(int* __restrict__ err)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, err);
+}
+
+int launch_wait_timeout_selftest(cudaStream_t s)
+{
+    int* err = device_error_word();
+    if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
+    k_wait_timeout_selftest<<<1, 32, 0, s>>>(err);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+}
+
 // ----------------------------------------------------------- host launchers
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode()

@@ -51,6 +51,8 @@ struct GemmPlan {
 
 // Device address of this library's error word on the current device.
 int* device_error_word();
+// One CTA whose bounded mbarrier wait runs out (records ITO_ERR_TIMEOUT).
+int launch_wait_timeout_selftest(cudaStream_t s);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (nullptr if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 get_encode();
