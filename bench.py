@@ -354,6 +354,15 @@ def run_ours(args, w):
     model.profile(False)
     model.set_overlap(1)
 
+    if args.stats_log and rank == 0:
+        # per-step NITI statistics (shift of every requantised tensor, weight shift,
+        # nonzero weight steps) for a few steps after the timed ones, one JSON line each
+        with open(args.stats_log, "w") as f:
+            for t in range(10):
+                model.train_step(xs[t % 2], ls[t % 2], stream=stream)
+                stream.synchronize()
+                f.write(json.dumps({"step": t, **{k: int(v) for k, v in model.stats().items()}}) + "\n")
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -533,6 +542,9 @@ def main():
     ap.add_argument("--op", choices=("fwd", "dgrad", "wgrad", "dfp16_fwd_f32", "bdfp16_fwd_f32"),
                     help="time one single-layer call instead")
     ap.add_argument("--block", type=int, default=512, help="Blocked-DFP block length for --op bdfp16_fwd_f32")
+    ap.add_argument("--stats-log", default=None,
+                    help="write per-step NITI statistics (shifts, nonzero updates) of 10 steps after the timed "
+                         "ones to this JSONL file")
     ap.add_argument("--shape", default="8192,4096,4096", help="B,IC,OC for --op")
     args = ap.parse_args()
     if args.warmup < 3:
