@@ -343,7 +343,12 @@ int ito_model_get_weights(const ito_model *m, int layer, int8_t *W, int on_host,
  * "m0" its bit-packed ReLU mask (packed_masks models),
  * "e0" int8 delta at the output of layer 0, "d1" int32 delta-propagation
  * contraction of layer 1, "g0" int32 weight gradient, "w0" int8 weights,
- * "stats" int32 scalars; see ito_model_stat_index). Writes the device
+ * "stats" int32 scalars; see ito_model_stat_index; "spec" int32 [6 * layers]:
+ * the forward and delta-propagation shift predictions the step used, the
+ * shifts the step computed, and 1 where the contraction's epilogue speculates,
+ * each block of 2 * layers indexed by weight layer, -1 where none; "spec_count"
+ * int64 [2]: predictions that held and that missed since creation, scored at
+ * the start of the following step (see ito_model_set_speculation)). Writes the device
  * pointer, the element type (1 = int8, 2 = int16, 4 = int32, 8 = int64) and
  * element count. The pointer stays valid until ito_model_destroy.
  * Errors: ITO_ERR_ARG (unknown name). */
@@ -402,6 +407,20 @@ int ito_model_use_graphs(ito_model *m, int enable);
  * The environment variable ITO_OVERLAP sets the mode of new models.
  * Errors: ITO_ERR_ARG (NULL model, mode outside 0..2). */
 int ito_model_set_overlap(ito_model *m, int mode);
+
+/* Speculative requantisation (default on; the environment variable
+ * ITO_SPECULATE=0 turns it off for new models). NITI's shift of a tensor
+ * depends on the whole tensor's max, so requantisation is a second pass over
+ * the int32 result. With speculation on, the epilogue of the forward and
+ * delta-propagation contractions (CTA-pair kernel; int8 row length a multiple
+ * of 16; no packed masks, static requantisation or ping-pong buffers) also
+ * writes the requantised int8 tensor and its bf16 copy using the shift the
+ * same tensor had in the previous step; the requantisation pass then computes
+ * this step's shift from the max and returns at once when it is the same, and
+ * otherwise rewrites both outputs. The result is NITI's in either case (the
+ * int32 tensor and its max are still written). Changing the setting
+ * synchronises the device and drops captured graphs. Errors: ITO_ERR_ARG. */
+int ito_model_set_speculation(ito_model *m, int enable);
 
 /* The same step from HOST buffers: copies x and labels into the model's
  * device buffers, runs the step, copies the stats array (ito_model_num_stats

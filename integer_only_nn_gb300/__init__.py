@@ -102,6 +102,7 @@ _SIGS = {
     "ito_dfp16_train_step": (_I, [_P, _P, _I32, _P]),
     "ito_model_use_graphs": (_I, [_P, _I]),
     "ito_model_set_overlap": (_I, [_P, _I]),
+    "ito_model_set_speculation": (_I, [_P, _I]),
     "ito_model_set_static_requant": (_I, [_P, _I, _P, _P, _P, _I, _P]),
     "ito_model_profile": (_I, [_P, _I]),
     "ito_model_profile_read": (_I, [_P, _P, _P, _P]),
@@ -463,6 +464,10 @@ class Model:
     def set_overlap(self, mode):
         """0: one stream; 1: backward bandwidth passes beside the contractions; 2: updates only"""
         _check(_lib.ito_model_set_overlap(self._h, int(mode)))
+
+    def set_speculation(self, enable=True):
+        """speculative requantisation in the contraction epilogues (exact; see include/ito.h)"""
+        _check(_lib.ito_model_set_speculation(self._h, int(bool(enable))))
 
     def use_graphs(self, enable=True):
         _check(_lib.ito_model_use_graphs(self._h, int(enable)))

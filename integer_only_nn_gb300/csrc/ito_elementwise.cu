@@ -132,14 +132,23 @@ __device__ __forceinline__ int32_t requant_one(int32_t y, int s, int relu, int g
 // The optional bit-packed ReLU masks hold one byte per eight elements of a
 // row (cols / 8 bytes per row; bit j is element j of the group): mask_out
 // receives (q > 0) of the result, gate_bits replaces the int8 gate.
+// s_pred (optional): the shift a speculative requantisation in the contraction's
+// epilogue used; when it equals this launch's shift, out8 and outb already hold
+// the result and the kernel returns at once. s_last (optional) receives the shift
+// (the next step's prediction).
 __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
                              const uint32_t* __restrict__ d_max, int target_bits, int relu,
                              const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
                              int64_t ldb, int32_t* __restrict__ d_shift, const uint8_t* __restrict__ gate_bits,
-                             uint8_t* __restrict__ mask_out)
+                             uint8_t* __restrict__ mask_out, const int32_t* __restrict__ s_pred,
+                             int32_t* __restrict__ s_last)
 {
     const int s = shift_for(*d_max, target_bits);
-    if (d_shift && blockIdx.x == 0 && threadIdx.x == 0) *d_shift = s;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (d_shift) *d_shift = s;
+        if (s_last) *s_last = s;
+    }
+    if (s_pred && *s_pred == s) return;
     const int64_t groups = rows * (cols >> 3);
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
@@ -177,10 +186,15 @@ __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_
 __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
                             const uint32_t* __restrict__ d_max, int target_bits, int relu,
                             const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
-                            int64_t ldb, int32_t* __restrict__ d_shift)
+                            int64_t ldb, int32_t* __restrict__ d_shift, const int32_t* __restrict__ s_pred,
+                            int32_t* __restrict__ s_last)
 {
     const int s = shift_for(*d_max, target_bits);
-    if (d_shift && blockIdx.x == 0 && threadIdx.x == 0) *d_shift = s;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (d_shift) *d_shift = s;
+        if (s_last) *s_last = s;
+    }
+    if (s_pred && *s_pred == s) return;
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int32_t q = requant_one(Y[i], s, relu, gate ? gate[i] > 0 : 1);
@@ -194,8 +208,10 @@ __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t
 
 int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
                    const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
-                   const uint8_t* gate_bits, uint8_t* mask_out)
+                   const uint8_t* gate_bits, uint8_t* mask_out, const int32_t* s_pred, int32_t* s_last)
 {
+    if (s_pred && (gate_bits || mask_out))
+        return set_error(ITO_ERR_UNSUPPORTED, "speculative requantisation with bit-packed masks");
     if (rows < 1 || cols < 1) return ITO_OK;
     const bool vec = cols % 8 == 0 && aligned(Y, 16) && aligned(out8, 8) && (!gate || aligned(gate, 8)) &&
                      (!outb || (aligned(outb, 16) && ldb % 8 == 0));
@@ -203,12 +219,53 @@ int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t*
         return set_error(ITO_ERR_UNSUPPORTED, "bit-packed masks need rows of a multiple of 8 elements");
     if (vec)
         k_requant_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(
-            Y, rows, cols, d_max, target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out);
+            Y, rows, cols, d_max, target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out, s_pred,
+            s_last);
     else
         k_requant_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(Y, rows, cols, d_max, target_bits, relu,
-                                                                          gate, out8, outb, ldb, d_shift);
+                                                                          gate, out8, outb, ldb, d_shift, s_pred,
+                                                                          s_last);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "requant launch: %s", cudaGetErrorString(e));
+}
+
+// --------------------------------------------- shift prediction (speculation)
+
+// At the start of a step: first score the previous step's speculation. Over the
+// slots a contraction epilogue speculated on (used[i] != 0, pred[i] >= 0),
+// count[0] += the predictions that held (pred[i] == last[i], the shift that step
+// computed) and count[1] += the ones that did not (both int64). Then this step's
+// predictions: pred[i] = last[i] where used and on, else -1 (no speculation).
+__global__ void k_roll_shift_predictions(int32_t* __restrict__ pred, const int32_t* __restrict__ last,
+                                         const int32_t* __restrict__ used, unsigned long long* __restrict__ count,
+                                         int n, int on)
+{
+    unsigned hits = 0, misses = 0;
+    for (int i = threadIdx.x; i < n; i += 32) {
+        const int32_t p = pred[i], l = last[i];
+        const bool u = used[i] != 0;
+        if (u && p >= 0) {
+            hits += p == l;
+            misses += p != l;
+        }
+        pred[i] = (on && u) ? l : -1;
+    }
+    hits = __reduce_add_sync(0xffffffffu, hits);
+    misses = __reduce_add_sync(0xffffffffu, misses);
+    if (threadIdx.x == 0) {
+        count[0] += hits;
+        count[1] += misses;
+    }
+}
+
+int launch_roll_shift_predictions(int32_t* pred, const int32_t* last, const int32_t* used, int64_t* count, int n,
+                                  int on, cudaStream_t s)
+{
+    if (n < 1) return ITO_OK;
+    k_roll_shift_predictions<<<1, 32, 0, s>>>(pred, last, used, reinterpret_cast<unsigned long long*>(count), n,
+                                              on);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "prediction launch: %s", cudaGetErrorString(e));
 }
 
 // ------------------------------------------- static requantisation + offsets

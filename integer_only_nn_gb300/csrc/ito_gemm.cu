@@ -330,6 +330,18 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
 // Exactness and the epilogue are as in k_gemm_tc; both CTAs' epilogue warps
 // release an accumulator buffer on the leader's barrier.
 
+// Speculative requantisation in the pair kernel's epilogue (FusedRq.pred set):
+// with the shift the same tensor had in the previous step, the epilogue also
+// writes q = sat8(rhu(y, s)) (ReLU'd, or zeroed where gate <= 0) as int8 and as
+// bf16. The requantisation kernel that follows computes the true shift from
+// this launch's max and rewrites both outputs only when it differs.
+struct FusedRq {
+    const int32_t* pred;   // predicted shift (device word; < 0: none this step); nullptr: off
+    const int8_t* gate;    // [M][ldg] int8 ReLU gate, or nullptr
+    int64_t ldg;
+    int relu;
+};
+
 struct Tc2Cfg {
     static constexpr int BM = 128;                          // rows of A per CTA (256 per pair)
     static constexpr int BN = 256;                          // columns per pair tile
@@ -345,12 +357,14 @@ struct Tc2Cfg {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
 };
 
+// Ten warps a CTA: three share one SM sub-partition's 16,384 registers, so a thread gets 168
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP, int use_tma_store,
-               int M, int N, int K, int chunk_kb, int group, int full_tiles, int parts, int32_t* __restrict__ C,
-               int64_t ldc, uint32_t* __restrict__ d_max, int* __restrict__ err)
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+               const __grid_constant__ CUtensorMap tmO8, const __grid_constant__ CUtensorMap tmOB, FusedRq fz,
+               int use_tma_store, int M, int N, int K, int chunk_kb, int group, int full_tiles, int parts,
+               int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
     using Cfg = Tc2Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -482,6 +496,11 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
         const int half = e >> 2;
         uint8_t* stg = staging + e * 4096;
         const uint32_t stg_row = smem_u32(stg) + lane * 128;
+        // speculative requantisation this launch: the predicted shift (< 0: none). The int32
+        // result then goes to L2 marked evict-first (only a misprediction reads it back) and
+        // so does the int8 copy (read in a later pass); the bf16 copy, the next contraction's
+        // operand, is stored with the default policy.
+        const int sp = fz.pred ? *fz.pred : -1;
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
@@ -489,6 +508,38 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
             const WorkItem wi = work_item(w, full_tiles, parts, num_chunks);
             int tm, tn;
             sched.coords(wi.tile, tm, tn);
+            const int row0 = tm * 2 * BM + (int)rank * BM + quad * 32;
+            const int col0 = tn * BN + half * HALF;
+            const bool fused = sp >= 0 && wi.slot < 0 && use_tma_store && row0 < M && col0 < N;
+            if (fused && fz.gate) {
+                // the gate tile (this warp's 32 rows x 128 int8 columns) into the staging buffer
+                // while the accumulator is still being computed, in the swizzled layout the
+                // stores use: coalesced 16-byte loads (lane L takes chunk L % 8 of rows
+                // 4 i + L / 8); outside the tensor the gate reads 0
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+                const int cc = lane & 7, rr = lane >> 3;
+                const bool col_in = col0 + cc * 16 < N;
+                const int8_t* gsrc = fz.gate + (int64_t)(row0 + rr) * fz.ldg + col0 + cc * 16;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    int4 gv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = (h * 4 + i) * 4 + rr;
+                        gv[i] = (col_in && row0 + r < M)
+                                    ? __ldg(reinterpret_cast<const int4*>(gsrc + (int64_t)(r - rr) * fz.ldg))
+                                    : make_int4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = (h * 4 + i) * 4 + rr;
+                        st_shared_v4(smem_u32(stg) + r * 128 + ((cc ^ (r & 7)) << 4), gv[i].x, gv[i].y, gv[i].z,
+                                     gv[i].w);
+                    }
+                }
+                __syncwarp();
+            }
             int32_t acc[HALF];
 #pragma unroll
             for (int i = 0; i < HALF; ++i) acc[i] = 0;
@@ -537,9 +588,28 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
             for (int i = 0; i < HALF; ++i) mx = max(mx, abs_u32(acc[i]));
             mx = __reduce_max_sync(0xffffffffu, mx);
             if (lane == 0 && mx != 0) atomicMax(d_max, mx);
-            const int row0 = tm * 2 * BM + (int)rank * BM + quad * 32;
-            const int col0 = tn * BN + half * HALF;
             if (use_tma_store) {
+                // speculative requantisation: the gate's open (> 0) bits of this lane's row, read
+                // from the staged tile before the staging buffer is reused
+                uint32_t open[HALF / 32];
+#pragma unroll
+                for (int k = 0; k < HALF / 32; ++k) open[k] = 0xffffffffu;
+                if (fused && fz.gate) {
+#pragma unroll
+                    for (int j = 0; j < HALF / 16; ++j) {
+                        const uint4 gv = ld_shared_v4(stg_row + ((j ^ (lane & 7)) << 4));
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                        uint32_t bits = 0;
+#pragma unroll
+                        for (int b = 0; b < 16; ++b) bits |= ((int8_t)(gw[b >> 2] >> (8 * (b & 3))) > 0 ? 1u : 0u) << b;
+                        if (j & 1)
+                            open[j >> 1] = (open[j >> 1] & 0xffffu) | (bits << 16);
+                        else
+                            open[j >> 1] = bits;
+                    }
+                    __syncwarp();
+                }
+                // the int32 result (evict-first in L2 when speculating: only a misprediction reads it)
 #pragma unroll
                 for (int g = 0; g < HALF / 32; ++g) {
                     if (row0 >= M || col0 + g * 32 >= N) continue;
@@ -552,8 +622,66 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, stg, col0 + g * 32, row0);
+                        if (fused)
+                            tma_store_2d_hint(&tmC, stg, col0 + g * 32, row0, l2_policy_evict_first());
+                        else
+                            tma_store_2d(&tmC, stg, col0 + g * 32, row0);
                         bulk_commit();
+                    }
+                }
+                if (fused) {
+                    // q = sat8(rhu(y, sp)), ReLU'd or zeroed where the gate is closed, as one
+                    // 32 x 128 int8 box (evict-first: a later pass reads it) and two 32 x 64 bf16
+                    // boxes (the next contraction's operand)
+                    uint32_t q8w[HALF / 4];      // the 128 int8 results, packed four to a word
+#pragma unroll
+                    for (int k = 0; k < HALF / 4; ++k) {
+                        uint32_t packed = 0;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const int i = 4 * k + b;
+                            int32_t q = sat8(rhu32(acc[i], sp));
+                            if ((fz.relu && q < 0) || !((open[i >> 5] >> (i & 31)) & 1u)) q = 0;
+                            packed |= ((uint32_t)(uint8_t)(int8_t)q) << (8 * b);
+                        }
+                        q8w[k] = packed;
+                    }
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), (int32_t)q8w[4 * j], (int32_t)q8w[4 * j + 1],
+                                     (int32_t)q8w[4 * j + 2], (int32_t)q8w[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d_hint(&tmO8, stg, col0, row0, l2_policy_evict_first());
+                        bulk_commit();
+                    }
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        if (col0 + g * 64 >= N) continue;
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint32_t wv[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const int i = g * 64 + j * 8 + 2 * h;
+                                const int8_t lo = (int8_t)(q8w[i >> 2] >> (8 * (i & 3)));
+                                const int8_t hi = (int8_t)(q8w[(i + 1) >> 2] >> (8 * ((i + 1) & 3)));
+                                wv[h] = (uint32_t)int_to_bf16_bits(lo) | ((uint32_t)int_to_bf16_bits(hi) << 16);
+                            }
+                            st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), (int32_t)wv[0], (int32_t)wv[1],
+                                         (int32_t)wv[2], (int32_t)wv[3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmOB, stg, col0 + g * 64, row0);
+                            bulk_commit();
+                        }
                     }
                 }
             } else {
@@ -882,8 +1010,10 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.mapP, p.use_tma_store, p.M, p.N, p.K,
-                                       p.chunk_kb, p.group, p.tail_full, p.tail_parts, p.C, p.ldc, p.d_max, p.err);
+    const FusedRq fz{p.rq_pred, p.rq_gate, p.rq_ldg, p.rq_relu};
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.mapP, p.mapO8, p.mapOB, fz,
+                                       p.use_tma_store, p.M, p.N, p.K, p.chunk_kb, p.group, p.tail_full, p.tail_parts,
+                                       p.C, p.ldc, p.d_max, p.err);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "pair gemm launch: %s", cudaGetErrorString(e));
     if (p.tail_parts > 1) {
         const TileSched sched{(p.M + 255) / 256, (p.N + 255) / 256, p.group};
@@ -1019,6 +1149,44 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
         if (cr != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)cr);
         p->use_tma_store = 1;
     }
+    return ITO_OK;
+}
+
+int gemm_plan_fuse_requant(GemmPlan* p, const int32_t* pred, int relu, const int8_t* gate, int64_t ldg,
+                           int8_t* out8, int64_t ld8, uint16_t* outb, int64_t ldb)
+{
+    p->rq_pred = nullptr;
+    // the pair kernel's TMA-store epilogue over whole tiles; int8 rows must be 16-byte multiples
+    if (!p->pair || !p->use_tma_store || p->tail_parts != 1 || !pred || !out8 || !outb) return ITO_OK;
+    if (p->N % 16 || ld8 % 16 || ldb % 8 || (reinterpret_cast<uintptr_t>(out8) & 15) ||
+        (reinterpret_cast<uintptr_t>(outb) & 15))
+        return ITO_OK;
+    if (gate && (ldg % 16 || (reinterpret_cast<uintptr_t>(gate) & 15))) return ITO_OK;
+    auto enc = get_encode();
+    if (!enc) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint32_t estr[2] = {1, 1};
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)p->N, (cuuint64_t)p->M};
+        cuuint64_t strides[1] = {(cuuint64_t)ld8};
+        cuuint32_t box[2] = {128, 32};
+        CUresult cr = enc(&p->mapO8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, out8, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (int8 out) failed (%d)", (int)cr);
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)p->N, (cuuint64_t)p->M};
+        cuuint64_t strides[1] = {(cuuint64_t)ldb * 2};
+        cuuint32_t box[2] = {64, 32};
+        CUresult cr = enc(&p->mapOB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, outb, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (bf16 out) failed (%d)", (int)cr);
+    }
+    p->rq_pred = pred;
+    p->rq_gate = gate;
+    p->rq_ldg = ldg;
+    p->rq_relu = relu;
     return ITO_OK;
 }
 

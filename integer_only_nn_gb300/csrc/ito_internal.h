@@ -38,6 +38,12 @@ struct GemmPlan {
     int pair;   // CTA-pair (cta_group::2) kernel
     int group;  // row tiles per raster group (L2 reuse)
     int tail_full, tail_parts;    // pair kernel: whole tiles, K pieces per remaining tile (1: no split)
+    // pair kernel: speculative requantisation in the epilogue (rq_pred != nullptr)
+    CUtensorMap mapO8, mapOB;
+    const int32_t* rq_pred;
+    const int8_t* rq_gate;
+    int64_t rq_ldg;
+    int rq_relu;
     int M, N, K, bn, chunk_kb;
     int splits, kb_per_split;     // split-K: slices of kb_per_split K blocks (splits == 1: none)
     int32_t* split_ws;            // [splits][M][ldc] int32 partials
@@ -73,6 +79,12 @@ struct DfpGemmPlan {
     int chunk_kb;                 // K blocks of 64 per exact chunk
     int pair;                     // CTA-pair kernel (256 x 64 tiles)
     int tail_full, tail_parts;    // pair kernel: whole tiles, K pieces per remaining tile (1: no split)
+    // pair kernel: speculative requantisation in the epilogue (rq_pred != nullptr)
+    CUtensorMap mapO8, mapOB;
+    const int32_t* rq_pred;
+    const int8_t* rq_gate;
+    int64_t rq_ldg;
+    int rq_relu;
     int64_t* tail_ws;             // [pieces][256][64] int64 partials of the split tiles
     bool a_mn, b_mn;
     int64_t* C;
@@ -140,6 +152,13 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
               int chunk_terms = kExactChunk);
 // bytes of split-K partials gemm_plan would use for this contraction (0: no split)
 size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc);
+// Turns on the speculative requantisation of a planned pair-kernel contraction:
+// out8 [M][ld8] int8 and outb [M][ldb] bf16 receive sat8(rhu(C, *pred)), ReLU'd if
+// relu, zeroed where gate [M][ldg] <= 0 (gate may be null). Leaves the plan
+// unfused (no error) when the contraction does not qualify (not the pair kernel,
+// a split last wave, N or pitches not multiples of 16 bytes).
+int gemm_plan_fuse_requant(GemmPlan* p, const int32_t* pred, int relu, const int8_t* gate, int64_t ldg,
+                           int8_t* out8, int64_t ld8, uint16_t* outb, int64_t ldb);
 int gemm_run(const GemmPlan& p, cudaStream_t s);
 int gemm_simt(const int8_t* A, int64_t sam, int64_t sak, const int8_t* B, int64_t sbn, int64_t sbk, int M, int N,
               int K, int32_t* C, int64_t ldc, uint32_t* d_max, cudaStream_t s);
@@ -156,9 +175,15 @@ int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* d
 // result is zeroed where gate <= 0 (delta propagation through a ReLU).
 // gate_bits / mask_out (optional, cols % 8 == 0): bit-packed ReLU masks, one
 // byte per 8 elements: read in place of the int8 gate / written from the result.
+// s_pred / s_last: see k_requant_v8 (speculative requantisation in a contraction epilogue)
 int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
                    const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
-                   const uint8_t* gate_bits = nullptr, uint8_t* mask_out = nullptr);
+                   const uint8_t* gate_bits = nullptr, uint8_t* mask_out = nullptr, const int32_t* s_pred = nullptr,
+                   int32_t* s_last = nullptr);
+// scores the last step's predictions into count[0] (held) / count[1] (missed) over the used
+// slots, then pred[i] = (on && used[i]) ? last[i] : -1 for i < n
+int launch_roll_shift_predictions(int32_t* pred, const int32_t* last, const int32_t* used, int64_t* count, int n,
+                                  int on, cudaStream_t s);
 int launch_u8_to_bf16(const uint8_t* src, int64_t rows, int64_t cols, uint16_t* dst, int64_t ldd, cudaStream_t s);
 // static per-channel requantisation: clip(floor((Y + off[c]) * mult[c] / 2^k[c]), relu ? 0 : -128, 127)
 int launch_requant_static(const int32_t* Y, int64_t rows, int64_t cols, const int32_t* off, const int32_t* mult,

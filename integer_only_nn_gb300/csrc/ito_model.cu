@@ -113,6 +113,16 @@ struct ito_model {
     // backward overlap: the bandwidth passes (requantisation of the propagated delta, the
     // weight and offset updates) run on a second stream beside the next contractions
     int overlap = 1;                    // 0: one stream; 1: requantisation and updates overlap; 2: updates only
+    // speculative requantisation: [0, nl) forward and [nl, 2nl) delta-propagation shift predictions,
+    // then the shifts of the last step in the same order, then 1 where the contraction's epilogue
+    // speculates (its plan is fused); spec_count: predictions that held, that missed (int64)
+    bool speculate = true;
+    int32_t* spec = nullptr;
+    int64_t* spec_count = nullptr;
+    int32_t* pred_y(int l) { return spec + l; }
+    int32_t* pred_d(int l) { return spec + (int)L.size() + l; }
+    int32_t* last_y(int l) { return spec + 2 * (int)L.size() + l; }
+    int32_t* last_d(int l) { return spec + 3 * (int)L.size() + l; }
     cudaStream_t side = nullptr;
     // [0] fork, [1] join, then per layer: propagated delta computed, requantised delta ready,
     // weight gradient computed
@@ -356,6 +366,15 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         m->split_ws_bytes = std::max(m->split_ws_bytes, need);
     }
     if (m->split_ws_bytes) ITO_TRY(m->alloc(&m->split_ws, m->split_ws_bytes / sizeof(int32_t)));
+    ITO_TRY(m->alloc(&m->spec, (size_t)6 * nl));
+    ITO_TRY(m->alloc(&m->spec_count, 2));
+    if (cudaMemset(m->spec, 0xff, sizeof(int32_t) * 4 * nl) != cudaSuccess)   // -1: no prediction yet
+        return set_error(ITO_ERR_CUDA, "memset");
+    static const int spec_env = [] {
+        const char* v = getenv("ITO_SPECULATE");
+        return v ? atoi(v) : 1;
+    }();
+    m->speculate = spec_env != 0;
 
     // contraction plans (tensor maps over the buffers above)
     for (int l = 0; l < nl; ++l) {
@@ -390,6 +409,30 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         // weight gradient: G[oc][k] = sum_m e[m][oc] in[m][k]
         ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax, m->split_ws,
                           m->split_ws_bytes, chunk));
+        // speculative requantisation in the epilogues of the forward contraction (its ReLU'd
+        // activation and bf16 copy) and of the delta propagation (the gated delta below); not
+        // with bit-packed masks, static requantisation, or shared (ping-pong) delta buffers
+        const bool plain = !m->opt.packed_masks && !m->opt.pingpong_grads;
+        if (plain && !conv && !L.static_q && L.ab)
+            ITO_TRY(gemm_plan_fuse_requant(&L.pf, m->pred_y(l), L.relu ? 1 : 0, nullptr, 0, L.a8, L.OC, L.ab,
+                                           L.lda));
+        if (plain && !conv && L.has_dgrad && !(l == m->n_conv && m->has_pool)) {
+            const MLayer& prev = m->L[l - 1];
+            if (prev.kind != ITO_LAYER_CONV3X3_RELU)
+                ITO_TRY(gemm_plan_fuse_requant(&L.pd, m->pred_d(l), 0, prev.relu ? prev.a8 : nullptr, L.IC, prev.e8,
+                                               L.IC, prev.eb, prev.lde));
+        }
+    }
+    {
+        // the slots whose contraction plan took the fused epilogue (a plan may decline it)
+        std::vector<int32_t> used(2 * nl, 0);
+        for (int l = 0; l < nl; ++l) {
+            used[l] = m->L[l].pf.rq_pred != nullptr;
+            used[nl + l] = m->L[l].pd.rq_pred != nullptr;
+        }
+        if (cudaMemcpy(m->spec + 4 * nl, used.data(), sizeof(int32_t) * 2 * nl, cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "memcpy");
     }
 
     // names of the stats entries
@@ -470,7 +513,8 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
         else
             ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
                        launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits, L.relu ? 1 : 0,
-                                      nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr, L.mask));
+                                      nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr, L.mask,
+                                      L.pf.rq_pred, m->last_y(l)));
         in8 = L.a8;
     }
     return ITO_OK;
@@ -531,7 +575,7 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
                 ITO_LAUNCH(m, r, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, true, prev.relu),
                            launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
                                           (prev.relu && !prev.mask) ? prev.a8 : nullptr, prev.e8, prev.eb, prev.lde,
-                                          m->sval(l, ST_DS), r, prev.mask, nullptr));
+                                          m->sval(l, ST_DS), r, prev.mask, nullptr, L.pd.rq_pred, m->last_d(l)));
             }
             if (r != s && cudaEventRecord(m->ev_delta(l), r) != cudaSuccess)
                 return set_error(ITO_ERR_CUDA, "stream ordering event failed");
@@ -656,6 +700,8 @@ int ito_model_tensor(const ito_model* m, const char* name, void** dev_ptr, int* 
     if (s == "p") return put(m->p32, 4, (int64_t)m->batch * m->pool_C);
     if (s == "pa") return put(m->pa8, 1, (int64_t)m->batch * m->pool_C);
     if (s == "pe") return put(m->pe8, 1, (int64_t)m->batch * m->pool_C);
+    if (s == "spec") return put(m->spec, 4, 6 * (int64_t)nl);
+    if (s == "spec_count") return put(m->spec_count, 8, 2);
     // per-layer tensors: a name prefix followed by the layer index
     size_t pos = 0;
     while (pos < s.size() && (s[pos] < '0' || s[pos] > '9')) ++pos;
@@ -750,6 +796,17 @@ int ito_model_profile_read(ito_model* m, double* ms, double* work, int64_t* laun
 
 int ito_model_kernels_per_step(const ito_model* m) { return m ? m->launches : 0; }
 
+int ito_model_set_speculation(ito_model* m, int enable)
+{
+    if (!m) return set_error(ITO_ERR_ARG, "NULL model");
+    if ((enable != 0) != m->speculate) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+        drop_graphs(m);   // captured steps encode the setting
+        m->speculate = enable != 0;
+    }
+    return ITO_OK;
+}
+
 int ito_model_set_overlap(ito_model* m, int mode)
 {
     if (!m || mode < 0 || mode > 2) return set_error(ITO_ERR_ARG, "bad model or overlap mode");
@@ -775,6 +832,10 @@ static int step_direct(ito_model* m, const int8_t* x, const int32_t* labels, cud
     m->launches = 0;
     cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * m->n_stats, s);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    // this step's shift predictions are the last step's shifts
+    const int nl = (int)m->L.size();
+    ITO_TRY(launch_roll_shift_predictions(m->spec, m->spec + 2 * nl, m->spec + 4 * nl, m->spec_count, 2 * nl,
+                                          m->speculate ? 1 : 0, s));
     ITO_TRY(model_forward(m, x, s));
     return model_backward(m, x, labels, s);
 }

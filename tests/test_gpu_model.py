@@ -105,3 +105,47 @@ def test_overlap_modes_give_identical_steps(index, pingpong):
         assert r.keys() == results[0].keys()
         for k in r:
             assert np.array_equal(np.asarray(r[k]), np.asarray(results[0][k])), (mode, k)
+
+
+@pytest.mark.parametrize("index,steps", [(0, 6), (1, 4), (5, 3), (3, 3)])
+def test_speculation_gives_identical_steps(index, steps):
+    """Speculative requantisation in the contraction epilogues changes no
+    result: with it on and off every tensor and statistic is the same after
+    each step. The predictions of step t are the shifts of step t-1 on the
+    slots whose contraction plan took the fused epilogue, and the model's
+    counters score each step's predictions at the start of the next."""
+    w = si.by_name(index)
+    runs = []
+    for on in (False, True):
+        g = GpuRun(w)
+        g.model.set_speculation(on)
+        runs.append(g)
+    nl = runs[0].n_layers
+    hits = misses = 0
+    for t in range(steps):
+        recs = []
+        for g in runs:
+            g.step(t)
+            recs.append(g.record())
+        assert recs[0].keys() == recs[1].keys()
+        for k in recs[0]:
+            assert np.array_equal(np.asarray(recs[0][k]), np.asarray(recs[1][k])), (t, k)
+        spec = runs[1].model.tensor("spec").cpu().numpy()
+        pred, last, used = spec[: 2 * nl], spec[2 * nl: 4 * nl], spec[4 * nl:]
+        off = runs[0].model.tensor("spec").cpu().numpy()
+        assert (off[: 2 * nl] == -1).all()
+        assert np.array_equal(off[2 * nl:], spec[2 * nl:]), t
+        assert (pred[used == 0] == -1).all()
+        # the counters hold the steps before this one
+        cnt = runs[1].model.tensor("spec_count").cpu().numpy()
+        assert (int(cnt[0]), int(cnt[1])) == (hits, misses), t
+        assert (runs[0].model.tensor("spec_count").cpu().numpy() == 0).all()
+        act = (used != 0) & (pred >= 0)
+        hits += int((pred[act] == last[act]).sum())
+        misses += int((pred[act] != last[act]).sum())
+        if t == 0:
+            assert not act.any()
+    if index in (1, 3, 5):
+        # the hidden layers' forward and delta-propagation contractions speculate
+        assert used.sum() > 0 and hits > 0
+    assert runs[0].ito.ito_get_error() == 0
