@@ -185,7 +185,7 @@ def oracle_step(w, weights, x, labels):
     return O.dfp16_step(weights, w.exp_w, x, w.exp_x, eta=w.eta, route="loops")
 
 
-def cpu_baseline(w, sample_batch):
+def cpu_baseline(w, sample_batch, min_seconds=10.0):
     """The CPU oracle (plain C loops, OpenMP over output rows) on one training
     step of `sample_batch` samples of workload w."""
     import numpy as np
@@ -194,13 +194,21 @@ def cpu_baseline(w, sample_batch):
     O.build()
     weights = si.make_weights(w)
     x, labels = si.make_batch(w, 0)
+    sample_batch = min(sample_batch, w.batch)
     x = np.ascontiguousarray(x[:sample_batch])
     labels = None if labels is None else np.ascontiguousarray(labels[:sample_batch])
+    # the same step repeated until about min_seconds of CPU work (the loops' cost does not
+    # depend on the values)
+    steps = 0
     t0 = time.perf_counter()
-    oracle_step(w, weights, x, labels)
-    dt = time.perf_counter() - t0
+    while True:
+        oracle_step(w, weights, x, labels)
+        steps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return sample_batch / dt, dt, cores
+    return steps * sample_batch / dt, dt, cores, steps, sample_batch
 
 
 def run_reference(args, w):
@@ -266,10 +274,10 @@ def run_ours(args, w):
     # context competes with the host cores
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, cores = cpu_baseline(w, args.cpu_batch)
+        v, dt, cores, nsteps, nsamp = cpu_baseline(w, args.cpu_batch)
         cpu = {"value": v, "unit": "samples/s", "cores": cores, "kind": "oracle",
-               "sample": "one oracle training step (C loops) on %d of the %d samples of %s, %.1f s"
-                         % (args.cpu_batch, w.batch, w.name, dt)}
+               "sample": "%d oracle training steps (C loops, OpenMP over output rows) on %d of the %d samples "
+                         "of %s, %.1f s" % (nsteps, nsamp, w.batch, w.name, dt)}
 
     if w.kind == "dfp16":
         return run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local)
@@ -279,8 +287,8 @@ def run_ours(args, w):
     for l, W in enumerate(si.make_weights(w)):
         model.set_weights(l, W, stream=stream)
     model.use_graphs(not args.no_graphs)
-    overlap_mode = int(os.environ.get("ITO_OVERLAP", "1"))
-    speculate = os.environ.get("ITO_SPECULATE", "1") != "0"
+    overlap_mode = model.overlap()
+    speculate = model.speculation()
     # NB distinct seeded batches resident in HBM; before each step (untimed) the step's batch
     # is copied into the model's fixed input buffers, which the captured step graph reads
     nb = NB_BATCHES
@@ -305,12 +313,8 @@ def run_ours(args, w):
     stream.synchronize()
     assert ito.ito_get_error() == 0
 
-    # per-kernel timing events (captured into the step graphs): re-capture, then read per step
-    model.profile(True)
-    for i in range(4):
-        step(i)
-    model.profile_read()
-    prof = {c: [0.0, 0.0, 0] for c in ("gemm", "requant", "update", "other")}
+    # the timed region: K steps, each after an untimed L2 flush and input copy, bracketed by
+    # CUDA events on the step's stream (no per-kernel events inside)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     clocks = Clocks(local)
@@ -326,21 +330,44 @@ def run_ours(args, w):
             starts[k].record(stream)
             model.train_step(xbuf, lbuf, stream=stream)
             ends[k].record(stream)
-            for c, (ms, work, n) in model.profile_read().items():
-                prof[c][0] += ms
-                prof[c][1] += work
-                prof[c][2] += n
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     spec1 = model.tensor("spec_count").cpu().tolist()
     total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    model.profile(False)
     err = ito.ito_get_error()
     if err != 0:
         raise RuntimeError("device error word %d after the timed steps" % err)
     total_ms = max_over_ranks(total_ms, dist)
     launches = model.kernels_per_step()
+
+    # per-kernel timing: the same K steps again with a pair of events around every launch,
+    # on the launch's own stream (captured into the step graphs as event-record nodes)
+    model.profile(True)
+    for i in range(4):
+        step(i)
+    model.profile_read()
+    prof = {c: [0.0, 0.0, 0] for c in ("gemm", "requant", "update", "other")}
+    pstarts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    pends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            flush.fill_(k & 0xFF)
+            xbuf.copy_(xs[k % nb])
+            lbuf.copy_(ls[k % nb])
+            pstarts[k].record(stream)
+            model.train_step(xbuf, lbuf, stream=stream)
+            pends[k].record(stream)
+            for c, (ms, work, n) in model.profile_read().items():
+                prof[c][0] += ms
+                prof[c][1] += work
+                prof[c][2] += n
+    torch.cuda.synchronize()
+    prof_ms = sum(s.elapsed_time(e) for s, e in zip(pstarts, pends))
+    model.profile(False)
+    if ito.ito_get_error() != 0:
+        raise RuntimeError("device error word set after the profiled steps")
 
     # end to end through the host-buffer entry point: each step copies its own
     # input batch (two alternating pinned batches) in and its stats out
@@ -411,23 +438,31 @@ def run_ours(args, w):
                    "l2": "flushed by a 256 MB write before every timed step; flush not timed",
                    "graphs": not args.no_graphs,
                    "backward_overlap": OVERLAP_MODES[overlap_mode],
-                   "speculative_requantisation": ("contraction epilogues requantise with the previous step's shift; "
-                                                  "the pass rewrites the outputs when this step's shift differs; "
-                                                  "%d of %d predictions held (the model's counters over the "
-                                                  "timed region)" % (spec_hits, spec_hits + spec_misses))
+                   "speculative_requantisation": ("forward and delta-propagation epilogues requantise with the "
+                                                  "previous step's shift and write no int32 result; a one-word "
+                                                  "check per contraction, and a re-launch of the contraction when "
+                                                  "this step's shift differs; %d of %d predictions held (the "
+                                                  "model's counters over the timed region)"
+                                                  % (spec_hits, spec_hits + spec_misses))
                                                  if speculate else "off",
                    "inputs": "%d seeded batches resident in HBM, each step's copied into the model's input "
                              "buffers before the step (not timed)" % nb,
                    "parallelism": "replicas" if world > 1 else "single"},
         "int_tops": algorithmic_ops(w) * world * K / (total_ms / 1000.0) / 1e12,
-        "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (bf16-embedded int8 contractions, all GEMM launches)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "k_gemm_tc2 / k_gemm_tc (bf16-embedded int8 contractions, every contraction launch "
+                               "of the step; re-launches after a misprediction are not counted as contractions)",
                      "achieved": g_tflops, "peak": peak, "unit": "TFLOP/s", "frac": g_tflops / peak,
                      "peak_source": "bf16_tflops_sustained, %s" % pk_src,
                      "traffic": gemm_traffic_per_launch(w), "traffic_unit": "bytes per launch (ncu, committed summary)",
-                     "launches_timed": g_n},
-        "passes": {"note": "kernel time per step by class over the timed steps (overlapped, speculative: a "
-                           "requantisation pass whose predicted shift held returns at once, its work done in the "
-                           "contraction epilogue); per-pass bandwidth is under 'isolated'",
+                     "launches_timed": g_n,
+                     "measured_over": "the same %d steps run again with an event pair around every launch on its "
+                                      "own stream (%.4f ms per step with the events, %.4f without)"
+                                      % (K, prof_ms / K, total_ms / K)},
+        "passes": {"note": "kernel time per step by class over the profiled steps (overlapped launches include "
+                           "their wait for SM resources; speculating contractions leave the requantisation class "
+                           "a one-word check and a re-launch that returns at once when the prediction held); "
+                           "per-pass bandwidth is under 'isolated'",
                    "hbm_peak_gbs": hbm, "peak_source": pk_src,
                    "ms_per_step": {k: v[0] / K for k, v in prof.items()}},
         "isolated": {"note": "the step on one stream (no bandwidth pass beside a contraction) and without "

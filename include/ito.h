@@ -343,10 +343,12 @@ int ito_model_get_weights(const ito_model *m, int layer, int8_t *W, int on_host,
  * "m0" its bit-packed ReLU mask (packed_masks models),
  * "e0" int8 delta at the output of layer 0, "d1" int32 delta-propagation
  * contraction of layer 1, "g0" int32 weight gradient, "w0" int8 weights,
- * "stats" int32 scalars; see ito_model_stat_index; "spec" int32 [6 * layers]:
+ * "stats" int32 scalars; see ito_model_stat_index; "spec" int32 [8 * layers]:
  * the forward and delta-propagation shift predictions the step used, the
- * shifts the step computed, and 1 where the contraction's epilogue speculates,
- * each block of 2 * layers indexed by weight layer, -1 where none; "spec_count"
+ * shifts the step computed, 1 where the contraction's epilogue speculates, and
+ * the re-launch words (0: the prediction held or none was made, else the
+ * step's shift + 1), each block of 2 * layers indexed by weight layer, -1 in
+ * the first two where none; "spec_count"
  * int64 [2]: predictions that held and that missed since creation, scored at
  * the start of the following step (see ito_model_set_speculation)). Writes the device
  * pointer, the element type (1 = int8, 2 = int16, 4 = int32, 8 = int64) and
@@ -398,29 +400,43 @@ int ito_model_use_graphs(ito_model *m, int enable);
 
 /* Stream layout of the backward pass (the results are the same in every mode):
  *   0: every launch on the caller's stream;
- *   1 (default): the requantisation of each propagated delta and the weight and
- *      offset updates run on a second, model-owned stream beside the next
- *      contractions (a bandwidth-bound pass shares the SMs with a tensor-core one);
+ *   1: the requantisation of each propagated delta and the weight and offset
+ *      updates run on a second, model-owned stream beside the next contractions
+ *      (a bandwidth-bound pass shares the SMs with a tensor-core one);
  *   2: only the weight updates run on the second stream.
  * Events order every read after its write; the step ends joined on the caller's
  * stream. Changing the mode synchronises the device and drops captured graphs.
- * The environment variable ITO_OVERLAP sets the mode of new models.
- * Errors: ITO_ERR_ARG (NULL model, mode outside 0..2). */
+ * The environment variable ITO_OVERLAP sets the mode of new models; without it
+ * a new model takes mode 1, or mode 0 when every delta propagation requantises
+ * speculatively (see ito_model_set_speculation), since the second stream would
+ * then hold only the updates. Errors: ITO_ERR_ARG (NULL model, mode outside 0..2). */
 int ito_model_set_overlap(ito_model *m, int mode);
+
+/* Writes the model's current backward stream layout (0, 1 or 2) to *mode.
+ * Errors: ITO_ERR_ARG (NULL argument). */
+int ito_model_get_overlap(const ito_model *m, int *mode);
 
 /* Speculative requantisation (default on; the environment variable
  * ITO_SPECULATE=0 turns it off for new models). NITI's shift of a tensor
  * depends on the whole tensor's max, so requantisation is a second pass over
  * the int32 result. With speculation on, the epilogue of the forward and
  * delta-propagation contractions (CTA-pair kernel; int8 row length a multiple
- * of 16; no packed masks, static requantisation or ping-pong buffers) also
- * writes the requantised int8 tensor and its bf16 copy using the shift the
- * same tensor had in the previous step; the requantisation pass then computes
- * this step's shift from the max and returns at once when it is the same, and
- * otherwise rewrites both outputs. The result is NITI's in either case (the
- * int32 tensor and its max are still written). Changing the setting
- * synchronises the device and drops captured graphs. Errors: ITO_ERR_ARG. */
+ * of 16; no packed masks, static requantisation or ping-pong buffers) writes
+ * the requantised int8 tensor and its bf16 copy using the shift the same
+ * tensor had in the previous step, and folds the max, but writes no int32
+ * result. A one-word check then computes this step's shift from the max; when
+ * it differs, a second launch of the same contraction recomputes the outputs
+ * with it (that launch returns at once when the prediction held). The int8,
+ * bf16 and scalar results are NITI's in either case; the int32 tensors "y<l>"
+ * and "d<l>" of those contractions are not written while speculation is on
+ * (the step with no prediction yet, the first, still writes them). Changing
+ * the setting synchronises the device and drops captured graphs.
+ * Errors: ITO_ERR_ARG. */
 int ito_model_set_speculation(ito_model *m, int enable);
+
+/* Writes 1 to *enabled when speculative requantisation is on for this model,
+ * else 0. Errors: ITO_ERR_ARG (NULL argument). */
+int ito_model_get_speculation(const ito_model *m, int *enabled);
 
 /* The same step from HOST buffers: copies x and labels into the model's
  * device buffers, runs the step, copies the stats array (ito_model_num_stats

@@ -103,6 +103,8 @@ _SIGS = {
     "ito_model_use_graphs": (_I, [_P, _I]),
     "ito_model_set_overlap": (_I, [_P, _I]),
     "ito_model_set_speculation": (_I, [_P, _I]),
+    "ito_model_get_speculation": (_I, [_P, _P]),
+    "ito_model_get_overlap": (_I, [_P, _P]),
     "ito_model_set_static_requant": (_I, [_P, _I, _P, _P, _P, _I, _P]),
     "ito_model_profile": (_I, [_P, _I]),
     "ito_model_profile_read": (_I, [_P, _P, _P, _P]),
@@ -468,6 +470,16 @@ class Model:
     def set_speculation(self, enable=True):
         """speculative requantisation in the contraction epilogues (exact; see include/ito.h)"""
         _check(_lib.ito_model_set_speculation(self._h, int(bool(enable))))
+
+    def overlap(self) -> int:
+        mode = ctypes.c_int()
+        _check(_lib.ito_model_get_overlap(self._h, ctypes.byref(mode)))
+        return mode.value
+
+    def speculation(self) -> bool:
+        on = ctypes.c_int()
+        _check(_lib.ito_model_get_speculation(self._h, ctypes.byref(on)))
+        return on.value == 1
 
     def use_graphs(self, enable=True):
         _check(_lib.ito_model_use_graphs(self._h, int(enable)))

@@ -74,6 +74,13 @@ __device__ __forceinline__ uint16_t int_to_bf16_bits(int32_t v)
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// Two small integers (|v| <= 256, exact in bf16) as one bf16x2 word, lo in the low half.
+__device__ __forceinline__ uint32_t int_pair_to_bf16x2(int32_t lo, int32_t hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn((float)lo, (float)hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
 // ------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)

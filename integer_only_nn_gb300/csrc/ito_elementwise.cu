@@ -133,22 +133,26 @@ __device__ __forceinline__ int32_t requant_one(int32_t y, int s, int relu, int g
 // row (cols / 8 bytes per row; bit j is element j of the group): mask_out
 // receives (q > 0) of the result, gate_bits replaces the int8 gate.
 // s_pred (optional): the shift a speculative requantisation in the contraction's
-// epilogue used; when it equals this launch's shift, out8 and outb already hold
-// the result and the kernel returns at once. s_last (optional) receives the shift
-// (the next step's prediction).
+// epilogue used (< 0: none this step). When it is >= 0 the contraction wrote no
+// int32 result: the kernel only records the shift, sets *redo to 0 when the
+// prediction held (out8 and outb hold the result) or to shift + 1 when it did not
+// (the contraction's re-launch rewrites them), and returns. s_last (optional)
+// receives the shift (the next step's prediction).
 __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
                              const uint32_t* __restrict__ d_max, int target_bits, int relu,
                              const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
                              int64_t ldb, int32_t* __restrict__ d_shift, const uint8_t* __restrict__ gate_bits,
                              uint8_t* __restrict__ mask_out, const int32_t* __restrict__ s_pred,
-                             int32_t* __restrict__ s_last)
+                             int32_t* __restrict__ s_last, int32_t* __restrict__ redo)
 {
     const int s = shift_for(*d_max, target_bits);
+    const int sp = s_pred ? *s_pred : -1;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (d_shift) *d_shift = s;
         if (s_last) *s_last = s;
+        if (redo) *redo = (sp >= 0 && sp != s) ? s + 1 : 0;
     }
-    if (s_pred && *s_pred == s) return;
+    if (sp >= 0) return;
     const int64_t groups = rows * (cols >> 3);
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
@@ -187,14 +191,16 @@ __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t
                             const uint32_t* __restrict__ d_max, int target_bits, int relu,
                             const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
                             int64_t ldb, int32_t* __restrict__ d_shift, const int32_t* __restrict__ s_pred,
-                            int32_t* __restrict__ s_last)
+                            int32_t* __restrict__ s_last, int32_t* __restrict__ redo)
 {
     const int s = shift_for(*d_max, target_bits);
+    const int sp = s_pred ? *s_pred : -1;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (d_shift) *d_shift = s;
         if (s_last) *s_last = s;
+        if (redo) *redo = (sp >= 0 && sp != s) ? s + 1 : 0;
     }
-    if (s_pred && *s_pred == s) return;
+    if (sp >= 0) return;
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int32_t q = requant_one(Y[i], s, relu, gate ? gate[i] > 0 : 1);
@@ -208,7 +214,8 @@ __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t
 
 int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
                    const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
-                   const uint8_t* gate_bits, uint8_t* mask_out, const int32_t* s_pred, int32_t* s_last)
+                   const uint8_t* gate_bits, uint8_t* mask_out, const int32_t* s_pred, int32_t* s_last,
+                   int32_t* redo)
 {
     if (s_pred && (gate_bits || mask_out))
         return set_error(ITO_ERR_UNSUPPORTED, "speculative requantisation with bit-packed masks");
@@ -220,11 +227,11 @@ int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t*
     if (vec)
         k_requant_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(
             Y, rows, cols, d_max, target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out, s_pred,
-            s_last);
+            s_last, redo);
     else
         k_requant_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(Y, rows, cols, d_max, target_bits, relu,
                                                                           gate, out8, outb, ldb, d_shift, s_pred,
-                                                                          s_last);
+                                                                          s_last, redo);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "requant launch: %s", cudaGetErrorString(e));
 }

@@ -330,16 +330,22 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
 // Exactness and the epilogue are as in k_gemm_tc; both CTAs' epilogue warps
 // release an accumulator buffer on the leader's barrier.
 
-// Speculative requantisation in the pair kernel's epilogue (FusedRq.pred set):
-// with the shift the same tensor had in the previous step, the epilogue also
-// writes q = sat8(rhu(y, s)) (ReLU'd, or zeroed where gate <= 0) as int8 and as
-// bf16. The requantisation kernel that follows computes the true shift from
-// this launch's max and rewrites both outputs only when it differs.
+// Speculative requantisation in the pair kernel's epilogue (FusedRq.pred set).
+// When *pred >= 0 (the shift the same tensor had in the previous step), the
+// epilogue writes q = sat8(rhu(y, *pred)) (ReLU'd, or zeroed where gate <= 0) as
+// int8 and as bf16 and does not write the int32 result; it still folds max|y|
+// into d_max. The check that follows (k_requant_v8 with s_pred) computes the true
+// shift s from the max and leaves *redo = 0 when s == *pred, else *redo = s + 1.
+// A second launch of the same plan with FusedRq.redo set then returns at once
+// when *redo == 0, and otherwise recomputes the contraction and writes q with
+// shift *redo - 1 (no int32 result, no max). When *pred < 0 (no prediction) the
+// first launch writes the int32 result and the requantisation pass runs in full.
 struct FusedRq {
     const int32_t* pred;   // predicted shift (device word; < 0: none this step); nullptr: off
     const int8_t* gate;    // [M][ldg] int8 ReLU gate, or nullptr
     int64_t ldg;
     int relu;
+    const int32_t* redo;   // the re-launch: 0 = nothing to do, else shift + 1; nullptr: first launch
 };
 
 struct Tc2Cfg {
@@ -370,6 +376,17 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;
     constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+
+    // the shift of a speculative requantisation (< 0: none); a re-launch whose first
+    // launch's prediction held returns here, in every CTA alike (one device word)
+    int sp = -1;
+    if (fz.redo) {
+        const int r = *fz.redo;
+        if (r <= 0) return;
+        sp = r - 1;
+    } else if (fz.pred) {
+        sp = *fz.pred;
+    }
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -496,11 +513,6 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
         const int half = e >> 2;
         uint8_t* stg = staging + e * 4096;
         const uint32_t stg_row = smem_u32(stg) + lane * 128;
-        // speculative requantisation this launch: the predicted shift (< 0: none). The int32
-        // result then goes to L2 marked evict-first (only a misprediction reads it back) and
-        // so does the int8 copy (read in a later pass); the bf16 copy, the next contraction's
-        // operand, is stored with the default policy.
-        const int sp = fz.pred ? *fz.pred : -1;
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
@@ -583,33 +595,77 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
                 }
                 continue;
             }
-            uint32_t mx = 0;
+            if (!fz.redo) {
+                uint32_t mx = 0;
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) mx = max(mx, abs_u32(acc[i]));
-            mx = __reduce_max_sync(0xffffffffu, mx);
-            if (lane == 0 && mx != 0) atomicMax(d_max, mx);
-            if (use_tma_store) {
-                // speculative requantisation: the gate's open (> 0) bits of this lane's row, read
-                // from the staged tile before the staging buffer is reused
-                uint32_t open[HALF / 32];
-#pragma unroll
-                for (int k = 0; k < HALF / 32; ++k) open[k] = 0xffffffffu;
-                if (fused && fz.gate) {
-#pragma unroll
-                    for (int j = 0; j < HALF / 16; ++j) {
-                        const uint4 gv = ld_shared_v4(stg_row + ((j ^ (lane & 7)) << 4));
-                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                        uint32_t bits = 0;
-#pragma unroll
-                        for (int b = 0; b < 16; ++b) bits |= ((int8_t)(gw[b >> 2] >> (8 * (b & 3))) > 0 ? 1u : 0u) << b;
-                        if (j & 1)
-                            open[j >> 1] = (open[j >> 1] & 0xffffu) | (bits << 16);
-                        else
-                            open[j >> 1] = bits;
-                    }
+                for (int i = 0; i < HALF; ++i) mx = max(mx, abs_u32(acc[i]));
+                mx = __reduce_max_sync(0xffffffffu, mx);
+                if (lane == 0 && mx != 0) atomicMax(d_max, mx);
+            }
+            if (fused) {
+                // speculative requantisation: q = sat8(rhu(y, sp)), ReLU'd or zeroed where the
+                // gate is closed, written over the staged gate tile (each lane reads and
+                // rewrites only its own row's 16-byte chunks), then stored as one 32 x 128 int8
+                // box and two 32 x 64 bf16 boxes; no int32 result
+                if (!fz.gate) {
+                    if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                 }
-                // the int32 result (evict-first in L2 when speculating: only a misprediction reads it)
+                uint32_t q8w[HALF / 4];      // the 128 int8 results, packed four to a word
+#pragma unroll
+                for (int j = 0; j < HALF / 16; ++j) {
+                    const uint32_t saddr = stg_row + ((j ^ (lane & 7)) << 4);
+                    uint4 gv = make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u);
+                    if (fz.gate) gv = ld_shared_v4(saddr);
+                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t packed = 0;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            int32_t q = sat8(rhu32(acc[j * 16 + 4 * k + b], sp));
+                            if (fz.relu) q = max(q, 0);
+                            if ((int8_t)(gw[k] >> (8 * b)) <= 0) q = 0;
+                            packed |= ((uint32_t)q & 0xffu) << (8 * b);
+                        }
+                        q8w[4 * j + k] = packed;
+                    }
+                    st_shared_v4(saddr, (int32_t)q8w[4 * j], (int32_t)q8w[4 * j + 1], (int32_t)q8w[4 * j + 2],
+                                 (int32_t)q8w[4 * j + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmO8, stg, col0, row0);
+                    bulk_commit();
+                }
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    if (col0 + g * 64 >= N) continue;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const int i = g * 64 + j * 8 + 2 * h;
+                            const int8_t lo = (int8_t)(q8w[i >> 2] >> (8 * (i & 3)));
+                            const int8_t hi = (int8_t)(q8w[(i + 1) >> 2] >> (8 * ((i + 1) & 3)));
+                            wv[h] = int_pair_to_bf16x2(lo, hi);
+                        }
+                        st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), (int32_t)wv[0], (int32_t)wv[1],
+                                     (int32_t)wv[2], (int32_t)wv[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmOB, stg, col0 + g * 64, row0);
+                        bulk_commit();
+                    }
+                }
+            } else if (use_tma_store) {
+                // the int32 result through the staging buffer, 32 x 32 boxes
 #pragma unroll
                 for (int g = 0; g < HALF / 32; ++g) {
                     if (row0 >= M || col0 + g * 32 >= N) continue;
@@ -622,66 +678,8 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (fused)
-                            tma_store_2d_hint(&tmC, stg, col0 + g * 32, row0, l2_policy_evict_first());
-                        else
-                            tma_store_2d(&tmC, stg, col0 + g * 32, row0);
+                        tma_store_2d(&tmC, stg, col0 + g * 32, row0);
                         bulk_commit();
-                    }
-                }
-                if (fused) {
-                    // q = sat8(rhu(y, sp)), ReLU'd or zeroed where the gate is closed, as one
-                    // 32 x 128 int8 box (evict-first: a later pass reads it) and two 32 x 64 bf16
-                    // boxes (the next contraction's operand)
-                    uint32_t q8w[HALF / 4];      // the 128 int8 results, packed four to a word
-#pragma unroll
-                    for (int k = 0; k < HALF / 4; ++k) {
-                        uint32_t packed = 0;
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            const int i = 4 * k + b;
-                            int32_t q = sat8(rhu32(acc[i], sp));
-                            if ((fz.relu && q < 0) || !((open[i >> 5] >> (i & 31)) & 1u)) q = 0;
-                            packed |= ((uint32_t)(uint8_t)(int8_t)q) << (8 * b);
-                        }
-                        q8w[k] = packed;
-                    }
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), (int32_t)q8w[4 * j], (int32_t)q8w[4 * j + 1],
-                                     (int32_t)q8w[4 * j + 2], (int32_t)q8w[4 * j + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d_hint(&tmO8, stg, col0, row0, l2_policy_evict_first());
-                        bulk_commit();
-                    }
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        if (col0 + g * 64 >= N) continue;
-                        if (lane == 0) bulk_wait_read_all();
-                        __syncwarp();
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            uint32_t wv[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const int i = g * 64 + j * 8 + 2 * h;
-                                const int8_t lo = (int8_t)(q8w[i >> 2] >> (8 * (i & 3)));
-                                const int8_t hi = (int8_t)(q8w[(i + 1) >> 2] >> (8 * ((i + 1) & 3)));
-                                wv[h] = (uint32_t)int_to_bf16_bits(lo) | ((uint32_t)int_to_bf16_bits(hi) << 16);
-                            }
-                            st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), (int32_t)wv[0], (int32_t)wv[1],
-                                         (int32_t)wv[2], (int32_t)wv[3]);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmOB, stg, col0 + g * 64, row0);
-                            bulk_commit();
-                        }
                     }
                 }
             } else {
@@ -1010,7 +1008,7 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const FusedRq fz{p.rq_pred, p.rq_gate, p.rq_ldg, p.rq_relu};
+    const FusedRq fz{p.rq_pred, p.rq_gate, p.rq_ldg, p.rq_relu, p.rq_redo};
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.mapP, p.mapO8, p.mapOB, fz,
                                        p.use_tma_store, p.M, p.N, p.K, p.chunk_kb, p.group, p.tail_full, p.tail_parts,
                                        p.C, p.ldc, p.d_max, p.err);

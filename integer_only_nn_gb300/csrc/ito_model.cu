@@ -61,6 +61,7 @@ struct MLayer {
     bool static_q = false;      // static per-channel requantisation with trained INT32 offsets
     int32_t *off32 = nullptr, *mult32 = nullptr, *k32 = nullptr, *og32 = nullptr;   // [OC] (Linear layers)
     GemmPlan pf{}, pd{}, pg{};
+    GemmPlan pf_redo{}, pd_redo{};   // re-launches of pf / pd after a shift misprediction
     bool has_dgrad = false;
     bool relu = false;
 };
@@ -115,7 +116,8 @@ struct ito_model {
     int overlap = 1;                    // 0: one stream; 1: requantisation and updates overlap; 2: updates only
     // speculative requantisation: [0, nl) forward and [nl, 2nl) delta-propagation shift predictions,
     // then the shifts of the last step in the same order, then 1 where the contraction's epilogue
-    // speculates (its plan is fused); spec_count: predictions that held, that missed (int64)
+    // speculates (its plan is fused), then the re-launch words (0: the prediction held, else the
+    // shift + 1); spec_count: predictions that held, that missed (int64)
     bool speculate = true;
     int32_t* spec = nullptr;
     int64_t* spec_count = nullptr;
@@ -123,6 +125,8 @@ struct ito_model {
     int32_t* pred_d(int l) { return spec + (int)L.size() + l; }
     int32_t* last_y(int l) { return spec + 2 * (int)L.size() + l; }
     int32_t* last_d(int l) { return spec + 3 * (int)L.size() + l; }
+    int32_t* redo_y(int l) { return spec + 6 * (int)L.size() + l; }
+    int32_t* redo_d(int l) { return spec + 7 * (int)L.size() + l; }
     cudaStream_t side = nullptr;
     // [0] fork, [1] join, then per layer: propagated delta computed, requantised delta ready,
     // weight gradient computed
@@ -366,7 +370,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         m->split_ws_bytes = std::max(m->split_ws_bytes, need);
     }
     if (m->split_ws_bytes) ITO_TRY(m->alloc(&m->split_ws, m->split_ws_bytes / sizeof(int32_t)));
-    ITO_TRY(m->alloc(&m->spec, (size_t)6 * nl));
+    ITO_TRY(m->alloc(&m->spec, (size_t)8 * nl));
     ITO_TRY(m->alloc(&m->spec_count, 2));
     if (cudaMemset(m->spec, 0xff, sizeof(int32_t) * 4 * nl) != cudaSuccess)   // -1: no prediction yet
         return set_error(ITO_ERR_CUDA, "memset");
@@ -423,6 +427,17 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
                                                L.IC, prev.eb, prev.lde));
         }
     }
+    for (auto& L : m->L) {
+        // the re-launches: the same plans, reading their re-launch word
+        if (L.pf.rq_pred) {
+            L.pf_redo = L.pf;
+            L.pf_redo.rq_redo = m->redo_y((int)(&L - m->L.data()));
+        }
+        if (L.pd.rq_pred) {
+            L.pd_redo = L.pd;
+            L.pd_redo.rq_redo = m->redo_d((int)(&L - m->L.data()));
+        }
+    }
     {
         // the slots whose contraction plan took the fused epilogue (a plan may decline it)
         std::vector<int32_t> used(2 * nl, 0);
@@ -444,13 +459,22 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
     m->stat_names.push_back({"pmax", nl * ST_PER_LAYER});
     m->stat_names.push_back({"ps", nl * ST_PER_LAYER + 1});
 
-    // second stream and ordering events of the backward overlap; ITO_OVERLAP=0 in the
-    // environment keeps every launch on the caller's stream
+    // second stream and ordering events of the backward overlap. ITO_OVERLAP in the
+    // environment sets the mode; without it the mode is 1 unless every delta propagation
+    // speculates: then the second stream would hold only the weight updates, which slow the
+    // contractions beside them by more than they take alone, and the mode is 0
     static const int overlap_env = [] {
         const char* v = getenv("ITO_OVERLAP");
-        return v ? atoi(v) : 1;
+        return v ? atoi(v) : -1;
     }();
-    m->overlap = overlap_env >= 0 && overlap_env <= 2 ? overlap_env : 1;
+    if (overlap_env >= 0 && overlap_env <= 2) {
+        m->overlap = overlap_env;
+    } else {
+        bool every_delta_speculates = m->speculate;
+        for (const MLayer& L : m->L)
+            if (L.has_dgrad && !L.pd.rq_pred) every_delta_speculates = false;
+        m->overlap = every_delta_speculates ? 0 : 1;
+    }
     if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess)
         return set_error(ITO_ERR_CUDA, "side stream creation failed");
     for (int i = 0; i < 2 + 3 * nl; ++i) {
@@ -510,11 +534,17 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
             ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
                        launch_requant_static(L.y32, L.rows_out, L.OC, L.off32, L.mult32, L.k32, L.relu ? 1 : 0, L.a8,
                                              L.ab, L.lda, L.mask, s));
-        else
-            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
+        else {
+            // speculating, this is the check of the prediction (the epilogue wrote the
+            // outputs, no int32 result), then the contraction's re-launch, which returns at
+            // once when the prediction held
+            const bool spec = m->speculate && L.pf.rq_pred;
+            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, spec ? 0.0 : requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
                        launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits, L.relu ? 1 : 0,
                                       nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr, L.mask,
-                                      L.pf.rq_pred, m->last_y(l)));
+                                      L.pf.rq_pred, m->last_y(l), spec ? m->redo_y(l) : nullptr));
+            if (spec) ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pf_redo, s));
+        }
         in8 = L.a8;
     }
     return ITO_OK;
@@ -533,9 +563,9 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
     const int B = m->batch;
     const int nl = (int)m->L.size();
     const ito_niti_params p = m->p;
-    // b: the update stream; r: the stream of the delta requantisation
+    // b: the update stream; r_side: the stream of the delta requantisation
     cudaStream_t b = m->overlap ? m->side : s;
-    cudaStream_t r = m->overlap == 1 ? m->side : s;
+    cudaStream_t r_side = m->overlap == 1 ? m->side : s;
     auto sync = [&](cudaEvent_t e, cudaStream_t from, cudaStream_t to) -> int {
         if (from == to) return ITO_OK;
         if (cudaEventRecord(e, from) != cudaSuccess || cudaStreamWaitEvent(to, e, 0) != cudaSuccess)
@@ -546,14 +576,20 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
     ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * top.OC + 4.0 * B,
                launch_top_error(top.a8, labels, B, top.OC, m->target_mag, top.e8, top.eb, top.lde, s));
     ITO_TRY(sync(m->ev_fork(), s, b));
+    bool delta_on_side = false;   // the layer above requantised this layer's delta on the side stream
     for (int l = nl - 1; l >= m->opt.trainable_from; --l) {
         MLayer& L = m->L[l];
         const bool conv = L.kind == ITO_LAYER_CONV3X3_RELU;
-        // this layer's delta (produced on b by the layer above) before its contractions
-        if (l < nl - 1 && r != s && cudaStreamWaitEvent(s, m->ev_delta(l + 1), 0) != cudaSuccess)
+        // this layer's delta (produced on the side stream by the layer above) before its contractions
+        if (delta_on_side && cudaStreamWaitEvent(s, m->ev_delta(l + 1), 0) != cudaSuccess)
             return set_error(ITO_ERR_CUDA, "stream ordering event failed");
+        delta_on_side = false;
         if (L.has_dgrad) {
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
+            // a speculating delta propagation checks its prediction and re-launches on s: both
+            // return at once when the prediction held
+            const bool spec = m->speculate && L.pd.rq_pred;
+            const cudaStream_t r = spec ? s : r_side;
             ITO_TRY(sync(m->ev_dgrad(l), s, r));   // the propagated delta is complete
             MLayer& prev = m->L[l - 1];
             if (conv) {
@@ -572,13 +608,18 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
                 ITO_LAUNCH(m, r, ITO_PROF_OTHER, 4.0 * B * m->pool_HW * m->pool_C,
                            launch_gap_bwd(m->pe8, prev.a8, B, m->pool_HW, m->pool_C, prev.e8, prev.eb, r));
             } else {
-                ITO_LAUNCH(m, r, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, true, prev.relu),
+                ITO_LAUNCH(m, r, ITO_PROF_REQUANT, spec ? 0.0 : requant_bytes((int64_t)B * L.IC, true, prev.relu),
                            launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
                                           (prev.relu && !prev.mask) ? prev.a8 : nullptr, prev.e8, prev.eb, prev.lde,
-                                          m->sval(l, ST_DS), r, prev.mask, nullptr, L.pd.rq_pred, m->last_d(l)));
+                                          m->sval(l, ST_DS), r, prev.mask, nullptr, L.pd.rq_pred, m->last_d(l),
+                                          spec ? m->redo_d(l) : nullptr));
+                if (spec) ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pd_redo, s));
             }
-            if (r != s && cudaEventRecord(m->ev_delta(l), r) != cudaSuccess)
-                return set_error(ITO_ERR_CUDA, "stream ordering event failed");
+            if (r != s) {
+                if (cudaEventRecord(m->ev_delta(l), r) != cudaSuccess)
+                    return set_error(ITO_ERR_CUDA, "stream ordering event failed");
+                delta_on_side = true;
+            }
         }
         ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
         ITO_TRY(sync(m->ev_wgrad(l), s, b));       // the weight gradient is complete
@@ -590,10 +631,10 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
         // the offsets' gradient reads this layer's delta, whose (ping-pong) buffer the next
         // requantisation overwrites: it runs on the requantisation stream, before that one
         if (L.static_q)
-            ITO_LAUNCH(m, r, ITO_PROF_UPDATE, (double)L.rows_out * L.OC + 12.0 * L.OC,
+            ITO_LAUNCH(m, r_side, ITO_PROF_UPDATE, (double)L.rows_out * L.OC + 12.0 * L.OC,
                        launch_offset_grad_update(L.e8, L.rows_out, L.OC, L.og32, m->umax(l, ST_OGMAX), L.off32,
                                                  p.target_bits, p.mu_weight, m->sval(l, ST_OGS), m->sval(l, ST_OWS),
-                                                 reinterpret_cast<uint32_t*>(m->sval(l, ST_ONZ)), r));
+                                                 reinterpret_cast<uint32_t*>(m->sval(l, ST_ONZ)), r_side));
     }
     ITO_TRY(sync(m->ev_join(), b, s));
     (void)x;
@@ -700,7 +741,7 @@ int ito_model_tensor(const ito_model* m, const char* name, void** dev_ptr, int* 
     if (s == "p") return put(m->p32, 4, (int64_t)m->batch * m->pool_C);
     if (s == "pa") return put(m->pa8, 1, (int64_t)m->batch * m->pool_C);
     if (s == "pe") return put(m->pe8, 1, (int64_t)m->batch * m->pool_C);
-    if (s == "spec") return put(m->spec, 4, 6 * (int64_t)nl);
+    if (s == "spec") return put(m->spec, 4, 8 * (int64_t)nl);
     if (s == "spec_count") return put(m->spec_count, 8, 2);
     // per-layer tensors: a name prefix followed by the layer index
     size_t pos = 0;
@@ -804,6 +845,20 @@ int ito_model_set_speculation(ito_model* m, int enable)
         drop_graphs(m);   // captured steps encode the setting
         m->speculate = enable != 0;
     }
+    return ITO_OK;
+}
+
+int ito_model_get_speculation(const ito_model* m, int* enabled)
+{
+    if (!m || !enabled) return set_error(ITO_ERR_ARG, "NULL argument");
+    *enabled = m->speculate ? 1 : 0;
+    return ITO_OK;
+}
+
+int ito_model_get_overlap(const ito_model* m, int* mode)
+{
+    if (!m || !mode) return set_error(ITO_ERR_ARG, "NULL argument");
+    *mode = m->overlap;
     return ITO_OK;
 }
 

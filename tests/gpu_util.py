@@ -64,11 +64,24 @@ class GpuRun:
         self.torch.cuda.synchronize()
         return x, labels
 
+    def unwritten_int32(self):
+        """The int32 contraction results the model does not write: with
+        speculative requantisation on, those of the contractions whose epilogue
+        requantises ("y<l>" forward, "d<l>" delta propagation)."""
+        if not self.model.speculation():
+            return set()
+        nl = self.n_layers
+        used = self.model.tensor("spec").cpu().numpy()[4 * nl: 6 * nl]
+        return {"y%d" % l for l in range(nl) if used[l]} | {"d%d" % l for l in range(nl) if used[nl + l]}
+
     def names(self, kinds=("y", "a", "e", "d", "g", "w")):
         out = []
         first = self.w.trainable_from
+        skip = self.unwritten_int32()
         for l in range(self.n_layers):
             for k in kinds:
+                if "%s%d" % (k, l) in skip:
+                    continue
                 if k == "d" and l <= first:
                     continue
                 if k in ("e", "g") and l < first:

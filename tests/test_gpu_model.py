@@ -22,11 +22,17 @@ def _oracle_step(w, weights, t, route):
     return O.cnn_step(weights, x, labels, w.convs)
 
 
-@pytest.mark.parametrize("index,steps,route", [(0, 100, "loops"), (1, 3, "loops"), (2, 2, "loops"),
-                                               (3, 1, "f64")])
-def test_model_lockstep_live(index, steps, route):
+@pytest.mark.parametrize("index,steps,route,speculate", [(0, 100, "loops", True), (1, 3, "loops", True),
+                                                         (1, 3, "loops", False), (2, 2, "loops", True),
+                                                         (3, 1, "f64", True)])
+def test_model_lockstep_live(index, steps, route, speculate):
+    """Every step's tensors and scalars against the oracle run live. With
+    speculative requantisation on (the default) the int32 results of the
+    speculating contractions are not written; the run with it off compares
+    them too."""
     w = si.by_name(index)
     g = GpuRun(w)
+    g.model.set_speculation(speculate)
     weights = si.make_weights(w)
     for t in range(steps):
         rec = _oracle_step(w, weights, t, route)
@@ -127,14 +133,20 @@ def test_speculation_gives_identical_steps(index, steps):
         for g in runs:
             g.step(t)
             recs.append(g.record())
-        assert recs[0].keys() == recs[1].keys()
-        for k in recs[0]:
+        # the speculating contractions write no int32 result; everything else is identical
+        assert set(recs[1].keys()) == set(recs[0].keys()) - runs[1].unwritten_int32()
+        for k in recs[1]:
             assert np.array_equal(np.asarray(recs[0][k]), np.asarray(recs[1][k])), (t, k)
         spec = runs[1].model.tensor("spec").cpu().numpy()
-        pred, last, used = spec[: 2 * nl], spec[2 * nl: 4 * nl], spec[4 * nl:]
+        pred, last, used = spec[: 2 * nl], spec[2 * nl: 4 * nl], spec[4 * nl: 6 * nl]
         off = runs[0].model.tensor("spec").cpu().numpy()
         assert (off[: 2 * nl] == -1).all()
-        assert np.array_equal(off[2 * nl:], spec[2 * nl:]), t
+        assert np.array_equal(off[2 * nl: 6 * nl], spec[2 * nl: 6 * nl]), t
+        # re-launch words: 0 where the prediction held (or none was made), else the shift + 1
+        redo = spec[6 * nl: 8 * nl]
+        act_now = (used != 0) & (pred >= 0)
+        assert np.array_equal(redo[act_now], np.where(pred[act_now] == last[act_now], 0, last[act_now] + 1)), t
+        assert (redo[~act_now] == 0).all(), t
         assert (pred[used == 0] == -1).all()
         # the counters hold the steps before this one
         cnt = runs[1].model.tensor("spec_count").cpu().numpy()
@@ -149,3 +161,39 @@ def test_speculation_gives_identical_steps(index, steps):
         # the hidden layers' forward and delta-propagation contractions speculate
         assert used.sum() > 0 and hits > 0
     assert runs[0].ito.ito_get_error() == 0
+
+
+@pytest.mark.parametrize("index,steps,route", [(1, 4, "loops"), (3, 2, "f64")])
+def test_mispredicted_shift_relaunch_matches_oracle(index, steps, route):
+    """Forced mispredictions: before steps 1, 2, ... every speculating slot's
+    prediction is set one or more off the true previous shift. The epilogue
+    then requantises with the wrong shift, the check records the step's shift
+    in the re-launch word, and the contraction's re-launch rewrites the int8
+    and bf16 outputs; every tensor and scalar still matches the oracle."""
+    import torch
+    w = si.by_name(index)
+    g = GpuRun(w)
+    assert g.model.speculation()
+    nl = g.n_layers
+    weights = si.make_weights(w)
+    for t in range(steps):
+        spec = g.model.tensor("spec")
+        used = spec[4 * nl: 6 * nl] != 0
+        if t > 0:
+            # the step's predictions are read from the previous step's shifts (the "last" block)
+            last = spec[2 * nl: 4 * nl]
+            last.copy_(torch.where(used, last + (1 if t % 2 else 3), last))
+            torch.cuda.synchronize()
+        rec = _oracle_step(w, weights, t, route)
+        g.step(t)
+        compare_records(rec, g.record(), t)
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+        spec = g.model.tensor("spec").cpu().numpy()
+        pred, last, used, redo = (spec[i * 2 * nl: (i + 1) * 2 * nl] for i in range(4))
+        if t > 0:
+            act = (used != 0) & (pred >= 0)
+            assert act.any()
+            # (a shift that itself moved by the offset makes a prediction hold by chance)
+            assert (pred[act] != last[act]).any(), t
+            assert np.array_equal(redo[act], np.where(pred[act] == last[act], 0, last[act] + 1)), t
+    assert g.ito.ito_get_error() == 0
