@@ -686,6 +686,20 @@ int ito_model_profile_read(ito_model *m, double *ms, double *work, int64_t *laun
 /* Number of kernels the model launches per training step. */
 int ito_model_kernels_per_step(const ito_model *m);
 
+/* Per-kernel timing of the DFP16 model, as ito_model_profile /
+ * ito_model_profile_read: an event pair on the launch's stream around every
+ * launch of a step; classes ITO_PROF_GEMM (limb contractions; work = executed
+ * bf16 operations, 8*M*N*K: four limb products per int16 multiply-add),
+ * ITO_PROF_REQUANT (down-conversions; work = algorithmic HBM bytes),
+ * ITO_PROF_UPDATE (weight updates; bytes) and ITO_PROF_OTHER. The model
+ * launches directly (no graphs), so every step's events are kept until read.
+ * Enabling synchronises the device. Errors: ITO_ERR_ARG, ITO_ERR_CUDA. */
+int ito_dfp16_model_profile(ito_dfp16_model *m, int enable);
+int ito_dfp16_model_profile_read(ito_dfp16_model *m, double *ms, double *work, int64_t *launches);
+
+/* Number of kernels the DFP16 model launched in its last training step. */
+int ito_dfp16_model_kernels_per_step(const ito_dfp16_model *m);
+
 #ifdef __cplusplus
 }
 #endif

@@ -100,6 +100,9 @@ _SIGS = {
     "ito_dfp16_model_stat_index": (_I, [_P, ctypes.c_char_p]),
     "ito_dfp16_model_read_stats": (_I, [_P, _P, _I]),
     "ito_dfp16_train_step": (_I, [_P, _P, _I32, _P]),
+    "ito_dfp16_model_profile": (_I, [_P, _I]),
+    "ito_dfp16_model_profile_read": (_I, [_P, _P, _P, _P]),
+    "ito_dfp16_model_kernels_per_step": (_I, [_P]),
     "ito_model_use_graphs": (_I, [_P, _I]),
     "ito_model_set_overlap": (_I, [_P, _I]),
     "ito_model_set_speculation": (_I, [_P, _I]),
@@ -686,6 +689,20 @@ class Dfp16Model:
 
     def train_step(self, x, exp_x, stream=None):
         _check(_lib.ito_dfp16_train_step(self._h, _ptr(x), int(exp_x), _stream(stream)))
+
+    def profile(self, enable=True):
+        _check(_lib.ito_dfp16_model_profile(self._h, int(enable)))
+
+    def profile_read(self):
+        """{class: (ms, work, launches)} summed since the last read."""
+        ms = (ctypes.c_double * 4)()
+        work = (ctypes.c_double * 4)()
+        n = (ctypes.c_int64 * 4)()
+        _check(_lib.ito_dfp16_model_profile_read(self._h, ms, work, n))
+        return {name: (ms[i], work[i], n[i]) for i, name in enumerate(("gemm", "down", "update", "other"))}
+
+    def kernels_per_step(self) -> int:
+        return _lib.ito_dfp16_model_kernels_per_step(self._h)
 
     def precision(self, layer):
         """-> (bits, exp_w) of a layer's weights"""

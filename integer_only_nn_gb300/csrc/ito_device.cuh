@@ -74,11 +74,17 @@ __device__ __forceinline__ uint16_t int_to_bf16_bits(int32_t v)
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
-// Two small integers (|v| <= 256, exact in bf16) as one bf16x2 word, lo in the low half.
+// Two small integers (|v| <= 256) as one bf16x2 word, lo in the low half, on the
+// integer and FP32 add pipes instead of the conversion units. The float with bit
+// pattern 0x4B400000 + v is 1.5 * 2^23 + v (its unit in the last place is 1, and
+// the mantissa field has room for any |v| < 2^22), so subtracting 1.5 * 2^23 gives
+// float(v) exactly. An integer of at most 8 significant bits has a float whose low
+// 16 bits are zero, so its bf16 is the float's high half.
 __device__ __forceinline__ uint32_t int_pair_to_bf16x2(int32_t lo, int32_t hi)
 {
-    __nv_bfloat162 v = __floats2bfloat162_rn((float)lo, (float)hi);
-    return *reinterpret_cast<uint32_t*>(&v);
+    const float flo = __fsub_rn(__int_as_float(0x4B400000 + lo), 12582912.0f);
+    const float fhi = __fsub_rn(__int_as_float(0x4B400000 + hi), 12582912.0f);
+    return __byte_perm(__float_as_uint(flo), __float_as_uint(fhi), 0x7632);
 }
 
 // ------------------------------------------------------------- PTX helpers

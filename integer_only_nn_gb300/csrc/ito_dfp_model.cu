@@ -97,6 +97,34 @@ struct ito_dfp16_model {
     int32_t* s32 = nullptr;            // [layers][D_N32] + [ex, ew]
     unsigned long long* s64 = nullptr; // [layers][D_N64]
     std::vector<void*> allocs;
+    // per-kernel timing (ito_dfp16_model_profile): an event pair around every launch, on the
+    // launch's stream; classes as ito_prof_class (the down-conversions count as requantisation)
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_ev;
+    std::vector<int> prof_cls;
+    std::vector<double> prof_work;
+    int prof_n = 0;
+    int launches = 0;                  // kernels launched by the last step
+
+    void mark_begin(cudaStream_t st)
+    {
+        ++launches;
+        if (!prof_on) return;
+        while (prof_ev.size() < (size_t)(2 * prof_n + 2)) {
+            cudaEvent_t e;
+            cudaEventCreate(&e);
+            prof_ev.push_back(e);
+        }
+        cudaEventRecord(prof_ev[2 * prof_n], st);
+    }
+    void mark_end(cudaStream_t st, int cls, double work)
+    {
+        if (!prof_on) return;
+        cudaEventRecord(prof_ev[2 * prof_n + 1], st);
+        prof_cls.push_back(cls);
+        prof_work.push_back(work);
+        ++prof_n;
+    }
 
     template <class T>
     int alloc(T** out, size_t count)
@@ -123,6 +151,21 @@ using namespace ito;
         int _r = (x);                \
         if (_r != ITO_OK) return _r; \
     } while (0)
+
+// a model launch, bracketed by the profiling events when they are on
+#define ITO_DLAUNCH(m, st, cls, work, call)      \
+    do {                                         \
+        (m)->mark_begin(st);                     \
+        int _r = (call);                         \
+        (m)->mark_end(st, cls, (double)(work));  \
+        if (_r != ITO_OK) return _r;             \
+    } while (0)
+
+// executed bf16 operations of a limb contraction: four limb products per int16 multiply-add
+static double dfp_gemm_ops(const DfpGemmPlan& g) { return 8.0 * g.M * (double)g.N * g.K; }
+
+// kernels one dfp_gemm_run launches: the contraction, and the reduction of a split last wave
+static int dfp_gemm_kernels(const DfpGemmPlan& g) { return 1 + ((g.pair && g.tail_parts > 1) ? 1 : 0); }
 
 static inline size_t al256(size_t n) { return (n + 255) & ~size_t(255); }
 
@@ -343,6 +386,7 @@ int ito_dfp16_model_destroy(ito_dfp16_model* m)
     if (!m) return ITO_OK;
     cudaDeviceSynchronize();
     for (cudaEvent_t e : m->sync_ev) cudaEventDestroy(e);
+    for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
     if (m->side) cudaStreamDestroy(m->side);
     for (void* p : m->allocs) cudaFree(p);
     delete m;
@@ -543,6 +587,41 @@ int ito_dfp16_model_read_stats(const ito_dfp16_model* m, int64_t* host_out, int 
     return ITO_OK;
 }
 
+int ito_dfp16_model_profile(ito_dfp16_model* m, int enable)
+{
+    if (!m) return set_error(ITO_ERR_ARG, "NULL model");
+    if (cudaDeviceSynchronize() != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
+    m->prof_on = enable != 0;
+    m->prof_n = 0;
+    m->prof_cls.clear();
+    m->prof_work.clear();
+    return ITO_OK;
+}
+
+int ito_dfp16_model_profile_read(ito_dfp16_model* m, double* ms, double* work, int64_t* launches)
+{
+    if (!m || !ms || !work || !launches) return set_error(ITO_ERR_ARG, "NULL argument");
+    for (int c = 0; c < ITO_PROF_NCLASS; ++c) {
+        ms[c] = work[c] = 0.0;
+        launches[c] = 0;
+    }
+    for (int i = 0; i < m->prof_n; ++i) {
+        float t = 0.f;
+        if (cudaEventSynchronize(m->prof_ev[2 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&t, m->prof_ev[2 * i], m->prof_ev[2 * i + 1]) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "profile event read failed");
+        ms[m->prof_cls[i]] += t;
+        work[m->prof_cls[i]] += m->prof_work[i];
+        launches[m->prof_cls[i]] += 1;
+    }
+    m->prof_n = 0;
+    m->prof_cls.clear();
+    m->prof_work.clear();
+    return ITO_OK;
+}
+
+int ito_dfp16_model_kernels_per_step(const ito_dfp16_model* m) { return m ? m->launches : 0; }
+
 int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, void* stream)
 {
     if (!m || !x) return set_error(ITO_ERR_ARG, "NULL argument");
@@ -553,16 +632,21 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
     if (cudaMemsetAsync(m->s32, 0, sizeof(int32_t) * nl * D_N32, s) != cudaSuccess ||
         cudaMemsetAsync(m->s64, 0, sizeof(unsigned long long) * nl * D_N64, s) != cudaSuccess)
         return set_error(ITO_ERR_CUDA, "memset");
-    k_set_i32<<<1, 1, 0, s>>>(m->ex(), exp_x);
-    ITO_TRY(launch_i16_to_limbs(x, B, m->L[0].IC, m->xh, m->xl, m->ldx, s));
+    m->launches = 0;
+    ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0, (k_set_i32<<<1, 1, 0, s>>>(m->ex(), exp_x), ITO_OK));
+    ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 6.0 * B * m->L[0].IC,
+                launch_i16_to_limbs(x, B, m->L[0].IC, m->xh, m->xl, m->ldx, s));
     for (int l = 0; l < nl; ++l) {
         DLayer& L = m->L[l];
         const int32_t* e_in = l == 0 ? m->ex() : m->i32(l - 1, D_EY);
-        ITO_TRY(dfp_gemm_run(L.pf, s));
-        ITO_TRY(launch_dfp_down(L.p64, B, L.OC, m->u64(l, D_PMAX), e_in, m->wexp_d + l, L.y16, L.yh, L.yl, L.ldy,
-                                m->i32(l, D_EY), m->i32(l, D_RS), s));
+        ITO_DLAUNCH(m, s, ITO_PROF_GEMM, dfp_gemm_ops(L.pf), dfp_gemm_run(L.pf, s));
+        m->launches += dfp_gemm_kernels(L.pf) - 1;
+        ITO_DLAUNCH(m, s, ITO_PROF_REQUANT, 14.0 * B * L.OC,
+                    launch_dfp_down(L.p64, B, L.OC, m->u64(l, D_PMAX), e_in, m->wexp_d + l, L.y16, L.yh, L.yl, L.ldy,
+                                    m->i32(l, D_EY), m->i32(l, D_RS), s));
     }
-    k_copy_i32<<<1, 1, 0, s>>>(m->i32(nl - 1, D_EE), m->i32(nl - 1, D_EY));
+    ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0,
+                (k_copy_i32<<<1, 1, 0, s>>>(m->i32(nl - 1, D_EE), m->i32(nl - 1, D_EY)), ITO_OK));
     // backward, top-down; with the overlap on, the contractions stay on s and the
     // down-conversions and the update go to the side stream b: the propagated delta's
     // down-conversion runs beside the weight gradient, the gradient's down-conversion
@@ -583,19 +667,25 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
             return set_error(ITO_ERR_CUDA, "stream ordering event failed");
         if (l > 0) {
             DLayer& P = m->L[l - 1];
-            ITO_TRY(dfp_gemm_run(L.pd, s));
+            ITO_DLAUNCH(m, s, ITO_PROF_GEMM, dfp_gemm_ops(L.pd), dfp_gemm_run(L.pd, s));
+        m->launches += dfp_gemm_kernels(L.pd) - 1;
             ITO_TRY(sync(ev(l, 0), s, b));
-            ITO_TRY(launch_dfp_down(L.pd64, B, L.IC, m->u64(l, D_PDMAX), m->i32(l, D_EE), m->wexp_d + l, P.e16, P.eh,
-                                    P.el, P.ldy, m->i32(l - 1, D_EE), m->i32(l, D_RSD), b));
+            ITO_DLAUNCH(m, b, ITO_PROF_REQUANT, 14.0 * B * L.IC,
+                        launch_dfp_down(L.pd64, B, L.IC, m->u64(l, D_PDMAX), m->i32(l, D_EE), m->wexp_d + l, P.e16,
+                                        P.eh, P.el, P.ldy, m->i32(l - 1, D_EE), m->i32(l, D_RSD), b));
             if (b != s && cudaEventRecord(ev(l, 1), b) != cudaSuccess)
                 return set_error(ITO_ERR_CUDA, "stream ordering event failed");
         }
-        ITO_TRY(dfp_gemm_run(L.pg, s));
+        ITO_DLAUNCH(m, s, ITO_PROF_GEMM, dfp_gemm_ops(L.pg), dfp_gemm_run(L.pg, s));
+        m->launches += dfp_gemm_kernels(L.pg) - 1;
         ITO_TRY(sync(ev(l, 2), s, b));
-        ITO_TRY(launch_dfp_down(L.pg64, L.OC, L.IC, m->u64(l, D_PGMAX), m->i32(l, D_EE), e_in, L.g16, nullptr, nullptr,
-                                0, m->i32(l, D_EG), m->i32(l, D_RSG), b, m->u64(l, D_GABS)));
-        ITO_TRY(launch_dfp_update(L.W, L.Wh, L.Wl, L.ldw, L.g16, L.OC, L.IC, m->i32(l, D_EG), m->wexp[l], m->eta,
-                                  m->i32(l, D_K), reinterpret_cast<uint32_t*>(m->i32(l, D_NZ)), b, m->wbits[l]));
+        ITO_DLAUNCH(m, b, ITO_PROF_REQUANT, 10.0 * L.OC * L.IC,
+                    launch_dfp_down(L.pg64, L.OC, L.IC, m->u64(l, D_PGMAX), m->i32(l, D_EE), e_in, L.g16, nullptr,
+                                    nullptr, 0, m->i32(l, D_EG), m->i32(l, D_RSG), b, m->u64(l, D_GABS)));
+        ITO_DLAUNCH(m, b, ITO_PROF_UPDATE, 10.0 * L.OC * L.IC,
+                    launch_dfp_update(L.W, L.Wh, L.Wl, L.ldw, L.g16, L.OC, L.IC, m->i32(l, D_EG), m->wexp[l], m->eta,
+                                      m->i32(l, D_K), reinterpret_cast<uint32_t*>(m->i32(l, D_NZ)), b,
+                                      m->wbits[l]));
     }
     ITO_TRY(sync(m->sync_ev[1], b, s));
     if (m->apt) {
@@ -603,8 +693,11 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
         if (m->apt_step % m->ap.eval_every == 0) {
             if (m->apt_nlog >= kAptMaxEvals)
                 return set_error(ITO_ERR_ARG, "more than %d Gavg evaluations in one epoch", kAptMaxEvals);
-            k_apt_log<<<1, 32 * ((nl + 31) / 32), 0, s>>>(m->s64, m->s32, nl, m->log_abs + (size_t)m->apt_nlog * nl,
-                                                          m->log_eg + (size_t)m->apt_nlog * nl);
+            ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0,
+                        (k_apt_log<<<1, 32 * ((nl + 31) / 32), 0, s>>>(m->s64, m->s32, nl,
+                                                                       m->log_abs + (size_t)m->apt_nlog * nl,
+                                                                       m->log_eg + (size_t)m->apt_nlog * nl),
+                         ITO_OK));
             ++m->apt_nlog;
         }
         ++m->apt_step;
