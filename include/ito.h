@@ -346,9 +346,10 @@ int ito_model_get_weights(const ito_model *m, int layer, int8_t *W, int on_host,
  * "stats" int32 scalars; see ito_model_stat_index; "spec" int32 [8 * layers]:
  * the forward and delta-propagation shift predictions the step used, the
  * shifts the step computed, 1 where the contraction's epilogue speculates, and
- * the re-launch words (0: the prediction held or none was made, else the
- * step's shift + 1), each block of 2 * layers indexed by weight layer, -1 in
- * the first two where none; "spec_count"
+ * the re-launch words (0: the prediction held, else the step's shift + 1: the
+ * re-launch recomputed the outputs; 0 where the slot does not speculate), each
+ * block of 2 * layers indexed by weight layer, -1 in the first two where none;
+ * "spec_count"
  * int64 [2]: predictions that held and that missed since creation, scored at
  * the start of the following step (see ito_model_set_speculation)). Writes the device
  * pointer, the element type (1 = int8, 2 = int16, 4 = int32, 8 = int64) and
@@ -424,13 +425,13 @@ int ito_model_get_overlap(const ito_model *m, int *mode);
  * of 16; no packed masks, static requantisation or ping-pong buffers) writes
  * the requantised int8 tensor and its bf16 copy using the shift the same
  * tensor had in the previous step, and folds the max, but writes no int32
- * result. A one-word check then computes this step's shift from the max; when
- * it differs, a second launch of the same contraction recomputes the outputs
- * with it (that launch returns at once when the prediction held). The int8,
- * bf16 and scalar results are NITI's in either case; the int32 tensors "y<l>"
- * and "d<l>" of those contractions are not written while speculation is on
- * (the step with no prediction yet, the first, still writes them). Changing
- * the setting synchronises the device and drops captured graphs.
+ * result. A second launch of the same contraction computes this step's shift
+ * from the max in its prologue and returns at once when the prediction held;
+ * otherwise (or when there was no prediction yet, as in the first step) it
+ * recomputes the contraction and writes the outputs with the step's shift. The
+ * int8, bf16 and scalar results are NITI's in either case; the int32 tensors
+ * "y<l>" and "d<l>" of those contractions are not written while speculation is
+ * on. Changing the setting synchronises the device and drops captured graphs.
  * Errors: ITO_ERR_ARG. */
 int ito_model_set_speculation(ito_model *m, int enable);
 

@@ -132,27 +132,19 @@ __device__ __forceinline__ int32_t requant_one(int32_t y, int s, int relu, int g
 // The optional bit-packed ReLU masks hold one byte per eight elements of a
 // row (cols / 8 bytes per row; bit j is element j of the group): mask_out
 // receives (q > 0) of the result, gate_bits replaces the int8 gate.
-// s_pred (optional): the shift a speculative requantisation in the contraction's
-// epilogue used (< 0: none this step). When it is >= 0 the contraction wrote no
-// int32 result: the kernel only records the shift, sets *redo to 0 when the
-// prediction held (out8 and outb hold the result) or to shift + 1 when it did not
-// (the contraction's re-launch rewrites them), and returns. s_last (optional)
-// receives the shift (the next step's prediction).
+// s_last (optional) receives the shift (a model's prediction of the same tensor's
+// shift in the next step, for the speculative requantisation of FusedRq).
 __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
                              const uint32_t* __restrict__ d_max, int target_bits, int relu,
                              const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
                              int64_t ldb, int32_t* __restrict__ d_shift, const uint8_t* __restrict__ gate_bits,
-                             uint8_t* __restrict__ mask_out, const int32_t* __restrict__ s_pred,
-                             int32_t* __restrict__ s_last, int32_t* __restrict__ redo)
+                             uint8_t* __restrict__ mask_out, int32_t* __restrict__ s_last)
 {
     const int s = shift_for(*d_max, target_bits);
-    const int sp = s_pred ? *s_pred : -1;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (d_shift) *d_shift = s;
         if (s_last) *s_last = s;
-        if (redo) *redo = (sp >= 0 && sp != s) ? s + 1 : 0;
     }
-    if (sp >= 0) return;
     const int64_t groups = rows * (cols >> 3);
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
@@ -190,17 +182,13 @@ __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_
 __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
                             const uint32_t* __restrict__ d_max, int target_bits, int relu,
                             const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
-                            int64_t ldb, int32_t* __restrict__ d_shift, const int32_t* __restrict__ s_pred,
-                            int32_t* __restrict__ s_last, int32_t* __restrict__ redo)
+                            int64_t ldb, int32_t* __restrict__ d_shift, int32_t* __restrict__ s_last)
 {
     const int s = shift_for(*d_max, target_bits);
-    const int sp = s_pred ? *s_pred : -1;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (d_shift) *d_shift = s;
         if (s_last) *s_last = s;
-        if (redo) *redo = (sp >= 0 && sp != s) ? s + 1 : 0;
     }
-    if (sp >= 0) return;
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int32_t q = requant_one(Y[i], s, relu, gate ? gate[i] > 0 : 1);
@@ -214,11 +202,8 @@ __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t
 
 int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
                    const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
-                   const uint8_t* gate_bits, uint8_t* mask_out, const int32_t* s_pred, int32_t* s_last,
-                   int32_t* redo)
+                   const uint8_t* gate_bits, uint8_t* mask_out, int32_t* s_last)
 {
-    if (s_pred && (gate_bits || mask_out))
-        return set_error(ITO_ERR_UNSUPPORTED, "speculative requantisation with bit-packed masks");
     if (rows < 1 || cols < 1) return ITO_OK;
     const bool vec = cols % 8 == 0 && aligned(Y, 16) && aligned(out8, 8) && (!gate || aligned(gate, 8)) &&
                      (!outb || (aligned(outb, 16) && ldb % 8 == 0));
@@ -226,12 +211,10 @@ int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t*
         return set_error(ITO_ERR_UNSUPPORTED, "bit-packed masks need rows of a multiple of 8 elements");
     if (vec)
         k_requant_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(
-            Y, rows, cols, d_max, target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out, s_pred,
-            s_last, redo);
+            Y, rows, cols, d_max, target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out, s_last);
     else
         k_requant_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(Y, rows, cols, d_max, target_bits, relu,
-                                                                          gate, out8, outb, ldb, d_shift, s_pred,
-                                                                          s_last, redo);
+                                                                          gate, out8, outb, ldb, d_shift, s_last);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "requant launch: %s", cudaGetErrorString(e));
 }
@@ -515,12 +498,45 @@ __global__ void k_top_error(const int8_t* __restrict__ logits, const int32_t* __
     }
 }
 
+// Rows of a multiple of 8 classes: a thread takes 8 consecutive logits of one row (one
+// 8-byte load, one 8-byte and one 16-byte store); rows over blockIdx.y (strided past 65535).
+__global__ void k_top_error_v8(const int8_t* __restrict__ logits, const int32_t* __restrict__ labels, int B, int C,
+                               int target_mag, int8_t* __restrict__ delta, uint16_t* __restrict__ deltab, int64_t ldb)
+{
+    const int groups = C >> 3;
+    for (int b = blockIdx.y; b < B; b += gridDim.y) {
+        const int label = labels[b];
+        for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += gridDim.x * blockDim.x) {
+            const int64_t i0 = (int64_t)b * C + 8 * g;
+            int8_t v[8];
+            *reinterpret_cast<uint2*>(v) = *reinterpret_cast<const uint2*>(logits + i0);
+            int8_t d[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                d[k] = (int8_t)sat8((int32_t)v[k] - (8 * g + k == label ? target_mag : 0));
+            *reinterpret_cast<uint2*>(delta + i0) = *reinterpret_cast<const uint2*>(d);
+            if (deltab)
+                *reinterpret_cast<uint4*>(deltab + (int64_t)b * ldb + 8 * g) =
+                    make_uint4(int_pair_to_bf16x2(d[0], d[1]), int_pair_to_bf16x2(d[2], d[3]),
+                               int_pair_to_bf16x2(d[4], d[5]), int_pair_to_bf16x2(d[6], d[7]));
+        }
+    }
+}
+
 int launch_top_error(const int8_t* logits, const int32_t* labels, int B, int C, int target_mag, int8_t* delta,
                      uint16_t* deltab, int64_t ldb, cudaStream_t s)
 {
     if (B < 1 || C < 1) return ITO_OK;
-    k_top_error<<<launch_grid_blocks((int64_t)B * C, 256), 256, 0, s>>>(logits, labels, B, C, target_mag, delta,
-                                                                         deltab, ldb);
+    const bool vec = C % 8 == 0 && aligned(logits, 8) && aligned(delta, 8) &&
+                     (!deltab || (aligned(deltab, 16) && ldb % 8 == 0));
+    if (vec) {
+        const int groups = C / 8;
+        const dim3 grid((groups + 127) / 128, B < 65535 ? B : 65535);
+        k_top_error_v8<<<grid, 128, 0, s>>>(logits, labels, B, C, target_mag, delta, deltab, ldb);
+    } else {
+        k_top_error<<<launch_grid_blocks((int64_t)B * C, 256), 256, 0, s>>>(logits, labels, B, C, target_mag, delta,
+                                                                             deltab, ldb);
+    }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "top error launch: %s", cudaGetErrorString(e));
 }

@@ -331,21 +331,25 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
 // release an accumulator buffer on the leader's barrier.
 
 // Speculative requantisation in the pair kernel's epilogue (FusedRq.pred set).
-// When *pred >= 0 (the shift the same tensor had in the previous step), the
-// epilogue writes q = sat8(rhu(y, *pred)) (ReLU'd, or zeroed where gate <= 0) as
-// int8 and as bf16 and does not write the int32 result; it still folds max|y|
-// into d_max. The check that follows (k_requant_v8 with s_pred) computes the true
-// shift s from the max and leaves *redo = 0 when s == *pred, else *redo = s + 1.
-// A second launch of the same plan with FusedRq.redo set then returns at once
-// when *redo == 0, and otherwise recomputes the contraction and writes q with
-// shift *redo - 1 (no int32 result, no max). When *pred < 0 (no prediction) the
-// first launch writes the int32 result and the requantisation pass runs in full.
+// The first launch folds max|y| into d_max and writes no int32 result. When
+// *pred >= 0 (the shift the same tensor had in the previous step) its epilogue
+// writes q = sat8(rhu(y, *pred)) (ReLU'd, or zeroed where gate <= 0) as int8 and
+// as bf16; when *pred < 0 (no prediction yet) it writes nothing else. A second
+// launch of the same plan with FusedRq.redo set computes, in its prologue, the
+// true shift s = max(0, bitlen(*d_max) - target_bits), records it (d_shift,
+// s_last, and *redo = 0 when the prediction held, else s + 1), and returns at once
+// when *pred == s; otherwise it recomputes the contraction and writes q with
+// shift s (no max, no int32 result).
 struct FusedRq {
     const int32_t* pred;   // predicted shift (device word; < 0: none this step); nullptr: off
     const int8_t* gate;    // [M][ldg] int8 ReLU gate, or nullptr
     int64_t ldg;
     int relu;
-    const int32_t* redo;   // the re-launch: 0 = nothing to do, else shift + 1; nullptr: first launch
+    // the re-launch (redo != nullptr): its record of this step's shift
+    int32_t* redo;         // 0 = the prediction held, else the shift + 1
+    int32_t* d_shift;      // the step's shift (statistics), may be null
+    int32_t* s_last;       // the step's shift (the next step's prediction), may be null
+    int target_bits;
 };
 
 struct Tc2Cfg {
@@ -377,13 +381,21 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
     constexpr int HALF = BN / 2;
     constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
 
-    // the shift of a speculative requantisation (< 0: none); a re-launch whose first
-    // launch's prediction held returns here, in every CTA alike (one device word)
+    // the shift of a speculative requantisation (< 0: none). A re-launch first checks the
+    // first launch's prediction against the step's max and returns, in every CTA alike,
+    // when it held
     int sp = -1;
     if (fz.redo) {
-        const int r = *fz.redo;
-        if (r <= 0) return;
-        sp = r - 1;
+        const int s_true = shift_for(*d_max, fz.target_bits);
+        const int p = *fz.pred;
+        const bool held = p >= 0 && p == s_true;
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            *fz.redo = held ? 0 : s_true + 1;
+            if (fz.d_shift) *fz.d_shift = s_true;
+            if (fz.s_last) *fz.s_last = s_true;
+        }
+        if (held) return;
+        sp = s_true;
     } else if (fz.pred) {
         sp = *fz.pred;
     }
@@ -664,6 +676,9 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
                         bulk_commit();
                     }
                 }
+            } else if (fz.pred) {
+                // a speculating launch with no prediction yet: the max only (above); the
+                // re-launch writes the outputs
             } else if (use_tma_store) {
                 // the int32 result through the staging buffer, 32 x 32 boxes
 #pragma unroll
@@ -1008,7 +1023,7 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const FusedRq fz{p.rq_pred, p.rq_gate, p.rq_ldg, p.rq_relu, p.rq_redo};
+    const FusedRq fz{p.rq_pred, p.rq_gate, p.rq_ldg, p.rq_relu, p.rq_redo, p.rq_d_shift, p.rq_s_last, p.rq_target_bits};
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.mapP, p.mapO8, p.mapOB, fz,
                                        p.use_tma_store, p.M, p.N, p.K, p.chunk_kb, p.group, p.tail_full, p.tail_parts,
                                        p.C, p.ldc, p.d_max, p.err);

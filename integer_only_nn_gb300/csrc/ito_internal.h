@@ -39,13 +39,16 @@ struct GemmPlan {
     int group;  // row tiles per raster group (L2 reuse)
     int tail_full, tail_parts;    // pair kernel: whole tiles, K pieces per remaining tile (1: no split)
     // pair kernel: speculative requantisation in the epilogue (rq_pred != nullptr); rq_redo
-    // set: the re-launch after a misprediction (see FusedRq)
+    // set: the re-launch that checks the prediction and recomputes on a miss (see FusedRq)
     CUtensorMap mapO8, mapOB;
     const int32_t* rq_pred;
     const int8_t* rq_gate;
     int64_t rq_ldg;
     int rq_relu;
-    const int32_t* rq_redo;
+    int32_t* rq_redo;
+    int32_t* rq_d_shift;
+    int32_t* rq_s_last;
+    int rq_target_bits;
     int M, N, K, bn, chunk_kb;
     int splits, kb_per_split;     // split-K: slices of kb_per_split K blocks (splits == 1: none)
     int32_t* split_ws;            // [splits][M][ldc] int32 partials
@@ -177,11 +180,10 @@ int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* d
 // result is zeroed where gate <= 0 (delta propagation through a ReLU).
 // gate_bits / mask_out (optional, cols % 8 == 0): bit-packed ReLU masks, one
 // byte per 8 elements: read in place of the int8 gate / written from the result.
-// s_pred / s_last / redo: see k_requant_v8 (speculative requantisation in a contraction epilogue)
+// s_last (optional) receives the shift as well (the next step's prediction of a speculating model)
 int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
                    const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
-                   const uint8_t* gate_bits = nullptr, uint8_t* mask_out = nullptr, const int32_t* s_pred = nullptr,
-                   int32_t* s_last = nullptr, int32_t* redo = nullptr);
+                   const uint8_t* gate_bits = nullptr, uint8_t* mask_out = nullptr, int32_t* s_last = nullptr);
 // scores the last step's predictions into count[0] (held) / count[1] (missed) over the used
 // slots, then pred[i] = (on && used[i]) ? last[i] : -1 for i < n
 int launch_roll_shift_predictions(int32_t* pred, const int32_t* last, const int32_t* used, int64_t* count, int n,

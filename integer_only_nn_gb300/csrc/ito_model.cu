@@ -61,7 +61,9 @@ struct MLayer {
     bool static_q = false;      // static per-channel requantisation with trained INT32 offsets
     int32_t *off32 = nullptr, *mult32 = nullptr, *k32 = nullptr, *og32 = nullptr;   // [OC] (Linear layers)
     GemmPlan pf{}, pd{}, pg{};
-    GemmPlan pf_redo{}, pd_redo{};   // re-launches of pf / pd after a shift misprediction
+    // speculative requantisation (see FusedRq): pf / pd with the requantising epilogue, and their
+    // re-launches, which check the shift prediction and recompute when it missed
+    GemmPlan pf_spec{}, pd_spec{}, pf_redo{}, pd_redo{};
     bool has_dgrad = false;
     bool relu = false;
 };
@@ -417,33 +419,39 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         // activation and bf16 copy) and of the delta propagation (the gated delta below); not
         // with bit-packed masks, static requantisation, or shared (ping-pong) delta buffers
         const bool plain = !m->opt.packed_masks && !m->opt.pingpong_grads;
+        L.pf_spec = L.pf;
+        L.pd_spec = L.pd;
         if (plain && !conv && !L.static_q && L.ab)
-            ITO_TRY(gemm_plan_fuse_requant(&L.pf, m->pred_y(l), L.relu ? 1 : 0, nullptr, 0, L.a8, L.OC, L.ab,
+            ITO_TRY(gemm_plan_fuse_requant(&L.pf_spec, m->pred_y(l), L.relu ? 1 : 0, nullptr, 0, L.a8, L.OC, L.ab,
                                            L.lda));
         if (plain && !conv && L.has_dgrad && !(l == m->n_conv && m->has_pool)) {
             const MLayer& prev = m->L[l - 1];
             if (prev.kind != ITO_LAYER_CONV3X3_RELU)
-                ITO_TRY(gemm_plan_fuse_requant(&L.pd, m->pred_d(l), 0, prev.relu ? prev.a8 : nullptr, L.IC, prev.e8,
-                                               L.IC, prev.eb, prev.lde));
+                ITO_TRY(gemm_plan_fuse_requant(&L.pd_spec, m->pred_d(l), 0, prev.relu ? prev.a8 : nullptr, L.IC,
+                                               prev.e8, L.IC, prev.eb, prev.lde));
         }
-    }
-    for (auto& L : m->L) {
-        // the re-launches: the same plans, reading their re-launch word
-        if (L.pf.rq_pred) {
-            L.pf_redo = L.pf;
-            L.pf_redo.rq_redo = m->redo_y((int)(&L - m->L.data()));
+        // the re-launches: the same plans, with the check of the prediction in their prologue
+        if (L.pf_spec.rq_pred) {
+            L.pf_redo = L.pf_spec;
+            L.pf_redo.rq_redo = m->redo_y(l);
+            L.pf_redo.rq_d_shift = m->sval(l, ST_YS);
+            L.pf_redo.rq_s_last = m->last_y(l);
+            L.pf_redo.rq_target_bits = m->p.target_bits;
         }
-        if (L.pd.rq_pred) {
-            L.pd_redo = L.pd;
-            L.pd_redo.rq_redo = m->redo_d((int)(&L - m->L.data()));
+        if (L.pd_spec.rq_pred) {
+            L.pd_redo = L.pd_spec;
+            L.pd_redo.rq_redo = m->redo_d(l);
+            L.pd_redo.rq_d_shift = m->sval(l, ST_DS);
+            L.pd_redo.rq_s_last = m->last_d(l);
+            L.pd_redo.rq_target_bits = m->p.target_bits;
         }
     }
     {
         // the slots whose contraction plan took the fused epilogue (a plan may decline it)
         std::vector<int32_t> used(2 * nl, 0);
         for (int l = 0; l < nl; ++l) {
-            used[l] = m->L[l].pf.rq_pred != nullptr;
-            used[nl + l] = m->L[l].pd.rq_pred != nullptr;
+            used[l] = m->L[l].pf_spec.rq_pred != nullptr;
+            used[nl + l] = m->L[l].pd_spec.rq_pred != nullptr;
         }
         if (cudaMemcpy(m->spec + 4 * nl, used.data(), sizeof(int32_t) * 2 * nl, cudaMemcpyHostToDevice) !=
             cudaSuccess)
@@ -472,7 +480,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
     } else {
         bool every_delta_speculates = m->speculate;
         for (const MLayer& L : m->L)
-            if (L.has_dgrad && !L.pd.rq_pred) every_delta_speculates = false;
+            if (L.has_dgrad && !L.pd_spec.rq_pred) every_delta_speculates = false;
         m->overlap = every_delta_speculates ? 0 : 1;
     }
     if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess)
@@ -529,21 +537,24 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
                        launch_requant(m->p32, B, m->pool_C, pmax, p.target_bits, 0, nullptr, m->pa8, m->pab,
                                       pad8(m->pool_C), m->stats + pl * ST_PER_LAYER + 1, s));
         }
-        ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
-        if (L.static_q)
-            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
-                       launch_requant_static(L.y32, L.rows_out, L.OC, L.off32, L.mult32, L.k32, L.relu ? 1 : 0, L.a8,
-                                             L.ab, L.lda, L.mask, s));
-        else {
-            // speculating, this is the check of the prediction (the epilogue wrote the
-            // outputs, no int32 result), then the contraction's re-launch, which returns at
-            // once when the prediction held
-            const bool spec = m->speculate && L.pf.rq_pred;
-            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, spec ? 0.0 : requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
-                       launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits, L.relu ? 1 : 0,
-                                      nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr, L.mask,
-                                      L.pf.rq_pred, m->last_y(l), spec ? m->redo_y(l) : nullptr));
-            if (spec) ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pf_redo, s));
+        if (m->speculate && L.pf_spec.rq_pred && !L.static_q) {
+            // speculating: the contraction requantises with the predicted shift in its
+            // epilogue; its re-launch checks the prediction against the max and returns at
+            // once when it held, else recomputes with the step's shift (requantisation class,
+            // no counted work)
+            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf_spec), gemm_run(L.pf_spec, s));
+            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pf_redo, s));
+        } else {
+            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
+            if (L.static_q)
+                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
+                           launch_requant_static(L.y32, L.rows_out, L.OC, L.off32, L.mult32, L.k32, L.relu ? 1 : 0,
+                                                 L.a8, L.ab, L.lda, L.mask, s));
+            else
+                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
+                           launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits,
+                                          L.relu ? 1 : 0, nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr,
+                                          L.mask, m->last_y(l)));
         }
         in8 = L.a8;
     }
@@ -584,12 +595,13 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
         if (delta_on_side && cudaStreamWaitEvent(s, m->ev_delta(l + 1), 0) != cudaSuccess)
             return set_error(ITO_ERR_CUDA, "stream ordering event failed");
         delta_on_side = false;
-        if (L.has_dgrad) {
+        if (L.has_dgrad && m->speculate && L.pd_spec.rq_pred) {
+            // speculating delta propagation and its re-launch, both on s (as in the forward)
+            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd_spec), gemm_run(L.pd_spec, s));
+            ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pd_redo, s));
+        } else if (L.has_dgrad) {
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
-            // a speculating delta propagation checks its prediction and re-launches on s: both
-            // return at once when the prediction held
-            const bool spec = m->speculate && L.pd.rq_pred;
-            const cudaStream_t r = spec ? s : r_side;
+            const cudaStream_t r = r_side;
             ITO_TRY(sync(m->ev_dgrad(l), s, r));   // the propagated delta is complete
             MLayer& prev = m->L[l - 1];
             if (conv) {
@@ -608,12 +620,10 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
                 ITO_LAUNCH(m, r, ITO_PROF_OTHER, 4.0 * B * m->pool_HW * m->pool_C,
                            launch_gap_bwd(m->pe8, prev.a8, B, m->pool_HW, m->pool_C, prev.e8, prev.eb, r));
             } else {
-                ITO_LAUNCH(m, r, ITO_PROF_REQUANT, spec ? 0.0 : requant_bytes((int64_t)B * L.IC, true, prev.relu),
+                ITO_LAUNCH(m, r, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, true, prev.relu),
                            launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
                                           (prev.relu && !prev.mask) ? prev.a8 : nullptr, prev.e8, prev.eb, prev.lde,
-                                          m->sval(l, ST_DS), r, prev.mask, nullptr, L.pd.rq_pred, m->last_d(l),
-                                          spec ? m->redo_d(l) : nullptr));
-                if (spec) ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pd_redo, s));
+                                          m->sval(l, ST_DS), r, prev.mask, nullptr, m->last_d(l)));
             }
             if (r != s) {
                 if (cudaEventRecord(m->ev_delta(l), r) != cudaSuccess)
@@ -784,6 +794,15 @@ int ito_model_set_static_requant(ito_model* m, int layer, const int32_t* offset,
         return set_error(ITO_ERR_CUDA, "static requant copy failed");
     if (on_host && cudaStreamSynchronize(s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
     L.static_q = true;
+    if (L.pf_spec.rq_pred) {
+        // the static requantisation replaces the dynamic shift: the forward slot no longer speculates
+        const int32_t zero = 0;
+        if (cudaDeviceSynchronize() != cudaSuccess ||
+            cudaMemcpy(m->spec + 4 * (int)m->L.size() + l, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "speculation flag update failed");
+        L.pf_spec = L.pf;
+        L.pf_redo = GemmPlan{};
+    }
     drop_graphs(m);
     return ITO_OK;
 }

@@ -142,11 +142,13 @@ def test_speculation_gives_identical_steps(index, steps):
         off = runs[0].model.tensor("spec").cpu().numpy()
         assert (off[: 2 * nl] == -1).all()
         assert np.array_equal(off[2 * nl: 6 * nl], spec[2 * nl: 6 * nl]), t
-        # re-launch words: 0 where the prediction held (or none was made), else the shift + 1
+        # re-launch words of the speculating slots: 0 where the prediction held, else the
+        # step's shift + 1 (a missed prediction, or none yet: the re-launch wrote the outputs)
         redo = spec[6 * nl: 8 * nl]
-        act_now = (used != 0) & (pred >= 0)
-        assert np.array_equal(redo[act_now], np.where(pred[act_now] == last[act_now], 0, last[act_now] + 1)), t
-        assert (redo[~act_now] == 0).all(), t
+        u = used != 0
+        held = u & (pred >= 0) & (pred == last)
+        assert np.array_equal(redo[u], np.where(held[u], 0, last[u] + 1)), t
+        assert (redo[~u] == 0).all(), t
         assert (pred[used == 0] == -1).all()
         # the counters hold the steps before this one
         cnt = runs[1].model.tensor("spec_count").cpu().numpy()
