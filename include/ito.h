@@ -313,12 +313,18 @@ int ito_model_create(const ito_layer_desc *layers, int n_layers, int batch, ito_
  *    Buffers": two ping-pong buffers sized batch * the largest layer output)
  *    instead of one per layer; layer l's delta lives in buffer l % 2, so after
  *    a step only the deltas of layers 0 and 1 remain readable (the tensor
- *    names e<l> of higher layers alias them). */
+ *    names e<l> of higher layers alias them);
+ *  - speculate_min_elems: speculative requantisation (ito_model_set_speculation)
+ *    covers only the contractions whose output has at least this many
+ *    elements; 0 = 4,194,304. Below that the requantisation pass is a few
+ *    microseconds and the re-launch, with its occasional recomputation, costs
+ *    more than it saves. */
 typedef struct ito_model_options {
     int32_t input_uint8;
     int32_t trainable_from;
     int32_t packed_masks;
     int32_t pingpong_grads;
+    int32_t speculate_min_elems;
 } ito_model_options;
 
 /* ito_model_create with options (NULL = all zero, the same as

@@ -37,7 +37,8 @@ class NitiParams(ctypes.Structure):
 
 class ModelOptions(ctypes.Structure):
     _fields_ = [("input_uint8", ctypes.c_int32), ("trainable_from", ctypes.c_int32),
-                ("packed_masks", ctypes.c_int32), ("pingpong_grads", ctypes.c_int32)]
+                ("packed_masks", ctypes.c_int32), ("pingpong_grads", ctypes.c_int32),
+                ("speculate_min_elems", ctypes.c_int32)]
 
 
 class AptParams(ctypes.Structure):
@@ -385,10 +386,11 @@ class Model:
     """An ito_model: a sequential int8 layer stack that trains with NITI."""
 
     def __init__(self, layers, batch, target_bits=7, mu_weight=2, target_mag=64, input_uint8=False,
-                 trainable_from=0, packed_masks=False, pingpong_grads=False):
+                 trainable_from=0, packed_masks=False, pingpong_grads=False, speculate_min_elems=0):
         arr = (LayerDesc * len(layers))(*layers)
         h = ctypes.c_void_p()
-        opt = ModelOptions(int(input_uint8), int(trainable_from), int(packed_masks), int(pingpong_grads))
+        opt = ModelOptions(int(input_uint8), int(trainable_from), int(packed_masks), int(pingpong_grads),
+                           int(speculate_min_elems))
         _check(_lib.ito_model_create_ex(arr, len(layers), batch, NitiParams(target_bits, mu_weight), target_mag,
                                         ctypes.byref(opt), ctypes.byref(h)))
         self._h = h

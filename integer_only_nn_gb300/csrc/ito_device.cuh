@@ -87,6 +87,16 @@ __device__ __forceinline__ uint32_t int_pair_to_bf16x2(int32_t lo, int32_t hi)
     return __byte_perm(__float_as_uint(flo), __float_as_uint(fhi), 0x7632);
 }
 
+// 0xff in each byte of g that is positive as a signed int8, 0x00 in the others. Bit 7
+// of ((g & 0x7f7f7f7f) + 0x7f7f7f7f) is set in a byte exactly when its low seven bits
+// are not all zero (0x7f + 0x7f = 0xfe: no carry reaches the next byte); a positive
+// byte is one of those with its sign bit clear.
+__device__ __forceinline__ uint32_t bytes_positive_mask(uint32_t g)
+{
+    const uint32_t pos = ((g & 0x7f7f7f7fu) + 0x7f7f7f7fu) & ~g & 0x80808080u;
+    return (pos >> 7) * 0xffu;
+}
+
 // ------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)

@@ -619,32 +619,38 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
                 // gate is closed, written over the staged gate tile (each lane reads and
                 // rewrites only its own row's 16-byte chunks), then stored as one 32 x 128 int8
                 // box and two 32 x 64 bf16 boxes; no int32 result
-                if (!fz.gate) {
+                // round half up as ((y >> (s - 1)) + 1) >> 1 (= floor((y + 2^(s-1)) / 2^s), and no
+                // addition that could overflow), the identity for s = 0; then the int8 (or ReLU)
+                // range; four results to a word
+                const int sh1 = sp > 0 ? sp - 1 : 0, rnd = sp > 0 ? 1 : 0;
+                const int qlo = fz.relu ? 0 : -128;
+                uint32_t q8w[HALF / 4];      // the 128 int8 results, packed four to a word
+#pragma unroll
+                for (int k = 0; k < HALF / 4; ++k) {
+                    int32_t q[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) q[b] = min(max(((acc[4 * k + b] >> sh1) + rnd) >> rnd, qlo), 127);
+                    q8w[k] = __byte_perm(__byte_perm((uint32_t)q[0], (uint32_t)q[1], 0x0040),
+                                         __byte_perm((uint32_t)q[2], (uint32_t)q[3], 0x0040), 0x5410);
+                }
+                if (fz.gate) {
+                    // zero where the staged gate byte is not positive
+#pragma unroll
+                    for (int j = 0; j < HALF / 16; ++j) {
+                        const uint4 gv = ld_shared_v4(stg_row + ((j ^ (lane & 7)) << 4));
+                        q8w[4 * j] &= bytes_positive_mask(gv.x);
+                        q8w[4 * j + 1] &= bytes_positive_mask(gv.y);
+                        q8w[4 * j + 2] &= bytes_positive_mask(gv.z);
+                        q8w[4 * j + 3] &= bytes_positive_mask(gv.w);
+                    }
+                } else {
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                 }
-                uint32_t q8w[HALF / 4];      // the 128 int8 results, packed four to a word
 #pragma unroll
-                for (int j = 0; j < HALF / 16; ++j) {
-                    const uint32_t saddr = stg_row + ((j ^ (lane & 7)) << 4);
-                    uint4 gv = make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u);
-                    if (fz.gate) gv = ld_shared_v4(saddr);
-                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t packed = 0;
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            int32_t q = sat8(rhu32(acc[j * 16 + 4 * k + b], sp));
-                            if (fz.relu) q = max(q, 0);
-                            if ((int8_t)(gw[k] >> (8 * b)) <= 0) q = 0;
-                            packed |= ((uint32_t)q & 0xffu) << (8 * b);
-                        }
-                        q8w[4 * j + k] = packed;
-                    }
-                    st_shared_v4(saddr, (int32_t)q8w[4 * j], (int32_t)q8w[4 * j + 1], (int32_t)q8w[4 * j + 2],
-                                 (int32_t)q8w[4 * j + 3]);
-                }
+                for (int j = 0; j < HALF / 16; ++j)
+                    st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), (int32_t)q8w[4 * j], (int32_t)q8w[4 * j + 1],
+                                 (int32_t)q8w[4 * j + 2], (int32_t)q8w[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

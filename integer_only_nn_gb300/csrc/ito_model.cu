@@ -419,12 +419,13 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         // activation and bf16 copy) and of the delta propagation (the gated delta below); not
         // with bit-packed masks, static requantisation, or shared (ping-pong) delta buffers
         const bool plain = !m->opt.packed_masks && !m->opt.pingpong_grads;
+        const int64_t spec_min = m->opt.speculate_min_elems > 0 ? m->opt.speculate_min_elems : (int64_t)1 << 22;
         L.pf_spec = L.pf;
         L.pd_spec = L.pd;
-        if (plain && !conv && !L.static_q && L.ab)
+        if (plain && !conv && !L.static_q && L.ab && L.rows_out * L.OC >= spec_min)
             ITO_TRY(gemm_plan_fuse_requant(&L.pf_spec, m->pred_y(l), L.relu ? 1 : 0, nullptr, 0, L.a8, L.OC, L.ab,
                                            L.lda));
-        if (plain && !conv && L.has_dgrad && !(l == m->n_conv && m->has_pool)) {
+        if (plain && !conv && L.has_dgrad && !(l == m->n_conv && m->has_pool) && L.rows_in * L.IC >= spec_min) {
             const MLayer& prev = m->L[l - 1];
             if (prev.kind != ITO_LAYER_CONV3X3_RELU)
                 ITO_TRY(gemm_plan_fuse_requant(&L.pd_spec, m->pred_d(l), 0, prev.relu ? prev.a8 : nullptr, L.IC,

@@ -36,7 +36,7 @@ def import_ito():
 class GpuRun:
     """A CUDA model of a seeded mlp/cnn workload, stepped one batch at a time."""
 
-    def __init__(self, workload, batch=None, packed_masks=False, pingpong_grads=False):
+    def __init__(self, workload, batch=None, packed_masks=False, pingpong_grads=False, speculate_min_elems=0):
         import torch
         self.torch = torch
         self.ito = import_ito()
@@ -44,7 +44,7 @@ class GpuRun:
         self.batch = batch or workload.batch
         self.model = self.ito.Model(self.ito.layers_for(workload), self.batch, input_uint8=workload.input_uint8,
                                     trainable_from=workload.trainable_from, packed_masks=packed_masks,
-                                    pingpong_grads=pingpong_grads)
+                                    pingpong_grads=pingpong_grads, speculate_min_elems=speculate_min_elems)
         self.pingpong = pingpong_grads
         self.n_layers = self.model.n_weight_layers
         for l, W in enumerate(si.make_weights(workload)):

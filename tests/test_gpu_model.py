@@ -123,7 +123,8 @@ def test_speculation_gives_identical_steps(index, steps):
     w = si.by_name(index)
     runs = []
     for on in (False, True):
-        g = GpuRun(w)
+        # every contraction that can speculate does, however small its output
+        g = GpuRun(w, speculate_min_elems=1)
         g.model.set_speculation(on)
         runs.append(g)
     nl = runs[0].n_layers
@@ -174,7 +175,7 @@ def test_mispredicted_shift_relaunch_matches_oracle(index, steps, route):
     and bf16 outputs; every tensor and scalar still matches the oracle."""
     import torch
     w = si.by_name(index)
-    g = GpuRun(w)
+    g = GpuRun(w, speculate_min_elems=1)
     assert g.model.speculation()
     nl = g.n_layers
     weights = si.make_weights(w)
@@ -199,3 +200,20 @@ def test_mispredicted_shift_relaunch_matches_oracle(index, steps, route):
             assert (pred[act] != last[act]).any(), t
             assert np.array_equal(redo[act], np.where(pred[act] == last[act], 0, last[act] + 1)), t
     assert g.ito.ito_get_error() == 0
+
+
+def test_speculation_covers_large_contractions_only():
+    """By default only contractions with at least 2^22 output elements
+    speculate: none of the 784-1024x3-10 MLP (batch 256), all the 4096-wide
+    forward and delta-propagation ones of the batch-8192 MLP (not its
+    1000-wide logits, whose row is not a multiple of 16 bytes)."""
+    g = GpuRun(si.by_name(1))
+    nl = g.n_layers
+    assert (g.model.tensor("spec").cpu().numpy()[4 * nl: 6 * nl] == 0).all()
+    assert g.model.overlap() == 1
+    g = GpuRun(si.by_name(3))
+    nl = g.n_layers
+    used = g.model.tensor("spec").cpu().numpy()[4 * nl: 6 * nl]
+    assert list(used[:nl]) == [1, 1, 1, 1, 0]
+    assert list(used[nl:]) == [0, 1, 1, 1, 1]
+    assert g.model.overlap() == 0
