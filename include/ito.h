@@ -452,6 +452,18 @@ int ito_model_get_speculation(const ito_model *m, int *enabled);
 int ito_train_step_host(ito_model *m, const int8_t *x_host, const int32_t *labels_host,
                         int32_t *stats_host, void *stream);
 
+/* The host-buffer step without waiting, for a pipeline of steps: the copy of x_host and
+ * labels_host goes on a model-owned copy stream into one of two model-owned device input
+ * buffers (alternating from call to call, after the step that last read that buffer),
+ * the step runs on `stream` after the copy, and the stats array (ito_model_num_stats
+ * int32) is copied to stats_host (may be NULL) on `stream`. So the copy of the next
+ * call's batch overlaps this step. The host buffers must be pinned for the copies to
+ * be asynchronous and must not change until the copy is done (synchronising `stream`
+ * after the next call, or after this one, is enough); stats_host holds this step's
+ * statistics once `stream` has passed it. Errors: ITO_ERR_ARG, ITO_ERR_CUDA. */
+int ito_train_step_host_async(ito_model *m, const int8_t *x_host, const int32_t *labels_host,
+                              int32_t *stats_host, void *stream);
+
 /* Forward pass only ("INTODT_Infer"): writes the int8 logits [batch][C]. */
 int ito_infer(ito_model *m, const int8_t *x, int8_t *logits, void *stream);
 

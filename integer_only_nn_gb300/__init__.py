@@ -81,6 +81,7 @@ _SIGS = {
     "ito_model_num_stats": (_I, [_P]),
     "ito_train_step": (_I, [_P, _P, _P, _P]),
     "ito_train_step_host": (_I, [_P, _P, _P, _P, _P]),
+    "ito_train_step_host_async": (_I, [_P, _P, _P, _P, _P]),
     "ito_infer": (_I, [_P, _P, _P, _P]),
     "ito_model_save": (_I, [_P, ctypes.c_char_p]),
     "ito_model_load": (_I, [_P, ctypes.c_char_p]),
@@ -464,6 +465,12 @@ class Model:
         """Host (pinned) torch tensors in, stats out; synchronises."""
         _check(_lib.ito_train_step_host(self._h, _ptr(x_host), _ptr(labels_host), _ptr(stats_host),
                                         _stream(stream)))
+
+    def train_step_host_async(self, x_host, labels_host, stats_host=None, stream=None):
+        """Host (pinned) torch tensors in, no wait: the next call's input copy overlaps this
+        step; synchronise the stream before reading stats_host or reusing the buffers."""
+        _check(_lib.ito_train_step_host_async(self._h, _ptr(x_host), _ptr(labels_host), _ptr(stats_host),
+                                              _stream(stream)))
 
     def infer(self, x, logits, stream=None):
         _check(_lib.ito_infer(self._h, _ptr(x), _ptr(logits), _stream(stream)))

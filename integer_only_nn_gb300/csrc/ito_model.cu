@@ -83,6 +83,13 @@ struct ito_model {
     // input
     int8_t* x8 = nullptr;        // model-owned input (host-path steps)
     int32_t* labels = nullptr;
+    // pipelined host-path steps: a second input buffer pair, the copy stream, and per buffer
+    // "copied" / "read by its step" events
+    int8_t* x8b = nullptr;
+    int32_t* labels_b = nullptr;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_copied[2] = {nullptr, nullptr}, ev_consumed[2] = {nullptr, nullptr};
+    int64_t async_steps = 0;
     uint16_t* xb = nullptr;      // bf16 copy of a Linear first layer's input
     int64_t ldx = 0;
     // pooling
@@ -301,6 +308,8 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
     // allocations
     ITO_TRY(m->alloc(&m->x8, (size_t)B * m->in_features));
     ITO_TRY(m->alloc(&m->labels, (size_t)B));
+    ITO_TRY(m->alloc(&m->x8b, (size_t)B * m->in_features));
+    ITO_TRY(m->alloc(&m->labels_b, (size_t)B));
     m->n_stats = nl * ST_PER_LAYER + 2;
     ITO_TRY(m->alloc(&m->stats, (size_t)m->n_stats));
     ITO_TRY(m->alloc(&m->discard_max, 1));
@@ -484,8 +493,13 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
             if (L.has_dgrad && !L.pd_spec.rq_pred) every_delta_speculates = false;
         m->overlap = every_delta_speculates ? 0 : 1;
     }
-    if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess)
-        return set_error(ITO_ERR_CUDA, "side stream creation failed");
+    if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "stream creation failed");
+    for (int i = 0; i < 2; ++i)
+        if (cudaEventCreateWithFlags(&m->ev_copied[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&m->ev_consumed[i], cudaEventDisableTiming) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "event creation failed");
     for (int i = 0; i < 2 + 3 * nl; ++i) {
         cudaEvent_t e;
         if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
@@ -696,7 +710,12 @@ int ito_model_destroy(ito_model* m)
     drop_graphs(m);
     for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
     for (cudaEvent_t e : m->sync_ev) cudaEventDestroy(e);
+    for (int i = 0; i < 2; ++i) {
+        if (m->ev_copied[i]) cudaEventDestroy(m->ev_copied[i]);
+        if (m->ev_consumed[i]) cudaEventDestroy(m->ev_consumed[i]);
+    }
     if (m->side) cudaStreamDestroy(m->side);
+    if (m->copy_stream) cudaStreamDestroy(m->copy_stream);
     for (void* p : m->allocs) cudaFree(p);
     delete m;
     return ITO_OK;
@@ -985,6 +1004,34 @@ int ito_train_step_host(ito_model* m, const int8_t* x_host, const int32_t* label
     }
     e = cudaStreamSynchronize(s);
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "step: %s", cudaGetErrorString(e));
+}
+
+int ito_train_step_host_async(ito_model* m, const int8_t* x_host, const int32_t* labels_host, int32_t* stats_host,
+                              void* stream)
+{
+    if (!m || !x_host || !labels_host) return set_error(ITO_ERR_ARG, "NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int i = (int)(m->async_steps & 1);
+    int8_t* xd = i ? m->x8b : m->x8;
+    int32_t* ld = i ? m->labels_b : m->labels;
+    // the copy waits for the step that last read this buffer, and the step for the copy
+    cudaError_t e = cudaStreamWaitEvent(m->copy_stream, m->ev_consumed[i], 0);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(xd, x_host, (size_t)m->batch * m->in_features, cudaMemcpyHostToDevice, m->copy_stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ld, labels_host, sizeof(int32_t) * m->batch, cudaMemcpyHostToDevice, m->copy_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(m->ev_copied[i], m->copy_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, m->ev_copied[i], 0);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "input copy: %s", cudaGetErrorString(e));
+    ITO_TRY(ito_train_step(m, xd, ld, stream));
+    if (stats_host) {
+        e = cudaMemcpyAsync(stats_host, m->stats, sizeof(int32_t) * m->n_stats, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "stats copy: %s", cudaGetErrorString(e));
+    }
+    e = cudaEventRecord(m->ev_consumed[i], s);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "event: %s", cudaGetErrorString(e));
+    ++m->async_steps;
+    return ITO_OK;
 }
 
 int ito_infer(ito_model* m, const int8_t* x, int8_t* logits, void* stream)

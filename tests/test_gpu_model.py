@@ -217,3 +217,33 @@ def test_speculation_covers_large_contractions_only():
     assert list(used[:nl]) == [1, 1, 1, 1, 0]
     assert list(used[nl:]) == [0, 1, 1, 1, 1]
     assert g.model.overlap() == 0
+
+
+@pytest.mark.parametrize("index,graphs", [(1, True), (0, False), (3, True)])
+def test_pipelined_host_steps_match_device_steps(index, graphs):
+    """ito_train_step_host_async (input copies on the model's copy stream into two
+    alternating buffers, overlapping the previous step) trains exactly as steps on device
+    inputs: the same weights and activations after every step, and the stats copied back
+    are the step's."""
+    import torch
+    w = si.by_name(index)
+    a, b = GpuRun(w), GpuRun(w)
+    stream = torch.cuda.Stream()
+    a.model.use_graphs(graphs)
+    batches = [si.make_batch(w, t) for t in range(5)]
+    xs_h = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x, _ in batches]
+    ls_h = [torch.from_numpy(np.ascontiguousarray(lab)).pin_memory() for _, lab in batches]
+    st_h = torch.zeros(a.model.num_stats(), dtype=torch.int32).pin_memory()
+    for t in range(len(batches)):
+        a.model.train_step_host_async(xs_h[t], ls_h[t], st_h, stream=stream)
+        if t % 2 == 1:
+            stream.synchronize()    # sometimes wait, sometimes queue two steps
+    stream.synchronize()
+    for t in range(len(batches)):
+        b.step(t)
+    names = [n for n in a.names(("a", "e", "w")) if n in b.names(("a", "e", "w"))]
+    for n in names:
+        assert np.array_equal(a.tensor(n), b.tensor(n)), n
+    stats_b = b.model.tensor("stats").cpu().numpy()
+    assert np.array_equal(st_h.numpy(), stats_b)
+    assert a.ito.ito_get_error() == 0
