@@ -36,6 +36,15 @@ int launch_grid_blocks(int64_t work_items, int threads)
 
 static inline bool aligned(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Offset of element i of a [rows][cols] tensor in a copy with row pitch ld; no division when
+// the copy is unpadded (ld == cols, the same for every thread of a launch).
+__device__ __forceinline__ int64_t pitched(int64_t i, int64_t cols, int64_t ld)
+{
+    if (ld == cols) return i;
+    const int64_t r = i / cols;
+    return r * ld + (i - r * cols);
+}
+
 // ------------------------------------------------------------- conversion
 
 __global__ void k_i8_to_bf16_v8(const int8_t* __restrict__ src, int64_t rows, int64_t cols,
@@ -45,15 +54,15 @@ __global__ void k_i8_to_bf16_v8(const int8_t* __restrict__ src, int64_t rows, in
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i0 = g << 3;
-        const int64_t r = i0 / cols, c = i0 - r * cols;
+        const int64_t off = pitched(i0, cols, ldd);
         const uint2 v = __ldg(reinterpret_cast<const uint2*>(src + i0));
         const int8_t* b = reinterpret_cast<const int8_t*>(&v);
         uint4 o;
         uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            ow[i] = (uint32_t)int_to_bf16_bits(b[2 * i]) | ((uint32_t)int_to_bf16_bits(b[2 * i + 1]) << 16);
-        *reinterpret_cast<uint4*>(dst + r * ldd + c) = o;
+            ow[i] = int_pair_to_bf16x2(b[2 * i], b[2 * i + 1]);
+        *reinterpret_cast<uint4*>(dst + off) = o;
     }
 }
 
@@ -62,8 +71,7 @@ __global__ void k_i8_to_bf16_1(const int8_t* __restrict__ src, int64_t rows, int
 {
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / cols, c = i - r * cols;
-        dst[r * ldd + c] = int_to_bf16_bits(src[i]);
+        dst[pitched(i, cols, ldd)] = int_to_bf16_bits(src[i]);
     }
 }
 
@@ -86,15 +94,15 @@ __global__ void k_u8_to_bf16_v8(const uint8_t* __restrict__ src, int64_t rows, i
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i0 = g << 3;
-        const int64_t r = i0 / cols, c = i0 - r * cols;
+        const int64_t off = pitched(i0, cols, ldd);
         const uint2 v = __ldg(reinterpret_cast<const uint2*>(src + i0));
         const uint8_t* b = reinterpret_cast<const uint8_t*>(&v);
         uint4 o;
         uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            ow[i] = (uint32_t)int_to_bf16_bits(b[2 * i]) | ((uint32_t)int_to_bf16_bits(b[2 * i + 1]) << 16);
-        *reinterpret_cast<uint4*>(dst + r * ldd + c) = o;
+            ow[i] = int_pair_to_bf16x2(b[2 * i], b[2 * i + 1]);
+        *reinterpret_cast<uint4*>(dst + off) = o;
     }
 }
 
@@ -103,8 +111,7 @@ __global__ void k_u8_to_bf16_1(const uint8_t* __restrict__ src, int64_t rows, in
 {
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / cols, c = i - r * cols;
-        dst[r * ldd + c] = int_to_bf16_bits(src[i]);
+        dst[pitched(i, cols, ldd)] = int_to_bf16_bits(src[i]);
     }
 }
 
@@ -170,11 +177,10 @@ __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_
         if (mask_out) mask_out[g] = (uint8_t)mbits;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            qb[i] = (uint32_t)int_to_bf16_bits(q8[2 * i]) | ((uint32_t)int_to_bf16_bits(q8[2 * i + 1]) << 16);
+            qb[i] = int_pair_to_bf16x2(q8[2 * i], q8[2 * i + 1]);
         *reinterpret_cast<uint2*>(out8 + i0) = *reinterpret_cast<const uint2*>(q8);
         if (outb) {
-            const int64_t r = i0 / cols, c = i0 - r * cols;
-            *reinterpret_cast<uint4*>(outb + r * ldb + c) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
+            *reinterpret_cast<uint4*>(outb + pitched(i0, cols, ldb)) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
         }
     }
 }
@@ -194,8 +200,7 @@ __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t
         const int32_t q = requant_one(Y[i], s, relu, gate ? gate[i] > 0 : 1);
         out8[i] = (int8_t)q;
         if (outb) {
-            const int64_t r = i / cols, c = i - r * cols;
-            outb[r * ldb + c] = int_to_bf16_bits(q);
+            outb[pitched(i, cols, ldb)] = int_to_bf16_bits(q);
         }
     }
 }
@@ -294,7 +299,7 @@ __global__ void k_requant_static_v8(const int32_t* __restrict__ Y, int64_t rows,
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            qb[i] = (uint32_t)int_to_bf16_bits(q8[2 * i]) | ((uint32_t)int_to_bf16_bits(q8[2 * i + 1]) << 16);
+            qb[i] = int_pair_to_bf16x2(q8[2 * i], q8[2 * i + 1]);
         *reinterpret_cast<uint2*>(out8 + i0) = *reinterpret_cast<const uint2*>(q8);
         if (outb) *reinterpret_cast<uint4*>(outb + r * ldb + c) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
         if (mask_out) mask_out[g] = (uint8_t)mbits;
@@ -430,11 +435,10 @@ __global__ void k_niti_update_v8(int8_t* __restrict__ W, uint16_t* __restrict__ 
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            wb[i] = (uint32_t)int_to_bf16_bits(w8[2 * i]) | ((uint32_t)int_to_bf16_bits(w8[2 * i + 1]) << 16);
+            wb[i] = int_pair_to_bf16x2(w8[2 * i], w8[2 * i + 1]);
         *reinterpret_cast<uint2*>(W + i0) = *reinterpret_cast<const uint2*>(w8);
         if (Wb) {
-            const int64_t r = i0 / cols, c = i0 - r * cols;
-            *reinterpret_cast<uint4*>(Wb + r * ldb + c) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+            *reinterpret_cast<uint4*>(Wb + pitched(i0, cols, ldb)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
         }
     }
     if (d_nonzero) count_nonzero(cnt, d_nonzero);
@@ -460,8 +464,7 @@ __global__ void k_niti_update_1(int8_t* __restrict__ W, uint16_t* __restrict__ W
         const int8_t nw = (int8_t)sat8(W[i] - dw);
         W[i] = nw;
         if (Wb) {
-            const int64_t r = i / cols, c = i - r * cols;
-            Wb[r * ldb + c] = int_to_bf16_bits(nw);
+            Wb[pitched(i, cols, ldb)] = int_to_bf16_bits(nw);
         }
     }
     if (d_nonzero) count_nonzero(cnt, d_nonzero);
