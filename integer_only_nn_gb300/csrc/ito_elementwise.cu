@@ -404,6 +404,34 @@ __device__ __forceinline__ void count_nonzero(uint32_t cnt, uint32_t* d_nonzero)
     block_atomic_add(d_nonzero, cnt);
 }
 
+// Steps 3-5 for eight consecutive weights from their loaded gradients and weights:
+// stores the new weights and their bf16 copy, returns how many moved.
+__device__ __forceinline__ uint32_t niti_update_group(int8_t* __restrict__ W, uint16_t* __restrict__ Wb, int64_t ldb,
+                                                      int64_t cols, int64_t i0, int4 g0, int4 g1, uint2 wold, int s,
+                                                      int ws)
+{
+    const int32_t gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    int8_t w8[8];
+    *reinterpret_cast<uint2*>(w8) = wold;
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int32_t dw = niti_step_delta(gv[i], s, ws);
+        cnt += dw != 0;
+        w8[i] = (int8_t)sat8(w8[i] - dw);          // Step 5
+    }
+    *reinterpret_cast<uint2*>(W + i0) = *reinterpret_cast<const uint2*>(w8);
+    if (Wb) {
+        uint32_t wb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wb[i] = int_pair_to_bf16x2(w8[2 * i], w8[2 * i + 1]);
+        *reinterpret_cast<uint4*>(Wb + pitched(i0, cols, ldb)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    }
+    return cnt;
+}
+
+// Two groups of eight per thread and iteration: both groups' loads are issued before either
+// is computed, so that more bytes are in flight per thread.
 __global__ void k_niti_update_v8(int8_t* __restrict__ W, uint16_t* __restrict__ Wb, int64_t ldb,
                                  const int32_t* __restrict__ G, int64_t rows, int64_t cols,
                                  const uint32_t* __restrict__ d_max, int target_bits, int mu_weight,
@@ -418,28 +446,22 @@ __global__ void k_niti_update_v8(int8_t* __restrict__ W, uint16_t* __restrict__ 
     }
     uint32_t cnt = 0;
     const int64_t groups = rows * (cols >> 3);
-    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
-         g += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i0 = g << 3;
-        const int4 g0 = __ldcs(reinterpret_cast<const int4*>(G + i0));
-        const int4 g1 = __ldcs(reinterpret_cast<const int4*>(G + i0 + 4));
-        const int32_t gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        int8_t w8[8];
-        *reinterpret_cast<uint2*>(w8) = *reinterpret_cast<const uint2*>(W + i0);
-        uint32_t wb[4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int32_t dw = niti_step_delta(gv[i], s, ws);
-            cnt += dw != 0;
-            w8[i] = (int8_t)sat8(w8[i] - dw);          // Step 5
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups; g += 2 * stride) {
+        const int64_t gb = g + stride;
+        const int64_t ia = g << 3, ib = gb << 3;
+        const int4 a0 = __ldcs(reinterpret_cast<const int4*>(G + ia));
+        const int4 a1 = __ldcs(reinterpret_cast<const int4*>(G + ia + 4));
+        const uint2 wa = *reinterpret_cast<const uint2*>(W + ia);
+        int4 b0 = make_int4(0, 0, 0, 0), b1 = b0;
+        uint2 wb = make_uint2(0, 0);
+        if (gb < groups) {
+            b0 = __ldcs(reinterpret_cast<const int4*>(G + ib));
+            b1 = __ldcs(reinterpret_cast<const int4*>(G + ib + 4));
+            wb = *reinterpret_cast<const uint2*>(W + ib);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            wb[i] = int_pair_to_bf16x2(w8[2 * i], w8[2 * i + 1]);
-        *reinterpret_cast<uint2*>(W + i0) = *reinterpret_cast<const uint2*>(w8);
-        if (Wb) {
-            *reinterpret_cast<uint4*>(Wb + pitched(i0, cols, ldb)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
-        }
+        cnt += niti_update_group(W, Wb, ldb, cols, ia, a0, a1, wa, s, ws);
+        if (gb < groups) cnt += niti_update_group(W, Wb, ldb, cols, ib, b0, b1, wb, s, ws);
     }
     if (d_nonzero) count_nonzero(cnt, d_nonzero);
 }
