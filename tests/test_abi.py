@@ -107,3 +107,38 @@ def test_host_side_argument_errors_new_entry_points():
     assert L.ito_bdfp16_to_float(None, dummy, 4, 4, 2, dummy, None) == ito.ITO_ERR_ARG
     assert L.ito_bdfp16_linear_fwd_f32(dummy, dummy, dummy, dummy, 4, 4, 4, 64, None, 0, dummy,
                                        None) == ito.ITO_ERR_ARG
+
+
+def test_host_side_argument_errors_model_controls():
+    """The model's stream, speculation and pipelining controls and the DFP16
+    model's profiling reject NULL arguments on the host (no GPU needed)."""
+    _lib_path()
+    import integer_only_nn_gb300 as ito
+    L = ito._lib
+    dummy = ctypes.c_void_p(256)
+    flag = ctypes.c_int(-7)
+    assert L.ito_model_get_speculation(None, ctypes.byref(flag)) == ito.ITO_ERR_ARG
+    assert L.ito_model_get_overlap(None, ctypes.byref(flag)) == ito.ITO_ERR_ARG
+    assert flag.value == -7                       # nothing written on error
+    assert L.ito_model_set_speculation(None, 1) == ito.ITO_ERR_ARG
+    assert L.ito_model_set_overlap(None, 0) == ito.ITO_ERR_ARG
+    assert L.ito_train_step_host_async(None, dummy, dummy, None, None) == ito.ITO_ERR_ARG
+    assert L.ito_train_step_host(None, dummy, dummy, None, None) == ito.ITO_ERR_ARG
+    assert L.ito_dfp16_model_profile(None, 1) == ito.ITO_ERR_ARG
+    ms = (ctypes.c_double * 4)()
+    n = (ctypes.c_int64 * 4)()
+    assert L.ito_dfp16_model_profile_read(None, ms, ms, n) == ito.ITO_ERR_ARG
+    assert L.ito_dfp16_model_kernels_per_step(None) == 0
+    assert L.ito_model_kernels_per_step(None) == 0
+
+
+def test_model_options_struct_matches_header():
+    """The binding's ModelOptions has the header's fields in order (int32 each)."""
+    import re
+    text = open(os.path.join(ROOT, "include", "ito.h")).read()
+    body = re.search(r"typedef struct ito_model_options \{(.*?)\} ito_model_options;", text, re.S).group(1)
+    fields = re.findall(r"int32_t\s+(\w+);", body)
+    _lib_path()
+    import integer_only_nn_gb300 as ito
+    assert [f for f, _ in ito.ModelOptions._fields_] == fields
+    assert ctypes.sizeof(ito.ModelOptions) == 4 * len(fields)
