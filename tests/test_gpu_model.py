@@ -247,3 +247,28 @@ def test_pipelined_host_steps_match_device_steps(index, graphs):
     stats_b = b.model.tensor("stats").cpu().numpy()
     assert np.array_equal(st_h.numpy(), stats_b)
     assert a.ito.ito_get_error() == 0
+
+
+@pytest.mark.parametrize("spec_min", [0, 1])
+def test_infer_matches_oracle_forward(spec_min):
+    """ito_infer (the forward pass alone, "INTODT_Infer") after a few training steps
+    gives the oracle's logits for the current weights, with the speculating forward
+    contractions (spec_min = 1: every eligible one, however small) and without."""
+    import torch
+    w = si.by_name(1)
+    g = GpuRun(w, speculate_min_elems=spec_min)
+    weights = si.make_weights(w)
+    for t in range(3):
+        rec = _oracle_step(w, weights, t, "loops")
+        g.step(t)
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+    x, labels = si.make_batch(w, 7)
+    logits = torch.empty((w.batch, w.dims[-1]), dtype=torch.int8, device="cuda")
+    g.model.infer(torch.from_numpy(np.ascontiguousarray(x)).cuda(), logits)
+    torch.cuda.synchronize()
+    ref = O.mlp_step(weights, x, labels, route="loops")
+    nl = len(weights)
+    assert np.array_equal(logits.cpu().numpy(), ref["a%d" % (nl - 1)])
+    for l in range(nl):
+        assert np.array_equal(g.tensor("a%d" % l), ref["a%d" % l]), l
+    assert g.ito.ito_get_error() == 0
