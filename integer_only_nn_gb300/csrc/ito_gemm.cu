@@ -1060,13 +1060,14 @@ static int split_count(int M, int N, int K)
     return (num_kb + per - 1) / per;
 }
 
-static bool pair_eligible(int M, int N, int splits)
+static bool pair_eligible(int M, int N, int splits, int min_pair_tiles = 1)
 {
     static const int pair_env = [] {
         const char* v = getenv("ITO_GEMM_PAIR");
         return v ? atoi(v) : 1;
     }();
-    return pair_env != 0 && M >= 256 && N >= 256 && splits == 1;
+    const int pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    return pair_env != 0 && M >= 256 && N >= 256 && splits == 1 && pair_tiles >= min_pair_tiles;
 }
 
 size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc)
@@ -1081,7 +1082,8 @@ size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc)
 }
 
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
-              int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws, size_t split_ws_bytes, int chunk_terms)
+              int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws, size_t split_ws_bytes, int chunk_terms,
+              int min_pair_tiles)
 {
     if (chunk_terms < 64 || chunk_terms > kExactChunk || chunk_terms % 64)
         return set_error(ITO_ERR_ARG, "gemm: exact chunk must be a multiple of 64 up to %d", kExactChunk);
@@ -1116,7 +1118,7 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
         p->split_ws = split_ws;
         p->split_stride = (int64_t)M * ldc;
     }
-    p->pair = pair_eligible(M, N, p->splits);
+    p->pair = pair_eligible(M, N, p->splits, min_pair_tiles);
     // tiles are rastered in groups of `group` row tiles; ITO_GEMM_GROUP overrides (tuning)
     static const int group_env = [] {
         const char* v = getenv("ITO_GEMM_GROUP");

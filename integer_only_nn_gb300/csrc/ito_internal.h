@@ -152,9 +152,11 @@ int launch_dfp_set_bits(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, int
 // split_ws (optional): room for split-K partials; without it (or when too
 // small) the contraction is not split.
 // chunk_terms: K terms per exact fp32 chunk (a multiple of 64, at most kExactChunk).
+// min_pair_tiles: the CTA-pair kernel only when the output has at least this many 256 x 256
+// tiles (below that the single-CTA kernel, with more CTAs and no cluster launch, is faster).
 int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool b_mn, int M, int N, int K,
               int32_t* C, int64_t ldc, uint32_t* d_max, int32_t* split_ws = nullptr, size_t split_ws_bytes = 0,
-              int chunk_terms = kExactChunk);
+              int chunk_terms = kExactChunk, int min_pair_tiles = 1);
 // bytes of split-K partials gemm_plan would use for this contraction (0: no split)
 size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc);
 // Turns on the speculative requantisation of a planned pair-kernel contraction:

@@ -413,22 +413,31 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         const int M = (int)L.rows_out;
         // a UINT8 input makes products up to 255 * 128: shorter exact chunks
         const int chunk = (l == 0 && m->opt.input_uint8) ? kExactChunkU8 : kExactChunk;
+        // The CTA-pair kernel only for contractions of at least 64 pair tiles: on fewer the
+        // single-CTA kernel is faster (784-1024x3-10 MLP, batch 256: 0.142 against 0.153 ms
+        // per step; the CNN 0.385 against 0.395 ms). A model that asks for speculative
+        // requantisation below its default size gets the pair kernel there (the requantising
+        // epilogue is the pair kernel's).
+        const int64_t spec_min = m->opt.speculate_min_elems > 0 ? m->opt.speculate_min_elems : (int64_t)1 << 22;
+        const bool spec_small = m->opt.speculate_min_elems > 0;
+        constexpr int kMinPairTiles = 64;
+        const int pair_f = spec_small && L.rows_out * L.OC >= spec_min ? 1 : kMinPairTiles;
+        const int pair_d = spec_small && L.rows_in * L.IC >= spec_min ? 1 : kMinPairTiles;
         // forward: Y[m][oc] = sum_k in[m][k] W[oc][k]
         ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax, m->split_ws,
-                          m->split_ws_bytes, chunk));
+                          m->split_ws_bytes, chunk, pair_f));
         // delta propagation: D[m][k] = sum_oc e[m][oc] W[oc][k]; for a conv this is the
         // patch-space delta, whose max is not the NITI max (col2im takes that)
         if (L.has_dgrad)
             ITO_TRY(gemm_plan(&L.pd, ev, false, wv, true, M, (int)L.K, L.OC, conv ? L.dcol : L.d32, L.K,
-                              conv ? m->discard_max : dmax, m->split_ws, m->split_ws_bytes));
+                              conv ? m->discard_max : dmax, m->split_ws, m->split_ws_bytes, kExactChunk, pair_d));
         // weight gradient: G[oc][k] = sum_m e[m][oc] in[m][k]
         ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax, m->split_ws,
-                          m->split_ws_bytes, chunk));
+                          m->split_ws_bytes, chunk, kMinPairTiles));
         // speculative requantisation in the epilogues of the forward contraction (its ReLU'd
         // activation and bf16 copy) and of the delta propagation (the gated delta below); not
         // with bit-packed masks, static requantisation, or shared (ping-pong) delta buffers
         const bool plain = !m->opt.packed_masks && !m->opt.pingpong_grads;
-        const int64_t spec_min = m->opt.speculate_min_elems > 0 ? m->opt.speculate_min_elems : (int64_t)1 << 22;
         L.pf_spec = L.pf;
         L.pd_spec = L.pd;
         if (plain && !conv && !L.static_q && L.ab && L.rows_out * L.OC >= spec_min)
