@@ -618,6 +618,17 @@ int ito_dfp16_model_read_stats(const ito_dfp16_model *m, int64_t *host_out, int 
  * [batch][dims[0]] with exponent exp_x. */
 int ito_dfp16_train_step(ito_dfp16_model *m, const int16_t *x, int32_t exp_x, void *stream);
 
+/* The DFP16 step from a host buffer without waiting, for a pipeline of steps: x_host (int16
+ * mantissas [batch][in], exponent exp_x) is copied on a model-owned copy stream into one of
+ * two model-owned device input buffers (alternating from call to call, after the step that
+ * last read that buffer), the step runs on `stream` after the copy, and the statistics, in
+ * the layout of ito_dfp16_model_read_stats (ito_dfp16_model_num_stats int64), are copied to
+ * stats_host (may be NULL) on `stream`. The copy of the next call's batch overlaps this
+ * step. Host buffers should be pinned; x_host must not change until `stream` has passed
+ * this step. Errors: ITO_ERR_ARG, ITO_ERR_EXPONENT, ITO_ERR_CUDA. */
+int ito_dfp16_train_step_host_async(ito_dfp16_model *m, const int16_t *x_host, int32_t exp_x,
+                                    int64_t *stats_host, void *stream);
+
 /* ------------------------------------------------------------------------
  * Adaptive precision training on the DFP16 model ("Adaptive Precision
  * Training for Resource Constrained Devices", section III: the Gavg metric of

@@ -102,6 +102,7 @@ _SIGS = {
     "ito_dfp16_model_stat_index": (_I, [_P, ctypes.c_char_p]),
     "ito_dfp16_model_read_stats": (_I, [_P, _P, _I]),
     "ito_dfp16_train_step": (_I, [_P, _P, _I32, _P]),
+    "ito_dfp16_train_step_host_async": (_I, [_P, _P, _I32, _P, _P]),
     "ito_dfp16_model_profile": (_I, [_P, _I]),
     "ito_dfp16_model_profile_read": (_I, [_P, _P, _P, _P]),
     "ito_dfp16_model_kernels_per_step": (_I, [_P]),
@@ -698,6 +699,16 @@ class Dfp16Model:
 
     def train_step(self, x, exp_x, stream=None):
         _check(_lib.ito_dfp16_train_step(self._h, _ptr(x), int(exp_x), _stream(stream)))
+
+    def train_step_host_async(self, x_host, exp_x, stats_host=None, stream=None):
+        """Host (pinned) int16 mantissas in, no wait: the next call's input copy overlaps this
+        step; stats_host (int64, num_stats()) holds the step's statistics once the stream
+        has passed it."""
+        _check(_lib.ito_dfp16_train_step_host_async(self._h, _ptr(x_host), int(exp_x), _ptr(stats_host),
+                                                    _stream(stream)))
+
+    def num_stats(self) -> int:
+        return _lib.ito_dfp16_model_num_stats(self._h)
 
     def profile(self, enable=True):
         _check(_lib.ito_dfp16_model_profile(self._h, int(enable)))

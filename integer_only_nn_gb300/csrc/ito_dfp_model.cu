@@ -92,6 +92,14 @@ struct ito_dfp16_model {
     cudaStream_t side = nullptr;
     std::vector<cudaEvent_t> sync_ev;  // [0] fork, [1] join, per layer: delta propagated, delta ready, wgrad done
     int16_t* x16 = nullptr;
+    // pipelined host-path steps (ito_dfp16_train_step_host_async): a second input buffer, the
+    // copy stream, per buffer "copied" / "read by its step" events, the statistics packed as
+    // ito_dfp16_model_read_stats lays them out
+    int16_t* x16b = nullptr;
+    int64_t* stats_packed = nullptr;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_copied[2] = {nullptr, nullptr}, ev_consumed[2] = {nullptr, nullptr};
+    int64_t async_steps = 0;
     uint16_t *xh = nullptr, *xl = nullptr;
     int64_t ldx = 0;
     int32_t* s32 = nullptr;            // [layers][D_N32] + [ex, ew]
@@ -387,7 +395,12 @@ int ito_dfp16_model_destroy(ito_dfp16_model* m)
     cudaDeviceSynchronize();
     for (cudaEvent_t e : m->sync_ev) cudaEventDestroy(e);
     for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
+    for (int i = 0; i < 2; ++i) {
+        if (m->ev_copied[i]) cudaEventDestroy(m->ev_copied[i]);
+        if (m->ev_consumed[i]) cudaEventDestroy(m->ev_consumed[i]);
+    }
     if (m->side) cudaStreamDestroy(m->side);
+    if (m->copy_stream) cudaStreamDestroy(m->copy_stream);
     for (void* p : m->allocs) cudaFree(p);
     delete m;
     return ITO_OK;
@@ -412,6 +425,8 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
     m->wbits.assign(nl, 16);
     m->ldx = pad8(dims[0]);
     ITO_TRY(m->alloc(&m->x16, (size_t)B * dims[0]));
+    ITO_TRY(m->alloc(&m->x16b, (size_t)B * dims[0]));
+    ITO_TRY(m->alloc(&m->stats_packed, (size_t)nl * (D_N32 + D_N64)));
     ITO_TRY(m->alloc(&m->xh, (size_t)B * m->ldx));
     ITO_TRY(m->alloc(&m->xl, (size_t)B * m->ldx));
     for (int l = 0; l < nl; ++l) {
@@ -474,8 +489,13 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
         return v ? atoi(v) : 1;
     }();
     m->overlap = overlap_env != 0;
-    if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess)
-        return set_error(ITO_ERR_CUDA, "side stream creation failed");
+    if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking) != cudaSuccess)
+        return set_error(ITO_ERR_CUDA, "stream creation failed");
+    for (int i = 0; i < 2; ++i)
+        if (cudaEventCreateWithFlags(&m->ev_copied[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&m->ev_consumed[i], cudaEventDisableTiming) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "event creation failed");
     for (int i = 0; i < 2 + 3 * nl; ++i) {
         cudaEvent_t e;
         if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
@@ -584,6 +604,48 @@ int ito_dfp16_model_read_stats(const ito_dfp16_model* m, int64_t* host_out, int 
         for (int k = 0; k < D_N32; ++k) host_out[l * (D_N32 + D_N64) + k] = a[l * D_N32 + k];
         for (int k = 0; k < D_N64; ++k) host_out[l * (D_N32 + D_N64) + D_N32 + k] = (int64_t)b[l * D_N64 + k];
     }
+    return ITO_OK;
+}
+
+// The statistics in the layout of ito_dfp16_model_read_stats: per layer its D_N32 int32 words
+// (sign-extended), then its D_N64 words.
+__global__ void k_dfp_pack_stats(const int32_t* __restrict__ s32, const unsigned long long* __restrict__ s64, int nl,
+                                 int64_t* __restrict__ out)
+{
+    for (int i = threadIdx.x; i < nl * (D_N32 + D_N64); i += blockDim.x) {
+        const int l = i / (D_N32 + D_N64), k = i - l * (D_N32 + D_N64);
+        out[i] = k < D_N32 ? (int64_t)s32[l * D_N32 + k] : (int64_t)s64[l * D_N64 + (k - D_N32)];
+    }
+}
+
+int ito_dfp16_train_step_host_async(ito_dfp16_model* m, const int16_t* x_host, int32_t exp_x, int64_t* stats_host,
+                                    void* stream)
+{
+    if (!m || !x_host) return set_error(ITO_ERR_ARG, "NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int i = (int)(m->async_steps & 1);
+    int16_t* xd = i ? m->x16b : m->x16;
+    const int nl = (int)m->L.size();
+    // the copy waits for the step that last read this buffer, and the step for the copy
+    cudaError_t e = cudaStreamWaitEvent(m->copy_stream, m->ev_consumed[i], 0);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(xd, x_host, sizeof(int16_t) * m->batch * m->L[0].IC, cudaMemcpyHostToDevice,
+                            m->copy_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(m->ev_copied[i], m->copy_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, m->ev_copied[i], 0);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "input copy: %s", cudaGetErrorString(e));
+    ITO_TRY(ito_dfp16_train_step(m, xd, exp_x, stream));
+    if (stats_host) {
+        k_dfp_pack_stats<<<1, 128, 0, s>>>(m->s32, m->s64, nl, m->stats_packed);
+        e = cudaGetLastError();
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(stats_host, m->stats_packed, sizeof(int64_t) * nl * (D_N32 + D_N64),
+                                cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "stats copy: %s", cudaGetErrorString(e));
+    }
+    e = cudaEventRecord(m->ev_consumed[i], s);
+    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "event: %s", cudaGetErrorString(e));
+    ++m->async_steps;
     return ITO_OK;
 }
 

@@ -1,6 +1,8 @@
 """DFP16 path on the GPU against the CPU oracle: exact int64 limb contractions
 (ragged shapes, extreme mantissas, chunk boundaries), down-conversion with its
 exponent, the integer update, and whole training steps in lockstep."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -227,3 +229,32 @@ def test_dfp_linear_fwd_f32_parity(ito):
     mant, e = ito.ito_dfp16_from_float(y)
     m_ref, e_ref = O.dfp_from_float(O.p64_to_float(P, -29))
     assert int(_h(e)[0]) == e_ref and np.array_equal(_h(mant), m_ref)
+
+
+def test_dfp_model_pipelined_host_steps():
+    """ito_dfp16_train_step_host_async (input copies on the model's copy stream into two
+    alternating buffers, overlapping the previous step) trains as steps on device inputs:
+    the same tensors after the last step, and the statistics copied back (in the layout
+    of ito_dfp16_model_read_stats) are the step's."""
+    import torch
+    w = si.Workload(97, "dfp16_small", "dfp16", 256, dims=(512, 384, 256), sigma=4096.0, lim=32767,
+                    exp_x=-12, exp_w=-17, eta=8)
+    a, b = DfpRun(w), DfpRun(w)
+    stream = torch.cuda.Stream()
+    xs = [torch.from_numpy(np.ascontiguousarray(si.make_batch(w, t)[0])).pin_memory() for t in range(5)]
+    st = torch.zeros(a.m.num_stats(), dtype=torch.int64).pin_memory()
+    for t in range(len(xs)):
+        a.m.train_step_host_async(xs[t], w.exp_x, st, stream=stream)
+        if t == 2:
+            stream.synchronize()
+    stream.synchronize()
+    for t in range(len(xs)):
+        b.step(t)
+    ra, rb = a.record(), b.record()
+    assert ra.keys() == rb.keys()
+    for k in ra:
+        assert np.array_equal(np.asarray(ra[k]), np.asarray(rb[k])), k
+    n = a.m.num_stats()
+    want = (ctypes.c_int64 * n)()
+    assert a.ito._lib.ito_dfp16_model_read_stats(a.m._h, want, n) == 0
+    assert list(st.numpy()) == list(want)
