@@ -142,3 +142,13 @@ def test_model_options_struct_matches_header():
     import integer_only_nn_gb300 as ito
     assert [f for f, _ in ito.ModelOptions._fields_] == fields
     assert ctypes.sizeof(ito.ModelOptions) == 4 * len(fields)
+
+
+def test_host_side_argument_errors_dfp16_pipelined_step():
+    """The pipelined DFP16 host step rejects a NULL model or input on the host."""
+    _lib_path()
+    import integer_only_nn_gb300 as ito
+    L = ito._lib
+    dummy = ctypes.c_void_p(256)
+    assert L.ito_dfp16_train_step_host_async(None, dummy, -12, None, None) == ito.ITO_ERR_ARG
+    assert L.ito_dfp16_model_num_stats(None) == 0
