@@ -60,6 +60,43 @@ __global__ void k_im2col_v8(const int8_t* __restrict__ x, int B, int H, int W, i
 }
 
 // one thread per patch-matrix element, including the pitch padding (written 0)
+// one thread per patch row (output pixel) when IC % 8 != 0: its 9 * IC taps in (kh, kw, ic)
+// order and the zero padding up to ldp, eight bf16 values per 16-byte store, the (tap, ic)
+// position advanced by counting instead of dividing; ldp % 8 == 0 and P 16-byte aligned
+__global__ void k_im2col_rows(const int8_t* __restrict__ x, int B, int H, int W, int IC, int OH, int OW, int stride,
+                              uint16_t* __restrict__ P, int64_t ldp)
+{
+    const int64_t rows = (int64_t)B * OH * OW;
+    const int K = 9 * IC;
+    for (int64_t m = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; m < rows; m += (int64_t)gridDim.x * blockDim.x) {
+        const int ow = (int)(m % OW);
+        const int64_t t = m / OW;
+        const int oh = (int)(t % OH);
+        const int b = (int)(t / OH);
+        uint16_t* dst = P + m * ldp;
+        int tap = 0, ic = 0;
+        for (int k0 = 0; k0 < ldp; k0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                int val = 0;
+                if (k0 + q < K) {
+                    const int ih = oh * stride - 1 + tap / 3, iw = ow * stride - 1 + tap % 3;
+                    if (ih >= 0 && ih < H && iw >= 0 && iw < W) val = x[(((int64_t)b * H + ih) * W + iw) * IC + ic];
+                    if (++ic == IC) {
+                        ic = 0;
+                        ++tap;
+                    }
+                }
+                v[q] = val;
+            }
+            *reinterpret_cast<uint4*>(dst + k0) = make_uint4(int_pair_to_bf16x2(v[0], v[1]), int_pair_to_bf16x2(v[2], v[3]),
+                                                             int_pair_to_bf16x2(v[4], v[5]), int_pair_to_bf16x2(v[6], v[7]));
+        }
+    }
+}
+
+// one thread per patch element (any ldp or alignment)
 __global__ void k_im2col_1(const int8_t* __restrict__ x, int B, int H, int W, int IC, int OH, int OW, int stride,
                            uint16_t* __restrict__ P, int64_t ldp)
 {
@@ -86,6 +123,9 @@ int launch_im2col(const int8_t* x, int B, int H, int W, int IC, int OH, int OW, 
     if (IC % 8 == 0 && ldp % 8 == 0 && aligned(x, 8) && aligned(P, 16)) {
         const int64_t n = (int64_t)B * OH * OW * 9 * (IC / 8);
         k_im2col_v8<<<launch_grid_blocks(n, 256), 256, 0, s>>>(x, B, H, W, IC, OH, OW, stride, P, ldp);
+    } else if (ldp % 8 == 0 && aligned(P, 16)) {
+        k_im2col_rows<<<launch_grid_blocks((int64_t)B * OH * OW, 128), 128, 0, s>>>(x, B, H, W, IC, OH, OW, stride, P,
+                                                                                  ldp);
     } else {
         const int64_t n = (int64_t)B * OH * OW * ldp;
         k_im2col_1<<<launch_grid_blocks(n, 256), 256, 0, s>>>(x, B, H, W, IC, OH, OW, stride, P, ldp);
@@ -196,8 +236,17 @@ __global__ void k_gap_fwd(const int8_t* __restrict__ A, int B, int HW, int C, in
         const int c = (int)(i % C);
         const int64_t b = i / C;
         const int8_t* src = A + b * HW * C + c;
+        // eight independent partial sums, so that eight loads are in flight per thread
+        int32_t part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        int p = 0;
+        for (; p + 8 <= HW; p += 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) part[u] += src[(int64_t)(p + u) * C];
+        }
+        for (; p < HW; ++p) part[0] += src[(int64_t)p * C];
         int32_t acc = 0;
-        for (int p = 0; p < HW; ++p) acc += src[(int64_t)p * C];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc += part[u];
         P[i] = acc;
         mx = max(mx, abs_u32(acc));
     }
