@@ -143,12 +143,24 @@ __global__ void k_col2im_v8(const int32_t* __restrict__ Dcol, int B, int H, int 
     const int64_t ldc = 9 * (int64_t)IC;
     const int64_t n = (int64_t)B * H * W * cg;
     uint32_t mx = 0;
+    const bool narrow = n <= 0x7fffffff;   // 32-bit index arithmetic (the same for every thread)
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int c8 = (int)(i % cg);
-        const int64_t pix = i / cg;
-        const int iw = (int)(pix % W);
-        const int ih = (int)((pix / W) % H);
-        const int b = (int)(pix / ((int64_t)W * H));
+        int c8, iw, ih, b;
+        int64_t pix;
+        if (narrow) {
+            const uint32_t u = (uint32_t)i, px = u / (uint32_t)cg, t = px / (uint32_t)W;
+            c8 = (int)(u - px * (uint32_t)cg);
+            iw = (int)(px - t * (uint32_t)W);
+            ih = (int)(t % (uint32_t)H);
+            b = (int)(t / (uint32_t)H);
+            pix = px;
+        } else {
+            c8 = (int)(i % cg);
+            pix = i / cg;
+            iw = (int)(pix % W);
+            ih = (int)((pix / W) % H);
+            b = (int)(pix / ((int64_t)W * H));
+        }
         int32_t acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
         for (int kh = 0; kh < 3; ++kh) {
@@ -260,6 +272,29 @@ int launch_gap_fwd(const int8_t* A, int B, int HW, int C, int32_t* P, uint32_t* 
 }
 
 // E[b][pos][c] = (A[b][pos][c] > 0) ? dP[b][c] : 0, plus bf16 copy (pitch C)
+// C % 8 == 0, E 8-byte and Eb 16-byte aligned: eight channels of one position per thread
+__global__ void k_gap_bwd_v8(const int8_t* __restrict__ dP, const int8_t* __restrict__ A, int B, int HW, int C,
+                             int8_t* __restrict__ E, uint16_t* __restrict__ Eb)
+{
+    const int64_t groups = (int64_t)B * HW * (C >> 3);
+    const int cg = C >> 3;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups; g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t pos = g / cg;                       // b * HW + p
+        const int c0 = (int)(g - pos * cg) * 8;
+        const int64_t b = pos / HW;
+        const int64_t i0 = pos * C + c0;
+        int8_t a[8], d[8], e[8];
+        *reinterpret_cast<uint2*>(a) = __ldg(reinterpret_cast<const uint2*>(A + i0));
+        *reinterpret_cast<uint2*>(d) = __ldg(reinterpret_cast<const uint2*>(dP + b * C + c0));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = a[j] > 0 ? d[j] : (int8_t)0;
+        *reinterpret_cast<uint2*>(E + i0) = *reinterpret_cast<const uint2*>(e);
+        if (Eb)
+            *reinterpret_cast<uint4*>(Eb + i0) = make_uint4(int_pair_to_bf16x2(e[0], e[1]), int_pair_to_bf16x2(e[2], e[3]),
+                                                            int_pair_to_bf16x2(e[4], e[5]), int_pair_to_bf16x2(e[6], e[7]));
+    }
+}
+
 __global__ void k_gap_bwd(const int8_t* __restrict__ dP, const int8_t* __restrict__ A, int B, int HW, int C,
                           int8_t* __restrict__ E, uint16_t* __restrict__ Eb)
 {
@@ -275,7 +310,10 @@ __global__ void k_gap_bwd(const int8_t* __restrict__ dP, const int8_t* __restric
 
 int launch_gap_bwd(const int8_t* dP, const int8_t* A, int B, int HW, int C, int8_t* E, uint16_t* Eb, cudaStream_t s)
 {
-    k_gap_bwd<<<launch_grid_blocks((int64_t)B * HW * C, 256), 256, 0, s>>>(dP, A, B, HW, C, E, Eb);
+    if (C % 8 == 0 && aligned(A, 8) && aligned(dP, 8) && aligned(E, 8) && (!Eb || aligned(Eb, 16)))
+        k_gap_bwd_v8<<<launch_grid_blocks((int64_t)B * HW * C / 8, 256), 256, 0, s>>>(dP, A, B, HW, C, E, Eb);
+    else
+        k_gap_bwd<<<launch_grid_blocks((int64_t)B * HW * C, 256), 256, 0, s>>>(dP, A, B, HW, C, E, Eb);
     return launched("gap bwd");
 }
 
