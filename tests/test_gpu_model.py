@@ -92,17 +92,19 @@ def test_model_graph_replay_lockstep(index, steps):
     assert g.ito.ito_get_error() == 0
 
 
-@pytest.mark.parametrize("index,pingpong", [(1, False), (6, True), (2, True)])
-def test_overlap_modes_give_identical_steps(index, pingpong):
+@pytest.mark.parametrize("index,pingpong,spec_min", [(1, False, 0), (6, True, 0), (2, True, 0), (1, False, 1)])
+def test_overlap_modes_give_identical_steps(index, pingpong, spec_min):
     """The backward overlap moves bandwidth passes to a second stream; every
     tensor and statistic after three steps is the same in all three modes
-    (one stream, requantisation + updates overlapped, updates only). The
-    default, overlapped mode is the one the lockstep and digest tests compare
-    with the oracle."""
+    (one stream, requantisation + updates overlapped, updates only), also with
+    speculative requantisation (whose checks and re-launches stay on the
+    caller's stream). A new model's default mode is the one the lockstep and
+    digest tests compare with the oracle."""
     w = si.by_name(index)
     results = []
     for mode in (0, 1, 2):
-        g = GpuRun(w, pingpong_grads=pingpong)
+        # spec_min = 1: every eligible contraction requantises speculatively
+        g = GpuRun(w, pingpong_grads=pingpong, speculate_min_elems=spec_min)
         g.model.set_overlap(mode)
         for t in range(3):
             g.step(t)
