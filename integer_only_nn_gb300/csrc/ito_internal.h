@@ -84,12 +84,6 @@ struct DfpGemmPlan {
     int chunk_kb;                 // K blocks of 64 per exact chunk
     int pair;                     // CTA-pair kernel (256 x 64 tiles)
     int tail_full, tail_parts;    // pair kernel: whole tiles, K pieces per remaining tile (1: no split)
-    // pair kernel: speculative requantisation in the epilogue (rq_pred != nullptr)
-    CUtensorMap mapO8, mapOB;
-    const int32_t* rq_pred;
-    const int8_t* rq_gate;
-    int64_t rq_ldg;
-    int rq_relu;
     int64_t* tail_ws;             // [pieces][256][64] int64 partials of the split tiles
     bool a_mn, b_mn;
     int64_t* C;
