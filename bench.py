@@ -185,30 +185,42 @@ def oracle_step(w, weights, x, labels):
     return O.dfp16_step(weights, w.exp_w, x, w.exp_x, eta=w.eta, route="loops")
 
 
-def cpu_baseline(w, sample_batch, min_seconds=10.0):
-    """The CPU oracle (plain C loops, OpenMP over output rows) on one training
-    step of `sample_batch` samples of workload w."""
+def cpu_baseline(w, sample_batch, min_seconds=10.0, single_seconds=3.0):
+    """The CPU oracle (plain C loops, OpenMP over output rows) on training steps of
+    `sample_batch` samples of workload w, repeated for about min_seconds with every
+    host core, then for about single_seconds on one thread (a smaller slice)."""
     import numpy as np
     import oracle as O
     import seeded_inputs as si
     O.build()
     weights = si.make_weights(w)
     x, labels = si.make_batch(w, 0)
+
+    def timed(n, seconds):
+        xs = np.ascontiguousarray(x[:n])
+        ls = None if labels is None else np.ascontiguousarray(labels[:n])
+        # the same step repeated (the loops' cost does not depend on the values)
+        steps = 0
+        t0 = time.perf_counter()
+        while True:
+            oracle_step(w, weights, xs, ls)
+            steps += 1
+            dt = time.perf_counter() - t0
+            if dt >= seconds:
+                return steps * n / dt, dt, steps
+
     sample_batch = min(sample_batch, w.batch)
-    x = np.ascontiguousarray(x[:sample_batch])
-    labels = None if labels is None else np.ascontiguousarray(labels[:sample_batch])
-    # the same step repeated until about min_seconds of CPU work (the loops' cost does not
-    # depend on the values)
-    steps = 0
-    t0 = time.perf_counter()
-    while True:
-        oracle_step(w, weights, x, labels)
-        steps += 1
-        dt = time.perf_counter() - t0
-        if dt >= min_seconds:
-            break
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return steps * sample_batch / dt, dt, cores, steps, sample_batch
+    cores = O.max_threads()
+    value, dt, steps = timed(sample_batch, min_seconds)
+    O.set_threads(1)
+    try:
+        n1 = max(1, min(sample_batch, sample_batch // 8))
+        v1, dt1, steps1 = timed(n1, single_seconds)
+    finally:
+        O.set_threads(cores)
+    single = {"value": v1, "cores": 1,
+              "sample": "%d steps on %d samples, %.1f s" % (steps1, n1, dt1)}
+    return value, dt, cores, steps, sample_batch, single
 
 
 def run_reference(args, w):
@@ -236,7 +248,7 @@ def run_reference(args, w):
         weights = [rec["w%d" % l] for l in range(len(weights))]
     dt = time.perf_counter() - t0
     value = sample * args.steps / dt
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    cores = O.max_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
@@ -274,10 +286,11 @@ def run_ours(args, w):
     # context competes with the host cores
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, cores, nsteps, nsamp = cpu_baseline(w, args.cpu_batch)
+        v, dt, cores, nsteps, nsamp, single = cpu_baseline(w, args.cpu_batch)
         cpu = {"value": v, "unit": "samples/s", "cores": cores, "kind": "oracle",
                "sample": "%d oracle training steps (C loops, OpenMP over output rows) on %d of the %d samples "
-                         "of %s, %.1f s" % (nsteps, nsamp, w.batch, w.name, dt)}
+                         "of %s, %.1f s" % (nsteps, nsamp, w.batch, w.name, dt),
+               "single_thread": single}
 
     if w.kind == "dfp16":
         return run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local)

@@ -56,6 +56,15 @@ def build(force: bool = False) -> str:
 _lib = None
 
 
+def set_threads(n: int) -> None:
+    """Threads of the C loops' OpenMP regions (timing only; results are the same)."""
+    lib().ora_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return lib().ora_max_threads()
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -63,6 +72,8 @@ def lib():
         P = ctypes.c_void_p
         i32, i64, u32, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
         sig = {
+            "ora_set_threads": (None, [ctypes.c_int]),
+            "ora_max_threads": (ctypes.c_int, []),
             "ora_bitlen": (i32, [u64]),
             "ora_shift_from_max": (i32, [u64, i32]),
             "ora_rhu": (i64, [i64, i32]),

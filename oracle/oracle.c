@@ -36,6 +36,7 @@
  * Readings where the pages leave a step open are stated at each function.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -777,3 +778,8 @@ int64_t ora_abs_sum16(const int16_t *x, int64_t n)
     for (int64_t i = 0; i < n; i++) s += x[i] < 0 ? -(int64_t)x[i] : (int64_t)x[i];
     return s;
 }
+
+/* Threads of the OpenMP loops over output rows (the results do not depend on it: every
+ * output element is computed by one thread, in the same order). */
+void ora_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
+int ora_max_threads(void) { return omp_get_max_threads(); }
