@@ -452,8 +452,6 @@ def run_ours(args, w):
     prof = {c: tuple(v) for c, v in prof.items()}
     g_tflops = g_work / (g_ms / 1000.0) / 1e12
     peak = float(pk["bf16_tflops_sustained"])
-    r_ms, r_work, _ = prof["requant"]
-    u_ms, u_work, _ = prof["update"]
     hbm = float(pk["hbm_gbs"])
     line = {
         "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world, "steps": K, "warmup": Wm,
