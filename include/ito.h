@@ -419,8 +419,9 @@ int ito_model_use_graphs(ito_model *m, int enable);
  * then hold only the updates. Errors: ITO_ERR_ARG (NULL model, mode outside 0..2). */
 int ito_model_set_overlap(ito_model *m, int mode);
 
-/* Writes the model's current backward stream layout (0, 1 or 2) to *mode.
- * Errors: ITO_ERR_ARG (NULL argument). */
+/* Writes the model's current backward stream layout (0, 1 or 2) to *mode (a
+ * scheduling control; the pages have no counterpart). Errors: ITO_ERR_ARG (NULL
+ * argument). */
 int ito_model_get_overlap(const ito_model *m, int *mode);
 
 /* Speculative requantisation (default on; the environment variable
@@ -442,7 +443,8 @@ int ito_model_get_overlap(const ito_model *m, int *mode);
 int ito_model_set_speculation(ito_model *m, int enable);
 
 /* Writes 1 to *enabled when speculative requantisation is on for this model,
- * else 0. Errors: ITO_ERR_ARG (NULL argument). */
+ * else 0 (a scheduling control; the pages have no counterpart). Errors:
+ * ITO_ERR_ARG (NULL argument). */
 int ito_model_get_speculation(const ito_model *m, int *enabled);
 
 /* The same step from HOST buffers: copies x and labels into the model's
@@ -452,7 +454,9 @@ int ito_model_get_speculation(const ito_model *m, int *enabled);
 int ito_train_step_host(ito_model *m, const int8_t *x_host, const int32_t *labels_host,
                         int32_t *stats_host, void *stream);
 
-/* The host-buffer step without waiting, for a pipeline of steps: the copy of x_host and
+/* The training step of "Integer On-Device Training: Overview", section 4 (forward,
+ * compute_loss, backward with the NITI update), from host buffers without waiting, for a
+ * pipeline of steps: the copy of x_host and
  * labels_host goes on a model-owned copy stream into one of two model-owned device input
  * buffers (alternating from call to call, after the step that last read that buffer),
  * the step runs on `stream` after the copy, and the stats array (ito_model_num_stats
@@ -618,7 +622,9 @@ int ito_dfp16_model_read_stats(const ito_dfp16_model *m, int64_t *host_out, int 
  * [batch][dims[0]] with exponent exp_x. */
 int ito_dfp16_train_step(ito_dfp16_model *m, const int16_t *x, int32_t exp_x, void *stream);
 
-/* The DFP16 step from a host buffer without waiting, for a pipeline of steps: x_host (int16
+/* The DFP16 training step (ito_dfp16_train_step; "Mixed Precision Training of Convolutional
+ * Neural Networks using Integer Operations", section 3) from a host buffer without waiting,
+ * for a pipeline of steps: x_host (int16
  * mantissas [batch][in], exponent exp_x) is copied on a model-owned copy stream into one of
  * two model-owned device input buffers (alternating from call to call, after the step that
  * last read that buffer), the step runs on `stream` after the copy, and the statistics, in
@@ -716,7 +722,8 @@ int ito_model_profile_read(ito_model *m, double *ms, double *work, int64_t *laun
 /* Number of kernels the model launches per training step. */
 int ito_model_kernels_per_step(const ito_model *m);
 
-/* Per-kernel timing of the DFP16 model, as ito_model_profile /
+/* Measurement (no counterpart in the pages). Per-kernel timing of the DFP16 model, as
+ * ito_model_profile /
  * ito_model_profile_read: an event pair on the launch's stream around every
  * launch of a step; classes ITO_PROF_GEMM (limb contractions; work = executed
  * bf16 operations, 8*M*N*K: four limb products per int16 multiply-add),
