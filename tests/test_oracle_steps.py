@@ -43,6 +43,137 @@ def test_tiny_dfp16_step_hand_worked():
         assert r[k] == g[k][0], k
 
 
+def _tiny_cnn():
+    g = load_golden("tiny_cnn_step.txt")
+    x = np.array(g["x"], np.int8).reshape(1, 4, 4, 1)
+    W0 = np.array(g["W0"], np.int8).reshape(1, 3, 3, 1)
+    W1 = np.array(g["W1"], np.int8).reshape(2, 3, 3, 1)
+    W2 = np.array(g["W2"], np.int8).reshape(2, 2)
+    convs = [(1, 1, 1), (1, 2, 2)]
+    return g, x, [W0, W1, W2], np.array(g["label"], np.int32), convs
+
+
+def test_tiny_cnn_step_hand_worked():
+    g, x, weights, labels, convs = _tiny_cnn()
+    r = O.cnn_step(weights, x, labels, convs)
+    for k in ("y0", "a0", "y1", "a1", "p", "pa", "y2", "a2", "e2", "d2", "pe", "g2", "w2",
+              "e1", "d1", "e0", "g1", "w1", "g0", "w0"):
+        assert r[k].ravel().tolist() == g[k], k
+    for k in ("ys0", "ys1", "ps", "ys2", "ds2", "gs2", "ws2", "nz2", "ds1", "gs1", "ws1", "nz1",
+              "gs0", "ws0", "nz0"):
+        assert r[k] == g[k][0], k
+
+
+def test_tiny_cnn_planted_post_update_conv_dgrad_is_caught():
+    """Conv delta propagation with the already-updated conv1 weights gives a
+    different e0 than the hand-worked step."""
+    g, x, weights, labels, convs = _tiny_cnn()
+    e1 = np.array(g["e1"], np.int8).reshape(1, 2, 2, 2)
+    a0 = np.array(g["a0"], np.int8).reshape(1, 4, 4, 1)
+    w1_new = np.array(g["w1"], np.int8).reshape(2, 3, 3, 1)
+    wrong, _, _ = O.requant_mask(O.conv2d_dgrad(e1, w1_new, (4, 4), 2), a0)
+    assert wrong.ravel().tolist() != g["e0"]
+    right, _, _ = O.requant_mask(O.conv2d_dgrad(e1, weights[1], (4, 4), 2), a0)
+    assert right.ravel().tolist() == g["e0"]
+
+
+def test_tiny_cnn_planted_pooled_delta_gate_is_caught():
+    """Gating the pooled delta by the pooled activation (pa > 0) zeroes the
+    channel whose pooled value rounded to 0 although some of its positions are
+    active; the hand-worked e1 keeps it."""
+    g, _, _, _, _ = _tiny_cnn()
+    pe = np.array([g["pe"]], np.int8)
+    pa = np.array([g["pa"]], np.int8)
+    a1 = np.array(g["a1"], np.int8).reshape(1, 2, 2, 2)
+    wrong = O.gap_bwd(np.where(pa > 0, pe, 0), a1)
+    assert wrong.ravel().tolist() != g["e1"]
+    assert O.gap_bwd(pe, a1).ravel().tolist() == g["e1"]
+
+
+def _tiny_dfp2():
+    g = load_golden("tiny_dfp16_2layer_step.txt")
+    W0 = np.array(g["W0"], np.int16).reshape(2, 2)
+    W1 = np.array(g["W1"], np.int16).reshape(1, 2)
+    x = np.array([g["x"]], np.int16)
+    return g, x, [W0, W1]
+
+
+def test_tiny_dfp16_two_layer_step_hand_worked():
+    g, x, weights = _tiny_dfp2()
+    r = O.dfp16_step(weights, g["exp_w"][0], x, g["exp_x"][0], eta=g["eta"][0])
+    for k in ("p0", "y0", "p1", "y1", "pd1", "e0", "pg1", "g1", "w1", "pg0", "g0", "w0"):
+        assert r[k].ravel().tolist() == g[k], k
+    for k in ("rs0", "ey0", "rs1", "ey1", "rsd1", "ee0", "rsg1", "eg1", "k1", "nz1",
+              "rsg0", "eg0", "k0", "nz0"):
+        assert r[k] == g[k][0], k
+    assert r["ee1"] == g["ey1"][0]
+
+
+def test_tiny_dfp16_planted_post_update_dgrad_is_caught():
+    """DFP delta propagation with layer 1's already-updated weights gives a
+    different e0 than the hand-worked step."""
+    g, x, weights = _tiny_dfp2()
+    e1 = np.array([g["y1"]], np.int16)
+    w1_new = np.array(g["w1"], np.int16).reshape(1, 2)
+    wrong, _, _, _ = O.dfp_down(O.dfp_linear_dgrad(e1, w1_new), g["ey1"][0] + g["exp_w"][0])
+    assert wrong.ravel().tolist() != g["e0"]
+
+
+def test_tiny_dfp16_planted_delta_exponent_mistake_is_caught():
+    """Giving the propagated delta the activation's exponent (E_e + E_y0)
+    instead of the weight's (E_e + E_W) changes E_G0 and so the update shift
+    and the updated layer-0 weights."""
+    g, x, weights = _tiny_dfp2()
+    e0 = np.array([g["e0"]], np.int16)
+    ee0_wrong = g["ey1"][0] + g["ey0"][0] + g["rsd1"][0]
+    assert ee0_wrong != g["ee0"][0]
+    gm, eg, _, _ = O.dfp_down(O.dfp_linear_wgrad(e0, x), ee0_wrong + g["exp_x"][0])
+    w_wrong, _ = O.dfp_update(weights[0], gm, g["exp_w"][0] + g["eta"][0] - eg)
+    assert w_wrong.ravel().tolist() != g["w0"]
+
+
+def _tiny_static():
+    g = load_golden("tiny_static_step.txt")
+    x = np.array(g["x"], np.int8).reshape(2, 2)
+    weights = [np.array(g["W0"], np.int8).reshape(2, 2), np.array(g["W1"], np.int8).reshape(2, 2)]
+    static_q = [dict(offset=np.array(g["off%d" % l], np.int32), mult=np.array(g["mult%d" % l], np.int32),
+                     k=np.array(g["k%d" % l], np.int32)) for l in range(2)]
+    return g, x, weights, np.array(g["labels"], np.int32), static_q
+
+
+def test_tiny_static_step_hand_worked():
+    g, x, weights, labels, static_q = _tiny_static()
+    r = O.mlp_step(weights, x, labels, static_q=static_q)
+    for k in ("y0", "a0", "y1", "a1", "e1", "d1", "e0", "g1", "w1", "og1", "g0", "w0", "og0"):
+        assert r[k].ravel().tolist() == g[k], k
+    for k in ("ds1", "gs1", "ws1", "ogs1", "ows1", "gs0", "ws0", "ogs0", "ows0"):
+        assert r[k] == g[k][0], k
+    for l in range(2):
+        assert r["off%d" % l].tolist() == g["new_off%d" % l]
+        assert "ys%d" % l not in r               # no dynamic forward shift on a static layer
+
+
+def test_tiny_static_planted_offset_gradient_from_propagated_delta_is_caught():
+    """An offset gradient read after the layer's delta buffer was reused for
+    the propagated delta (e0 instead of e1) gives a different layer-1 offset
+    gradient than the hand-worked step."""
+    g, _, _, _, _ = _tiny_static()
+    wrong = O.offset_grad(np.array(g["e0"], np.int8).reshape(2, 2))
+    assert wrong.tolist() != g["og1"]
+    assert O.offset_grad(np.array(g["e1"], np.int8).reshape(2, 2)).tolist() == g["og1"]
+
+
+def test_tiny_static_planted_offset_after_multiply_is_caught():
+    """Adding the offset after the multiply (y*mult + off) instead of before it
+    changes the hand-worked layer-0 activations."""
+    g, x, weights, _, static_q = _tiny_static()
+    y0 = O.linear_fwd(x, weights[0])
+    q = static_q[0]
+    wrong = np.clip(np.floor_divide(y0.astype(np.int64) * q["mult"] + q["offset"], 1 << q["k"].astype(np.int64)),
+                    0, 127)
+    assert wrong.ravel().tolist() != g["a0"]
+
+
 def _check_nitI_invariants(rec, n_layers):
     for k, v in rec.items():
         if isinstance(v, np.ndarray) and v.dtype == np.int8:
