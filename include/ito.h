@@ -137,7 +137,9 @@ int ito_linear_fwd(const int8_t *x, const int8_t *W, int B, int IC, int OC, int 
  *    with ITO_ERR_SHAPE before anything is enqueued.
  *  - The first call on a device looks up the array's device address on that
  *    device (the device must be current); make that first call before any
- *    stream capture.
+ *    stream capture. The address is kept per device context: after a
+ *    cudaDeviceReset the next call on that device looks it up again, so make
+ *    that call, too, before any stream capture.
  *  - All calls share the array: calls whose work overlaps on the GPU (for
  *    instance on two streams without ordering) race on it. Serialise them.
  * Outputs, errors and stream semantics as ito_linear_fwd. */
@@ -187,7 +189,8 @@ int ito_niti_update(int8_t *W, const int32_t *G, int64_t n, const uint32_t *d_ma
  * Overview", section 4: compute_loss reads the int8 logits and writes dy):
  *   delta[b][j] = sat_int8(logits[b][j] - target_mag * [j == labels[b]])
  * logits: int8 [B][C]; labels: int32 [B] in [0, C); delta: int8 [B][C].
- * A label outside [0, C) contributes no target (the row is copied).
+ * A label outside [0, C) has no class to take the target: the kernel copies
+ * that row and records ITO_ERR_ARG in the device error word (ito_get_error).
  * Errors: ITO_ERR_ARG, ITO_ERR_SHAPE. */
 int ito_top_error(const int8_t *logits, const int32_t *labels, int B, int C, int32_t target_mag,
                   int8_t *delta, void *stream);
@@ -392,8 +395,9 @@ int ito_model_num_stats(const ito_model *m);
  * layers, top error against `labels`, then for each layer from the top down:
  * delta propagation with the pre-update weights (not for the first layer),
  * weight gradient, NITI update. x: int8 [batch][in_features] (NHWC for a conv
- * first layer); labels: int32 [batch]. Enqueued on `stream`; no host
- * synchronisation. */
+ * first layer); labels: int32 [batch] in [0, classes) (an out-of-range label
+ * records ITO_ERR_ARG in the device error word, as in ito_top_error).
+ * Enqueued on `stream`; no host synchronisation. */
 int ito_train_step(ito_model *m, const int8_t *x, const int32_t *labels, void *stream);
 
 /* Replays whole training steps as CUDA graphs (enable != 0) or launches
@@ -413,8 +417,7 @@ int ito_model_use_graphs(ito_model *m, int enable);
  *   2: only the weight updates run on the second stream.
  * Events order every read after its write; the step ends joined on the caller's
  * stream. Changing the mode synchronises the device and drops captured graphs.
- * The environment variable ITO_OVERLAP sets the mode of new models; without it
- * a new model takes mode 1, or mode 0 when every delta propagation requantises
+ * A new model takes mode 1, or mode 0 when every delta propagation requantises
  * speculatively (see ito_model_set_speculation), since the second stream would
  * then hold only the updates. Errors: ITO_ERR_ARG (NULL model, mode outside 0..2). */
 int ito_model_set_overlap(ito_model *m, int mode);
@@ -424,8 +427,7 @@ int ito_model_set_overlap(ito_model *m, int mode);
  * argument). */
 int ito_model_get_overlap(const ito_model *m, int *mode);
 
-/* Speculative requantisation (default on; the environment variable
- * ITO_SPECULATE=0 turns it off for new models). NITI's shift of a tensor
+/* Speculative requantisation (on by default in a new model). NITI's shift of a tensor
  * depends on the whole tensor's max, so requantisation is a second pass over
  * the int32 result. With speculation on, the epilogue of the forward and
  * delta-propagation contractions (CTA-pair kernel; int8 row length a multiple

@@ -731,12 +731,6 @@ static void dfp_tail_split(int M, int N, int K, int* full, int* parts)
     const int tiles = ((M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((N + Cfg::BN - 1) / Cfg::BN);
     *full = tiles;
     *parts = 1;
-    // ITO_DFP_TAIL=0 in the environment turns the split off
-    static const int tail_env = [] {
-        const char* v = getenv("ITO_DFP_TAIL");
-        return v ? atoi(v) : 1;
-    }();
-    if (!tail_env) return;
     const int clusters = dfp2_clusters();
     const int num_chunks = ((K + Cfg::BK - 1) / Cfg::BK + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
     if (clusters < 1 || tiles % clusters == 0) return;
@@ -810,12 +804,8 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
     if ((r = make_map_bf16(&p->mapAh, Ah, a_mn ? 64 : 128)) || (r = make_map_bf16(&p->mapAl, Al, a_mn ? 64 : 128)) ||
         (r = make_map_bf16(&p->mapBh, Bh, 64)) || (r = make_map_bf16(&p->mapBl, Bl, 64)))
         return r;
-    // CTA-pair kernel when there are at least 256 rows; ITO_DFP_PAIR=0 forces the single-CTA kernel
-    static const int pair_env = [] {
-        const char* v = getenv("ITO_DFP_PAIR");
-        return v ? atoi(v) : 1;
-    }();
-    p->pair = pair_env != 0 && M >= 256 && C != nullptr;
+    // CTA-pair kernel when there are at least 256 rows
+    p->pair = M >= 256 && C != nullptr;
     p->tail_full = ((M + 255) / 256) * ((N + 63) / 64);
     p->tail_parts = 1;
     if (p->pair && tail_ws) {

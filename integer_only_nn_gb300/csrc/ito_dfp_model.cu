@@ -484,11 +484,7 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
     k_set_i32<<<1, 1>>>(m->ew(), m->exp_w);
     if (cudaMemcpy(m->wexp_d, m->wexp.data(), sizeof(int32_t) * nl, cudaMemcpyHostToDevice) != cudaSuccess)
         return set_error(ITO_ERR_CUDA, "weight exponent copy");
-    static const int overlap_env = [] {
-        const char* v = getenv("ITO_OVERLAP");
-        return v ? atoi(v) : 1;
-    }();
-    m->overlap = overlap_env != 0;
+    m->overlap = true;
     if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking) != cudaSuccess)
         return set_error(ITO_ERR_CUDA, "stream creation failed");

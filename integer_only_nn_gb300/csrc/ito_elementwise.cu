@@ -510,12 +510,17 @@ int launch_niti_update(int8_t* W, uint16_t* Wb, int64_t ldb, const int32_t* G, i
 
 // -------------------------------------------------------------- top error
 
+// A label outside [0, C) has no class to take the target: the row is copied and
+// ITO_ERR_ARG is recorded in the device error word (once per row, by the thread
+// that handles the row's first class).
 __global__ void k_top_error(const int8_t* __restrict__ logits, const int32_t* __restrict__ labels, int B, int C,
-                            int target_mag, int8_t* __restrict__ delta, uint16_t* __restrict__ deltab, int64_t ldb)
+                            int target_mag, int8_t* __restrict__ delta, uint16_t* __restrict__ deltab, int64_t ldb,
+                            int* __restrict__ err)
 {
     const int64_t n = (int64_t)B * C;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int b = (int)(i / C), j = (int)(i - (int64_t)b * C);
+        if (j == 0 && (labels[b] < 0 || labels[b] >= C)) raise_device_error(err, ITO_ERR_ARG);
         const int32_t t = (labels[b] == j) ? target_mag : 0;
         const int32_t d = sat8((int32_t)logits[i] - t);
         delta[i] = (int8_t)d;
@@ -526,11 +531,13 @@ __global__ void k_top_error(const int8_t* __restrict__ logits, const int32_t* __
 // Rows of a multiple of 8 classes: a thread takes 8 consecutive logits of one row (one
 // 8-byte load, one 8-byte and one 16-byte store); rows over blockIdx.y (strided past 65535).
 __global__ void k_top_error_v8(const int8_t* __restrict__ logits, const int32_t* __restrict__ labels, int B, int C,
-                               int target_mag, int8_t* __restrict__ delta, uint16_t* __restrict__ deltab, int64_t ldb)
+                               int target_mag, int8_t* __restrict__ delta, uint16_t* __restrict__ deltab, int64_t ldb,
+                               int* __restrict__ err)
 {
     const int groups = C >> 3;
     for (int b = blockIdx.y; b < B; b += gridDim.y) {
         const int label = labels[b];
+        if (blockIdx.x == 0 && threadIdx.x == 0 && (label < 0 || label >= C)) raise_device_error(err, ITO_ERR_ARG);
         for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += gridDim.x * blockDim.x) {
             const int64_t i0 = (int64_t)b * C + 8 * g;
             int8_t v[8];
@@ -552,15 +559,17 @@ int launch_top_error(const int8_t* logits, const int32_t* labels, int B, int C, 
                      uint16_t* deltab, int64_t ldb, cudaStream_t s)
 {
     if (B < 1 || C < 1) return ITO_OK;
+    int* err = device_error_word();
+    if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     const bool vec = C % 8 == 0 && aligned(logits, 8) && aligned(delta, 8) &&
                      (!deltab || (aligned(deltab, 16) && ldb % 8 == 0));
     if (vec) {
         const int groups = C / 8;
         const dim3 grid((groups + 127) / 128, B < 65535 ? B : 65535);
-        k_top_error_v8<<<grid, 128, 0, s>>>(logits, labels, B, C, target_mag, delta, deltab, ldb);
+        k_top_error_v8<<<grid, 128, 0, s>>>(logits, labels, B, C, target_mag, delta, deltab, ldb, err);
     } else {
         k_top_error<<<launch_grid_blocks((int64_t)B * C, 256), 256, 0, s>>>(logits, labels, B, C, target_mag, delta,
-                                                                             deltab, ldb);
+                                                                             deltab, ldb, err);
     }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "top error launch: %s", cudaGetErrorString(e));

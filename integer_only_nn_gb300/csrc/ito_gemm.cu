@@ -20,9 +20,6 @@
 // forward (x.W^T), delta-propagation (delta.W) and weight-gradient
 // (delta^T.a) contractions read the same row-major tensors without any
 // transpose pass.
-//
-// SIMT path (k_gemm_simt): a plain tiled int32 kernel with arbitrary strides,
-// used as an independent on-GPU cross-check of the tensor-core path.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -724,59 +721,6 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
     }
 }
 
-// --------------------------------------------------------------- SIMT path
-
-constexpr int SIMT_BM = 64, SIMT_BN = 64, SIMT_BK = 32;
-
-__global__ void __launch_bounds__(256)
-    k_gemm_simt(const int8_t* __restrict__ A, int64_t sam, int64_t sak, const int8_t* __restrict__ B, int64_t sbn,
-                int64_t sbk, int M, int N, int K, int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max)
-{
-    __shared__ int8_t As[SIMT_BK][SIMT_BM];
-    __shared__ int8_t Bs[SIMT_BK][SIMT_BN];
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int m0 = blockIdx.y * SIMT_BM, n0 = blockIdx.x * SIMT_BN;
-    int32_t acc[4][4] = {};
-    for (int k0 = 0; k0 < K; k0 += SIMT_BK) {
-#pragma unroll
-        for (int i = 0; i < (SIMT_BM * SIMT_BK) / 256; ++i) {
-            const int idx = threadIdx.x + 256 * i;
-            const int r = idx % SIMT_BM, k = idx / SIMT_BM;
-            const int gm = m0 + r, gn = n0 + r, gk = k0 + k;
-            As[k][r] = (gm < M && gk < K) ? A[gm * sam + gk * sak] : (int8_t)0;
-            Bs[k][r] = (gn < N && gk < K) ? B[gn * sbn + gk * sbk] : (int8_t)0;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int k = 0; k < SIMT_BK; ++k) {
-            int32_t a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a[i] = As[k][ty * 4 + i];
-                b[i] = Bs[k][tx * 4 + i];
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] += a[i] * b[j];
-        }
-        __syncthreads();
-    }
-    uint32_t mx = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int gm = m0 + ty * 4 + i, gn = n0 + tx * 4 + j;
-            if (gm < M && gn < N) {
-                C[gm * ldc + gn] = acc[i][j];
-                mx = max(mx, abs_u32(acc[i][j]));
-            }
-        }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((threadIdx.x & 31) == 0 && mx != 0) atomicMax(d_max, mx);
-}
-
 // ------------------------------------------------------ failure self-test
 
 // One CTA waits on an mbarrier that nothing completes: the bounded wait gives
@@ -1062,12 +1006,8 @@ static int split_count(int M, int N, int K)
 
 static bool pair_eligible(int M, int N, int splits, int min_pair_tiles = 1)
 {
-    static const int pair_env = [] {
-        const char* v = getenv("ITO_GEMM_PAIR");
-        return v ? atoi(v) : 1;
-    }();
     const int pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    return pair_env != 0 && M >= 256 && N >= 256 && splits == 1 && pair_tiles >= min_pair_tiles;
+    return M >= 256 && N >= 256 && splits == 1 && pair_tiles >= min_pair_tiles;
 }
 
 size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc)
@@ -1107,7 +1047,7 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
     p->err = device_error_word();
     if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     p->bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
-    // CTA-pair kernel for large tiles; ITO_GEMM_PAIR=0 in the environment forces the single-CTA kernel
+    // CTA-pair kernel for large tiles
     p->splits = 1;
     p->kb_per_split = (K + 63) / 64;
     const int splits = split_count(M, N, K);
@@ -1119,12 +1059,8 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
         p->split_stride = (int64_t)M * ldc;
     }
     p->pair = pair_eligible(M, N, p->splits, min_pair_tiles);
-    // tiles are rastered in groups of `group` row tiles; ITO_GEMM_GROUP overrides (tuning)
-    static const int group_env = [] {
-        const char* v = getenv("ITO_GEMM_GROUP");
-        return v ? atoi(v) : 0;
-    }();
-    p->group = group_env > 0 ? group_env : 16;
+    // tiles are rastered in groups of 16 row tiles
+    p->group = 16;
     // pair kernel: split the last partial wave along K when the workspace holds the partial tiles
     p->tail_full = ((M + 255) / 256) * ((N + 255) / 256);
     p->tail_parts = 1;
@@ -1231,17 +1167,6 @@ int gemm_run(const GemmPlan& p, cudaStream_t s)
     ITO_TC_CASE(64)
 #undef ITO_TC_CASE
     return set_error(ITO_ERR_ARG, "gemm: bad tile width");
-}
-
-int gemm_simt(const int8_t* A, int64_t sam, int64_t sak, const int8_t* B, int64_t sbn, int64_t sbk, int M, int N,
-              int K, int32_t* C, int64_t ldc, uint32_t* d_max, cudaStream_t s)
-{
-    if (M < 1 || N < 1 || K < 1) return set_error(ITO_ERR_SHAPE, "gemm: empty contraction");
-    dim3 grid((N + SIMT_BN - 1) / SIMT_BN, (M + SIMT_BM - 1) / SIMT_BM);
-    k_gemm_simt<<<grid, 256, 0, s>>>(A, sam, sak, B, sbn, sbk, M, N, K, C, ldc, d_max);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "simt gemm launch: %s", cudaGetErrorString(e));
-    return ITO_OK;
 }
 
 }  // namespace ito

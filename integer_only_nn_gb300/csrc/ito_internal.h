@@ -161,8 +161,6 @@ size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc);
 int gemm_plan_fuse_requant(GemmPlan* p, const int32_t* pred, int relu, const int8_t* gate, int64_t ldg,
                            int8_t* out8, int64_t ld8, uint16_t* outb, int64_t ldb);
 int gemm_run(const GemmPlan& p, cudaStream_t s);
-int gemm_simt(const int8_t* A, int64_t sam, int64_t sak, const int8_t* B, int64_t sbn, int64_t sbk, int M, int N,
-              int K, int32_t* C, int64_t ldc, uint32_t* d_max, cudaStream_t s);
 
 // ---- bandwidth kernels (ito_elementwise.cu)
 

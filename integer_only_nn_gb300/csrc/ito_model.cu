@@ -385,11 +385,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
     ITO_TRY(m->alloc(&m->spec_count, 2));
     if (cudaMemset(m->spec, 0xff, sizeof(int32_t) * 4 * nl) != cudaSuccess)   // -1: no prediction yet
         return set_error(ITO_ERR_CUDA, "memset");
-    static const int spec_env = [] {
-        const char* v = getenv("ITO_SPECULATE");
-        return v ? atoi(v) : 1;
-    }();
-    m->speculate = spec_env != 0;
+    m->speculate = true;   // ito_model_set_speculation turns it off
 
     // contraction plans (tensor maps over the buffers above)
     for (int l = 0; l < nl; ++l) {
@@ -486,17 +482,11 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
     m->stat_names.push_back({"pmax", nl * ST_PER_LAYER});
     m->stat_names.push_back({"ps", nl * ST_PER_LAYER + 1});
 
-    // second stream and ordering events of the backward overlap. ITO_OVERLAP in the
-    // environment sets the mode; without it the mode is 1 unless every delta propagation
-    // speculates: then the second stream would hold only the weight updates, which slow the
-    // contractions beside them by more than they take alone, and the mode is 0
-    static const int overlap_env = [] {
-        const char* v = getenv("ITO_OVERLAP");
-        return v ? atoi(v) : -1;
-    }();
-    if (overlap_env >= 0 && overlap_env <= 2) {
-        m->overlap = overlap_env;
-    } else {
+    // second stream and ordering events of the backward overlap: mode 1 unless every delta
+    // propagation speculates; then the second stream would hold only the weight updates,
+    // which slow the contractions beside them by more than they take alone, and the mode is
+    // 0 (ito_model_set_overlap changes it)
+    {
         bool every_delta_speculates = m->speculate;
         for (const MLayer& L : m->L)
             if (L.has_dgrad && !L.pd_spec.rq_pred) every_delta_speculates = false;

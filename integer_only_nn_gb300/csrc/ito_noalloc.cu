@@ -6,14 +6,19 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds ITO_NOALLOC_SCRATCH_BYTES of it until the process exits. Host
 // code must not hand the array's name to a kernel: on the host that name is a
-// stand-in symbol, not a device address. Its device address is looked up once
-// per device, with that device current, by the first call on that device.
+// stand-in symbol, not a device address. Its device address is looked up with
+// the device current, by the first call in each context of that device: the
+// cache is keyed on the driver's process-unique context id, so a
+// cudaDeviceReset (which destroys the primary context and with it the array's
+// old address) makes the next call look the address up again.
 //
 // All calls share the one array and it keeps the previous call's contents.
 // Each call overwrites every scratch byte the contraction reads, so nothing has
 // to start at zero; two calls whose work overlaps on the GPU (different
 // streams, no ordering between them) race on the array.
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "ito_device.cuh"
 #include "ito_internal.h"
@@ -27,13 +32,43 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[ITO_NOALLOC_SCR
 namespace {
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchSlot {
+    unsigned long long ctx_id;   // context the address belongs to (0: none yet)
+    void* addr;
+};
+ScratchSlot g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
 inline size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
-// Device address of the scratch array on the current device (looked up on the
-// first call per device).
+// Process-unique id of the calling thread's current context, 0 when there is
+// none yet or the driver entry points are unavailable (then the address is
+// looked up again).
+unsigned long long current_context_id()
+{
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current context of the current
+// device (looked up by the first call in each context).
 int scratch_address(void** out)
 {
     int dev = -1;
@@ -41,14 +76,17 @@ int scratch_address(void** out)
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return set_error(ITO_ERR_UNSUPPORTED, "device index %d", dev);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchSlot& slot = g_scratch[dev];
+    const unsigned long long id = current_context_id();
+    if (!slot.addr || id == 0 || slot.ctx_id != id) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
             return set_error(ITO_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-        g_scratch_addr[dev] = p;
+        slot.addr = p;
+        slot.ctx_id = current_context_id();   // the lookup may have created the primary context
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return ITO_OK;
 }
 

@@ -142,6 +142,24 @@ def test_top_error(ito):
     assert np.array_equal(_host(d), O.top_error(logits, labels, 64))
 
 
+@pytest.mark.parametrize("C", [1000, 10])   # eight-class groups, and the per-element kernel
+def test_top_error_bad_label_sets_error_word(ito, C):
+    """The oracle rejects a label outside [0, C); the kernel reports it through
+    the device error word (ITO_ERR_ARG) and leaves the valid rows right."""
+    B = 64
+    logits = i8((B, C))
+    labels = rng.integers(0, C, B).astype(np.int32)
+    assert ito.ito_get_error() == 0
+    for bad in (C, -1):
+        lab = labels.copy()
+        lab[5] = bad
+        d = _host(ito.ito_top_error(_dev(logits), _dev(lab), 64))
+        assert ito.ito_get_error() == ito.ITO_ERR_ARG
+        assert ito.ito_get_error() == 0                 # read and cleared
+        ok = np.arange(B) != 5
+        assert np.array_equal(d[ok], O.top_error(logits[ok], lab[ok], 64))
+
+
 def test_wgrad_longest_contraction_extreme_values(ito):
     """K = 131072 terms of (-128) * 127 = -16256: the sum -2,130,706,432 is just
     inside int32 (split-K slices and chunk drains must add exactly)."""

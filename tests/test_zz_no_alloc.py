@@ -1,14 +1,15 @@
 """ito_linear_fwd_noalloc, the forward Linear entry point for callers that
 cannot allocate device memory while they run (it uses a scratch array built
 into the library instead of a caller workspace), against ito_linear_fwd, the
-workspace entry point: bit-identical outputs on two calls in a row, and a clear
-rejection of sizes beyond the built-in scratch.
+workspace entry point, and against the CPU oracle: bit-identical outputs on two
+calls in a row, and a clear rejection of sizes beyond the built-in scratch.
 
 This file is collected last on purpose, so that a run that stops at the first
 failure has already run every other test; it also passes on its own."""
 import numpy as np
 import pytest
 
+import oracle as O
 from gpu_util import import_ito
 
 pytestmark = pytest.mark.gpu
@@ -42,6 +43,12 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
         got = ito.ito_linear_fwd_noalloc(xd, Wd, relu, out=out)
         torch.cuda.synchronize()
         _same(ref, got)
+        y32 = O.linear_fwd(x, W)
+        y8, shift, mx = O.requant(y32, relu=bool(relu))
+        assert np.array_equal(got[0].cpu().numpy(), y32)
+        assert (int(got[1].cpu().numpy()[0]) & 0xFFFFFFFF) == mx
+        assert int(got[2].cpu().numpy()[0]) == shift
+        assert np.array_equal(got[3].cpu().numpy(), y8)
     assert ito.ito_get_error() == 0
 
 
