@@ -9,13 +9,17 @@ ReLU, Linear 4096->1000), one full forward / delta propagation / weight
 gradient / NITI update per step, seeded synthetic int8 data.
 
 Prints one JSON line (rank 0). `value` is training samples/s of the whole job
-(every rank runs its own replica: the step has no cross-GPU exchange here);
-device time per step is taken with CUDA events on the step's stream, with L2
+(every rank runs its own replica: the step has no cross-GPU exchange here).
+Device time per step is taken with CUDA events on the step's stream, with L2
 flushed (a 256 MB write) before every timed step and the flush left out of the
-timing. `roofline` is the tensor-core contraction class timed live with events
-around each of its launches; `e2e` is the same metric through the host-buffer
-C-ABI call (ito_train_step_host: input copy, step, stats copy back);
-`cpu_baseline` is the CPU oracle on a bounded sample of the same workload.
+timing; `ms_per_step` is the median over five loops of K steps. `roofline` is
+the tensor-core contraction class timed with events around each of its
+launches (the same steps run again), against the measured burst bf16 peak;
+`e2e` is the same metric through the host-buffer C-ABI calls (input copy, step,
+stats copy); `cpu_baseline` is the CPU oracle on a bounded sample of the same
+workload. With one GPU, `workloads` adds the other seeded workloads (default
+0, 1, 2 and 4), each timed the same way in the same process, with its
+contraction fraction, nonzero weight updates and CPU-oracle rate.
 
 --impl reference runs the CPU oracle (the reference of this build: the pages
 publish no implementation) on the same workload, a bounded batch slice per
@@ -188,7 +192,8 @@ def oracle_step(w, weights, x, labels):
 def cpu_baseline(w, sample_batch, min_seconds=10.0, single_seconds=3.0):
     """The CPU oracle (plain C loops, OpenMP over output rows) on training steps of
     `sample_batch` samples of workload w, repeated for about min_seconds with every
-    host core, then for about single_seconds on one thread (a smaller slice)."""
+    host core, then (unless single_seconds is None) for about single_seconds on one
+    thread (a smaller slice)."""
     import numpy as np
     import oracle as O
     import seeded_inputs as si
@@ -212,6 +217,8 @@ def cpu_baseline(w, sample_batch, min_seconds=10.0, single_seconds=3.0):
     sample_batch = min(sample_batch, w.batch)
     cores = O.max_threads()
     value, dt, steps = timed(sample_batch, min_seconds)
+    if single_seconds is None:
+        return value, dt, cores, steps, sample_batch, None
     O.set_threads(1)
     try:
         n1 = max(1, min(sample_batch, sample_batch // 8))
@@ -264,6 +271,200 @@ def run_reference(args, w):
     return 0
 
 
+REPEATS = 5   # timed loops of K steps; the reported step time is their median
+
+
+def timed_median(K, repeats, stream, flush, before, step):
+    """Device ms per step: the median over `repeats` loops of K steps. Each step
+    runs after an untimed L2 flush and `before(k)`, between CUDA events on
+    `stream`. Returns (median, per-loop list)."""
+    import torch
+    per = []
+    for _ in range(repeats):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for k in range(K):
+                flush.fill_(k & 0xFF)
+                before(k)
+                starts[k].record(stream)
+                step(k)
+                ends[k].record(stream)
+        torch.cuda.synchronize()
+        per.append(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K)
+    return statistics.median(per), per
+
+
+def profiled_steps(model, K, stream, flush, before, step, classes):
+    """The same steps again with an event pair around every launch (on the
+    launch's own stream): {class: [ms, work, launches]} summed over K steps, and
+    the device ms per step with those events."""
+    import torch
+    model.profile(True)
+    for i in range(4):
+        with torch.cuda.stream(stream):
+            before(i)
+        step(i)
+    model.profile_read()
+    prof = {c: [0.0, 0.0, 0] for c in classes}
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            flush.fill_(k & 0xFF)
+            before(k)
+            starts[k].record(stream)
+            step(k)
+            ends[k].record(stream)
+            for c, (ms, work, n) in model.profile_read().items():
+                prof[c][0] += ms
+                prof[c][1] += work
+                prof[c][2] += n
+    torch.cuda.synchronize()
+    model.profile(False)
+    return prof, sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
+
+
+class ModelRun:
+    """An ito_model of an int8 workload with NB_BATCHES seeded batches resident
+    in HBM; before each step (untimed) the step's batch is copied into the
+    model's fixed input buffers, which the captured step graphs read."""
+
+    def __init__(self, w, graphs=True):
+        import torch
+        import integer_only_nn_gb300 as ito
+        import seeded_inputs as si
+        self.w = w
+        self.stream = torch.cuda.Stream()   # a side stream, so that steps can replay from graphs
+        self.model = ito.Model(ito.layers_for(w), w.batch)
+        for l, W in enumerate(si.make_weights(w)):
+            self.model.set_weights(l, W, stream=self.stream)
+        self.model.use_graphs(graphs)
+        self.xs, self.ls = [], []
+        for t in range(NB_BATCHES):
+            x, labels = si.make_batch(w, t)
+            self.xs.append(torch.from_numpy(x).cuda())
+            self.ls.append(torch.from_numpy(labels).cuda())
+        self.xbuf, self.lbuf = torch.empty_like(self.xs[0]), torch.empty_like(self.ls[0])
+        torch.cuda.synchronize()
+
+    def before(self, k):
+        self.xbuf.copy_(self.xs[k % NB_BATCHES])
+        self.lbuf.copy_(self.ls[k % NB_BATCHES])
+
+    def step(self, k):
+        self.model.train_step(self.xbuf, self.lbuf, stream=self.stream)
+
+    def warm(self, n):
+        import torch
+        for i in range(n):
+            with torch.cuda.stream(self.stream):
+                self.before(i)
+            self.step(i)
+        self.stream.synchronize()
+
+    def nonzero_updates(self):
+        st = self.model.stats()
+        per = [st["nz%d" % l] for l in range(len(self.model_layers()))]
+        return sum(per), per
+
+    def model_layers(self):
+        l = 0
+        while self.model.stat_index("nz%d" % l) >= 0:
+            l += 1
+        return range(l)
+
+
+class DfpRun:
+    """An ito_dfp16_model with two seeded input batches resident in HBM,
+    alternating; with adaptive precision the epoch-end adjustment (a host
+    synchronisation) runs inside the step that ends an epoch."""
+
+    def __init__(self, w):
+        import torch
+        import integer_only_nn_gb300 as ito
+        import seeded_inputs as si
+        self.w = w
+        self.stream = torch.cuda.current_stream()
+        self.model = ito.Dfp16Model(list(w.dims), w.batch, w.exp_w, w.eta)
+        for l, W in enumerate(si.make_weights(w)):
+            self.model.set_weights(l, W)
+        self.xs = [torch.from_numpy(si.make_batch(w, t)[0]).cuda() for t in range(2)]
+        a = w.apt
+        if a is not None:
+            self.model.apt_enable(a.k_init, a.k_min, a.k_max, a.t_min, a.t_max, a.eval_every)
+        self.step_no = 0
+        torch.cuda.synchronize()
+
+    def before(self, k):
+        pass
+
+    def _epoch_end(self):
+        a = self.w.apt
+        if a is not None and self.step_no % a.epoch == a.epoch - 1:
+            self.model.apt_epoch_end()
+        self.step_no += 1
+
+    def step(self, k):
+        self.model.train_step(self.xs[k % 2], self.w.exp_x)
+        self._epoch_end()
+
+    def step_host_async(self, xh, st_h):
+        self.model.train_step_host_async(xh, self.w.exp_x, st_h)
+        self._epoch_end()
+
+    def warm(self, n):
+        import torch
+        for i in range(n):
+            self.step(i)
+        torch.cuda.synchronize()
+
+    def nonzero_updates(self):
+        st = self.model.stats()
+        per = [int(st["nz%d" % l]) for l in range(self.model.n_layers)]
+        return sum(per), per
+
+
+def gemm_roofline(prof, pk, pk_src):
+    """Contraction rate over the profiled launches against the measured burst
+    bf16 peak (the contraction launches are timed inside steps of a few ms, not
+    a seconds-long loop); the sustained figure beside it."""
+    g_ms, g_work, g_n = prof["gemm"]
+    achieved = g_work / (g_ms / 1000.0) / 1e12
+    burst, sust = float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"])
+    return {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s", "frac": achieved / burst,
+            "peak_source": "bf16_tflops (burst), %s" % pk_src, "peak_sustained": sust,
+            "frac_of_sustained": achieved / sust, "launches_timed": g_n}
+
+
+def workload_entry(w, args, flush, pk, pk_src, cpu):
+    """Step time, throughput, contraction roofline fraction and nonzero weight
+    updates of one more workload, timed in the same process as the headline."""
+    run = DfpRun(w) if w.kind == "dfp16" else ModelRun(w, graphs=not args.no_graphs)
+    K = args.steps
+    run.warm(args.warmup)
+    ms, per = timed_median(K, REPEATS, run.stream, flush, run.before, run.step)
+    nz, nz_per = run.nonzero_updates()
+    classes = ("gemm", "down", "update", "other") if w.kind == "dfp16" else ("gemm", "requant", "update", "other")
+    prof, prof_ms = profiled_steps(run.model, K, run.stream, flush, run.before, run.step, classes)
+    ops = algorithmic_ops(w)
+    e = {"batch": w.batch, "ms_per_step": ms, "ms_per_step_repeats": per, "samples_per_s": w.batch / (ms / 1e3),
+         "gemm_roofline": gemm_roofline(prof, pk, pk_src), "gemm_ms_per_step": prof["gemm"][0] / K,
+         "kernels_per_step": run.model.kernels_per_step(),
+         "nonzero_updates_per_step": {"last_step": nz, "per_layer": nz_per}}
+    if w.kind == "dfp16":
+        e["int16_tops"] = ops / (ms / 1e3) / 1e12
+        e["executed_limb_tops"] = 4 * ops / (ms / 1e3) / 1e12
+        e["gemm_roofline"]["work"] = "executed bf16 operations, 8*M*N*K per contraction"
+    else:
+        e["int_tops"] = ops / (ms / 1e3) / 1e12
+    if cpu is not None:
+        e["cpu_baseline"] = cpu
+    del run
+    return e
+
+
 def run_ours(args, w):
     import torch
     import integer_only_nn_gb300 as ito
@@ -282,112 +483,83 @@ def run_ours(args, w):
         if dist is not None:
             dist.barrier()
 
-    # cpu baseline first (rank 0, one GPU): before the GPU work, so no CUDA
-    # context competes with the host cores
+    # CPU baselines first (rank 0, one GPU), before any GPU work
     cpu = None
+    extra = [] if (world > 1 or args.no_workloads) else [int(v) for v in args.workloads.split(",") if v != ""]
+    extra = [si.by_name(i) for i in extra if si.by_name(i).name != w.name]
+    extra_cpu = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt, cores, nsteps, nsamp, single = cpu_baseline(w, args.cpu_batch)
         cpu = {"value": v, "unit": "samples/s", "cores": cores, "kind": "oracle",
                "sample": "%d oracle training steps (C loops, OpenMP over output rows) on %d of the %d samples "
                          "of %s, %.1f s" % (nsteps, nsamp, w.batch, w.name, dt),
                "single_thread": single}
+        for x in extra:
+            v, dt, cores, nsteps, nsamp, _ = cpu_baseline(x, args.cpu_batch, min_seconds=3.0, single_seconds=None)
+            extra_cpu[x.name] = {"value": v, "unit": "samples/s", "cores": cores, "kind": "oracle",
+                                 "sample": "%d steps on %d of %d samples, %.1f s" % (nsteps, nsamp, x.batch, dt)}
 
+    pk, pk_src = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     if w.kind == "dfp16":
-        return run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local)
-    # the step runs on a side stream so that it can replay from CUDA graphs
-    stream = torch.cuda.Stream()
-    model = ito.Model(ito.layers_for(w), w.batch)
-    for l, W in enumerate(si.make_weights(w)):
-        model.set_weights(l, W, stream=stream)
-    model.use_graphs(not args.no_graphs)
+        line = run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local, flush, pk, pk_src)
+    else:
+        line = run_ours_model(args, w, cpu, barrier, dist, world, rank, local, flush, pk, pk_src)
+    if line is not None and extra:
+        line["workloads"] = {x.name: workload_entry(x, args, flush, pk, pk_src, extra_cpu.get(x.name))
+                             for x in extra}
+        if ito.ito_get_error() != 0:
+            raise RuntimeError("device error word set after the extra workloads")
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_ours_model(args, w, cpu, barrier, dist, world, rank, local, flush, pk, pk_src):
+    import torch
+    import integer_only_nn_gb300 as ito
+    run = ModelRun(w, graphs=not args.no_graphs)
+    model, stream = run.model, run.stream
     overlap_mode = model.overlap()
     speculate = model.speculation()
-    # NB distinct seeded batches resident in HBM; before each step (untimed) the step's batch
-    # is copied into the model's fixed input buffers, which the captured step graph reads
-    nb = NB_BATCHES
-    xs, ls = [], []
-    for t in range(nb):
-        x, labels = si.make_batch(w, t)
-        xs.append(torch.from_numpy(x).cuda())
-        ls.append(torch.from_numpy(labels).cuda())
-    xbuf, lbuf = torch.empty_like(xs[0]), torch.empty_like(ls[0])
-    torch.cuda.synchronize()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     K, Wm = args.steps, args.warmup
-
-    def step(t):
-        with torch.cuda.stream(stream):
-            xbuf.copy_(xs[t % nb])
-            lbuf.copy_(ls[t % nb])
-        model.train_step(xbuf, lbuf, stream=stream)
-
-    for i in range(Wm):
-        step(i)
-    stream.synchronize()
+    run.warm(Wm)
     assert ito.ito_get_error() == 0
 
-    # the timed region: K steps, each after an untimed L2 flush and input copy, bracketed by
-    # CUDA events on the step's stream (no per-kernel events inside)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    # the timed region: REPEATS loops of K steps, each step after an untimed L2 flush and
+    # input copy, bracketed by CUDA events on the step's stream (no per-kernel events inside)
     clocks = Clocks(local)
     barrier()
     torch.cuda.synchronize()
     spec0 = model.tensor("spec_count").cpu().tolist()
     clocks.start()
-    with torch.cuda.stream(stream):
-        for k in range(K):
-            flush.fill_(k & 0xFF)
-            xbuf.copy_(xs[k % nb])
-            lbuf.copy_(ls[k % nb])
-            starts[k].record(stream)
-            model.train_step(xbuf, lbuf, stream=stream)
-            ends[k].record(stream)
+    ms, per = timed_median(K, REPEATS, stream, flush, run.before, run.step)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     spec1 = model.tensor("spec_count").cpu().tolist()
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
     err = ito.ito_get_error()
     if err != 0:
         raise RuntimeError("device error word %d after the timed steps" % err)
-    total_ms = max_over_ranks(total_ms, dist)
+    nz, nz_per = run.nonzero_updates()
+    ms = max_over_ranks(ms, dist)
     launches = model.kernels_per_step()
 
-    # per-kernel timing: the same K steps again with a pair of events around every launch,
-    # on the launch's own stream (captured into the step graphs as event-record nodes)
-    model.profile(True)
-    for i in range(4):
-        step(i)
-    model.profile_read()
-    prof = {c: [0.0, 0.0, 0] for c in ("gemm", "requant", "update", "other")}
-    pstarts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    pends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for k in range(K):
-            flush.fill_(k & 0xFF)
-            xbuf.copy_(xs[k % nb])
-            lbuf.copy_(ls[k % nb])
-            pstarts[k].record(stream)
-            model.train_step(xbuf, lbuf, stream=stream)
-            pends[k].record(stream)
-            for c, (ms, work, n) in model.profile_read().items():
-                prof[c][0] += ms
-                prof[c][1] += work
-                prof[c][2] += n
-    torch.cuda.synchronize()
-    prof_ms = sum(s.elapsed_time(e) for s, e in zip(pstarts, pends))
-    model.profile(False)
+    # per-kernel timing: the same K steps again with a pair of events around every launch
+    prof, prof_ms = profiled_steps(model, K, stream, flush, run.before, run.step,
+                                   ("gemm", "requant", "update", "other"))
     if ito.ito_get_error() != 0:
         raise RuntimeError("device error word set after the profiled steps")
 
     # end to end through the host-buffer entry points: each step copies its own input
-    # batch (the NB resident batches' pinned host copies, in turn) in and its stats out.
+    # batch (the resident batches' pinned host copies, in turn) in and its stats out.
     # Pipelined (ito_train_step_host_async: the next batch's copy overlaps the step, one
     # wait after the last step) and blocking (ito_train_step_host: a wait every step).
-    xs_h = [x.cpu().pin_memory() for x in xs]
-    ls_h = [lab.cpu().pin_memory() for lab in ls]
+    nb = NB_BATCHES
+    xs_h = [x.cpu().pin_memory() for x in run.xs]
+    ls_h = [lab.cpu().pin_memory() for lab in run.ls]
     x_h, l_h = xs_h[0], ls_h[0]
     st_h = torch.zeros(model.num_stats(), dtype=torch.int32).pin_memory()
     for i in range(3):
@@ -413,20 +585,9 @@ def run_ours(args, w):
     # with a contraction (the timed steps above overlap them); per-kernel figures only
     model.set_overlap(0)
     model.set_speculation(False)
-    model.profile(True)
-    for i in range(4):
-        step(i)
-    model.profile_read()
     iso_steps = 10
-    iso = {c: [0.0, 0.0, 0] for c in prof}
-    for k in range(iso_steps):
-        flush.fill_(k & 0xFF)
-        step(k)
-        for c, (ms, work, n) in model.profile_read().items():
-            iso[c][0] += ms
-            iso[c][1] += work
-            iso[c][2] += n
-    model.profile(False)
+    iso, _ = profiled_steps(model, iso_steps, stream, flush, run.before, run.step,
+                            ("gemm", "requant", "update", "other"))
     model.set_overlap(overlap_mode)
     model.set_speculation(speculate)
 
@@ -437,61 +598,45 @@ def run_ours(args, w):
         # nonzero weight steps) for a few steps after the timed ones, one JSON line each
         with open(args.stats_log, "w") as f:
             for t in range(10):
-                step(t)
-                stream.synchronize()
+                run.warm(1)
                 f.write(json.dumps({"step": t, **{k: int(v) for k, v in model.stats().items()}}) + "\n")
 
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
-        return 0
-    pk, pk_src = peaks()
+        return None
     samples = world * w.batch * K
-    value = job_throughput(w.batch * K, world, total_ms / 1000.0)
-    g_ms, g_work, g_n = prof["gemm"]
-    prof = {c: tuple(v) for c, v in prof.items()}
-    g_tflops = g_work / (g_ms / 1000.0) / 1e12
-    peak = float(pk["bf16_tflops_sustained"])
+    value = job_throughput(w.batch, world, ms / 1000.0)
+    roof = gemm_roofline(prof, pk, pk_src)
+    roof.update({"kernel": "k_gemm_tc2 / k_gemm_tc (bf16-embedded int8 contractions; re-launches after a "
+                           "misprediction not counted)",
+                 "traffic": gemm_traffic_per_launch(w), "traffic_unit": "bytes per launch (ncu, committed summary)",
+                 "measured_over": "the same %d steps run again with an event pair around every launch "
+                                  "(%.4f ms per step with the events)" % (K, prof_ms)})
     hbm = float(pk["hbm_gbs"])
     line = {
         "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world, "steps": K, "warmup": Wm,
-        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims),
-                   "l2": "flushed by a 256 MB write before every timed step; flush not timed",
-                   "graphs": not args.no_graphs,
-                   "backward_overlap": OVERLAP_MODES[overlap_mode],
-                   "speculative_requantisation": ("forward and delta-propagation epilogues requantise with the "
-                                                  "previous step's shift and write no int32 result; a one-word "
-                                                  "check per contraction, and a re-launch of the contraction when "
-                                                  "this step's shift differs; %d of %d predictions held (the "
-                                                  "model's counters over the timed region)"
-                                                  % (spec_hits, spec_hits + spec_misses))
-                                                 if speculate else "off",
-                   "inputs": "%d seeded batches resident in HBM, each step's copied into the model's input "
-                             "buffers before the step (not timed)" % nb,
+                   "l2": "flushed before every step (256 MB write, untimed)",
+                   "timing": "median of %d loops of %d steps" % (REPEATS, K),
+                   "graphs": not args.no_graphs, "backward_overlap": overlap_mode,
+                   "speculation": ("on, %d/%d shift predictions held" % (spec_hits, spec_hits + spec_misses))
+                                  if speculate else "off",
+                   "inputs": "%d resident batches" % nb,
                    "parallelism": "replicas" if world > 1 else "single"},
-        "int_tops": algorithmic_ops(w) * world * K / (total_ms / 1000.0) / 1e12,
-        "roofline": {"bound": "tensor",
-                     "kernel": "k_gemm_tc2 / k_gemm_tc (bf16-embedded int8 contractions, every contraction launch "
-                               "of the step; re-launches after a misprediction are not counted as contractions)",
-                     "achieved": g_tflops, "peak": peak, "unit": "TFLOP/s", "frac": g_tflops / peak,
-                     "peak_source": "bf16_tflops_sustained, %s" % pk_src,
-                     "traffic": gemm_traffic_per_launch(w), "traffic_unit": "bytes per launch (ncu, committed summary)",
-                     "launches_timed": g_n,
-                     "measured_over": "the same %d steps run again with an event pair around every launch on its "
-                                      "own stream (%.4f ms per step with the events, %.4f without)"
-                                      % (K, prof_ms / K, total_ms / K)},
+        "ms_per_step_repeats": per,
+        "int_tops": algorithmic_ops(w) * world / (ms / 1000.0) / 1e12,
+        "nonzero_updates_per_step": {"last_step": nz, "per_layer": nz_per,
+                                     "note": "weight steps that are nonzero (Step 4's operand is the shifted, "
+                                             "saturated gradient: none once the gradient shift reaches 10)"},
+        "roofline": roof,
         "passes": {"note": "kernel time per step by class over the profiled steps (overlapped launches include "
-                           "their wait for SM resources; speculating contractions leave the requantisation class "
-                           "a one-word check and a re-launch that returns at once when the prediction held); "
-                           "per-pass bandwidth is under 'isolated'",
+                           "their wait for SM resources); per-pass bandwidth is under 'isolated'",
                    "hbm_peak_gbs": hbm, "peak_source": pk_src,
                    "ms_per_step": {k: v[0] / K for k, v in prof.items()}},
-        "isolated": {"note": "the step on one stream (no bandwidth pass beside a contraction) and without "
-                             "speculative requantisation, %d steps: per-kernel rates of every pass" % iso_steps,
+        "isolated": {"note": "one stream, no speculation, %d steps: per-kernel rates" % iso_steps,
                      "gemm_tflops": iso["gemm"][1] / (iso["gemm"][0] / 1000.0) / 1e12,
-                     "gemm_frac": iso["gemm"][1] / (iso["gemm"][0] / 1000.0) / 1e12 / peak,
+                     "gemm_frac": iso["gemm"][1] / (iso["gemm"][0] / 1000.0) / 1e12 / roof["peak"],
                      "requant_gbs": iso["requant"][1] / (iso["requant"][0] / 1000.0) / 1e9,
                      "update_gbs": iso["update"][1] / (iso["update"][0] / 1000.0) / 1e9,
                      "ms_per_step": {c: v[0] / iso_steps for c, v in iso.items()}},
@@ -503,14 +648,12 @@ def run_ours(args, w):
                 "blocking_value": samples / e2e_sync_s,
                 "blocking_call": "ito_train_step_host (copy, step, stats copy, wait, every step)"},
         "gpu_launches": launches * K,
+        "gpu_launches_all_repeats": launches * K * REPEATS,
         "clocks": clk,
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
-    print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+    return line
 
 
 def run_op(args):
@@ -559,135 +702,83 @@ def run_op(args):
     return 0
 
 
-def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local):
+def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local, flush, pk, pk_src):
     """Step time of the DFP16 workload (device-timed with CUDA events)."""
     import torch
     import integer_only_nn_gb300 as ito
-    import seeded_inputs as si
-    stream = torch.cuda.current_stream()
-    model = ito.Dfp16Model(list(w.dims), w.batch, w.exp_w, w.eta)
-    for l, W in enumerate(si.make_weights(w)):
-        model.set_weights(l, W)
-    xs = [torch.from_numpy(si.make_batch(w, t)[0]).cuda() for t in range(2)]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    run = DfpRun(w)
+    model, stream = run.model, run.stream
     K = args.steps
-    apt = w.apt
-    if apt is not None:
-        # adaptive precision (Algorithm 2): the epoch-end adjustment, with its host
-        # synchronisation, runs inside the timed window of the step that ends an epoch
-        model.apt_enable(apt.k_init, apt.k_min, apt.k_max, apt.t_min, apt.t_max, apt.eval_every)
-    step_no = [0]
-
-    def one_step(x):
-        model.train_step(x, w.exp_x)
-        if apt is not None and step_no[0] % apt.epoch == apt.epoch - 1:
-            model.apt_epoch_end()
-        step_no[0] += 1
-
-    for i in range(args.warmup):
-        one_step(xs[i % 2])
-    torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    run.warm(args.warmup)
     clocks = Clocks(local)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
-    for k in range(K):
-        flush.fill_(k & 0xFF)
-        starts[k].record(stream)
-        one_step(xs[k % 2])
-        ends[k].record(stream)
+    ms, per = timed_median(K, REPEATS, stream, flush, run.before, run.step)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     if ito.ito_get_error() != 0:
         raise RuntimeError("device error word set after the timed steps")
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    total_ms = max_over_ranks(total_ms, dist)
+    nz, nz_per = run.nonzero_updates()
+    ms = max_over_ranks(ms, dist)
     launches = model.kernels_per_step()
 
     # per-kernel timing: the same K steps again with an event pair around every launch
-    model.profile(True)
-    prof = {c: [0.0, 0.0, 0] for c in ("gemm", "down", "update", "other")}
-    pstarts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    pends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for k in range(K):
-        flush.fill_(k & 0xFF)
-        pstarts[k].record(stream)
-        one_step(xs[k % 2])
-        pends[k].record(stream)
-        for c, (ms, work, n) in model.profile_read().items():
-            prof[c][0] += ms
-            prof[c][1] += work
-            prof[c][2] += n
-    torch.cuda.synchronize()
-    prof_ms = sum(s.elapsed_time(e) for s, e in zip(pstarts, pends))
-    model.profile(False)
+    prof, prof_ms = profiled_steps(model, K, stream, flush, run.before, run.step, ("gemm", "down", "update", "other"))
 
     # end to end through the public API: each step copies its input mantissas from pinned
     # host memory and its statistics back. Pipelined (ito_dfp16_train_step_host_async: the
     # next batch's copy overlaps the step, one wait after the last step) and blocking (a
     # host-to-device copy, the step and a statistics read with a wait, every step)
-    xs_h = [x.cpu().pin_memory() for x in xs]
+    xs_h = [x.cpu().pin_memory() for x in run.xs]
     st_h = torch.zeros(model.num_stats(), dtype=torch.int64).pin_memory()
-
-    def one_step_host(xh):
-        model.train_step_host_async(xh, w.exp_x, st_h)
-        if apt is not None and step_no[0] % apt.epoch == apt.epoch - 1:
-            model.apt_epoch_end()
-        step_no[0] += 1
-
     for i in range(3):
-        one_step_host(xs_h[i % 2])
+        run.step_host_async(xs_h[i % 2], st_h)
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
     for k in range(K):
-        one_step_host(xs_h[k % 2])
+        run.step_host_async(xs_h[k % 2], st_h)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist)
     for i in range(3):
-        xd = xs_h[i % 2].to("cuda", non_blocking=True)
-        one_step(xd)
+        run.xs[i % 2] = xs_h[i % 2].to("cuda", non_blocking=True)
+        run.step(i)
         model.stats()
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for k in range(K):
-        xd = xs_h[k % 2].to("cuda", non_blocking=True)
-        one_step(xd)
-        st = model.stats()
+        run.xs[k % 2] = xs_h[k % 2].to("cuda", non_blocking=True)
+        run.step(k)
+        model.stats()
     e2e_sync_s = max_over_ranks(time.perf_counter() - t0, dist)
     if ito.ito_get_error() != 0:
         raise RuntimeError("device error word set after the end-to-end steps")
     if rank != 0:
-        return 0
-    pk, pk_src = peaks()
-    peak = float(pk["bf16_tflops_sustained"])
-    g_ms, g_work, g_n = prof["gemm"]
-    g_tflops = g_work / (g_ms / 1000.0) / 1e12
+        return None
     ops = algorithmic_ops(w)
-    line = {"metric": METRIC, "value": world * w.batch * K / (total_ms / 1000.0), "unit": "samples/s",
-            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+    roof = gemm_roofline(prof, pk, pk_src)
+    roof.update({"kernel": "k_gemm_dfp2 / k_gemm_dfp (int16 limb contractions: four bf16 limb products per "
+                           "int16 multiply-add, exact int64 sums)",
+                 "work": "executed bf16 operations, 8*M*N*K per contraction", "traffic": None,
+                 "measured_over": "the same %d steps run again with an event pair around every launch "
+                                  "(%.4f ms per step with the events)" % (K, prof_ms)})
+    line = {"metric": METRIC, "value": world * w.batch / (ms / 1000.0), "unit": "samples/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int16 (DFP16)",
             "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "dims": list(w.dims), "eta": w.eta,
-                       "l2": "flushed by a 256 MB write before every timed step; flush not timed",
-                       "inputs": "2 seeded batches resident in HBM, alternating",
+                       "l2": "flushed before every step (256 MB write, untimed)",
+                       "timing": "median of %d loops of %d steps" % (REPEATS, K),
+                       "inputs": "2 resident batches, alternating",
                        "parallelism": "replicas" if world > 1 else "single"},
-            "int16_tops": ops * world * K / (total_ms / 1000.0) / 1e12,
-            "executed_limb_tops": 4 * ops * world * K / (total_ms / 1000.0) / 1e12,
-            "roofline": {"bound": "tensor",
-                         "kernel": "k_gemm_dfp2 / k_gemm_dfp (int16 limb contractions: four bf16 limb products "
-                                   "per int16 multiply-add, exact int64 sums)",
-                         "achieved": g_tflops, "peak": peak, "unit": "TFLOP/s", "frac": g_tflops / peak,
-                         "work": "executed bf16 operations, 8*M*N*K per contraction",
-                         "peak_source": "bf16_tflops_sustained, %s" % pk_src, "traffic": None,
-                         "launches_timed": g_n,
-                         "measured_over": "the same %d steps run again with an event pair around every launch "
-                                          "(%.4f ms per step with the events, %.4f without)"
-                                          % (K, prof_ms / K, total_ms / K)},
+            "ms_per_step_repeats": per,
+            "int16_tops": ops * world / (ms / 1000.0) / 1e12,
+            "executed_limb_tops": 4 * ops * world / (ms / 1000.0) / 1e12,
+            "nonzero_updates_per_step": {"last_step": nz, "per_layer": nz_per},
+            "roofline": roof,
             "passes": {"ms_per_step": {c: v[0] / K for c, v in prof.items()},
                        "down_gbs": prof["down"][1] / (prof["down"][0] / 1000.0) / 1e9 if prof["down"][0] else None,
                        "update_gbs": (prof["update"][1] / (prof["update"][0] / 1000.0) / 1e9
@@ -701,15 +792,16 @@ def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local):
                     "blocking_value": world * w.batch * K / e2e_sync_s,
                     "blocking_call": "host-to-device copy, ito_dfp16_train_step, statistics read, every step"},
             "gpu_launches": launches * K,
+            "gpu_launches_all_repeats": launches * K * REPEATS,
             "clocks": clk}
+    apt = w.apt
     if apt is not None:
         line["config"]["apt"] = {"k_init": apt.k_init, "k_min": apt.k_min, "k_max": apt.k_max, "t_min": apt.t_min,
                                  "t_max": str(apt.t_max), "epoch_steps": apt.epoch, "eval_every": apt.eval_every}
         line["apt_bits_after"] = [model.precision(l)[0] for l in range(model.n_layers)]
     if cpu is not None:
         line["cpu_baseline"] = cpu
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 def main():
@@ -722,6 +814,9 @@ def main():
     ap.add_argument("--cpu-batch", type=int, default=128, help="samples in the CPU-oracle baseline step")
     ap.add_argument("--ref-batch", type=int, default=16, help="samples per reference-arm oracle step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default="0,1,2,4",
+                    help="more workloads timed after the headline one, reported under 'workloads'")
+    ap.add_argument("--no-workloads", action="store_true", help="time the headline workload only")
     ap.add_argument("--no-graphs", action="store_true", help="launch every kernel directly (no CUDA graphs)")
     ap.add_argument("--op", choices=("fwd", "dgrad", "wgrad", "dfp16_fwd_f32", "bdfp16_fwd_f32"),
                     help="time one single-layer call instead")

@@ -125,6 +125,7 @@ class Workload:
     fc: tuple = ()            # cnn: (IC, OC) of the final Linear
     sigma: float = 32.0       # weight normal sigma
     lim: int = 127            # clamp for weights and inputs
+    in_lim: int = 127         # mlp/cnn: int8 inputs uniform in [-in_lim, in_lim]
     exp_x: int = 0            # dfp16 shared exponents of input and weights
     exp_w: int = 0
     eta: int = 20             # dfp16 integer SGD learning rate 2^-eta (on the batch-summed gradient)
@@ -157,6 +158,10 @@ WORKLOADS = (
     Workload(7, "dfp16_2048x3_b2048_apt6", "dfp16", 2048, dims=(2048, 2048, 2048, 2048),
              sigma=4096.0, lim=32767, exp_x=-12, exp_w=-17,
              apt=AptSetting(k_init=6, k_min=2, k_max=16, t_min=100.0, t_max=float("inf"), epoch=10, eval_every=1)),
+    # the 4096-wide MLP at batch 256 with inputs in [-7, 7]: the first layer's weight
+    # gradient is small enough for its weights to move (the wider-input workloads' do not)
+    Workload(8, "mlp4096x4-1000_b256_x7", "mlp", 256, dims=(4096, 4096, 4096, 4096, 4096, 1000),
+             classes=1000, in_lim=7),
 )
 
 
@@ -211,8 +216,8 @@ def input_shape(w: Workload) -> tuple:
 
 
 def make_batch(w: Workload, step: int):
-    """(x, labels) for one step. mlp/cnn: int8 x uniform in [-127, 127] (uint8
-    in [0, 255] for a UINT8-input workload), int32 labels uniform in
+    """(x, labels) for one step. mlp/cnn: int8 x uniform in [-in_lim, in_lim]
+    (uint8 in [0, 255] for a UINT8-input workload), int32 labels uniform in
     [0, classes). dfp16: int16 x = round(N(0, sigma)) clamped, labels None."""
     shp = input_shape(w)
     n = int(np.prod(shp))
@@ -222,7 +227,7 @@ def make_batch(w: Workload, step: int):
     if w.input_uint8:
         x = uniform_int(w.seed, batch_stream(step, 0), n, 0, 255).astype(np.uint8).reshape(shp)
     else:
-        x = uniform_int(w.seed, batch_stream(step, 0), n, -127, 127).astype(np.int8).reshape(shp)
+        x = uniform_int(w.seed, batch_stream(step, 0), n, -w.in_lim, w.in_lim).astype(np.int8).reshape(shp)
     labels = uniform_int(w.seed, batch_stream(step, 1), w.batch, 0, w.classes - 1).astype(np.int32)
     return x, labels
 

@@ -204,6 +204,32 @@ def test_mispredicted_shift_relaunch_matches_oracle(index, steps, route):
     assert g.ito.ito_get_error() == 0
 
 
+def test_moving_weights_at_4096_width_with_speculation():
+    """The 4096-wide MLP at batch 256 with inputs in [-7, 7]: the first layer's
+    weights move every step (its gradient shift is 7, weight shift 5), while
+    every forward and delta-propagation contraction that can runs on the CTA
+    pair with a speculating epilogue. Four steps in lockstep with the oracle:
+    the speculating forward of layer 0 reads weights that changed since the
+    step whose shift it predicts from."""
+    w = si.by_name(8)
+    g = GpuRun(w, speculate_min_elems=1)
+    assert g.model.speculation()
+    nl = g.n_layers
+    weights = si.make_weights(w)
+    moved = 0
+    for t in range(4):
+        rec = _oracle_step(w, weights, t, "f64")
+        g.step(t)
+        compare_records(rec, g.record(), t)
+        assert rec["nz0"] > 0
+        moved += int((rec["w0"] != weights[0]).sum())
+        weights = [rec["w%d" % l] for l in range(len(weights))]
+        used = g.model.tensor("spec").cpu().numpy()[4 * nl: 6 * nl]
+        assert used[0] != 0 and used[nl + 1] != 0      # layer 0 forward, layer 1 delta propagation
+    assert moved > 0
+    assert g.ito.ito_get_error() == 0
+
+
 def test_speculation_covers_large_contractions_only():
     """By default only contractions with at least 2^22 output elements
     speculate: none of the 784-1024x3-10 MLP (batch 256), all the 4096-wide

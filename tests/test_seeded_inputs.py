@@ -49,3 +49,11 @@ def test_workload_shapes():
     assert [a.shape for a in ws] == [(64, 3, 3, 3), (128, 3, 3, 64), (256, 3, 3, 128), (10, 256)]
     x, labels = si.make_batch(si.by_name(4), 0)
     assert x.dtype == np.int16 and labels is None
+
+
+def test_narrow_input_workload():
+    w = si.by_name(8)
+    x, labels = si.make_batch(w, 0)
+    assert x.shape == (256, 4096) and x.min() == -7 and x.max() == 7
+    assert labels.max() <= 999
+    assert si.weight_shapes(w) == si.weight_shapes(si.by_name(3))
