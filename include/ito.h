@@ -561,6 +561,32 @@ int ito_dfp16_linear_fwd_f32(const int16_t *x, const int32_t *d_exp_x, const int
                              int B, int IC, int OC, void *workspace, size_t workspace_bytes, int64_t *p64,
                              uint64_t *d_max, float *y, void *stream);
 
+/* DFP16 Linear forward with an FP32 output by the page's partial-accumulation
+ * scheme ("Mixed Precision Training of Convolutional Neural Networks using
+ * Integer Operations", section 4, "Handling overflows": INT16 products overflow
+ * an INT32 accumulator after a few terms, so the kernels keep the accumulation
+ * chains short and shift the inputs by one bit, convert each chain's INT32
+ * partial to FP32, scale it by 2^(E_inp + E_wt) and accumulate it in FP32):
+ *   x'  = input_shift ? round-half-up(x / 2) : x,  E_inp = *d_exp_x + input_shift
+ *   for each chain j of `chain` consecutive ic (the last one shorter):
+ *     p_j = (sum over the chain of x'[b][ic] * W[oc][ic]) modulo 2^32, as a
+ *           two's-complement INT32 accumulator holds it
+ *     t_j = float(float(p_j) * 2^(E_inp + *d_exp_w))  (to nearest even; the
+ *           scaling itself is exact)
+ *   y[b][oc] = (((0 + t_0) + t_1) + ...) with every addition rounded to float.
+ * The page fixes no chain length: chain is a multiple of 64 in [64, 512]. A
+ * chain whose sum leaves int32 wraps, as the page's hardware would; the
+ * one-bit shift makes that impossible for chains of up to 3 terms and rare in
+ * practice. x: int16 [B][IC] with exponent *d_exp_x; W: int16 [OC][IC] with
+ * *d_exp_w; y: float [B][OC]. Workspace as ito_dfp16_linear_fwd. Exponents
+ * outside int8 raise ITO_ERR_EXPONENT in the device error word.
+ * Errors: ITO_ERR_ARG (NULL pointer, bad chain or input_shift, workspace),
+ * ITO_ERR_SHAPE. */
+int ito_dfp16_linear_fwd_f32_chained(const int16_t *x, const int32_t *d_exp_x, const int16_t *W,
+                                     const int32_t *d_exp_w, int B, int IC, int OC, int32_t chain,
+                                     int32_t input_shift, void *workspace, size_t workspace_bytes, float *y,
+                                     void *stream);
+
 /* Blocked-DFP ("Mixed Precision Training of Convolutional Neural Networks
  * using Integer Operations", section 3: Blocked-DFP raises the effective
  * range with several fine-grained exponents per tensor; the page gives no

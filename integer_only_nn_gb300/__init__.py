@@ -93,6 +93,7 @@ _SIGS = {
     "ito_dfp16_from_float": (_I, [_P, _I64, _P, _P, _P, _P]),
     "ito_dfp16_to_float": (_I, [_P, _P, _I64, _P, _P]),
     "ito_dfp16_linear_fwd_f32": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P, _P, _P, _P]),
+    "ito_dfp16_linear_fwd_f32_chained": (_I, [_P, _P, _P, _P, _I, _I, _I, _I32, _I32, _P, _SZ, _P, _P]),
     "ito_dfp16_model_create": (_I, [_P, _I, _I, _I32, _I32, ctypes.POINTER(_P)]),
     "ito_dfp16_model_destroy": (_I, [_P]),
     "ito_dfp16_model_set_weights": (_I, [_P, _I, _P, _I, _P]),
@@ -650,6 +651,18 @@ def ito_dfp16_linear_fwd_f32(x, exp_x, W, exp_w, stream=None):
     _check(_lib.ito_dfp16_linear_fwd_f32(_ptr(x), _ptr(exp_x), _ptr(W), _ptr(exp_w), B, IC, OC, _aligned256(ws), n,
                                          _ptr(p64), _ptr(mx), _ptr(y), _stream(stream)))
     return p64, y
+
+
+def ito_dfp16_linear_fwd_f32_chained(x, exp_x, W, exp_w, chain, input_shift=1, stream=None):
+    """-> y float32 [B][OC] (FP32 partial accumulation over INT32 chains of `chain` terms)"""
+    torch = _torch()
+    B, IC = x.shape
+    OC = W.shape[0]
+    y = torch.empty((B, OC), dtype=torch.float32, device="cuda")
+    ws, n = _dfp_ws(B, IC, OC)
+    _check(_lib.ito_dfp16_linear_fwd_f32_chained(_ptr(x), _ptr(exp_x), _ptr(W), _ptr(exp_w), B, IC, OC, int(chain),
+                                                 int(input_shift), _aligned256(ws), n, _ptr(y), _stream(stream)))
+    return y
 
 
 class Dfp16Model:

@@ -50,27 +50,39 @@ __device__ __forceinline__ void limb_split(int32_t v, int32_t& h, int32_t& l)
 // product to float or int rounds once, like ldexpf
 __device__ __forceinline__ double pow2d(int k) { return __longlong_as_double((long long)(k + 1023) << 52); }
 
-// Blocked-DFP operands (BLOCKED): the exact chunk is one exponent block of the
-// contraction; after each chunk the epilogue scales its exact int64 partial by
-// 2^(ex[row][chunk] + ew[col][chunk]) and adds it in double, and the tile is
-// written as float (Y) instead of int64 (C).
-struct DfpBlocked {
-    const int8_t* ex;   // [M][nb]
-    const int8_t* ew;   // [N][nb]
+// Drain modes of the limb kernel. DFP_EXACT: the tile's exact int64 sums go to C.
+// The two FP32-output modes write the tile as float (Y) instead:
+// DFP_BLOCKED (Blocked-DFP operands): the exact chunk is one exponent block of
+//   the contraction; after each chunk the epilogue scales its exact int64
+//   partial by 2^(ex[row][chunk] + ew[col][chunk]) and adds it in double.
+// DFP_CHAINED (the FP32 partial accumulation of "Mixed Precision Training...",
+//   section 4, "Handling overflows"): the exact chunk is one accumulation chain;
+//   its sum is taken modulo 2^32 as an INT32 accumulator would hold it, converted
+//   to float, scaled by 2^(*d_ex + shift + *d_ew) (exact in double, rounded once
+//   to float) and added to the float output in chain order.
+enum DfpDrain { DFP_EXACT = 0, DFP_BLOCKED = 1, DFP_CHAINED = 2 };
+
+struct DfpF32Out {
+    const int8_t* ex;     // DFP_BLOCKED: [M][nb]
+    const int8_t* ew;     // DFP_BLOCKED: [N][nb]
     int nb;
-    float* Y;           // [M][ldy]
+    const int32_t* d_ex;  // DFP_CHAINED: input and weight exponents (device scalars)
+    const int32_t* d_ew;
+    int shift;            // DFP_CHAINED: 1 when the inputs were shifted right by one bit
+    float* Y;             // [M][ldy]
     int64_t ldy;
 };
 
-template <bool A_MN, bool B_MN, bool BLOCKED>
+template <bool A_MN, bool B_MN, int MODE>
 __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
     k_gemm_dfp(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
                const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
-               int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, DfpBlocked bk,
+               int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, DfpF32Out bk,
                int* __restrict__ err)
 {
     using Cfg = DfpCfg;
+    constexpr bool F32OUT = MODE != DFP_EXACT;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;                        // 32 columns per epilogue warp
     constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
@@ -215,17 +227,24 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
         bool ok = true;
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             const int tm = t / num_n, tn = t % num_n;
-            // BLOCKED: the double sums live in the same registers as the int64 ones
+            // FP32 outputs: the double (BLOCKED) or float (CHAINED) sums live in the same
+            // registers as the int64 ones; both start at +0
             int64_t acc[HALF];
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) acc[i] = BLOCKED ? __double_as_longlong(0.0) : 0;
-            const int brow = tm * BM + quad * 32 + lane;                  // this thread's row (BLOCKED)
+            for (int i = 0; i < HALF; ++i) acc[i] = 0;
+            const int brow = tm * BM + quad * 32 + lane;                  // this thread's row (FP32 outputs)
+            int e_chain = 0;                                              // CHAINED: 2^e scales every chain
+            if (MODE == DFP_CHAINED) {
+                const int ex = *bk.d_ex, ew = *bk.d_ew;
+                if (ex < -128 || ex > 127 || ew < -128 || ew > 127) raise_device_error(err, ITO_ERR_EXPONENT);
+                e_chain = max(-300, min(300, ex + bk.shift + ew));
+            }
             for (int c = 0; c < num_chunks; ++c) {
                 if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) +
                                        (uint32_t)(buf * Cfg::BUF_COLS + half * HALF);
-                if (!BLOCKED) {
+                if (MODE == DFP_EXACT) {
                     // one accumulator at a time keeps 16 staging registers live
 #pragma unroll
                     for (int j = 0; j < HALF / 16; ++j) {
@@ -241,7 +260,7 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
                         }
                     }
                 } else {
-                    const int exr = brow < M ? bk.ex[(int64_t)brow * bk.nb + c] : 0;
+                    const int exr = MODE == DFP_BLOCKED && brow < M ? bk.ex[(int64_t)brow * bk.nb + c] : 0;
 #pragma unroll
                     for (int j = 0; j < HALF / 16; ++j) {
                         int64_t pj[16];
@@ -257,13 +276,28 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
                             for (int i = 0; i < 16; ++i)
                                 pj[i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) << sh;
                         }
-                        // the chunk's exact partial (below 2^53) times a power of two: exact
+                        if (MODE == DFP_BLOCKED) {
+                            // the chunk's exact partial (below 2^53) times a power of two: exact
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int col = tn * BN + half * HALF + j * 16 + i;
-                            const int e = exr + (col < N ? bk.ew[(int64_t)col * bk.nb + c] : 0);
-                            acc[j * 16 + i] = __double_as_longlong(__longlong_as_double(acc[j * 16 + i]) +
-                                                                   (double)pj[i] * pow2d(e));
+                            for (int i = 0; i < 16; ++i) {
+                                const int col = tn * BN + half * HALF + j * 16 + i;
+                                const int e = exr + (col < N ? bk.ew[(int64_t)col * bk.nb + c] : 0);
+                                acc[j * 16 + i] = __double_as_longlong(__longlong_as_double(acc[j * 16 + i]) +
+                                                                       (double)pj[i] * pow2d(e));
+                            }
+                        } else {
+                            // the chain as an INT32 accumulator holds it (two's complement, modulo
+                            // 2^32), to float, scaled exactly in double and rounded once, then one
+                            // float addition per chain in chain order
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int32_t p32 = (int32_t)(uint32_t)(unsigned long long)pj[i];
+                                const float term =
+                                    __double2float_rn(__dmul_rn((double)__int2float_rn(p32), pow2d(e_chain)));
+                                acc[j * 16 + i] =
+                                    (uint32_t)__float_as_uint(__fadd_rn(__uint_as_float((uint32_t)acc[j * 16 + i]),
+                                                                        term));
+                            }
                         }
                     }
                 }
@@ -273,13 +307,15 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
                 if (++buf == 2) { buf = 0; buf_phase ^= 1; }
             }
             if (!ok) break;
-            if (BLOCKED) {
+            if (F32OUT) {
                 const int col0 = tn * BN + half * HALF;
                 if (brow < M) {
                     float* dst = bk.Y + (int64_t)brow * bk.ldy + col0;
 #pragma unroll
                     for (int i = 0; i < HALF; ++i)
-                        if (col0 + i < N) dst[i] = __double2float_rn(__longlong_as_double(acc[i]));
+                        if (col0 + i < N)
+                            dst[i] = MODE == DFP_BLOCKED ? __double2float_rn(__longlong_as_double(acc[i]))
+                                                         : __uint_as_float((uint32_t)acc[i]);
                 }
                 continue;
             }
@@ -757,10 +793,10 @@ size_t dfp_split_ws_bytes(int M, int N, int K)
     return parts > 1 ? (size_t)(tiles - full) * parts * 256 * 64 * sizeof(int64_t) : 0;
 }
 
-template <bool A_MN, bool B_MN, bool BLOCKED = false>
+template <bool A_MN, bool B_MN, int MODE = DFP_EXACT>
 static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
 {
-    auto kern = k_gemm_dfp<A_MN, B_MN, BLOCKED>;
+    auto kern = k_gemm_dfp<A_MN, B_MN, MODE>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DfpCfg::SMEM_BYTES) !=
@@ -770,7 +806,7 @@ static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
     }
     const int tiles = ((p.M + DfpCfg::BM - 1) / DfpCfg::BM) * ((p.N + DfpCfg::BN - 1) / DfpCfg::BN);
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    const DfpBlocked bk{p.ex, p.ew, p.nb, p.Y, p.ldy};
+    const DfpF32Out bk{p.ex, p.ew, p.nb, p.d_ex, p.d_ew, p.shift, p.Y, p.ldy};
     kern<<<grid, DfpCfg::THREADS, DfpCfg::SMEM_BYTES, s>>>(p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.mapC,
                                                            p.use_tma_store, p.M, p.N, p.K, p.chunk_kb, p.C, p.ldc,
                                                            p.d_max, bk, p.err);
@@ -854,9 +890,30 @@ int dfp_gemm_plan_blocked(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al
     return ITO_OK;
 }
 
+int dfp_gemm_plan_chained(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, const Bf16View& Bh,
+                          const Bf16View& Bl, int M, int N, int K, int chain, const int32_t* d_ex,
+                          const int32_t* d_ew, int shift, float* Y, int64_t ldy)
+{
+    if (chain < 64 || chain > 512 || chain % 64)
+        return set_error(ITO_ERR_ARG, "chained DFP: chain must be a multiple of 64 in [64, 512]");
+    if (!d_ex || !d_ew || !Y) return set_error(ITO_ERR_ARG, "chained DFP: NULL exponent or output pointer");
+    // single-CTA kernel, every tile whole: the chains of an output are added in order by one thread
+    int r = dfp_gemm_plan(p, Ah, Al, false, Bh, Bl, false, M, N, K, nullptr, 0, nullptr, nullptr, 0);
+    if (r) return r;
+    p->chunk_kb = chain / 64;
+    p->blocked = 2;
+    p->d_ex = d_ex;
+    p->d_ew = d_ew;
+    p->shift = shift ? 1 : 0;
+    p->Y = Y;
+    p->ldy = ldy;
+    return ITO_OK;
+}
+
 int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s)
 {
-    if (p.blocked) return launch_dfp<false, false, true>(p, s);
+    if (p.blocked == 1) return launch_dfp<false, false, DFP_BLOCKED>(p, s);
+    if (p.blocked == 2) return launch_dfp<false, false, DFP_CHAINED>(p, s);
     if (p.pair) {
         if (!p.a_mn && !p.b_mn) return launch_dfp2<false, false>(p, s);
         if (!p.a_mn && p.b_mn) return launch_dfp2<false, true>(p, s);
@@ -871,24 +928,27 @@ int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s)
 
 // ---------------------------------------------------------- limb planes
 
+// shift = 1: the mantissas are first shifted right by one bit, rounding half up
+// (the input shift of the FP32 partial accumulation)
 __global__ void k_i16_to_limbs(const int16_t* __restrict__ src, int64_t rows, int64_t cols,
-                               uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int64_t ldl)
+                               uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int64_t ldl, int shift)
 {
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / cols, c = i - r * cols;
         int32_t h, l;
-        limb_split(src[i], h, l);
+        const int32_t v = src[i];
+        limb_split(shift ? (v + 1) >> 1 : v, h, l);
         hi[r * ldl + c] = int_to_bf16_bits(h);
         lo[r * ldl + c] = int_to_bf16_bits(l);
     }
 }
 
 int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t* hi, uint16_t* lo, int64_t ldl,
-                        cudaStream_t s)
+                        cudaStream_t s, int shift)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
-    k_i16_to_limbs<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(src, rows, cols, hi, lo, ldl);
+    k_i16_to_limbs<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(src, rows, cols, hi, lo, ldl, shift);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "limb launch: %s", cudaGetErrorString(e));
 }

@@ -328,6 +328,26 @@ int ito_dfp16_linear_fwd_f32(const int16_t* x, const int32_t* d_exp_x, const int
     return launch_p64_to_float(p64, (int64_t)B * OC, d_exp_x, d_exp_w, y, s);
 }
 
+int ito_dfp16_linear_fwd_f32_chained(const int16_t* x, const int32_t* d_exp_x, const int16_t* W,
+                                     const int32_t* d_exp_w, int B, int IC, int OC, int32_t chain, int32_t input_shift,
+                                     void* workspace, size_t workspace_bytes, float* y, void* stream)
+{
+    ITO_TRY(dfp_check(x, W, y, y, B, IC, OC, workspace, workspace_bytes));
+    if (!d_exp_x || !d_exp_w) return set_error(ITO_ERR_ARG, "NULL scalar pointer");
+    if (input_shift != 0 && input_shift != 1) return set_error(ITO_ERR_ARG, "input_shift must be 0 or 1");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t ld = pad8(IC);
+    Planes xa = planes_at(workspace, (size_t)B * ld);
+    Planes wb = planes_at(static_cast<char*>(workspace) + dws_a(B, IC, OC), (size_t)OC * ld);
+    DfpGemmPlan g;
+    ITO_TRY(dfp_gemm_plan_chained(&g, Bf16View{xa.h, B, IC, ld}, Bf16View{xa.l, B, IC, ld},
+                                  Bf16View{wb.h, OC, IC, ld}, Bf16View{wb.l, OC, IC, ld}, B, OC, IC, chain, d_exp_x,
+                                  d_exp_w, input_shift, y, OC));
+    ITO_TRY(launch_i16_to_limbs(x, B, IC, xa.h, xa.l, ld, s, input_shift));
+    ITO_TRY(launch_i16_to_limbs(W, OC, IC, wb.h, wb.l, ld, s));
+    return dfp_gemm_run(g, s);
+}
+
 int ito_bdfp16_from_float(const float* f, int64_t rows, int64_t cols, int32_t block, int16_t* mant, int8_t* exps,
                           void* stream)
 {

@@ -90,11 +90,15 @@ struct DfpGemmPlan {
     int64_t ldc;
     unsigned long long* d_max;
     int* err;
-    // Blocked-DFP forward (blocked != 0): one exponent per chunk-long block of K
+    // FP32-output forward: blocked = 1 for Blocked-DFP (one exponent per chunk-long
+    // block of K), 2 for the chained FP32 partial accumulation (one chain per chunk)
     int blocked;
     const int8_t* ex;             // [M][nb]
     const int8_t* ew;             // [N][nb]
     int nb;
+    const int32_t* d_ex;          // chained: device exponents of the input and the weights
+    const int32_t* d_ew;
+    int shift;                    // chained: inputs shifted right by one bit
     float* Y;                     // [M][ldy] float output
     int64_t ldy;
 };
@@ -105,6 +109,13 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
                   const Bf16View& Bl, bool b_mn, int M, int N, int K, int64_t* C, int64_t ldc,
                   unsigned long long* d_max, int64_t* tail_ws = nullptr, size_t tail_ws_bytes = 0);
 size_t dfp_split_ws_bytes(int M, int N, int K);
+// Chained FP32 partial accumulation (forward, both operands K-major): chains of `chain` K
+// terms (64..512, a multiple of 64), each wrapped to int32, converted to float, scaled by
+// 2^(*d_ex + shift + *d_ew) and added to Y in chain order; the A limb planes must hold the
+// inputs already shifted when shift = 1
+int dfp_gemm_plan_chained(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, const Bf16View& Bh,
+                          const Bf16View& Bl, int M, int N, int K, int chain, const int32_t* d_ex,
+                          const int32_t* d_ew, int shift, float* Y, int64_t ldy);
 // Blocked-DFP forward: Y[m][n] = float(sum over K blocks j, in order, in double, of
 // P_j * 2^(ex[m][j] + ew[n][j])), P_j the exact int64 sum over block j (block: 64..512, multiple of 64)
 int dfp_gemm_plan_blocked(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, const Bf16View& Bh,
@@ -114,7 +125,7 @@ int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s);
 
 // int16 [rows][cols] -> bf16 limb planes hi/lo [rows][ldl]
 int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t* hi, uint16_t* lo, int64_t ldl,
-                        cudaStream_t s);
+                        cudaStream_t s, int shift = 0);
 // DFP down-conversion of P with exponent *d_ea + *d_eb: Rs from *d_max,
 // out16 = sat16(rhu(P, Rs)) (+ limb planes if hi != null), *d_exp_out = Ea + Eb + Rs,
 // *d_rs = Rs; an exponent outside int8 raises ITO_ERR_EXPONENT in the error word.

@@ -112,6 +112,7 @@ def lib():
             "ora_dfp_from_float": (i32, [P, i64, P]),
             "ora_dfp_to_float": (None, [P, i64, i32, P]),
             "ora_p64_to_float": (None, [P, i64, i32, P]),
+            "ora_dfp_linear_fwd_f32_chained": (None, [P, i32, P, i32] + [ctypes.c_int] * 5 + [P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -451,6 +452,21 @@ def p64_to_float(P, e: int):
     out = np.empty(P.shape, np.float32)
     lib().ora_p64_to_float(_p(P), P.size, e, _p(out))
     return out
+
+
+def dfp_linear_fwd_f32_chained(x, ex: int, W, ew: int, chain: int, input_shift: bool = True):
+    """Linear forward with FP32 output by the partial-accumulation scheme of
+    [DFP] section 4 (ora_dfp_linear_fwd_f32_chained): inputs shifted by one bit,
+    INT32 chains of `chain` terms, each converted to FP32, scaled by
+    2^(E_inp + E_wt) and accumulated in FP32 in chain order."""
+    x, W = _c(x, np.int16), _c(W, np.int16)
+    B, IC = x.shape
+    OC = W.shape[0]
+    assert W.shape == (OC, IC)
+    y = np.empty((B, OC), np.float32)
+    lib().ora_dfp_linear_fwd_f32_chained(_p(x), int(ex), _p(W), int(ew), B, IC, OC, int(chain), int(input_shift),
+                                         _p(y))
+    return y
 
 
 def bdfp_from_float(f, block: int):

@@ -722,6 +722,54 @@ void ora_p64_to_float(const int64_t *P, int64_t n, int32_t E, float *out)
     for (int64_t i = 0; i < n; i++) out[i] = ldexpf((float)P[i], E);
 }
 
+/* Linear forward with FP32 output by the page's partial-accumulation scheme
+ * ([DFP] section 4, "Handling overflows": INT16 products overflow an INT32
+ * accumulator after a few terms, so the kernels keep accumulation chains short,
+ * shift the inputs by one bit, convert each chain's INT32 partial to FP32, scale
+ * it by 2^(E_inp + E_wt) and accumulate it into the FP32 output). Steps, in the
+ * page's order:
+ *   1. with input_shift = 1 every input mantissa becomes rhu(x, 1) and the
+ *      input exponent E_inp = ex + 1 (with 0, x and ex unchanged);
+ *   2. the contraction over IC is cut into chains of `chain` consecutive terms
+ *      (the last one shorter when chain does not divide IC);
+ *   3. a chain's products sum in an INT32 accumulator that wraps modulo 2^32 as
+ *      the hardware's two's-complement accumulator does (the page's point is
+ *      that the shift and the chain length keep this from happening);
+ *   4. the chain's INT32 value is converted to FP32 (to nearest, ties to even)
+ *      and scaled by 2^(E_inp + ew), the product formed exactly in double and
+ *      rounded once to FP32;
+ *   5. the terms are added to the FP32 output, which starts at 0, in increasing
+ *      chain order, each addition rounded to FP32.
+ * Readings (the page fixes none of them): the chain length is a parameter, the
+ * shift rounds half up as the down-conversion does, and the accumulator wraps. */
+void ora_dfp_linear_fwd_f32_chained(const int16_t *x, int32_t ex, const int16_t *W, int32_t ew, int B, int IC,
+                                    int OC, int chain, int input_shift, float *y)
+{
+    if (chain < 1) ora_fail("chain length must be >= 1");
+    const int32_t e_inp = input_shift ? ex + 1 : ex;
+    const double scale = ldexp(1.0, e_inp + ew);
+#pragma omp parallel for schedule(static)
+    for (int b = 0; b < B; b++)
+        for (int oc = 0; oc < OC; oc++) {
+            float out = 0.0f;
+            for (int k0 = 0; k0 < IC; k0 += chain) {
+                const int k1 = k0 + chain < IC ? k0 + chain : IC;
+                uint32_t acc = 0;                     /* INT32 accumulator, two's complement */
+                for (int k = k0; k < k1; k++) {
+                    int64_t xv = x[(int64_t)b * IC + k];
+                    if (input_shift) xv = ora_rhu(xv, 1);
+                    const int64_t prod = xv * (int64_t)W[(int64_t)oc * IC + k];
+                    acc += (uint32_t)(prod & 0xFFFFFFFF);
+                }
+                const int64_t p32 = acc >= 0x80000000u ? (int64_t)acc - ((int64_t)1 << 32) : (int64_t)acc;
+                const float pf = (float)p32;
+                const float term = (float)((double)pf * scale);
+                out = out + term;
+            }
+            y[(int64_t)b * OC + oc] = out;
+        }
+}
+
 /* Integer SGD on a DFP weight tensor of `bits`-bit mantissas (bits <= 16)
  * with exponent E_W, learning rate 2^-eta: W <- W - G * 2^(E_G - eta - E_W).
  * With k = E_W + eta - E_G the step is dW = rhu(Gm, k) for k >= 0 and

@@ -105,6 +105,14 @@ def test_host_side_argument_errors_new_entry_points():
     # Blocked-DFP
     assert L.ito_bdfp16_from_float(dummy, 4, 4, 0, dummy, dummy, None) == ito.ITO_ERR_SHAPE
     assert L.ito_bdfp16_to_float(None, dummy, 4, 4, 2, dummy, None) == ito.ITO_ERR_ARG
+    big = ctypes.c_size_t(1 << 30)
+    for chain, shift in ((100, 1), (32, 1), (1024, 0), (64, 2)):
+        assert L.ito_dfp16_linear_fwd_f32_chained(dummy, dummy, dummy, dummy, 4, 64, 4, chain, shift, dummy, big,
+                                                  dummy, None) == ito.ITO_ERR_ARG
+    assert L.ito_dfp16_linear_fwd_f32_chained(dummy, None, dummy, dummy, 4, 64, 4, 64, 1, dummy, big, dummy,
+                                              None) == ito.ITO_ERR_ARG
+    assert L.ito_dfp16_linear_fwd_f32_chained(dummy, dummy, dummy, dummy, 4, 64, 4, 64, 1, None, 0, dummy,
+                                              None) == ito.ITO_ERR_ARG
     assert L.ito_bdfp16_linear_fwd_f32(dummy, dummy, dummy, dummy, 4, 4, 4, 64, None, 0, dummy,
                                        None) == ito.ITO_ERR_ARG
 
