@@ -158,9 +158,9 @@ WORKLOADS = (
     Workload(7, "dfp16_2048x3_b2048_apt6", "dfp16", 2048, dims=(2048, 2048, 2048, 2048),
              sigma=4096.0, lim=32767, exp_x=-12, exp_w=-17,
              apt=AptSetting(k_init=6, k_min=2, k_max=16, t_min=100.0, t_max=float("inf"), epoch=10, eval_every=1)),
-    # the 4096-wide MLP at batch 256 with inputs in [-7, 7]: the first layer's weight
+    # the 4096-wide MLP at batch 1024 with inputs in [-7, 7]: the first layer's weight
     # gradient is small enough for its weights to move (the wider-input workloads' do not)
-    Workload(8, "mlp4096x4-1000_b256_x7", "mlp", 256, dims=(4096, 4096, 4096, 4096, 4096, 1000),
+    Workload(8, "mlp4096x4-1000_b1024_x7", "mlp", 1024, dims=(4096, 4096, 4096, 4096, 4096, 1000),
              classes=1000, in_lim=7),
 )
 

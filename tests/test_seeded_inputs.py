@@ -54,6 +54,6 @@ def test_workload_shapes():
 def test_narrow_input_workload():
     w = si.by_name(8)
     x, labels = si.make_batch(w, 0)
-    assert x.shape == (256, 4096) and x.min() == -7 and x.max() == 7
+    assert x.shape == (1024, 4096) and x.min() == -7 and x.max() == 7
     assert labels.max() <= 999
     assert si.weight_shapes(w) == si.weight_shapes(si.by_name(3))
