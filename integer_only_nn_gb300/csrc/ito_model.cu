@@ -64,9 +64,6 @@ struct MLayer {
     // speculative requantisation (see FusedRq): pf / pd with the requantising epilogue, and their
     // re-launches, which check the shift prediction and recompute when it missed
     GemmPlan pf_spec{}, pd_spec{}, pf_redo{}, pd_redo{};
-    // one-wave fusion (WaveFuse): pf / pd / pg with the NITI step in the epilogue (wave.mode
-    // WAVE_OFF where the contraction does not qualify); used while no layer is static
-    GemmPlan pf_w{}, pd_w{}, pg_w{};
     bool has_dgrad = false;
     bool relu = false;
 };
@@ -471,14 +468,10 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         // one-wave fusion (WaveFuse) of single-CTA contractions whose tiles all fit on the
         // device at once: the forward and delta-propagation epilogues requantise, the weight
         // gradient's applies the NITI update, so their separate passes are not launched. Not
-        // with bit-packed masks or ping-pong delta buffers, nor (at run time) while a layer is
-        // statically requantised; a conv layer's delta propagation goes through col2im and the
-        // pooled delta through the pooling backward, so those keep their passes
-        L.pf_w = L.pf;
-        L.pd_w = L.pd;
-        L.pg_w = L.pg;
-        L.pf_w.wave = L.pd_w.wave = L.pg_w.wave = WaveFuse{};
-        if (plain) {
+        // with bit-packed masks, ping-pong delta buffers or static requantisation; a conv
+        // layer's delta propagation goes through col2im and the pooled delta through the
+        // pooling backward, so those keep their passes
+        if (plain && !L.static_q) {
             if (!L.pf_spec.rq_pred) {
                 WaveFuse wf{};
                 wf.mode = WAVE_REQUANT;
@@ -491,7 +484,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
                 wf.ldb = L.lda;
                 wf.d_shift = m->sval(l, ST_YS);
                 wf.s_last = m->last_y(l);
-                ITO_TRY(gemm_plan_fuse_wave(&L.pf_w, wf));
+                ITO_TRY(gemm_plan_fuse_wave(&L.pf, wf));
             }
             if (L.has_dgrad && !conv && !L.pd_spec.rq_pred && !(l == m->n_conv && m->has_pool) &&
                 m->L[l - 1].kind != ITO_LAYER_CONV3X3_RELU) {
@@ -508,7 +501,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
                 wf.ldb = prev.lde;
                 wf.d_shift = m->sval(l, ST_DS);
                 wf.s_last = m->last_d(l);
-                ITO_TRY(gemm_plan_fuse_wave(&L.pd_w, wf));
+                ITO_TRY(gemm_plan_fuse_wave(&L.pd, wf));
             }
             WaveFuse wf{};
             wf.mode = WAVE_UPDATE;
@@ -522,7 +515,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
             wf.d_shift = m->sval(l, ST_GS);
             wf.d_wshift = m->sval(l, ST_WS);
             wf.d_nonzero = reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ));
-            ITO_TRY(gemm_plan_fuse_wave(&L.pg_w, wf));
+            ITO_TRY(gemm_plan_fuse_wave(&L.pg, wf));
         }
     }
     {
@@ -589,14 +582,6 @@ static double requant_bytes(int64_t n, bool bf16, bool gate)
     return (double)n * (4 + 1 + (bf16 ? 2 : 0) + (gate ? 1 : 0));
 }
 
-// a statically requantised layer anywhere in the model (those take no one-wave fusion)
-static bool any_static(const ito_model* m)
-{
-    for (const MLayer& L : m->L)
-        if (L.static_q) return true;
-    return false;
-}
-
 static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
 {
     const int B = m->batch;
@@ -630,9 +615,9 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
             // no counted work)
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf_spec), gemm_run(L.pf_spec, s));
             ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pf_redo, s));
-        } else if (L.pf_w.wave.mode != WAVE_OFF && !any_static(m)) {
+        } else if (L.pf.wave.mode != WAVE_OFF) {
             // one wave: the contraction requantises in its epilogue
-            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf_w), gemm_run(L.pf_w, s));
+            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
         } else {
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
             if (L.static_q)
@@ -672,7 +657,6 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
             return set_error(ITO_ERR_CUDA, "stream ordering event failed");
         return ITO_OK;
     };
-    const bool static_model = any_static(m);
     MLayer& top = m->L[nl - 1];
     ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * top.OC + 4.0 * B,
                launch_top_error(top.a8, labels, B, top.OC, m->target_mag, top.e8, top.eb, top.lde, s));
@@ -689,9 +673,9 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
             // speculating delta propagation and its re-launch, both on s (as in the forward)
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd_spec), gemm_run(L.pd_spec, s));
             ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pd_redo, s));
-        } else if (L.has_dgrad && L.pd_w.wave.mode != WAVE_OFF && !static_model) {
+        } else if (L.has_dgrad && L.pd.wave.mode != WAVE_OFF) {
             // one wave: the delta propagation requantises and gates in its epilogue
-            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd_w), gemm_run(L.pd_w, s));
+            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
         } else if (L.has_dgrad) {
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
             const cudaStream_t r = r_side;
@@ -724,11 +708,8 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
                 delta_on_side = true;
             }
         }
-        if (L.pg_w.wave.mode != WAVE_OFF && !static_model) {
-            // one wave: the weight gradient applies the NITI update in its epilogue
-            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg_w), gemm_run(L.pg_w, s));
-        } else {
-            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
+        ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
+        if (L.pg.wave.mode == WAVE_OFF) {
             ITO_TRY(sync(m->ev_wgrad(l), s, b));       // the weight gradient is complete
             // G read (4 B), W read and written (1 + 1 B), bf16 copy written (2 B)
             ITO_LAUNCH(m, b, ITO_PROF_UPDATE, 8.0 * L.OC * L.K,
