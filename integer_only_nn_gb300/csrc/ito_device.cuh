@@ -59,14 +59,6 @@ __device__ __forceinline__ int64_t rhu64(int64_t y, int s)
 }
 
 __device__ __forceinline__ int32_t sat8(int32_t v) { return v < -128 ? -128 : (v > 127 ? 127 : v); }
-
-// weight_delta of Steps 3-4: round(sat8(round(G >> s)) >> ws); the operand
-// of the second shift is G_quantized, as the step is written.
-__device__ __forceinline__ int32_t niti_step_delta(int32_t g, int s, int ws)
-{
-    const int32_t gq = sat8(rhu32(g, s));     // Step 3
-    return rhu32(gq, ws);                     // Step 4
-}
 __device__ __forceinline__ int64_t sat16s(int64_t v) { return v < -32767 ? -32767 : (v > 32767 ? 32767 : v); }
 
 __device__ __forceinline__ uint32_t abs_u32(int32_t v)
@@ -172,33 +164,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             }
         }
     }
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Grid-wide barrier for one thread per CTA on a counter that is zero before the
-// launch: returns true once `n` CTAs have arrived, with every write those CTAs
-// made before arriving visible; false after kWaitTimeoutNs (ITO_ERR_TIMEOUT
-// raised in the error word). All n CTAs must be resident at once (a cooperative
-// launch), and the counter must be zeroed again before the next launch.
-__device__ __forceinline__ bool grid_arrive_wait(uint32_t* count, uint32_t n, int* err)
-{
-    __threadfence();   // release: this CTA's earlier writes and atomics before its arrival
-    atomicAdd(count, 1u);
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu(count) < n) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            raise_device_error(err, ITO_ERR_TIMEOUT);
-            return false;
-        }
-        __nanosleep(64);
-    }
-    return true;
 }
 
 // 2-D tiled TMA load into shared memory, completing on an mbarrier.

@@ -391,6 +391,13 @@ int launch_offset_grad_update(const int8_t* delta, int64_t rows, int64_t cols, i
 
 // ------------------------------------------------------------ NITI update
 
+// weight_delta of Steps 3-4: round(sat8(round(G >> s)) >> ws); the operand
+// of the second shift is G_quantized, as the step is written.
+__device__ __forceinline__ int32_t niti_step_delta(int32_t g, int s, int ws)
+{
+    const int32_t gq = sat8(rhu32(g, s));     // Step 3
+    return rhu32(gq, ws);                     // Step 4
+}
 
 __device__ __forceinline__ void count_nonzero(uint32_t cnt, uint32_t* d_nonzero)
 {

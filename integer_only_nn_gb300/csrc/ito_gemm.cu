@@ -93,114 +93,16 @@ struct TcCfg {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
-// One-wave fusion (WaveFuse): the epilogue thread of `row` finishes columns
-// [col0, col0 + HALF) of its tile from the int32 values in registers.
-template <int HALF>
-__device__ __forceinline__ void wave_requant(const WaveFuse& wf, const int32_t (&acc)[HALF], int row, int col0,
-                                             int N, int s)
-{
-#pragma unroll
-    for (int g = 0; g < HALF / 16; ++g) {
-        const int c = col0 + g * 16;
-        if (c >= N) continue;
-        const bool full = wf.vec && c + 16 <= N;
-        int8_t gt[16];
-        if (wf.gate) {
-            const int8_t* gp = wf.gate + (int64_t)row * wf.ldg + c;
-            if (full) {
-                *reinterpret_cast<uint4*>(gt) = *reinterpret_cast<const uint4*>(gp);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) gt[j] = c + j < N ? gp[j] : 0;
-            }
-        }
-        int8_t q[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            int32_t v = sat8(rhu32(acc[g * 16 + j], s));
-            if (wf.relu) v = v > 0 ? v : 0;
-            if (wf.gate && gt[j] <= 0) v = 0;
-            q[j] = (int8_t)v;
-        }
-        int8_t* o = wf.out8 + (int64_t)row * wf.ld8 + c;
-        uint16_t* ob = wf.outb ? wf.outb + (int64_t)row * wf.ldb + c : nullptr;
-        if (full) {
-            *reinterpret_cast<uint4*>(o) = *reinterpret_cast<const uint4*>(q);
-            if (ob) {
-                reinterpret_cast<uint4*>(ob)[0] = make_uint4(int_pair_to_bf16x2(q[0], q[1]), int_pair_to_bf16x2(q[2], q[3]),
-                                                             int_pair_to_bf16x2(q[4], q[5]), int_pair_to_bf16x2(q[6], q[7]));
-                reinterpret_cast<uint4*>(ob)[1] =
-                    make_uint4(int_pair_to_bf16x2(q[8], q[9]), int_pair_to_bf16x2(q[10], q[11]),
-                               int_pair_to_bf16x2(q[12], q[13]), int_pair_to_bf16x2(q[14], q[15]));
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (c + j < N) {
-                    o[j] = q[j];
-                    if (ob) ob[j] = int_to_bf16_bits(q[j]);
-                }
-        }
-    }
-}
-
-template <int HALF>
-__device__ __forceinline__ uint32_t wave_update(const WaveFuse& wf, const int32_t (&acc)[HALF], int row, int col0,
-                                                int N, int s, int ws)
-{
-    uint32_t nz = 0;
-#pragma unroll
-    for (int g = 0; g < HALF / 16; ++g) {
-        const int c = col0 + g * 16;
-        if (c >= N) continue;
-        const bool full = wf.vec && c + 16 <= N;
-        int8_t* wp = wf.out8 + (int64_t)row * wf.ld8 + c;
-        int8_t w[16];
-        if (full) {
-            *reinterpret_cast<uint4*>(w) = *reinterpret_cast<const uint4*>(wp);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = c + j < N ? wp[j] : 0;
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int32_t dw = niti_step_delta(acc[g * 16 + j], s, ws);
-            nz += (dw != 0 && c + j < N) ? 1u : 0u;
-            w[j] = (int8_t)sat8((int32_t)w[j] - dw);
-        }
-        uint16_t* ob = wf.outb ? wf.outb + (int64_t)row * wf.ldb + c : nullptr;
-        if (full) {
-            *reinterpret_cast<uint4*>(wp) = *reinterpret_cast<const uint4*>(w);
-            if (ob) {
-                reinterpret_cast<uint4*>(ob)[0] = make_uint4(int_pair_to_bf16x2(w[0], w[1]), int_pair_to_bf16x2(w[2], w[3]),
-                                                             int_pair_to_bf16x2(w[4], w[5]), int_pair_to_bf16x2(w[6], w[7]));
-                reinterpret_cast<uint4*>(ob)[1] =
-                    make_uint4(int_pair_to_bf16x2(w[8], w[9]), int_pair_to_bf16x2(w[10], w[11]),
-                               int_pair_to_bf16x2(w[12], w[13]), int_pair_to_bf16x2(w[14], w[15]));
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (c + j < N) {
-                    wp[j] = w[j];
-                    if (ob) ob[j] = int_to_bf16_bits(w[j]);
-                }
-        }
-    }
-    return nz;
-}
-
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
               int splits, int kb_per_split, int64_t split_stride, int32_t* __restrict__ C, int64_t ldc,
-              uint32_t* __restrict__ d_max, int* __restrict__ err, const WaveFuse wf)
+              uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
     // Work item w covers output tile w / splits and the K slice w % splits; with
     // splits > 1 each slice writes an int32 partial tile at C + slice * split_stride
-    // (plain stores, no max) and a reduction kernel adds the slices. With one-wave
-    // fusion (wf.mode) every CTA holds exactly one tile and no split.
+    // (plain stores, no max) and a reduction kernel adds the slices.
     using Cfg = TcCfg<BN>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;                             // columns per epilogue warp
@@ -213,9 +115,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     uint64_t* empty_bar = full_bar + STAGES;
     uint64_t* accf_bar = empty_bar + STAGES;   // [2] accumulator buffer filled
     uint64_t* acce_bar = accf_bar + 2;         // [2] accumulator buffer drained
-    uint64_t* wave_in = acce_bar + 2;          // one-wave fusion: this CTA's maxima are folded
-    uint64_t* wave_out = acce_bar + 3;         // one-wave fusion: the grid's max is known
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -239,8 +139,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
             mbar_init(&accf_bar[b], 1);
             mbar_init(&acce_bar[b], Cfg::EPI_WARPS);
         }
-        mbar_init(wave_in, Cfg::EPI_WARPS);
-        mbar_init(wave_out, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
@@ -402,43 +300,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < HALF; ++i)
                         if (col0 + i < N) dst[i] = acc[i];
-                }
-            }
-            if (BN <= 128 && wf.mode != WAVE_OFF) {
-                // every CTA holds one tile (so each barrier below completes once): when all
-                // CTAs have folded their max (the grid barrier), finish the NITI step from
-                // the registers. Every wait is bounded; a failed one aborts the CTA.
-                volatile uint32_t* wave_max = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(wave_in);   // after this warp's atomicMax
-                if (e == 0 && lane == 0) {
-                    bool okw = mbar_wait(wave_in, 0, abort_flag, err);
-                    if (okw) okw = grid_arrive_wait(wf.bar, gridDim.x, err);
-                    if (okw)
-                        *wave_max = ld_acquire_gpu(d_max);
-                    else
-                        *abort_flag = 1;
-                    mbar_arrive(wave_out);              // releases the other warps either way
-                }
-                if (!mbar_wait(wave_out, 0, abort_flag, err) || *abort_flag) break;
-                const int sh = shift_for(*wave_max, wf.target_bits);
-                const int row = row0 + lane;
-                const bool first = blockIdx.x == 0 && e == 0 && lane == 0;
-                if (wf.mode == WAVE_REQUANT) {
-                    if (row < M) wave_requant<HALF>(wf, acc, row, col0, N, sh);
-                    if (first) {
-                        if (wf.d_shift) *wf.d_shift = sh;
-                        if (wf.s_last) *wf.s_last = sh;
-                    }
-                } else {
-                    const int ws = sh > wf.mu_weight ? sh - wf.mu_weight : 0;
-                    uint32_t nz = row < M ? wave_update<HALF>(wf, acc, row, col0, N, sh, ws) : 0u;
-                    nz = __reduce_add_sync(0xffffffffu, nz);
-                    if (lane == 0 && nz != 0 && wf.d_nonzero) atomicAdd(wf.d_nonzero, nz);
-                    if (first) {
-                        if (wf.d_shift) *wf.d_shift = sh;
-                        if (wf.d_wshift) *wf.d_wshift = ws;
-                    }
                 }
             }
         }
@@ -1005,29 +866,11 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
     const int items = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + BN - 1) / BN) * p.splits;
     const int grid = items < num_sms() ? items : num_sms();
     const bool split = p.splits > 1;
-    cudaError_t e;
-    if (p.wave.mode != WAVE_OFF) {
-        // one tile per CTA, all resident at once: the epilogue's grid barrier needs it
-        if (split || items > grid) return set_error(ITO_ERR_ARG, "gemm: one-wave fusion needs one tile per CTA");
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(items);
-        cfg.blockDim = dim3(Cfg::THREADS);
-        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.use_tma_store, p.M, p.N, p.K, p.chunk_kb, 1,
-                               p.kb_per_split, p.split_stride, p.C, p.ldc, p.d_max, p.err, p.wave);
-    } else {
-        kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(p.mapA, p.mapB, p.mapC, split ? 0 : p.use_tma_store, p.M,
-                                                         p.N, p.K, p.chunk_kb, p.splits, p.kb_per_split,
-                                                         p.split_stride, split ? p.split_ws : p.C, p.ldc,
-                                                         split ? nullptr : p.d_max, p.err, p.wave);
-        e = cudaGetLastError();
-    }
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(p.mapA, p.mapB, p.mapC, split ? 0 : p.use_tma_store, p.M, p.N,
+                                                     p.K, p.chunk_kb, p.splits, p.kb_per_split, p.split_stride,
+                                                     split ? p.split_ws : p.C, p.ldc, split ? nullptr : p.d_max,
+                                                     p.err);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
     if (split) {
         k_splitk_reduce<<<launch_grid_blocks((int64_t)p.M * p.N, 256), 256, 0, s>>>(
@@ -1216,10 +1059,6 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
         p->split_stride = (int64_t)M * ldc;
     }
     p->pair = pair_eligible(M, N, p->splits, min_pair_tiles);
-    // few output tiles on the single-CTA kernel: narrower tiles (down to 64 columns) while
-    // they still fit in one wave put more SMs to work on the same contraction
-    if (!p->pair && p->splits == 1)
-        while (p->bn > 64 && ((M + 127) / 128) * ((N + p->bn / 2 - 1) / (p->bn / 2)) <= num_sms()) p->bn /= 2;
     // tiles are rastered in groups of 16 row tiles
     p->group = 16;
     // pair kernel: split the last partial wave along K when the workspace holds the partial tiles
@@ -1305,21 +1144,6 @@ int gemm_plan_fuse_requant(GemmPlan* p, const int32_t* pred, int relu, const int
     p->rq_gate = gate;
     p->rq_ldg = ldg;
     p->rq_relu = relu;
-    return ITO_OK;
-}
-
-int gemm_plan_fuse_wave(GemmPlan* p, const WaveFuse& wf)
-{
-    p->wave = WaveFuse{};
-    if (wf.mode == WAVE_OFF) return ITO_OK;
-    if (!wf.bar || !wf.out8 || !p->d_max) return set_error(ITO_ERR_ARG, "gemm: one-wave fusion without outputs");
-    // (the 256-column tile keeps the epilogue without it: its registers are full)
-    const int tiles = ((p->M + 127) / 128) * ((p->N + p->bn - 1) / p->bn);
-    if (p->pair || p->splits != 1 || p->bn > 128 || tiles > num_sms()) return ITO_OK;
-    auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
-    p->wave = wf;
-    p->wave.vec = al16(wf.out8) && wf.ld8 % 16 == 0 && (!wf.gate || (al16(wf.gate) && wf.ldg % 16 == 0)) &&
-                  (!wf.outb || (al16(wf.outb) && wf.ldb % 8 == 0));
     return ITO_OK;
 }
 

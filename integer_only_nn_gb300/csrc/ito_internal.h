@@ -31,31 +31,6 @@ struct Bf16View {
 
 // A prepared tensor-core contraction C[M][N] = sum_k A(m,k) B(n,k):
 // A is [M][K] (K-major) or [K][M] (a_mn); B is [N][K] or [K][N] (b_mn).
-// One-wave fusion of the single-CTA contraction (GemmPlan.wave, mode != 0): when
-// every output tile has its own resident CTA (a cooperative launch), the CTAs
-// meet at a grid barrier after folding max |C| and finish the NITI step from the
-// tile still in registers: WAVE_REQUANT writes out8 = sat8(rhu(C, s)) (ReLU'd, or
-// zeroed where gate <= 0) and its bf16 copy; WAVE_UPDATE applies the NITI update
-// to the weights out8 (in place) and their bf16 copy outb. The int32 result is
-// still written. `bar` is an arrival counter that must be zero before each launch.
-enum WaveMode { WAVE_OFF = 0, WAVE_REQUANT = 1, WAVE_UPDATE = 2 };
-struct WaveFuse {
-    int mode;
-    uint32_t* bar;
-    int target_bits, relu, mu_weight;
-    const int8_t* gate;      // [M][ldg] or nullptr (requantise)
-    int64_t ldg;
-    int8_t* out8;            // [M][ld8]: the requantised result, or the weights updated in place
-    int64_t ld8;
-    uint16_t* outb;          // [M][ldb] bf16 copy of out8, or nullptr
-    int64_t ldb;
-    int vec;                 // 16-byte aligned rows: vector loads and stores
-    int32_t* d_shift;        // the step's shift (may be null)
-    int32_t* d_wshift;       // WAVE_UPDATE: the weight shift (may be null)
-    uint32_t* d_nonzero;     // WAVE_UPDATE: nonzero weight steps are added here (may be null)
-    int32_t* s_last;         // WAVE_REQUANT: the shift again (next step's prediction; may be null)
-};
-
 struct GemmPlan {
     CUtensorMap mapA, mapB, mapC;
     CUtensorMap mapP;             // pair kernel: partial tiles of the split last wave (in split_ws)
@@ -83,7 +58,6 @@ struct GemmPlan {
     int64_t ldc;
     uint32_t* d_max;
     int* err;
-    WaveFuse wave;                // single-CTA kernel, one wave: the NITI step in the epilogue
 };
 
 // Device address of this library's error word on the current device.
@@ -197,10 +171,6 @@ size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc);
 // a split last wave, N or pitches not multiples of 16 bytes).
 int gemm_plan_fuse_requant(GemmPlan* p, const int32_t* pred, int relu, const int8_t* gate, int64_t ldg,
                            int8_t* out8, int64_t ld8, uint16_t* outb, int64_t ldb);
-// Turns on one-wave fusion (see WaveFuse) when the plan qualifies: the single-CTA
-// kernel, no split, every tile on its own SM. Leaves wave.mode = WAVE_OFF (no
-// error) otherwise; the caller then runs the separate pass.
-int gemm_plan_fuse_wave(GemmPlan* p, const WaveFuse& wf);
 int gemm_run(const GemmPlan& p, cudaStream_t s);
 
 // ---- bandwidth kernels (ito_elementwise.cu)

@@ -102,10 +102,6 @@ struct ito_model {
     uint16_t* gbufb[2] = {nullptr, nullptr};
     int32_t* stats = nullptr;
     int n_stats = 0;
-    // arrival counters of the one-wave fused contractions (three per layer), after the stats
-    // in the same allocation and zeroed with them before every step
-    int n_wave = 0;
-    uint32_t* wave_bar(int i) { return reinterpret_cast<uint32_t*>(stats + n_stats) + i; }
     uint32_t* discard_max = nullptr;   // max target of the patch-space conv delta (not a NITI tensor)
     int32_t* split_ws = nullptr;       // split-K partials, shared by the step's contractions (one stream)
     size_t split_ws_bytes = 0;
@@ -315,8 +311,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
     ITO_TRY(m->alloc(&m->x8b, (size_t)B * m->in_features));
     ITO_TRY(m->alloc(&m->labels_b, (size_t)B));
     m->n_stats = nl * ST_PER_LAYER + 2;
-    m->n_wave = 3 * nl;
-    ITO_TRY(m->alloc(&m->stats, (size_t)(m->n_stats + m->n_wave)));
+    ITO_TRY(m->alloc(&m->stats, (size_t)m->n_stats));
     ITO_TRY(m->alloc(&m->discard_max, 1));
     if (m->n_conv == 0) {
         m->ldx = pad8(m->in_features);
@@ -465,58 +460,6 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
             L.pd_redo.rq_s_last = m->last_d(l);
             L.pd_redo.rq_target_bits = m->p.target_bits;
         }
-        // one-wave fusion (WaveFuse) of single-CTA contractions whose tiles all fit on the
-        // device at once: the forward and delta-propagation epilogues requantise, the weight
-        // gradient's applies the NITI update, so their separate passes are not launched. Not
-        // with bit-packed masks, ping-pong delta buffers or static requantisation; a conv
-        // layer's delta propagation goes through col2im and the pooled delta through the
-        // pooling backward, so those keep their passes
-        if (plain && !L.static_q) {
-            if (!L.pf_spec.rq_pred) {
-                WaveFuse wf{};
-                wf.mode = WAVE_REQUANT;
-                wf.bar = m->wave_bar(3 * l);
-                wf.target_bits = m->p.target_bits;
-                wf.relu = L.relu ? 1 : 0;
-                wf.out8 = L.a8;
-                wf.ld8 = L.OC;
-                wf.outb = L.ab;
-                wf.ldb = L.lda;
-                wf.d_shift = m->sval(l, ST_YS);
-                wf.s_last = m->last_y(l);
-                ITO_TRY(gemm_plan_fuse_wave(&L.pf, wf));
-            }
-            if (L.has_dgrad && !conv && !L.pd_spec.rq_pred && !(l == m->n_conv && m->has_pool) &&
-                m->L[l - 1].kind != ITO_LAYER_CONV3X3_RELU) {
-                const MLayer& prev = m->L[l - 1];
-                WaveFuse wf{};
-                wf.mode = WAVE_REQUANT;
-                wf.bar = m->wave_bar(3 * l + 1);
-                wf.target_bits = m->p.target_bits;
-                wf.gate = prev.relu ? prev.a8 : nullptr;
-                wf.ldg = L.IC;
-                wf.out8 = prev.e8;
-                wf.ld8 = L.IC;
-                wf.outb = prev.eb;
-                wf.ldb = prev.lde;
-                wf.d_shift = m->sval(l, ST_DS);
-                wf.s_last = m->last_d(l);
-                ITO_TRY(gemm_plan_fuse_wave(&L.pd, wf));
-            }
-            WaveFuse wf{};
-            wf.mode = WAVE_UPDATE;
-            wf.bar = m->wave_bar(3 * l + 2);
-            wf.target_bits = m->p.target_bits;
-            wf.mu_weight = m->p.mu_weight;
-            wf.out8 = L.W8;
-            wf.ld8 = L.K;
-            wf.outb = L.Wb;
-            wf.ldb = L.ldw;
-            wf.d_shift = m->sval(l, ST_GS);
-            wf.d_wshift = m->sval(l, ST_WS);
-            wf.d_nonzero = reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ));
-            ITO_TRY(gemm_plan_fuse_wave(&L.pg, wf));
-        }
     }
     {
         // the slots whose contraction plan took the fused epilogue (a plan may decline it)
@@ -615,9 +558,6 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
             // no counted work)
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf_spec), gemm_run(L.pf_spec, s));
             ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pf_redo, s));
-        } else if (L.pf.wave.mode != WAVE_OFF) {
-            // one wave: the contraction requantises in its epilogue
-            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
         } else {
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
             if (L.static_q)
@@ -673,9 +613,6 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
             // speculating delta propagation and its re-launch, both on s (as in the forward)
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd_spec), gemm_run(L.pd_spec, s));
             ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pd_redo, s));
-        } else if (L.has_dgrad && L.pd.wave.mode != WAVE_OFF) {
-            // one wave: the delta propagation requantises and gates in its epilogue
-            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
         } else if (L.has_dgrad) {
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
             const cudaStream_t r = r_side;
@@ -709,14 +646,12 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
             }
         }
         ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
-        if (L.pg.wave.mode == WAVE_OFF) {
-            ITO_TRY(sync(m->ev_wgrad(l), s, b));       // the weight gradient is complete
-            // G read (4 B), W read and written (1 + 1 B), bf16 copy written (2 B)
-            ITO_LAUNCH(m, b, ITO_PROF_UPDATE, 8.0 * L.OC * L.K,
-                       launch_niti_update(L.W8, L.Wb, L.ldw, L.g32, L.OC, L.K, m->umax(l, ST_GMAX),
-                                          p.target_bits, p.mu_weight, m->sval(l, ST_GS), m->sval(l, ST_WS),
-                                          reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ)), b));
-        }
+        ITO_TRY(sync(m->ev_wgrad(l), s, b));       // the weight gradient is complete
+        // G read (4 B), W read and written (1 + 1 B), bf16 copy written (2 B)
+        ITO_LAUNCH(m, b, ITO_PROF_UPDATE, 8.0 * L.OC * L.K,
+                   launch_niti_update(L.W8, L.Wb, L.ldw, L.g32, L.OC, L.K, m->umax(l, ST_GMAX), p.target_bits,
+                                      p.mu_weight, m->sval(l, ST_GS), m->sval(l, ST_WS),
+                                      reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ)), b));
         // the offsets' gradient reads this layer's delta, whose (ping-pong) buffer the next
         // requantisation overwrites: it runs on the requantisation stream, before that one
         if (L.static_q)
@@ -988,7 +923,7 @@ int ito_model_use_graphs(ito_model* m, int enable)
 static int step_direct(ito_model* m, const int8_t* x, const int32_t* labels, cudaStream_t s)
 {
     m->launches = 0;
-    cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * (m->n_stats + m->n_wave), s);
+    cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * m->n_stats, s);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
     // this step's shift predictions are the last step's shifts
     const int nl = (int)m->L.size();
@@ -1103,7 +1038,7 @@ int ito_infer(ito_model* m, const int8_t* x, int8_t* logits, void* stream)
     if (!m || !x || !logits) return set_error(ITO_ERR_ARG, "NULL argument");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     m->launches = 0;
-    cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * (m->n_stats + m->n_wave), s);
+    cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * m->n_stats, s);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
     ITO_TRY(model_forward(m, x, s));
     const MLayer& top = m->L.back();
