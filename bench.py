@@ -426,6 +426,13 @@ class DfpRun:
         return sum(per), per
 
 
+def rate(entry, unit):
+    """work / time of a profiled class [ms, work, launches] in `unit` per second
+    (None when the class had no launches)."""
+    ms, work, _ = entry
+    return work / (ms / 1000.0) / unit if ms > 0 else None
+
+
 def gemm_roofline(prof, pk, pk_src):
     """Contraction rate over the profiled launches against the measured burst
     bf16 peak (the contraction launches are timed inside steps of a few ms, not
@@ -449,9 +456,10 @@ def workload_entry(w, args, flush, pk, pk_src, cpu):
     classes = ("gemm", "down", "update", "other") if w.kind == "dfp16" else ("gemm", "requant", "update", "other")
     prof, prof_ms = profiled_steps(run.model, K, run.stream, flush, run.before, run.step, classes)
     ops = algorithmic_ops(w)
+    kernels = run.model.kernels_per_step()
     e = {"batch": w.batch, "ms_per_step": ms, "ms_per_step_repeats": per, "samples_per_s": w.batch / (ms / 1e3),
          "gemm_roofline": gemm_roofline(prof, pk, pk_src), "gemm_ms_per_step": prof["gemm"][0] / K,
-         "kernels_per_step": run.model.kernels_per_step(),
+         "kernels_per_step": kernels,
          "nonzero_updates_per_step": {"last_step": nz, "per_layer": nz_per}}
     if w.kind == "dfp16":
         e["int16_tops"] = ops / (ms / 1e3) / 1e12
@@ -634,11 +642,12 @@ def run_ours_model(args, w, cpu, barrier, dist, world, rank, local, flush, pk, p
                            "their wait for SM resources); per-pass bandwidth is under 'isolated'",
                    "hbm_peak_gbs": hbm, "peak_source": pk_src,
                    "ms_per_step": {k: v[0] / K for k, v in prof.items()}},
-        "isolated": {"note": "one stream, no speculation, %d steps: per-kernel rates" % iso_steps,
-                     "gemm_tflops": iso["gemm"][1] / (iso["gemm"][0] / 1000.0) / 1e12,
-                     "gemm_frac": iso["gemm"][1] / (iso["gemm"][0] / 1000.0) / 1e12 / roof["peak"],
-                     "requant_gbs": iso["requant"][1] / (iso["requant"][0] / 1000.0) / 1e9,
-                     "update_gbs": iso["update"][1] / (iso["update"][0] / 1000.0) / 1e9,
+        "isolated": {"note": "one stream, no speculation, %d steps: per-kernel rates (null for a class with "
+                             "no launches: contractions that requantise or update in their epilogue)" % iso_steps,
+                     "gemm_tflops": rate(iso["gemm"], 1e12),
+                     "gemm_frac": rate(iso["gemm"], 1e12) / roof["peak"],
+                     "requant_gbs": rate(iso["requant"], 1e9),
+                     "update_gbs": rate(iso["update"], 1e9),
                      "ms_per_step": {c: v[0] / iso_steps for c, v in iso.items()}},
         "e2e": {"value": samples / e2e_s, "unit": "samples/s",
                 "h2d_bytes_per_step": int(x_h.numel() + 4 * l_h.numel()),
@@ -780,9 +789,8 @@ def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local, flush, pk, p
             "nonzero_updates_per_step": {"last_step": nz, "per_layer": nz_per},
             "roofline": roof,
             "passes": {"ms_per_step": {c: v[0] / K for c, v in prof.items()},
-                       "down_gbs": prof["down"][1] / (prof["down"][0] / 1000.0) / 1e9 if prof["down"][0] else None,
-                       "update_gbs": (prof["update"][1] / (prof["update"][0] / 1000.0) / 1e9
-                                      if prof["update"][0] else None),
+                       "down_gbs": rate(prof["down"], 1e9),
+                       "update_gbs": rate(prof["update"], 1e9),
                        "note": "down-conversions and updates run on a second stream beside the contractions: "
                                "their times include waits for SM resources"},
             "e2e": {"value": world * w.batch * K / e2e_s, "unit": "samples/s",

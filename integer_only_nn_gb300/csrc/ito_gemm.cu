@@ -1059,6 +1059,10 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
         p->split_stride = (int64_t)M * ldc;
     }
     p->pair = pair_eligible(M, N, p->splits, min_pair_tiles);
+    // few output tiles on the single-CTA kernel: narrower tiles (down to 64 columns) while
+    // they still fit in one wave put more SMs to work on the same contraction
+    if (!p->pair && p->splits == 1)
+        while (p->bn > 64 && ((M + 127) / 128) * ((N + p->bn / 2 - 1) / (p->bn / 2)) <= num_sms()) p->bn /= 2;
     // tiles are rastered in groups of 16 row tiles
     p->group = 16;
     // pair kernel: split the last partial wave along K when the workspace holds the partial tiles
