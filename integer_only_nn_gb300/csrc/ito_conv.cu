@@ -35,6 +35,8 @@ static int launched(const char* what)
 __global__ void k_im2col_v8(const int8_t* __restrict__ x, int B, int H, int W, int IC, int OH, int OW, int stride,
                             uint16_t* __restrict__ P, int64_t ldp)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int cg = IC >> 3;
     const int64_t n = (int64_t)B * OH * OW * 9 * cg;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -66,6 +68,8 @@ __global__ void k_im2col_v8(const int8_t* __restrict__ x, int B, int H, int W, i
 __global__ void k_im2col_rows(const int8_t* __restrict__ x, int B, int H, int W, int IC, int OH, int OW, int stride,
                               uint16_t* __restrict__ P, int64_t ldp)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t rows = (int64_t)B * OH * OW;
     const int K = 9 * IC;
     for (int64_t m = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; m < rows; m += (int64_t)gridDim.x * blockDim.x) {
@@ -100,6 +104,8 @@ __global__ void k_im2col_rows(const int8_t* __restrict__ x, int B, int H, int W,
 __global__ void k_im2col_1(const int8_t* __restrict__ x, int B, int H, int W, int IC, int OH, int OW, int stride,
                            uint16_t* __restrict__ P, int64_t ldp)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t K = 9 * (int64_t)IC;
     const int64_t n = (int64_t)B * OH * OW * ldp;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -122,13 +128,13 @@ int launch_im2col(const int8_t* x, int B, int H, int W, int IC, int OH, int OW, 
 {
     if (IC % 8 == 0 && ldp % 8 == 0 && aligned(x, 8) && aligned(P, 16)) {
         const int64_t n = (int64_t)B * OH * OW * 9 * (IC / 8);
-        k_im2col_v8<<<launch_grid_blocks(n, 256), 256, 0, s>>>(x, B, H, W, IC, OH, OW, stride, P, ldp);
+        launch_pdl(k_im2col_v8, launch_grid_blocks(n, 256), 256, 0, s, x, B, H, W, IC, OH, OW, stride, P, ldp);
     } else if (ldp % 8 == 0 && aligned(P, 16)) {
-        k_im2col_rows<<<launch_grid_blocks((int64_t)B * OH * OW, 128), 128, 0, s>>>(x, B, H, W, IC, OH, OW, stride, P,
+        launch_pdl(k_im2col_rows, launch_grid_blocks((int64_t)B * OH * OW, 128), 128, 0, s, x, B, H, W, IC, OH, OW, stride, P,
                                                                                   ldp);
     } else {
         const int64_t n = (int64_t)B * OH * OW * ldp;
-        k_im2col_1<<<launch_grid_blocks(n, 256), 256, 0, s>>>(x, B, H, W, IC, OH, OW, stride, P, ldp);
+        launch_pdl(k_im2col_1, launch_grid_blocks(n, 256), 256, 0, s, x, B, H, W, IC, OH, OW, stride, P, ldp);
     }
     return launched("im2col");
 }
@@ -139,6 +145,8 @@ int launch_im2col(const int8_t* x, int B, int H, int W, int IC, int OH, int OW, 
 __global__ void k_col2im_v8(const int32_t* __restrict__ Dcol, int B, int H, int W, int IC, int OH, int OW,
                             int stride, int32_t* __restrict__ D, uint32_t* __restrict__ d_max)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int cg = IC >> 3;
     const int64_t ldc = 9 * (int64_t)IC;
     const int64_t n = (int64_t)B * H * W * cg;
@@ -194,6 +202,8 @@ __global__ void k_col2im_v8(const int32_t* __restrict__ Dcol, int B, int H, int 
 __global__ void k_col2im_1(const int32_t* __restrict__ Dcol, int B, int H, int W, int IC, int OH, int OW,
                            int stride, int32_t* __restrict__ D, uint32_t* __restrict__ d_max)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t ldc = 9 * (int64_t)IC;
     const int64_t n = (int64_t)B * H * W * IC;
     uint32_t mx = 0;
@@ -228,10 +238,10 @@ int launch_col2im(const int32_t* Dcol, int B, int H, int W, int IC, int OH, int 
 {
     if (IC % 8 == 0 && aligned(Dcol, 16) && aligned(D, 16)) {
         const int64_t n = (int64_t)B * H * W * (IC / 8);
-        k_col2im_v8<<<launch_grid_blocks(n, 256), 256, 0, s>>>(Dcol, B, H, W, IC, OH, OW, stride, D, d_max);
+        launch_pdl(k_col2im_v8, launch_grid_blocks(n, 256), 256, 0, s, Dcol, B, H, W, IC, OH, OW, stride, D, d_max);
     } else {
         const int64_t n = (int64_t)B * H * W * IC;
-        k_col2im_1<<<launch_grid_blocks(n, 256), 256, 0, s>>>(Dcol, B, H, W, IC, OH, OW, stride, D, d_max);
+        launch_pdl(k_col2im_1, launch_grid_blocks(n, 256), 256, 0, s, Dcol, B, H, W, IC, OH, OW, stride, D, d_max);
     }
     return launched("col2im");
 }
@@ -242,6 +252,8 @@ int launch_col2im(const int32_t* Dcol, int B, int H, int W, int IC, int OH, int 
 __global__ void k_gap_fwd(const int8_t* __restrict__ A, int B, int HW, int C, int32_t* __restrict__ P,
                           uint32_t* __restrict__ d_max)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t n = (int64_t)B * C;
     uint32_t mx = 0;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -267,7 +279,7 @@ __global__ void k_gap_fwd(const int8_t* __restrict__ A, int B, int HW, int C, in
 
 int launch_gap_fwd(const int8_t* A, int B, int HW, int C, int32_t* P, uint32_t* d_max, cudaStream_t s)
 {
-    k_gap_fwd<<<launch_grid_blocks((int64_t)B * C, 256), 256, 0, s>>>(A, B, HW, C, P, d_max);
+    launch_pdl(k_gap_fwd, launch_grid_blocks((int64_t)B * C, 256), 256, 0, s, A, B, HW, C, P, d_max);
     return launched("gap fwd");
 }
 
@@ -276,6 +288,8 @@ int launch_gap_fwd(const int8_t* A, int B, int HW, int C, int32_t* P, uint32_t* 
 __global__ void k_gap_bwd_v8(const int8_t* __restrict__ dP, const int8_t* __restrict__ A, int B, int HW, int C,
                              int8_t* __restrict__ E, uint16_t* __restrict__ Eb)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t groups = (int64_t)B * HW * (C >> 3);
     const int cg = C >> 3;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups; g += (int64_t)gridDim.x * blockDim.x) {
@@ -298,6 +312,8 @@ __global__ void k_gap_bwd_v8(const int8_t* __restrict__ dP, const int8_t* __rest
 __global__ void k_gap_bwd(const int8_t* __restrict__ dP, const int8_t* __restrict__ A, int B, int HW, int C,
                           int8_t* __restrict__ E, uint16_t* __restrict__ Eb)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t n = (int64_t)B * HW * C;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int c = (int)(i % C);
@@ -311,9 +327,9 @@ __global__ void k_gap_bwd(const int8_t* __restrict__ dP, const int8_t* __restric
 int launch_gap_bwd(const int8_t* dP, const int8_t* A, int B, int HW, int C, int8_t* E, uint16_t* Eb, cudaStream_t s)
 {
     if (C % 8 == 0 && aligned(A, 8) && aligned(dP, 8) && aligned(E, 8) && (!Eb || aligned(Eb, 16)))
-        k_gap_bwd_v8<<<launch_grid_blocks((int64_t)B * HW * C / 8, 256), 256, 0, s>>>(dP, A, B, HW, C, E, Eb);
+        launch_pdl(k_gap_bwd_v8, launch_grid_blocks((int64_t)B * HW * C / 8, 256), 256, 0, s, dP, A, B, HW, C, E, Eb);
     else
-        k_gap_bwd<<<launch_grid_blocks((int64_t)B * HW * C, 256), 256, 0, s>>>(dP, A, B, HW, C, E, Eb);
+        launch_pdl(k_gap_bwd, launch_grid_blocks((int64_t)B * HW * C, 256), 256, 0, s, dP, A, B, HW, C, E, Eb);
     return launched("gap bwd");
 }
 

@@ -166,6 +166,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Programmatic dependent launch. Every kernel of this library starts with
+// griddep_wait(): when it was launched with programmatic stream serialisation
+// (launch_pdl) it may already be resident while the previous kernel in the
+// stream finishes, and the wait returns once that kernel has completed and its
+// memory operations are visible; for a plain launch it returns at once. Only
+// then does the kernel touch global memory, and it allows the next kernel to be
+// scheduled (griddep_launch_dependents), which waits the same way.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2-D tiled TMA load into shared memory, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y)
 {

@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
                int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, DfpF32Out bk,
                int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     using Cfg = DfpCfg;
     constexpr bool F32OUT = MODE != DFP_EXACT;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -409,6 +411,8 @@ __global__ void k_tail_reduce64(const int64_t* __restrict__ P, int tail_tiles, i
                                 int M, int N, int64_t ldc, int64_t* __restrict__ C,
                                 unsigned long long* __restrict__ d_max)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     constexpr int TR = 256, TC = 64;
     const int64_t n = (int64_t)tail_tiles * TR * (TC / 2);
     unsigned long long mx = 0;
@@ -462,6 +466,8 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
                 int K, int full_tiles, int parts, int64_t* __restrict__ C, int64_t ldc,
                 int64_t* __restrict__ tail_ws, unsigned long long* __restrict__ d_max, int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     using Cfg = Dfp2Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;                         // 32 columns per epilogue warp
@@ -709,19 +715,21 @@ static int launch_dfp2(const DfpGemmPlan& p, cudaStream_t s)
     cfg.blockDim = dim3(Cfg::THREADS);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.M, p.N, p.K, p.tail_full,
                                        p.tail_parts, p.C, p.ldc, p.tail_ws, p.d_max, p.err);
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "dfp pair gemm launch: %s", cudaGetErrorString(e));
     if (p.tail_parts > 1) {
         const int tail = tiles - p.tail_full;
-        k_tail_reduce64<<<launch_grid_blocks((int64_t)tail * 256 * 32, 256), 256, 0, s>>>(
+        launch_pdl(k_tail_reduce64, launch_grid_blocks((int64_t)tail * 256 * 32, 256), 256, 0, s, 
             p.tail_ws, tail, p.tail_parts, p.tail_full, num_n, p.M, p.N, p.ldc, p.C, p.d_max);
         e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "dfp tail reduce launch: %s", cudaGetErrorString(e));
@@ -807,7 +815,7 @@ static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
     const int tiles = ((p.M + DfpCfg::BM - 1) / DfpCfg::BM) * ((p.N + DfpCfg::BN - 1) / DfpCfg::BN);
     const int grid = tiles < num_sms() ? tiles : num_sms();
     const DfpF32Out bk{p.ex, p.ew, p.nb, p.d_ex, p.d_ew, p.shift, p.Y, p.ldy};
-    kern<<<grid, DfpCfg::THREADS, DfpCfg::SMEM_BYTES, s>>>(p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.mapC,
+    launch_pdl(kern, grid, DfpCfg::THREADS, DfpCfg::SMEM_BYTES, s, p.mapAh, p.mapAl, p.mapBh, p.mapBl, p.mapC,
                                                            p.use_tma_store, p.M, p.N, p.K, p.chunk_kb, p.C, p.ldc,
                                                            p.d_max, bk, p.err);
     cudaError_t e = cudaGetLastError();
@@ -933,6 +941,8 @@ int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s)
 __global__ void k_i16_to_limbs(const int16_t* __restrict__ src, int64_t rows, int64_t cols,
                                uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int64_t ldl, int shift)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / cols, c = i - r * cols;
@@ -948,7 +958,7 @@ int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t
                         cudaStream_t s, int shift)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
-    k_i16_to_limbs<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(src, rows, cols, hi, lo, ldl, shift);
+    launch_pdl(k_i16_to_limbs, launch_grid_blocks(rows * cols, 256), 256, 0, s, src, rows, cols, hi, lo, ldl, shift);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "limb launch: %s", cudaGetErrorString(e));
 }
@@ -968,6 +978,8 @@ __global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t 
                            int32_t* __restrict__ d_rs, unsigned long long* __restrict__ d_abs_sum,
                            int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     // section 3.1: Rs brings max |P| within 15 magnitude bits; the new exponent is Ea + Eb + Rs
     const unsigned long long m = *d_max;
     const int bl = m ? 64 - __clzll((long long)m) : 0;
@@ -1004,6 +1016,8 @@ __global__ void k_dfp_down_v4(const int64_t* __restrict__ P, int rows, int cols,
                               int32_t* __restrict__ d_exp_out, int32_t* __restrict__ d_rs,
                               unsigned long long* __restrict__ d_abs_sum, int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const unsigned long long m = *d_max;
     const int bl = m ? 64 - __clzll((long long)m) : 0;
     const int rs = bl > 15 ? bl - 15 : 0;
@@ -1055,10 +1069,10 @@ int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned
     if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     if (cols % 4 == 0 && rows * cols < (1LL << 31) && ldl % 4 == 0 && al(P, 16) && al(out16, 8) &&
         (!hi || (al(hi, 8) && al(lo, 8))))
-        k_dfp_down_v4<<<launch_grid_blocks(rows * cols / 4, 256), 256, 0, s>>>(
+        launch_pdl(k_dfp_down_v4, launch_grid_blocks(rows * cols / 4, 256), 256, 0, s, 
             P, (int)rows, (int)cols, d_max, d_ea, d_eb, out16, hi, lo, (int)ldl, d_exp_out, d_rs, d_abs_sum, err);
     else
-        k_dfp_down<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(P, rows, cols, d_max, d_ea, d_eb, out16, hi,
+        launch_pdl(k_dfp_down, launch_grid_blocks(rows * cols, 256), 256, 0, s, P, rows, cols, d_max, d_ea, d_eb, out16, hi,
                                                                          lo, ldl, d_exp_out, d_rs, d_abs_sum, err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp down launch: %s", cudaGetErrorString(e));
@@ -1069,6 +1083,8 @@ int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned
 // max |f| as float bits (non-negative floats order like their bit patterns)
 __global__ void k_absmax_f32(const float* __restrict__ f, int64_t n, unsigned int* __restrict__ d_bits)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     uint32_t mx = 0;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         mx = max(mx, __float_as_uint(f[i]) & 0x7fffffffu);
@@ -1089,6 +1105,8 @@ __device__ __forceinline__ int frexp_exponent(uint32_t bits)
 __global__ void k_dfp_from_float(const float* __restrict__ f, int64_t n, const unsigned int* __restrict__ d_bits,
                                  int16_t* __restrict__ out, int32_t* __restrict__ d_exp, int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t bits = *d_bits;
     const int E = bits ? frexp_exponent(bits) - 15 : 0;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -1107,6 +1125,8 @@ __global__ void k_dfp_from_float(const float* __restrict__ f, int64_t n, const u
 __global__ void k_dfp_to_float(const int16_t* __restrict__ m, int64_t n, const int32_t* __restrict__ d_exp,
                                float* __restrict__ out)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const double sc = pow2d(*d_exp);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         out[i] = __double2float_rn((double)m[i] * sc);
@@ -1116,6 +1136,8 @@ __global__ void k_dfp_to_float(const int16_t* __restrict__ m, int64_t n, const i
 __global__ void k_p64_to_float(const int64_t* __restrict__ P, int64_t n, const int32_t* __restrict__ d_ea,
                                const int32_t* __restrict__ d_eb, float* __restrict__ out)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const double sc = pow2d(*d_ea + *d_eb);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         out[i] = __double2float_rn((double)__ll2float_rn(P[i]) * sc);
@@ -1127,8 +1149,8 @@ int launch_dfp_from_float(const float* f, int64_t n, unsigned int* d_bits, int16
     int* err = device_error_word();
     if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     if (cudaMemsetAsync(d_bits, 0, sizeof(unsigned int), s) != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset");
-    k_absmax_f32<<<launch_grid_blocks(n, 256), 256, 0, s>>>(f, n, d_bits);
-    k_dfp_from_float<<<launch_grid_blocks(n, 256), 256, 0, s>>>(f, n, d_bits, out, d_exp, err);
+    launch_pdl(k_absmax_f32, launch_grid_blocks(n, 256), 256, 0, s, f, n, d_bits);
+    launch_pdl(k_dfp_from_float, launch_grid_blocks(n, 256), 256, 0, s, f, n, d_bits, out, d_exp, err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "float->dfp launch: %s", cudaGetErrorString(e));
 }
@@ -1141,6 +1163,8 @@ int launch_dfp_from_float(const float* f, int64_t n, unsigned int* d_bits, int16
 __global__ void k_bdfp_from_float(const float* __restrict__ f, int64_t rows, int64_t cols, int block,
                                   int16_t* __restrict__ out, int8_t* __restrict__ exps, int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t nb = (cols + block - 1) / block;
     const int64_t nblocks = rows * nb;
     const int lane = threadIdx.x & 31;
@@ -1172,6 +1196,8 @@ __global__ void k_bdfp_from_float(const float* __restrict__ f, int64_t rows, int
 __global__ void k_bdfp_to_float(const int16_t* __restrict__ m, const int8_t* __restrict__ exps, int64_t rows,
                                 int64_t cols, int block, float* __restrict__ out)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t nb = (cols + block - 1) / block;
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -1187,7 +1213,7 @@ int launch_bdfp_from_float(const float* f, int64_t rows, int64_t cols, int block
     int* err = device_error_word();
     if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     const int64_t nblocks = rows * ((cols + block - 1) / block);
-    k_bdfp_from_float<<<launch_grid_blocks(nblocks * 32, 256), 256, 0, s>>>(f, rows, cols, block, out, exps, err);
+    launch_pdl(k_bdfp_from_float, launch_grid_blocks(nblocks * 32, 256), 256, 0, s, f, rows, cols, block, out, exps, err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "float->bdfp launch: %s", cudaGetErrorString(e));
 }
@@ -1196,7 +1222,7 @@ int launch_bdfp_to_float(const int16_t* m, const int8_t* exps, int64_t rows, int
                          cudaStream_t s)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
-    k_bdfp_to_float<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(m, exps, rows, cols, block, out);
+    launch_pdl(k_bdfp_to_float, launch_grid_blocks(rows * cols, 256), 256, 0, s, m, exps, rows, cols, block, out);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "bdfp->float launch: %s", cudaGetErrorString(e));
 }
@@ -1204,7 +1230,7 @@ int launch_bdfp_to_float(const int16_t* m, const int8_t* exps, int64_t rows, int
 int launch_dfp_to_float(const int16_t* m, int64_t n, const int32_t* d_exp, float* out, cudaStream_t s)
 {
     if (n < 1) return ITO_OK;
-    k_dfp_to_float<<<launch_grid_blocks(n, 256), 256, 0, s>>>(m, n, d_exp, out);
+    launch_pdl(k_dfp_to_float, launch_grid_blocks(n, 256), 256, 0, s, m, n, d_exp, out);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp->float launch: %s", cudaGetErrorString(e));
 }
@@ -1213,7 +1239,7 @@ int launch_p64_to_float(const int64_t* P, int64_t n, const int32_t* d_ea, const 
                         cudaStream_t s)
 {
     if (n < 1) return ITO_OK;
-    k_p64_to_float<<<launch_grid_blocks(n, 256), 256, 0, s>>>(P, n, d_ea, d_eb, out);
+    launch_pdl(k_p64_to_float, launch_grid_blocks(n, 256), 256, 0, s, P, n, d_ea, d_eb, out);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "p64->float launch: %s", cudaGetErrorString(e));
 }
@@ -1225,6 +1251,8 @@ __global__ void k_dfp_update(int16_t* __restrict__ W, uint16_t* __restrict__ hi,
                              const int32_t* __restrict__ d_exp_g, int32_t exp_w, int32_t eta, int32_t lim,
                              int32_t* __restrict__ d_k, uint32_t* __restrict__ d_nonzero)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     // W * 2^Ew <- W * 2^Ew - G * 2^Eg * 2^-eta  =>  dW = G * 2^-(Ew + eta - Eg); W saturates to +-lim
     const int k = exp_w + eta - *d_exp_g;
     if (d_k && blockIdx.x == 0 && threadIdx.x == 0) *d_k = k;
@@ -1255,6 +1283,8 @@ __global__ void k_dfp_update_v4(int16_t* __restrict__ W, uint16_t* __restrict__ 
                                 const int32_t* __restrict__ d_exp_g, int32_t exp_w, int32_t eta, int32_t lim,
                                 int32_t* __restrict__ d_k, uint32_t* __restrict__ d_nonzero)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int k = exp_w + eta - *d_exp_g;
     if (d_k && blockIdx.x == 0 && threadIdx.x == 0) *d_k = k;
     const int kl = -k > 17 ? 17 : -k;     // a left shift past 17 bits saturates every difference anyway
@@ -1299,10 +1329,10 @@ int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const
     const int32_t lim = (1 << (bits - 1)) - 1;
     if (cols % 4 == 0 && rows * cols < (1LL << 31) && ldl % 4 == 0 && al(W, 8) && al(G, 8) &&
         (!hi || (al(hi, 8) && al(lo, 8))))
-        k_dfp_update_v4<<<launch_grid_blocks(rows * cols / 4, 256), 256, 0, s>>>(
+        launch_pdl(k_dfp_update_v4, launch_grid_blocks(rows * cols / 4, 256), 256, 0, s, 
             W, hi, lo, (int)ldl, G, (int)rows, (int)cols, d_exp_g, exp_w, eta, lim, d_k, d_nonzero);
     else
-        k_dfp_update<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(W, hi, lo, ldl, G, rows, cols, d_exp_g,
+        launch_pdl(k_dfp_update, launch_grid_blocks(rows * cols, 256), 256, 0, s, W, hi, lo, ldl, G, rows, cols, d_exp_g,
                                                                            exp_w, eta, lim, d_k, d_nonzero);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp update launch: %s", cudaGetErrorString(e));
@@ -1319,6 +1349,8 @@ int launch_dfp_update(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, const
 __global__ void k_dfp_set_bits(int16_t* __restrict__ W, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
                                int64_t ldl, int64_t rows, int64_t cols, int d, int32_t lim)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t v = d >= 0 ? (int64_t)W[i] * ((int64_t)1 << d) : rhu64(W[i], -d);
@@ -1340,7 +1372,7 @@ int launch_dfp_set_bits(int16_t* W, uint16_t* hi, uint16_t* lo, int64_t ldl, int
     if (bits_old < 2 || bits_old > 16 || bits_new < 2 || bits_new > 16)
         return set_error(ITO_ERR_ARG, "weight precision must be 2 .. 16 bits");
     if (rows < 1 || cols < 1 || bits_old == bits_new) return ITO_OK;
-    k_dfp_set_bits<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(W, hi, lo, ldl, rows, cols,
+    launch_pdl(k_dfp_set_bits, launch_grid_blocks(rows * cols, 256), 256, 0, s, W, hi, lo, ldl, rows, cols,
                                                                        bits_new - bits_old, (1 << (bits_new - 1)) - 1);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "precision change launch: %s", cudaGetErrorString(e));

@@ -37,8 +37,12 @@
 
 namespace ito {
 
-__global__ void k_set_i32(int32_t* p, int32_t v) { *p = v; }
-__global__ void k_copy_i32(int32_t* dst, const int32_t* src) { *dst = *src; }
+__global__ void k_set_i32(int32_t* p, int32_t v) {
+    griddep_wait();
+    griddep_launch_dependents(); *p = v; }
+__global__ void k_copy_i32(int32_t* dst, const int32_t* src) {
+    griddep_wait();
+    griddep_launch_dependents(); *dst = *src; }
 
 enum { D_EY = 0, D_EE, D_RS, D_RSD, D_RSG, D_EG, D_K, D_NZ, D_N32 };
 enum { D_PMAX = 0, D_PDMAX, D_PGMAX, D_GABS, D_N64 };
@@ -48,6 +52,8 @@ constexpr int kAptMaxEvals = 256;   // logged Gavg evaluations per epoch
 __global__ void k_apt_log(const unsigned long long* __restrict__ s64, const int32_t* __restrict__ s32, int nl,
                           unsigned long long* __restrict__ log_abs, int32_t* __restrict__ log_eg)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int l = threadIdx.x;
     if (l < nl) {
         log_abs[l] = s64[l * D_N64 + D_GABS];
@@ -501,7 +507,7 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
         ITO_TRY(dfp_gemm_plan(&L.pg, eh, el, true, ih, il, true, L.OC, L.IC, B, L.pg64, L.IC, m->u64(l, D_PGMAX),
                               m->tail_ws, m->tail_ws_bytes));
     }
-    k_set_i32<<<1, 1>>>(m->ew(), m->exp_w);
+    launch_pdl(k_set_i32, 1, 1, 0, 0, m->ew(), m->exp_w);
     if (cudaMemcpy(m->wexp_d, m->wexp.data(), sizeof(int32_t) * nl, cudaMemcpyHostToDevice) != cudaSuccess)
         return set_error(ITO_ERR_CUDA, "weight exponent copy");
     m->overlap = true;
@@ -628,6 +634,8 @@ int ito_dfp16_model_read_stats(const ito_dfp16_model* m, int64_t* host_out, int 
 __global__ void k_dfp_pack_stats(const int32_t* __restrict__ s32, const unsigned long long* __restrict__ s64, int nl,
                                  int64_t* __restrict__ out)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     for (int i = threadIdx.x; i < nl * (D_N32 + D_N64); i += blockDim.x) {
         const int l = i / (D_N32 + D_N64), k = i - l * (D_N32 + D_N64);
         out[i] = k < D_N32 ? (int64_t)s32[l * D_N32 + k] : (int64_t)s64[l * D_N64 + (k - D_N32)];
@@ -652,7 +660,7 @@ int ito_dfp16_train_step_host_async(ito_dfp16_model* m, const int16_t* x_host, i
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "input copy: %s", cudaGetErrorString(e));
     ITO_TRY(ito_dfp16_train_step(m, xd, exp_x, stream));
     if (stats_host) {
-        k_dfp_pack_stats<<<1, 128, 0, s>>>(m->s32, m->s64, nl, m->stats_packed);
+        launch_pdl(k_dfp_pack_stats, 1, 128, 0, s, m->s32, m->s64, nl, m->stats_packed);
         e = cudaGetLastError();
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(stats_host, m->stats_packed, sizeof(int64_t) * nl * (D_N32 + D_N64),
@@ -711,7 +719,7 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
         cudaMemsetAsync(m->s64, 0, sizeof(unsigned long long) * nl * D_N64, s) != cudaSuccess)
         return set_error(ITO_ERR_CUDA, "memset");
     m->launches = 0;
-    ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0, (k_set_i32<<<1, 1, 0, s>>>(m->ex(), exp_x), ITO_OK));
+    ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0, (launch_pdl(k_set_i32, 1, 1, 0, s, m->ex(), exp_x), ITO_OK));
     ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 6.0 * B * m->L[0].IC,
                 launch_i16_to_limbs(x, B, m->L[0].IC, m->xh, m->xl, m->ldx, s));
     for (int l = 0; l < nl; ++l) {
@@ -724,7 +732,7 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
                                     m->i32(l, D_EY), m->i32(l, D_RS), s));
     }
     ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0,
-                (k_copy_i32<<<1, 1, 0, s>>>(m->i32(nl - 1, D_EE), m->i32(nl - 1, D_EY)), ITO_OK));
+                (launch_pdl(k_copy_i32, 1, 1, 0, s, m->i32(nl - 1, D_EE), m->i32(nl - 1, D_EY)), ITO_OK));
     // backward, top-down; with the overlap on, the contractions stay on s and the
     // down-conversions and the update go to the side stream b: the propagated delta's
     // down-conversion runs beside the weight gradient, the gradient's down-conversion
@@ -772,7 +780,7 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
             if (m->apt_nlog >= kAptMaxEvals)
                 return set_error(ITO_ERR_ARG, "more than %d Gavg evaluations in one epoch", kAptMaxEvals);
             ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0,
-                        (k_apt_log<<<1, 32 * ((nl + 31) / 32), 0, s>>>(m->s64, m->s32, nl,
+                        (launch_pdl(k_apt_log, 1, 32 * ((nl + 31) / 32), 0, s, m->s64, m->s32, nl,
                                                                        m->log_abs + (size_t)m->apt_nlog * nl,
                                                                        m->log_eg + (size_t)m->apt_nlog * nl),
                          ITO_OK));
@@ -803,7 +811,7 @@ int ito_dfp16_model_set_precision(ito_dfp16_model* m, int layer, int32_t bits, v
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DLayer& L = m->L[layer];
     ITO_TRY(launch_dfp_set_bits(L.W, L.Wh, L.Wl, L.ldw, L.OC, L.IC, m->wbits[layer], bits, s));
-    k_set_i32<<<1, 1, 0, s>>>(m->wexp_d + layer, e);
+    launch_pdl(k_set_i32, 1, 1, 0, s, m->wexp_d + layer, e);
     m->wbits[layer] = bits;
     m->wexp[layer] = e;
     cudaError_t ce = cudaGetLastError();

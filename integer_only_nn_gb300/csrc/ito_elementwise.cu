@@ -50,6 +50,8 @@ __device__ __forceinline__ int64_t pitched(int64_t i, int64_t cols, int64_t ld)
 __global__ void k_i8_to_bf16_v8(const int8_t* __restrict__ src, int64_t rows, int64_t cols,
                                 uint16_t* __restrict__ dst, int64_t ldd)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t groups = rows * (cols >> 3);
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
@@ -69,6 +71,8 @@ __global__ void k_i8_to_bf16_v8(const int8_t* __restrict__ src, int64_t rows, in
 __global__ void k_i8_to_bf16_1(const int8_t* __restrict__ src, int64_t rows, int64_t cols, uint16_t* __restrict__ dst,
                                int64_t ldd)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         dst[pitched(i, cols, ldd)] = int_to_bf16_bits(src[i]);
@@ -79,9 +83,9 @@ int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* d
 {
     if (rows < 1 || cols < 1) return ITO_OK;
     if (cols % 8 == 0 && ldd % 8 == 0 && aligned(src, 8) && aligned(dst, 16))
-        k_i8_to_bf16_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(src, rows, cols, dst, ldd);
+        launch_pdl(k_i8_to_bf16_v8, launch_grid_blocks(rows * cols / 8, 256), 256, 0, s, src, rows, cols, dst, ldd);
     else
-        k_i8_to_bf16_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(src, rows, cols, dst, ldd);
+        launch_pdl(k_i8_to_bf16_1, launch_grid_blocks(rows * cols, 256), 256, 0, s, src, rows, cols, dst, ldd);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "convert launch: %s", cudaGetErrorString(e));
 }
@@ -90,6 +94,8 @@ int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* d
 __global__ void k_u8_to_bf16_v8(const uint8_t* __restrict__ src, int64_t rows, int64_t cols,
                                 uint16_t* __restrict__ dst, int64_t ldd)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t groups = rows * (cols >> 3);
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
@@ -109,6 +115,8 @@ __global__ void k_u8_to_bf16_v8(const uint8_t* __restrict__ src, int64_t rows, i
 __global__ void k_u8_to_bf16_1(const uint8_t* __restrict__ src, int64_t rows, int64_t cols, uint16_t* __restrict__ dst,
                                int64_t ldd)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         dst[pitched(i, cols, ldd)] = int_to_bf16_bits(src[i]);
@@ -119,9 +127,9 @@ int launch_u8_to_bf16(const uint8_t* src, int64_t rows, int64_t cols, uint16_t* 
 {
     if (rows < 1 || cols < 1) return ITO_OK;
     if (cols % 8 == 0 && ldd % 8 == 0 && aligned(src, 8) && aligned(dst, 16))
-        k_u8_to_bf16_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(src, rows, cols, dst, ldd);
+        launch_pdl(k_u8_to_bf16_v8, launch_grid_blocks(rows * cols / 8, 256), 256, 0, s, src, rows, cols, dst, ldd);
     else
-        k_u8_to_bf16_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(src, rows, cols, dst, ldd);
+        launch_pdl(k_u8_to_bf16_1, launch_grid_blocks(rows * cols, 256), 256, 0, s, src, rows, cols, dst, ldd);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "convert launch: %s", cudaGetErrorString(e));
 }
@@ -147,6 +155,8 @@ __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_
                              int64_t ldb, int32_t* __restrict__ d_shift, const uint8_t* __restrict__ gate_bits,
                              uint8_t* __restrict__ mask_out, int32_t* __restrict__ s_last)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int s = shift_for(*d_max, target_bits);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (d_shift) *d_shift = s;
@@ -190,6 +200,8 @@ __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t
                             const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
                             int64_t ldb, int32_t* __restrict__ d_shift, int32_t* __restrict__ s_last)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int s = shift_for(*d_max, target_bits);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (d_shift) *d_shift = s;
@@ -215,10 +227,10 @@ int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t*
     if ((gate_bits || mask_out) && !vec)
         return set_error(ITO_ERR_UNSUPPORTED, "bit-packed masks need rows of a multiple of 8 elements");
     if (vec)
-        k_requant_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(
+        launch_pdl(k_requant_v8, launch_grid_blocks(rows * cols / 8, 256), 256, 0, s, 
             Y, rows, cols, d_max, target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out, s_last);
     else
-        k_requant_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(Y, rows, cols, d_max, target_bits, relu,
+        launch_pdl(k_requant_1, launch_grid_blocks(rows * cols, 256), 256, 0, s, Y, rows, cols, d_max, target_bits, relu,
                                                                           gate, out8, outb, ldb, d_shift, s_last);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "requant launch: %s", cudaGetErrorString(e));
@@ -235,6 +247,8 @@ __global__ void k_roll_shift_predictions(int32_t* __restrict__ pred, const int32
                                          const int32_t* __restrict__ used, unsigned long long* __restrict__ count,
                                          int n, int on)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     unsigned hits = 0, misses = 0;
     for (int i = threadIdx.x; i < n; i += 32) {
         const int32_t p = pred[i], l = last[i];
@@ -257,7 +271,7 @@ int launch_roll_shift_predictions(int32_t* pred, const int32_t* last, const int3
                                   int on, cudaStream_t s)
 {
     if (n < 1) return ITO_OK;
-    k_roll_shift_predictions<<<1, 32, 0, s>>>(pred, last, used, reinterpret_cast<unsigned long long*>(count), n,
+    launch_pdl(k_roll_shift_predictions, 1, 32, 0, s, pred, last, used, reinterpret_cast<unsigned long long*>(count), n,
                                               on);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "prediction launch: %s", cudaGetErrorString(e));
@@ -281,6 +295,8 @@ __global__ void k_requant_static_v8(const int32_t* __restrict__ Y, int64_t rows,
                                     const int32_t* __restrict__ ksh, int relu, int8_t* __restrict__ out8,
                                     uint16_t* __restrict__ outb, int64_t ldb, uint8_t* __restrict__ mask_out)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int32_t lo = relu ? 0 : -128;
     const int64_t groups = rows * (cols >> 3);
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
@@ -311,6 +327,8 @@ __global__ void k_requant_static_1(const int32_t* __restrict__ Y, int64_t rows, 
                                    const int32_t* __restrict__ ksh, int relu, int8_t* __restrict__ out8,
                                    uint16_t* __restrict__ outb, int64_t ldb)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int32_t lo = relu ? 0 : -128;
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -329,10 +347,10 @@ int launch_requant_static(const int32_t* Y, int64_t rows, int64_t cols, const in
     const bool vec = cols % 8 == 0 && aligned(Y, 16) && aligned(out8, 8) && (!outb || (aligned(outb, 16) && ldb % 8 == 0));
     if (mask_out && !vec) return set_error(ITO_ERR_UNSUPPORTED, "bit-packed masks need rows of a multiple of 8");
     if (vec)
-        k_requant_static_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(Y, rows, cols, off, mult, ksh,
+        launch_pdl(k_requant_static_v8, launch_grid_blocks(rows * cols / 8, 256), 256, 0, s, Y, rows, cols, off, mult, ksh,
                                                                                       relu, out8, outb, ldb, mask_out);
     else
-        k_requant_static_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(Y, rows, cols, off, mult, ksh, relu,
+        launch_pdl(k_requant_static_1, launch_grid_blocks(rows * cols, 256), 256, 0, s, Y, rows, cols, off, mult, ksh, relu,
                                                                                  out8, outb, ldb);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "static requant launch: %s", cudaGetErrorString(e));
@@ -342,6 +360,8 @@ int launch_requant_static(const int32_t* Y, int64_t rows, int64_t cols, const in
 __global__ void k_offset_grad(const int8_t* __restrict__ delta, int64_t rows, int64_t cols, int32_t* __restrict__ g,
                               uint32_t* __restrict__ d_max)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     uint32_t mx = 0;
     for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols; c += (int64_t)gridDim.x * blockDim.x) {
         int32_t acc = 0;
@@ -358,6 +378,8 @@ __global__ void k_offset_update(int32_t* __restrict__ off, const int32_t* __rest
                                 int32_t* __restrict__ d_shift, int32_t* __restrict__ d_wshift,
                                 uint32_t* __restrict__ d_nonzero)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int s = shift_for(*d_max, target_bits);
     const int ws = s - mu_weight > 0 ? s - mu_weight : 0;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -380,10 +402,10 @@ int launch_offset_grad_update(const int8_t* delta, int64_t rows, int64_t cols, i
                               uint32_t* d_nonzero, cudaStream_t s)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
-    k_offset_grad<<<launch_grid_blocks(cols, 256), 256, 0, s>>>(delta, rows, cols, g, d_max);
+    launch_pdl(k_offset_grad, launch_grid_blocks(cols, 256), 256, 0, s, delta, rows, cols, g, d_max);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "offset grad launch: %s", cudaGetErrorString(e));
-    k_offset_update<<<launch_grid_blocks(cols, 256), 256, 0, s>>>(off, g, cols, d_max, target_bits, mu_weight, d_shift,
+    launch_pdl(k_offset_update, launch_grid_blocks(cols, 256), 256, 0, s, off, g, cols, d_max, target_bits, mu_weight, d_shift,
                                                                   d_wshift, d_nonzero);
     e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "offset update launch: %s", cudaGetErrorString(e));
@@ -438,6 +460,8 @@ __global__ void k_niti_update_v8(int8_t* __restrict__ W, uint16_t* __restrict__ 
                                  int32_t* __restrict__ d_shift, int32_t* __restrict__ d_wshift,
                                  uint32_t* __restrict__ d_nonzero)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int s = shift_for(*d_max, target_bits);
     const int ws = s - mu_weight > 0 ? s - mu_weight : 0;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -472,6 +496,8 @@ __global__ void k_niti_update_1(int8_t* __restrict__ W, uint16_t* __restrict__ W
                                 int32_t* __restrict__ d_shift, int32_t* __restrict__ d_wshift,
                                 uint32_t* __restrict__ d_nonzero)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int s = shift_for(*d_max, target_bits);
     const int ws = s - mu_weight > 0 ? s - mu_weight : 0;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -499,10 +525,10 @@ int launch_niti_update(int8_t* W, uint16_t* Wb, int64_t ldb, const int32_t* G, i
     if (rows < 1 || cols < 1) return ITO_OK;
     const bool vec = cols % 8 == 0 && aligned(W, 8) && aligned(G, 16) && (!Wb || (aligned(Wb, 16) && ldb % 8 == 0));
     if (vec)
-        k_niti_update_v8<<<launch_grid_blocks(rows * cols / 8, 256), 256, 0, s>>>(
+        launch_pdl(k_niti_update_v8, launch_grid_blocks(rows * cols / 8, 256), 256, 0, s, 
             W, Wb, ldb, G, rows, cols, d_max, target_bits, mu_weight, d_shift, d_wshift, d_nonzero);
     else
-        k_niti_update_1<<<launch_grid_blocks(rows * cols, 256), 256, 0, s>>>(
+        launch_pdl(k_niti_update_1, launch_grid_blocks(rows * cols, 256), 256, 0, s, 
             W, Wb, ldb, G, rows, cols, d_max, target_bits, mu_weight, d_shift, d_wshift, d_nonzero);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "update launch: %s", cudaGetErrorString(e));
@@ -517,6 +543,8 @@ __global__ void k_top_error(const int8_t* __restrict__ logits, const int32_t* __
                             int target_mag, int8_t* __restrict__ delta, uint16_t* __restrict__ deltab, int64_t ldb,
                             int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t n = (int64_t)B * C;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int b = (int)(i / C), j = (int)(i - (int64_t)b * C);
@@ -534,6 +562,8 @@ __global__ void k_top_error_v8(const int8_t* __restrict__ logits, const int32_t*
                                int target_mag, int8_t* __restrict__ delta, uint16_t* __restrict__ deltab, int64_t ldb,
                                int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int groups = C >> 3;
     for (int b = blockIdx.y; b < B; b += gridDim.y) {
         const int label = labels[b];
@@ -566,9 +596,9 @@ int launch_top_error(const int8_t* logits, const int32_t* labels, int B, int C, 
     if (vec) {
         const int groups = C / 8;
         const dim3 grid((groups + 127) / 128, B < 65535 ? B : 65535);
-        k_top_error_v8<<<grid, 128, 0, s>>>(logits, labels, B, C, target_mag, delta, deltab, ldb, err);
+        launch_pdl(k_top_error_v8, grid, 128, 0, s, logits, labels, B, C, target_mag, delta, deltab, ldb, err);
     } else {
-        k_top_error<<<launch_grid_blocks((int64_t)B * C, 256), 256, 0, s>>>(logits, labels, B, C, target_mag, delta,
+        launch_pdl(k_top_error, launch_grid_blocks((int64_t)B * C, 256), 256, 0, s, logits, labels, B, C, target_mag, delta,
                                                                              deltab, ldb, err);
     }
     cudaError_t e = cudaGetLastError();

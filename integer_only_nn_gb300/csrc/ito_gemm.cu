@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
               int splits, int kb_per_split, int64_t split_stride, int32_t* __restrict__ C, int64_t ldc,
               uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     // Work item w covers output tile w / splits and the K slice w % splits; with
     // splits > 1 each slice writes an int32 partial tile at C + slice * split_stride
     // (plain stores, no max) and a reduction kernel adds the slices.
@@ -373,6 +375,8 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
                int use_tma_store, int M, int N, int K, int chunk_kb, int group, int full_tiles, int parts,
                int32_t* __restrict__ C, int64_t ldc, uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     using Cfg = Tc2Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;
@@ -728,6 +732,8 @@ __global__ void __launch_bounds__(Tc2Cfg::THREADS, 1)
 // kernel returns (the wait every pipeline barrier of the contractions uses).
 __global__ void k_wait_timeout_selftest(int* __restrict__ err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x == 0) {
@@ -743,7 +749,7 @@ int launch_wait_timeout_selftest(cudaStream_t s)
 {
     int* err = device_error_word();
     if (!err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
-    k_wait_timeout_selftest<<<1, 32, 0, s>>>(err);
+    launch_pdl(k_wait_timeout_selftest, 1, 32, 0, s, err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
 }
@@ -801,6 +807,8 @@ int num_sms()
 __global__ void k_splitk_reduce(const int32_t* __restrict__ P, int splits, int64_t stride, int M, int N, int64_t ldc,
                                 int32_t* __restrict__ C, uint32_t* __restrict__ d_max)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t n = (int64_t)M * N;
     uint32_t mx = 0;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -821,6 +829,8 @@ __global__ void k_tail_reduce(const int32_t* __restrict__ P, int tail_tiles, int
                               TileSched sched, int M, int N, int64_t ldc, int32_t* __restrict__ C,
                               uint32_t* __restrict__ d_max)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     constexpr int T = 256;
     const int64_t n = (int64_t)tail_tiles * T * (T / 4);
     uint32_t mx = 0;
@@ -866,14 +876,14 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
     const int items = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + BN - 1) / BN) * p.splits;
     const int grid = items < num_sms() ? items : num_sms();
     const bool split = p.splits > 1;
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(p.mapA, p.mapB, p.mapC, split ? 0 : p.use_tma_store, p.M, p.N,
+    launch_pdl(kern, grid, Cfg::THREADS, Cfg::SMEM_BYTES, s, p.mapA, p.mapB, p.mapC, split ? 0 : p.use_tma_store, p.M, p.N,
                                                      p.K, p.chunk_kb, p.splits, p.kb_per_split, p.split_stride,
                                                      split ? p.split_ws : p.C, p.ldc, split ? nullptr : p.d_max,
                                                      p.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
     if (split) {
-        k_splitk_reduce<<<launch_grid_blocks((int64_t)p.M * p.N, 256), 256, 0, s>>>(
+        launch_pdl(k_splitk_reduce, launch_grid_blocks((int64_t)p.M * p.N, 256), 256, 0, s, 
             p.split_ws, p.splits, p.split_stride, p.M, p.N, p.ldc, p.C, p.d_max);
         e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "split-K reduce launch: %s", cudaGetErrorString(e));
@@ -966,13 +976,15 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     cfg.blockDim = dim3(Cfg::THREADS);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const FusedRq fz{p.rq_pred, p.rq_gate, p.rq_ldg, p.rq_relu, p.rq_redo, p.rq_d_shift, p.rq_s_last, p.rq_target_bits};
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapA, p.mapB, p.mapC, p.mapP, p.mapO8, p.mapOB, fz,
                                        p.use_tma_store, p.M, p.N, p.K, p.chunk_kb, p.group, p.tail_full, p.tail_parts,
@@ -981,7 +993,7 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     if (p.tail_parts > 1) {
         const TileSched sched{(p.M + 255) / 256, (p.N + 255) / 256, p.group};
         const int tail = tiles - p.tail_full;
-        k_tail_reduce<<<launch_grid_blocks((int64_t)tail * 256 * 64, 256), 256, 0, s>>>(
+        launch_pdl(k_tail_reduce, launch_grid_blocks((int64_t)tail * 256 * 64, 256), 256, 0, s, 
             p.split_ws, tail, p.tail_parts, p.tail_full, sched, p.M, p.N, p.ldc, p.C, p.d_max);
         e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "tail reduce launch: %s", cudaGetErrorString(e));

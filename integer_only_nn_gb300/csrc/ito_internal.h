@@ -10,6 +10,28 @@
 
 namespace ito {
 
+// Launches a kernel of this library with programmatic stream serialisation:
+// it may be scheduled while the previous kernel in the stream finishes (its
+// launch and CTA dispatch overlap that kernel's tail). Each kernel waits for its
+// predecessor (griddep_wait) before it touches global memory, so the stream
+// order of every memory access is the same as with a plain launch.
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Records an error text for ito_last_error_string() and returns `code`.
 int set_error(int code, const char* fmt, ...);
 
