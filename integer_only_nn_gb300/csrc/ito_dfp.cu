@@ -81,8 +81,6 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
                int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, DfpF32Out bk,
                int* __restrict__ err)
 {
-    griddep_wait();
-    griddep_launch_dependents();
     using Cfg = DfpCfg;
     constexpr bool F32OUT = MODE != DFP_EXACT;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -128,6 +126,9 @@ __global__ void __launch_bounds__(DfpCfg::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // on-chip setup above overlaps the previous kernel; global memory only from here on
+    griddep_wait();
+    griddep_launch_dependents();
 
     // tiles in row-major order over (m, n): consecutive CTAs share the A band
     if (warp == 0) {
@@ -466,8 +467,6 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
                 int K, int full_tiles, int parts, int64_t* __restrict__ C, int64_t ldc,
                 int64_t* __restrict__ tail_ws, unsigned long long* __restrict__ d_max, int* __restrict__ err)
 {
-    griddep_wait();
-    griddep_launch_dependents();
     using Cfg = Dfp2Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;                         // 32 columns per epilogue warp
@@ -514,6 +513,9 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // on-chip setup above overlaps the previous kernel; global memory only from here on
+    griddep_wait();
+    griddep_launch_dependents();
 
     // tiles in row-major order over (m, n): consecutive clusters share the A band
     if (warp == 0) {

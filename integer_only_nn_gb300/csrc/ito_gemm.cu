@@ -100,8 +100,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
               int splits, int kb_per_split, int64_t split_stride, int32_t* __restrict__ C, int64_t ldc,
               uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
-    griddep_wait();
-    griddep_launch_dependents();
     // Work item w covers output tile w / splits and the K slice w % splits; with
     // splits > 1 each slice writes an int32 partial tile at C + slice * split_stride
     // (plain stores, no max) and a reduction kernel adds the slices.
@@ -154,6 +152,9 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // on-chip setup above overlaps the previous kernel; global memory only from here on
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == 0) {
         // ---------------- TMA producer
