@@ -683,6 +683,338 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
     }
 }
 
+// ------------------------------------------- limb-stacked CTA-pair kernel
+//
+// The exact contraction with the two limb planes stacked along M inside a CTA
+// pair: for a 128 x 128 output tile, the leader CTA loads the high plane of
+// those 128 rows of A and of those 128 columns of B, the other CTA the low
+// planes of the same rows and columns. One tcgen05 cta_group::2 MMA of
+// M = 256 (the leader's A_hi rows, then the peer's A_lo rows) by N = 256 (the
+// leader's B_hi half, then the peer's B_lo half) per 16-term K step computes all
+// four limb products: the leader's tensor memory receives [hh | hl] of its
+// rows, the peer's [lh | ll] of the same rows. Per CTA and per operation that
+// moves the int8 pair kernel's shared-memory bytes (one 16 KB A plane and one
+// 16 KB B plane a K block), half of what the both-planes layout needs. Each
+// accumulator gets one limb product (at most 2^14) per K term, so a chunk of
+// 1024 terms is exact; two 256-column buffers fill the 512 columns. Each CTA
+// keeps its int64 partial of the tile in registers across chunks (leader:
+// 65536 hh + 256 hl, peer: 256 lh + ll); at the end of a tile the peer stores
+// its partial to C, the leader adds it to its own, folds max |P| and stores the
+// result (a bounded handshake of two cluster mbarriers orders the two).
+struct Dfp3Cfg {
+    static constexpr int BM = 128, BN = 128, BK = 64;      // output tile 128 x 128 per pair
+    static constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's limb plane of A
+    static constexpr int B_BYTES = BN * BK * 2;             // 16 KB: this CTA's limb plane of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = 6;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + EPI_WARPS * 32;
+    static constexpr int BUF_COLS = 2 * BN;                 // [x B_hi | x B_lo] per buffer
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int CHUNK_KB = 1024 / BK;              // exact chunk: 1024 K terms
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(Dfp3Cfg::THREADS, 1)
+    k_gemm_dfp3(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+                const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, int M, int N,
+                int K, int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max,
+                int* __restrict__ err)
+{
+    using Cfg = Dfp3Cfg;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int HALF = BN / 2;                          // 64 output columns per epilogue warp
+    constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, 2 * BN, A_MN, B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t* empty_bar = full_bar + STAGES;
+    uint64_t* accf_bar = empty_bar + STAGES;
+    uint64_t* acce_bar = accf_bar + 2;
+    uint64_t* xfull_bar = acce_bar + 2;    // leader: the peer's partial of the tile is in C
+    uint64_t* xempty_bar = acce_bar + 3;   // peer: the leader has taken the previous one
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (K + BK - 1) / BK;
+    const int num_chunks = (num_kb + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf_bar[b], 1);
+            mbar_init(&acce_bar[b], 2 * Cfg::EPI_WARPS);   // epilogue warps of both CTAs
+        }
+        mbar_init(xfull_bar, Cfg::EPI_WARPS);              // arrivals of the peer's epilogue warps
+        mbar_init(xempty_bar, Cfg::EPI_WARPS);             // arrivals of the leader's epilogue warps
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(leader ? &tmAh : &tmAl);
+        prefetch_tensormap(leader ? &tmBh : &tmBl);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // on-chip setup above overlaps the previous kernel; global memory only from here on
+    griddep_wait();
+    griddep_launch_dependents();
+
+    // tiles in row-major order over (m, n): consecutive clusters share the A band
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs): this CTA's limb plane of A and of B
+        if (lane == 0) {
+            const CUtensorMap* tmA = leader ? &tmAh : &tmAl;
+            const CUtensorMap* tmB = leader ? &tmBh : &tmBl;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+                const int rowA = (t / num_n) * BM, colB = (t % num_n) * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
+                    const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                    uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
+                    uint8_t* sB = sA + Cfg::A_BYTES;
+                    if (!A_MN) {
+                        tma_load_2d_pair(tmA, fb, sA, kb * BK, rowA);
+                    } else {
+                        tma_load_2d_pair(tmA, fb, sA, rowA, kb * BK);
+                        tma_load_2d_pair(tmA, fb, sA + 8192, rowA + 64, kb * BK);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d_pair(tmB, fb, sB, kb * BK, colB);
+                    } else {
+                        tma_load_2d_pair(tmB, fb, sB, colB, kb * BK);
+                        tma_load_2d_pair(tmB, fb, sB + 8192, colB + 64, kb * BK);
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: one thread of the leader CTA
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+                for (int c = 0; ok && c < num_chunks; ++c) {
+                    if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * Cfg::BUF_COLS);
+                    const int kb0 = c * Cfg::CHUNK_KB;
+                    const int kb1 = min(num_kb, kb0 + Cfg::CHUNK_KB);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full_bar[stage], phase, abort_flag, err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                        const uint32_t b0 = a0 + Cfg::A_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, 8192, 1024)
+                                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                            const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
+                                                     : smem_desc_sw128(b0 + k * 32, 16, 1024);
+                            tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        tc_commit_pair_mc(&empty_bar[stage], 0x3);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_mc(&accf_bar[buf], 0x3);
+                    if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue (both CTAs): this CTA's limb partial of the tile's rows
+        const int e = warp - 2;
+        const int quad = warp & 3;
+        const int half = e >> 2;
+        // leader: 65536 x [A_hi B_hi] + 256 x [A_hi B_lo]; peer: 256 x [A_lo B_hi] + [A_lo B_lo]
+        const int32_t scale0 = leader ? 65536 : 256, scale1 = leader ? 256 : 1;
+        int buf = 0;
+        uint32_t buf_phase = 0, x_phase = 0;
+        bool ok = true;
+        for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+            int64_t acc[HALF];
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) acc[i] = 0;
+            for (int c = 0; c < num_chunks; ++c) {
+                if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) +
+                                       (uint32_t)(buf * Cfg::BUF_COLS + half * HALF);
+#pragma unroll
+                for (int j = 0; j < HALF / 16; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + j * 16, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) * scale0;
+                    tmem_ld16(taddr + BN + j * 16, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) * scale1;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[buf]), 0));
+                if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+            }
+            if (!ok) break;
+            const int row = (t / num_n) * BM + quad * 32 + lane;
+            const int col0 = (t % num_n) * BN + half * HALF;
+            int64_t* dst = C + (int64_t)row * ldc + col0;
+            const bool full_row = row < M && col0 + HALF <= N && (ldc & 1) == 0 &&
+                                  (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+            if (!leader) {
+                // the peer's partial into C, then (once the leader has taken the previous
+                // tile's) the signal on the leader's barrier
+                if (row < M) {
+#pragma unroll
+                    for (int i = 0; i < HALF; i += 2) {
+                        if (full_row) {
+                            *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(acc[i], acc[i + 1]);
+                        } else {
+                            if (col0 + i < N) dst[i] = acc[i];
+                            if (col0 + i + 1 < N) dst[i + 1] = acc[i + 1];
+                        }
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    if (!mbar_wait(xempty_bar, x_phase ^ 1, abort_flag, err))
+                        ok = false;
+                    else
+                        mbar_arrive_cluster(mapa_shared(smem_u32(xfull_bar), 0));
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                x_phase ^= 1;
+                continue;
+            }
+            // leader: wait for the peer's partial, add, fold the max, store the result
+            if (!mbar_wait(xfull_bar, x_phase, abort_flag, err)) { ok = false; break; }
+            x_phase ^= 1;
+            __threadfence();
+            unsigned long long mx = 0;
+            if (row < M) {
+#pragma unroll
+                for (int i = 0; i < HALF; i += 2) {
+                    int64_t p0 = acc[i], p1 = acc[i + 1];
+                    if (full_row) {
+                        const longlong2 v = __ldcg(reinterpret_cast<const longlong2*>(dst + i));
+                        p0 += v.x;
+                        p1 += v.y;
+                        *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(p0, p1);
+                    } else {
+                        if (col0 + i < N) {
+                            p0 += __ldcg(dst + i);
+                            dst[i] = p0;
+                        } else {
+                            p0 = 0;
+                        }
+                        if (col0 + i + 1 < N) {
+                            p1 += __ldcg(dst + i + 1);
+                            dst[i + 1] = p1;
+                        } else {
+                            p1 = 0;
+                        }
+                    }
+                    const unsigned long long a0 = (unsigned long long)(p0 < 0 ? -p0 : p0);
+                    const unsigned long long a1 = (unsigned long long)(p1 < 0 ? -p1 : p1);
+                    mx = a0 > mx ? a0 : mx;
+                    mx = a1 > mx ? a1 : mx;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(xempty_bar), 1));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long v = __shfl_xor_sync(0xffffffffu, mx, o);
+                mx = v > mx ? v : mx;
+            }
+            if (lane == 0 && mx != 0) atomicMax(d_max, mx);
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();   // the pair's MMAs, drains and exchanges are complete in both CTAs
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <bool A_MN, bool B_MN>
+static int launch_dfp3(const DfpGemmPlan& p, cudaStream_t s)
+{
+    using Cfg = Dfp3Cfg;
+    auto kern = k_gemm_dfp3<A_MN, B_MN>;
+    static int max_clusters = 0;
+    if (!max_clusters) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(2 * num_sms());
+        q.blockDim = dim3(Cfg::THREADS);
+        q.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = 2;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1)
+            return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
+        max_clusters = n;
+    }
+    const int tiles = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + Cfg::BN - 1) / Cfg::BN);
+    const int clusters = tiles < max_clusters ? tiles : max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh3, p.mapBl3, p.M, p.N, p.K, p.C, p.ldc,
+                                       p.d_max, p.err);
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp stacked gemm launch: %s", cudaGetErrorString(e));
+}
+
 template <bool A_MN, bool B_MN>
 static int launch_dfp2(const DfpGemmPlan& p, cudaStream_t s)
 {
@@ -850,11 +1182,17 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
     if ((r = make_map_bf16(&p->mapAh, Ah, a_mn ? 64 : 128)) || (r = make_map_bf16(&p->mapAl, Al, a_mn ? 64 : 128)) ||
         (r = make_map_bf16(&p->mapBh, Bh, 64)) || (r = make_map_bf16(&p->mapBl, Bl, 64)))
         return r;
-    // CTA-pair kernel when there are at least 256 rows
+    // CTA-pair kernels when there are at least 256 rows: the limb-stacked one (128 x 128 tiles,
+    // B tensor maps of 128-row boxes when B is K-major) unless the caller gave room for a split
+    // last wave, which the both-planes kernel (256 x 64 tiles) takes
     p->pair = M >= 256 && C != nullptr;
+    p->stacked = p->pair && N >= 128;
+    if (p->stacked &&
+        ((r = make_map_bf16(&p->mapBh3, Bh, b_mn ? 64 : 128)) || (r = make_map_bf16(&p->mapBl3, Bl, b_mn ? 64 : 128))))
+        return r;
     p->tail_full = ((M + 255) / 256) * ((N + 63) / 64);
     p->tail_parts = 1;
-    if (p->pair && tail_ws) {
+    if (p->pair && !p->stacked && tail_ws) {
         int full, parts;
         dfp_tail_split(M, N, K, &full, &parts);
         const size_t need = parts > 1 ? (size_t)(p->tail_full - full) * parts * 256 * 64 * sizeof(int64_t) : 0;
@@ -924,6 +1262,12 @@ int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s)
 {
     if (p.blocked == 1) return launch_dfp<false, false, DFP_BLOCKED>(p, s);
     if (p.blocked == 2) return launch_dfp<false, false, DFP_CHAINED>(p, s);
+    if (p.stacked) {
+        if (!p.a_mn && !p.b_mn) return launch_dfp3<false, false>(p, s);
+        if (!p.a_mn && p.b_mn) return launch_dfp3<false, true>(p, s);
+        if (p.a_mn && p.b_mn) return launch_dfp3<true, true>(p, s);
+        return launch_dfp3<true, false>(p, s);
+    }
     if (p.pair) {
         if (!p.a_mn && !p.b_mn) return launch_dfp2<false, false>(p, s);
         if (!p.a_mn && p.b_mn) return launch_dfp2<false, true>(p, s);

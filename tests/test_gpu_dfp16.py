@@ -73,8 +73,11 @@ def test_dfp_wgrad(ito, B, IC, OC):
     _check_down(P, -32, g, eg, rs, mx)
 
 
-# at least 256 rows: the CTA-pair limb kernel (256 x 64 tiles, 1024-term chunks)
-PAIR_SHAPES = [(256, 64, 64), (300, 1000, 130), (513, 2049, 200), (1024, 4096, 64), (2048, 1100, 96)]
+# at least 256 rows: the CTA-pair limb kernels, 1024-term chunks (the limb-stacked one with
+# 128 x 128 tiles where the output has at least 128 columns, else 256 x 64 tiles); the last
+# two shapes take the limb-stacked kernel in all three contractions, ragged in M, N and K
+PAIR_SHAPES = [(256, 64, 64), (300, 1000, 130), (513, 2049, 200), (1024, 4096, 64), (2048, 1100, 96),
+               (1100, 700, 300), (600, 520, 260)]
 
 
 @pytest.mark.parametrize("B,IC,OC", PAIR_SHAPES)
@@ -90,12 +93,13 @@ def test_dfp_pair_fwd_dgrad_wgrad(ito, B, IC, OC):
     assert ito.ito_get_error() == 0
 
 
-def test_dfp_pair_extreme_chunks(ito):
-    """256+ rows, all products (-32767)^2: each of the pair kernel's four limb
+@pytest.mark.parametrize("OC", [70, 200])      # both pair kernels
+def test_dfp_pair_extreme_chunks(ito, OC):
+    """256+ rows, all products (-32767)^2: each of the pair kernels' limb
     accumulators reaches 2^24 exactly at a 1024-term chunk."""
     for K in (1023, 1024, 1025, 2048, 4096):
         x = np.full((300, K), -32767, np.int16)
-        W = np.full((70, K), -32767, np.int16)
+        W = np.full((OC, K), -32767, np.int16)
         W[1::2] = 32767
         p64, _, _, _, _ = ito.ito_dfp16_linear_fwd(_dev(x), ito._i32dev(0), _dev(W), ito._i32dev(0))
         P = _h(p64)
