@@ -58,7 +58,7 @@ def peaks():
         return dict(FALLBACK), "fallback"
 
 
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "k_gemm_tc__dram_per_launch__mlp4096x4-1000_b8192.md")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "k_gemm_tc2__dram_per_launch__ops_8192x4096x4096.md")
 GEMM_SOURCES = [os.path.join(ROOT, "integer_only_nn_gb300", "csrc", f) for f in ("ito_gemm.cu", "ito_device.cuh")]
 
 
@@ -616,7 +616,9 @@ def run_ours_model(args, w, cpu, barrier, dist, world, rank, local, flush, pk, p
     roof = gemm_roofline(prof, pk, pk_src)
     roof.update({"kernel": "k_gemm_tc2 / k_gemm_tc (bf16-embedded int8 contractions; re-launches after a "
                            "misprediction not counted)",
-                 "traffic": gemm_traffic_per_launch(w), "traffic_unit": "bytes per launch (ncu, committed summary)",
+                 "traffic": gemm_traffic_per_launch(w),
+                 "traffic_unit": "bytes per launch (ncu, committed summary: one launch of each 4096-wide contraction "
+                                 "kind at the step's shapes, averaged over the step's mix)",
                  "measured_over": "the same %d steps run again with an event pair around every launch "
                                   "(%.4f ms per step with the events)" % (K, prof_ms)})
     hbm = float(pk["hbm_gbs"])
