@@ -683,59 +683,52 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
     }
 }
 
-// ------------------------------------------- limb-stacked CTA-pair kernel
+// ------------------------------------------- wide-tile CTA-pair kernel
 //
-// The exact contraction with the two limb planes stacked along M inside a CTA
-// pair: for a 128 x 128 output tile, the leader CTA loads the high plane of
-// those 128 rows of A and of those 128 columns of B, the other CTA the low
-// planes of the same rows and columns. One tcgen05 cta_group::2 MMA of
-// M = 256 (the leader's A_hi rows, then the peer's A_lo rows) by N = 256 (the
-// leader's B_hi half, then the peer's B_lo half) per 16-term K step computes all
-// four limb products: the leader's tensor memory receives [hh | hl] of its
-// rows, the peer's [lh | ll] of the same rows. Per CTA and per operation that
-// moves the int8 pair kernel's shared-memory bytes (one 16 KB A plane and one
-// 16 KB B plane a K block), half of what the both-planes layout needs. Each
-// accumulator gets one limb product (at most 2^14) per K term, so a chunk of
-// 1024 terms is exact; two 256-column buffers fill the 512 columns. Each CTA
-// keeps its int64 partial of the tile in registers across chunks (leader:
-// 65536 hh + 256 hl, peer: 256 lh + ll); at the end of a tile the peer stores
-// its partial to C, the leader adds it to its own, folds max |P| and stores the
-// result (a bounded handshake of two cluster mbarriers orders the two).
-struct Dfp3Cfg {
-    static constexpr int BM = 128, BN = 128, BK = 64;      // output tile 128 x 128 per pair
-    static constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's limb plane of A
-    static constexpr int B_BYTES = BN * BK * 2;             // 16 KB: this CTA's limb plane of B
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = 6;
+// The exact contraction on a CTA pair with 256 x 128 output tiles: each CTA
+// loads both limb planes of its 128 rows of A and ONE limb plane of the tile's
+// 128 columns of B (the leader the high plane, the other CTA the low plane),
+// so the pair's B operand [B_hi | B_lo] (N = 256) is split between the two
+// CTAs as an M = 256 MMA reads it. Two MMAs per 16-term K step:
+// A_hi x [B_hi | B_lo] into [hh | hl] and A_lo x [B_hi | B_lo] into [lh | ll],
+// four 128-column fp32 accumulators that fill the 512 tensor-memory columns
+// (one buffer: the MMAs of the next chunk wait for the drain). Against the
+// 64-column tile this halves the A bytes per operation moved into and read
+// from shared memory. Each accumulator gets one limb product (at most 2^14) per
+// K term, so an exact chunk is 1024 terms; after a chunk the epilogue adds
+// 65536 hh + 256 (hl + lh) + ll into the tile's int64 sums in registers.
+struct Dfp4Cfg {
+    static constexpr int BM = 128, BN = 128, BK = 64;      // BM rows per CTA (256 per pair), BN columns
+    static constexpr int A_PLANE = BM * BK * 2;             // 16 KB
+    static constexpr int B_PLANE = BN * BK * 2;             // 16 KB: one limb plane of the tile's B
+    static constexpr int STAGE_BYTES = 2 * A_PLANE + B_PLANE;
+    static constexpr int STAGES = 4;
     static constexpr int EPI_WARPS = 8;
     static constexpr int THREADS = 64 + EPI_WARPS * 32;
-    static constexpr int BUF_COLS = 2 * BN;                 // [x B_hi | x B_lo] per buffer
-    static constexpr int TMEM_COLS = 512;
+    static constexpr int TMEM_COLS = 512;                   // hh, hl, lh, ll at +0, +128, +256, +384
     static constexpr int CHUNK_KB = 1024 / BK;              // exact chunk: 1024 K terms
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 };
 
 template <bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(Dfp3Cfg::THREADS, 1)
-    k_gemm_dfp3(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+__global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
+    k_gemm_dfp4(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                 const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, int M, int N,
                 int K, int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max,
                 int* __restrict__ err)
 {
-    using Cfg = Dfp3Cfg;
+    using Cfg = Dfp4Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
-    constexpr int HALF = BN / 2;                          // 64 output columns per epilogue warp
+    constexpr int HALF = BN / 2;                          // 64 columns per epilogue warp
     constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, 2 * BN, A_MN, B_MN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
     uint64_t* empty_bar = full_bar + STAGES;
-    uint64_t* accf_bar = empty_bar + STAGES;
-    uint64_t* acce_bar = accf_bar + 2;
-    uint64_t* xfull_bar = acce_bar + 2;    // leader: the peer's partial of the tile is in C
-    uint64_t* xempty_bar = acce_bar + 3;   // peer: the leader has taken the previous one
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 4);
+    uint64_t* accf_bar = empty_bar + STAGES;   // the chunk's accumulators are complete
+    uint64_t* acce_bar = accf_bar + 1;         // they have been drained (both CTAs)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -743,7 +736,7 @@ __global__ void __launch_bounds__(Dfp3Cfg::THREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-    const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+    const int num_m = (M + 2 * BM - 1) / (2 * BM), num_n = (N + BN - 1) / BN;
     const int num_tiles = num_m * num_n;
     const int num_kb = (K + BK - 1) / BK;
     const int num_chunks = (num_kb + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
@@ -753,15 +746,12 @@ __global__ void __launch_bounds__(Dfp3Cfg::THREADS, 1)
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&accf_bar[b], 1);
-            mbar_init(&acce_bar[b], 2 * Cfg::EPI_WARPS);   // epilogue warps of both CTAs
-        }
-        mbar_init(xfull_bar, Cfg::EPI_WARPS);              // arrivals of the peer's epilogue warps
-        mbar_init(xempty_bar, Cfg::EPI_WARPS);             // arrivals of the leader's epilogue warps
+        mbar_init(accf_bar, 1);
+        mbar_init(acce_bar, 2 * Cfg::EPI_WARPS);   // epilogue warps of both CTAs
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tensormap(leader ? &tmAh : &tmAl);
+        prefetch_tensormap(&tmAh);
+        prefetch_tensormap(&tmAl);
         prefetch_tensormap(leader ? &tmBh : &tmBl);
     }
     if (warp == 1) {
@@ -778,26 +768,30 @@ __global__ void __launch_bounds__(Dfp3Cfg::THREADS, 1)
 
     // tiles in row-major order over (m, n): consecutive clusters share the A band
     if (warp == 0) {
-        // ---------------- TMA producer (both CTAs): this CTA's limb plane of A and of B
+        // ---------------- TMA producer (both CTAs): loads complete on the leader's barrier
         if (lane == 0) {
-            const CUtensorMap* tmA = leader ? &tmAh : &tmAl;
             const CUtensorMap* tmB = leader ? &tmBh : &tmBl;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int t = cluster; ok && t < num_tiles; t += nclusters) {
-                const int rowA = (t / num_n) * BM, colB = (t % num_n) * BN;
+                const int rowA = (t / num_n) * 2 * BM + (int)rank * BM, colB = (t % num_n) * BN;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
                     if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
                     const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
-                    uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
-                    uint8_t* sB = sA + Cfg::A_BYTES;
+                    uint8_t* sAh = smem + stage * Cfg::STAGE_BYTES;
+                    uint8_t* sAl = sAh + Cfg::A_PLANE;
+                    uint8_t* sB = sAl + Cfg::A_PLANE;
                     if (!A_MN) {
-                        tma_load_2d_pair(tmA, fb, sA, kb * BK, rowA);
+                        tma_load_2d_pair(&tmAh, fb, sAh, kb * BK, rowA);
+                        tma_load_2d_pair(&tmAl, fb, sAl, kb * BK, rowA);
                     } else {
-                        tma_load_2d_pair(tmA, fb, sA, rowA, kb * BK);
-                        tma_load_2d_pair(tmA, fb, sA + 8192, rowA + 64, kb * BK);
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j) {
+                            tma_load_2d_pair(&tmAh, fb, sAh + j * 8192, rowA + j * 64, kb * BK);
+                            tma_load_2d_pair(&tmAl, fb, sAl + j * 8192, rowA + j * 64, kb * BK);
+                        }
                     }
                     if (!B_MN) {
                         tma_load_2d_pair(tmB, fb, sB, kb * BK, colB);
@@ -813,156 +807,110 @@ __global__ void __launch_bounds__(Dfp3Cfg::THREADS, 1)
         // ---------------- MMA issuer: one thread of the leader CTA
         if (leader && lane == 0) {
             int stage = 0;
-            uint32_t phase = 0;
-            int buf = 0;
-            uint32_t buf_phase = 0;
+            uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
+            const uint32_t d_hi = tmem_base;               // [hh | hl]
+            const uint32_t d_lo = tmem_base + 2 * BN;      // [lh | ll]
             for (int t = cluster; ok && t < num_tiles; t += nclusters) {
                 for (int c = 0; ok && c < num_chunks; ++c) {
-                    if (!mbar_wait(&acce_bar[buf], buf_phase ^ 1, abort_flag, err)) { ok = false; break; }
+                    if (!mbar_wait(acce_bar, acc_phase ^ 1, abort_flag, err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * Cfg::BUF_COLS);
                     const int kb0 = c * Cfg::CHUNK_KB;
                     const int kb1 = min(num_kb, kb0 + Cfg::CHUNK_KB);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&full_bar[stage], phase, abort_flag, err)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t a0 = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-                        const uint32_t b0 = a0 + Cfg::A_BYTES;
+                        const uint32_t ah0 = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                        const uint32_t al0 = ah0 + Cfg::A_PLANE;
+                        const uint32_t b0 = al0 + Cfg::A_PLANE;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
-                            const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, 8192, 1024)
-                                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                            const uint32_t ao = A_MN ? k * 2048 : k * 32;
+                            const uint32_t albo = A_MN ? 8192 : 16;
+                            const uint64_t ah = smem_desc_sw128(ah0 + ao, albo, 1024);
+                            const uint64_t al = smem_desc_sw128(al0 + ao, albo, 1024);
                             const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
                                                      : smem_desc_sw128(b0 + k * 32, 16, 1024);
-                            tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+                            tc_mma_bf16_pair(d_hi, ah, bd, IDESC, acc);
+                            tc_mma_bf16_pair(d_lo, al, bd, IDESC, acc);
                         }
                         tc_commit_pair_mc(&empty_bar[stage], 0x3);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
                     if (!ok) break;
-                    tc_commit_pair_mc(&accf_bar[buf], 0x3);
-                    if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+                    tc_commit_pair_mc(accf_bar, 0x3);
+                    acc_phase ^= 1;
                 }
             }
         }
     } else {
-        // ---------------- epilogue (both CTAs): this CTA's limb partial of the tile's rows
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile
         const int e = warp - 2;
         const int quad = warp & 3;
         const int half = e >> 2;
-        // leader: 65536 x [A_hi B_hi] + 256 x [A_hi B_lo]; peer: 256 x [A_lo B_hi] + [A_lo B_lo]
-        const int32_t scale0 = leader ? 65536 : 256, scale1 = leader ? 256 : 1;
-        int buf = 0;
-        uint32_t buf_phase = 0, x_phase = 0;
+        uint32_t acc_phase = 0;
         bool ok = true;
         for (int t = cluster; ok && t < num_tiles; t += nclusters) {
             int64_t acc[HALF];
 #pragma unroll
             for (int i = 0; i < HALF; ++i) acc[i] = 0;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * HALF);
             for (int c = 0; c < num_chunks; ++c) {
-                if (!mbar_wait(&accf_bar[buf], buf_phase, abort_flag, err)) { ok = false; break; }
+                if (!mbar_wait(accf_bar, acc_phase, abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) +
-                                       (uint32_t)(buf * Cfg::BUF_COLS + half * HALF);
+                // 65536 hh + 256 hl + 256 lh + ll, one accumulator at a time
+#pragma unroll 1
+                for (int part = 0; part < 4; ++part) {
+                    const int32_t scale = part == 0 ? 65536 : (part == 3 ? 1 : 256);
 #pragma unroll
-                for (int j = 0; j < HALF / 16; ++j) {
-                    uint32_t r[16];
-                    tmem_ld16(taddr + j * 16, r);
-                    tmem_ld_wait();
+                    for (int j = 0; j < HALF / 16; ++j) {
+                        uint32_t r[16];
+                        tmem_ld16(taddr + part * BN + j * 16, r);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) * scale0;
-                    tmem_ld16(taddr + BN + j * 16, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) * scale1;
+                        for (int i = 0; i < 16; ++i)
+                            acc[j * 16 + i] += (int64_t)__float2int_rn(__uint_as_float(r[i])) * scale;
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[buf]), 0));
-                if (++buf == 2) { buf = 0; buf_phase ^= 1; }
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acce_bar), 0));
+                acc_phase ^= 1;
             }
             if (!ok) break;
-            const int row = (t / num_n) * BM + quad * 32 + lane;
-            const int col0 = (t % num_n) * BN + half * HALF;
-            int64_t* dst = C + (int64_t)row * ldc + col0;
-            const bool full_row = row < M && col0 + HALF <= N && (ldc & 1) == 0 &&
-                                  (reinterpret_cast<uintptr_t>(C) & 15) == 0;
-            if (!leader) {
-                // the peer's partial into C, then (once the leader has taken the previous
-                // tile's) the signal on the leader's barrier
-                if (row < M) {
-#pragma unroll
-                    for (int i = 0; i < HALF; i += 2) {
-                        if (full_row) {
-                            *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(acc[i], acc[i + 1]);
-                        } else {
-                            if (col0 + i < N) dst[i] = acc[i];
-                            if (col0 + i + 1 < N) dst[i + 1] = acc[i + 1];
-                        }
-                    }
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) {
-                    if (!mbar_wait(xempty_bar, x_phase ^ 1, abort_flag, err))
-                        ok = false;
-                    else
-                        mbar_arrive_cluster(mapa_shared(smem_u32(xfull_bar), 0));
-                }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                x_phase ^= 1;
-                continue;
-            }
-            // leader: wait for the peer's partial, add, fold the max, store the result
-            if (!mbar_wait(xfull_bar, x_phase, abort_flag, err)) { ok = false; break; }
-            x_phase ^= 1;
-            __threadfence();
             unsigned long long mx = 0;
-            if (row < M) {
 #pragma unroll
-                for (int i = 0; i < HALF; i += 2) {
-                    int64_t p0 = acc[i], p1 = acc[i + 1];
-                    if (full_row) {
-                        const longlong2 v = __ldcg(reinterpret_cast<const longlong2*>(dst + i));
-                        p0 += v.x;
-                        p1 += v.y;
-                        *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(p0, p1);
-                    } else {
-                        if (col0 + i < N) {
-                            p0 += __ldcg(dst + i);
-                            dst[i] = p0;
-                        } else {
-                            p0 = 0;
-                        }
-                        if (col0 + i + 1 < N) {
-                            p1 += __ldcg(dst + i + 1);
-                            dst[i + 1] = p1;
-                        } else {
-                            p1 = 0;
-                        }
-                    }
-                    const unsigned long long a0 = (unsigned long long)(p0 < 0 ? -p0 : p0);
-                    const unsigned long long a1 = (unsigned long long)(p1 < 0 ? -p1 : p1);
-                    mx = a0 > mx ? a0 : mx;
-                    mx = a1 > mx ? a1 : mx;
-                }
+            for (int i = 0; i < HALF; ++i) {
+                const unsigned long long a = (unsigned long long)(acc[i] < 0 ? -acc[i] : acc[i]);
+                mx = a > mx ? a : mx;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(xempty_bar), 1));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const unsigned long long v = __shfl_xor_sync(0xffffffffu, mx, o);
                 mx = v > mx ? v : mx;
             }
             if (lane == 0 && mx != 0) atomicMax(d_max, mx);
+            // the int64 result from registers: 64 consecutive values per row
+            const int row = (t / num_n) * 2 * BM + (int)rank * BM + quad * 32 + lane;
+            const int col0 = (t % num_n) * BN + half * HALF;
+            if (row < M) {
+                int64_t* dst = C + (int64_t)row * ldc + col0;
+                if (col0 + HALF <= N && (ldc & 1) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
+#pragma unroll
+                    for (int i = 0; i < HALF; i += 2)
+                        *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(acc[i], acc[i + 1]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i)
+                        if (col0 + i < N) dst[i] = acc[i];
+                }
+            }
         }
     }
 
     tc_fence_before();
-    cluster_sync();   // the pair's MMAs, drains and exchanges are complete in both CTAs
+    cluster_sync();   // the pair's MMAs and drains are complete in both CTAs
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
@@ -970,10 +918,10 @@ __global__ void __launch_bounds__(Dfp3Cfg::THREADS, 1)
 }
 
 template <bool A_MN, bool B_MN>
-static int launch_dfp3(const DfpGemmPlan& p, cudaStream_t s)
+static int launch_dfp4(const DfpGemmPlan& p, cudaStream_t s)
 {
-    using Cfg = Dfp3Cfg;
-    auto kern = k_gemm_dfp3<A_MN, B_MN>;
+    using Cfg = Dfp4Cfg;
+    auto kern = k_gemm_dfp4<A_MN, B_MN>;
     static int max_clusters = 0;
     if (!max_clusters) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
@@ -994,7 +942,7 @@ static int launch_dfp3(const DfpGemmPlan& p, cudaStream_t s)
             return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
         max_clusters = n;
     }
-    const int tiles = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + Cfg::BN - 1) / Cfg::BN);
+    const int tiles = ((p.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((p.N + Cfg::BN - 1) / Cfg::BN);
     const int clusters = tiles < max_clusters ? tiles : max_clusters;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
@@ -1012,7 +960,7 @@ static int launch_dfp3(const DfpGemmPlan& p, cudaStream_t s)
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh3, p.mapBl3, p.M, p.N, p.K, p.C, p.ldc,
                                        p.d_max, p.err);
-    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp stacked gemm launch: %s", cudaGetErrorString(e));
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp wide gemm launch: %s", cudaGetErrorString(e));
 }
 
 template <bool A_MN, bool B_MN>
@@ -1182,9 +1130,9 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
     if ((r = make_map_bf16(&p->mapAh, Ah, a_mn ? 64 : 128)) || (r = make_map_bf16(&p->mapAl, Al, a_mn ? 64 : 128)) ||
         (r = make_map_bf16(&p->mapBh, Bh, 64)) || (r = make_map_bf16(&p->mapBl, Bl, 64)))
         return r;
-    // CTA-pair kernels when there are at least 256 rows: the limb-stacked one (128 x 128 tiles,
-    // B tensor maps of 128-row boxes when B is K-major) unless the caller gave room for a split
-    // last wave, which the both-planes kernel (256 x 64 tiles) takes
+    // CTA-pair kernels when there are at least 256 rows: the wide-tile one (256 x 128 tiles,
+    // B tensor maps of 128-row boxes when B is K-major) when the output has 128 columns or more,
+    // else the 256 x 64 one (which splits a partial last wave along K when given room)
     p->pair = M >= 256 && C != nullptr;
     p->stacked = p->pair && N >= 128;
     if (p->stacked &&
@@ -1263,10 +1211,10 @@ int dfp_gemm_run(const DfpGemmPlan& p, cudaStream_t s)
     if (p.blocked == 1) return launch_dfp<false, false, DFP_BLOCKED>(p, s);
     if (p.blocked == 2) return launch_dfp<false, false, DFP_CHAINED>(p, s);
     if (p.stacked) {
-        if (!p.a_mn && !p.b_mn) return launch_dfp3<false, false>(p, s);
-        if (!p.a_mn && p.b_mn) return launch_dfp3<false, true>(p, s);
-        if (p.a_mn && p.b_mn) return launch_dfp3<true, true>(p, s);
-        return launch_dfp3<true, false>(p, s);
+        if (!p.a_mn && !p.b_mn) return launch_dfp4<false, false>(p, s);
+        if (!p.a_mn && p.b_mn) return launch_dfp4<false, true>(p, s);
+        if (p.a_mn && p.b_mn) return launch_dfp4<true, true>(p, s);
+        return launch_dfp4<true, false>(p, s);
     }
     if (p.pair) {
         if (!p.a_mn && !p.b_mn) return launch_dfp2<false, false>(p, s);

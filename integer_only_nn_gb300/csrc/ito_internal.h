@@ -105,7 +105,7 @@ struct DfpGemmPlan {
     int M, N, K;
     int chunk_kb;                 // K blocks of 64 per exact chunk
     int pair;                     // CTA-pair kernel (256 x 64 tiles)
-    int stacked;                  // limb-stacked CTA-pair kernel (128 x 128 tiles; see k_gemm_dfp3)
+    int stacked;                  // wide-tile CTA-pair kernel (256 x 128 tiles; see k_gemm_dfp4)
     CUtensorMap mapBh3, mapBl3;   // its B maps (128-row boxes when B is K-major)
     int tail_full, tail_parts;    // pair kernel: whole tiles, K pieces per remaining tile (1: no split)
     int64_t* tail_ws;             // [pieces][256][64] int64 partials of the split tiles
