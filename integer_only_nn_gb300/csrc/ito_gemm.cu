@@ -805,20 +805,63 @@ int num_sms()
 
 // C[r][c] = sum over slices of P[s][r][c]; max |C| folded into *d_max. Integer
 // addition wraps modulo 2^32, so the slice order cannot change a result that fits int32.
+// C = the sum of the `splits` partial results (exact: integer addition modulo 2^32);
+// max |C| folded into *d_max. Four consecutive columns a thread when the rows allow
+// 16-byte loads, eight slices' loads in flight.
 __global__ void k_splitk_reduce(const int32_t* __restrict__ P, int splits, int64_t stride, int M, int N, int64_t ldc,
-                                int32_t* __restrict__ C, uint32_t* __restrict__ d_max)
+                                int32_t* __restrict__ C, uint32_t* __restrict__ d_max, int vec)
 {
     griddep_wait();
     griddep_launch_dependents();
-    const int64_t n = (int64_t)M * N;
     uint32_t mx = 0;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / N, c = i - r * N;
-        const int64_t off = r * ldc + c;
-        int32_t acc = 0;
-        for (int s = 0; s < splits; ++s) acc += __ldcs(P + s * stride + off);
-        C[off] = acc;
-        mx = max(mx, abs_u32(acc));
+    if (vec) {
+        const int gpr = N >> 2;
+        const int64_t n = (int64_t)M * gpr;
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t r = i / gpr;
+            const int64_t off = r * ldc + ((i - r * gpr) << 2);
+            int4 acc = make_int4(0, 0, 0, 0);
+            int s = 0;
+            for (; s + 8 <= splits; s += 8) {
+                int4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = __ldcs(reinterpret_cast<const int4*>(P + (s + u) * stride + off));
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    acc.x += v[u].x;
+                    acc.y += v[u].y;
+                    acc.z += v[u].z;
+                    acc.w += v[u].w;
+                }
+            }
+            for (; s < splits; ++s) {
+                const int4 v = __ldcs(reinterpret_cast<const int4*>(P + s * stride + off));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            *reinterpret_cast<int4*>(C + off) = acc;
+            mx = max(max(max(mx, abs_u32(acc.x)), abs_u32(acc.y)), max(abs_u32(acc.z), abs_u32(acc.w)));
+        }
+    } else {
+        const int64_t n = (int64_t)M * N;
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t r = i / N, c = i - r * N;
+            const int64_t off = r * ldc + c;
+            int32_t acc = 0;
+            int s = 0;
+            for (; s + 8 <= splits; s += 8) {
+                int32_t v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = __ldcs(P + (s + u) * stride + off);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) acc += v[u];
+            }
+            for (; s < splits; ++s) acc += __ldcs(P + s * stride + off);
+            C[off] = acc;
+            mx = max(mx, abs_u32(acc));
+        }
     }
     block_atomic_max(d_max, mx);
 }
@@ -884,8 +927,11 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
     if (split) {
-        launch_pdl(k_splitk_reduce, launch_grid_blocks((int64_t)p.M * p.N, 256), 256, 0, s, 
-            p.split_ws, p.splits, p.split_stride, p.M, p.N, p.ldc, p.C, p.d_max);
+        const int vec = p.N % 4 == 0 && p.ldc % 4 == 0 && p.split_stride % 4 == 0 &&
+                        (reinterpret_cast<uintptr_t>(p.split_ws) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(p.C) & 15) == 0;
+        launch_pdl(k_splitk_reduce, launch_grid_blocks((int64_t)p.M * p.N / (vec ? 4 : 1), 256), 256, 0, s,
+                   p.split_ws, p.splits, p.split_stride, p.M, p.N, p.ldc, p.C, p.d_max, vec);
         e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "split-K reduce launch: %s", cudaGetErrorString(e));
     }
@@ -1002,12 +1048,31 @@ static int launch_tc2(const GemmPlan& p, cudaStream_t s)
     return ITO_OK;
 }
 
+// Tile width of the single-CTA kernel for N output columns: the fewest computed
+// columns, a 64-column tile counted one and a half times (its B tile is too
+// narrow to keep the MMA fed from shared memory); ties go to the wider tile.
+// N = 576 takes 128 (640 columns computed, against 768 at 256).
+static int choose_bn(int N)
+{
+    int best = 256;
+    int64_t best_cost = INT64_MAX;
+    for (int bn = 256; bn >= 64; bn /= 2) {
+        const int64_t cols = (int64_t)((N + bn - 1) / bn) * bn;
+        const int64_t cost = bn == 64 ? 3 * cols : 2 * cols;
+        if (cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 // K slices for a contraction with few output tiles and a long K on the
 // single-CTA kernel (1 = no split): enough work items to cover the SMs, each
 // slice at least one K block.
 static int split_count(int M, int N, int K)
 {
-    const int bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+    const int bn = choose_bn(N);
     const int tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
     const int num_kb = (K + 63) / 64;
     if (num_kb < 32 || 2 * tiles > num_sms()) return 1;
@@ -1059,7 +1124,7 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
     p->chunk_kb = chunk_terms / 64;
     p->err = device_error_word();
     if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
-    p->bn = N > 128 ? 256 : (N > 64 ? 128 : 64);
+    p->bn = choose_bn(N);
     // CTA-pair kernel for large tiles
     p->splits = 1;
     p->kb_per_split = (K + 63) / 64;
