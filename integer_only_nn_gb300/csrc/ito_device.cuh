@@ -291,6 +291,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                  : "memory");
 }
 
+// 3-D tiled TMA store from shared memory (coordinates x innermost).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // An L2 cache policy that marks the lines it touches for early eviction: for outputs no
 // later kernel of the same pass reads back soon, so that they do not displace operands.
 __device__ __forceinline__ uint64_t l2_policy_evict_first()

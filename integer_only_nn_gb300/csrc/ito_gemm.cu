@@ -96,13 +96,15 @@ struct TcCfg {
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K, int chunk_kb,
+              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS, int use_tma_store,
+              int split_tma, int M, int N, int K, int chunk_kb,
               int splits, int kb_per_split, int64_t split_stride, int32_t* __restrict__ C, int64_t ldc,
               uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
     // Work item w covers output tile w / splits and the K slice w % splits; with
     // splits > 1 each slice writes an int32 partial tile at C + slice * split_stride
-    // (plain stores, no max) and a reduction kernel adds the slices.
+    // (no max; by TMA through tmS, the partials as [splits][M][N], when split_tma) and a
+    // reduction kernel adds the slices.
     using Cfg = TcCfg<BN>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;                             // columns per epilogue warp
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
             if (lane == 0 && mx != 0 && d_max) atomicMax(d_max, mx);
             const int row0 = tm * BM + quad * 32;
             const int col0 = tn * BN + half * HALF;
-            if (use_tma_store) {
+            if (use_tma_store || split_tma) {
                 // 32 x 32 boxes through shared memory (128-byte swizzle: 16-byte chunk j of
                 // row r sits at chunk j ^ (r % 8)), written out by TMA; the edges are clipped
 #pragma unroll
@@ -292,7 +294,10 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, stg, col0 + g * 32, row0);
+                        if (split_tma)
+                            tma_store_3d(&tmS, stg, col0 + g * 32, row0, w % splits);
+                        else
+                            tma_store_2d(&tmC, stg, col0 + g * 32, row0);
                         bulk_commit();
                     }
                 }
@@ -920,10 +925,9 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
     const int items = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + BN - 1) / BN) * p.splits;
     const int grid = items < num_sms() ? items : num_sms();
     const bool split = p.splits > 1;
-    launch_pdl(kern, grid, Cfg::THREADS, Cfg::SMEM_BYTES, s, p.mapA, p.mapB, p.mapC, split ? 0 : p.use_tma_store, p.M, p.N,
-                                                     p.K, p.chunk_kb, p.splits, p.kb_per_split, p.split_stride,
-                                                     split ? p.split_ws : p.C, p.ldc, split ? nullptr : p.d_max,
-                                                     p.err);
+    launch_pdl(kern, grid, Cfg::THREADS, Cfg::SMEM_BYTES, s, p.mapA, p.mapB, p.mapC, p.mapS,
+               split ? 0 : p.use_tma_store, split ? p.split_tma : 0, p.M, p.N, p.K, p.chunk_kb, p.splits,
+               p.kb_per_split, p.split_stride, split ? p.split_ws : p.C, p.ldc, split ? nullptr : p.d_max, p.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
     if (split) {
@@ -1175,6 +1179,19 @@ int gemm_plan(GemmPlan* p, const Bf16View& A, bool a_mn, const Bf16View& B, bool
     r = make_map_bf16(&p->mapB, B, b_mn ? 64 : (p->pair ? 128 : p->bn));
     if (r) return r;
     // int32 output through TMA stores when its rows are 16-byte aligned; plain stores otherwise
+    if (p->splits > 1 && (reinterpret_cast<uintptr_t>(p->split_ws) & 15) == 0 && (ldc & 3) == 0) {
+        // the split partials [splits][M][N] (pitch ldc): a slice's 32-row boxes clip at its own M
+        auto enc = get_encode();
+        cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)p->splits};
+        cuuint64_t strides[2] = {(cuuint64_t)ldc * 4, (cuuint64_t)p->split_stride * 4};
+        cuuint32_t box[3] = {32, 32, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult cr = enc(&p->mapS, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, p->split_ws, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (partials) failed (%d)", (int)cr);
+        p->split_tma = 1;
+    }
     p->use_tma_store = 0;
     if ((reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 3) == 0) {
         auto enc = get_encode();

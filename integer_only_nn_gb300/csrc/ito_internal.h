@@ -74,6 +74,8 @@ struct GemmPlan {
     int M, N, K, bn, chunk_kb;
     int splits, kb_per_split;     // split-K: slices of kb_per_split K blocks (splits == 1: none)
     int32_t* split_ws;            // [splits][M][ldc] int32 partials
+    CUtensorMap mapS;             // split-K: the partials as a 3-D tensor [splits][M][N] (TMA stores)
+    int split_tma;
     int64_t split_stride;
     bool a_mn, b_mn;
     int32_t* C;
