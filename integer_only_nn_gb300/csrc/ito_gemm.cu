@@ -811,61 +811,53 @@ int num_sms()
 // C[r][c] = sum over slices of P[s][r][c]; max |C| folded into *d_max. Integer
 // addition wraps modulo 2^32, so the slice order cannot change a result that fits int32.
 // C = the sum of the `splits` partial results (exact: integer addition modulo 2^32);
-// max |C| folded into *d_max. Four consecutive columns a thread when the rows allow
-// 16-byte loads, eight slices' loads in flight.
+// max |C| folded into *d_max. A warp per group of outputs (four consecutive columns
+// when the rows allow 16-byte loads, else one): its lanes load different slices, so
+// every load of a group is in flight at once, and a shuffle tree adds the lanes'
+// sums. Contractions split many ways over few outputs (a conv weight gradient: 147
+// slices of 64 x 27 outputs) keep the whole grid busy this way.
 __global__ void k_splitk_reduce(const int32_t* __restrict__ P, int splits, int64_t stride, int M, int N, int64_t ldc,
                                 int32_t* __restrict__ C, uint32_t* __restrict__ d_max, int vec)
 {
     griddep_wait();
     griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int gpr = vec ? N >> 2 : N;   // groups per row
+    const int64_t groups = (int64_t)M * gpr;
     uint32_t mx = 0;
-    if (vec) {
-        const int gpr = N >> 2;
-        const int64_t n = (int64_t)M * gpr;
-        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-            const int64_t r = i / gpr;
-            const int64_t off = r * ldc + ((i - r * gpr) << 2);
+    for (int64_t g = warp0; g < groups; g += nwarps) {
+        const int64_t r = g / gpr;
+        const int64_t off = r * ldc + (g - r * gpr) * (vec ? 4 : 1);
+        if (vec) {
             int4 acc = make_int4(0, 0, 0, 0);
-            int s = 0;
-            for (; s + 8 <= splits; s += 8) {
-                int4 v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) v[u] = __ldcs(reinterpret_cast<const int4*>(P + (s + u) * stride + off));
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    acc.x += v[u].x;
-                    acc.y += v[u].y;
-                    acc.z += v[u].z;
-                    acc.w += v[u].w;
-                }
-            }
-            for (; s < splits; ++s) {
-                const int4 v = __ldcs(reinterpret_cast<const int4*>(P + s * stride + off));
+            for (int sl = lane; sl < splits; sl += 32) {
+                const int4 v = __ldcs(reinterpret_cast<const int4*>(P + sl * stride + off));
                 acc.x += v.x;
                 acc.y += v.y;
                 acc.z += v.z;
                 acc.w += v.w;
             }
-            *reinterpret_cast<int4*>(C + off) = acc;
-            mx = max(max(max(mx, abs_u32(acc.x)), abs_u32(acc.y)), max(abs_u32(acc.z), abs_u32(acc.w)));
-        }
-    } else {
-        const int64_t n = (int64_t)M * N;
-        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-            const int64_t r = i / N, c = i - r * N;
-            const int64_t off = r * ldc + c;
-            int32_t acc = 0;
-            int s = 0;
-            for (; s + 8 <= splits; s += 8) {
-                int32_t v[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) v[u] = __ldcs(P + (s + u) * stride + off);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) acc += v[u];
+            for (int o = 16; o > 0; o >>= 1) {
+                acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+                acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+                acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+                acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
             }
-            for (; s < splits; ++s) acc += __ldcs(P + s * stride + off);
-            C[off] = acc;
-            mx = max(mx, abs_u32(acc));
+            if (lane == 0) {
+                *reinterpret_cast<int4*>(C + off) = acc;
+                mx = max(max(max(mx, abs_u32(acc.x)), abs_u32(acc.y)), max(abs_u32(acc.z), abs_u32(acc.w)));
+            }
+        } else {
+            int32_t acc = 0;
+            for (int sl = lane; sl < splits; sl += 32) acc += __ldcs(P + sl * stride + off);
+            acc = __reduce_add_sync(0xffffffffu, acc);
+            if (lane == 0) {
+                C[off] = acc;
+                mx = max(mx, abs_u32(acc));
+            }
         }
     }
     block_atomic_max(d_max, mx);
@@ -934,7 +926,7 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
         const int vec = p.N % 4 == 0 && p.ldc % 4 == 0 && p.split_stride % 4 == 0 &&
                         (reinterpret_cast<uintptr_t>(p.split_ws) & 15) == 0 &&
                         (reinterpret_cast<uintptr_t>(p.C) & 15) == 0;
-        launch_pdl(k_splitk_reduce, launch_grid_blocks((int64_t)p.M * p.N / (vec ? 4 : 1), 256), 256, 0, s,
+        launch_pdl(k_splitk_reduce, launch_grid_blocks((int64_t)p.M * p.N / (vec ? 4 : 1) * 32, 256), 256, 0, s,
                    p.split_ws, p.splits, p.split_stride, p.M, p.N, p.ldc, p.C, p.d_max, vec);
         e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "split-K reduce launch: %s", cudaGetErrorString(e));
