@@ -703,7 +703,9 @@ struct Dfp4Cfg {
     static constexpr int B_PLANE = BN * BK * 2;             // 16 KB: one limb plane of the tile's B
     static constexpr int STAGE_BYTES = 2 * A_PLANE + B_PLANE;
     static constexpr int STAGES = 4;
-    static constexpr int EPI_WARPS = 8;
+    // 16 epilogue warps, each 32 TMEM lanes x 32 columns of the four accumulators: the
+    // drain, which the next chunk's MMAs wait for, is spread over twice the warps
+    static constexpr int EPI_WARPS = 16;
     static constexpr int THREADS = 64 + EPI_WARPS * 32;
     static constexpr int TMEM_COLS = 512;                   // hh, hl, lh, ll at +0, +128, +256, +384
     static constexpr int CHUNK_KB = 1024 / BK;              // exact chunk: 1024 K terms
@@ -719,7 +721,7 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
 {
     using Cfg = Dfp4Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
-    constexpr int HALF = BN / 2;                          // 64 columns per epilogue warp
+    constexpr int COLS = BN / (Cfg::EPI_WARPS / 4);       // 32 output columns per epilogue warp
     constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, 2 * BN, A_MN, B_MN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -847,15 +849,15 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
     } else {
         // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile
         const int e = warp - 2;
-        const int quad = warp & 3;
-        const int half = e >> 2;
+        const int quad = warp & 3;            // TMEM lanes this warp may access
+        const int cg = e >> 2;                // which 32-column group of the tile
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int t = cluster; ok && t < num_tiles; t += nclusters) {
-            int64_t acc[HALF];
+            int64_t acc[COLS];
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) acc[i] = 0;
-            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * HALF);
+            for (int i = 0; i < COLS; ++i) acc[i] = 0;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cg * COLS);
             for (int c = 0; c < num_chunks; ++c) {
                 if (!mbar_wait(accf_bar, acc_phase, abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
@@ -864,7 +866,7 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
                 for (int part = 0; part < 4; ++part) {
                     const int32_t scale = part == 0 ? 65536 : (part == 3 ? 1 : 256);
 #pragma unroll
-                    for (int j = 0; j < HALF / 16; ++j) {
+                    for (int j = 0; j < COLS / 16; ++j) {
                         uint32_t r[16];
                         tmem_ld16(taddr + part * BN + j * 16, r);
                         tmem_ld_wait();
@@ -881,7 +883,7 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
             if (!ok) break;
             unsigned long long mx = 0;
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) {
+            for (int i = 0; i < COLS; ++i) {
                 const unsigned long long a = (unsigned long long)(acc[i] < 0 ? -acc[i] : acc[i]);
                 mx = a > mx ? a : mx;
             }
@@ -891,18 +893,18 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
                 mx = v > mx ? v : mx;
             }
             if (lane == 0 && mx != 0) atomicMax(d_max, mx);
-            // the int64 result from registers: 64 consecutive values per row
+            // the int64 result from registers: 32 consecutive values per row
             const int row = (t / num_n) * 2 * BM + (int)rank * BM + quad * 32 + lane;
-            const int col0 = (t % num_n) * BN + half * HALF;
+            const int col0 = (t % num_n) * BN + cg * COLS;
             if (row < M) {
                 int64_t* dst = C + (int64_t)row * ldc + col0;
-                if (col0 + HALF <= N && (ldc & 1) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
+                if (col0 + COLS <= N && (ldc & 1) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
 #pragma unroll
-                    for (int i = 0; i < HALF; i += 2)
+                    for (int i = 0; i < COLS; i += 2)
                         *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(acc[i], acc[i + 1]);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < HALF; ++i)
+                    for (int i = 0; i < COLS; ++i)
                         if (col0 + i < N) dst[i] = acc[i];
                 }
             }
