@@ -709,15 +709,20 @@ struct Dfp4Cfg {
     static constexpr int THREADS = 64 + EPI_WARPS * 32;
     static constexpr int TMEM_COLS = 512;                   // hh, hl, lh, ll at +0, +128, +256, +384
     static constexpr int CHUNK_KB = 1024 / BK;              // exact chunk: 1024 K terms
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    // one 32-row x 8-column int64 store box per epilogue warp: the result leaves by TMA
+    static constexpr int STAGING_BYTES = EPI_WARPS * 32 * 8 * 8;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
 };
+static_assert(Dfp4Cfg::SMEM_BYTES <= 227 * 1024, "wide-tile kernel: shared memory above the per-CTA limit");
+// a CTA's last tile stages each warp's whole 32 x 32 block in the (then idle) pipeline stages
+static_assert(Dfp4Cfg::EPI_WARPS * 32 * 32 * 8 <= Dfp4Cfg::STAGES * Dfp4Cfg::STAGE_BYTES, "stages too small");
 
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
     k_gemm_dfp4(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
-                const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, int M, int N,
-                int K, int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max,
-                int* __restrict__ err)
+                const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
+                const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K,
+                int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, int* __restrict__ err)
 {
     using Cfg = Dfp4Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -726,7 +731,8 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint8_t* staging = smem + STAGES * Cfg::STAGE_BYTES;     // 1024-aligned
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
     uint64_t* empty_bar = full_bar + STAGES;
     uint64_t* accf_bar = empty_bar + STAGES;   // the chunk's accumulators are complete
     uint64_t* acce_bar = accf_bar + 1;         // they have been drained (both CTAs)
@@ -894,9 +900,39 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
             }
             if (lane == 0 && mx != 0) atomicMax(d_max, mx);
             // the int64 result from registers: 32 consecutive values per row
-            const int row = (t / num_n) * 2 * BM + (int)rank * BM + quad * 32 + lane;
+            const int row0 = (t / num_n) * 2 * BM + (int)rank * BM + quad * 32;
+            const int row = row0 + lane;
             const int col0 = (t % num_n) * BN + cg * COLS;
-            if (row < M) {
+            if (use_tma_store) {
+                // 32 x 8 boxes (row-major, 64 bytes a row) written out by TMA, the edges clipped.
+                // Before the CTA's last tile they go one at a time through this warp's 2 KB
+                // slot; for the last tile (every MMA done, no load left) the warp stages its
+                // whole block in the pipeline stages and issues the four stores at once.
+                const bool last = t + nclusters >= num_tiles;
+                uint8_t* stg = last ? smem + e * (32 * COLS * 8) : staging + e * (32 * 8 * 8);
+#pragma unroll
+                for (int g = 0; g < COLS / 8; ++g) {
+                    uint8_t* box = last ? stg + g * (32 * 8 * 8) : stg;
+                    if (!last) {
+                        if (lane == 0) bulk_wait_read_all();   // the slot's previous box has been read
+                        __syncwarp();
+                    }
+                    const uint32_t srow = smem_u32(box) + lane * 64;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int64_t v0 = acc[g * 8 + 2 * j], v1 = acc[g * 8 + 2 * j + 1];
+                        st_shared_v4(srow + j * 16, (int32_t)v0, (int32_t)(v0 >> 32), (int32_t)v1,
+                                     (int32_t)(v1 >> 32));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (row0 < M && col0 + g * 8 < N) tma_store_2d(&tmC, box, col0 + g * 8, row0);
+                        if (!last) bulk_commit();
+                    }
+                }
+                if (last && lane == 0) bulk_commit();
+            } else if (row < M) {
                 int64_t* dst = C + (int64_t)row * ldc + col0;
                 if (col0 + COLS <= N && (ldc & 1) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
 #pragma unroll
@@ -909,6 +945,7 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -960,8 +997,8 @@ static int launch_dfp4(const DfpGemmPlan& p, cudaStream_t s)
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh3, p.mapBl3, p.M, p.N, p.K, p.C, p.ldc,
-                                       p.d_max, p.err);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh3, p.mapBl3, p.mapC8, p.use_tma_store8,
+                                       p.M, p.N, p.K, p.C, p.ldc, p.d_max, p.err);
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp wide gemm launch: %s", cudaGetErrorString(e));
 }
 
@@ -1164,6 +1201,12 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (P) failed (%d)", (int)cr);
         p->use_tma_store = 1;
+        // the wide-tile kernel's 32 x 8 boxes, unswizzled
+        cuuint32_t box8[2] = {8, 32};
+        cr = enc(&p->mapC8, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, C, dims, strides, box8, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (P, 8) failed (%d)", (int)cr);
+        p->use_tma_store8 = 1;
     }
     return ITO_OK;
 }

@@ -93,7 +93,7 @@ struct ito_dfp16_model {
     int64_t* tail_ws = nullptr;        // partial tiles of split last waves (shared by the step's contractions)
     size_t tail_ws_bytes = 0;
     // backward overlap: down-conversions of the propagated delta and of the weight gradient,
-    // and the update, run on a second stream beside the next contraction (ITO_OVERLAP=0: off)
+    // and the update, run on a second stream beside the next contraction
     bool overlap = true;
     cudaStream_t side = nullptr;
     std::vector<cudaEvent_t> sync_ev;  // [0] fork, [1] join, per layer: delta propagated, delta ready, wgrad done

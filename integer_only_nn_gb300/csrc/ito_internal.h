@@ -104,6 +104,8 @@ int make_map_bf16(CUtensorMap* map, const Bf16View& v, int box_rows);
 struct DfpGemmPlan {
     CUtensorMap mapAh, mapAl, mapBh, mapBl, mapC;
     int use_tma_store;
+    CUtensorMap mapC8;            // the wide-tile kernel's result boxes (32 rows x 8 int64)
+    int use_tma_store8;
     int M, N, K;
     int chunk_kb;                 // K blocks of 64 per exact chunk
     int pair;                     // CTA-pair kernel (256 x 64 tiles)

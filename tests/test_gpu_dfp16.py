@@ -93,6 +93,29 @@ def test_dfp_pair_fwd_dgrad_wgrad(ito, B, IC, OC):
     assert ito.ito_get_error() == 0
 
 
+# The wide-tile kernel's result leaves through shared memory and TMA in 32 x 8 boxes, one
+# at a time before a pair's last tile and all at once (staged in the idle pipeline
+# stages) for it: a partial last wave, several tiles per pair, ragged M, N and K (boxes
+# clipped at both edges), each contraction twice in a row
+WIDE_SHAPES = [(1100, 1000, 2000), (2048, 1000, 1100), (2048, 2048, 2048), (512, 2048, 2048), (777, 3000, 1500)]
+
+
+@pytest.mark.parametrize("B,IC,OC", WIDE_SHAPES)
+def test_dfp_pair_wide_tile_stores(ito, B, IC, OC):
+    x, W = i16((B, IC)), i16((OC, IC))
+    e = i16((B, OC))
+    for _ in range(2):
+        p64, mx, _, _, _ = ito.ito_dfp16_linear_fwd(_dev(x), ito._i32dev(-12), _dev(W), ito._i32dev(-17))
+        P = O.dfp_linear_fwd(x, W)
+        assert np.array_equal(_h(p64), P)
+        assert int(_h(mx)[0]) == int(np.abs(P).max())
+    p64, _, _, _, _ = ito.ito_dfp16_linear_bwd_delta(_dev(e), ito._i32dev(-20), _dev(W), ito._i32dev(-17))
+    assert np.array_equal(_h(p64), O.dfp_linear_dgrad(e, W))
+    p64, _, _, _, _ = ito.ito_dfp16_linear_wgrad(_dev(e), ito._i32dev(-20), _dev(x), ito._i32dev(-12))
+    assert np.array_equal(_h(p64), O.dfp_linear_wgrad(e, x))
+    assert ito.ito_get_error() == 0
+
+
 @pytest.mark.parametrize("OC", [70, 200])      # both pair kernels
 def test_dfp_pair_extreme_chunks(ito, OC):
     """256+ rows, all products (-32767)^2: each of the pair kernels' limb
