@@ -685,29 +685,30 @@ __global__ void __launch_bounds__(Dfp2Cfg::THREADS, 1)
 
 // ------------------------------------------- wide-tile CTA-pair kernel
 //
-// The exact contraction on a CTA pair with 256 x 128 output tiles: each CTA
-// loads both limb planes of its 128 rows of A and ONE limb plane of the tile's
-// 128 columns of B (the leader the high plane, the other CTA the low plane),
-// so the pair's B operand [B_hi | B_lo] (N = 256) is split between the two
-// CTAs as an M = 256 MMA reads it. Two MMAs per 16-term K step:
-// A_hi x [B_hi | B_lo] into [hh | hl] and A_lo x [B_hi | B_lo] into [lh | ll],
-// four 128-column fp32 accumulators that fill the 512 tensor-memory columns
-// (one buffer: the MMAs of the next chunk wait for the drain). Against the
-// 64-column tile this halves the A bytes per operation moved into and read
-// from shared memory. Each accumulator gets one limb product (at most 2^14) per
-// K term, so an exact chunk is 1024 terms; after a chunk the epilogue adds
-// 65536 hh + 256 (hl + lh) + ll into the tile's int64 sums in registers.
+// The exact contraction on a CTA pair with 256 x bn output tiles (bn = 128, or
+// 112 where that fills the last wave better): each CTA loads both limb planes of
+// its 128 rows of A and ONE limb plane of the tile's bn columns of B (the leader
+// the high plane, the other CTA the low plane), so the pair's B operand
+// [B_hi | B_lo] (N = 2 bn) is split between the two CTAs as an M = 256 MMA reads
+// it. Two MMAs per 16-term K step: A_hi x [B_hi | B_lo] into [hh | hl] at tensor-
+// memory column 0 and A_lo x [B_hi | B_lo] into [lh | ll] at column 256, four
+// bn-column fp32 accumulators in the 512 tensor-memory columns (one buffer: the
+// MMAs of the next chunk wait for the drain). Against the 64-column tile this
+// halves the A bytes per operation moved into and read from shared memory. Each
+// accumulator gets one limb product (at most 2^14) per K term, so an exact chunk
+// is 1024 terms; after a chunk the epilogue adds 65536 hh + 256 (hl + lh) + ll
+// into the tile's int64 sums in registers.
 struct Dfp4Cfg {
-    static constexpr int BM = 128, BN = 128, BK = 64;      // BM rows per CTA (256 per pair), BN columns
+    static constexpr int BM = 128, BN = 128, BK = 64;      // BM rows per CTA (256 per pair), BN columns at most
     static constexpr int A_PLANE = BM * BK * 2;             // 16 KB
-    static constexpr int B_PLANE = BN * BK * 2;             // 16 KB: one limb plane of the tile's B
+    static constexpr int B_PLANE = BN * BK * 2;             // 16 KB: one limb plane of B (BN columns loaded)
     static constexpr int STAGE_BYTES = 2 * A_PLANE + B_PLANE;
     static constexpr int STAGES = 4;
     // 16 epilogue warps, each 32 TMEM lanes x 32 columns of the four accumulators: the
     // drain, which the next chunk's MMAs wait for, is spread over twice the warps
     static constexpr int EPI_WARPS = 16;
     static constexpr int THREADS = 64 + EPI_WARPS * 32;
-    static constexpr int TMEM_COLS = 512;                   // hh, hl, lh, ll at +0, +128, +256, +384
+    static constexpr int TMEM_COLS = 512;                   // hh, hl, lh, ll at +0, +bn, +256, +256 + bn
     static constexpr int CHUNK_KB = 1024 / BK;              // exact chunk: 1024 K terms
     // one 32-row x 8-column int64 store box per epilogue warp: the result leaves by TMA
     static constexpr int STAGING_BYTES = EPI_WARPS * 32 * 8 * 8;
@@ -721,13 +722,13 @@ template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
     k_gemm_dfp4(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                 const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
-                const __grid_constant__ CUtensorMap tmC, int use_tma_store, int M, int N, int K,
+                const __grid_constant__ CUtensorMap tmC, int use_tma_store, int bn, int M, int N, int K,
                 int64_t* __restrict__ C, int64_t ldc, unsigned long long* __restrict__ d_max, int* __restrict__ err)
 {
     using Cfg = Dfp4Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
-    constexpr int COLS = BN / (Cfg::EPI_WARPS / 4);       // 32 output columns per epilogue warp
-    constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, 2 * BN, A_MN, B_MN);
+    constexpr int COLS = BN / (Cfg::EPI_WARPS / 4);       // 32 output columns per epilogue warp (fewer past bn)
+    const uint32_t idesc = idesc_bf16_f32(2 * BM, 2 * bn, A_MN, B_MN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -744,7 +745,7 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-    const int num_m = (M + 2 * BM - 1) / (2 * BM), num_n = (N + BN - 1) / BN;
+    const int num_m = (M + 2 * BM - 1) / (2 * BM), num_n = (N + bn - 1) / bn;
     const int num_tiles = num_m * num_n;
     const int num_kb = (K + BK - 1) / BK;
     const int num_chunks = (num_kb + Cfg::CHUNK_KB - 1) / Cfg::CHUNK_KB;
@@ -783,7 +784,7 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int t = cluster; ok && t < num_tiles; t += nclusters) {
-                const int rowA = (t / num_n) * 2 * BM + (int)rank * BM, colB = (t % num_n) * BN;
+                const int rowA = (t / num_n) * 2 * BM + (int)rank * BM, colB = (t % num_n) * bn;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, err)) { ok = false; break; }
                     if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
@@ -818,7 +819,7 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             const uint32_t d_hi = tmem_base;               // [hh | hl]
-            const uint32_t d_lo = tmem_base + 2 * BN;      // [lh | ll]
+            const uint32_t d_lo = tmem_base + 256;         // [lh | ll]
             for (int t = cluster; ok && t < num_tiles; t += nclusters) {
                 for (int c = 0; ok && c < num_chunks; ++c) {
                     if (!mbar_wait(acce_bar, acc_phase ^ 1, abort_flag, err)) { ok = false; break; }
@@ -840,8 +841,8 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
                             const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
                                                      : smem_desc_sw128(b0 + k * 32, 16, 1024);
                             const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-                            tc_mma_bf16_pair(d_hi, ah, bd, IDESC, acc);
-                            tc_mma_bf16_pair(d_lo, al, bd, IDESC, acc);
+                            tc_mma_bf16_pair(d_hi, ah, bd, idesc, acc);
+                            tc_mma_bf16_pair(d_lo, al, bd, idesc, acc);
                         }
                         tc_commit_pair_mc(&empty_bar[stage], 0x3);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -857,6 +858,7 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
         const int e = warp - 2;
         const int quad = warp & 3;            // TMEM lanes this warp may access
         const int cg = e >> 2;                // which 32-column group of the tile
+        const int valid = min(COLS, bn - cg * COLS);   // its columns inside the tile (16 or 32)
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int t = cluster; ok && t < num_tiles; t += nclusters) {
@@ -871,10 +873,13 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
 #pragma unroll 1
                 for (int part = 0; part < 4; ++part) {
                     const int32_t scale = part == 0 ? 65536 : (part == 3 ? 1 : 256);
+                    const uint32_t poff = (uint32_t)((part & 1) * bn + (part >> 1) * 256);
 #pragma unroll
                     for (int j = 0; j < COLS / 16; ++j) {
+                        // past the tile's bn columns this reads unused accumulator columns;
+                        // those sums are neither stored nor counted in the max
                         uint32_t r[16];
-                        tmem_ld16(taddr + part * BN + j * 16, r);
+                        tmem_ld16(taddr + poff + j * 16, r);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
@@ -887,11 +892,17 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
                 acc_phase ^= 1;
             }
             if (!ok) break;
+            // the int64 result from registers: 32 consecutive values per row (the last 16
+            // outside the tile when the warp's group has only 16 columns)
+            const int row0 = (t / num_n) * 2 * BM + (int)rank * BM + quad * 32;
+            const int row = row0 + lane;
+            const int col0 = (t % num_n) * bn + cg * COLS;
+            const int ncols = min(valid, N - col0);   // columns of this warp's block inside C (may be <= 0)
             unsigned long long mx = 0;
 #pragma unroll
             for (int i = 0; i < COLS; ++i) {
                 const unsigned long long a = (unsigned long long)(acc[i] < 0 ? -acc[i] : acc[i]);
-                mx = a > mx ? a : mx;
+                if (i < 16 || valid == COLS) mx = a > mx ? a : mx;
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -899,10 +910,6 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
                 mx = v > mx ? v : mx;
             }
             if (lane == 0 && mx != 0) atomicMax(d_max, mx);
-            // the int64 result from registers: 32 consecutive values per row
-            const int row0 = (t / num_n) * 2 * BM + (int)rank * BM + quad * 32;
-            const int row = row0 + lane;
-            const int col0 = (t % num_n) * BN + cg * COLS;
             if (use_tma_store) {
                 // 32 x 8 boxes (row-major, 64 bytes a row) written out by TMA, the edges clipped.
                 // Before the CTA's last tile they go one at a time through this warp's 2 KB
@@ -927,21 +934,21 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (row0 < M && col0 + g * 8 < N) tma_store_2d(&tmC, box, col0 + g * 8, row0);
+                        if (row0 < M && g * 8 < ncols) tma_store_2d(&tmC, box, col0 + g * 8, row0);
                         if (!last) bulk_commit();
                     }
                 }
                 if (last && lane == 0) bulk_commit();
             } else if (row < M) {
                 int64_t* dst = C + (int64_t)row * ldc + col0;
-                if (col0 + COLS <= N && (ldc & 1) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
+                if (ncols == COLS && (ldc & 1) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
 #pragma unroll
                     for (int i = 0; i < COLS; i += 2)
                         *reinterpret_cast<longlong2*>(dst + i) = make_longlong2(acc[i], acc[i + 1]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < COLS; ++i)
-                        if (col0 + i < N) dst[i] = acc[i];
+                        if (i < ncols) dst[i] = acc[i];
                 }
             }
         }
@@ -956,15 +963,19 @@ __global__ void __launch_bounds__(Dfp4Cfg::THREADS, 1)
     }
 }
 
-template <bool A_MN, bool B_MN>
-static int launch_dfp4(const DfpGemmPlan& p, cudaStream_t s)
+// CTA pairs of k_gemm_dfp4 resident at once (all operand layouts share one occupancy);
+// the first call also raises every instance's shared-memory limit. 0 on failure.
+static int dfp4_clusters()
 {
     using Cfg = Dfp4Cfg;
-    auto kern = k_gemm_dfp4<A_MN, B_MN>;
-    static int max_clusters = 0;
-    if (!max_clusters) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
-            return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
+    static int n = 0;
+    if (!n) {
+        void (*kerns[4])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, int, int, int, int, int,
+                         int64_t*, int64_t, unsigned long long*, int*) = {
+            k_gemm_dfp4<false, false>, k_gemm_dfp4<false, true>, k_gemm_dfp4<true, false>, k_gemm_dfp4<true, true>};
+        for (auto k : kerns)
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+                return 0;
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(2 * num_sms());
         q.blockDim = dim3(Cfg::THREADS);
@@ -976,12 +987,33 @@ static int launch_dfp4(const DfpGemmPlan& p, cudaStream_t s)
         qa[0].val.clusterDim.z = 1;
         q.attrs = qa;
         q.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1)
-            return set_error(ITO_ERR_CUDA, "no CTA pair fits on this device");
-        max_clusters = n;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, k_gemm_dfp4<false, false>, &q) != cudaSuccess || c < 1) return 0;
+        n = c;
     }
-    const int tiles = ((p.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((p.N + Cfg::BN - 1) / Cfg::BN);
+    return n;
+}
+
+// Tile width of the wide-tile kernel: 112 columns instead of 128 when the tiles then
+// fill their waves enough better (waves x width at least 5% smaller; e.g. a 2048 x 2048
+// output on 76 pairs: 152 tiles of 112 columns in two full waves, against 128 tiles of
+// 128 columns whose second wave leaves 24 pairs idle).
+static int dfp4_width(int M, int N, int clusters)
+{
+    if (clusters < 1) return 128;
+    const int num_m = (M + 255) / 256;
+    auto cost = [&](int bn) { return (double)((num_m * ((N + bn - 1) / bn) + clusters - 1) / clusters) * bn; };
+    return cost(112) < 0.95 * cost(128) ? 112 : 128;
+}
+
+template <bool A_MN, bool B_MN>
+static int launch_dfp4(const DfpGemmPlan& p, cudaStream_t s)
+{
+    using Cfg = Dfp4Cfg;
+    auto kern = k_gemm_dfp4<A_MN, B_MN>;
+    const int max_clusters = dfp4_clusters();
+    if (max_clusters < 1) return set_error(ITO_ERR_CUDA, "no CTA pair of the wide-tile kernel fits on this device");
+    const int tiles = ((p.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((p.N + p.bn4 - 1) / p.bn4);
     const int clusters = tiles < max_clusters ? tiles : max_clusters;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
@@ -998,7 +1030,7 @@ static int launch_dfp4(const DfpGemmPlan& p, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p.mapAh, p.mapAl, p.mapBh3, p.mapBl3, p.mapC8, p.use_tma_store8,
-                                       p.M, p.N, p.K, p.C, p.ldc, p.d_max, p.err);
+                                       p.bn4, p.M, p.N, p.K, p.C, p.ldc, p.d_max, p.err);
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp wide gemm launch: %s", cudaGetErrorString(e));
 }
 
@@ -1145,7 +1177,7 @@ static int launch_dfp(const DfpGemmPlan& p, cudaStream_t s)
 
 int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a_mn, const Bf16View& Bh,
                   const Bf16View& Bl, bool b_mn, int M, int N, int K, int64_t* C, int64_t ldc,
-                  unsigned long long* d_max, int64_t* tail_ws, size_t tail_ws_bytes)
+                  unsigned long long* d_max, int64_t* tail_ws, size_t tail_ws_bytes, bool fill_waves)
 {
     if (M < 1 || N < 1 || K < 1) return set_error(ITO_ERR_SHAPE, "dfp gemm: empty contraction");
     if (K > (1 << 20)) return set_error(ITO_ERR_SHAPE, "dfp gemm: contraction longer than 2^20");
@@ -1174,6 +1206,7 @@ int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a
     // else the 256 x 64 one (which splits a partial last wave along K when given room)
     p->pair = M >= 256 && C != nullptr;
     p->stacked = p->pair && N >= 128;
+    p->bn4 = p->stacked && fill_waves ? dfp4_width(M, N, dfp4_clusters()) : 128;
     if (p->stacked &&
         ((r = make_map_bf16(&p->mapBh3, Bh, b_mn ? 64 : 128)) || (r = make_map_bf16(&p->mapBl3, Bl, b_mn ? 64 : 128))))
         return r;

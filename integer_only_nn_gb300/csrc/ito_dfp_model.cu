@@ -501,11 +501,14 @@ static int dfp_build(ito_dfp16_model* m, const int32_t* dims, int nl)
         }
         ITO_TRY(dfp_gemm_plan(&L.pf, ih, il, false, wh, wl, false, B, L.OC, L.IC, L.p64, L.OC, m->u64(l, D_PMAX),
                               m->tail_ws, m->tail_ws_bytes));
+        // the backward contractions run beside down-conversions and updates on the side
+        // stream (when the overlap is on), which take the SMs of a partial last wave
+        const bool fill = !m->overlap;
         if (l > 0)
             ITO_TRY(dfp_gemm_plan(&L.pd, eh, el, false, wh, wl, true, B, L.IC, L.OC, L.pd64, L.IC, m->u64(l, D_PDMAX),
-                                  m->tail_ws, m->tail_ws_bytes));
+                                  m->tail_ws, m->tail_ws_bytes, fill));
         ITO_TRY(dfp_gemm_plan(&L.pg, eh, el, true, ih, il, true, L.OC, L.IC, B, L.pg64, L.IC, m->u64(l, D_PGMAX),
-                              m->tail_ws, m->tail_ws_bytes));
+                              m->tail_ws, m->tail_ws_bytes, fill));
     }
     launch_pdl(k_set_i32, 1, 1, 0, 0, m->ew(), m->exp_w);
     if (cudaMemcpy(m->wexp_d, m->wexp.data(), sizeof(int32_t) * nl, cudaMemcpyHostToDevice) != cudaSuccess)

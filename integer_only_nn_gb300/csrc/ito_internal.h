@@ -109,7 +109,8 @@ struct DfpGemmPlan {
     int M, N, K;
     int chunk_kb;                 // K blocks of 64 per exact chunk
     int pair;                     // CTA-pair kernel (256 x 64 tiles)
-    int stacked;                  // wide-tile CTA-pair kernel (256 x 128 tiles; see k_gemm_dfp4)
+    int stacked;                  // wide-tile CTA-pair kernel (256 x bn4 tiles; see k_gemm_dfp4)
+    int bn4;                      // its tile width: 128 or 112
     CUtensorMap mapBh3, mapBl3;   // its B maps (128-row boxes when B is K-major)
     int tail_full, tail_parts;    // pair kernel: whole tiles, K pieces per remaining tile (1: no split)
     int64_t* tail_ws;             // [pieces][256][64] int64 partials of the split tiles
@@ -133,9 +134,13 @@ struct DfpGemmPlan {
 
 // tail_ws (optional): room for the int64 partial tiles of a split last wave
 // (dfp_split_ws_bytes); without it the pair kernel runs every tile whole.
+// fill_waves: the wide-tile kernel may narrow its tiles to 112 columns so that they fill
+// the last wave; false keeps 128 (a contraction with work of another stream beside it
+// leaves that work the SMs of its partial last wave).
 int dfp_gemm_plan(DfpGemmPlan* p, const Bf16View& Ah, const Bf16View& Al, bool a_mn, const Bf16View& Bh,
                   const Bf16View& Bl, bool b_mn, int M, int N, int K, int64_t* C, int64_t ldc,
-                  unsigned long long* d_max, int64_t* tail_ws = nullptr, size_t tail_ws_bytes = 0);
+                  unsigned long long* d_max, int64_t* tail_ws = nullptr, size_t tail_ws_bytes = 0,
+                  bool fill_waves = true);
 size_t dfp_split_ws_bytes(int M, int N, int K);
 // Chained FP32 partial accumulation (forward, both operands K-major): chains of `chain` K
 // terms (64..512, a multiple of 64), each wrapped to int32, converted to float, scaled by
