@@ -294,6 +294,15 @@ int ito_conv2d_bwd_delta(const int8_t* delta, const int8_t* Wt, const int8_t* a_
     ITO_TRY(launch_i8_to_bf16(delta, g.rows_out, OC, eb, g.lde, s));
     ITO_TRY(launch_i8_to_bf16(Wt, OC, g.K, Wb, g.ldp, s));
     ITO_TRY(cuda_ok(cudaMemsetAsync(d_max, 0, sizeof(uint32_t), s), "memset"));
+    if (conv_dgrad_s2_eligible(B, H, W, IC, OC, stride)) {
+        // stride 2: each parity phase of the input-space delta is its own contraction, written
+        // straight into d32 with its max
+        ConvS2Plan sp;
+        ITO_TRY(conv_dgrad_s2_plan(&sp, eb, g.lde, Wb, g.ldp, B, H, W, IC, OC, d32, d_max));
+        ITO_TRY(conv_dgrad_s2_run(sp, s));
+        return launch_requant(d32, g.rows_in, IC, d_max, p.target_bits, 0, a_prev, delta_prev, nullptr, 0, d_shift,
+                              s);
+    }
     // patch-space delta Dcol[(b,oh,ow)][k] = sum_oc delta[(b,oh,ow)][oc] W[oc][k]; its max is not
     // the NITI max (col2im takes that), so the contraction folds it into a scratch word
     uint32_t* discard = reinterpret_cast<uint32_t*>(conv_slot(workspace, sz, 5));

@@ -97,6 +97,36 @@ int num_sms();
 // 128-byte swizzle, zero fill outside the view.
 int make_map_bf16(CUtensorMap* map, const Bf16View& v, int box_rows);
 
+// ---- stride-2 convolution delta propagation by parity phases (ito_conv_dgrad.cu)
+
+// Geometry of the phase kernel: output grid B x OH x OW (input H = 2 OH, W = 2 OW),
+// IC input channels in tiles of 64, OC delta channels in blocks of 64; a row tile is
+// ba images x oha output rows x OW columns (128 positions), n_iblk tiles per image column.
+struct S2Geom {
+    int B, OH, OW, IC;
+    int oc_blocks, n_tiles;
+    int oha, ba, n_iblk, m_tiles;
+};
+
+struct ConvS2Plan {
+    CUtensorMap mapE;       // delta's bf16 copy [B][OH][OW][OC], 4-D
+    CUtensorMap mapW;       // weights' bf16 copy [OC][9 IC], MN-major boxes
+    CUtensorMap mapD[4];    // phase (py, px) = (i >> 1, i & 1) of the int32 delta D [B][H][W][IC]
+    S2Geom g;
+    uint32_t* d_max;
+    int* err;
+};
+
+// true when the phase kernel takes this convolution: stride 2, even H and W, OW in
+// {8, 16, 32}, OH a power of two with OH * OW >= 32, IC and OC multiples of 64
+bool conv_dgrad_s2_eligible(int B, int H, int W, int IC, int OC, int stride);
+// D[b][y][x][ic] = sum over the taps reaching (y, x) of E[b][oh][ow][oc] W[oc][kh][kw][ic]
+// for a 3x3, pad-1, stride-2 convolution; E: [B*OH*OW][lde] bf16, W: [OC][ldw] bf16
+// (9 IC used); max |D| folded into *d_max (atomicMax; the caller zeroes it)
+int conv_dgrad_s2_plan(ConvS2Plan* p, const uint16_t* eb, int64_t lde, const uint16_t* Wb, int64_t ldw, int B,
+                       int H, int W, int IC, int OC, int32_t* D, uint32_t* d_max);
+int conv_dgrad_s2_run(const ConvS2Plan& p, cudaStream_t s);
+
 // ---- DFP16 limb contraction (ito_dfp.cu)
 
 // P[M][N] (int64, exact) = sum_k A(m,k) B(n,k) for int16 operands given as two

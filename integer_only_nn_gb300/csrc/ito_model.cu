@@ -64,6 +64,9 @@ struct MLayer {
     // speculative requantisation (see FusedRq): pf / pd with the requantising epilogue, and their
     // re-launches, which check the shift prediction and recompute when it missed
     GemmPlan pf_spec{}, pd_spec{}, pf_redo{}, pd_redo{};
+    // stride-2 conv: the input-space delta by parity phases (no patch-space delta, no gather)
+    bool s2 = false;
+    ConvS2Plan ps2{};
     bool has_dgrad = false;
     bool relu = false;
 };
@@ -367,7 +370,8 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         if (conv) {
             L.ldp = pad8(L.K);
             ITO_TRY(m->alloc(&L.Pb, (size_t)L.rows_out * L.ldp));
-            if (L.has_dgrad) ITO_TRY(m->alloc(&L.dcol, (size_t)L.rows_out * L.K));
+            L.s2 = L.has_dgrad && conv_dgrad_s2_eligible(B, L.H, L.W, L.IC, L.OC, L.stride);
+            if (L.has_dgrad && !L.s2) ITO_TRY(m->alloc(&L.dcol, (size_t)L.rows_out * L.K));
         }
     }
 
@@ -423,8 +427,11 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax, m->split_ws,
                           m->split_ws_bytes, chunk, pair_f));
         // delta propagation: D[m][k] = sum_oc e[m][oc] W[oc][k]; for a conv this is the
-        // patch-space delta, whose max is not the NITI max (col2im takes that)
-        if (L.has_dgrad)
+        // patch-space delta, whose max is not the NITI max (col2im takes that), except for a
+        // stride-2 conv, whose input-space delta comes straight from its parity phases
+        if (L.s2)
+            ITO_TRY(conv_dgrad_s2_plan(&L.ps2, L.eb, L.lde, L.Wb, L.ldw, B, L.H, L.W, L.IC, L.OC, L.d32, dmax));
+        else if (L.has_dgrad)
             ITO_TRY(gemm_plan(&L.pd, ev, false, wv, true, M, (int)L.K, L.OC, conv ? L.dcol : L.d32, L.K,
                               conv ? m->discard_max : dmax, m->split_ws, m->split_ws_bytes, kExactChunk, pair_d));
         // weight gradient: G[oc][k] = sum_m e[m][oc] in[m][k]
@@ -614,14 +621,19 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd_spec), gemm_run(L.pd_spec, s));
             ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pd_redo, s));
         } else if (L.has_dgrad) {
-            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
+            if (L.s2)
+                ITO_LAUNCH(m, s, ITO_PROF_GEMM, 2.0 * L.rows_in * L.IC * 9 * L.OC / 4,
+                           conv_dgrad_s2_run(L.ps2, s));
+            else
+                ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
             const cudaStream_t r = r_side;
             ITO_TRY(sync(m->ev_dgrad(l), s, r));   // the propagated delta is complete
             MLayer& prev = m->L[l - 1];
             if (conv) {
-                ITO_LAUNCH(m, r, ITO_PROF_OTHER, 4.0 * L.rows_out * L.K + 4.0 * L.rows_in * L.IC,
-                           launch_col2im(L.dcol, B, L.H, L.W, L.IC, L.OH, L.OW, L.stride, L.d32,
-                                         m->umax(l, ST_DMAX), r));
+                if (!L.s2)
+                    ITO_LAUNCH(m, r, ITO_PROF_OTHER, 4.0 * L.rows_out * L.K + 4.0 * L.rows_in * L.IC,
+                               launch_col2im(L.dcol, B, L.H, L.W, L.IC, L.OH, L.OW, L.stride, L.d32,
+                                             m->umax(l, ST_DMAX), r));
                 ITO_LAUNCH(m, r, ITO_PROF_REQUANT, requant_bytes(L.rows_in * L.IC, true, true),
                            launch_requant(L.d32, L.rows_in, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
                                           prev.mask ? nullptr : prev.a8, prev.e8, prev.eb, prev.lde,

@@ -78,6 +78,41 @@ def test_conv2d_bwd_delta(ito, B, H, W, IC, OC, stride, gated):
     assert np.array_equal(_host(dp), ep)
 
 
+# Stride-2 shapes taken by the parity-phase delta propagation (even H and W, OW of 8, 16
+# or 32, channels in multiples of 64): a row tile of two images with one or three in
+# the batch, 32 output columns, a 4 x 32 input (four images to a row tile), 512 delta
+# channels (the four-tap phase sums 2048 terms: two exact chunks)
+PHASE = [(1, 16, 16, 64, 64, 2), (3, 16, 16, 128, 64, 2), (2, 64, 64, 64, 64, 2), (2, 4, 32, 64, 128, 2),
+         (2, 16, 16, 64, 512, 2)]
+
+
+@pytest.mark.parametrize("B,H,W,IC,OC,stride", PHASE)
+@pytest.mark.parametrize("gated", [False, True])
+def test_conv2d_bwd_delta_stride2_phases(ito, B, H, W, IC, OC, stride, gated):
+    OH, OW = O.conv_out(H, 3, stride), O.conv_out(W, 3, stride)
+    e, Wt = i8((B, OH, OW, OC)), i8((OC, 3, 3, IC), -127, 127)
+    a_prev = i8((B, H, W, IC), -3, 127) if gated else None
+    d32, mx, sh, dp = ito.ito_conv2d_bwd_delta(_dev(e), _dev(Wt), _dev(a_prev) if gated else None, (H, W), stride)
+    D = O.conv2d_dgrad(e, Wt, (H, W), stride)
+    ep, s, m = O.requant_mask(D, a_prev)
+    assert np.array_equal(_host(d32), D)
+    assert (_u32(mx), int(_host(sh)[0])) == (m, s)
+    assert np.array_equal(_host(dp), ep)
+
+
+def test_conv2d_bwd_delta_stride2_extreme(ito):
+    """Every product (-128)(-127): the interior positions of the four-tap phase sum
+    4 x 512 = 2048 of them, 1024 to an exact chunk."""
+    B, H, W, IC, OC = 2, 16, 16, 64, 512
+    e = np.full((B, 8, 8, OC), -128, np.int8)
+    Wt = np.full((OC, 3, 3, IC), -127, np.int8)
+    d32, mx, _, _ = ito.ito_conv2d_bwd_delta(_dev(e), _dev(Wt), None, (H, W), 2)
+    D = O.conv2d_dgrad(e, Wt, (H, W), 2)
+    assert int(D.max()) == 4 * OC * 128 * 127
+    assert np.array_equal(_host(d32), D)
+    assert _u32(mx) == int(np.abs(D).max())
+
+
 @pytest.mark.parametrize("B,H,W,IC,OC,stride", FULL + RAGGED)
 def test_conv2d_wgrad(ito, B, H, W, IC, OC, stride):
     OH, OW = O.conv_out(H, 3, stride), O.conv_out(W, 3, stride)
