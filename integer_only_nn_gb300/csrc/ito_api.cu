@@ -67,13 +67,21 @@ static int cuda_ok(cudaError_t e, const char* what)
 // Geometry of a 3x3, pad-1 conv over NHWC input [B][H][W][IC] with weights
 // [OC][3][3][IC]: a Linear layer over the im2col patch matrix [rows_out][K].
 struct ConvGeom {
+    int B, H, W, IC, stride;
     int OH, OW;
     int64_t rows_in, rows_out, K, ldp, lde;
+    bool s2;   // stride 2 on parity planes (no patches; see ito_conv_tc.cu)
 };
 
 static ConvGeom conv_geom(int B, int H, int W, int IC, int OC, int stride)
 {
     ConvGeom g;
+    g.B = B;
+    g.H = H;
+    g.W = W;
+    g.IC = IC;
+    g.stride = stride;
+    g.s2 = conv_dgrad_s2_eligible(B, H, W, IC, OC, stride);
     g.OH = (H - 1) / stride + 1;
     g.OW = (W - 1) / stride + 1;
     g.rows_in = (int64_t)B * H * W;
@@ -84,7 +92,8 @@ static ConvGeom conv_geom(int B, int H, int W, int IC, int OC, int stride)
     return g;
 }
 
-// Workspace slots: 0 bf16 patches [rows_out][ldp]; 1 bf16 weights [OC][ldp];
+// Workspace slots: 0 bf16 patches [rows_out][ldp] (for a stride-2 conv on parity planes
+// the bf16 copy of the input [rows_in][IC], which is smaller); 1 bf16 weights [OC][ldp];
 // 2 bf16 delta [rows_out][lde]; 3 int32 patch-space delta [rows_out][K];
 // 4 split-K partials of the largest of the three contractions; 5 one uint32
 // receiving the (unused) max of the patch-space delta.
@@ -97,7 +106,8 @@ static void conv_slots(const ConvGeom& g, int OC, size_t sz[6])
     sz[3] = align256((size_t)4 * g.rows_out * g.K);
     size_t a = gemm_split_ws_bytes(M, OC, K, OC), b = gemm_split_ws_bytes(M, K, OC, K),
            c = gemm_split_ws_bytes(OC, K, M, K);
-    sz[4] = align256(std::max(a, std::max(b, c)));
+    const size_t d = conv_wgrad_s2_ws_bytes(g.B, g.H, g.W, g.IC, OC);
+    sz[4] = align256(std::max(std::max(a, d), std::max(b, c)));
     sz[5] = 256;
 }
 
@@ -265,6 +275,16 @@ int ito_conv2d_fwd(const int8_t* x, const int8_t* Wt, int B, int H, int W, int I
     conv_slots(g, OC, sz);
     uint16_t* Pb = reinterpret_cast<uint16_t*>(conv_slot(workspace, sz, 0));
     uint16_t* Wb = reinterpret_cast<uint16_t*>(conv_slot(workspace, sz, 1));
+    if (g.s2) {
+        // the input's bf16 copy, read through its parity planes
+        ITO_TRY(launch_i8_to_bf16(x, g.rows_in, IC, Pb, IC, s));
+        ITO_TRY(launch_i8_to_bf16(Wt, OC, g.K, Wb, g.ldp, s));
+        ITO_TRY(cuda_ok(cudaMemsetAsync(d_max, 0, sizeof(uint32_t), s), "memset"));
+        ConvIgPlan ip;
+        ITO_TRY(conv_fwd_s2_plan(&ip, Pb, IC, Wb, g.ldp, B, H, W, IC, OC, y32, d_max));
+        ITO_TRY(conv_igemm_run(ip, s));
+        return launch_requant(y32, g.rows_out, OC, d_max, p.target_bits, relu, nullptr, y, nullptr, 0, d_shift, s);
+    }
     ITO_TRY(launch_im2col(x, B, H, W, IC, g.OH, g.OW, stride, Pb, g.ldp, s));
     ITO_TRY(launch_i8_to_bf16(Wt, OC, g.K, Wb, g.ldp, s));
     ITO_TRY(cuda_ok(cudaMemsetAsync(d_max, 0, sizeof(uint32_t), s), "memset"));
@@ -294,7 +314,7 @@ int ito_conv2d_bwd_delta(const int8_t* delta, const int8_t* Wt, const int8_t* a_
     ITO_TRY(launch_i8_to_bf16(delta, g.rows_out, OC, eb, g.lde, s));
     ITO_TRY(launch_i8_to_bf16(Wt, OC, g.K, Wb, g.ldp, s));
     ITO_TRY(cuda_ok(cudaMemsetAsync(d_max, 0, sizeof(uint32_t), s), "memset"));
-    if (conv_dgrad_s2_eligible(B, H, W, IC, OC, stride)) {
+    if (g.s2) {
         // stride 2: each parity phase of the input-space delta is its own contraction, written
         // straight into d32 with its max
         ConvS2Plan sp;
@@ -328,6 +348,15 @@ int ito_conv2d_wgrad(const int8_t* delta, const int8_t* x, int B, int H, int W, 
     conv_slots(g, OC, sz);
     uint16_t* Pb = reinterpret_cast<uint16_t*>(conv_slot(workspace, sz, 0));
     uint16_t* eb = reinterpret_cast<uint16_t*>(conv_slot(workspace, sz, 2));
+    if (g.s2) {
+        ITO_TRY(launch_i8_to_bf16(x, g.rows_in, IC, Pb, IC, s));
+        ITO_TRY(launch_i8_to_bf16(delta, g.rows_out, OC, eb, g.lde, s));
+        ITO_TRY(cuda_ok(cudaMemsetAsync(d_max, 0, sizeof(uint32_t), s), "memset"));
+        ConvIgPlan ip;
+        ITO_TRY(conv_wgrad_s2_plan(&ip, eb, g.lde, Pb, IC, B, H, W, IC, OC, G, d_max,
+                                   reinterpret_cast<int32_t*>(conv_slot(workspace, sz, 4)), sz[4]));
+        return conv_igemm_run(ip, s);
+    }
     ITO_TRY(launch_im2col(x, B, H, W, IC, g.OH, g.OW, stride, Pb, g.ldp, s));
     ITO_TRY(launch_i8_to_bf16(delta, g.rows_out, OC, eb, g.lde, s));
     ITO_TRY(cuda_ok(cudaMemsetAsync(d_max, 0, sizeof(uint32_t), s), "memset"));

@@ -922,16 +922,19 @@ static int launch_tc(const GemmPlan& p, cudaStream_t s)
                p.kb_per_split, p.split_stride, split ? p.split_ws : p.C, p.ldc, split ? nullptr : p.d_max, p.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
-    if (split) {
-        const int vec = p.N % 4 == 0 && p.ldc % 4 == 0 && p.split_stride % 4 == 0 &&
-                        (reinterpret_cast<uintptr_t>(p.split_ws) & 15) == 0 &&
-                        (reinterpret_cast<uintptr_t>(p.C) & 15) == 0;
-        launch_pdl(k_splitk_reduce, launch_grid_blocks((int64_t)p.M * p.N / (vec ? 4 : 1) * 32, 256), 256, 0, s,
-                   p.split_ws, p.splits, p.split_stride, p.M, p.N, p.ldc, p.C, p.d_max, vec);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "split-K reduce launch: %s", cudaGetErrorString(e));
-    }
+    if (split) return launch_splitk_reduce(p.split_ws, p.splits, p.split_stride, p.M, p.N, p.ldc, p.C, p.d_max, s);
     return ITO_OK;
+}
+
+int launch_splitk_reduce(const int32_t* P, int splits, int64_t stride, int M, int N, int64_t ldc, int32_t* C,
+                         uint32_t* d_max, cudaStream_t s)
+{
+    const int vec = N % 4 == 0 && ldc % 4 == 0 && stride % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0 &&
+                    (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+    launch_pdl(k_splitk_reduce, launch_grid_blocks((int64_t)M * N / (vec ? 4 : 1) * 32, 256), 256, 0, s, P, splits,
+               stride, M, N, ldc, C, d_max, vec);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "split-K reduce launch: %s", cudaGetErrorString(e));
 }
 
 // CTA pairs of k_gemm_tc2<A_MN, B_MN> that fit on the device at once (its

@@ -127,6 +127,37 @@ int conv_dgrad_s2_plan(ConvS2Plan* p, const uint16_t* eb, int64_t lde, const uin
                        int H, int W, int IC, int OC, int32_t* D, uint32_t* d_max);
 int conv_dgrad_s2_run(const ConvS2Plan& p, cudaStream_t s);
 
+// Forward and weight gradient of the same convolutions on the four parity planes of the
+// bf16 NHWC input X [B][H][W][ldx] (no patches; see k_conv_igemm).
+enum { CONV_FWD = 0, CONV_WGRAD = 1 };
+struct IgGeom {
+    int B, OH, OW, IC, ic_blocks;
+    int oha, ba, n_iblk;          // forward row tiles: ba images x oha rows x OW (128 positions)
+    int ohb, bb, n_iblk_w;        // weight-gradient position blocks: bb images x ohb rows x OW (64)
+    int m_tiles, n_tiles, num_kb, splits, kb_per_split, rows;
+};
+struct ConvIgPlan {
+    int mode;
+    CUtensorMap mapX[4];          // parity planes (py, px) = (i >> 1, i & 1)
+    CUtensorMap mapOp;            // forward: W [OC][9 IC] K-major; weight gradient: E [positions][OC] MN-major
+    CUtensorMap mapOut;           // Y [positions][OC], G [OC][9 IC], or G's K-slice partials
+    IgGeom g;
+    int32_t* G;                   // weight gradient with K slices: the result the reduction writes
+    int32_t* ws;
+    int OC, K9;
+    uint32_t* d_max;
+    int* err;
+};
+// Y[(b,oh,ow)][oc] (rows of OC) = the convolution; max |Y| into *d_max (the caller zeroes it)
+int conv_fwd_s2_plan(ConvIgPlan* p, const uint16_t* xb, int64_t ldx, const uint16_t* Wb, int64_t ldw, int B, int H,
+                     int W, int IC, int OC, int32_t* Y, uint32_t* d_max);
+// G[oc][(kh,kw,ic)] (rows of 9 IC) = sum over positions of E x X; max |G| into *d_max; K slices
+// over the positions when ws holds conv_wgrad_s2_ws_bytes
+int conv_wgrad_s2_plan(ConvIgPlan* p, const uint16_t* eb, int64_t lde, const uint16_t* xb, int64_t ldx, int B,
+                       int H, int W, int IC, int OC, int32_t* G, uint32_t* d_max, int32_t* ws, size_t ws_bytes);
+size_t conv_wgrad_s2_ws_bytes(int B, int H, int W, int IC, int OC);
+int conv_igemm_run(const ConvIgPlan& p, cudaStream_t s);
+
 // ---- DFP16 limb contraction (ito_dfp.cu)
 
 // P[M][N] (int64, exact) = sum_k A(m,k) B(n,k) for int16 operands given as two
@@ -235,6 +266,9 @@ size_t gemm_split_ws_bytes(int M, int N, int K, int64_t ldc);
 int gemm_plan_fuse_requant(GemmPlan* p, const int32_t* pred, int relu, const int8_t* gate, int64_t ldg,
                            int8_t* out8, int64_t ld8, uint16_t* outb, int64_t ldb);
 int gemm_run(const GemmPlan& p, cudaStream_t s);
+// C[m][n] = sum over s < splits of P[s * stride + m * ldc + n] (exact), max |C| into *d_max
+int launch_splitk_reduce(const int32_t* P, int splits, int64_t stride, int M, int N, int64_t ldc, int32_t* C,
+                         uint32_t* d_max, cudaStream_t s);
 
 // ---- bandwidth kernels (ito_elementwise.cu)
 

@@ -67,6 +67,10 @@ struct MLayer {
     // stride-2 conv: the input-space delta by parity phases (no patch-space delta, no gather)
     bool s2 = false;
     ConvS2Plan ps2{};
+    // stride-2 conv after a conv: forward and weight gradient on the parity planes of the
+    // previous layer's bf16 output copy (no im2col patches)
+    bool ig = false;
+    ConvIgPlan pig_f{}, pig_g{};
     bool has_dgrad = false;
     bool relu = false;
 };
@@ -308,6 +312,12 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
             if (m->L[l].relu && m->L[l].OC % 8)
                 return set_error(ITO_ERR_UNSUPPORTED, "packed masks need ReLU widths that are multiples of 8");
 
+    for (int l = 1; l < nl; ++l) {
+        MLayer& L = m->L[l];
+        L.ig = L.kind == ITO_LAYER_CONV3X3_RELU && m->L[l - 1].kind == ITO_LAYER_CONV3X3_RELU &&
+               conv_dgrad_s2_eligible(B, L.H, L.W, L.IC, L.OC, L.stride);
+    }
+
     // allocations
     ITO_TRY(m->alloc(&m->x8, (size_t)B * m->in_features));
     ITO_TRY(m->alloc(&m->labels, (size_t)B));
@@ -336,7 +346,8 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         ITO_TRY(m->alloc(&L.a8, (size_t)L.rows_out * L.OC));
         L.lda = pad8(L.OC);
         const bool next_linear = l + 1 < nl && m->L[l + 1].kind != ITO_LAYER_CONV3X3_RELU && !conv;
-        if (next_linear) ITO_TRY(m->alloc(&L.ab, (size_t)L.rows_out * L.lda));
+        const bool next_planes = l + 1 < nl && m->L[l + 1].ig;   // the next conv reads this output's bf16 copy
+        if (next_linear || next_planes) ITO_TRY(m->alloc(&L.ab, (size_t)L.rows_out * L.lda));
         L.lde = pad8(L.OC);
         if (m->opt.pingpong_grads) {
             // two delta buffers for all layers: layer l writes buffer l % 2, which no layer
@@ -369,7 +380,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         if (L.has_dgrad) ITO_TRY(m->alloc(&L.d32, (size_t)L.rows_in * L.IC));
         if (conv) {
             L.ldp = pad8(L.K);
-            ITO_TRY(m->alloc(&L.Pb, (size_t)L.rows_out * L.ldp));
+            if (!L.ig) ITO_TRY(m->alloc(&L.Pb, (size_t)L.rows_out * L.ldp));
             L.s2 = L.has_dgrad && conv_dgrad_s2_eligible(B, L.H, L.W, L.IC, L.OC, L.stride);
             if (L.has_dgrad && !L.s2) ITO_TRY(m->alloc(&L.dcol, (size_t)L.rows_out * L.K));
         }
@@ -382,6 +393,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         size_t need = gemm_split_ws_bytes(M, L.OC, (int)L.K, L.OC);
         if (L.has_dgrad) need = std::max(need, gemm_split_ws_bytes(M, (int)L.K, L.OC, L.K));
         need = std::max(need, gemm_split_ws_bytes(L.OC, (int)L.K, M, L.K));
+        if (L.ig) need = std::max(need, conv_wgrad_s2_ws_bytes(B, L.H, L.W, L.IC, L.OC));
         m->split_ws_bytes = std::max(m->split_ws_bytes, need);
     }
     if (m->split_ws_bytes) ITO_TRY(m->alloc(&m->split_ws, m->split_ws_bytes / sizeof(int32_t)));
@@ -423,9 +435,17 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         constexpr int kMinPairTiles = 64;
         const int pair_f = spec_small && L.rows_out * L.OC >= spec_min ? 1 : kMinPairTiles;
         const int pair_d = spec_small && L.rows_in * L.IC >= spec_min ? 1 : kMinPairTiles;
-        // forward: Y[m][oc] = sum_k in[m][k] W[oc][k]
-        ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax, m->split_ws,
-                          m->split_ws_bytes, chunk, pair_f));
+        if (L.ig) {
+            // forward and weight gradient on the parity planes of the previous conv's bf16 output
+            const MLayer& prev = m->L[l - 1];
+            ITO_TRY(conv_fwd_s2_plan(&L.pig_f, prev.ab, prev.lda, L.Wb, L.ldw, B, L.H, L.W, L.IC, L.OC, L.y32, ymax));
+            ITO_TRY(conv_wgrad_s2_plan(&L.pig_g, L.eb, L.lde, prev.ab, prev.lda, B, L.H, L.W, L.IC, L.OC, L.g32, gmax,
+                                       m->split_ws, m->split_ws_bytes));
+        } else {
+            // forward: Y[m][oc] = sum_k in[m][k] W[oc][k]
+            ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax, m->split_ws,
+                              m->split_ws_bytes, chunk, pair_f));
+        }
         // delta propagation: D[m][k] = sum_oc e[m][oc] W[oc][k]; for a conv this is the
         // patch-space delta, whose max is not the NITI max (col2im takes that), except for a
         // stride-2 conv, whose input-space delta comes straight from its parity phases
@@ -435,8 +455,9 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
             ITO_TRY(gemm_plan(&L.pd, ev, false, wv, true, M, (int)L.K, L.OC, conv ? L.dcol : L.d32, L.K,
                               conv ? m->discard_max : dmax, m->split_ws, m->split_ws_bytes, kExactChunk, pair_d));
         // weight gradient: G[oc][k] = sum_m e[m][oc] in[m][k]
-        ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax, m->split_ws,
-                          m->split_ws_bytes, chunk, kMinPairTiles));
+        if (!L.ig)
+            ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax, m->split_ws,
+                              m->split_ws_bytes, chunk, kMinPairTiles));
         // speculative requantisation in the epilogues of the forward contraction (its ReLU'd
         // activation and bf16 copy) and of the delta propagation (the gated delta below); not
         // with bit-packed masks, static requantisation, or shared (ping-pong) delta buffers
@@ -546,7 +567,7 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
     const int8_t* in8 = x;
     for (int l = 0; l < nl; ++l) {
         MLayer& L = m->L[l];
-        if (L.kind == ITO_LAYER_CONV3X3_RELU) {
+        if (L.kind == ITO_LAYER_CONV3X3_RELU && !L.ig) {
             ITO_LAUNCH(m, s, ITO_PROF_OTHER, (double)L.rows_in * L.IC + 2.0 * L.rows_out * L.ldp,
                        launch_im2col(in8, B, L.H, L.W, L.IC, L.OH, L.OW, L.stride, L.Pb, L.ldp, s));
         } else if (l == m->n_conv && m->has_pool) {
@@ -566,7 +587,10 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
             ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf_spec), gemm_run(L.pf_spec, s));
             ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pf_redo, s));
         } else {
-            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
+            if (L.ig)
+                ITO_LAUNCH(m, s, ITO_PROF_GEMM, 2.0 * L.rows_out * L.OC * L.K, conv_igemm_run(L.pig_f, s));
+            else
+                ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pf), gemm_run(L.pf, s));
             if (L.static_q)
                 ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
                            launch_requant_static(L.y32, L.rows_out, L.OC, L.off32, L.mult32, L.k32, L.relu ? 1 : 0,
@@ -657,7 +681,10 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
                 delta_on_side = true;
             }
         }
-        ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
+        if (L.ig)
+            ITO_LAUNCH(m, s, ITO_PROF_GEMM, 2.0 * L.rows_out * L.OC * L.K, conv_igemm_run(L.pig_g, s));
+        else
+            ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, s));
         ITO_TRY(sync(m->ev_wgrad(l), s, b));       // the weight gradient is complete
         // G read (4 B), W read and written (1 + 1 B), bf16 copy written (2 B)
         ITO_LAUNCH(m, b, ITO_PROF_UPDATE, 8.0 * L.OC * L.K,

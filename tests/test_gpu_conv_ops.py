@@ -51,7 +51,14 @@ def test_full_shapes_are_the_workload():
     assert [f[1] for f in FULL] == [32, 32, 16]
 
 
-@pytest.mark.parametrize("B,H,W,IC,OC,stride", FULL + RAGGED)
+# Stride-2 shapes taken by the parity-plane kernels (even H and W, OW of 8, 16 or 32,
+# channels in multiples of 64): a row tile of two images with one or three in the batch,
+# 32 output columns, a 4 x 32 input (four images to a row tile), 512 delta channels (the
+# four-tap delta phase sums 2048 terms: two exact chunks)
+PHASE = [(1, 16, 16, 64, 64, 2), (3, 16, 16, 128, 64, 2), (2, 64, 64, 64, 64, 2), (2, 4, 32, 64, 128, 2),
+         (2, 16, 16, 64, 512, 2)]
+
+@pytest.mark.parametrize("B,H,W,IC,OC,stride", FULL + RAGGED + PHASE)
 @pytest.mark.parametrize("relu", [0, 1])
 def test_conv2d_fwd(ito, B, H, W, IC, OC, stride, relu):
     x, Wt = i8((B, H, W, IC), -127, 127), i8((OC, 3, 3, IC), -127, 127)
@@ -76,14 +83,6 @@ def test_conv2d_bwd_delta(ito, B, H, W, IC, OC, stride, gated):
     assert np.array_equal(_host(d32), D)
     assert (_u32(mx), int(_host(sh)[0])) == (m, s)
     assert np.array_equal(_host(dp), ep)
-
-
-# Stride-2 shapes taken by the parity-phase delta propagation (even H and W, OW of 8, 16
-# or 32, channels in multiples of 64): a row tile of two images with one or three in
-# the batch, 32 output columns, a 4 x 32 input (four images to a row tile), 512 delta
-# channels (the four-tap phase sums 2048 terms: two exact chunks)
-PHASE = [(1, 16, 16, 64, 64, 2), (3, 16, 16, 128, 64, 2), (2, 64, 64, 64, 64, 2), (2, 4, 32, 64, 128, 2),
-         (2, 16, 16, 64, 512, 2)]
 
 
 @pytest.mark.parametrize("B,H,W,IC,OC,stride", PHASE)
@@ -113,7 +112,7 @@ def test_conv2d_bwd_delta_stride2_extreme(ito):
     assert _u32(mx) == int(np.abs(D).max())
 
 
-@pytest.mark.parametrize("B,H,W,IC,OC,stride", FULL + RAGGED)
+@pytest.mark.parametrize("B,H,W,IC,OC,stride", FULL + RAGGED + PHASE)
 def test_conv2d_wgrad(ito, B, H, W, IC, OC, stride):
     OH, OW = O.conv_out(H, 3, stride), O.conv_out(W, 3, stride)
     e, x = i8((B, OH, OW, OC)), i8((B, H, W, IC), 0, 127)
@@ -121,6 +120,29 @@ def test_conv2d_wgrad(ito, B, H, W, IC, OC, stride):
     Gref = O.conv2d_wgrad(e, x, 3, stride)
     assert np.array_equal(_host(G), Gref)
     assert _u32(mx) == O.absmax32(Gref)
+
+
+def test_conv2d_stride2_planes_extreme(ito):
+    """Every product (-127)(-127) or (-128)(-127) on the parity-plane kernels: the forward of
+    the third conv sums 9 x 128 = 1152 terms at interior positions (two exact chunks);
+    the second conv's weight gradient sums 128 x 16 x 16 = 32768 terms for the centre
+    tap, over K slices added by the reduction."""
+    B, H, W, IC, OC = 4, 16, 16, 128, 64
+    x = np.full((B, H, W, IC), -127, np.int8)
+    Wt = np.full((OC, 3, 3, IC), -127, np.int8)
+    y32, mx, _, _ = ito.ito_conv2d_fwd(_dev(x), _dev(Wt), 2, 0)
+    Y = O.conv2d_fwd(x, Wt, 2)
+    assert int(Y.max()) == 9 * IC * 127 * 127
+    assert np.array_equal(_host(y32), Y)
+    assert _u32(mx) == int(np.abs(Y).max())
+    B, H, W, IC, OC = 128, 32, 32, 64, 128
+    e = np.full((B, 16, 16, OC), -128, np.int8)
+    x = np.full((B, H, W, IC), -127, np.int8)
+    G, mx = ito.ito_conv2d_wgrad(_dev(e), _dev(x), 2)
+    Gr = O.conv2d_wgrad(e, x, 3, 2)
+    assert int(Gr.max()) == B * 16 * 16 * 128 * 127
+    assert np.array_equal(_host(G), Gr)
+    assert _u32(mx) == int(np.abs(Gr).max())
 
 
 def test_conv2d_wgrad_extreme_long_contraction(ito):
