@@ -771,7 +771,7 @@ def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local, flush, pk, p
         return None
     ops = algorithmic_ops(w)
     roof = gemm_roofline(prof, pk, pk_src)
-    roof.update({"kernel": "k_gemm_dfp2 / k_gemm_dfp (int16 limb contractions: four bf16 limb products per "
+    roof.update({"kernel": "k_gemm_dfp4 / k_gemm_dfp2 / k_gemm_dfp (int16 limb contractions: four bf16 limb products per "
                            "int16 multiply-add, exact int64 sums)",
                  "work": "executed bf16 operations, 8*M*N*K per contraction", "traffic": None,
                  "measured_over": "the same %d steps run again with an event pair around every launch "
