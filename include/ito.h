@@ -208,7 +208,12 @@ int ito_top_error(const int8_t *logits, const int32_t *labels, int B, int C, int
 
 /* Bytes of device workspace any of ito_conv2d_fwd / _bwd_delta / _wgrad
  * needs for these sizes (0 on invalid sizes): bf16 patch, weight and delta
- * copies, the int32 patch-space delta, split-K partials and one scratch word. */
+ * copies, the int32 patch-space delta, split-K partials and one scratch word.
+ * A stride-2 conv with even H and W, OW = W/2 of 8, 16 or 32, OH = H/2 a power
+ * of two with OH*OW >= 32, and IC, OC multiples of 64 is contracted without
+ * patches (the input's bf16 copy is read through its four parity planes, the
+ * propagated delta by its four parity phases); it uses the same workspace
+ * (the patch slot holds the input's bf16 copy) and gives the same results. */
 size_t ito_conv2d_workspace_size(int B, int H, int W, int IC, int OC, int stride);
 
 /* Forward 3x3 conv + requantisation:
