@@ -153,7 +153,7 @@ __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_
                              const uint32_t* __restrict__ d_max, int target_bits, int relu,
                              const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
                              int64_t ldb, int32_t* __restrict__ d_shift, const uint8_t* __restrict__ gate_bits,
-                             uint8_t* __restrict__ mask_out, int32_t* __restrict__ s_last)
+                             uint8_t* __restrict__ mask_out, int32_t* __restrict__ s_last, TopErr te)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -192,13 +192,28 @@ __global__ void k_requant_v8(const int32_t* __restrict__ Y, int64_t rows, int64_
         if (outb) {
             *reinterpret_cast<uint4*>(outb + pitched(i0, cols, ldb)) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
         }
+        if (te.labels) {
+            // the top error of these eight logits (as k_top_error_v8)
+            const int64_t row = i0 / cols;
+            const int64_t c0 = i0 - row * cols;
+            const int label = te.labels[row];
+            if (c0 == 0 && (label < 0 || label >= cols)) raise_device_error(te.err, ITO_ERR_ARG);
+            int8_t d[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d[i] = (int8_t)sat8((int32_t)q8[i] - (c0 + i == label ? te.target_mag : 0));
+            *reinterpret_cast<uint2*>(te.e8 + i0) = *reinterpret_cast<const uint2*>(d);
+            if (te.eb)
+                *reinterpret_cast<uint4*>(te.eb + pitched(i0, cols, te.lde)) =
+                    make_uint4(int_pair_to_bf16x2(d[0], d[1]), int_pair_to_bf16x2(d[2], d[3]),
+                               int_pair_to_bf16x2(d[4], d[5]), int_pair_to_bf16x2(d[6], d[7]));
+        }
     }
 }
 
 __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t cols,
                             const uint32_t* __restrict__ d_max, int target_bits, int relu,
                             const int8_t* __restrict__ gate, int8_t* __restrict__ out8, uint16_t* __restrict__ outb,
-                            int64_t ldb, int32_t* __restrict__ d_shift, int32_t* __restrict__ s_last)
+                            int64_t ldb, int32_t* __restrict__ d_shift, int32_t* __restrict__ s_last, TopErr te)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -214,24 +229,40 @@ __global__ void k_requant_1(const int32_t* __restrict__ Y, int64_t rows, int64_t
         if (outb) {
             outb[pitched(i, cols, ldb)] = int_to_bf16_bits(q);
         }
+        if (te.labels) {
+            // the top error of this logit (as k_top_error)
+            const int64_t row = i / cols, c = i - row * cols;
+            const int label = te.labels[row];
+            if (c == 0 && (label < 0 || label >= cols)) raise_device_error(te.err, ITO_ERR_ARG);
+            const int32_t d = sat8(q - (c == label ? te.target_mag : 0));
+            te.e8[i] = (int8_t)d;
+            if (te.eb) te.eb[pitched(i, cols, te.lde)] = int_to_bf16_bits(d);
+        }
     }
 }
 
 int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t* d_max, int target_bits, int relu,
                    const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
-                   const uint8_t* gate_bits, uint8_t* mask_out, int32_t* s_last)
+                   const uint8_t* gate_bits, uint8_t* mask_out, int32_t* s_last, const TopErr* top)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
+    TopErr te{};
+    if (top) {
+        te = *top;
+        te.err = device_error_word();
+        if (!te.err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
+    }
     const bool vec = cols % 8 == 0 && aligned(Y, 16) && aligned(out8, 8) && (!gate || aligned(gate, 8)) &&
-                     (!outb || (aligned(outb, 16) && ldb % 8 == 0));
+                     (!outb || (aligned(outb, 16) && ldb % 8 == 0)) &&
+                     (!top || (aligned(te.e8, 8) && (!te.eb || (aligned(te.eb, 16) && te.lde % 8 == 0))));
     if ((gate_bits || mask_out) && !vec)
         return set_error(ITO_ERR_UNSUPPORTED, "bit-packed masks need rows of a multiple of 8 elements");
     if (vec)
-        launch_pdl(k_requant_v8, launch_grid_blocks(rows * cols / 8, 256), 256, 0, s, 
-            Y, rows, cols, d_max, target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out, s_last);
+        launch_pdl(k_requant_v8, launch_grid_blocks(rows * cols / 8, 256), 256, 0, s, Y, rows, cols, d_max,
+                   target_bits, relu, gate, out8, outb, ldb, d_shift, gate_bits, mask_out, s_last, te);
     else
-        launch_pdl(k_requant_1, launch_grid_blocks(rows * cols, 256), 256, 0, s, Y, rows, cols, d_max, target_bits, relu,
-                                                                          gate, out8, outb, ldb, d_shift, s_last);
+        launch_pdl(k_requant_1, launch_grid_blocks(rows * cols, 256), 256, 0, s, Y, rows, cols, d_max, target_bits,
+                   relu, gate, out8, outb, ldb, d_shift, s_last, te);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "requant launch: %s", cudaGetErrorString(e));
 }
@@ -275,6 +306,73 @@ int launch_roll_shift_predictions(int32_t* pred, const int32_t* last, const int3
                                               on);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "prediction launch: %s", cudaGetErrorString(e));
+}
+
+// The start of a training (or inference) step in one launch: the step's statistics
+// block zeroed and the shift predictions rolled (as k_roll_shift_predictions, n_pred > 0)
+// by block 0, and a Linear first layer's int8 or uint8 input converted to its bf16 copy
+// by all blocks (x == nullptr: none).
+__global__ void k_step_begin(int32_t* __restrict__ stats, int n_stats, int32_t* __restrict__ pred,
+                             const int32_t* __restrict__ last, const int32_t* __restrict__ used,
+                             unsigned long long* __restrict__ count, int n_pred, int on, const void* __restrict__ x,
+                             int x_u8, int64_t rows, int64_t cols, uint16_t* __restrict__ xb, int64_t ldx, int vec)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < n_stats; i += blockDim.x) stats[i] = 0;
+        if (threadIdx.x < 32 && n_pred > 0) {
+            unsigned hits = 0, misses = 0;
+            for (int i = threadIdx.x; i < n_pred; i += 32) {
+                const int32_t p = pred[i], l = last[i];
+                const bool u = used[i] != 0;
+                if (u && p >= 0) {
+                    hits += p == l;
+                    misses += p != l;
+                }
+                pred[i] = (on && u) ? l : -1;
+            }
+            hits = __reduce_add_sync(0xffffffffu, hits);
+            misses = __reduce_add_sync(0xffffffffu, misses);
+            if (threadIdx.x == 0) {
+                count[0] += hits;
+                count[1] += misses;
+            }
+        }
+    }
+    if (!x) return;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if (vec) {
+        const int64_t groups = rows * (cols >> 3);
+        for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups; g += stride) {
+            const int64_t i0 = g << 3;
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(x) + i0));
+            const uint8_t* b = reinterpret_cast<const uint8_t*>(&v);
+            int32_t t[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t[k] = x_u8 ? (int32_t)b[k] : (int32_t)(int8_t)b[k];
+            *reinterpret_cast<uint4*>(xb + pitched(i0, cols, ldx)) =
+                make_uint4(int_pair_to_bf16x2(t[0], t[1]), int_pair_to_bf16x2(t[2], t[3]),
+                           int_pair_to_bf16x2(t[4], t[5]), int_pair_to_bf16x2(t[6], t[7]));
+        }
+    } else {
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < rows * cols; i += stride) {
+            const uint8_t b = static_cast<const uint8_t*>(x)[i];
+            xb[pitched(i, cols, ldx)] = int_to_bf16_bits(x_u8 ? (int32_t)b : (int32_t)(int8_t)b);
+        }
+    }
+}
+
+int launch_step_begin(int32_t* stats, int n_stats, int32_t* pred, const int32_t* last, const int32_t* used,
+                      int64_t* count, int n_pred, int on, const void* x, int x_u8, int64_t rows, int64_t cols,
+                      uint16_t* xb, int64_t ldx, cudaStream_t s)
+{
+    const bool vec = x && cols % 8 == 0 && ldx % 8 == 0 && aligned(x, 8) && aligned(xb, 16);
+    const int blocks = x ? launch_grid_blocks(vec ? rows * cols / 8 : rows * cols, 256) : 1;
+    launch_pdl(k_step_begin, blocks, 256, 0, s, stats, n_stats, pred, last, used,
+               reinterpret_cast<unsigned long long*>(count), n_pred, on, x, x_u8, rows, cols, xb, ldx, vec ? 1 : 0);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "step start launch: %s", cudaGetErrorString(e));
 }
 
 // ------------------------------------------- static requantisation + offsets

@@ -159,6 +159,7 @@ struct ito_model {
     std::vector<double> prof_work;
     int prof_n = 0;
     int launches = 0;                      // kernels launched by the current / last step
+    bool top_fused = false;                // this step's forward wrote the top error
 
     // during a capture the record must be "external" to become a graph node (the flag is
     // rejected on a stream that is not capturing)
@@ -553,17 +554,28 @@ static double requant_bytes(int64_t n, bool bf16, bool gate)
     return (double)n * (4 + 1 + (bf16 ? 2 : 0) + (gate ? 1 : 0));
 }
 
-static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
+// The start of a step: statistics zeroed, shift predictions rolled (a training step), and a
+// Linear first layer's input converted to its bf16 copy, in one launch.
+static int model_begin(ito_model* m, const int8_t* x, bool train, cudaStream_t s)
+{
+    const int B = m->batch;
+    const int nl = (int)m->L.size();
+    const bool conv_in = m->n_conv > 0;
+    ITO_LAUNCH(m, s, ITO_PROF_OTHER, conv_in ? 4.0 * m->n_stats : 3.0 * B * m->in_features + 4.0 * m->n_stats,
+               launch_step_begin(m->stats, m->n_stats, m->spec, m->spec + 2 * nl, m->spec + 4 * nl, m->spec_count,
+                                 train ? 2 * nl : 0, m->speculate ? 1 : 0, conv_in ? nullptr : x,
+                                 m->opt.input_uint8 ? 1 : 0, B, m->in_features, m->xb, m->ldx, s));
+    return ITO_OK;
+}
+
+// labels: the step's labels (the top error is computed beside the logits' requantisation),
+// or nullptr (inference)
+static int model_forward(ito_model* m, const int8_t* x, const int32_t* labels, cudaStream_t s)
 {
     const int B = m->batch;
     const int nl = (int)m->L.size();
     const ito_niti_params p = m->p;
-    if (m->n_conv == 0 && m->opt.input_uint8)
-        ITO_LAUNCH(m, s, ITO_PROF_OTHER, 3.0 * B * m->in_features,
-                   launch_u8_to_bf16(reinterpret_cast<const uint8_t*>(x), B, m->in_features, m->xb, m->ldx, s));
-    else if (m->n_conv == 0)
-        ITO_LAUNCH(m, s, ITO_PROF_OTHER, 3.0 * B * m->in_features,
-                   launch_i8_to_bf16(x, B, m->in_features, m->xb, m->ldx, s));
+    m->top_fused = false;
     const int8_t* in8 = x;
     for (int l = 0; l < nl; ++l) {
         MLayer& L = m->L[l];
@@ -595,11 +607,17 @@ static int model_forward(ito_model* m, const int8_t* x, cudaStream_t s)
                 ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
                            launch_requant_static(L.y32, L.rows_out, L.OC, L.off32, L.mult32, L.k32, L.relu ? 1 : 0,
                                                  L.a8, L.ab, L.lda, L.mask, s));
-            else
-                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false),
+            else {
+                // the logits' requantisation also writes the top error (the backward's first delta)
+                const bool top = l == nl - 1 && labels;
+                const TopErr te{labels, m->target_mag, L.e8, L.eb, L.lde, nullptr};
+                ITO_LAUNCH(m, s, ITO_PROF_REQUANT,
+                           requant_bytes(L.rows_out * L.OC, L.ab != nullptr, false) + (top ? 3.0 * B * L.OC : 0.0),
                            launch_requant(L.y32, L.rows_out, L.OC, m->umax(l, ST_YMAX), p.target_bits,
                                           L.relu ? 1 : 0, nullptr, L.a8, L.ab, L.lda, m->sval(l, ST_YS), s, nullptr,
-                                          L.mask, m->last_y(l)));
+                                          L.mask, m->last_y(l), top ? &te : nullptr));
+                m->top_fused = top;
+            }
         }
         in8 = L.a8;
     }
@@ -629,8 +647,9 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
         return ITO_OK;
     };
     MLayer& top = m->L[nl - 1];
-    ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * top.OC + 4.0 * B,
-               launch_top_error(top.a8, labels, B, top.OC, m->target_mag, top.e8, top.eb, top.lde, s));
+    if (!m->top_fused)
+        ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * top.OC + 4.0 * B,
+                   launch_top_error(top.a8, labels, B, top.OC, m->target_mag, top.e8, top.eb, top.lde, s));
     ITO_TRY(sync(m->ev_fork(), s, b));
     bool delta_on_side = false;   // the layer above requantised this layer's delta on the side stream
     for (int l = nl - 1; l >= m->opt.trainable_from; --l) {
@@ -962,13 +981,9 @@ int ito_model_use_graphs(ito_model* m, int enable)
 static int step_direct(ito_model* m, const int8_t* x, const int32_t* labels, cudaStream_t s)
 {
     m->launches = 0;
-    cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * m->n_stats, s);
-    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
-    // this step's shift predictions are the last step's shifts
-    const int nl = (int)m->L.size();
-    ITO_TRY(launch_roll_shift_predictions(m->spec, m->spec + 2 * nl, m->spec + 4 * nl, m->spec_count, 2 * nl,
-                                          m->speculate ? 1 : 0, s));
-    ITO_TRY(model_forward(m, x, s));
+    // statistics zeroed, this step's shift predictions = the last step's shifts, input in bf16
+    ITO_TRY(model_begin(m, x, true, s));
+    ITO_TRY(model_forward(m, x, labels, s));
     return model_backward(m, x, labels, s);
 }
 
@@ -1077,11 +1092,10 @@ int ito_infer(ito_model* m, const int8_t* x, int8_t* logits, void* stream)
     if (!m || !x || !logits) return set_error(ITO_ERR_ARG, "NULL argument");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     m->launches = 0;
-    cudaError_t e = cudaMemsetAsync(m->stats, 0, sizeof(int32_t) * m->n_stats, s);
-    if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
-    ITO_TRY(model_forward(m, x, s));
+    ITO_TRY(model_begin(m, x, false, s));
+    ITO_TRY(model_forward(m, x, nullptr, s));
     const MLayer& top = m->L.back();
-    e = cudaMemcpyAsync(logits, top.a8, (size_t)top.rows_out * top.OC, cudaMemcpyDeviceToDevice, s);
+    cudaError_t e = cudaMemcpyAsync(logits, top.a8, (size_t)top.rows_out * top.OC, cudaMemcpyDeviceToDevice, s);
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "logits copy: %s", cudaGetErrorString(e));
 }
 
