@@ -419,12 +419,17 @@ int ito_model_use_graphs(ito_model *m, int enable);
  *   1: the requantisation of each propagated delta and the weight and offset
  *      updates run on a second, model-owned stream beside the next contractions
  *      (a bandwidth-bound pass shares the SMs with a tensor-core one);
- *   2: only the weight updates run on the second stream.
+ *   2: only the weight updates run on the second stream;
+ *   3: the delta chain (delta propagation, its requantisation, the next layer's delta
+ *      propagation) stays on the caller's stream and each layer's weight gradient and
+ *      update run on the second stream (the weight gradients with their own split-K
+ *      workspace); not with ping-pong delta buffers or static requantisation.
  * Events order every read after its write; the step ends joined on the caller's
  * stream. Changing the mode synchronises the device and drops captured graphs.
- * A new model takes mode 1, or mode 0 when every delta propagation requantises
- * speculatively (see ito_model_set_speculation), since the second stream would
- * then hold only the updates. Errors: ITO_ERR_ARG (NULL model, mode outside 0..2). */
+ * A new model takes mode 1, or, when every delta propagation requantises
+ * speculatively (see ito_model_set_speculation), mode 3 (mode 0 where mode 3 is not
+ * possible). Errors: ITO_ERR_ARG (NULL model, mode outside 0..3), ITO_ERR_UNSUPPORTED
+ * (mode 3 with ping-pong delta buffers or static requantisation). */
 int ito_model_set_overlap(ito_model *m, int mode);
 
 /* Writes the model's current backward stream layout (0, 1 or 2) to *mode (a

@@ -112,6 +112,7 @@ struct ito_model {
     uint32_t* discard_max = nullptr;   // max target of the patch-space conv delta (not a NITI tensor)
     int32_t* split_ws = nullptr;       // split-K partials, shared by the step's contractions (one stream)
     size_t split_ws_bytes = 0;
+    int32_t* split_ws_g = nullptr;     // the weight gradients' own (they may run beside the others, mode 3)
     std::vector<void*> allocs;
     std::vector<std::pair<std::string, int>> stat_names;
     // CUDA-graph replay of whole steps, keyed by the caller's input pointers
@@ -129,7 +130,9 @@ struct ito_model {
     std::vector<GraphEntry> graphs;
     // backward overlap: the bandwidth passes (requantisation of the propagated delta, the
     // weight and offset updates) run on a second stream beside the next contractions
-    int overlap = 1;                    // 0: one stream; 1: requantisation and updates overlap; 2: updates only
+    int overlap = 1;                    // 0: one stream; 1: requantisation and updates overlap; 2: updates only;
+                                        // 3: weight gradients and updates beside the delta chain
+    bool overlap3_ok = false;           // mode 3 is possible (no ping-pong buffers, no static requantisation)
     // speculative requantisation: [0, nl) forward and [nl, 2nl) delta-propagation shift predictions,
     // then the shifts of the last step in the same order, then 1 where the contraction's epilogue
     // speculates (its plan is fused), then the re-launch words (0: the prediction held, else the
@@ -398,6 +401,14 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
         m->split_ws_bytes = std::max(m->split_ws_bytes, need);
     }
     if (m->split_ws_bytes) ITO_TRY(m->alloc(&m->split_ws, m->split_ws_bytes / sizeof(int32_t)));
+    // mode 3 runs each weight gradient beside the next delta propagation: their partials
+    // get their own workspace, and the delta buffers must not be shared
+    m->overlap3_ok = !m->opt.pingpong_grads;
+    for (const MLayer& L : m->L)
+        if (L.static_q) m->overlap3_ok = false;
+    if (m->overlap3_ok && m->split_ws_bytes)
+        ITO_TRY(m->alloc(&m->split_ws_g, m->split_ws_bytes / sizeof(int32_t)));
+    int32_t* const ws_g = m->overlap3_ok ? m->split_ws_g : m->split_ws;
     ITO_TRY(m->alloc(&m->spec, (size_t)8 * nl));
     ITO_TRY(m->alloc(&m->spec_count, 2));
     if (cudaMemset(m->spec, 0xff, sizeof(int32_t) * 4 * nl) != cudaSuccess)   // -1: no prediction yet
@@ -441,7 +452,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
             const MLayer& prev = m->L[l - 1];
             ITO_TRY(conv_fwd_s2_plan(&L.pig_f, prev.ab, prev.lda, L.Wb, L.ldw, B, L.H, L.W, L.IC, L.OC, L.y32, ymax));
             ITO_TRY(conv_wgrad_s2_plan(&L.pig_g, L.eb, L.lde, prev.ab, prev.lda, B, L.H, L.W, L.IC, L.OC, L.g32, gmax,
-                                       m->split_ws, m->split_ws_bytes));
+                                       ws_g, m->split_ws_bytes));
         } else {
             // forward: Y[m][oc] = sum_k in[m][k] W[oc][k]
             ITO_TRY(gemm_plan(&L.pf, in, false, wv, false, M, L.OC, (int)L.K, L.y32, L.OC, ymax, m->split_ws,
@@ -457,7 +468,7 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
                               conv ? m->discard_max : dmax, m->split_ws, m->split_ws_bytes, kExactChunk, pair_d));
         // weight gradient: G[oc][k] = sum_m e[m][oc] in[m][k]
         if (!L.ig)
-            ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax, m->split_ws,
+            ITO_TRY(gemm_plan(&L.pg, ev, true, in, true, L.OC, (int)L.K, M, L.g32, L.K, gmax, ws_g,
                               m->split_ws_bytes, chunk, kMinPairTiles));
         // speculative requantisation in the epilogues of the forward contraction (its ReLU'd
         // activation and bf16 copy) and of the delta propagation (the gated delta below); not
@@ -513,13 +524,15 @@ static int build_model(ito_model* m, const ito_layer_desc* d, int n)
 
     // second stream and ordering events of the backward overlap: mode 1 unless every delta
     // propagation speculates; then the second stream would hold only the weight updates,
-    // which slow the contractions beside them by more than they take alone, and the mode is
-    // 0 (ito_model_set_overlap changes it)
+    // which slow the contractions beside them by more than they take alone, so it takes the
+    // weight gradients too (mode 3: they fill the partial last waves of the delta
+    // propagations; batch-8192 MLP 1.996 -> 1.976 ms a step), or nothing (mode 0) where mode 3
+    // is not possible (ito_model_set_overlap changes it)
     {
         bool every_delta_speculates = m->speculate;
         for (const MLayer& L : m->L)
             if (L.has_dgrad && !L.pd_spec.rq_pred) every_delta_speculates = false;
-        m->overlap = every_delta_speculates ? 0 : 1;
+        m->overlap = every_delta_speculates ? (m->overlap3_ok ? 3 : 0) : 1;
     }
     if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -632,6 +645,77 @@ static int model_forward(ito_model* m, const int8_t* x, const int32_t* labels, c
 // every read after its write: b waits for the delta-propagation result (delta ready)
 // and for the weight gradient (before the update); s waits for the requantised delta
 // before the next layer's contractions read it; s joins b at the end of the step.
+// Backward in overlap mode 3: the delta chain (delta propagation, its requantisation, the
+// next layer's delta propagation ...) on s; each layer's weight gradient and update on the
+// second stream w, the weight gradient once its delta is ready (event ev_delta(l) on s), the
+// update once the delta propagation that read the old weights is done (ev_dgrad(l)).
+// The weight gradients use their own split-K workspace; the step ends joined on s.
+static int model_backward_split(ito_model* m, cudaStream_t s)
+{
+    const int B = m->batch;
+    const int nl = (int)m->L.size();
+    const ito_niti_params p = m->p;
+    cudaStream_t w = m->side;
+    auto sync = [&](cudaEvent_t e, cudaStream_t from, cudaStream_t to) -> int {
+        if (cudaEventRecord(e, from) != cudaSuccess || cudaStreamWaitEvent(to, e, 0) != cudaSuccess)
+            return set_error(ITO_ERR_CUDA, "stream ordering event failed");
+        return ITO_OK;
+    };
+    for (int l = nl - 1; l >= m->opt.trainable_from; --l) {
+        MLayer& L = m->L[l];
+        const bool conv = L.kind == ITO_LAYER_CONV3X3_RELU;
+        ITO_TRY(sync(m->ev_delta(l), s, w));   // this layer's delta is ready
+        if (L.ig)
+            ITO_LAUNCH(m, w, ITO_PROF_GEMM, 2.0 * L.rows_out * L.OC * L.K, conv_igemm_run(L.pig_g, w));
+        else
+            ITO_LAUNCH(m, w, ITO_PROF_GEMM, gemm_ops(L.pg), gemm_run(L.pg, w));
+        if (L.has_dgrad) {
+            if (m->speculate && L.pd_spec.rq_pred) {
+                ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd_spec), gemm_run(L.pd_spec, s));
+                ITO_LAUNCH(m, s, ITO_PROF_REQUANT, 0.0, gemm_run(L.pd_redo, s));
+            } else {
+                if (L.s2)
+                    ITO_LAUNCH(m, s, ITO_PROF_GEMM, 2.0 * L.rows_in * L.IC * 9 * L.OC / 4,
+                               conv_dgrad_s2_run(L.ps2, s));
+                else
+                    ITO_LAUNCH(m, s, ITO_PROF_GEMM, gemm_ops(L.pd), gemm_run(L.pd, s));
+            }
+            // the update below may overwrite the weights once this delta propagation is done
+            ITO_TRY(sync(m->ev_dgrad(l), s, w));
+            if (!(m->speculate && L.pd_spec.rq_pred)) {
+                MLayer& prev = m->L[l - 1];
+                if (conv) {
+                    if (!L.s2)
+                        ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * L.rows_out * L.K + 4.0 * L.rows_in * L.IC,
+                                   launch_col2im(L.dcol, B, L.H, L.W, L.IC, L.OH, L.OW, L.stride, L.d32,
+                                                 m->umax(l, ST_DMAX), s));
+                    ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes(L.rows_in * L.IC, true, true),
+                               launch_requant(L.d32, L.rows_in, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
+                                              prev.mask ? nullptr : prev.a8, prev.e8, prev.eb, prev.lde,
+                                              m->sval(l, ST_DS), s, prev.mask, nullptr));
+                } else if (l == m->n_conv && m->has_pool) {
+                    ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, false, false),
+                               launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0, nullptr, m->pe8,
+                                              nullptr, 0, m->sval(l, ST_DS), s));
+                    ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * m->pool_HW * m->pool_C,
+                               launch_gap_bwd(m->pe8, prev.a8, B, m->pool_HW, m->pool_C, prev.e8, prev.eb, s));
+                } else {
+                    ITO_LAUNCH(m, s, ITO_PROF_REQUANT, requant_bytes((int64_t)B * L.IC, true, prev.relu),
+                               launch_requant(L.d32, B, L.IC, m->umax(l, ST_DMAX), p.target_bits, 0,
+                                              (prev.relu && !prev.mask) ? prev.a8 : nullptr, prev.e8, prev.eb,
+                                              prev.lde, m->sval(l, ST_DS), s, prev.mask, nullptr, m->last_d(l)));
+                }
+            }
+        }
+        // G read (4 B), W read and written (1 + 1 B), bf16 copy written (2 B)
+        ITO_LAUNCH(m, w, ITO_PROF_UPDATE, 8.0 * L.OC * L.K,
+                   launch_niti_update(L.W8, L.Wb, L.ldw, L.g32, L.OC, L.K, m->umax(l, ST_GMAX), p.target_bits,
+                                      p.mu_weight, m->sval(l, ST_GS), m->sval(l, ST_WS),
+                                      reinterpret_cast<uint32_t*>(m->sval(l, ST_NZ)), w));
+    }
+    return sync(m->ev_join(), w, s);
+}
+
 static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, cudaStream_t s)
 {
     const int B = m->batch;
@@ -651,6 +735,7 @@ static int model_backward(ito_model* m, const int8_t* x, const int32_t* labels, 
         ITO_LAUNCH(m, s, ITO_PROF_OTHER, 4.0 * B * top.OC + 4.0 * B,
                    launch_top_error(top.a8, labels, B, top.OC, m->target_mag, top.e8, top.eb, top.lde, s));
     ITO_TRY(sync(m->ev_fork(), s, b));
+    if (m->overlap == 3) return model_backward_split(m, s);
     bool delta_on_side = false;   // the layer above requantised this layer's delta on the side stream
     for (int l = nl - 1; l >= m->opt.trainable_from; --l) {
         MLayer& L = m->L[l];
@@ -960,7 +1045,9 @@ int ito_model_get_overlap(const ito_model* m, int* mode)
 
 int ito_model_set_overlap(ito_model* m, int mode)
 {
-    if (!m || mode < 0 || mode > 2) return set_error(ITO_ERR_ARG, "bad model or overlap mode");
+    if (!m || mode < 0 || mode > 3) return set_error(ITO_ERR_ARG, "bad model or overlap mode");
+    if (mode == 3 && !m->overlap3_ok)
+        return set_error(ITO_ERR_UNSUPPORTED, "overlap mode 3 needs unshared delta buffers and dynamic requantisation");
     if (mode != m->overlap) {
         if (cudaDeviceSynchronize() != cudaSuccess) return set_error(ITO_ERR_CUDA, "sync");
         drop_graphs(m);   // captured steps encode the stream layout

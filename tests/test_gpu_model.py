@@ -92,27 +92,36 @@ def test_model_graph_replay_lockstep(index, steps):
     assert g.ito.ito_get_error() == 0
 
 
-@pytest.mark.parametrize("index,pingpong,spec_min", [(1, False, 0), (6, True, 0), (2, True, 0), (1, False, 1)])
+@pytest.mark.parametrize("index,pingpong,spec_min", [(1, False, 0), (6, True, 0), (2, True, 0), (1, False, 1),
+                                                    (2, False, 0), (0, False, 0), (3, False, 0)])
 def test_overlap_modes_give_identical_steps(index, pingpong, spec_min):
-    """The backward overlap moves bandwidth passes to a second stream; every
-    tensor and statistic after three steps is the same in all three modes
-    (one stream, requantisation + updates overlapped, updates only), also with
-    speculative requantisation (whose checks and re-launches stay on the
-    caller's stream). A new model's default mode is the one the lockstep and
-    digest tests compare with the oracle."""
+    """The backward overlap moves work to a second stream; every tensor and
+    statistic after three steps is the same in every mode (one stream,
+    requantisation + updates overlapped, updates only, and, without ping-pong
+    delta buffers or static requantisation, weight gradients + updates beside
+    the delta chain), also with speculative requantisation (whose checks and
+    re-launches stay on the caller's stream). A new model's default mode is the
+    one the lockstep and digest tests compare with the oracle."""
     w = si.by_name(index)
+    modes = (0, 1, 2) if pingpong or w.static_requant else (0, 1, 2, 3)
     results = []
-    for mode in (0, 1, 2):
+    for mode in modes:
         # spec_min = 1: every eligible contraction requantises speculatively
         g = GpuRun(w, pingpong_grads=pingpong, speculate_min_elems=spec_min)
         g.model.set_overlap(mode)
         for t in range(3):
             g.step(t)
         results.append(g.record())
-    for mode, r in zip((1, 2), results[1:]):
+    for mode, r in zip(modes[1:], results[1:]):
         assert r.keys() == results[0].keys()
         for k in r:
             assert np.array_equal(np.asarray(r[k]), np.asarray(results[0][k])), (mode, k)
+
+
+def test_overlap_mode_3_refused_with_shared_delta_buffers():
+    g = GpuRun(si.by_name(1), pingpong_grads=True)
+    with pytest.raises(g.ito.ItoError):
+        g.model.set_overlap(3)
 
 
 @pytest.mark.parametrize("index,steps", [(0, 6), (1, 4), (5, 3), (3, 3)])
