@@ -308,3 +308,23 @@ def test_infer_matches_oracle_forward(spec_min):
     for l in range(nl):
         assert np.array_equal(g.tensor("a%d" % l).ravel(), ref["a%d" % l].ravel()), l
     assert g.ito.ito_get_error() == 0
+
+
+@pytest.mark.parametrize("index", [0, 3])
+def test_model_step_bad_label_sets_error_word(index):
+    """A label outside [0, C) in a training step (where the oracle's top error aborts)
+    records ITO_ERR_ARG in the device error word: the logits' requantisation, which
+    computes the top error, checks every row's label (the 10-class scalar pass and the
+    1000-class vectorised one)."""
+    import torch
+    w = si.by_name(index)
+    g = GpuRun(w)
+    x, labels = si.make_batch(w, 0)
+    labels = labels.copy()
+    labels[len(labels) // 2] = w.classes
+    assert g.ito.ito_get_error() == 0
+    g.model.train_step(torch.from_numpy(np.ascontiguousarray(x)).cuda(),
+                       torch.from_numpy(np.ascontiguousarray(labels)).cuda())
+    torch.cuda.synchronize()
+    assert g.ito.ito_get_error() == g.ito.ITO_ERR_ARG
+    assert g.ito.ito_get_error() == 0
