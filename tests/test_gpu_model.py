@@ -328,3 +328,34 @@ def test_model_step_bad_label_sets_error_word(index):
     torch.cuda.synchronize()
     assert g.ito.ito_get_error() == g.ito.ITO_ERR_ARG
     assert g.ito.ito_get_error() == 0
+
+
+@pytest.mark.parametrize("index", [1, 2])
+def test_overlap_mode_3_in_graphs(index):
+    """Overlap mode 3 captured into a CUDA graph (cross-stream events as graph edges) on a
+    non-default stream trains exactly as mode 1 stepping directly: every tensor and
+    statistic after four steps (one direct step, the capture and its launch, two replays;
+    the same input buffers, refilled each step)."""
+    import torch
+    w = si.by_name(index)
+    a, b = GpuRun(w), GpuRun(w)
+    a.model.set_overlap(1)
+    b.model.set_overlap(3)
+    b.model.use_graphs(True)
+    stream = torch.cuda.Stream()
+    x0, l0 = si.make_batch(w, 0)
+    xd = torch.empty(x0.shape, dtype=torch.int8, device="cuda")
+    ld = torch.empty(l0.shape, dtype=torch.int32, device="cuda")
+    for t in range(4):
+        a.step(t)
+        x, labels = si.make_batch(w, t)
+        xd.copy_(torch.from_numpy(np.ascontiguousarray(x)))
+        ld.copy_(torch.from_numpy(np.ascontiguousarray(labels)))
+        torch.cuda.synchronize()
+        b.model.train_step(xd, ld, stream=stream)
+        torch.cuda.synchronize()
+    ra, rb = a.record(), b.record()
+    assert ra.keys() == rb.keys()
+    for k in ra:
+        assert np.array_equal(np.asarray(ra[k]), np.asarray(rb[k])), k
+    assert a.ito.ito_get_error() == 0
