@@ -49,10 +49,11 @@ namespace ito {
         if (_r != ITO_OK) return _r; \
     } while (0)
 
+// Tiles of all three kernels: 128 rows x 64 columns of the result, K blocks of 64 terms.
 struct S2Cfg {
     static constexpr int BM = 128, BN = 64, BK = 64;
-    static constexpr int A_BYTES = BM * BK * 2;       // 16 KB: 128 output positions x 64 delta channels
-    static constexpr int B_BYTES = BN * BK * 2;       // 8 KB: 64 delta channels x 64 input channels
+    static constexpr int A_BYTES = BM * BK * 2;       // 16 KB: 128 rows x 64 K terms (bf16)
+    static constexpr int B_BYTES = BN * BK * 2;       // 8 KB: 64 columns x 64 K terms
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = 6;
     static constexpr int EPI_WARPS = 8;               // 4 lane quarters x 2 column halves of 32
@@ -62,6 +63,7 @@ struct S2Cfg {
     static constexpr int STAGING_BYTES = EPI_WARPS * 4096;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
 };
+static_assert(S2Cfg::SMEM_BYTES <= 227 * 1024, "conv kernels: shared memory above the per-CTA limit");
 
 // The phases in the order their tiles are handed out (most taps first): (py, px).
 __device__ __forceinline__ void s2_phase(int po, int& py, int& px)
@@ -650,7 +652,7 @@ static int ig_check(const uint16_t* xb, int64_t ldx, int B, int H, int W, int IC
     return ITO_OK;
 }
 
-static void ig_geom(IgGeom& g, int B, int H, int W, int IC, int OC)
+static void ig_geom(IgGeom& g, int B, int H, int W, int IC)
 {
     g.B = B;
     g.OH = H / 2;
@@ -663,7 +665,6 @@ static void ig_geom(IgGeom& g, int B, int H, int W, int IC, int OC)
     g.ohb = g.OH < 64 / g.OW ? g.OH : 64 / g.OW;
     g.bb = 64 / (g.OW * g.ohb);
     g.n_iblk_w = g.OH / g.ohb;
-    (void)OC;
 }
 
 int conv_fwd_s2_plan(ConvIgPlan* p, const uint16_t* xb, int64_t ldx, const uint16_t* Wb, int64_t ldw, int B, int H,
@@ -675,7 +676,7 @@ int conv_fwd_s2_plan(ConvIgPlan* p, const uint16_t* xb, int64_t ldx, const uint1
     *p = ConvIgPlan{};
     p->mode = CONV_FWD;
     IgGeom& g = p->g;
-    ig_geom(g, B, H, W, IC, OC);
+    ig_geom(g, B, H, W, IC);
     g.m_tiles = ((B + g.ba - 1) / g.ba) * g.n_iblk;
     g.n_tiles = OC / 64;
     g.num_kb = 9 * g.ic_blocks;
@@ -694,7 +695,7 @@ size_t conv_wgrad_s2_ws_bytes(int B, int H, int W, int IC, int OC)
 {
     if (!conv_dgrad_s2_eligible(B, H, W, IC, OC, 2)) return 0;
     IgGeom g;
-    ig_geom(g, B, H, W, IC, OC);
+    ig_geom(g, B, H, W, IC);
     const int tiles = ((OC + 127) / 128) * (9 * IC / 64);
     const int num_kb = (B + g.bb - 1) / g.bb * g.n_iblk_w;
     int splits = num_sms() / tiles;
@@ -712,7 +713,7 @@ int conv_wgrad_s2_plan(ConvIgPlan* p, const uint16_t* eb, int64_t lde, const uin
     *p = ConvIgPlan{};
     p->mode = CONV_WGRAD;
     IgGeom& g = p->g;
-    ig_geom(g, B, H, W, IC, OC);
+    ig_geom(g, B, H, W, IC);
     const int K9 = 9 * IC;
     g.m_tiles = (OC + 127) / 128;
     g.n_tiles = K9 / 64;
