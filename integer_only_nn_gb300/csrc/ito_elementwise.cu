@@ -90,50 +90,6 @@ int launch_i8_to_bf16(const int8_t* src, int64_t rows, int64_t cols, uint16_t* d
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "convert launch: %s", cudaGetErrorString(e));
 }
 
-// uint8 input (a partial model's input from a frozen prefix): values 0..255, exact in bf16
-__global__ void k_u8_to_bf16_v8(const uint8_t* __restrict__ src, int64_t rows, int64_t cols,
-                                uint16_t* __restrict__ dst, int64_t ldd)
-{
-    griddep_wait();
-    griddep_launch_dependents();
-    const int64_t groups = rows * (cols >> 3);
-    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
-         g += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i0 = g << 3;
-        const int64_t off = pitched(i0, cols, ldd);
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(src + i0));
-        const uint8_t* b = reinterpret_cast<const uint8_t*>(&v);
-        uint4 o;
-        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            ow[i] = int_pair_to_bf16x2(b[2 * i], b[2 * i + 1]);
-        *reinterpret_cast<uint4*>(dst + off) = o;
-    }
-}
-
-__global__ void k_u8_to_bf16_1(const uint8_t* __restrict__ src, int64_t rows, int64_t cols, uint16_t* __restrict__ dst,
-                               int64_t ldd)
-{
-    griddep_wait();
-    griddep_launch_dependents();
-    const int64_t n = rows * cols;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        dst[pitched(i, cols, ldd)] = int_to_bf16_bits(src[i]);
-    }
-}
-
-int launch_u8_to_bf16(const uint8_t* src, int64_t rows, int64_t cols, uint16_t* dst, int64_t ldd, cudaStream_t s)
-{
-    if (rows < 1 || cols < 1) return ITO_OK;
-    if (cols % 8 == 0 && ldd % 8 == 0 && aligned(src, 8) && aligned(dst, 16))
-        launch_pdl(k_u8_to_bf16_v8, launch_grid_blocks(rows * cols / 8, 256), 256, 0, s, src, rows, cols, dst, ldd);
-    else
-        launch_pdl(k_u8_to_bf16_1, launch_grid_blocks(rows * cols, 256), 256, 0, s, src, rows, cols, dst, ldd);
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "convert launch: %s", cudaGetErrorString(e));
-}
-
 // --------------------------------------------------------------- requant
 
 // q = sat8(rhu(y, s)); ReLU; gate
@@ -267,51 +223,16 @@ int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t*
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "requant launch: %s", cudaGetErrorString(e));
 }
 
-// --------------------------------------------- shift prediction (speculation)
+// --------------------------------------------- start of a step
 
-// At the start of a step: first score the previous step's speculation. Over the
-// slots a contraction epilogue speculated on (used[i] != 0, pred[i] >= 0),
-// count[0] += the predictions that held (pred[i] == last[i], the shift that step
-// computed) and count[1] += the ones that did not (both int64). Then this step's
-// predictions: pred[i] = last[i] where used and on, else -1 (no speculation).
-__global__ void k_roll_shift_predictions(int32_t* __restrict__ pred, const int32_t* __restrict__ last,
-                                         const int32_t* __restrict__ used, unsigned long long* __restrict__ count,
-                                         int n, int on)
-{
-    griddep_wait();
-    griddep_launch_dependents();
-    unsigned hits = 0, misses = 0;
-    for (int i = threadIdx.x; i < n; i += 32) {
-        const int32_t p = pred[i], l = last[i];
-        const bool u = used[i] != 0;
-        if (u && p >= 0) {
-            hits += p == l;
-            misses += p != l;
-        }
-        pred[i] = (on && u) ? l : -1;
-    }
-    hits = __reduce_add_sync(0xffffffffu, hits);
-    misses = __reduce_add_sync(0xffffffffu, misses);
-    if (threadIdx.x == 0) {
-        count[0] += hits;
-        count[1] += misses;
-    }
-}
-
-int launch_roll_shift_predictions(int32_t* pred, const int32_t* last, const int32_t* used, int64_t* count, int n,
-                                  int on, cudaStream_t s)
-{
-    if (n < 1) return ITO_OK;
-    launch_pdl(k_roll_shift_predictions, 1, 32, 0, s, pred, last, used, reinterpret_cast<unsigned long long*>(count), n,
-                                              on);
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "prediction launch: %s", cudaGetErrorString(e));
-}
-
-// The start of a training (or inference) step in one launch: the step's statistics
-// block zeroed and the shift predictions rolled (as k_roll_shift_predictions, n_pred > 0)
-// by block 0, and a Linear first layer's int8 or uint8 input converted to its bf16 copy
-// by all blocks (x == nullptr: none).
+// The start of a training (or inference) step in one launch: the step's statistics block
+// zeroed and, for n_pred > 0, the shift predictions rolled by block 0, and a Linear first
+// layer's int8 or uint8 (a partial model's input from a frozen prefix; 0..255, exact in
+// bf16) input converted to its bf16 copy by all blocks (x == nullptr: none). Rolling the
+// predictions first scores the previous step's speculation: over the slots a contraction
+// epilogue speculated on (used[i] != 0, pred[i] >= 0), count[0] += the predictions that
+// held (pred[i] == last[i], the shift that step computed) and count[1] += the ones that did
+// not (both int64); then pred[i] = last[i] where used and on, else -1 (no speculation).
 __global__ void k_step_begin(int32_t* __restrict__ stats, int n_stats, int32_t* __restrict__ pred,
                              const int32_t* __restrict__ last, const int32_t* __restrict__ used,
                              unsigned long long* __restrict__ count, int n_pred, int on, const void* __restrict__ x,

@@ -298,16 +298,13 @@ int launch_requant(const int32_t* Y, int64_t rows, int64_t cols, const uint32_t*
                    const int8_t* gate, int8_t* out8, uint16_t* outb, int64_t ldb, int32_t* d_shift, cudaStream_t s,
                    const uint8_t* gate_bits = nullptr, uint8_t* mask_out = nullptr, int32_t* s_last = nullptr,
                    const TopErr* top = nullptr);
-// scores the last step's predictions into count[0] (held) / count[1] (missed) over the used
-// slots, then pred[i] = (on && used[i]) ? last[i] : -1 for i < n
-int launch_roll_shift_predictions(int32_t* pred, const int32_t* last, const int32_t* used, int64_t* count, int n,
-                                  int on, cudaStream_t s);
-// a step's start in one kernel: stats[0..n_stats) = 0, the predictions rolled (n_pred > 0),
-// and x (int8, or uint8 when x_u8) [rows][cols] converted to bf16 xb (pitch ldx) unless x is null
+// a step's start in one kernel: stats[0..n_stats) = 0, the predictions rolled (n_pred > 0:
+// the last step's scored into count[0] held / count[1] missed over the used slots, then
+// pred[i] = (on && used[i]) ? last[i] : -1), and x (int8, or uint8 when x_u8) [rows][cols]
+// converted to bf16 xb (pitch ldx) unless x is null
 int launch_step_begin(int32_t* stats, int n_stats, int32_t* pred, const int32_t* last, const int32_t* used,
                       int64_t* count, int n_pred, int on, const void* x, int x_u8, int64_t rows, int64_t cols,
                       uint16_t* xb, int64_t ldx, cudaStream_t s);
-int launch_u8_to_bf16(const uint8_t* src, int64_t rows, int64_t cols, uint16_t* dst, int64_t ldd, cudaStream_t s);
 // static per-channel requantisation: clip(floor((Y + off[c]) * mult[c] / 2^k[c]), relu ? 0 : -128, 127)
 int launch_requant_static(const int32_t* Y, int64_t rows, int64_t cols, const int32_t* off, const int32_t* mult,
                           const int32_t* ksh, int relu, int8_t* out8, uint16_t* outb, int64_t ldb, uint8_t* mask_out,
