@@ -790,10 +790,7 @@ def run_ours_dfp16(args, w, cpu, barrier, dist, world, rank, local, flush, pk, p
                            "int16 multiply-add, exact int64 sums)",
                  "work": "executed bf16 operations, 8*M*N*K per contraction", "traffic": None,
                  "measured_over": "the same %d steps run again with an event pair around every launch "
-                                  "(%.4f ms per step with the events)%s" % (
-                                      K, prof_ms, "" if prof_mode == overlap_mode else
-                                      ", in backward overlap mode %d (the timed steps' mode %d runs weight "
-                                      "gradients beside delta propagations on shared SMs)" % (prof_mode, overlap_mode))})
+                                  "(%.4f ms per step with the events)" % (K, prof_ms)})
     line = {"metric": METRIC, "value": world * w.batch / (ms / 1000.0), "unit": "samples/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int16 (DFP16)",
