@@ -49,21 +49,26 @@ namespace ito {
         if (_r != ITO_OK) return _r; \
     } while (0)
 
-// Tiles of all three kernels: 128 rows x 64 columns of the result, K blocks of 64 terms.
+// Tiles of all three kernels: 128 rows x BN (64 or 128) columns of the result, K blocks of
+// 64 terms. These contractions are paced by their operand loads (a few K blocks of 4-D
+// boxes per tile), so where the result has a multiple of 128 columns the wider tile, which
+// loads each A tile once for twice the columns, is taken.
+template <int BN_>
 struct S2Cfg {
-    static constexpr int BM = 128, BN = 64, BK = 64;
+    static constexpr int BM = 128, BN = BN_, BK = 64;
     static constexpr int A_BYTES = BM * BK * 2;       // 16 KB: 128 rows x 64 K terms (bf16)
-    static constexpr int B_BYTES = BN * BK * 2;       // 8 KB: 64 columns x 64 K terms
+    static constexpr int B_BYTES = BN * BK * 2;       // 8 or 16 KB: BN columns x 64 K terms
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = 6;
-    static constexpr int EPI_WARPS = 8;               // 4 lane quarters x 2 column halves of 32
+    static constexpr int EPI_WARPS = 8;               // 4 lane quarters x 2 column halves of BN / 2
     static constexpr int THREADS = 64 + EPI_WARPS * 32;
-    static constexpr int TMEM_COLS = 128;             // two 64-column accumulators
+    static constexpr int TMEM_COLS = 2 * BN;          // two accumulators
     static constexpr int CHUNK_KB = 1024 / BK;        // exact chunk: 1024 terms
-    static constexpr int STAGING_BYTES = EPI_WARPS * 4096;
+    static constexpr int STAGING_BYTES = EPI_WARPS * 4096;   // one 32 x 32 int32 box per epilogue warp
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
 };
-static_assert(S2Cfg::SMEM_BYTES <= 227 * 1024, "conv kernels: shared memory above the per-CTA limit");
+static_assert(S2Cfg<64>::SMEM_BYTES <= 227 * 1024 && S2Cfg<128>::SMEM_BYTES <= 227 * 1024,
+              "conv kernels: shared memory above the per-CTA limit");
 
 // The phases in the order their tiles are handed out (most taps first): (py, px).
 __device__ __forceinline__ void s2_phase(int po, int& py, int& px)
@@ -84,13 +89,14 @@ __device__ __forceinline__ void s2_tap(int py, int px, int t, int& dh, int& kh, 
     kw = px ? (tx == 0 ? 0 : 2) : 1;
 }
 
-__global__ void __launch_bounds__(S2Cfg::THREADS, 1)
+template <int BN_>
+__global__ void __launch_bounds__(S2Cfg<BN_>::THREADS, 1)
     k_conv_dgrad_s2(const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmD0, const __grid_constant__ CUtensorMap tmD1,
                     const __grid_constant__ CUtensorMap tmD2, const __grid_constant__ CUtensorMap tmD3, S2Geom g,
                     uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
-    using Cfg = S2Cfg;
+    using Cfg = S2Cfg<BN_>;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;
     constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, true);
@@ -167,8 +173,11 @@ __global__ void __launch_bounds__(S2Cfg::THREADS, 1)
                     uint8_t* sB = sA + Cfg::A_BYTES;
                     // E[b0.., i0 + dh.., dw.., ocb * 64..]: 128 rows of 128 bytes (0 past the grid)
                     tma_load_4d(&tmE, &full_bar[stage], sA, ocb * 64, dw, i0 + dh, b0);
-                    // W[oc][kh][kw][ic] as [OC][9 IC], MN-major: rows ocb * 64.., columns tap * IC + nt * 64..
-                    tma_load_2d(&tmW, &full_bar[stage], sB, (kh * 3 + kw) * g.IC + nt * BN, ocb * 64);
+                    // W[oc][kh][kw][ic] as [OC][9 IC], MN-major: rows ocb * 64.., columns tap * IC + nt * BN..
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(&tmW, &full_bar[stage], sB + j * 8192, (kh * 3 + kw) * g.IC + nt * BN + j * 64,
+                                    ocb * 64);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
@@ -257,19 +266,22 @@ __global__ void __launch_bounds__(S2Cfg::THREADS, 1)
             if (lane == 0 && mx != 0) atomicMax(d_max, mx);
             const int b = b0 + b_off;
             if (b >= g.B) continue;
-            // one 32 x 32 box (128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8))
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
+            // 32 x 32 boxes (128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8))
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), acc[4 * j], acc[4 * j + 1], acc[4 * j + 2],
-                             acc[4 * j + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                const CUtensorMap* tmD = py ? (px ? &tmD3 : &tmD2) : (px ? &tmD1 : &tmD0);
-                tma_store_4d(tmD, stg, nt * BN + half * HALF, 0, i0 + i_off, b);
-                bulk_commit();
+            for (int gq = 0; gq < HALF / 32; ++gq) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), acc[gq * 32 + 4 * j], acc[gq * 32 + 4 * j + 1],
+                                 acc[gq * 32 + 4 * j + 2], acc[gq * 32 + 4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const CUtensorMap* tmD = py ? (px ? &tmD3 : &tmD2) : (px ? &tmD1 : &tmD0);
+                    tma_store_4d(tmD, stg, nt * BN + half * HALF + gq * 32, 0, i0 + i_off, b);
+                    bulk_commit();
+                }
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -311,7 +323,8 @@ int conv_dgrad_s2_plan(ConvS2Plan* p, const uint16_t* eb, int64_t lde, const uin
     g.OW = W / 2;
     g.IC = IC;
     g.oc_blocks = OC / 64;
-    g.n_tiles = IC / 64;
+    p->bn = IC % 128 == 0 ? 128 : 64;
+    g.n_tiles = IC / p->bn;
     g.oha = g.OH < 128 / g.OW ? g.OH : 128 / g.OW;
     g.ba = 128 / (g.OW * g.oha);
     g.n_iblk = g.OH / g.oha;
@@ -349,24 +362,30 @@ int conv_dgrad_s2_plan(ConvS2Plan* p, const uint16_t* eb, int64_t lde, const uin
     return ITO_OK;
 }
 
-int conv_dgrad_s2_run(const ConvS2Plan& p, cudaStream_t s)
+template <int BN>
+static int launch_dgrad_s2(const ConvS2Plan& p, cudaStream_t s)
 {
+    using Cfg = S2Cfg<BN>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(k_conv_dgrad_s2, cudaFuncAttributeMaxDynamicSharedMemorySize, S2Cfg::SMEM_BYTES) !=
+        if (cudaFuncSetAttribute(k_conv_dgrad_s2<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
             cudaSuccess)
             return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
         attr_set = true;
     }
     const int items = 4 * p.g.m_tiles * p.g.n_tiles;
     const int grid = items < num_sms() ? items : num_sms();
-    launch_pdl(k_conv_dgrad_s2, grid, S2Cfg::THREADS, S2Cfg::SMEM_BYTES, s, p.mapE, p.mapW, p.mapD[0], p.mapD[1],
+    launch_pdl(k_conv_dgrad_s2<BN>, grid, Cfg::THREADS, Cfg::SMEM_BYTES, s, p.mapE, p.mapW, p.mapD[0], p.mapD[1],
                p.mapD[2], p.mapD[3], p.g, p.d_max, p.err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK
                             : set_error(ITO_ERR_CUDA, "stride-2 delta propagation launch: %s", cudaGetErrorString(e));
 }
 
+int conv_dgrad_s2_run(const ConvS2Plan& p, cudaStream_t s)
+{
+    return p.bn == 128 ? launch_dgrad_s2<128>(p, s) : launch_dgrad_s2<64>(p, s);
+}
 
 // ------------------------------------------------ forward and weight gradient
 
@@ -388,14 +407,14 @@ __device__ __forceinline__ void ig_tap(int tap, int& plane, int& sh, int& sw)
 //   B: the tap's plane box {64 ic, OW, ohb, bb} (MN-major: 64 positions of 128 bytes); out: G,
 //   or with several slices their int32 partials [slice][OC][9 IC] (3-D map, no max) for
 //   launch_splitk_reduce.
-template <int MODE>
-__global__ void __launch_bounds__(S2Cfg::THREADS, 1)
+template <int MODE, int BN_>
+__global__ void __launch_bounds__(S2Cfg<BN_>::THREADS, 1)
     k_conv_igemm(const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmX1,
                  const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmX3,
                  const __grid_constant__ CUtensorMap tmOp, const __grid_constant__ CUtensorMap tmOut, IgGeom g,
                  uint32_t* __restrict__ d_max, int* __restrict__ err)
 {
-    using Cfg = S2Cfg;
+    using Cfg = S2Cfg<BN_>;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, STAGES = Cfg::STAGES;
     constexpr int HALF = BN / 2;
     constexpr bool W_ = MODE == CONV_WGRAD;
@@ -479,13 +498,18 @@ __global__ void __launch_bounds__(S2Cfg::THREADS, 1)
                         tma_load_4d(plane_map(plane), &full_bar[stage], sA, icb * 64, sw, i0 + sh, b0);
                         tma_load_2d(&tmOp, &full_bar[stage], sB, tap * g.IC + icb * 64, nt * BN);
                     } else {
-                        // A: E positions kb * 64.., channels mt * 128..; B: the tap's plane at position block kb
-                        const int tap = nt / g.ic_blocks, icb = nt - tap * g.ic_blocks;
-                        ig_tap(tap, plane, sh, sw);
+                        // A: E positions kb * 64.., channels mt * 128..; B: for each 64 of the tile's
+                        // columns (a tap's input channels), that tap's plane at position block kb
                         const int b0 = (kb / g.n_iblk_w) * g.bb, i0 = (kb % g.n_iblk_w) * g.ohb;
                         tma_load_2d(&tmOp, &full_bar[stage], sA, mt * BM, kb * 64);
                         tma_load_2d(&tmOp, &full_bar[stage], sA + 8192, mt * BM + 64, kb * 64);
-                        tma_load_4d(plane_map(plane), &full_bar[stage], sB, icb * 64, sw, i0 + sh, b0);
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j) {
+                            const int c = nt * BN + j * 64;
+                            const int tap = c / g.IC, icb = (c - tap * g.IC) / 64;
+                            ig_tap(tap, plane, sh, sw);
+                            tma_load_4d(plane_map(plane), &full_bar[stage], sB + j * 8192, icb * 64, sw, i0 + sh, b0);
+                        }
                     }
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -579,20 +603,23 @@ __global__ void __launch_bounds__(S2Cfg::THREADS, 1)
             const int row = W_ ? mt * BM + quad * 32 : ((mt / g.n_iblk) * g.ba * g.OH + (mt % g.n_iblk) * g.oha) * g.OW + quad * 32;
             const int col = nt * BN + half * HALF;
             if (row >= g.rows) continue;
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), acc[4 * j], acc[4 * j + 1], acc[4 * j + 2],
-                             acc[4 * j + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                if (partial)
-                    tma_store_3d(&tmOut, stg, col, row, w % g.splits);
-                else
-                    tma_store_2d(&tmOut, stg, col, row);
-                bulk_commit();
+            for (int gq = 0; gq < HALF / 32; ++gq) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(stg_row + ((j ^ (lane & 7)) << 4), acc[gq * 32 + 4 * j], acc[gq * 32 + 4 * j + 1],
+                                 acc[gq * 32 + 4 * j + 2], acc[gq * 32 + 4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (partial)
+                        tma_store_3d(&tmOut, stg, col + gq * 32, row, w % g.splits);
+                    else
+                        tma_store_2d(&tmOut, stg, col + gq * 32, row);
+                    bulk_commit();
+                }
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -678,7 +705,8 @@ int conv_fwd_s2_plan(ConvIgPlan* p, const uint16_t* xb, int64_t ldx, const uint1
     IgGeom& g = p->g;
     ig_geom(g, B, H, W, IC);
     g.m_tiles = ((B + g.ba - 1) / g.ba) * g.n_iblk;
-    g.n_tiles = OC / 64;
+    p->bn = OC % 128 == 0 ? 128 : 64;
+    g.n_tiles = OC / p->bn;
     g.num_kb = 9 * g.ic_blocks;
     g.splits = 1;
     g.kb_per_split = g.num_kb;
@@ -687,7 +715,7 @@ int conv_fwd_s2_plan(ConvIgPlan* p, const uint16_t* xb, int64_t ldx, const uint1
     p->err = device_error_word();
     if (!p->err) return set_error(ITO_ERR_CUDA, "device error word unavailable");
     IG_TRY(plane_maps(p->mapX, xb, ldx, B, H, W, IC, g.oha, g.ba));
-    IG_TRY(make_map_bf16(&p->mapOp, Bf16View{Wb, OC, 9 * (int64_t)IC, ldw}, 64));
+    IG_TRY(make_map_bf16(&p->mapOp, Bf16View{Wb, OC, 9 * (int64_t)IC, ldw}, p->bn));
     return int32_out_map(&p->mapOut, Y, g.rows, OC, OC);
 }
 
@@ -696,7 +724,7 @@ size_t conv_wgrad_s2_ws_bytes(int B, int H, int W, int IC, int OC)
     if (!conv_dgrad_s2_eligible(B, H, W, IC, OC, 2)) return 0;
     IgGeom g;
     ig_geom(g, B, H, W, IC);
-    const int tiles = ((OC + 127) / 128) * (9 * IC / 64);
+    const int tiles = ((OC + 127) / 128) * (9 * IC / (IC % 128 == 0 ? 128 : 64));
     const int num_kb = (B + g.bb - 1) / g.bb * g.n_iblk_w;
     int splits = num_sms() / tiles;
     if (splits > num_kb) splits = num_kb;
@@ -716,7 +744,8 @@ int conv_wgrad_s2_plan(ConvIgPlan* p, const uint16_t* eb, int64_t lde, const uin
     ig_geom(g, B, H, W, IC);
     const int K9 = 9 * IC;
     g.m_tiles = (OC + 127) / 128;
-    g.n_tiles = K9 / 64;
+    p->bn = IC % 128 == 0 ? 128 : 64;   // a 128-column tile: one tap's 128 input channels
+    g.n_tiles = K9 / p->bn;
     // position blocks of 64 (whole rows of one image, or whole images), in flat position order
     g.num_kb = (B + g.bb - 1) / g.bb * g.n_iblk_w;
     g.rows = OC;
@@ -748,25 +777,34 @@ int conv_wgrad_s2_plan(ConvIgPlan* p, const uint16_t* eb, int64_t lde, const uin
     return r == CUDA_SUCCESS ? ITO_OK : set_error(ITO_ERR_CUDA, "cuTensorMapEncodeTiled (partials) failed (%d)", (int)r);
 }
 
-int conv_igemm_run(const ConvIgPlan& p, cudaStream_t s)
+template <int MODE, int BN>
+static int launch_igemm(const ConvIgPlan& p, cudaStream_t s)
 {
-    static bool attr_set[2] = {false, false};
-    auto kern = p.mode == CONV_WGRAD ? k_conv_igemm<CONV_WGRAD> : k_conv_igemm<CONV_FWD>;
-    if (!attr_set[p.mode]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S2Cfg::SMEM_BYTES) != cudaSuccess)
+    using Cfg = S2Cfg<BN>;
+    auto kern = k_conv_igemm<MODE, BN>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
             return set_error(ITO_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(cudaGetLastError()));
-        attr_set[p.mode] = true;
+        attr_set = true;
     }
     const int items = p.g.m_tiles * p.g.n_tiles * p.g.splits;
     const int grid = items < num_sms() ? items : num_sms();
-    const bool partial = p.mode == CONV_WGRAD && p.g.splits > 1;
-    launch_pdl(kern, grid, S2Cfg::THREADS, S2Cfg::SMEM_BYTES, s, p.mapX[0], p.mapX[1], p.mapX[2], p.mapX[3],
-               p.mapOp, p.mapOut, p.g, partial ? nullptr : p.d_max, p.err);
+    const bool partial = MODE == CONV_WGRAD && p.g.splits > 1;
+    launch_pdl(kern, grid, Cfg::THREADS, Cfg::SMEM_BYTES, s, p.mapX[0], p.mapX[1], p.mapX[2], p.mapX[3], p.mapOp,
+               p.mapOut, p.g, partial ? nullptr : p.d_max, p.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(ITO_ERR_CUDA, "stride-2 conv launch: %s", cudaGetErrorString(e));
     if (partial)
         return launch_splitk_reduce(p.ws, p.g.splits, (int64_t)p.OC * p.K9, p.OC, p.K9, p.K9, p.G, p.d_max, s);
     return ITO_OK;
+}
+
+int conv_igemm_run(const ConvIgPlan& p, cudaStream_t s)
+{
+    if (p.mode == CONV_WGRAD)
+        return p.bn == 128 ? launch_igemm<CONV_WGRAD, 128>(p, s) : launch_igemm<CONV_WGRAD, 64>(p, s);
+    return p.bn == 128 ? launch_igemm<CONV_FWD, 128>(p, s) : launch_igemm<CONV_FWD, 64>(p, s);
 }
 
 }  // namespace ito

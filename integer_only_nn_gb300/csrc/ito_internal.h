@@ -113,6 +113,7 @@ struct ConvS2Plan {
     CUtensorMap mapW;       // weights' bf16 copy [OC][9 IC], MN-major boxes
     CUtensorMap mapD[4];    // phase (py, px) = (i >> 1, i & 1) of the int32 delta D [B][H][W][IC]
     S2Geom g;
+    int bn;                 // tile width (128 where IC is a multiple of 128, else 64)
     uint32_t* d_max;
     int* err;
 };
@@ -138,6 +139,7 @@ struct IgGeom {
 };
 struct ConvIgPlan {
     int mode;
+    int bn;                       // tile width: 128 where the result's columns allow, else 64
     CUtensorMap mapX[4];          // parity planes (py, px) = (i >> 1, i & 1)
     CUtensorMap mapOp;            // forward: W [OC][9 IC] K-major; weight gradient: E [positions][OC] MN-major
     CUtensorMap mapOut;           // Y [positions][OC], G [OC][9 IC], or G's K-slice partials
