@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(S2Cfg<BN_>::THREADS, 1)
         // ---------------- epilogue: drain into int32, max, store through the phase's map
         const int e = warp - 2;
         const int quad = warp & 3;               // TMEM lanes this warp may access
-        const int half = e >> 2;                 // which 32 of the tile's 64 columns
+        const int half = e >> 2;                 // which half (BN / 2 columns) of the tile
         uint8_t* stg = staging + e * 4096;       // this warp's 32 x 32 int32 store box
         const uint32_t stg_row = smem_u32(stg) + lane * 128;
         // this warp's 32 rows of the tile: (32 / OW) output rows of one image
@@ -399,12 +399,14 @@ __device__ __forceinline__ void ig_tap(int tap, int& plane, int& sh, int& sw)
 }
 
 // FWD: Y[(b,oh,ow)][oc] = sum over taps and ic of X[b][2oh+kh-1][2ow+kw-1][ic] W[oc][kh][kw][ic].
-//   Items: row tiles of 128 output positions x 64 output channels; K = 9 taps x IC.
-//   A: the tap's plane box {64 ic, OW, oha, ba}; B: W [OC][9 IC] K-major; out: 2-D map over Y.
+//   Items: row tiles of 128 output positions x BN output channels; K = 9 taps x IC.
+//   A: the tap's plane box {64 ic, OW, oha, ba}; B: W [OC][9 IC] K-major (BN rows); out: 2-D
+//   map over Y.
 // WGRAD: G[oc][(kh,kw,ic)] = sum over positions (b,oh,ow) of E[(b,oh,ow)][oc] X[b][2oh+kh-1][2ow+kw-1][ic].
-//   Items: tiles of 128 output channels x 64 columns (one tap's 64 input channels) x K slice;
+//   Items: tiles of 128 output channels x BN columns (a tap's input channels, 64 or 128) x K slice;
 //   K = positions in blocks of 64 (bb images x ohb rows x OW). A: E [positions][OC] MN-major;
-//   B: the tap's plane box {64 ic, OW, ohb, bb} (MN-major: 64 positions of 128 bytes); out: G,
+//   B: per 64 columns the tap's plane box {64 ic, OW, ohb, bb} (MN-major: 64 positions of 128
+//   bytes); out: G,
 //   or with several slices their int32 partials [slice][OC][9 IC] (3-D map, no max) for
 //   launch_splitk_reduce.
 template <int MODE, int BN_>
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(S2Cfg<BN_>::THREADS, 1)
                     uint8_t* sB = sA + Cfg::A_BYTES;
                     int plane, sh, sw;
                     if (!W_) {
-                        // A: the tap's plane at the row tile; B: W rows nt * 64.., K columns tap * IC + icb * 64
+                        // A: the tap's plane at the row tile; B: W rows nt * BN.., K columns tap * IC + icb * 64
                         const int tap = kb / g.ic_blocks, icb = kb - tap * g.ic_blocks;
                         ig_tap(tap, plane, sh, sw);
                         const int b0 = (mt / g.n_iblk) * g.ba, i0 = (mt % g.n_iblk) * g.oha;
@@ -559,7 +561,7 @@ __global__ void __launch_bounds__(S2Cfg<BN_>::THREADS, 1)
         // ---------------- epilogue: drain into int32, max, one 32 x 32 box through TMA
         const int e = warp - 2;
         const int quad = warp & 3;               // TMEM lanes this warp may access
-        const int half = e >> 2;                 // which 32 of the tile's 64 columns
+        const int half = e >> 2;                 // which half (BN / 2 columns) of the tile
         uint8_t* stg = staging + e * 4096;
         const uint32_t stg_row = smem_u32(stg) + lane * 128;
         int buf = 0;
