@@ -1347,7 +1347,8 @@ __global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t 
                            const unsigned long long* __restrict__ d_max, const int32_t* __restrict__ d_ea,
                            const int32_t* __restrict__ d_eb, int16_t* __restrict__ out16, uint16_t* __restrict__ hi,
                            uint16_t* __restrict__ lo, int64_t ldl, int32_t* __restrict__ d_exp_out,
-                           int32_t* __restrict__ d_rs, unsigned long long* __restrict__ d_abs_sum,
+                           int32_t* __restrict__ d_exp_out2, int32_t* __restrict__ d_rs,
+                           unsigned long long* __restrict__ d_abs_sum,
                            int* __restrict__ err)
 {
     griddep_wait();
@@ -1359,6 +1360,7 @@ __global__ void k_dfp_down(const int64_t* __restrict__ P, int64_t rows, int64_t 
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         const int e = *d_ea + (d_eb ? *d_eb : 0) + rs;
         if (d_exp_out) *d_exp_out = e;
+        if (d_exp_out2) *d_exp_out2 = e;
         if (d_rs) *d_rs = rs;
         if (e < -128 || e > 127) raise_device_error(err, ITO_ERR_EXPONENT);
     }
@@ -1385,7 +1387,7 @@ __global__ void k_dfp_down_v4(const int64_t* __restrict__ P, int rows, int cols,
                               const unsigned long long* __restrict__ d_max, const int32_t* __restrict__ d_ea,
                               const int32_t* __restrict__ d_eb, int16_t* __restrict__ out16,
                               uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int ldl,
-                              int32_t* __restrict__ d_exp_out, int32_t* __restrict__ d_rs,
+                              int32_t* __restrict__ d_exp_out, int32_t* __restrict__ d_exp_out2, int32_t* __restrict__ d_rs,
                               unsigned long long* __restrict__ d_abs_sum, int* __restrict__ err)
 {
     griddep_wait();
@@ -1396,6 +1398,7 @@ __global__ void k_dfp_down_v4(const int64_t* __restrict__ P, int rows, int cols,
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         const int e = *d_ea + (d_eb ? *d_eb : 0) + rs;
         if (d_exp_out) *d_exp_out = e;
+        if (d_exp_out2) *d_exp_out2 = e;
         if (d_rs) *d_rs = rs;
         if (e < -128 || e > 127) raise_device_error(err, ITO_ERR_EXPONENT);
     }
@@ -1434,7 +1437,7 @@ static inline bool al(const void* p, int a) { return (reinterpret_cast<uintptr_t
 
 int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned long long* d_max, const int32_t* d_ea,
                     const int32_t* d_eb, int16_t* out16, uint16_t* hi, uint16_t* lo, int64_t ldl, int32_t* d_exp_out,
-                    int32_t* d_rs, cudaStream_t s, unsigned long long* d_abs_sum)
+                    int32_t* d_rs, cudaStream_t s, unsigned long long* d_abs_sum, int32_t* d_exp_out2)
 {
     if (rows < 1 || cols < 1) return ITO_OK;
     int* err = device_error_word();
@@ -1442,10 +1445,11 @@ int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned
     if (cols % 4 == 0 && rows * cols < (1LL << 31) && ldl % 4 == 0 && al(P, 16) && al(out16, 8) &&
         (!hi || (al(hi, 8) && al(lo, 8))))
         launch_pdl(k_dfp_down_v4, launch_grid_blocks(rows * cols / 4, 256), 256, 0, s, 
-            P, (int)rows, (int)cols, d_max, d_ea, d_eb, out16, hi, lo, (int)ldl, d_exp_out, d_rs, d_abs_sum, err);
+            P, (int)rows, (int)cols, d_max, d_ea, d_eb, out16, hi, lo, (int)ldl, d_exp_out, d_exp_out2, d_rs, d_abs_sum,
+            err);
     else
         launch_pdl(k_dfp_down, launch_grid_blocks(rows * cols, 256), 256, 0, s, P, rows, cols, d_max, d_ea, d_eb, out16, hi,
-                                                                         lo, ldl, d_exp_out, d_rs, d_abs_sum, err);
+                   lo, ldl, d_exp_out, d_exp_out2, d_rs, d_abs_sum, err);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ITO_OK : set_error(ITO_ERR_CUDA, "dfp down launch: %s", cudaGetErrorString(e));
 }

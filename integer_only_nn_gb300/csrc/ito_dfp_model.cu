@@ -40,9 +40,16 @@ namespace ito {
 __global__ void k_set_i32(int32_t* p, int32_t v) {
     griddep_wait();
     griddep_launch_dependents(); *p = v; }
-__global__ void k_copy_i32(int32_t* dst, const int32_t* src) {
+// The start of a DFP16 step: its statistics blocks zeroed and the input exponent set.
+__global__ void k_dfp_step_begin(int32_t* __restrict__ s32, int n32, unsigned long long* __restrict__ s64, int n64,
+                                 int32_t* __restrict__ ex, int32_t exp_x)
+{
     griddep_wait();
-    griddep_launch_dependents(); *dst = *src; }
+    griddep_launch_dependents();
+    for (int i = threadIdx.x; i < n32; i += blockDim.x) s32[i] = 0;
+    for (int i = threadIdx.x; i < n64; i += blockDim.x) s64[i] = 0;
+    if (threadIdx.x == 0) *ex = exp_x;
+}
 
 enum { D_EY = 0, D_EE, D_RS, D_RSD, D_RSG, D_EG, D_K, D_NZ, D_N32 };
 enum { D_PMAX = 0, D_PDMAX, D_PGMAX, D_GABS, D_N64 };
@@ -718,11 +725,12 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int B = m->batch;
     const int nl = (int)m->L.size();
-    if (cudaMemsetAsync(m->s32, 0, sizeof(int32_t) * nl * D_N32, s) != cudaSuccess ||
-        cudaMemsetAsync(m->s64, 0, sizeof(unsigned long long) * nl * D_N64, s) != cudaSuccess)
-        return set_error(ITO_ERR_CUDA, "memset");
     m->launches = 0;
-    ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0, (launch_pdl(k_set_i32, 1, 1, 0, s, m->ex(), exp_x), ITO_OK));
+    // statistics zeroed and the input exponent set in one launch (no memset nodes, which would
+    // break the programmatic launch chain)
+    ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0,
+                (launch_pdl(k_dfp_step_begin, 1, 256, 0, s, m->s32, nl * D_N32, m->s64, nl * D_N64, m->ex(), exp_x),
+                 ITO_OK));
     ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 6.0 * B * m->L[0].IC,
                 launch_i16_to_limbs(x, B, m->L[0].IC, m->xh, m->xl, m->ldx, s));
     for (int l = 0; l < nl; ++l) {
@@ -730,12 +738,12 @@ int ito_dfp16_train_step(ito_dfp16_model* m, const int16_t* x, int32_t exp_x, vo
         const int32_t* e_in = l == 0 ? m->ex() : m->i32(l - 1, D_EY);
         ITO_DLAUNCH(m, s, ITO_PROF_GEMM, dfp_gemm_ops(L.pf), dfp_gemm_run(L.pf, s));
         m->launches += dfp_gemm_kernels(L.pf) - 1;
+        // the top layer's output exponent is also its delta's (the backward's first D_EE)
         ITO_DLAUNCH(m, s, ITO_PROF_REQUANT, 14.0 * B * L.OC,
                     launch_dfp_down(L.p64, B, L.OC, m->u64(l, D_PMAX), e_in, m->wexp_d + l, L.y16, L.yh, L.yl, L.ldy,
-                                    m->i32(l, D_EY), m->i32(l, D_RS), s));
+                                    m->i32(l, D_EY), m->i32(l, D_RS), s, nullptr,
+                                    l == nl - 1 ? m->i32(nl - 1, D_EE) : nullptr));
     }
-    ITO_DLAUNCH(m, s, ITO_PROF_OTHER, 0.0,
-                (launch_pdl(k_copy_i32, 1, 1, 0, s, m->i32(nl - 1, D_EE), m->i32(nl - 1, D_EY)), ITO_OK));
     // backward, top-down; with the overlap on, the contractions stay on s and the
     // down-conversions and the update go to the side stream b: the propagated delta's
     // down-conversion runs beside the weight gradient, the gradient's down-conversion

@@ -228,7 +228,8 @@ int launch_i16_to_limbs(const int16_t* src, int64_t rows, int64_t cols, uint16_t
 // d_abs_sum (optional): sum of |out16| is added to it (exact).
 int launch_dfp_down(const int64_t* P, int64_t rows, int64_t cols, const unsigned long long* d_max, const int32_t* d_ea,
                     const int32_t* d_eb, int16_t* out16, uint16_t* hi, uint16_t* lo, int64_t ldl, int32_t* d_exp_out,
-                    int32_t* d_rs, cudaStream_t s, unsigned long long* d_abs_sum = nullptr);
+                    int32_t* d_rs, cudaStream_t s, unsigned long long* d_abs_sum = nullptr,
+                    int32_t* d_exp_out2 = nullptr);   // a second copy of the exponent
 // float -> DFP16 (exponent from max |f|; d_bits: device scratch for the max's bits),
 // DFP16 -> float, and float(P) * 2^(Ea + Eb)
 int launch_dfp_from_float(const float* f, int64_t n, unsigned int* d_bits, int16_t* out, int32_t* d_exp,
