@@ -160,3 +160,21 @@ def test_host_side_argument_errors_dfp16_pipelined_step():
     dummy = ctypes.c_void_p(256)
     assert L.ito_dfp16_train_step_host_async(None, dummy, -12, None, None) == ito.ITO_ERR_ARG
     assert L.ito_dfp16_model_num_stats(None) == 0
+
+
+def test_header_compiles_as_c_and_cpp(tmp_path):
+    """include/ito.h is a C header (plain types, no C++ in the declarations): it compiles as
+    C99 with warnings on and as C++17."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc") or not shutil.which("g++"):
+        pytest.skip("no host C compiler")
+    inc = os.path.join(ROOT, "include")
+    src = tmp_path / "use.c"
+    src.write_text('#include "ito.h"\nint main(void) { return ito_get_error() == 0 ? 0 : 1; }\n')
+    for cmd in (["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", inc, "-c", str(src), "-o",
+                 str(tmp_path / "c.o")],
+                ["g++", "-std=c++17", "-Wall", "-Werror", "-x", "c++", "-I", inc, "-c", str(src), "-o",
+                 str(tmp_path / "cpp.o")]):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
